@@ -1,0 +1,435 @@
+/*
+ * oracle.c -- plain, slow, f64 CPU reference for the quantized weight-streaming
+ * decode path.  TEST INFRASTRUCTURE ONLY: it is used by tests/, by the smoke
+ * check and by the benchmark's CPU-baseline leg, never by the product path.
+ * It shares no code, header, table or constant with the CUDA library.
+ *
+ * Sources (three pages of the "infer" project, pg_infer 0.1.3-alpha):
+ *   [compute]  crates/infer-compute/README.md
+ *   [engine]   crates/infer-inference/README.md
+ *   [perf]     crates/infer-inference/PERFORMANCE.md
+ *
+ * The pages name the formats (Q4_0, Q4_K, Q6_K; "GGUF-compatible -- Q4_K/Q6_K
+ * formats match Ollama's quantization", [compute] §Design Principles item 8)
+ * but print no byte layout.  The layouts below are the plainest reading of
+ * "GGUF-compatible": the public GGUF block formats, restated here in prose and
+ * written from that understanding.  Every weight is decoded to an f64 value
+ * and every sum is accumulated in f64 in index order.  There is no blocking,
+ * no fusion and no reordering beyond what each definition states.
+ *
+ * Pins: every function here is checked by tests/test_oracle_*.py against
+ * hand-decoded byte fixtures, closed forms, library routines on special
+ * cases, or brute force (see the test files).  Nothing is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define QO_Q4_0 2
+#define QO_Q4_K 12
+#define QO_Q6_K 14
+
+/* ---------------------------------------------------------------------------
+ * IEEE-754 binary16 -> double, by bit arithmetic (sign, 5-bit exponent with
+ * bias 15, 10-bit fraction; exponent 0 is subnormal, 31 is inf/NaN).
+ * ------------------------------------------------------------------------- */
+double qo_half(uint16_t h)
+{
+    int sign = (h >> 15) & 1;
+    int expo = (h >> 10) & 31;
+    int frac = h & 1023;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)frac, -24);                 /* frac * 2^-10 * 2^-14 */
+    } else if (expo == 31) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(1024 + frac), expo - 25);  /* (1 + frac/1024) * 2^(e-15) */
+    }
+    return sign ? -v : v;
+}
+
+static uint16_t rd16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* ---------------------------------------------------------------------------
+ * Q4_0 ([compute] §Shaders "Q4_0 matvec"): 32 weights in 18 bytes.
+ *   bytes 0..1  d (binary16)
+ *   bytes 2..17 qs[16]: weight j (0..15) is the low nibble of qs[j],
+ *               weight 16+j is the high nibble of qs[j]
+ *   w = d * (q - 8)
+ * ------------------------------------------------------------------------- */
+void qo_dequant_q4_0(const uint8_t *blk, double out[32])
+{
+    double d = qo_half(rd16(blk));
+    const uint8_t *qs = blk + 2;
+    for (int j = 0; j < 16; ++j) {
+        int lo = qs[j] & 15;
+        int hi = qs[j] >> 4;
+        out[j] = d * (double)(lo - 8);
+        out[16 + j] = d * (double)(hi - 8);
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Q4_K ([compute] §Shaders "Q4_K/Q6_K" row, q4k_matvec): a super-block of 256
+ * weights in 144 bytes, eight sub-blocks of 32 weights.
+ *   bytes 0..1   d    (binary16)  super-block scale of the sub-block scales
+ *   bytes 2..3   dmin (binary16)  super-block scale of the sub-block mins
+ *   bytes 4..15  sc[12]: eight 6-bit scales and eight 6-bit mins, packed:
+ *       sub-block s < 4 : scale = sc[s] & 63,  min = sc[s+4] & 63
+ *       sub-block s >= 4: scale = (sc[s+4] & 15) | ((sc[s-4] >> 6) << 4)
+ *                         min   = (sc[s+4] >> 4) | ((sc[s]   >> 6) << 4)
+ *   bytes 16..143 qs[128], four chunks of 32 bytes; in chunk c (0..3), byte
+ *       qs[32c + l] holds weight 64c + l (sub-block 2c) in its low nibble and
+ *       weight 64c + 32 + l (sub-block 2c+1) in its high nibble.
+ *   w = d * scale[s] * q - dmin * min[s]
+ * ------------------------------------------------------------------------- */
+void qo_q4_k_scale_min(const uint8_t *sc, int s, int *scale, int *mn)
+{
+    if (s < 4) {
+        *scale = sc[s] & 63;
+        *mn = sc[s + 4] & 63;
+    } else {
+        *scale = (sc[s + 4] & 15) | ((sc[s - 4] >> 6) << 4);
+        *mn = (sc[s + 4] >> 4) | ((sc[s] >> 6) << 4);
+    }
+}
+
+void qo_dequant_q4_k(const uint8_t *blk, double out[256])
+{
+    double d = qo_half(rd16(blk));
+    double dmin = qo_half(rd16(blk + 2));
+    const uint8_t *sc = blk + 4;
+    const uint8_t *qs = blk + 16;
+    for (int c = 0; c < 4; ++c) {
+        int s_lo = 2 * c, s_hi = 2 * c + 1;
+        int sc_lo, m_lo, sc_hi, m_hi;
+        qo_q4_k_scale_min(sc, s_lo, &sc_lo, &m_lo);
+        qo_q4_k_scale_min(sc, s_hi, &sc_hi, &m_hi);
+        for (int l = 0; l < 32; ++l) {
+            int byte = qs[32 * c + l];
+            int q_lo = byte & 15;
+            int q_hi = byte >> 4;
+            out[64 * c + l] = d * (double)sc_lo * (double)q_lo - dmin * (double)m_lo;
+            out[64 * c + 32 + l] = d * (double)sc_hi * (double)q_hi - dmin * (double)m_hi;
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Q6_K ([compute] §Shaders, q6k_matvec): 256 weights in 210 bytes.
+ *   bytes 0..127   ql[128]  low 4 bits
+ *   bytes 128..191 qh[64]   high 2 bits, four per byte
+ *   bytes 192..207 sc[16]   signed 8-bit scales, one per 16 weights
+ *   bytes 208..209 d        (binary16)
+ * For each half h (weights 128h .. 128h+127) and l = 0..31:
+ *   weight 128h +      l : low  nibble of ql[64h + l],      bits (qh[32h+l] >> 0) & 3
+ *   weight 128h + 32 + l : low  nibble of ql[64h + 32 + l], bits (qh[32h+l] >> 2) & 3
+ *   weight 128h + 64 + l : high nibble of ql[64h + l],      bits (qh[32h+l] >> 4) & 3
+ *   weight 128h + 96 + l : high nibble of ql[64h + 32 + l], bits (qh[32h+l] >> 6) & 3
+ *   q = (nibble | bits << 4) - 32, in [-32, 31];  w = d * sc[i / 16] * q
+ * ------------------------------------------------------------------------- */
+void qo_dequant_q6_k(const uint8_t *blk, double out[256])
+{
+    const uint8_t *ql = blk;
+    const uint8_t *qh = blk + 128;
+    const int8_t *sc = (const int8_t *)(blk + 192);
+    double d = qo_half(rd16(blk + 208));
+    for (int h = 0; h < 2; ++h) {
+        for (int l = 0; l < 32; ++l) {
+            int a = ql[64 * h + l];
+            int b = ql[64 * h + 32 + l];
+            int hb = qh[32 * h + l];
+            int q[4];
+            q[0] = ((a & 15) | (((hb >> 0) & 3) << 4)) - 32;
+            q[1] = ((b & 15) | (((hb >> 2) & 3) << 4)) - 32;
+            q[2] = ((a >> 4) | (((hb >> 4) & 3) << 4)) - 32;
+            q[3] = ((b >> 4) | (((hb >> 6) & 3) << 4)) - 32;
+            for (int k = 0; k < 4; ++k) {
+                int i = 128 * h + 32 * k + l;
+                out[i] = d * (double)sc[i / 16] * (double)q[k];
+            }
+        }
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * Format table.
+ * ------------------------------------------------------------------------- */
+int qo_block_weights(int fmt)
+{
+    switch (fmt) {
+    case QO_Q4_0: return 32;
+    case QO_Q4_K: return 256;
+    case QO_Q6_K: return 256;
+    default: return 0;
+    }
+}
+
+int qo_block_bytes(int fmt)
+{
+    switch (fmt) {
+    case QO_Q4_0: return 18;
+    case QO_Q4_K: return 144;
+    case QO_Q6_K: return 210;
+    default: return 0;
+    }
+}
+
+static void dequant_block(int fmt, const uint8_t *blk, double *out)
+{
+    if (fmt == QO_Q4_0) qo_dequant_q4_0(blk, out);
+    else if (fmt == QO_Q4_K) qo_dequant_q4_k(blk, out);
+    else qo_dequant_q6_k(blk, out);
+}
+
+/* Dense f64 copy of rows [0, rows) of a row-major quantized matrix: row r is a
+ * contiguous run of hidden / QK blocks.  Returns 0, or -1 on a bad shape. */
+int qo_dequant_rows(int fmt, const uint8_t *W, int64_t rows, int64_t hidden, double *out)
+{
+    int qk = qo_block_weights(fmt), bb = qo_block_bytes(fmt);
+    if (qk == 0 || hidden % qk != 0) return -1;
+    int64_t nb = hidden / qk;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t b = 0; b < nb; ++b)
+            dequant_block(fmt, W + (r * nb + b) * bb, out + r * hidden + b * qk);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Quantized matrix-vector product ([compute] §Quick Start
+ * "backend.q4k_matvec(&q4k_data, &x, rows, hidden)").
+ *   y[b][r]     = sum_i w[r][i] * x[b][i]          (f64, index order)
+ *   bound[b][r] = sum_i |w[r][i] * x[b][i]|
+ * x is [batch][hidden]; y and bound are [batch][rows].  Only rows in
+ * [row_begin, row_end) are written, so a caller may split the rows.
+ * ------------------------------------------------------------------------- */
+int qo_matvec(int fmt, const uint8_t *W, int64_t rows, int64_t hidden,
+              const double *x, int batch, int64_t row_begin, int64_t row_end,
+              double *y, double *bound)
+{
+    int qk = qo_block_weights(fmt), bb = qo_block_bytes(fmt);
+    if (qk == 0 || hidden % qk != 0 || batch < 1) return -1;
+    if (row_begin < 0 || row_end > rows || row_begin > row_end) return -1;
+    int64_t nb = hidden / qk;
+    double *wrow = (double *)malloc(sizeof(double) * (size_t)(hidden > 0 ? hidden : 1));
+    if (!wrow) return -2;
+    for (int64_t r = row_begin; r < row_end; ++r) {
+        for (int64_t b = 0; b < nb; ++b)
+            dequant_block(fmt, W + (r * nb + b) * bb, wrow + b * qk);
+        for (int bt = 0; bt < batch; ++bt) {
+            const double *xb = x + (int64_t)bt * hidden;
+            double acc = 0.0, mag = 0.0;
+            for (int64_t i = 0; i < hidden; ++i) {
+                double t = wrow[i] * xb[i];
+                acc += t;
+                mag += fabs(t);
+            }
+            y[(int64_t)bt * rows + r] = acc;
+            if (bound) bound[(int64_t)bt * rows + r] = mag;
+        }
+    }
+    free(wrow);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * GELU, tanh form ([compute] §Shaders "geglu_gelu_tanh"; [perf] §Activation
+ * Function Support, Gemma rows).  The pages name it and print no formula; this
+ * is the standard tanh approximation of GELU:
+ *   gelu(t) = 0.5 t (1 + tanh( sqrt(2/pi) (t + 0.044715 t^3) ))
+ * ------------------------------------------------------------------------- */
+double qo_gelu_tanh(double t)
+{
+    const double k = sqrt(2.0 / M_PI);
+    return 0.5 * t * (1.0 + tanh(k * (t + 0.044715 * t * t * t)));
+}
+
+/* ---------------------------------------------------------------------------
+ * RMS norm ([compute] §Shaders "rms_norm"; [engine] §Key Components
+ * residual.rs): y_i = x_i / sqrt(mean_j x_j^2 + eps) * w_i.
+ * The weight multiplies as given (no 1 + w offset).
+ * ------------------------------------------------------------------------- */
+void qo_rms_norm(const double *x, const double *w, int64_t n, double eps, double *y)
+{
+    double ss = 0.0;
+    for (int64_t i = 0; i < n; ++i) ss += x[i] * x[i];
+    double inv = 1.0 / sqrt(ss / (double)n + eps);
+    for (int64_t i = 0; i < n; ++i) y[i] = x[i] * inv * w[i];
+}
+
+/* residual_add ([compute] §Shaders "Element-wise"): h_i <- h_i + y_i. */
+void qo_residual_add(double *h, const double *y, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i) h[i] += y[i];
+}
+
+/* ---------------------------------------------------------------------------
+ * Attention at sequence length 1 ([compute] §Architecture, decode.rs
+ * "norm -> QKV -> attend -> O").  With one key, the softmax over one score is
+ * exactly 1, so each query head's output is the value vector of the KV head it
+ * reads.  Query head h reads KV head h / (n_q_heads / n_kv_heads) (contiguous
+ * grouped-query grouping).  q and k do not enter the result.
+ *   attn[h * head_dim + i] = v[(h / group) * head_dim + i]
+ * ------------------------------------------------------------------------- */
+int qo_attn_seq1(const double *v, int n_q_heads, int n_kv_heads, int head_dim, double *attn)
+{
+    if (n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return -1;
+    int group = n_q_heads / n_kv_heads;
+    for (int h = 0; h < n_q_heads; ++h)
+        for (int i = 0; i < head_dim; ++i)
+            attn[h * head_dim + i] = v[(h / group) * head_dim + i];
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Gated FFN ([compute] §Shaders "Q4_K fused FFN": q4k_ffn_gate_up then
+ * q4k_geglu_gelu_tanh_down; [engine] §WalkFfn steps 1-3: gate and up
+ * projections, GEGLU, then the down projection).
+ *   g = Wg x,  u = Wu x            (inter rows, hidden columns)
+ *   m_j = gelu_tanh(g_j) * u_j     (the gate takes the activation)
+ *   y = Wd m                       (hidden rows, inter columns)
+ *   bound_y[i] = sum_j |wd[i][j] * m_j|
+ * Any of the outputs except y may be NULL.
+ * ------------------------------------------------------------------------- */
+int qo_ffn(int fmt_gu, const uint8_t *Wg, const uint8_t *Wu, int fmt_d, const uint8_t *Wd,
+           int64_t hidden, int64_t inter, const double *x,
+           double *g, double *u, double *m, double *y, double *bound_y)
+{
+    double *gg = (double *)malloc(sizeof(double) * (size_t)inter);
+    double *uu = (double *)malloc(sizeof(double) * (size_t)inter);
+    double *mm = (double *)malloc(sizeof(double) * (size_t)inter);
+    int rc = -2;
+    if (!gg || !uu || !mm) goto done;
+    rc = qo_matvec(fmt_gu, Wg, inter, hidden, x, 1, 0, inter, gg, NULL);
+    if (rc) goto done;
+    rc = qo_matvec(fmt_gu, Wu, inter, hidden, x, 1, 0, inter, uu, NULL);
+    if (rc) goto done;
+    for (int64_t j = 0; j < inter; ++j) mm[j] = qo_gelu_tanh(gg[j]) * uu[j];
+    rc = qo_matvec(fmt_d, Wd, hidden, inter, mm, 1, 0, hidden, y, bound_y);
+    if (rc) goto done;
+    if (g) memcpy(g, gg, sizeof(double) * (size_t)inter);
+    if (u) memcpy(u, uu, sizeof(double) * (size_t)inter);
+    if (m) memcpy(m, mm, sizeof(double) * (size_t)inter);
+done:
+    free(gg);
+    free(uu);
+    free(mm);
+    return rc;
+}
+
+/* ---------------------------------------------------------------------------
+ * One decoder layer of the single-token chain ([compute] §Architecture and
+ * §Quick Start decode_token; [perf] §Post-Norm Architecture: Gemma-3 applies
+ * a norm after attention and after the FFN as well as before them).
+ *
+ * post_norms = 1 (Gemma-3 sandwich):
+ *   n1 = rms_norm(h, w_in)
+ *   q, k, v = Wq n1, Wk n1, Wv n1
+ *   a  = attention at seq 1 (value broadcast, see qo_attn_seq1)
+ *   o  = Wo a
+ *   h1 = h + rms_norm(o, w_post_attn)
+ *   n2 = rms_norm(h1, w_pre_ffn)
+ *   f  = FFN(n2)
+ *   h' = h1 + rms_norm(f, w_post_ffn)
+ * post_norms = 0 (pre-norm only): h1 = h + o, h' = h1 + f; w_post_* unused.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    int fmt_qkv, fmt_o, fmt_gu, fmt_down;
+    const uint8_t *Wq, *Wk, *Wv, *Wo, *Wg, *Wu, *Wd;
+    const double *w_in, *w_post_attn, *w_pre_ffn, *w_post_ffn;
+} qo_layer;
+
+typedef struct {
+    int64_t hidden, inter;
+    int n_q_heads, n_kv_heads, head_dim;
+    double eps;
+    int post_norms;
+} qo_dims;
+
+/* Optional per-layer trace; any pointer may be NULL. */
+typedef struct {
+    double *n1, *q, *k, *v, *attn, *o, *h1, *n2, *g, *u, *m, *f, *bound_f;
+} qo_trace;
+
+int qo_layer_forward(const qo_layer *L, const qo_dims *D, const double *h, double *h_out,
+                     qo_trace *T)
+{
+    int64_t H = D->hidden, I = D->inter;
+    int64_t qd = (int64_t)D->n_q_heads * D->head_dim;
+    int64_t kd = (int64_t)D->n_kv_heads * D->head_dim;
+    size_t need = (size_t)(H * 6 + qd * 2 + kd * 2 + I * 3);
+    double *buf = (double *)malloc(sizeof(double) * need);
+    if (!buf) return -2;
+    double *n1 = buf, *q = n1 + H, *k = q + qd, *v = k + kd, *a = v + kd, *o = a + qd;
+    double *h1 = o + H, *n2 = h1 + H, *t = n2 + H, *f = t + H;
+    double *g = f + H, *u = g + I, *m = u + I;
+    int rc;
+
+    qo_rms_norm(h, L->w_in, H, D->eps, n1);
+    rc = qo_matvec(L->fmt_qkv, L->Wq, qd, H, n1, 1, 0, qd, q, NULL);
+    if (!rc) rc = qo_matvec(L->fmt_qkv, L->Wk, kd, H, n1, 1, 0, kd, k, NULL);
+    if (!rc) rc = qo_matvec(L->fmt_qkv, L->Wv, kd, H, n1, 1, 0, kd, v, NULL);
+    if (!rc) rc = qo_attn_seq1(v, D->n_q_heads, D->n_kv_heads, D->head_dim, a);
+    if (!rc) rc = qo_matvec(L->fmt_o, L->Wo, H, qd, a, 1, 0, H, o, NULL);
+    if (rc) { free(buf); return rc; }
+
+    memcpy(h1, h, sizeof(double) * (size_t)H);
+    if (D->post_norms) {
+        qo_rms_norm(o, L->w_post_attn, H, D->eps, t);
+        qo_residual_add(h1, t, H);
+    } else {
+        qo_residual_add(h1, o, H);
+    }
+    qo_rms_norm(h1, L->w_pre_ffn, H, D->eps, n2);
+    rc = qo_ffn(L->fmt_gu, L->Wg, L->Wu, L->fmt_down, L->Wd, H, I, n2, g, u, m, f,
+                T ? T->bound_f : NULL);
+    if (rc) { free(buf); return rc; }
+    memcpy(h_out, h1, sizeof(double) * (size_t)H);
+    if (D->post_norms) {
+        qo_rms_norm(f, L->w_post_ffn, H, D->eps, t);
+        qo_residual_add(h_out, t, H);
+    } else {
+        qo_residual_add(h_out, f, H);
+    }
+
+    if (T) {
+        if (T->n1) memcpy(T->n1, n1, sizeof(double) * (size_t)H);
+        if (T->q) memcpy(T->q, q, sizeof(double) * (size_t)qd);
+        if (T->k) memcpy(T->k, k, sizeof(double) * (size_t)kd);
+        if (T->v) memcpy(T->v, v, sizeof(double) * (size_t)kd);
+        if (T->attn) memcpy(T->attn, a, sizeof(double) * (size_t)qd);
+        if (T->o) memcpy(T->o, o, sizeof(double) * (size_t)H);
+        if (T->h1) memcpy(T->h1, h1, sizeof(double) * (size_t)H);
+        if (T->n2) memcpy(T->n2, n2, sizeof(double) * (size_t)H);
+        if (T->g) memcpy(T->g, g, sizeof(double) * (size_t)I);
+        if (T->u) memcpy(T->u, u, sizeof(double) * (size_t)I);
+        if (T->m) memcpy(T->m, m, sizeof(double) * (size_t)I);
+        if (T->f) memcpy(T->f, f, sizeof(double) * (size_t)H);
+    }
+    free(buf);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Top-k indices of v by value, descending; equal values keep the lower index
+ * first ([perf] §Production Benchmark "top 5" predictions).  Plain repeated
+ * selection: k passes over v.
+ * ------------------------------------------------------------------------- */
+int qo_topk(const double *v, int64_t n, int k, int64_t *idx)
+{
+    if (k < 0 || k > n) return -1;
+    for (int j = 0; j < k; ++j) {
+        int64_t best = -1;
+        for (int64_t i = 0; i < n; ++i) {
+            int taken = 0;
+            for (int p = 0; p < j; ++p)
+                if (idx[p] == i) { taken = 1; break; }
+            if (taken) continue;
+            if (best < 0 || v[i] > v[best]) best = i;
+        }
+        idx[j] = best;
+    }
+    return 0;
+}
