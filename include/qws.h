@@ -1,0 +1,209 @@
+/*
+ * qws.h -- quantized weight streaming for single-token decode on GB300 (sm_103a).
+ *
+ * A C ABI over hand-written CUDA kernels that multiply packed GGUF-style
+ * weight matrices (Q4_K, Q6_K, Q4_0) by f32 activation vectors, decoding the
+ * blocks in registers as they stream from HBM.  The calls restate the compute
+ * backend of the "infer" project (crates/infer-compute/README.md, §Quick Start:
+ * q4k_matvec(W, x, rows, hidden), decode_token(layers, x, hidden, inter, q_dim,
+ * kv_dim, ...); §Shaders: q4k_matvec, q6k_matvec, Q4_0 matvec, q4k_qkv_proj,
+ * q4k_ffn_gate_up, q4k_geglu_gelu_tanh_down, rms_norm, residual_add).
+ *
+ * Conventions shared by every call
+ *  - Pointers named W*, x, y, h, q, k, v, w_* and ws are DEVICE pointers owned
+ *    by the caller (for example torch tensors' data_ptr()).  The library never
+ *    allocates, frees or retains them.  `layers` and `dims` are HOST pointers,
+ *    read during the call only.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Every call
+ *    is asynchronous on that stream: a QWS_OK return means the work was
+ *    enqueued.  Calls that overlap on the GPU must not share output or
+ *    workspace buffers.
+ *  - Weight layout: row-major; row r is the contiguous run of hidden/QK blocks
+ *    that covers columns 0..hidden-1 (QK = 256 for Q4_K and Q6_K, 32 for
+ *    Q4_0).  Block layouts are the public GGUF ones:
+ *        Q4_K 144 B: f16 d, f16 dmin, 12 B packed 6-bit scales/mins, 128 B nibbles
+ *        Q6_K 210 B: 128 B low nibbles, 64 B high 2-bit fields, 16 int8 scales, f16 d
+ *        Q4_0  18 B: f16 d, 16 B nibbles
+ *  - Activations: x is f32 [batch][hidden], y is f32 [batch][rows], both
+ *    row-major and dense.
+ *  - Accuracy: every result is an f32 accumulation of exact products; it stays
+ *    within 1e-5 * sum_i |w_i x_i| of the exact value per output for |x| in
+ *    [2^-66, 2^38] (outside that range products lose bits or overflow).
+ *  - Errors: arguments are checked on the host before anything is enqueued.
+ *      QWS_ERR_NULL      a required pointer is NULL
+ *      QWS_ERR_SHAPE     a size is negative, zero where it may not be, or not a
+ *                        multiple of 256 (hidden / inter), or above a limit
+ *      QWS_ERR_ALIGN     W* not 16-byte aligned, or an f32 pointer not 4-byte aligned
+ *      QWS_ERR_FORMAT    unknown qws_format
+ *      QWS_ERR_WORKSPACE ws NULL or ws_bytes below qws_workspace_bytes(...)
+ *      QWS_ERR_CUDA      the CUDA runtime refused the launch (message in
+ *                        qws_last_error())
+ *    Nothing is enqueued when a call returns an error.  rows == 0 returns
+ *    QWS_OK without a launch.  A bounded wait that expires inside a kernel
+ *    (a wedged pipeline) records a code that qws_device_error() returns.
+ *  - Limits: hidden/64 <= 320 per matvec column range (hidden <= 20480);
+ *    batch * (rows slots) fits 320 threads: batch <= 320 / (hidden / 64).
+ */
+#ifndef QWS_H
+#define QWS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* qws_stream; /* = cudaStream_t */
+
+typedef enum {
+  QWS_OK = 0,
+  QWS_ERR_NULL = 1,
+  QWS_ERR_SHAPE = 2,
+  QWS_ERR_ALIGN = 3,
+  QWS_ERR_FORMAT = 4,
+  QWS_ERR_WORKSPACE = 5,
+  QWS_ERR_CUDA = 6,
+  QWS_ERR_TIMEOUT = 7
+} qws_status;
+
+/* GGUF type ids. */
+typedef enum { QWS_Q4_0 = 2, QWS_Q4_K = 12, QWS_Q6_K = 14 } qws_format;
+
+/* Operations for qws_workspace_bytes(). */
+typedef enum {
+  QWS_OP_MATVEC = 0,      /* qws_matvec / qws_q4_0_matvec with split_k > 1 */
+  QWS_OP_FFN = 1,         /* qws_q4k_ffn_gate_up_geglu_down                */
+  QWS_OP_DECODE_CHAIN = 2 /* qws_decode_chain                              */
+} qws_op;
+
+/* ------------------------------------------------------------------------
+ * Quantized matrix-vector products.
+ * infer-compute README §Quick Start "backend.q4k_matvec(&q4k_data, &x, rows,
+ * hidden)" and §Shaders rows "Q4_0 matvec", "Q4_K/Q6_K" (q4k_matvec,
+ * q6k_matvec):   y[b][r] = sum_i dequant(W)[r][i] * x[b][i].
+ *   W      rows x hidden weights in `fmt` (device, 16-byte aligned)
+ *   x      [batch][hidden] f32 (device, 4-byte aligned)
+ *   y      [batch][rows]   f32 (device, 4-byte aligned), overwritten
+ *   rows   >= 0;  hidden > 0, hidden % 256 == 0;  1 <= batch
+ * ---------------------------------------------------------------------- */
+qws_status qws_q4k_matvec(const void* W, const float* x, float* y, int64_t rows, int64_t hidden,
+                          int batch, qws_stream stream);
+qws_status qws_q6k_matvec(const void* W, const float* x, float* y, int64_t rows, int64_t hidden,
+                          int batch, qws_stream stream);
+
+/* Q4_0 matvec with an optional split-K path (the 262144-row lm_head).
+ *   split_k  0 = library choice, 1 = single pass, S > 1 = S partial sums over
+ *            hidden slices of hidden/S columns (S must divide hidden/256),
+ *            written to the workspace and then added in a fixed order, so
+ *            results are run-to-run identical.
+ *   ws, ws_bytes  workspace of at least
+ *            qws_workspace_bytes(QWS_OP_MATVEC, rows, hidden, 0, batch, S)
+ *            bytes (device, 16-byte aligned); may be NULL when split_k == 1. */
+qws_status qws_q4_0_matvec(const void* W, const float* x, float* y, int64_t rows, int64_t hidden,
+                           int batch, int split_k, void* ws, size_t ws_bytes, qws_stream stream);
+
+/* Any format, with the same split-K option. */
+qws_status qws_matvec(qws_format fmt, const void* W, const float* x, float* y, int64_t rows,
+                      int64_t hidden, int batch, int split_k, void* ws, size_t ws_bytes,
+                      qws_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Fused Q/K/V projection (infer-compute README §Shaders, q4k_qkv_proj): the
+ * three Q4_K matrices share x and are streamed in one launch.
+ *   q = Wq x (q_dim rows), k = Wk x (kv_dim rows), v = Wv x (kv_dim rows)
+ *   Wq q_dim x hidden, Wk and Wv kv_dim x hidden, Q4_K (device, 16-B aligned)
+ *   x [hidden], q [q_dim], k [kv_dim], v [kv_dim] f32 (device)
+ * ---------------------------------------------------------------------- */
+qws_status qws_q4k_qkv_proj(const void* Wq, const void* Wk, const void* Wv, const float* x,
+                            float* q, float* k, float* v, int64_t hidden, int64_t q_dim,
+                            int64_t kv_dim, qws_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Gated FFN (infer-compute README §Shaders "Q4_K fused FFN": q4k_ffn_gate_up,
+ * q4k_geglu_gelu_tanh_down; infer-inference README §WalkFfn steps 1-3):
+ *   g = Wg x, u = Wu x            (one pass over x for both, inter rows)
+ *   m = gelu_tanh(g) * u          (in the epilogue of the gate/up pass)
+ *   y = Wd m                      (hidden rows, inter columns)
+ *   Wg, Wu inter x hidden Q4_K; Wd hidden x inter in wd_fmt (Q6_K or Q4_K)
+ *   x [hidden], y [hidden] f32; ws >= qws_workspace_bytes(QWS_OP_FFN, 0,
+ *   hidden, inter, 1, 0) bytes; m is left in the first inter floats of ws.
+ * ---------------------------------------------------------------------- */
+qws_status qws_q4k_ffn_gate_up_geglu_down(const void* Wg, const void* Wu, const void* Wd,
+                                          qws_format wd_fmt, const float* x, float* y,
+                                          int64_t hidden, int64_t inter, void* ws,
+                                          size_t ws_bytes, qws_stream stream);
+
+/* First half of the FFN alone: m = gelu_tanh(Wg x) * (Wu x), m [inter]. */
+qws_status qws_q4k_ffn_gate_up_geglu(const void* Wg, const void* Wu, const float* x, float* m,
+                                     int64_t hidden, int64_t inter, qws_stream stream);
+
+/* ------------------------------------------------------------------------
+ * rms_norm (infer-compute README §Shaders "Normalization"):
+ *   y[b][i] = x[b][i] / sqrt(mean_j x[b][j]^2 + eps) * w[i]
+ * x, y [batch][n], w [n] f32 (device); y may equal x.  n > 0, batch >= 1.
+ * residual_add (§Shaders "Element-wise"):  h[b][i] += y[b][i].
+ * ---------------------------------------------------------------------- */
+qws_status qws_rms_norm(const float* x, const float* w, float* y, int64_t n, float eps,
+                        int batch, qws_stream stream);
+qws_status qws_residual_add(float* h, const float* y, int64_t n, int batch, qws_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Decoder chain at sequence length 1 (infer-compute README §Architecture:
+ * "single command buffer ... for all 34 layers", §Quick Start decode_token;
+ * infer-inference PERFORMANCE.md §Post-Norm Architecture).  Per layer:
+ *   n1 = rms_norm(h, w_in); q, k, v = QKV(n1); a = v broadcast to the query
+ *   heads (one key: softmax = 1; head i reads kv head i / (nq / nkv));
+ *   o = Wo a;  h1 = h + rms_norm(o, w_post_attn)      (post_norms = 1)
+ *              h1 = h + o                              (post_norms = 0)
+ *   n2 = rms_norm(h1, w_pre_ffn); f = FFN(n2);
+ *   h  = h1 + rms_norm(f, w_post_ffn)  (post_norms = 1)  or  h1 + f.
+ * All layers run in ONE persistent cooperative launch; weights of the next
+ * step stream into shared memory while the grid waits at a step boundary.
+ *   layers   host array of n_layers descriptors (1 <= n_layers <= 64)
+ *   h        [hidden] f32 device, in/out
+ *   ws       >= qws_workspace_bytes(QWS_OP_DECODE_CHAIN, 0, hidden, inter, 1, 0)
+ * Limits: formats Q4_K for q/k/v/o/gate/up, Q4_K or Q6_K for down; hidden,
+ * inter, n_q_heads*head_dim multiples of 256 and <= 20480; n_q_heads a
+ * multiple of n_kv_heads.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  const void *Wq, *Wk, *Wv, *Wo, *Wg, *Wu, *Wd;
+  qws_format fmt_qkv, fmt_o, fmt_gu, fmt_down;
+  const float *w_in, *w_post_attn, *w_pre_ffn, *w_post_ffn; /* [hidden] each */
+} qws_layer;
+
+typedef struct {
+  int64_t hidden, inter;
+  int n_q_heads, n_kv_heads, head_dim;
+  float eps;
+  int post_norms;
+} qws_dims;
+
+qws_status qws_decode_chain(const qws_layer* layers, int n_layers, float* h,
+                            const qws_dims* dims, void* ws, size_t ws_bytes, qws_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Bookkeeping.
+ * qws_workspace_bytes: bytes of workspace an op needs (0 if none); for
+ *   QWS_OP_MATVEC pass the split count in split_k (0 = the library's choice).
+ * qws_last_error: message of the calling thread's last failed call ("" if
+ *   none).  The pointer stays valid until that thread's next call.
+ * qws_device_error: waits for the device, returns the OR of the error codes
+ *   recorded by kernels since the last call (1 = a consumer gave up waiting
+ *   for data, 2 = a producer gave up waiting for a free stage, 4 = a grid
+ *   barrier gave up, 8 = a producer gave up draining its copies) and clears
+ *   them.  Returns QWS_ERR_TIMEOUT when the code is non-zero.
+ * qws_version: library version string.
+ * ---------------------------------------------------------------------- */
+size_t qws_workspace_bytes(qws_op op, int64_t rows, int64_t hidden, int64_t inter, int batch,
+                           int split_k);
+const char* qws_last_error(void);
+qws_status qws_device_error(unsigned* code);
+const char* qws_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QWS_H */

@@ -1,0 +1,91 @@
+"""ctypes loader for libqws.so (built in-tree by build.py).
+
+Loading fails loudly: there is no CPU path behind these calls.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libqws.so")
+
+QWS_OK = 0
+STATUS_NAMES = {
+    0: "QWS_OK", 1: "QWS_ERR_NULL", 2: "QWS_ERR_SHAPE", 3: "QWS_ERR_ALIGN",
+    4: "QWS_ERR_FORMAT", 5: "QWS_ERR_WORKSPACE", 6: "QWS_ERR_CUDA", 7: "QWS_ERR_TIMEOUT",
+}
+Q4_0, Q4_K, Q6_K = 2, 12, 14
+OP_MATVEC, OP_FFN, OP_DECODE_CHAIN = 0, 1, 2
+
+
+class QwsLayer(C.Structure):
+    _fields_ = [
+        ("Wq", C.c_void_p), ("Wk", C.c_void_p), ("Wv", C.c_void_p), ("Wo", C.c_void_p),
+        ("Wg", C.c_void_p), ("Wu", C.c_void_p), ("Wd", C.c_void_p),
+        ("fmt_qkv", C.c_int), ("fmt_o", C.c_int), ("fmt_gu", C.c_int), ("fmt_down", C.c_int),
+        ("w_in", C.c_void_p), ("w_post_attn", C.c_void_p), ("w_pre_ffn", C.c_void_p),
+        ("w_post_ffn", C.c_void_p),
+    ]
+
+
+class QwsDims(C.Structure):
+    _fields_ = [
+        ("hidden", C.c_int64), ("inter", C.c_int64),
+        ("n_q_heads", C.c_int), ("n_kv_heads", C.c_int), ("head_dim", C.c_int),
+        ("eps", C.c_float), ("post_norms", C.c_int),
+    ]
+
+
+# name -> (restype, argtypes); mirrors include/qws.h
+P, F, I64, I, SZ, U = C.c_void_p, C.c_void_p, C.c_int64, C.c_int, C.c_size_t, C.c_uint
+SIGNATURES = {
+    "qws_q4k_matvec": (I, [P, F, F, I64, I64, I, P]),
+    "qws_q6k_matvec": (I, [P, F, F, I64, I64, I, P]),
+    "qws_q4_0_matvec": (I, [P, F, F, I64, I64, I, I, P, SZ, P]),
+    "qws_matvec": (I, [I, P, F, F, I64, I64, I, I, P, SZ, P]),
+    "qws_q4k_qkv_proj": (I, [P, P, P, F, F, F, F, I64, I64, I64, P]),
+    "qws_q4k_ffn_gate_up_geglu_down": (I, [P, P, P, I, F, F, I64, I64, P, SZ, P]),
+    "qws_q4k_ffn_gate_up_geglu": (I, [P, P, F, F, I64, I64, P]),
+    "qws_rms_norm": (I, [F, F, F, I64, C.c_float, I, P]),
+    "qws_residual_add": (I, [F, F, I64, I, P]),
+    "qws_decode_chain": (I, [C.POINTER(QwsLayer), I, F, C.POINTER(QwsDims), P, SZ, P]),
+    "qws_workspace_bytes": (SZ, [I, I64, I64, I64, I, I]),
+    "qws_last_error": (C.c_char_p, []),
+    "qws_device_error": (I, [C.POINTER(U)]),
+    "qws_version": (C.c_char_p, []),
+}
+
+_lib = None
+_lock = threading.Lock()
+
+
+class QwsError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+def lib():
+    """The loaded library.  Raises if libqws.so has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with "
+                    "`python -m quantized_weight_streaming_q4k_gb300.build`")
+            h = C.CDLL(LIB_PATH)
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(h, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = h
+        return _lib
+
+
+def check(status: int) -> None:
+    if status != QWS_OK:
+        msg = lib().qws_last_error()
+        raise QwsError(status, msg.decode() if msg else "")

@@ -1,0 +1,302 @@
+// abi.cu -- the C ABI declared in include/qws.h: argument checks (on the host,
+// before anything is enqueued), workspace sizing and dispatch to launchers.
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <string>
+
+#include "../../include/qws.h"
+#include "launch.h"
+
+namespace {
+
+thread_local std::string tl_error;
+
+qws_status fail(qws_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  tl_error = buf;
+  return st;
+}
+
+qws_status ok() {
+  tl_error.clear();
+  return QWS_OK;
+}
+
+qws_status cuda_fail(cudaError_t e, const char* what, const std::string& why) {
+  if (!why.empty())
+    return fail(e == cudaErrorInvalidValue ? QWS_ERR_SHAPE : QWS_ERR_CUDA, "%s: %s", what,
+                why.c_str());
+  return fail(QWS_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+bool known_format(int fmt) { return fmt == QWS_Q4_0 || fmt == QWS_Q4_K || fmt == QWS_Q6_K; }
+
+constexpr int64_t kMaxHidden = 20480;  // 320 lane units of 64 columns
+
+#define QWS_CHECK_PTR(p) \
+  if (!(p)) return fail(QWS_ERR_NULL, "%s: %s is NULL", fn, #p)
+#define QWS_CHECK_W(p)                                                         \
+  do {                                                                         \
+    QWS_CHECK_PTR(p);                                                          \
+    if (!aligned(p, 16)) return fail(QWS_ERR_ALIGN, "%s: %s is not 16-byte aligned", fn, #p); \
+  } while (0)
+#define QWS_CHECK_F(p)                                                         \
+  do {                                                                         \
+    QWS_CHECK_PTR(p);                                                          \
+    if (!aligned(p, 4)) return fail(QWS_ERR_ALIGN, "%s: %s is not 4-byte aligned", fn, #p); \
+  } while (0)
+
+size_t round256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Split count the library picks: 1 unless batch * (hidden/S)/64 must shrink
+// to fit the 320 consumer lanes.
+int auto_splits(int64_t hidden, int batch) {
+  const int64_t nb = hidden / 256;
+  for (int64_t s = 1; s <= nb; ++s) {
+    if (nb % s) continue;
+    if ((hidden / s / 64) * batch <= 320) return static_cast<int>(s);
+  }
+  return -1;
+}
+
+qws_status check_matvec(const char* fn, int fmt, const void* W, const float* x, const float* y,
+                        int64_t rows, int64_t hidden, int batch) {
+  if (!known_format(fmt)) return fail(QWS_ERR_FORMAT, "%s: unknown format %d", fn, fmt);
+  QWS_CHECK_W(W);
+  QWS_CHECK_F(x);
+  QWS_CHECK_F(y);
+  if (rows < 0) return fail(QWS_ERR_SHAPE, "%s: rows = %lld < 0", fn, (long long)rows);
+  if (hidden <= 0 || hidden % 256)
+    return fail(QWS_ERR_SHAPE, "%s: hidden = %lld is not a positive multiple of 256", fn,
+                (long long)hidden);
+  if (batch < 1) return fail(QWS_ERR_SHAPE, "%s: batch = %d < 1", fn, batch);
+  if (rows > (int64_t(1) << 31) / batch)
+    return fail(QWS_ERR_SHAPE, "%s: rows * batch above 2^31", fn);
+  return QWS_OK;
+}
+
+qws_status run_matvec(const char* fn, int fmt, const void* W, const float* x, float* y,
+                      int64_t rows, int64_t hidden, int batch, int split_k, void* ws,
+                      size_t ws_bytes, cudaStream_t st) {
+  qws_status rc = check_matvec(fn, fmt, W, x, y, rows, hidden, batch);
+  if (rc != QWS_OK) return rc;
+  if (split_k < 0) return fail(QWS_ERR_SHAPE, "%s: split_k = %d < 0", fn, split_k);
+  int S = split_k == 0 ? auto_splits(hidden, batch) : split_k;
+  if (S < 1)
+    return fail(QWS_ERR_SHAPE, "%s: batch %d too large for hidden %lld", fn, batch,
+                (long long)hidden);
+  if ((hidden / 256) % S)
+    return fail(QWS_ERR_SHAPE, "%s: split_k = %d does not divide hidden/256 = %lld", fn, S,
+                (long long)(hidden / 256));
+  const int64_t Ks = hidden / S;
+  if (Ks > kMaxHidden)
+    return fail(QWS_ERR_SHAPE, "%s: hidden / split_k = %lld above %lld; use split_k", fn,
+                (long long)Ks, (long long)kMaxHidden);
+  if ((Ks / 64) * batch > 320)
+    return fail(QWS_ERR_SHAPE, "%s: batch * hidden / split_k / 64 = %lld above 320", fn,
+                (long long)((Ks / 64) * batch));
+  if (S > 1) {
+    if (qws::row_bytes_of(fmt, hidden) % 16 || qws::row_bytes_of(fmt, Ks) % 16)
+      return fail(QWS_ERR_SHAPE, "%s: split rows are not 16-byte multiples for this format", fn);
+    const size_t need = qws_workspace_bytes(QWS_OP_MATVEC, rows, hidden, 0, batch, S);
+    if (!ws || ws_bytes < need)
+      return fail(QWS_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", fn, ws_bytes, need);
+    if (!aligned(ws, 16)) return fail(QWS_ERR_ALIGN, "%s: ws is not 16-byte aligned", fn);
+  }
+  if (rows == 0) return ok();
+  std::string why;
+  qws::Seg seg{static_cast<const uint8_t*>(W), S > 1 ? static_cast<float*>(ws) : y, rows, 0};
+  cudaError_t e = qws::launch_matvec(fmt, qws::EPI_STORE, &seg, 1, nullptr, x, hidden, batch, S,
+                                     st, &why);
+  if (e != cudaSuccess) return cuda_fail(e, fn, why);
+  if (S > 1) {
+    e = qws::launch_splitk_reduce(static_cast<const float*>(ws), y, rows * batch, S, st);
+    if (e != cudaSuccess) return cuda_fail(e, fn, "");
+  }
+  return ok();
+}
+
+}  // namespace
+
+extern "C" {
+
+qws_status qws_q4k_matvec(const void* W, const float* x, float* y, int64_t rows, int64_t hidden,
+                          int batch, qws_stream stream) {
+  return run_matvec("qws_q4k_matvec", QWS_Q4_K, W, x, y, rows, hidden, batch, 1, nullptr, 0,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+qws_status qws_q6k_matvec(const void* W, const float* x, float* y, int64_t rows, int64_t hidden,
+                          int batch, qws_stream stream) {
+  return run_matvec("qws_q6k_matvec", QWS_Q6_K, W, x, y, rows, hidden, batch, 1, nullptr, 0,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+qws_status qws_q4_0_matvec(const void* W, const float* x, float* y, int64_t rows, int64_t hidden,
+                           int batch, int split_k, void* ws, size_t ws_bytes, qws_stream stream) {
+  return run_matvec("qws_q4_0_matvec", QWS_Q4_0, W, x, y, rows, hidden, batch, split_k, ws,
+                    ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+qws_status qws_matvec(qws_format fmt, const void* W, const float* x, float* y, int64_t rows,
+                      int64_t hidden, int batch, int split_k, void* ws, size_t ws_bytes,
+                      qws_stream stream) {
+  return run_matvec("qws_matvec", fmt, W, x, y, rows, hidden, batch, split_k, ws, ws_bytes,
+                    reinterpret_cast<cudaStream_t>(stream));
+}
+
+qws_status qws_q4k_qkv_proj(const void* Wq, const void* Wk, const void* Wv, const float* x,
+                            float* q, float* k, float* v, int64_t hidden, int64_t q_dim,
+                            int64_t kv_dim, qws_stream stream) {
+  const char* fn = "qws_q4k_qkv_proj";
+  QWS_CHECK_W(Wq);
+  QWS_CHECK_W(Wk);
+  QWS_CHECK_W(Wv);
+  QWS_CHECK_F(x);
+  QWS_CHECK_F(q);
+  QWS_CHECK_F(k);
+  QWS_CHECK_F(v);
+  if (hidden <= 0 || hidden % 256 || hidden > kMaxHidden)
+    return fail(QWS_ERR_SHAPE, "%s: hidden = %lld (need a multiple of 256 in (0, 20480])", fn,
+                (long long)hidden);
+  if (q_dim < 0 || kv_dim < 0) return fail(QWS_ERR_SHAPE, "%s: negative q_dim / kv_dim", fn);
+  if (q_dim + 2 * kv_dim == 0) return ok();
+  qws::Seg segs[3];
+  int n = 0;
+  if (q_dim) segs[n++] = qws::Seg{static_cast<const uint8_t*>(Wq), q, q_dim, 0};
+  if (kv_dim) {
+    segs[n++] = qws::Seg{static_cast<const uint8_t*>(Wk), k, kv_dim, 0};
+    segs[n++] = qws::Seg{static_cast<const uint8_t*>(Wv), v, kv_dim, 0};
+  }
+  std::string why;
+  cudaError_t e = qws::launch_matvec(QWS_Q4_K, qws::EPI_STORE, segs, n, nullptr, x, hidden, 1, 1,
+                                     reinterpret_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess) return cuda_fail(e, fn, why);
+  return ok();
+}
+
+static qws_status check_ffn_shape(const char* fn, int64_t hidden, int64_t inter) {
+  if (hidden <= 0 || hidden % 256 || hidden > kMaxHidden)
+    return fail(QWS_ERR_SHAPE, "%s: hidden = %lld (need a multiple of 256 in (0, 20480])", fn,
+                (long long)hidden);
+  if (inter <= 0 || inter % 256 || inter > kMaxHidden)
+    return fail(QWS_ERR_SHAPE, "%s: inter = %lld (need a multiple of 256 in (0, 20480])", fn,
+                (long long)inter);
+  return QWS_OK;
+}
+
+qws_status qws_q4k_ffn_gate_up_geglu(const void* Wg, const void* Wu, const float* x, float* m,
+                                     int64_t hidden, int64_t inter, qws_stream stream) {
+  const char* fn = "qws_q4k_ffn_gate_up_geglu";
+  QWS_CHECK_W(Wg);
+  QWS_CHECK_W(Wu);
+  QWS_CHECK_F(x);
+  QWS_CHECK_F(m);
+  qws_status rc = check_ffn_shape(fn, hidden, inter);
+  if (rc != QWS_OK) return rc;
+  qws::Seg seg{static_cast<const uint8_t*>(Wg), m, inter, 0};
+  std::string why;
+  cudaError_t e = qws::launch_matvec(QWS_Q4_K, qws::EPI_GEGLU, &seg, 1,
+                                     static_cast<const uint8_t*>(Wu), x, hidden, 1, 1,
+                                     reinterpret_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess) return cuda_fail(e, fn, why);
+  return ok();
+}
+
+qws_status qws_q4k_ffn_gate_up_geglu_down(const void* Wg, const void* Wu, const void* Wd,
+                                          qws_format wd_fmt, const float* x, float* y,
+                                          int64_t hidden, int64_t inter, void* ws,
+                                          size_t ws_bytes, qws_stream stream) {
+  const char* fn = "qws_q4k_ffn_gate_up_geglu_down";
+  QWS_CHECK_W(Wg);
+  QWS_CHECK_W(Wu);
+  QWS_CHECK_W(Wd);
+  QWS_CHECK_F(x);
+  QWS_CHECK_F(y);
+  if (wd_fmt != QWS_Q4_K && wd_fmt != QWS_Q6_K)
+    return fail(QWS_ERR_FORMAT, "%s: wd_fmt must be Q4_K or Q6_K", fn);
+  qws_status rc = check_ffn_shape(fn, hidden, inter);
+  if (rc != QWS_OK) return rc;
+  const size_t need = qws_workspace_bytes(QWS_OP_FFN, 0, hidden, inter, 1, 0);
+  if (!ws || ws_bytes < need)
+    return fail(QWS_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", fn, ws_bytes, need);
+  if (!aligned(ws, 16)) return fail(QWS_ERR_ALIGN, "%s: ws is not 16-byte aligned", fn);
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  float* m = static_cast<float*>(ws);
+  qws::Seg seg{static_cast<const uint8_t*>(Wg), m, inter, 0};
+  std::string why;
+  cudaError_t e = qws::launch_matvec(QWS_Q4_K, qws::EPI_GEGLU, &seg, 1,
+                                     static_cast<const uint8_t*>(Wu), x, hidden, 1, 1, st, &why);
+  if (e != cudaSuccess) return cuda_fail(e, fn, why);
+  qws::Seg dseg{static_cast<const uint8_t*>(Wd), y, hidden, 0};
+  e = qws::launch_matvec(wd_fmt, qws::EPI_STORE, &dseg, 1, nullptr, m, inter, 1, 1, st, &why);
+  if (e != cudaSuccess) return cuda_fail(e, fn, why);
+  return ok();
+}
+
+qws_status qws_rms_norm(const float* x, const float* w, float* y, int64_t n, float eps,
+                        int batch, qws_stream stream) {
+  const char* fn = "qws_rms_norm";
+  QWS_CHECK_F(x);
+  QWS_CHECK_F(w);
+  QWS_CHECK_F(y);
+  if (n <= 0) return fail(QWS_ERR_SHAPE, "%s: n = %lld <= 0", fn, (long long)n);
+  if (batch < 1 || batch > 65535) return fail(QWS_ERR_SHAPE, "%s: batch = %d", fn, batch);
+  if (!(eps >= 0.f)) return fail(QWS_ERR_SHAPE, "%s: eps must be >= 0", fn);
+  cudaError_t e =
+      qws::launch_rms_norm(x, w, y, n, eps, batch, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn, "");
+  return ok();
+}
+
+qws_status qws_residual_add(float* h, const float* y, int64_t n, int batch, qws_stream stream) {
+  const char* fn = "qws_residual_add";
+  QWS_CHECK_F(h);
+  QWS_CHECK_F(y);
+  if (n < 0) return fail(QWS_ERR_SHAPE, "%s: n = %lld < 0", fn, (long long)n);
+  if (batch < 1) return fail(QWS_ERR_SHAPE, "%s: batch = %d < 1", fn, batch);
+  if (n == 0) return ok();
+  cudaError_t e =
+      qws::launch_residual_add(h, y, n, batch, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn, "");
+  return ok();
+}
+
+size_t qws_workspace_bytes(qws_op op, int64_t rows, int64_t hidden, int64_t inter, int batch,
+                           int split_k) {
+  switch (op) {
+    case QWS_OP_MATVEC: {
+      if (rows <= 0 || hidden <= 0 || batch < 1) return 0;
+      const int S = split_k == 0 ? auto_splits(hidden, batch) : split_k;
+      if (S <= 1) return 0;
+      return round256(sizeof(float) * static_cast<size_t>(S) * batch * rows);
+    }
+    case QWS_OP_FFN:
+      return inter > 0 ? round256(sizeof(float) * static_cast<size_t>(inter)) : 0;
+    case QWS_OP_DECODE_CHAIN:
+      return qws::chain_workspace_bytes(hidden, inter);
+  }
+  return 0;
+}
+
+const char* qws_last_error(void) { return tl_error.c_str(); }
+
+qws_status qws_device_error(unsigned* code) {
+  if (!code) return fail(QWS_ERR_NULL, "qws_device_error: code is NULL");
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return cuda_fail(e, "qws_device_error", "");
+  *code = qws::read_clear_matvec_errors() | qws::read_clear_chain_errors();
+  return *code ? fail(QWS_ERR_TIMEOUT, "device error code 0x%x", *code) : ok();
+}
+
+const char* qws_version(void) { return "qws 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

@@ -1,0 +1,414 @@
+// engine.cuh -- the weight-streaming pipeline shared by every kernel.
+//
+// One CTA = one producer warp + one reducer warp + C consumer threads
+// (C <= kMaxConsumers), specialised and linked only by mbarriers:
+//
+//  producer (one lane)  : walks the CTA's tiles in order; for each tile waits
+//                         for a free ring stage, then issues 1-D bulk copies
+//                         (cp.async.bulk, TMA) of the tile's packed rows from
+//                         HBM into that stage; completion is counted in bytes
+//                         on the stage's "full" mbarrier.  Weights never depend
+//                         on activations, so the producer runs ahead of the
+//                         consumers by up to the ring depth.
+//  consumers            : each thread owns one 64-column lane unit of the row
+//                         and one row slot g; its activations live in
+//                         registers for the whole phase (formats.cuh).  For a
+//                         landed stage, slot g computes rows g, g+G, ...; every
+//                         thread writes one partial per row into the stage's
+//                         partial buffer, then each warp arrives on the stage's
+//                         "ready" mbarrier.  Consumers never wait for each other.
+//  reducer (one warp)   : waits for "ready", sums each row's U partials in a
+//                         fixed order (deterministic), runs the epilogue
+//                         (store / GEGLU), then frees the stage ("empty").
+//
+// A tile is T consecutive rows of one matrix segment (QKV stacks three
+// segments) or, for the gated FFN, T rows of the gate matrix followed by the
+// same T rows of the up matrix in one stage.  Every wait is bounded
+// (device_common.cuh); a timeout seen by any consumer ends all consumers at the
+// next named barrier.
+#pragma once
+
+#include <cstdint>
+
+#include "device_common.cuh"
+#include "formats.cuh"
+
+namespace qws {
+
+constexpr int kMaxSeg = 3;
+constexpr int kMaxConsumers = 320;
+constexpr int kProducerThreads = 32;
+constexpr int kReducerThreads = 32;
+constexpr int kRoleThreads = kProducerThreads + kReducerThreads;  // consumers start here
+constexpr int kConsumerBar = 1;     // named barrier id used by the consumer threads
+
+enum : int { EPI_STORE = 0, EPI_GEGLU = 1 };
+
+struct Seg {
+  const uint8_t* W;   // packed rows of this segment
+  float* y;           // one output per row
+  int64_t rows;
+  int tiles;          // ceil(rows / T)
+};
+
+struct Phase {
+  int fmt;            // 2 (Q4_0), 12 (Q4_K), 14 (Q6_K)
+  int epi;            // EPI_STORE or EPI_GEGLU
+  int nseg;
+  Seg seg[kMaxSeg];
+  const uint8_t* W2;  // EPI_GEGLU: up matrix, same shape as seg[0] (the gate)
+  int64_t K;          // columns (weights per row)
+  int64_t row_bytes;
+  int B;              // activation vectors (batch); x is [B][K], y is [B][rows]
+  int U;              // lane units per row = K / 64
+  int G;              // row slots per activation vector (B * G * U <= consumers)
+  int T;              // rows per tile (per matrix for EPI_GEGLU)
+  int n_tiles;
+  int64_t row_stride; // bytes between consecutive rows in global memory
+                      // (> row_bytes when the phase covers a column slice)
+  int cta0, ncta;     // CTAs [cta0, cta0 + ncta) of the grid serve this phase
+};
+
+struct TileRef {
+  const uint8_t* W;   // segment's weights (row 0 of the segment)
+  float* y;           // segment's outputs
+  int64_t seg_rows;
+  int64_t r0;         // first row of the tile within the segment
+  int nrows;
+};
+
+// Segment lookup with constant indices only, so a Phase never needs to live
+// in local memory.
+__device__ __forceinline__ TileRef tile_ref(const Phase& P, int t) {
+  TileRef tr;
+  tr.W = P.seg[0].W;
+  tr.y = P.seg[0].y;
+  tr.seg_rows = P.seg[0].rows;
+  int prev_tiles = P.seg[0].tiles;
+  bool more = true;
+#pragma unroll
+  for (int i = 1; i < kMaxSeg; ++i) {
+    if (more && i < P.nseg && t >= prev_tiles) {
+      t -= prev_tiles;
+      tr.W = P.seg[i].W;
+      tr.y = P.seg[i].y;
+      tr.seg_rows = P.seg[i].rows;
+      prev_tiles = P.seg[i].tiles;
+    } else {
+      more = false;
+    }
+  }
+  tr.r0 = static_cast<int64_t>(t) * P.T;
+  const int64_t rem = tr.seg_rows - tr.r0;
+  tr.nrows = static_cast<int>(rem < P.T ? rem : P.T);
+  return tr;
+}
+
+// Shared-memory ring.  Layout: full[S], ready[S], empty[S] mbarriers, S
+// partial buffers of red_floats floats (one per stage), the activation
+// staging buffer (xs_floats), then S stages of stage_bytes (128-B aligned,
+// each with >= 16 B of slack after the largest tile for the 2-byte-aligned
+// Q6_K word loads).
+// Partial-buffer and staging row stride: U rounded up to an odd number of
+// floats, so lanes walking rows (or units) hit distinct banks.
+__host__ __device__ constexpr int red_stride(int U) { return U | 1; }
+
+struct Ring {
+  uint64_t* full;
+  uint64_t* ready;
+  uint64_t* empty;
+  float* red;
+  float* xs;          // activation staging, transposed [64][U | 1]
+  uint8_t* stages;
+  uint32_t S;
+  uint32_t stage_bytes;
+  uint32_t red_floats;
+  uint32_t xs_floats;
+  __device__ __forceinline__ uint8_t* stage(uint32_t s) const {
+    return stages + static_cast<size_t>(s) * stage_bytes;
+  }
+};
+
+__host__ __device__ constexpr size_t ring_header_bytes(uint32_t S, uint32_t red_floats,
+                                                       uint32_t xs_floats) {
+  return ((24u * S + 4u * S * red_floats + 4u * xs_floats + 127u) / 128u) * 128u;
+}
+
+__host__ __device__ constexpr size_t ring_smem_bytes(uint32_t S, uint32_t stage_bytes,
+                                                    uint32_t red_floats, uint32_t xs_floats) {
+  return ring_header_bytes(S, red_floats, xs_floats) + static_cast<size_t>(S) * stage_bytes;
+}
+
+__device__ __forceinline__ Ring make_ring(uint8_t* smem, uint32_t S, uint32_t stage_bytes,
+                                          uint32_t red_floats, uint32_t xs_floats) {
+  Ring R;
+  R.full = reinterpret_cast<uint64_t*>(smem);
+  R.ready = R.full + S;
+  R.empty = R.ready + S;
+  R.red = reinterpret_cast<float*>(R.empty + S);
+  R.xs = R.red + static_cast<size_t>(S) * red_floats;
+  R.stages = smem + ring_header_bytes(S, red_floats, xs_floats);
+  R.S = S;
+  R.stage_bytes = stage_bytes;
+  R.red_floats = red_floats;
+  R.xs_floats = xs_floats;
+  return R;
+}
+
+// Called by one thread before the role split (followed by __syncthreads()).
+__device__ __forceinline__ void ring_init(const Ring& R, int consumer_warps) {
+  for (uint32_t s = 0; s < R.S; ++s) {
+    mbar_init(&R.full[s], 1);
+    mbar_init(&R.ready[s], static_cast<uint32_t>(consumer_warps));
+    mbar_init(&R.empty[s], 1);
+  }
+  fence_barrier_init();
+}
+
+// ------------------------------------------------------------------ producer
+// Fills stage s for tile t of phase P.  Rows are contiguous, so a tile is one
+// copy (two for the gated pair).  A copy's start is 16-byte aligned because T
+// is a multiple of the rows needed to make T * row_bytes a multiple of 16; only
+// the last tile of a matrix can end off a 16-byte boundary, and those < 16 tail
+// bytes are moved with plain loads/stores before the arrive (release) that
+// publishes the stage.
+__device__ __forceinline__ void copy_tail(uint8_t* dst, const uint8_t* src, uint32_t from,
+                                          uint32_t to) {
+  for (uint32_t i = from; i < to; ++i) dst[i] = src[i];
+}
+
+__device__ __forceinline__ void fill_stage(const Phase& P, int t, const Ring& R, uint32_t s,
+                                           uint64_t pol) {
+  const TileRef tr = tile_ref(P, t);
+  uint8_t* dst = R.stage(s);
+  const uint32_t bytes = static_cast<uint32_t>(tr.nrows * P.row_bytes);
+  const uint32_t bulk = bytes & ~15u;
+  const uint8_t* g = tr.W + tr.r0 * P.row_bytes;
+  const bool pair = P.epi == EPI_GEGLU;
+  const uint8_t* up = pair ? P.W2 + tr.r0 * P.row_bytes : nullptr;
+  uint8_t* dst_up = dst + static_cast<size_t>(P.T) * P.row_bytes;
+  if (P.row_stride != P.row_bytes) {
+    // column slice (split-K): one copy per row; row_bytes and row_stride are
+    // multiples of 16 here (checked on the host)
+    mbar_arrive_expect_tx(&R.full[s], bytes);
+    const uint8_t* src = tr.W + tr.r0 * P.row_stride;
+    for (int i = 0; i < tr.nrows; ++i)
+      bulk_copy_g2s(dst + static_cast<size_t>(i) * P.row_bytes, src + i * P.row_stride,
+                    static_cast<uint32_t>(P.row_bytes), &R.full[s], pol);
+    return;
+  }
+  copy_tail(dst, g, bulk, bytes);
+  if (pair) copy_tail(dst_up, up, bulk, bytes);
+  mbar_arrive_expect_tx(&R.full[s], pair ? 2u * bulk : bulk);
+  if (bulk) {
+    bulk_copy_g2s(dst, g, bulk, &R.full[s], pol);
+    if (pair) bulk_copy_g2s(dst_up, up, bulk, &R.full[s], pol);
+  }
+}
+
+// PhaseList: count() and get(i) -> Phase, evaluated identically by producer
+// and consumers.
+template <class PhaseList>
+__device__ void run_producer(const PhaseList& L, const Ring& R, unsigned* err) {
+  const uint64_t pol = l2_policy_evict_first();
+  uint32_t k = 0;
+  bool ok = true;
+  const int nph = L.count();
+  for (int p = 0; p < nph && ok; ++p) {
+    const Phase P = L.get(p);
+    const int c = static_cast<int>(blockIdx.x) - P.cta0;
+    if (c < 0 || c >= P.ncta) continue;
+    for (int t = c; t < P.n_tiles; t += P.ncta) {
+      const uint32_t s = k % R.S, ph = (k / R.S) & 1u;
+      if (!mbar_wait(&R.empty[s], ph ^ 1u)) {
+        atomicOr(err, kErrEmptyWait);
+        ok = false;
+        break;
+      }
+      fill_stage(P, t, R, s, pol);
+      ++k;
+    }
+  }
+  // Do not leave while copies into this CTA's shared memory are in flight.
+  const uint32_t first = k > R.S ? k - R.S : 0u;
+  for (uint32_t i = first; i < k; ++i) {
+    if (!mbar_wait(&R.full[i % R.S], (i / R.S) & 1u)) atomicOr(err, kErrDrain);
+  }
+}
+
+// ------------------------------------------------------------------ consumers
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// Activation loaders: x(col) for the phase's input vector.
+struct XPlain {            // global, written before this launch
+  const float* p;
+  __device__ __forceinline__ float operator()(int64_t i) const { return p[i]; }
+};
+struct XCoherent {         // global, written by other CTAs of this launch
+  const float* p;
+  __device__ __forceinline__ float operator()(int64_t i) const { return ld_cg(p + i); }
+};
+struct XShared {           // shared memory, prepared by this CTA
+  const float* p;
+  __device__ __forceinline__ float operator()(int64_t i) const { return p[i]; }
+};
+
+// Unit-local activation loader over the transposed staging buffer:
+// element l of unit u lives at xs[l * US + u] (US odd: conflict-free reads
+// for consecutive u, and conflict-free writes for consecutive l).
+struct XUnit {
+  const float* xs;
+  int US;
+  int u;
+  __device__ __forceinline__ float operator()(int l) const { return xs[l * US + u]; }
+};
+
+// Copies activation vector `src` (K columns) into the transposed staging
+// buffer with coalesced reads.  Called by all C consumer threads.
+template <class Unit, class Src>
+__device__ __forceinline__ void stage_x(float* xs, int US, const Src& src, int64_t K, int ctid,
+                                        int C) {
+  for (int64_t col = ctid; col < K; col += C) {
+    int u, l;
+    Unit::unit_of(col, u, l);
+    xs[l * US + u] = src(col);
+  }
+}
+
+// Consume all tiles of phase P assigned to this CTA.  `k` is the CTA's running
+// tile counter (producer and reducer walk the same order).  Thread ctid owns
+// unit u = ctid % U and slot g = ctid / U; slot g serves activation vector
+// b = g / G and rows gg, gg + G, ... of each tile (gg = g % G).  x_of(b)
+// returns a column loader of vector b; vectors are staged one at a time
+// through shared memory.  With STAGED = false the caller has already written
+// the single vector (B = 1) into R.xs.  Returns false on a timeout.
+template <class Unit, bool STAGED = true, class XOf>
+__device__ __forceinline__ bool consume_phase(const Phase& P, const Ring& R, uint32_t& k,
+                                              const XOf& x_of, int ctid, int C, unsigned* err) {
+  const int cta = static_cast<int>(blockIdx.x) - P.cta0;
+  if (cta < 0 || cta >= P.ncta) return true;
+  const int U = P.U, G = P.G, US = red_stride(P.U);
+  const int u = ctid % U, g = ctid / U;
+  const int b = g / G, gg = g % G;
+  const bool active = b < P.B;
+  const int lane = ctid & 31;
+  const bool pair = P.epi == EPI_GEGLU;
+  const int slots = pair ? 2 * P.T : P.T;      // partial rows per vector
+  Unit unit;
+  if (STAGED) {
+    for (int bb = 0; bb < P.B; ++bb) {
+      if (bb) bar_sync(kConsumerBar, C);       // previous vector fully read
+      stage_x<Unit>(R.xs, US, x_of(bb), P.K, ctid, C);
+      bar_sync(kConsumerBar, C);
+      if (active && b == bb) unit.setup(u, XUnit{R.xs, US, u});
+    }
+  } else if (active) {
+    unit.setup(u, XUnit{R.xs, US, u});
+  }
+  for (int t = cta; t < P.n_tiles; t += P.ncta, ++k) {
+    const uint32_t s = k % R.S, ph = (k / R.S) & 1u;
+    if (!mbar_wait(&R.full[s], ph)) {
+      atomicOr(err, kErrFullWait);
+      return false;
+    }
+    const TileRef tr = tile_ref(P, t);
+    const uint8_t* st = R.stage(s);
+    float* red = R.red + static_cast<size_t>(s) * R.red_floats;
+    const int nr = pair ? 2 * tr.nrows : tr.nrows;
+    if (active) {
+      for (int r = gg; r < nr; r += G) {
+        const int slot = (pair && r >= tr.nrows) ? P.T + (r - tr.nrows) : r;
+        red[(b * slots + slot) * US + u] = unit.row(st + static_cast<size_t>(slot) * P.row_bytes);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&R.ready[s]);
+  }
+  return true;
+}
+
+// Reduce all tiles of phase P for this CTA (one warp).  Output i of a tile is
+// (vector b, row o), i = b * nrows + o.  Lanes form groups of gsz lanes per
+// output (gsz = 32 when the tile has one output, 1 when it has >= 32); each
+// lane adds a fixed strided subset of the row's partials, then the group adds
+// its lanes with a fixed xor tree: the order never changes between runs.
+// epi(P, tr, b, o, v, v2) stores the result (v2 = the up row for GEGLU).
+template <class Epi>
+__device__ __forceinline__ bool reduce_phase(const Phase& P, const Ring& R, uint32_t& k,
+                                             const Epi& epi, unsigned* err) {
+  const int cta = static_cast<int>(blockIdx.x) - P.cta0;
+  if (cta < 0 || cta >= P.ncta) return true;
+  const int lane = threadIdx.x & 31;
+  const int U = P.U, US = red_stride(P.U);
+  const bool pair = P.epi == EPI_GEGLU;
+  const int slots = pair ? 2 * P.T : P.T;
+  for (int t = cta; t < P.n_tiles; t += P.ncta, ++k) {
+    const uint32_t s = k % R.S, ph = (k / R.S) & 1u;
+    if (!mbar_wait(&R.ready[s], ph)) {
+      atomicOr(err, kErrFullWait);
+      return false;
+    }
+    const TileRef tr = tile_ref(P, t);
+    const float* red = R.red + static_cast<size_t>(s) * R.red_floats;
+    const int n_out = P.B * tr.nrows;
+    int gsz = 32;
+    while (gsz > 1 && gsz * n_out > 32) gsz >>= 1;
+    const int per_pass = 32 / gsz;
+    const int sub = lane % gsz;
+    for (int base = 0; base < n_out; base += per_pass) {
+      const int oi = base + lane / gsz;
+      const bool valid = oi < n_out;
+      const int ob = valid ? oi / tr.nrows : 0;
+      const int o = valid ? oi - ob * tr.nrows : 0;
+      const float* rr = red + (ob * slots + o) * US;
+      float v = 0.f, v2 = 0.f;
+      if (valid) {
+        for (int c = sub; c < U; c += gsz) v += rr[c];
+        if (pair)
+          for (int c = sub; c < U; c += gsz) v2 += rr[P.T * US + c];
+      }
+      for (int w = gsz >> 1; w > 0; w >>= 1) {
+        v += __shfl_xor_sync(0xFFFFFFFFu, v, w);
+        v2 += __shfl_xor_sync(0xFFFFFFFFu, v2, w);
+      }
+      if (valid && sub == 0) epi(P, tr, ob, o, v, v2);
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&R.empty[s]);
+  }
+  return true;
+}
+
+// GELU, tanh form: 0.5 t (1 + tanh(sqrt(2/pi) (t + 0.044715 t^3)))
+// (infer-compute README §Shaders, geglu_gelu_tanh).
+__device__ __forceinline__ float gelu_tanh(float t) {
+  const float k = 0.7978845608028654f;  // sqrt(2/pi)
+  return 0.5f * t * (1.0f + tanhf(k * fmaf(0.044715f * t, t * t, t)));
+}
+
+struct EpiStore {
+  __device__ __forceinline__ void operator()(const Phase& P, const TileRef& tr, int b, int o,
+                                             float v, float) const {
+    tr.y[b * tr.seg_rows + tr.r0 + o] = v;
+  }
+};
+
+struct EpiGeglu {
+  __device__ __forceinline__ void operator()(const Phase& P, const TileRef& tr, int b, int o,
+                                             float g, float u) const {
+    tr.y[b * tr.seg_rows + tr.r0 + o] = gelu_tanh(g) * u;
+  }
+};
+
+// Loader factories: vector b of a [B][stride] activation array.
+struct XOfPlain {
+  const float* x;
+  int64_t stride;
+  __device__ __forceinline__ XPlain operator()(int b) const { return XPlain{x + b * stride}; }
+};
+
+}  // namespace qws

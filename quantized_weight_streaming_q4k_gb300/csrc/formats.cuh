@@ -1,0 +1,329 @@
+// formats.cuh -- per-lane decoders for the three GGUF block formats.
+//
+// Block layouts (infer-compute README, §Design Principles "GGUF-compatible" and
+// §Shaders Q4_0 / Q4_K / Q6_K rows; the public GGUF layouts):
+//   Q4_K 144 B / 256 w : f16 d, f16 dmin, 12 B packed 6-bit scales+mins, 128 B nibbles
+//                        w = d*sc[s]*q - dmin*m[s]     (eight 32-weight sub-blocks)
+//   Q6_K 210 B / 256 w : 128 B low nibbles, 64 B 2-bit highs, 16 int8 scales, f16 d
+//                        w = d*sc[i/16]*(q-32)
+//   Q4_0  18 B /  32 w : f16 d, 16 B nibbles;  w = d*(q-8)
+//
+// Lane unit.  Every lane owns a fixed group of 64 columns of the row ("unit")
+// and keeps the matching 64 activations in registers for the whole phase
+// (x-stationary).  The weight bytes of one row stream through shared memory;
+// for each row the lane decodes its unit and returns a partial dot product.
+//
+// Decode without int->float conversion.  A 4- or 6-bit field masked in place
+// inside a 32-bit word, with every other bit zero, is a valid subnormal
+// float: q * 2^(pos - 149) where pos is the field's bit position (pos <= 16,
+// so the field stays below the exponent bits).  The activation for that weight
+// is stored pre-scaled as x * 2^(kE - pos), so the FMA product is exactly
+// q * x * 2^(kE - 149) = q * x * 2^-60, accumulated in f32.  One LOP per weight
+// replaces shift + convert; the 2^60 and the sub-block scales are applied once
+// per sub-block.  Fields whose bit position would reach the exponent are
+// shifted down by 8 or 12 first.  Pre-scaling by a power of two is exact for
+// |x| in [2^-66, 2^38]; outside that range products lose bits or overflow.
+#pragma once
+
+#include <cstdint>
+
+#include "device_common.cuh"
+
+namespace qws {
+
+constexpr int kE = 89;                 // x' = x * 2^(kE - pos)
+constexpr int kUnitWeights = 64;       // columns per lane unit, all formats
+
+__device__ __forceinline__ float bits(uint32_t v) { return __uint_as_float(v); }
+
+// ---------------------------------------------------------------------------
+// Nibble positions inside one 32-bit word of four bytes (b = byte 0..3).
+// Low nibble of byte b:  b=0 bits 0-3, b=1 bits 8-11, b=2 bits 16-19 (direct);
+//                        b=3 bits 24-27 -> (w >> 12) bits 12-15.
+// High nibble of byte b: b=0 bits 4-7, b=1 bits 12-15 (direct);
+//                        b=2 bits 20-23 -> (w >> 12) bits 8-11;
+//                        b=3 bits 28-31 -> (w >> 12) bits 16-19.
+// ---------------------------------------------------------------------------
+__host__ __device__ constexpr int pos_lo(int b) { return b == 0 ? 0 : b == 1 ? 8 : b == 2 ? 16 : 12; }
+__host__ __device__ constexpr int pos_hi(int b) { return b == 0 ? 4 : b == 1 ? 12 : b == 2 ? 8 : 16; }
+
+// lo[0..3] += low nibbles of bytes 0..3 times xl[0..3]; same for the high
+// nibbles with xh.  Two accumulator pairs per nibble class (packed FMA).
+__device__ __forceinline__ void nibble_word(uint32_t w, const float* xl, const float* xh,
+                                            float& l0, float& l1, float& h0, float& h1) {
+  const uint32_t s = w >> 12;
+  fma2(l0, l1, bits(w & 0xFu), bits(w & 0xF00u), xl[0], xl[1]);
+  fma2(l0, l1, bits(w & 0xF0000u), bits(s & 0xF000u), xl[2], xl[3]);
+  fma2(h0, h1, bits(w & 0xF0u), bits(w & 0xF000u), xh[0], xh[1]);
+  fma2(h0, h1, bits(s & 0xF00u), bits(s & 0xF0000u), xh[2], xh[3]);
+}
+
+// ---------------------------------------------------------------------------
+// Q4_K.  Unit u -> super-block kb = u/4, chunk c = u%4: the 32 qs bytes
+// qs[32c .. 32c+31] (weights 64c+l of sub-block 2c in the low nibbles and
+// 64c+32+l of sub-block 2c+1 in the high nibbles) plus the block header.
+// ---------------------------------------------------------------------------
+struct UnitQ4K {
+  static constexpr int kFmt = 12;
+  static constexpr int kBlockW = 256;
+  static constexpr int kBlockBytes = 144;
+  float xa[32];   // sub-block 2c,   column 64c + l,      pre-scaled
+  float xb[32];   // sub-block 2c+1, column 64c + 32 + l, pre-scaled
+  float sxa, sxb; // plain sums of x over the two sub-blocks
+  uint32_t off;   // byte offset of the block header within the row
+  uint32_t qoff;  // byte offset of the chunk within the block
+  uint32_t sh;    // bit offset of the scale pair inside the 4-scale word
+  bool hi;        // sub-blocks 4..7 (scales split across two byte groups)
+
+  // Unit u covers columns 64u .. 64u + 63; unit-local index l = col % 64.
+  __device__ __forceinline__ static void unit_of(int64_t col, int& u, int& l) {
+    u = static_cast<int>(col >> 6);
+    l = static_cast<int>(col & 63);
+  }
+
+  // xu(l): activation of unit-local column l (0..63).
+  template <class XU>
+  __device__ __forceinline__ void setup(int u, const XU& xu) {
+    const int kb = u >> 2, c = u & 3;
+    off = static_cast<uint32_t>(kb) * kBlockBytes;
+    qoff = 16u + 32u * c;
+    sh = 16u * (c & 1);
+    hi = c >= 2;
+    float sa = 0.f, sb = 0.f;
+#pragma unroll
+    for (int l = 0; l < 32; ++l) {
+      const float va = xu(l), vb = xu(32 + l);
+      sa += va;
+      sb += vb;
+      xa[l] = va * exp2i(kE - pos_lo(l & 3));
+      xb[l] = vb * exp2i(kE - pos_hi(l & 3));
+    }
+    sxa = sa;
+    sxb = sb;
+  }
+
+  // Partial dot product of this unit with the row whose bytes start at rp.
+  __device__ __forceinline__ float row(const uint8_t* rp) const {
+    const uint8_t* bp = rp + off;
+    const uint4 hd = *reinterpret_cast<const uint4*>(bp);
+    const uint4 q0 = *reinterpret_cast<const uint4*>(bp + qoff);
+    const uint4 q1 = *reinterpret_cast<const uint4*>(bp + qoff + 16);
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+    nibble_word(q0.x, xa + 0, xb + 0, a0, a1, b0, b1);
+    nibble_word(q0.y, xa + 4, xb + 4, a0, a1, b0, b1);
+    nibble_word(q0.z, xa + 8, xb + 8, a0, a1, b0, b1);
+    nibble_word(q0.w, xa + 12, xb + 12, a0, a1, b0, b1);
+    nibble_word(q1.x, xa + 16, xb + 16, a0, a1, b0, b1);
+    nibble_word(q1.y, xa + 20, xb + 20, a0, a1, b0, b1);
+    nibble_word(q1.z, xa + 24, xb + 24, a0, a1, b0, b1);
+    nibble_word(q1.w, xa + 28, xb + 28, a0, a1, b0, b1);
+    // 6-bit scales / mins of all eight sub-blocks, one per byte:
+    //   s < 4 : sc[s] & 63 and sc[s+4] & 63
+    //   s >= 4: (sc[s+4] & 15) | (sc[s-4] >> 6) << 4  and
+    //           (sc[s+4] >> 4) | (sc[s]   >> 6) << 4
+    const uint32_t S = hi ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u))
+                          : (hd.y & 0x3F3F3F3Fu);
+    const uint32_t M = hi ? (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u))
+                          : (hd.z & 0x3F3F3F3Fu);
+    const float sca = static_cast<float>((S >> sh) & 0xFFu);
+    const float scb = static_cast<float>((S >> (sh + 8)) & 0xFFu);
+    const float mna = static_cast<float>((M >> sh) & 0xFFu);
+    const float mnb = static_cast<float>((M >> (sh + 8)) & 0xFFu);
+    const float d = half_bits_to_float(hd.x) * exp2i(60);
+    const float dmin = half_bits_to_float(hd.x >> 16);
+    const float qx = fmaf(sca, a0 + a1, scb * (b0 + b1));
+    const float mx = fmaf(mna, sxa, mnb * sxb);
+    return fmaf(d, qx, -dmin * mx);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Q6_K.  Unit u -> super-block kb = u/4, half h = (u/2)%2, column group
+// j = u%2: weights 128h + 32a + 16j + i for a = 0..3, i = 0..15.  Bytes:
+// ql[64h+16j ..+16] (a=0 low nibbles, a=2 high), ql[64h+32+16j ..+16] (a=1,
+// a=3), qh[32h+16j ..+16] (2-bit fields a=0..3 at bits 0,2,4,6), scales
+// sc[8h+2a+j].  Blocks are 210 B, so a block starts on a 2-byte boundary:
+// the lane loads aligned words and funnel-shifts them.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void load16_a2(const uint8_t* p, uint32_t (&w)[4]) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const uint32_t* q = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+  const uint32_t s = static_cast<uint32_t>(a & 3u) * 8u;
+  const uint32_t r0 = q[0], r1 = q[1], r2 = q[2], r3 = q[3], r4 = q[4];
+  w[0] = __funnelshift_r(r0, r1, s);
+  w[1] = __funnelshift_r(r1, r2, s);
+  w[2] = __funnelshift_r(r2, r3, s);
+  w[3] = __funnelshift_r(r3, r4, s);
+}
+
+struct UnitQ6K {
+  static constexpr int kFmt = 14;
+  static constexpr int kBlockW = 256;
+  static constexpr int kBlockBytes = 210;
+  float x[4][16];   // [a][i], pre-scaled by 2^(kE - pos(i%4))
+  float sx32[4];    // 32 * sum_i x[a][i] * 2^-60 (the -32 offset, in product units)
+  uint32_t off, oA, oB, oQ;
+  uint32_t j;       // column group within the half
+  bool sh8;         // half h = 1: scales 8..15
+
+  // Column 256kb + 128h + 32a + 16j + i belongs to unit 4kb + 2h + j with
+  // unit-local index l = 16a + i.
+  __device__ __forceinline__ static void unit_of(int64_t col, int& u, int& l) {
+    const int kb = static_cast<int>(col >> 8), r = static_cast<int>(col & 255);
+    const int h = r >> 7, a = (r >> 5) & 3, j = (r >> 4) & 1, i = r & 15;
+    u = 4 * kb + 2 * h + j;
+    l = 16 * a + i;
+  }
+
+  template <class XU>
+  __device__ __forceinline__ void setup(int u, const XU& xu) {
+    const int kb = u >> 2, h = (u >> 1) & 1, j = u & 1;
+    off = static_cast<uint32_t>(kb) * kBlockBytes;
+    oA = 64u * h + 16u * j;
+    oB = 64u * h + 32u + 16u * j;
+    oQ = 128u + 32u * h + 16u * j;
+    this->j = static_cast<uint32_t>(j);
+    sh8 = h != 0;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      float s = 0.f;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const float v = xu(16 * a + i);
+        s += v;
+        const int pos = (i & 3) == 0 ? 0 : (i & 3) == 1 ? 8 : 16;
+        x[a][i] = v * exp2i(kE - pos);
+      }
+      sx32[a] = s * exp2i(5 - 60);
+    }
+  }
+
+  __device__ __forceinline__ float row(const uint8_t* rp) const {
+    const uint8_t* bp = rp + off;
+    uint32_t WA[4], WB[4], H[4], SC[4];
+    load16_a2(bp + oA, WA);
+    load16_a2(bp + oB, WB);
+    load16_a2(bp + oQ, H);
+    load16_a2(bp + 192, SC);  // the 16 int8 scales
+    const uintptr_t da = reinterpret_cast<uintptr_t>(bp + 208);
+    const uint32_t dw = *reinterpret_cast<const uint32_t*>(da & ~uintptr_t(3));
+    const float d = half_bits_to_float(dw >> ((da & 3u) * 8u)) * exp2i(60);
+    float p[4][2];
+#pragma unroll
+    for (int a = 0; a < 4; ++a) p[a][0] = p[a][1] = 0.f;
+    constexpr uint32_t M = 0x0F0F0F0Fu;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const uint32_t wa = WA[t], wb = WB[t], hh = H[t];
+      // 6-bit quants of four consecutive columns, one per byte (bits 6,7 of
+      // each byte are don't-care; the extraction masks drop them)
+      const uint32_t v0 = (wa & M) | ((hh << 4) & ~M);
+      const uint32_t v1 = (wb & M) | ((hh << 2) & ~M);
+      const uint32_t v2 = ((wa >> 4) & M) | (hh & ~M);
+      const uint32_t v3 = ((wb >> 4) & M) | ((hh >> 2) & ~M);
+      const uint32_t vv[4] = {v0, v1, v2, v3};
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        const uint32_t v = vv[a];
+        fma2(p[a][0], p[a][1], bits(v & 0x3Fu), bits(v & 0x3F00u), x[a][4 * t], x[a][4 * t + 1]);
+        fma2(p[a][0], p[a][1], bits(v & 0x3F0000u), bits((v >> 8) & 0x3F0000u), x[a][4 * t + 2],
+             x[a][4 * t + 3]);
+      }
+    }
+    // scale of weights 128h + 32a + 16j + i is sc[(128h + 32a + 16j) / 16] = sc[8h + 2a + j]:
+    // byte j + 2a of the 8 scale bytes of half h
+    const uint32_t s_lo = sh8 ? SC[2] : SC[0];
+    const uint32_t s_hi = sh8 ? SC[3] : SC[1];
+    float acc = 0.f;
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const uint32_t wsc = a < 2 ? s_lo : s_hi;
+      const uint32_t shift = 8u * (j + 2u * (a & 1));
+      const int sc = static_cast<int>(static_cast<int8_t>((wsc >> shift) & 0xFFu));
+      acc = fmaf(static_cast<float>(sc), (p[a][0] + p[a][1]) - sx32[a], acc);
+    }
+    return d * acc;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Q4_0.  Unit u -> blocks 2u and 2u+1 (36 bytes at row offset 36u, 4-byte
+// aligned when the row length is a multiple of 16 bytes).  Words w0..w8:
+//   w0 = d0 | qs0[0..1] << 16,  w1..w3 = qs0[2..13],  w4 = qs0[14..15] | d1 << 16,
+//   w5..w8 = qs1[0..15].
+// Block 0 weight j is the low nibble of qs0[j], weight 16+j the high nibble.
+// ---------------------------------------------------------------------------
+struct UnitQ40 {
+  static constexpr int kFmt = 2;
+  static constexpr int kBlockW = 32;
+  static constexpr int kBlockBytes = 18;
+  float e0[4];               // qs0[0..1] via w0 >> 12: lo0 hi0 lo1 hi1 (pos 4, 8, 12, 16)
+  float xl0[12], xh0[12];    // qs0[2..13]: low / high nibble columns 2+k / 18+k
+  float g0[4];               // qs0[14..15] via w4: lo14 hi14 lo15 hi15 (pos 0, 4, 8, 12)
+  float xl1[16], xh1[16];    // qs1[0..15]
+  float s8_0, s8_1;          // 8 * sum(x) * 2^-60 per block
+  uint32_t off;
+
+  // Unit u covers columns 64u .. 64u + 63 (blocks 2u, 2u+1).
+  __device__ __forceinline__ static void unit_of(int64_t col, int& u, int& l) {
+    u = static_cast<int>(col >> 6);
+    l = static_cast<int>(col & 63);
+  }
+
+  template <class XU>
+  __device__ __forceinline__ void setup(int u, const XU& xu) {
+    off = 36u * static_cast<uint32_t>(u);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int c = 0; c < 32; ++c) s0 += xu(c);
+#pragma unroll
+    for (int c = 32; c < 64; ++c) s1 += xu(c);
+    s8_0 = s0 * exp2i(3 - 60);
+    s8_1 = s1 * exp2i(3 - 60);
+    e0[0] = xu(0) * exp2i(kE - 4);
+    e0[1] = xu(16) * exp2i(kE - 8);
+    e0[2] = xu(1) * exp2i(kE - 12);
+    e0[3] = xu(17) * exp2i(kE - 16);
+#pragma unroll
+    for (int k = 0; k < 12; ++k) {
+      xl0[k] = xu(2 + k) * exp2i(kE - pos_lo(k & 3));
+      xh0[k] = xu(18 + k) * exp2i(kE - pos_hi(k & 3));
+    }
+    g0[0] = xu(14) * exp2i(kE - 0);
+    g0[1] = xu(30) * exp2i(kE - 4);
+    g0[2] = xu(15) * exp2i(kE - 8);
+    g0[3] = xu(31) * exp2i(kE - 12);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      xl1[k] = xu(32 + k) * exp2i(kE - pos_lo(k & 3));
+      xh1[k] = xu(48 + k) * exp2i(kE - pos_hi(k & 3));
+    }
+  }
+
+  __device__ __forceinline__ float row(const uint8_t* rp) const {
+    const uint32_t* q = reinterpret_cast<const uint32_t*>(rp + off);
+    const uint32_t w0 = q[0], w1 = q[1], w2 = q[2], w3 = q[3], w4 = q[4];
+    const uint32_t w5 = q[5], w6 = q[6], w7 = q[7], w8 = q[8];
+    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+    const uint32_t s = w0 >> 12;
+    fma2(a0, a1, bits(s & 0xF0u), bits(s & 0xF00u), e0[0], e0[1]);
+    fma2(a0, a1, bits(s & 0xF000u), bits(s & 0xF0000u), e0[2], e0[3]);
+    nibble_word(w1, xl0 + 0, xh0 + 0, a0, a1, b0, b1);
+    nibble_word(w2, xl0 + 4, xh0 + 4, a0, a1, b0, b1);
+    nibble_word(w3, xl0 + 8, xh0 + 8, a0, a1, b0, b1);
+    fma2(b0, b1, bits(w4 & 0xFu), bits(w4 & 0xF0u), g0[0], g0[1]);
+    fma2(b0, b1, bits(w4 & 0xF00u), bits(w4 & 0xF000u), g0[2], g0[3]);
+    float c0 = 0.f, c1 = 0.f, e0a = 0.f, e1a = 0.f;
+    nibble_word(w5, xl1 + 0, xh1 + 0, c0, c1, e0a, e1a);
+    nibble_word(w6, xl1 + 4, xh1 + 4, c0, c1, e0a, e1a);
+    nibble_word(w7, xl1 + 8, xh1 + 8, c0, c1, e0a, e1a);
+    nibble_word(w8, xl1 + 12, xh1 + 12, c0, c1, e0a, e1a);
+    const float d0 = half_bits_to_float(w0) * exp2i(60);
+    const float d1 = half_bits_to_float(w4 >> 16) * exp2i(60);
+    const float p0 = ((a0 + a1) + (b0 + b1)) - s8_0;
+    const float p1 = ((c0 + c1) + (e0a + e1a)) - s8_1;
+    return fmaf(d0, p0, d1 * p1);
+  }
+};
+
+}  // namespace qws

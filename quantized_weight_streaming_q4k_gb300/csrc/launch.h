@@ -1,0 +1,106 @@
+// launch.h -- host-side planning and launchers shared by the C-ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <string>
+
+#include "engine.cuh"
+
+namespace qws {
+
+inline int64_t block_weights(int fmt) { return fmt == 2 ? 32 : 256; }
+inline int64_t block_bytes(int fmt) { return fmt == 2 ? 18 : fmt == 12 ? 144 : fmt == 14 ? 210 : 0; }
+inline int64_t row_bytes_of(int fmt, int64_t K) { return K / block_weights(fmt) * block_bytes(fmt); }
+
+inline int64_t gcd64(int64_t a, int64_t b) {
+  while (b) {
+    const int64_t t = a % b;
+    a = b;
+    b = t;
+  }
+  return a;
+}
+
+// Tile / ring geometry of one phase.
+struct TilePlan {
+  int U, G, T, C;
+  uint32_t stage_need;   // bytes of the largest tile (both matrices when paired)
+  uint32_t red_floats;
+};
+
+// Chooses row slots G and rows per tile T for a phase with K columns and B
+// activation vectors.  T is a multiple of G (every slot gets the same number
+// of rows) and of the rows that make T * row_bytes a multiple of 16 (aligned
+// bulk copies).  rows_hint sizes tiles so that small matrices still spread
+// over the grid.  Returns false (with a reason) if the shape does not fit.
+inline bool plan_tiles(int fmt, int epi, int64_t K, int B, int64_t rows_hint, int sms,
+                       uint32_t tile_target, TilePlan& tp, std::string& why) {
+  const int64_t RB = row_bytes_of(fmt, K);
+  if (K % kUnitWeights) {
+    why = "hidden is not a multiple of 64";
+    return false;
+  }
+  const int64_t U = K / kUnitWeights;
+  if (U > kMaxConsumers) {
+    why = "more than 320 lane units per row (hidden > 20480 in one pass)";
+    return false;
+  }
+  const int64_t gmax = kMaxConsumers / (U * B);
+  if (gmax < 1) {
+    why = "batch * hidden / 64 exceeds 320 lanes";
+    return false;
+  }
+  const int pairm = epi == EPI_GEGLU ? 2 : 1;
+  const int64_t align = 16 / gcd64(RB, 16);
+  int64_t G = gmax, T0 = 0;
+  for (; G >= 1; --G) {
+    T0 = G / gcd64(G, align) * align;
+    if (T0 * RB * pairm <= 48 * 1024) break;
+  }
+  if (G < 1) {
+    G = 1;
+    T0 = align;
+  }
+  int64_t m = static_cast<int64_t>(tile_target) / (T0 * RB * pairm);
+  if (m < 1) m = 1;
+  // small matrices: aim for about one tile per CTA slot of the grid
+  const int64_t per = (rows_hint + 2 * sms - 1) / (2 * static_cast<int64_t>(sms));
+  const int64_t m_small = (per + T0 - 1) / T0;
+  if (m_small >= 1 && m_small < m) m = m_small;
+  tp.U = static_cast<int>(U);
+  tp.G = static_cast<int>(G);
+  tp.T = static_cast<int>(T0 * m);
+  tp.C = static_cast<int>((B * G * U + 31) / 32 * 32);
+  tp.stage_need = static_cast<uint32_t>(tp.T * RB * pairm);
+  tp.red_floats = static_cast<uint32_t>(B * tp.T * pairm * red_stride(static_cast<int>(U)));
+  return true;
+}
+
+inline uint32_t round_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
+
+// dynamic shared memory a streaming CTA uses (one CTA per SM)
+constexpr size_t kSmemBudget = 200 * 1024;
+
+// ---------------------------------------------------------------- launchers
+// All return cudaSuccess or the CUDA error; *why gets a message on failure.
+int device_sms();
+
+// y (or split partials) for segments of one format; epi = EPI_STORE/EPI_GEGLU.
+cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uint8_t* W2,
+                          const float* x, int64_t K, int B, int splits, cudaStream_t st,
+                          std::string* why);
+// y[b][r] = sum_s part[s][b][r]
+cudaError_t launch_splitk_reduce(const float* part, float* y, int64_t n, int splits,
+                                 cudaStream_t st);
+cudaError_t launch_rms_norm(const float* x, const float* w, float* y, int64_t n, float eps,
+                            int batch, cudaStream_t st);
+cudaError_t launch_residual_add(float* h, const float* y, int64_t n, int batch, cudaStream_t st);
+unsigned read_clear_matvec_errors();
+
+// decode chain (chain.cu)
+size_t chain_workspace_bytes(int64_t hidden, int64_t inter);
+unsigned read_clear_chain_errors();
+
+}  // namespace qws

@@ -1,0 +1,270 @@
+// matvec.cu -- standalone streaming kernels: quantized matvec (any format,
+// optional column split), fused QKV (three stacked segments), gate/up with the
+// GEGLU epilogue, the split-K reduction, rms_norm and residual_add.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <mutex>
+
+#include "launch.h"
+
+namespace qws {
+
+__device__ unsigned g_err_matvec;
+
+struct MatvecParams {
+  Phase P;                 // phase of column slice 0
+  const float* x;          // [B][x_stride]
+  int64_t x_stride;
+  int cps;                 // CTAs per column slice
+  int64_t w_slice_off;     // byte offset between column slices within a row
+  int64_t x_slice_off;     // column offset between slices
+  int64_t y_slice_off;     // float offset between slices' partial outputs
+  uint32_t S, stage_bytes, red_floats, xs_floats;
+};
+
+struct OnePhase {
+  Phase P;
+  __device__ __forceinline__ int count() const { return 1; }
+  __device__ __forceinline__ Phase get(int) const { return P; }
+};
+
+template <class Unit, class Epi>
+__global__ void __launch_bounds__(kRoleThreads + kMaxConsumers)
+    matvec_kernel(const __grid_constant__ MatvecParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const Ring R = make_ring(smem, p.S, p.stage_bytes, p.red_floats, p.xs_floats);
+  const int C = static_cast<int>(blockDim.x) - kRoleThreads;
+  // this CTA's column slice
+  const int slice = static_cast<int>(blockIdx.x) / p.cps;
+  Phase P = p.P;
+  P.cta0 = slice * p.cps;
+  P.ncta = p.cps;
+  if (slice > 0) {
+    P.seg[0].W += slice * p.w_slice_off;
+    P.seg[0].y += slice * p.y_slice_off;
+  }
+  if (threadIdx.x == 0) ring_init(R, C / 32);
+  __syncthreads();
+  uint32_t k = 0;
+  if (threadIdx.x < kProducerThreads) {
+    if (threadIdx.x == 0) run_producer(OnePhase{P}, R, &g_err_matvec);
+  } else if (threadIdx.x < kRoleThreads) {
+    reduce_phase(P, R, k, Epi{}, &g_err_matvec);
+  } else {
+    consume_phase<Unit>(P, R, k, XOfPlain{p.x + slice * p.x_slice_off, p.x_stride},
+                        static_cast<int>(threadIdx.x) - kRoleThreads, C, &g_err_matvec);
+  }
+}
+
+__global__ void splitk_reduce_kernel(const float* __restrict__ part, float* __restrict__ y,
+                                     int64_t n, int splits) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float acc = part[i];
+    for (int s = 1; s < splits; ++s) acc += part[s * n + i];
+    y[i] = acc;
+  }
+}
+
+// One CTA per vector; sum of squares in a fixed order (per-thread strided
+// partials, then a fixed shuffle tree and a fixed pass over the warp sums).
+__global__ void __launch_bounds__(1024) rms_norm_kernel(const float* __restrict__ x,
+                                                        const float* __restrict__ w,
+                                                        float* __restrict__ y, int64_t n,
+                                                        float eps) {
+  __shared__ float wsum[32];
+  __shared__ float inv_s;
+  const float* xb = x + blockIdx.x * n;
+  float* yb = y + blockIdx.x * n;
+  float ss = 0.f;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) ss = fmaf(xb[i], xb[i], ss);
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) t += wsum[i];
+    inv_s = 1.0f / sqrtf(t / static_cast<float>(n) + eps);
+  }
+  __syncthreads();
+  const float inv = inv_s;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) yb[i] = xb[i] * inv * w[i];
+}
+
+__global__ void residual_add_kernel(float* __restrict__ h, const float* __restrict__ y,
+                                    int64_t n) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x)
+    h[i] += y[i];
+}
+
+// ------------------------------------------------------------------ host side
+int device_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int sms = 0;
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  sms = sms > 0 ? sms : 1;
+  if (dev >= 0 && dev < 64) cache[dev] = sms;
+  return sms;
+}
+
+// Per (device, kernel, threads, smem): the dynamic-smem opt-in is set once and
+// the occupancy is queried once.
+struct KernelCacheEntry {
+  int dev;
+  const void* fn;
+  int threads;
+  size_t smem;
+  int bps;
+};
+
+static int cached_blocks_per_sm(const void* fn, int threads, size_t smem) {
+  static std::mutex mu;
+  static KernelCacheEntry entries[256];
+  static int n = 0;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  for (int i = 0; i < n; ++i)
+    if (entries[i].dev == dev && entries[i].fn == fn && entries[i].threads == threads &&
+        entries[i].smem == smem)
+      return entries[i].bps;
+  int optin = 0;
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  int bps = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, fn, threads, smem) != cudaSuccess)
+    bps = 0;
+  if (bps < 1) bps = 1;
+  if (n < 256) entries[n++] = KernelCacheEntry{dev, fn, threads, smem, bps};
+  return bps;
+}
+
+template <class Unit, class Epi>
+static int blocks_per_sm(int threads, size_t smem) {
+  return cached_blocks_per_sm(reinterpret_cast<const void*>(matvec_kernel<Unit, Epi>), threads,
+                              smem);
+}
+
+template <class Unit, class Epi>
+static cudaError_t launch_one(const MatvecParams& p, int threads, size_t smem, int grid,
+                              cudaStream_t st) {
+  blocks_per_sm<Unit, Epi>(threads, smem);  // makes sure the smem opt-in is set
+  matvec_kernel<Unit, Epi><<<grid, threads, smem, st>>>(p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uint8_t* W2,
+                          const float* x, int64_t K, int B, int splits, cudaStream_t st,
+                          std::string* why) {
+  const int sms = device_sms();
+  const int64_t Ks = K / splits;
+  int64_t rows_total = 0;
+  for (int i = 0; i < nseg; ++i) rows_total += segs[i].rows;
+  TilePlan tp;
+  std::string reason;
+  if (!plan_tiles(fmt, epi, Ks, B, rows_total * splits, sms, 24 * 1024, tp, reason)) {
+    if (why) *why = reason;
+    return cudaErrorInvalidValue;
+  }
+  MatvecParams p{};
+  Phase& P = p.P;
+  P.fmt = fmt;
+  P.epi = epi;
+  P.nseg = nseg;
+  P.n_tiles = 0;
+  for (int i = 0; i < nseg; ++i) {
+    P.seg[i] = segs[i];
+    P.seg[i].tiles = static_cast<int>((segs[i].rows + tp.T - 1) / tp.T);
+    P.n_tiles += P.seg[i].tiles;
+  }
+  P.W2 = W2;
+  P.K = Ks;
+  P.row_bytes = row_bytes_of(fmt, Ks);
+  P.row_stride = row_bytes_of(fmt, K);
+  P.B = B;
+  P.U = tp.U;
+  P.G = tp.G;
+  P.T = tp.T;
+  p.x = x;
+  p.x_stride = K;
+  p.w_slice_off = P.row_bytes;
+  p.x_slice_off = Ks;
+  p.y_slice_off = static_cast<int64_t>(B) * segs[0].rows;
+  p.stage_bytes = round_up(tp.stage_need + 16, 128);
+  p.red_floats = tp.red_floats;
+  p.xs_floats = static_cast<uint32_t>(kUnitWeights * red_stride(tp.U));
+  // ring: as deep as the shared memory left after the partial and staging
+  // buffers allows (one CTA per SM), 2..16 stages
+  const size_t fixed = ring_header_bytes(16, p.red_floats, p.xs_floats);
+  const size_t budget = kSmemBudget > fixed ? kSmemBudget - fixed : 0;
+  p.S = static_cast<uint32_t>(std::max<size_t>(2, std::min<size_t>(16, budget / p.stage_bytes)));
+  const size_t smem = ring_smem_bytes(p.S, p.stage_bytes, p.red_floats, p.xs_floats);
+  const int threads = kRoleThreads + tp.C;
+
+  int bps = 1;
+  switch (fmt * 2 + epi) {
+    case 12 * 2 + EPI_STORE: bps = blocks_per_sm<UnitQ4K, EpiStore>(threads, smem); break;
+    case 12 * 2 + EPI_GEGLU: bps = blocks_per_sm<UnitQ4K, EpiGeglu>(threads, smem); break;
+    case 14 * 2 + EPI_STORE: bps = blocks_per_sm<UnitQ6K, EpiStore>(threads, smem); break;
+    case 2 * 2 + EPI_STORE: bps = blocks_per_sm<UnitQ40, EpiStore>(threads, smem); break;
+    default:
+      if (why) *why = "unsupported format / epilogue";
+      return cudaErrorInvalidValue;
+  }
+  // CTAs per column slice: enough to cover the slice's tiles, and all slices
+  // together about fill the device
+  const int64_t slots = static_cast<int64_t>(bps) * sms;
+  int64_t cps = std::max<int64_t>(1, slots / splits);
+  cps = std::min<int64_t>(cps, P.n_tiles);
+  p.cps = static_cast<int>(cps);
+  P.cta0 = 0;
+  P.ncta = p.cps;
+  const int grid = static_cast<int>(cps * splits);
+  switch (fmt * 2 + epi) {
+    case 12 * 2 + EPI_STORE: return launch_one<UnitQ4K, EpiStore>(p, threads, smem, grid, st);
+    case 12 * 2 + EPI_GEGLU: return launch_one<UnitQ4K, EpiGeglu>(p, threads, smem, grid, st);
+    case 14 * 2 + EPI_STORE: return launch_one<UnitQ6K, EpiStore>(p, threads, smem, grid, st);
+    default: return launch_one<UnitQ40, EpiStore>(p, threads, smem, grid, st);
+  }
+}
+
+cudaError_t launch_splitk_reduce(const float* part, float* y, int64_t n, int splits,
+                                 cudaStream_t st) {
+  const int threads = 256;
+  const int64_t blocks = std::min<int64_t>((n + threads - 1) / threads, 4 * device_sms());
+  splitk_reduce_kernel<<<static_cast<int>(std::max<int64_t>(blocks, 1)), threads, 0, st>>>(
+      part, y, n, splits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rms_norm(const float* x, const float* w, float* y, int64_t n, float eps,
+                            int batch, cudaStream_t st) {
+  const int threads = n >= 1024 ? 1024 : static_cast<int>((n + 31) / 32 * 32);
+  rms_norm_kernel<<<batch, threads, 0, st>>>(x, w, y, n, eps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_residual_add(float* h, const float* y, int64_t n, int batch,
+                                cudaStream_t st) {
+  const int64_t total = n * batch;
+  const int threads = 256;
+  const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, 4 * device_sms());
+  residual_add_kernel<<<static_cast<int>(std::max<int64_t>(blocks, 1)), threads, 0, st>>>(h, y,
+                                                                                          total);
+  return cudaGetLastError();
+}
+
+unsigned read_clear_matvec_errors() {
+  unsigned v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_matvec, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(g_err_matvec, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace qws

@@ -1,0 +1,185 @@
+"""Thin torch-facing binding over the C ABI (include/qws.h).
+
+Argument marshalling only: every function passes device pointers, sizes and
+the current CUDA stream to libqws.so; all arithmetic runs in its kernels.
+Outputs are allocated with torch when ``out`` is not given (PyTorch is the
+allocator, the library allocates nothing).
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _lib
+from ._lib import OP_DECODE_CHAIN, OP_FFN, OP_MATVEC, Q4_0, Q4_K, Q6_K, QwsError, check, lib
+
+__all__ = [
+    "Q4_0", "Q4_K", "Q6_K", "QwsError", "q4k_matvec", "q6k_matvec", "q4_0_matvec", "matvec",
+    "q4k_qkv_proj", "q4k_ffn_gate_up_geglu", "q4k_ffn_gate_up_geglu_down", "rms_norm",
+    "residual_add", "decode_chain", "workspace_bytes", "device_error", "Layer", "Dims",
+    "stream_handle",
+]
+
+
+def stream_handle(stream: torch.cuda.Stream | None = None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+def _dev(t: torch.Tensor, name: str, dtype: torch.dtype | None = None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr()
+
+
+def _out(out, shape, like: torch.Tensor) -> torch.Tensor:
+    if out is None:
+        return torch.empty(shape, dtype=torch.float32, device=like.device)
+    return out
+
+
+def workspace_bytes(op: int, rows: int = 0, hidden: int = 0, inter: int = 0, batch: int = 1,
+                    split_k: int = 0) -> int:
+    return int(lib().qws_workspace_bytes(op, rows, hidden, inter, batch, split_k))
+
+
+def _mv(name: str, W, x, rows: int, hidden: int, batch: int, out, stream):
+    y = _out(out, (batch, rows) if batch > 1 else (rows,), x)
+    fn = getattr(lib(), name)
+    check(fn(_dev(W, "W", torch.uint8), _dev(x, "x", torch.float32),
+             _dev(y, "y", torch.float32), rows, hidden, batch, stream_handle(stream)))
+    return y
+
+
+def q4k_matvec(W, x, rows: int, hidden: int, batch: int = 1, out=None, stream=None):
+    """y = dequant_Q4_K(W) @ x; x [batch, hidden] (or [hidden]), y [batch, rows]."""
+    return _mv("qws_q4k_matvec", W, x, rows, hidden, batch, out, stream)
+
+
+def q6k_matvec(W, x, rows: int, hidden: int, batch: int = 1, out=None, stream=None):
+    return _mv("qws_q6k_matvec", W, x, rows, hidden, batch, out, stream)
+
+
+def matvec(fmt: int, W, x, rows: int, hidden: int, batch: int = 1, split_k: int = 1,
+           workspace=None, out=None, stream=None):
+    y = _out(out, (batch, rows) if batch > 1 else (rows,), x)
+    ws_ptr, ws_bytes = (0, 0) if workspace is None else (_dev(workspace, "workspace"),
+                                                          workspace.numel() * workspace.element_size())
+    check(lib().qws_matvec(fmt, _dev(W, "W", torch.uint8), _dev(x, "x", torch.float32),
+                           _dev(y, "y", torch.float32), rows, hidden, batch, split_k,
+                           ws_ptr or None, ws_bytes, stream_handle(stream)))
+    return y
+
+
+def q4_0_matvec(W, x, rows: int, hidden: int, batch: int = 1, split_k: int = 1, workspace=None,
+                out=None, stream=None):
+    y = _out(out, (batch, rows) if batch > 1 else (rows,), x)
+    ws_ptr, ws_bytes = (0, 0) if workspace is None else (_dev(workspace, "workspace"),
+                                                          workspace.numel() * workspace.element_size())
+    check(lib().qws_q4_0_matvec(_dev(W, "W", torch.uint8), _dev(x, "x", torch.float32),
+                                _dev(y, "y", torch.float32), rows, hidden, batch, split_k,
+                                ws_ptr or None, ws_bytes, stream_handle(stream)))
+    return y
+
+
+def q4k_qkv_proj(Wq, Wk, Wv, x, hidden: int, q_dim: int, kv_dim: int, out=None, stream=None):
+    if out is None:
+        q = torch.empty(q_dim, dtype=torch.float32, device=x.device)
+        k = torch.empty(kv_dim, dtype=torch.float32, device=x.device)
+        v = torch.empty(kv_dim, dtype=torch.float32, device=x.device)
+    else:
+        q, k, v = out
+    check(lib().qws_q4k_qkv_proj(_dev(Wq, "Wq", torch.uint8), _dev(Wk, "Wk", torch.uint8),
+                                 _dev(Wv, "Wv", torch.uint8), _dev(x, "x", torch.float32),
+                                 _dev(q, "q", torch.float32), _dev(k, "k", torch.float32),
+                                 _dev(v, "v", torch.float32), hidden, q_dim, kv_dim,
+                                 stream_handle(stream)))
+    return q, k, v
+
+
+def q4k_ffn_gate_up_geglu(Wg, Wu, x, hidden: int, inter: int, out=None, stream=None):
+    m = _out(out, (inter,), x)
+    check(lib().qws_q4k_ffn_gate_up_geglu(_dev(Wg, "Wg", torch.uint8), _dev(Wu, "Wu", torch.uint8),
+                                          _dev(x, "x", torch.float32), _dev(m, "m", torch.float32),
+                                          hidden, inter, stream_handle(stream)))
+    return m
+
+
+def q4k_ffn_gate_up_geglu_down(Wg, Wu, Wd, wd_fmt: int, x, hidden: int, inter: int,
+                               workspace=None, out=None, stream=None):
+    y = _out(out, (hidden,), x)
+    need = workspace_bytes(OP_FFN, 0, hidden, inter, 1, 0)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    check(lib().qws_q4k_ffn_gate_up_geglu_down(
+        _dev(Wg, "Wg", torch.uint8), _dev(Wu, "Wu", torch.uint8), _dev(Wd, "Wd", torch.uint8),
+        wd_fmt, _dev(x, "x", torch.float32), _dev(y, "y", torch.float32), hidden, inter,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        stream_handle(stream)))
+    return y
+
+
+def rms_norm(x, w, eps: float, batch: int = 1, out=None, stream=None):
+    y = _out(out, tuple(x.shape), x)
+    n = x.numel() // batch
+    check(lib().qws_rms_norm(_dev(x, "x", torch.float32), _dev(w, "w", torch.float32),
+                             _dev(y, "y", torch.float32), n, float(eps), batch,
+                             stream_handle(stream)))
+    return y
+
+
+def residual_add(h, y, batch: int = 1, stream=None):
+    n = h.numel() // batch
+    check(lib().qws_residual_add(_dev(h, "h", torch.float32), _dev(y, "y", torch.float32), n,
+                                 batch, stream_handle(stream)))
+    return h
+
+
+Layer = _lib.QwsLayer
+Dims = _lib.QwsDims
+
+
+def make_layer(t: dict) -> Layer:
+    """qws_layer from a dict of device tensors (Wq..Wd uint8, w_* float32) and formats."""
+    return Layer(
+        _dev(t["Wq"], "Wq", torch.uint8), _dev(t["Wk"], "Wk", torch.uint8),
+        _dev(t["Wv"], "Wv", torch.uint8), _dev(t["Wo"], "Wo", torch.uint8),
+        _dev(t["Wg"], "Wg", torch.uint8), _dev(t["Wu"], "Wu", torch.uint8),
+        _dev(t["Wd"], "Wd", torch.uint8),
+        int(t["fmt_qkv"]), int(t["fmt_o"]), int(t["fmt_gu"]), int(t["fmt_down"]),
+        _dev(t["w_in"], "w_in", torch.float32), _dev(t["w_post_attn"], "w_post_attn", torch.float32),
+        _dev(t["w_pre_ffn"], "w_pre_ffn", torch.float32),
+        _dev(t["w_post_ffn"], "w_post_ffn", torch.float32))
+
+
+def make_dims(d: dict) -> Dims:
+    return Dims(int(d["hidden"]), int(d["inter"]), int(d["n_q_heads"]), int(d["n_kv_heads"]),
+                int(d["head_dim"]), float(d["eps"]), int(d["post_norms"]))
+
+
+def decode_chain(layers, h, dims: dict, workspace=None, stream=None):
+    """Runs len(layers) decoder layers on h (in place).  layers: list of dicts
+    of device tensors (see make_layer) or prepared Layer structs."""
+    n = len(layers)
+    arr = (Layer * n)(*[L if isinstance(L, Layer) else make_layer(L) for L in layers])
+    D = make_dims(dims)
+    need = workspace_bytes(OP_DECODE_CHAIN, 0, dims["hidden"], dims["inter"], 1, 0)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=h.device)
+    check(lib().qws_decode_chain(arr, n, _dev(h, "h", torch.float32), C.byref(D),
+                                 _dev(workspace, "workspace"),
+                                 workspace.numel() * workspace.element_size(),
+                                 stream_handle(stream)))
+    return h
+
+
+def device_error() -> int:
+    """Waits for the device; returns (and clears) the kernels' error code (0 = none)."""
+    code = C.c_uint(0)
+    lib().qws_device_error(C.byref(code))
+    return int(code.value)

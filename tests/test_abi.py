@@ -1,0 +1,120 @@
+"""C-ABI checks that need no GPU: the library loads, exports every function
+include/qws.h declares, and rejects bad arguments on the host before any CUDA
+call (every case below returns before the first CUDA runtime call)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from quantized_weight_streaming_q4k_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "qws.h")
+
+OK, NULL, SHAPE, ALIGN, FORMAT, WORKSPACE = 0, 1, 2, 3, 4, 5
+A = 0x10000          # a 16-byte-aligned fake device address (never dereferenced)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(qws_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_expected_calls():
+    names = declared_functions()
+    for n in ["qws_q4k_matvec", "qws_q6k_matvec", "qws_q4_0_matvec", "qws_q4k_qkv_proj",
+              "qws_q4k_ffn_gate_up_geglu_down", "qws_rms_norm", "qws_residual_add",
+              "qws_decode_chain", "qws_workspace_bytes", "qws_last_error", "qws_device_error"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    # and the Python binding covers them all
+    assert set(declared_functions()) <= set(_lib.SIGNATURES)
+
+
+def test_version(lib):
+    assert b"sm_103a" in lib.qws_version()
+
+
+def _err(lib):
+    return lib.qws_last_error().decode()
+
+
+def test_matvec_null_pointers(lib):
+    assert lib.qws_q4k_matvec(None, A, A, 10, 256, 1, None) == NULL
+    assert "W is NULL" in _err(lib)
+    assert lib.qws_q4k_matvec(A, None, A, 10, 256, 1, None) == NULL
+    assert lib.qws_q6k_matvec(A, A, None, 10, 256, 1, None) == NULL
+
+
+def test_matvec_shapes(lib):
+    assert lib.qws_q4k_matvec(A, A, A, -1, 256, 1, None) == SHAPE
+    assert lib.qws_q4k_matvec(A, A, A, 10, 0, 1, None) == SHAPE
+    assert lib.qws_q4k_matvec(A, A, A, 10, 300, 1, None) == SHAPE
+    assert lib.qws_q4_0_matvec(A, A, A, 10, 96, 1, 1, None, 0, None) == SHAPE
+    assert lib.qws_q4k_matvec(A, A, A, 10, 256, 0, None) == SHAPE
+    assert lib.qws_q4k_matvec(A, A, A, 10, 40960, 1, None) == SHAPE     # one pass <= 20480
+    assert lib.qws_q4k_matvec(A, A, A, 10, 2560, 9, None) == SHAPE      # 9 * 40 > 320 lanes
+    assert "320" in _err(lib)
+
+
+def test_matvec_alignment(lib):
+    assert lib.qws_q4k_matvec(A + 8, A, A, 10, 256, 1, None) == ALIGN
+    assert lib.qws_q4k_matvec(A, A + 2, A, 10, 256, 1, None) == ALIGN
+    assert lib.qws_q4k_matvec(A, A, A + 1, 10, 256, 1, None) == ALIGN
+
+
+def test_matvec_format_and_zero_rows(lib):
+    assert lib.qws_matvec(7, A, A, A, 10, 256, 1, 1, None, 0, None) == FORMAT
+    # zero rows: valid, nothing enqueued (no CUDA call happens)
+    assert lib.qws_q4k_matvec(A, A, A, 0, 256, 1, None) == OK
+
+
+def test_splitk_workspace_checks(lib):
+    need = lib.qws_workspace_bytes(_lib.OP_MATVEC, 1000, 2560, 0, 1, 5)
+    assert need >= 5 * 1000 * 4
+    assert lib.qws_q4_0_matvec(A, A, A, 1000, 2560, 1, 5, None, 0, None) == WORKSPACE
+    assert lib.qws_q4_0_matvec(A, A, A, 1000, 2560, 1, 5, A, need - 1, None) == WORKSPACE
+    assert lib.qws_q4_0_matvec(A, A, A, 1000, 2560, 1, 3, A, need, None) == SHAPE   # 3 !| 10
+    assert lib.qws_q4_0_matvec(A, A, A, 1000, 2560, 1, -1, A, need, None) == SHAPE
+    assert lib.qws_workspace_bytes(_lib.OP_MATVEC, 1000, 2560, 0, 1, 1) == 0
+    # large hidden needs a split: library choice picks one that fits 320 lanes
+    assert lib.qws_workspace_bytes(_lib.OP_MATVEC, 10, 40960, 0, 1, 0) >= 2 * 10 * 4
+
+
+def test_qkv_and_ffn_checks(lib):
+    assert lib.qws_q4k_qkv_proj(A, A, None, A, A, A, A, 2560, 2048, 1024, None) == NULL
+    assert lib.qws_q4k_qkv_proj(A, A, A, A, A, A, A, 2500, 2048, 1024, None) == SHAPE
+    assert lib.qws_q4k_qkv_proj(A, A, A, A, A, A, A, 2560, 0, 0, None) == OK
+    need = lib.qws_workspace_bytes(_lib.OP_FFN, 0, 2560, 10240, 1, 0)
+    assert need >= 10240 * 4
+    assert lib.qws_q4k_ffn_gate_up_geglu_down(A, A, A, 2, A, A, 2560, 10240, A, need,
+                                              None) == FORMAT
+    assert lib.qws_q4k_ffn_gate_up_geglu_down(A, A, A, 14, A, A, 2560, 10240, A, need - 4,
+                                              None) == WORKSPACE
+    assert lib.qws_q4k_ffn_gate_up_geglu_down(A, A, A, 14, A, A, 2560, 1000, A, need,
+                                              None) == SHAPE
+    assert lib.qws_q4k_ffn_gate_up_geglu(A, A, A, None, 2560, 10240, None) == NULL
+
+
+def test_vector_op_checks(lib):
+    assert lib.qws_rms_norm(A, None, A, 10, C.c_float(1e-6), 1, None) == NULL
+    assert lib.qws_rms_norm(A, A, A, 0, C.c_float(1e-6), 1, None) == SHAPE
+    assert lib.qws_rms_norm(A, A, A, 10, C.c_float(-1.0), 1, None) == SHAPE
+    assert lib.qws_residual_add(A, A, -1, 1, None) == SHAPE
+    assert lib.qws_residual_add(A, A, 0, 1, None) == OK
+
+
+def test_device_error_null(lib):
+    assert lib.qws_device_error(None) == NULL
