@@ -270,6 +270,15 @@ qws_status qws_residual_add(float* h, const float* y, int64_t n, int batch, qws_
   return ok();
 }
 
+qws_status qws_decode_chain(const qws_layer* layers, int n_layers, float* h,
+                            const qws_dims* dims, void* ws, size_t ws_bytes, qws_stream stream) {
+  std::string err;
+  const qws_status st = qws::decode_chain(layers, n_layers, h, dims, ws, ws_bytes,
+                                          reinterpret_cast<cudaStream_t>(stream), err);
+  if (st != QWS_OK) return fail(st, "%s", err.c_str());
+  return ok();
+}
+
 size_t qws_workspace_bytes(qws_op op, int64_t rows, int64_t hidden, int64_t inter, int batch,
                            int split_k) {
   switch (op) {

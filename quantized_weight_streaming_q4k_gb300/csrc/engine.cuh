@@ -85,7 +85,7 @@ __device__ __forceinline__ TileRef tile_ref(const Phase& P, int t) {
   tr.y = P.seg[0].y;
   tr.seg_rows = P.seg[0].rows;
   int prev_tiles = P.seg[0].tiles;
-  bool more = true;
+  bool more = P.nseg > 1;
 #pragma unroll
   for (int i = 1; i < kMaxSeg; ++i) {
     if (more && i < P.nseg && t >= prev_tiles) {
@@ -155,6 +155,19 @@ __device__ __forceinline__ Ring make_ring(uint8_t* smem, uint32_t S, uint32_t st
   return R;
 }
 
+// Position in the ring: stage index and phase parity, advanced per tile
+// (no division in the loops).
+struct RingPos {
+  uint32_t s = 0, ph = 0, n = 0;  // n = tiles passed so far
+  __device__ __forceinline__ void advance(uint32_t S) {
+    ++n;
+    if (++s == S) {
+      s = 0;
+      ph ^= 1u;
+    }
+  }
+};
+
 // Called by one thread before the role split (followed by __syncthreads()).
 __device__ __forceinline__ void ring_init(const Ring& R, int consumer_warps) {
   for (uint32_t s = 0; s < R.S; ++s) {
@@ -211,7 +224,7 @@ __device__ __forceinline__ void fill_stage(const Phase& P, int t, const Ring& R,
 template <class PhaseList>
 __device__ void run_producer(const PhaseList& L, const Ring& R, unsigned* err) {
   const uint64_t pol = l2_policy_evict_first();
-  uint32_t k = 0;
+  RingPos pos;
   bool ok = true;
   const int nph = L.count();
   for (int p = 0; p < nph && ok; ++p) {
@@ -219,17 +232,17 @@ __device__ void run_producer(const PhaseList& L, const Ring& R, unsigned* err) {
     const int c = static_cast<int>(blockIdx.x) - P.cta0;
     if (c < 0 || c >= P.ncta) continue;
     for (int t = c; t < P.n_tiles; t += P.ncta) {
-      const uint32_t s = k % R.S, ph = (k / R.S) & 1u;
-      if (!mbar_wait(&R.empty[s], ph ^ 1u)) {
+      if (!mbar_wait(&R.empty[pos.s], pos.ph ^ 1u)) {
         atomicOr(err, kErrEmptyWait);
         ok = false;
         break;
       }
-      fill_stage(P, t, R, s, pol);
-      ++k;
+      fill_stage(P, t, R, pos.s, pol);
+      pos.advance(R.S);
     }
   }
   // Do not leave while copies into this CTA's shared memory are in flight.
+  const uint32_t k = pos.n;
   const uint32_t first = k > R.S ? k - R.S : 0u;
   for (uint32_t i = first; i < k; ++i) {
     if (!mbar_wait(&R.full[i % R.S], (i / R.S) & 1u)) atomicOr(err, kErrDrain);
@@ -287,7 +300,7 @@ __device__ __forceinline__ void stage_x(float* xs, int US, const Src& src, int64
 // through shared memory.  With STAGED = false the caller has already written
 // the single vector (B = 1) into R.xs.  Returns false on a timeout.
 template <class Unit, bool STAGED = true, class XOf>
-__device__ __forceinline__ bool consume_phase(const Phase& P, const Ring& R, uint32_t& k,
+__device__ __forceinline__ bool consume_phase(const Phase& P, const Ring& R, RingPos& pos,
                                               const XOf& x_of, int ctid, int C, unsigned* err) {
   const int cta = static_cast<int>(blockIdx.x) - P.cta0;
   if (cta < 0 || cta >= P.ncta) return true;
@@ -298,6 +311,7 @@ __device__ __forceinline__ bool consume_phase(const Phase& P, const Ring& R, uin
   const int lane = ctid & 31;
   const bool pair = P.epi == EPI_GEGLU;
   const int slots = pair ? 2 * P.T : P.T;      // partial rows per vector
+  const size_t rb = static_cast<size_t>(P.row_bytes);
   Unit unit;
   if (STAGED) {
     for (int bb = 0; bb < P.B; ++bb) {
@@ -309,24 +323,38 @@ __device__ __forceinline__ bool consume_phase(const Phase& P, const Ring& R, uin
   } else if (active) {
     unit.setup(u, XUnit{R.xs, US, u});
   }
-  for (int t = cta; t < P.n_tiles; t += P.ncta, ++k) {
-    const uint32_t s = k % R.S, ph = (k / R.S) & 1u;
-    if (!mbar_wait(&R.full[s], ph)) {
+  float* const red_b = R.red + static_cast<size_t>(b * slots) * US + u;
+  for (int t = cta; t < P.n_tiles; t += P.ncta) {
+    if (!mbar_wait(&R.full[pos.s], pos.ph)) {
       atomicOr(err, kErrFullWait);
       return false;
     }
     const TileRef tr = tile_ref(P, t);
-    const uint8_t* st = R.stage(s);
-    float* red = R.red + static_cast<size_t>(s) * R.red_floats;
+    const uint8_t* st = R.stage(pos.s);
+    float* red = red_b + static_cast<size_t>(pos.s) * R.red_floats;
     const int nr = pair ? 2 * tr.nrows : tr.nrows;
-    if (active) {
-      for (int r = gg; r < nr; r += G) {
-        const int slot = (pair && r >= tr.nrows) ? P.T + (r - tr.nrows) : r;
-        red[(b * slots + slot) * US + u] = unit.row(st + static_cast<size_t>(slot) * P.row_bytes);
+    if (active && gg < nr) {
+      // row r of the tile lives at slot(r) rows into the stage; the next
+      // row's bytes are loaded while the current one is decoded
+      int r = gg;
+      int slot = (pair && r >= tr.nrows) ? P.T + (r - tr.nrows) : r;
+      typename Unit::Frag f;
+      unit.load(st + slot * rb, f);
+      for (;;) {
+        const int rn = r + G;
+        const int slot_n = (pair && rn >= tr.nrows) ? P.T + (rn - tr.nrows) : rn;
+        typename Unit::Frag fn;
+        if (rn < nr) unit.load(st + slot_n * rb, fn);
+        red[slot * US] = unit.compute(f);
+        if (rn >= nr) break;
+        r = rn;
+        slot = slot_n;
+        f = fn;
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(&R.ready[s]);
+    if (lane == 0) mbar_arrive(&R.ready[pos.s]);
+    pos.advance(R.S);
   }
   return true;
 }
@@ -338,7 +366,7 @@ __device__ __forceinline__ bool consume_phase(const Phase& P, const Ring& R, uin
 // its lanes with a fixed xor tree: the order never changes between runs.
 // epi(P, tr, b, o, v, v2) stores the result (v2 = the up row for GEGLU).
 template <class Epi>
-__device__ __forceinline__ bool reduce_phase(const Phase& P, const Ring& R, uint32_t& k,
+__device__ __forceinline__ bool reduce_phase(const Phase& P, const Ring& R, RingPos& pos,
                                              const Epi& epi, unsigned* err) {
   const int cta = static_cast<int>(blockIdx.x) - P.cta0;
   if (cta < 0 || cta >= P.ncta) return true;
@@ -346,9 +374,9 @@ __device__ __forceinline__ bool reduce_phase(const Phase& P, const Ring& R, uint
   const int U = P.U, US = red_stride(P.U);
   const bool pair = P.epi == EPI_GEGLU;
   const int slots = pair ? 2 * P.T : P.T;
-  for (int t = cta; t < P.n_tiles; t += P.ncta, ++k) {
-    const uint32_t s = k % R.S, ph = (k / R.S) & 1u;
-    if (!mbar_wait(&R.ready[s], ph)) {
+  for (int t = cta; t < P.n_tiles; t += P.ncta) {
+    const uint32_t s = pos.s;
+    if (!mbar_wait(&R.ready[s], pos.ph)) {
       atomicOr(err, kErrFullWait);
       return false;
     }
@@ -379,6 +407,7 @@ __device__ __forceinline__ bool reduce_phase(const Phase& P, const Ring& R, uint
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&R.empty[s]);
+    pos.advance(R.S);
   }
   return true;
 }

@@ -102,12 +102,21 @@ struct UnitQ4K {
     sxb = sb;
   }
 
-  // Partial dot product of this unit with the row whose bytes start at rp.
-  __device__ __forceinline__ float row(const uint8_t* rp) const {
+  // Bytes of one row this unit reads: the block header and its 32-byte chunk.
+  struct Frag {
+    uint4 hd, q0, q1;
+  };
+
+  __device__ __forceinline__ void load(const uint8_t* rp, Frag& f) const {
     const uint8_t* bp = rp + off;
-    const uint4 hd = *reinterpret_cast<const uint4*>(bp);
-    const uint4 q0 = *reinterpret_cast<const uint4*>(bp + qoff);
-    const uint4 q1 = *reinterpret_cast<const uint4*>(bp + qoff + 16);
+    f.hd = *reinterpret_cast<const uint4*>(bp);
+    f.q0 = *reinterpret_cast<const uint4*>(bp + qoff);
+    f.q1 = *reinterpret_cast<const uint4*>(bp + qoff + 16);
+  }
+
+  // Partial dot product of this unit with one row (its bytes in f).
+  __device__ __forceinline__ float compute(const Frag& f) const {
+    const uint4 hd = f.hd, q0 = f.q0, q1 = f.q1;
     float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
     nibble_word(q0.x, xa + 0, xb + 0, a0, a1, b0, b1);
     nibble_word(q0.y, xa + 4, xb + 4, a0, a1, b0, b1);
@@ -134,6 +143,12 @@ struct UnitQ4K {
     const float qx = fmaf(sca, a0 + a1, scb * (b0 + b1));
     const float mx = fmaf(mna, sxa, mnb * sxb);
     return fmaf(d, qx, -dmin * mx);
+  }
+
+  __device__ __forceinline__ float row(const uint8_t* rp) const {
+    Frag f;
+    load(rp, f);
+    return compute(f);
   }
 };
 
@@ -198,23 +213,31 @@ struct UnitQ6K {
     }
   }
 
-  __device__ __forceinline__ float row(const uint8_t* rp) const {
-    const uint8_t* bp = rp + off;
+  struct Frag {
     uint32_t WA[4], WB[4], H[4], SC[4];
-    load16_a2(bp + oA, WA);
-    load16_a2(bp + oB, WB);
-    load16_a2(bp + oQ, H);
-    load16_a2(bp + 192, SC);  // the 16 int8 scales
+    uint32_t dbits;
+  };
+
+  __device__ __forceinline__ void load(const uint8_t* rp, Frag& f) const {
+    const uint8_t* bp = rp + off;
+    load16_a2(bp + oA, f.WA);
+    load16_a2(bp + oB, f.WB);
+    load16_a2(bp + oQ, f.H);
+    load16_a2(bp + 192, f.SC);  // the 16 int8 scales
     const uintptr_t da = reinterpret_cast<uintptr_t>(bp + 208);
     const uint32_t dw = *reinterpret_cast<const uint32_t*>(da & ~uintptr_t(3));
-    const float d = half_bits_to_float(dw >> ((da & 3u) * 8u)) * exp2i(60);
+    f.dbits = dw >> ((da & 3u) * 8u);
+  }
+
+  __device__ __forceinline__ float compute(const Frag& f) const {
+    const float d = half_bits_to_float(f.dbits) * exp2i(60);
     float p[4][2];
 #pragma unroll
     for (int a = 0; a < 4; ++a) p[a][0] = p[a][1] = 0.f;
     constexpr uint32_t M = 0x0F0F0F0Fu;
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      const uint32_t wa = WA[t], wb = WB[t], hh = H[t];
+      const uint32_t wa = f.WA[t], wb = f.WB[t], hh = f.H[t];
       // 6-bit quants of four consecutive columns, one per byte (bits 6,7 of
       // each byte are don't-care; the extraction masks drop them)
       const uint32_t v0 = (wa & M) | ((hh << 4) & ~M);
@@ -232,8 +255,8 @@ struct UnitQ6K {
     }
     // scale of weights 128h + 32a + 16j + i is sc[(128h + 32a + 16j) / 16] = sc[8h + 2a + j]:
     // byte j + 2a of the 8 scale bytes of half h
-    const uint32_t s_lo = sh8 ? SC[2] : SC[0];
-    const uint32_t s_hi = sh8 ? SC[3] : SC[1];
+    const uint32_t s_lo = sh8 ? f.SC[2] : f.SC[0];
+    const uint32_t s_hi = sh8 ? f.SC[3] : f.SC[1];
     float acc = 0.f;
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
@@ -243,6 +266,12 @@ struct UnitQ6K {
       acc = fmaf(static_cast<float>(sc), (p[a][0] + p[a][1]) - sx32[a], acc);
     }
     return d * acc;
+  }
+
+  __device__ __forceinline__ float row(const uint8_t* rp) const {
+    Frag f;
+    load(rp, f);
+    return compute(f);
   }
 };
 
@@ -300,10 +329,19 @@ struct UnitQ40 {
     }
   }
 
-  __device__ __forceinline__ float row(const uint8_t* rp) const {
+  struct Frag {
+    uint32_t w[9];
+  };
+
+  __device__ __forceinline__ void load(const uint8_t* rp, Frag& f) const {
     const uint32_t* q = reinterpret_cast<const uint32_t*>(rp + off);
-    const uint32_t w0 = q[0], w1 = q[1], w2 = q[2], w3 = q[3], w4 = q[4];
-    const uint32_t w5 = q[5], w6 = q[6], w7 = q[7], w8 = q[8];
+#pragma unroll
+    for (int i = 0; i < 9; ++i) f.w[i] = q[i];
+  }
+
+  __device__ __forceinline__ float compute(const Frag& f) const {
+    const uint32_t w0 = f.w[0], w1 = f.w[1], w2 = f.w[2], w3 = f.w[3], w4 = f.w[4];
+    const uint32_t w5 = f.w[5], w6 = f.w[6], w7 = f.w[7], w8 = f.w[8];
     float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
     const uint32_t s = w0 >> 12;
     fma2(a0, a1, bits(s & 0xF0u), bits(s & 0xF00u), e0[0], e0[1]);
@@ -323,6 +361,12 @@ struct UnitQ40 {
     const float p0 = ((a0 + a1) + (b0 + b1)) - s8_0;
     const float p1 = ((c0 + c1) + (e0a + e1a)) - s8_1;
     return fmaf(d0, p0, d1 * p1);
+  }
+
+  __device__ __forceinline__ float row(const uint8_t* rp) const {
+    Frag f;
+    load(rp, f);
+    return compute(f);
   }
 };
 

@@ -6,6 +6,7 @@
 #include <cstdint>
 #include <string>
 
+#include "../../include/qws.h"
 #include "engine.cuh"
 
 namespace qws {
@@ -57,7 +58,7 @@ inline bool plan_tiles(int fmt, int epi, int64_t K, int B, int64_t rows_hint, in
   int64_t G = gmax, T0 = 0;
   for (; G >= 1; --G) {
     T0 = G / gcd64(G, align) * align;
-    if (T0 * RB * pairm <= 48 * 1024) break;
+    if (T0 * RB * pairm <= 64 * 1024) break;
   }
   if (G < 1) {
     G = 1;
@@ -80,8 +81,10 @@ inline bool plan_tiles(int fmt, int epi, int64_t K, int B, int64_t rows_hint, in
 
 inline uint32_t round_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
-// dynamic shared memory a streaming CTA uses (one CTA per SM)
-constexpr size_t kSmemBudget = 200 * 1024;
+// dynamic shared memory a streaming CTA uses (one CTA per SM), and the
+// target bytes of one tile (per stage)
+constexpr size_t kSmemBudget = 216 * 1024;
+constexpr uint32_t kTileTarget = 46 * 1024;
 
 // ---------------------------------------------------------------- launchers
 // All return cudaSuccess or the CUDA error; *why gets a message on failure.
@@ -102,5 +105,7 @@ unsigned read_clear_matvec_errors();
 // decode chain (chain.cu)
 size_t chain_workspace_bytes(int64_t hidden, int64_t inter);
 unsigned read_clear_chain_errors();
+qws_status decode_chain(const qws_layer* layers, int n_layers, float* h, const qws_dims* d,
+                        void* ws, size_t ws_bytes, cudaStream_t st, std::string& err);
 
 }  // namespace qws

@@ -47,13 +47,13 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers)
   }
   if (threadIdx.x == 0) ring_init(R, C / 32);
   __syncthreads();
-  uint32_t k = 0;
+  RingPos pos;
   if (threadIdx.x < kProducerThreads) {
     if (threadIdx.x == 0) run_producer(OnePhase{P}, R, &g_err_matvec);
   } else if (threadIdx.x < kRoleThreads) {
-    reduce_phase(P, R, k, Epi{}, &g_err_matvec);
+    reduce_phase(P, R, pos, Epi{}, &g_err_matvec);
   } else {
-    consume_phase<Unit>(P, R, k, XOfPlain{p.x + slice * p.x_slice_off, p.x_stride},
+    consume_phase<Unit>(P, R, pos, XOfPlain{p.x + slice * p.x_slice_off, p.x_stride},
                         static_cast<int>(threadIdx.x) - kRoleThreads, C, &g_err_matvec);
   }
 }
@@ -168,7 +168,7 @@ cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uin
   for (int i = 0; i < nseg; ++i) rows_total += segs[i].rows;
   TilePlan tp;
   std::string reason;
-  if (!plan_tiles(fmt, epi, Ks, B, rows_total * splits, sms, 24 * 1024, tp, reason)) {
+  if (!plan_tiles(fmt, epi, Ks, B, rows_total * splits, sms, kTileTarget, tp, reason)) {
     if (why) *why = reason;
     return cudaErrorInvalidValue;
   }
@@ -199,11 +199,10 @@ cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uin
   p.stage_bytes = round_up(tp.stage_need + 16, 128);
   p.red_floats = tp.red_floats;
   p.xs_floats = static_cast<uint32_t>(kUnitWeights * red_stride(tp.U));
-  // ring: as deep as the shared memory left after the partial and staging
-  // buffers allows (one CTA per SM), 2..16 stages
-  const size_t fixed = ring_header_bytes(16, p.red_floats, p.xs_floats);
-  const size_t budget = kSmemBudget > fixed ? kSmemBudget - fixed : 0;
-  p.S = static_cast<uint32_t>(std::max<size_t>(2, std::min<size_t>(16, budget / p.stage_bytes)));
+  // ring: as deep as the shared-memory budget allows (one CTA per SM), 2..16
+  p.S = 16;
+  while (p.S > 2 && ring_smem_bytes(p.S, p.stage_bytes, p.red_floats, p.xs_floats) > kSmemBudget)
+    --p.S;
   const size_t smem = ring_smem_bytes(p.S, p.stage_bytes, p.red_floats, p.xs_floats);
   const int threads = kRoleThreads + tp.C;
 

@@ -1,0 +1,134 @@
+"""GPU parity of the decode chain (qws_decode_chain) against the oracle.
+
+Layer tolerance (derived in the design doc from the step tolerances): a layer adds
+two branches to h, a = post-attention branch and b = post-FFN branch, each an
+RMS-normalised matvec output.  Per element:
+    |h'_gpu - h'_ref| <= 1e-4 * (|h| + |a| + |b|) + 1e-4 * (rms(a) + rms(b))
+checked teacher-forced: the oracle runs each layer on the GPU's input to that
+layer.  One launch over L layers must equal L single-layer launches bit for bit
+(the kernel is deterministic), and the end-to-end relative L2 error against the
+oracle is reported and bounded.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_weight_streaming_q4k_gb300 import build, ops, synth
+
+pytestmark = pytest.mark.gpu
+
+SMALL = dict(hidden=512, inter=1024, n_q_heads=4, n_kv_heads=2, head_dim=128, eps=1e-6,
+             post_norms=1)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    build.build()
+    torch.cuda.set_device(0)
+    yield
+    assert ops.device_error() == 0
+
+
+def to_dev(L):
+    out = {}
+    for k, v in L.items():
+        out[k] = torch.from_numpy(np.ascontiguousarray(v)).cuda() if isinstance(v, np.ndarray) else v
+    return out
+
+
+def check_layer(h_in, h_gpu, L, dims):
+    ref, tr = oracle.layer_forward(L, dims, h_in, trace=True)
+    h = h_in.astype(np.float64)
+    a = tr["h1"] - h                      # post-attention branch (normed o, or o)
+    b = ref - tr["h1"]                    # post-FFN branch
+    tol = 1e-4 * (np.abs(h) + np.abs(a) + np.abs(b)) + 1e-4 * (
+        np.sqrt(np.mean(a * a)) + np.sqrt(np.mean(b * b)))
+    err = np.abs(h_gpu.astype(np.float64) - ref)
+    assert np.all(err <= tol), f"worst err/tol {np.max(err / tol):.3e}"
+    return float(np.max(err / tol)), ref
+
+
+def run_chain(layers_dev, h0, dims):
+    h = torch.from_numpy(h0.copy()).cuda()
+    ops.decode_chain(layers_dev, h, dims)
+    torch.cuda.synchronize()
+    return h.cpu().numpy()
+
+
+@pytest.mark.parametrize("post_norms", [1, 0])
+@pytest.mark.parametrize("fmt_down", [oracle.Q6_K, oracle.Q4_K])
+def test_chain_small_teacher_forced(post_norms, fmt_down):
+    dims = dict(SMALL, post_norms=post_norms)
+    n = 3
+    layers = [synth.chain_layer(l, dims, fmt_down=fmt_down, workload=50 + post_norms) for l in range(n)]
+    ldev = [to_dev(L) for L in layers]
+    h0 = synth.normal_vector(synth.rng(51, post_norms), dims["hidden"])
+    h = h0
+    outs = []
+    for l in range(n):
+        hg = run_chain([ldev[l]], h, dims)
+        check_layer(h, hg, layers[l], dims)
+        outs.append(hg)
+        h = hg
+    # one launch over n layers == n single-layer launches, bit for bit
+    hall = run_chain(ldev, h0, dims)
+    assert np.array_equal(hall, outs[-1])
+    # run-to-run identical
+    assert np.array_equal(run_chain(ldev, h0, dims), hall)
+
+
+def test_chain_small_end_to_end():
+    dims = SMALL
+    n = 4
+    layers = [synth.chain_layer(l, dims, workload=52) for l in range(n)]
+    ldev = [to_dev(L) for L in layers]
+    h0 = synth.normal_vector(synth.rng(53), dims["hidden"])
+    hg = run_chain(ldev, h0, dims)
+    ref = h0.astype(np.float64)
+    for L in layers:
+        ref = oracle.layer_forward(L, dims, ref)
+    rel = np.linalg.norm(hg - ref) / np.linalg.norm(ref)
+    print(f"chain small 4 layers: relative L2 error {rel:.2e}")
+    assert rel < 1e-4
+
+
+def test_chain_full_size_gemma3_4b():
+    """34 Gemma-3-4B-shaped layers: teacher-forced parity on layers 0, 1, 33,
+    bit-exact equality of one 34-layer launch with 34 single-layer launches,
+    and end-to-end relative L2 error against the oracle."""
+    dims = synth.GEMMA3_4B
+    n = 34
+    layers = [synth.chain_layer(l, dims) for l in range(n)]
+    ldev = [to_dev(L) for L in layers]
+    h0 = synth.normal_vector(synth.rng(synth.W_CHAIN, 99), dims["hidden"])
+    hs = [h0]
+    for l in range(n):
+        hs.append(run_chain([ldev[l]], hs[-1], dims))
+    worst = []
+    for l in (0, 1, n - 1):
+        w, _ = check_layer(hs[l], hs[l + 1], layers[l], dims)
+        worst.append(w)
+    hall = run_chain(ldev, h0, dims)
+    assert np.array_equal(hall, hs[-1])
+    ref = h0.astype(np.float64)
+    for L in layers:
+        ref = oracle.layer_forward(L, dims, ref)
+    rel = np.linalg.norm(hall - ref) / np.linalg.norm(ref)
+    print(f"chain 34 layers: worst teacher-forced err/tol {max(worst):.3e}, "
+          f"end-to-end relative L2 {rel:.2e}")
+    assert rel < 1e-3
+
+
+def test_chain_rejects_bad_arguments():
+    dims = dict(SMALL)
+    L = to_dev(synth.chain_layer(0, dims))
+    h = torch.zeros(dims["hidden"], device="cuda")
+    with pytest.raises(ops.QwsError):
+        ops.decode_chain([L], h, dict(dims, hidden=500))
+    with pytest.raises(ops.QwsError):
+        ops.decode_chain([dict(L, fmt_qkv=oracle.Q6_K)], h, dims)
+    with pytest.raises(ops.QwsError):
+        ops.decode_chain([L], h, dict(dims, n_q_heads=3))
