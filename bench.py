@@ -1,0 +1,365 @@
+"""Benchmark: one single-token decode step of a Gemma-3-4B-shaped model.
+
+step = qws_decode_chain over 34 layers (Q4_K q/k/v/o/gate/up, Q6_K down,
+       sandwich rms_norms) + final rms_norm + Q4_0 lm_head (262144 x 2560).
+Metric: achieved HBM GB/s of the packed-weight stream (+ vector bytes), with
+microseconds per token of the 34-layer chain reported alongside.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+For N > 1 launch with torchrun; every rank runs an independent replica of the
+step on its own GPU (the path has no data exchange; "replicas only").
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = ("Q4_K GEMV achieved HBM GB/s (% of GB300 peak); µs/token for 34-layer chain")
+WORKLOAD = ("decode step, batch 1: 34-layer Gemma-3-4B chain (hidden 2560, inter 10240, q 8x256, "
+            "kv 4x256; Q4_K q/k/v/o/gate/up, Q6_K down, rms_norm eps 1e-6 sandwich norms, "
+            "attention at seq 1) + final rms_norm + Q4_0 lm_head 262144x2560")
+N_LAYERS = 34
+VOCAB = 262144
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["engine.cuh", "formats.cuh", "device_common.cuh", "chain.cu"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for n in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "quantized_weight_streaming_q4k_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic():
+    """dram bytes per chain launch from the committed ncu summary, if it was
+    taken on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "chain_kernel_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("kernel_hash") != kernel_hash():
+        return None
+    return float(d["bytes_per_launch"])
+
+
+def algorithmic_bytes(dims):
+    from quantized_weight_streaming_q4k_gb300 import synth
+    H, I = dims["hidden"], dims["inter"]
+    qd = dims["n_q_heads"] * dims["head_dim"]
+    kd = dims["n_kv_heads"] * dims["head_dim"]
+    q4k = lambda r, c: synth.n_blocks(synth.Q4_K, r, c) * 144
+    q6k = lambda r, c: synth.n_blocks(synth.Q6_K, r, c) * 210
+    layer_w = q4k(qd + 2 * kd, H) + q4k(H, qd) + 2 * q4k(I, H) + q6k(H, I)
+    norm_w = 4 * H * 4
+    chain = N_LAYERS * (layer_w + norm_w) + 2 * H * 4          # + h in and out
+    lm_head = synth.n_blocks(synth.Q4_0, VOCAB, H) * 18 + H * 4 + VOCAB * 4
+    final_norm = 3 * H * 4
+    return chain, final_norm, lm_head
+
+
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, ident: str):
+        self.ident = ident
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.ident}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    return world, rank, local
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+def cpu_oracle_sample(max_seconds: float = 15.0):
+    """Times the oracle (as it stands) on a bounded sample of the same step:
+    whole decoder layers of the chain workload, single host thread."""
+    import oracle
+    from quantized_weight_streaming_q4k_gb300 import synth
+    dims = synth.GEMMA3_4B
+    chain_b, _, _ = algorithmic_bytes(dims)
+    per_layer = chain_b / N_LAYERS
+    h = synth.normal_vector(synth.rng(synth.W_CHAIN, 99), dims["hidden"]).astype(np.float64)
+    layers_done, t0 = 0, time.perf_counter()
+    elapsed = 0.0
+    while True:
+        L = synth.chain_layer(layers_done % N_LAYERS, dims)
+        t1 = time.perf_counter()
+        h = oracle.layer_forward(L, dims, h)
+        elapsed += time.perf_counter() - t1
+        layers_done += 1
+        if elapsed > max_seconds or layers_done >= N_LAYERS:
+            break
+    del t0
+    return {"value": per_layer * layers_done / elapsed / 1e9, "unit": "GB/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{layers_done} of {N_LAYERS} decoder layers of the same workload "
+                      f"({per_layer * layers_done / 1e6:.0f} MB of packed weights), f64 oracle, "
+                      f"{elapsed:.1f} s on 1 host thread"}
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the f64 CPU oracle, timed on the host's cores."""
+    if rank != 0:
+        return
+    import oracle
+    from quantized_weight_streaming_q4k_gb300 import synth
+    dims = synth.GEMMA3_4B
+    chain_b, _, _ = algorithmic_bytes(dims)
+    per_layer = chain_b / N_LAYERS
+    h = synth.normal_vector(synth.rng(synth.W_CHAIN, 99), dims["hidden"]).astype(np.float64)
+    L = synth.chain_layer(0, dims)
+    for _ in range(max(0, min(args.warmup, 1))):
+        oracle.layer_forward(L, dims, h)
+    times = []
+    for s in range(args.steps):
+        t = time.perf_counter()
+        h = oracle.layer_forward(L, dims, h)
+        times.append(time.perf_counter() - t)
+    tot = sum(times)
+    value = per_layer * len(times) / tot / 1e9
+    out = {"metric": METRIC, "value": value, "unit": "GB/s", "impl": "reference",
+           "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": 1e3 * tot / len(times), "higher_is_better": True, "scaling": "weak",
+           "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": WORKLOAD, "sample": "one decoder layer per step"},
+           "cpu_baseline": {"value": value, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                            "sample": "one of the 34 decoder layers per step (59.8 MB of "
+                                      "packed weights), f64 oracle, 1 host thread"},
+           "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    print(json.dumps(out))
+
+
+def run_gpu(args, world, rank, local):
+    import torch
+
+    from quantized_weight_streaming_q4k_gb300 import build, ops, synth
+    build.build()
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    dims = synth.GEMMA3_4B
+    H = dims["hidden"]
+    chain_b, fnorm_b, lm_b = algorithmic_bytes(dims)
+
+    # ---- inputs, resident in HBM
+    layers = []
+    for l in range(N_LAYERS):
+        L = synth.chain_layer(l, dims)
+        layers.append({k: (torch.from_numpy(v).to(dev) if isinstance(v, np.ndarray) else v)
+                       for k, v in L.items()})
+    structs = [ops.make_layer(L) for L in layers]
+    g = synth.rng(synth.W_LM_HEAD, 0)
+    W_lm = torch.from_numpy(synth.q4_0_matrix(g, VOCAB, H)).to(dev)
+    w_final = torch.from_numpy(synth.norm_weights(synth.rng(synth.W_CHAIN, synth.T_NFINAL), H)).to(dev)
+    h0 = torch.from_numpy(synth.normal_vector(synth.rng(synth.W_CHAIN, 99), H)).to(dev)
+    h = torch.empty_like(h0)
+    hn = torch.empty_like(h0)
+    logits = torch.empty(VOCAB, device=dev)
+    ws = torch.empty(ops.workspace_bytes(ops.OP_DECODE_CHAIN, 0, H, dims["inter"]),
+                     dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        h.copy_(h0)
+        if ev:
+            ev[0].record(stream)
+        ops.decode_chain(structs, h, dims, workspace=ws)
+        if ev:
+            ev[1].record(stream)
+        ops.rms_norm(h, w_final, dims["eps"], out=hn)
+        ops.q4_0_matvec(W_lm, hn, VOCAB, H, out=logits)
+        if ev:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    ident = (uuid if uuid.startswith("GPU-") else f"GPU-{uuid}") if uuid else str(local)
+    clocks = ClockSampler(ident)
+    clocks.start()
+    barrier(world)
+    torch.cuda.synchronize()
+    start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    total_ms = start.elapsed_time(stop)
+    chain_ms = [a.elapsed_time(b) for a, b, _ in evs]
+    lm_ms = [b.elapsed_time(c) for _, b, c in evs]
+    assert ops.device_error() == 0
+    total_ms = max_over_ranks(total_ms, world)
+
+    # ---- end to end through host buffers (pinned): h0 in, logits out
+    h_host = h0.cpu().pin_memory()
+    logits_host = torch.empty(VOCAB, dtype=torch.float32).pin_memory()
+
+    def step_e2e():
+        h.copy_(h_host, non_blocking=True)
+        ops.decode_chain(structs, h, dims, workspace=ws)
+        ops.rms_norm(h, w_final, dims["eps"], out=hn)
+        ops.q4_0_matvec(W_lm, hn, VOCAB, H, out=logits)
+        logits_host.copy_(logits, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step_e2e()
+    torch.cuda.synchronize()
+    e_steps = max(1, min(args.steps, 200))
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(e_steps):
+        step_e2e()
+    b.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(a.elapsed_time(b), world) / e_steps
+
+    bytes_step = chain_b + fnorm_b + lm_b
+    ms_step = total_ms / args.steps
+    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+    chain_avg = statistics.mean(chain_ms)
+    peak, peak_kind = peaks()
+    achieved = chain_b / (chain_avg * 1e-3) / 1e9
+    if rank != 0:
+        return
+    out = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded random Q4_K/Q6_K/Q4_0 blocks, Gemma-3-4B shapes)",
+        "config": {"workload": WORKLOAD, "n_layers": N_LAYERS, "vocab": VOCAB, "batch": 1,
+                   "l2": "inputs larger than L2: 2.41 GB of weights streamed per step",
+                   "parallelism": f"replicas x{world}"},
+        "chain_us_per_token": 1e3 * chain_avg,
+        "lm_head_us": 1e3 * statistics.mean(lm_ms),
+        "bytes_per_step": bytes_step,
+        "roofline": {"bound": "hbm", "kernel": "chain_kernel (34-layer decode chain)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_kind,
+                     "traffic": profiled_traffic()},
+        "e2e": {"value": world * bytes_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+                "h2d_bytes_per_step": H * 4, "d2h_bytes_per_step": VOCAB * 4,
+                "ms_per_step": e2e_ms},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clk,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_oracle_sample()
+    print(json.dumps(out))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = dist_init()
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_gpu(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

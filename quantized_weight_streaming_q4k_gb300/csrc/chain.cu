@@ -118,13 +118,20 @@ __device__ __forceinline__ float block_sum(float v, float* wsum, int ctid, int C
 }
 
 // 1 / sqrt(mean(v^2) + eps) over n values read through ld_cg (other CTAs'
-// outputs), identical in every CTA.
+// outputs), identical in every CTA.  Loads go out 8 at a time.
 __device__ __forceinline__ float inv_rms_global(const float* v, int64_t n, float eps,
                                                 float* wsum, int ctid, int C) {
+  constexpr int kChunk = 8;
   float ss = 0.f;
-  for (int64_t i = ctid; i < n; i += C) {
-    const float t = ld_cg(v + i);
-    ss = fmaf(t, t, ss);
+  for (int64_t base = ctid; base < n; base += static_cast<int64_t>(kChunk) * C) {
+    float t[kChunk];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const int64_t i = base + static_cast<int64_t>(j) * C;
+      t[j] = i < n ? ld_cg(v + i) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) ss = fmaf(t[j], t[j], ss);
   }
   ss = block_sum(ss, wsum, ctid, C);
   return 1.0f / sqrtf(ss / static_cast<float>(n) + eps);
@@ -139,7 +146,9 @@ struct NormSrc {  // vec[i] * inv * w[i]
   const float* vec;
   const float* w;
   float inv;
-  __device__ __forceinline__ float operator()(int64_t i) const { return vec[i] * inv * w[i]; }
+  __device__ __forceinline__ float operator()(int64_t i) const {
+    return __fmul_rn(__fmul_rn(vec[i], inv), w[i]);
+  }
 };
 
 struct GatherSrc {  // attention at seq 1: query head i / hd reads kv head (i / hd) / group
@@ -151,19 +160,79 @@ struct GatherSrc {  // attention at seq 1: query head i / hd reads kv head (i / 
   }
 };
 
-// hout[i] = base[i] + (post ? add[i] * inv * w[i] : add[i]) into shared vec;
-// CTA 0 also stores it to global `store` (if non-null).  Returns nothing;
-// base may be a global vector written by other CTAs (read with ld_cg).
+// vec[i] = base[i] + (post ? add[i] * inv * w[i] : add[i]); CTA 0 also stores
+// it to global `store` (if non-null).  base and add may be written by other
+// CTAs (read with ld_cg).  Loads go out 8 elements at a time.
 __device__ __forceinline__ void residual_into(float* vec, const float* base, const float* add,
                                               const float* w, float inv, bool post,
                                               float* store, int64_t n, int ctid, int C) {
-  for (int64_t i = ctid; i < n; i += C) {
-    const float a = ld_cg(add + i);
-    const float r = ld_cg(base + i) + (post ? a * inv * w[i] : a);
-    vec[i] = r;
-    if (store) store[i] = r;
+  constexpr int kChunk = 8;
+  for (int64_t b0 = ctid; b0 < n; b0 += static_cast<int64_t>(kChunk) * C) {
+    float a[kChunk], h[kChunk], ww[kChunk];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const int64_t i = b0 + static_cast<int64_t>(j) * C;
+      const bool in = i < n;
+      a[j] = in ? ld_cg(add + i) : 0.f;
+      h[j] = in ? ld_cg(base + i) : 0.f;
+      ww[j] = (in && post) ? w[i] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const int64_t i = b0 + static_cast<int64_t>(j) * C;
+      if (i < n) {
+        // explicit roundings: the same value must come out of every call site
+        const float r = __fadd_rn(h[j], post ? __fmul_rn(__fmul_rn(a[j], inv), ww[j]) : a[j]);
+        vec[i] = r;
+        if (store) store[i] = r;
+      }
+    }
   }
 }
+
+// vec[i] = src[i] (and store[i] = src[i] if store), loads 8 at a time.
+__device__ __forceinline__ void copy_into(float* vec, const float* src, float* store, int64_t n,
+                                          int ctid, int C) {
+  constexpr int kChunk = 8;
+  for (int64_t b0 = ctid; b0 < n; b0 += static_cast<int64_t>(kChunk) * C) {
+    float t[kChunk];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const int64_t i = b0 + static_cast<int64_t>(j) * C;
+      t[j] = i < n ? ld_cg(src + i) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const int64_t i = b0 + static_cast<int64_t>(j) * C;
+      if (i < n) {
+        vec[i] = t[j];
+        if (store) store[i] = t[j];
+      }
+    }
+  }
+}
+
+// The per-format decode loops and the two reducer epilogues as separate
+// functions: each gets the whole register budget instead of sharing one
+// allocation with every other role and phase of the kernel.
+__device__ __noinline__ bool chain_consume_q4k(const Phase& P, const Ring& R, RingPos& pos,
+                                               int ctid, int C) {
+  return consume_phase<UnitQ4K, false, false>(P, R, pos, XOfPlain{nullptr, 0}, ctid, C, &g_err_chain);
+}
+__device__ __noinline__ bool chain_consume_q6k(const Phase& P, const Ring& R, RingPos& pos,
+                                               int ctid, int C) {
+  return consume_phase<UnitQ6K, false, false>(P, R, pos, XOfPlain{nullptr, 0}, ctid, C, &g_err_chain);
+}
+__device__ __forceinline__ bool chain_reduce(const Phase& P, const Ring& R, RingPos& pos) {
+  return P.epi == EPI_GEGLU ? reduce_phase(P, R, pos, EpiGeglu{}, &g_err_chain)
+                            : reduce_phase(P, R, pos, EpiStore{}, &g_err_chain);
+}
+
+// Builds the input vector of phase ph into the staging buffer R.xs (all
+// consumer threads; ends with a consumer barrier).  Kept out of line: it runs
+// once per phase and must not inflate the decode loop's registers.
+__device__ __noinline__ void chain_prologue(const ChainParams& p, int ph, const Ring& R,
+                                            float* vec, float* wsum, bool q6, int ctid, int C);
 
 // ------------------------------------------------------------------ kernel
 __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
@@ -195,12 +264,12 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
     const int lane = threadIdx.x & 31;
     for (int ph = 0; ph < nph; ++ph) {
       const Phase P = phases.get(ph);
-      bool ok = (P.epi == EPI_GEGLU) ? reduce_phase(P, R, pos, EpiGeglu{}, &g_err_chain)
-                                     : reduce_phase(P, R, pos, EpiStore{}, &g_err_chain);
+      bool ok = chain_reduce(P, R, pos);
       __syncwarp();
       if (lane == 0) {
         if (ok) {
-          __threadfence();
+          // __syncwarp above orders the warp's epilogue stores before this
+          // lane's release; the release-add publishes them at gpu scope
           red_release_gpu_add(p.counter, 1u);
           const unsigned target = static_cast<unsigned>(ph + 1) * gridDim.x;
           const long long t0 = clock64();
@@ -223,77 +292,143 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
 
   // ---------------- consumers
   const int ctid = static_cast<int>(threadIdx.x) - kRoleThreads;
-  const int64_t H = p.H;
-  const bool post = p.post_norms != 0;
-  const int group = p.n_q_heads / p.n_kv_heads;
+  const bool down_q6k = p.kp[PH_DOWN].fmt == 14;
   for (int ph = 0; ph < nph; ++ph) {
-    const int l = ph >> 2, kind = ph & 3;
     if (ph > 0) {
       bar_sync(kChainBar, C + 32);   // previous phase complete on every CTA
       if (*abort_flag) return;
     }
     const Phase P = phases.get(ph);
-    const ChainLayer& L = p.L[l];
-    const int US = red_stride(P.U);
-    bool ok = true;
-    if (kind == PH_QKV) {
-      // h = layer input; n1 = rms_norm(h, w_in)
-      if (l == 0) {
-        for (int64_t i = ctid; i < H; i += C) vec[i] = p.h[i];
-      } else {
-        const ChainLayer& Lp = p.L[l - 1];
-        const float inv_f = post ? inv_rms_global(p.f, H, p.eps, wsum, ctid, C) : 1.f;
-        residual_into(vec, p.h1, p.f, Lp.w_pff, inv_f, post, blockIdx.x == 0 ? p.hin : nullptr,
-                      H, ctid, C);
-      }
-      if (l == 0 && blockIdx.x == 0)
-        for (int64_t i = ctid; i < H; i += C) p.hin[i] = vec[i];
-      __threadfence();
-      bar_sync(kConsumerBar, C);
-      float ss = 0.f;
-      for (int64_t i = ctid; i < H; i += C) ss = fmaf(vec[i], vec[i], ss);
-      const float inv = 1.0f / sqrtf(block_sum(ss, wsum, ctid, C) / static_cast<float>(H) + p.eps);
-      stage_x<UnitQ4K>(R.xs, US, NormSrc{vec, L.w_in, inv}, P.K, ctid, C);
-      bar_sync(kConsumerBar, C);
-      ok = consume_phase<UnitQ4K, false>(P, R, pos, XOfPlain{nullptr, 0}, ctid, C, &g_err_chain);
-    } else if (kind == PH_O) {
-      stage_x<UnitQ4K>(R.xs, US, GatherSrc{p.v, p.head_dim, group}, P.K, ctid, C);
-      bar_sync(kConsumerBar, C);
-      ok = consume_phase<UnitQ4K, false>(P, R, pos, XOfPlain{nullptr, 0}, ctid, C, &g_err_chain);
-    } else if (kind == PH_GU) {
-      // h1 = h + rms_norm(o, w_post_attn) (or h + o); n2 = rms_norm(h1, w_pre_ffn)
-      const float inv_o = post ? inv_rms_global(p.o, H, p.eps, wsum, ctid, C) : 1.f;
-      residual_into(vec, p.hin, p.o, L.w_pa, inv_o, post, blockIdx.x == 0 ? p.h1 : nullptr, H,
-                    ctid, C);
-      __threadfence();
-      bar_sync(kConsumerBar, C);
-      float ss = 0.f;
-      for (int64_t i = ctid; i < H; i += C) ss = fmaf(vec[i], vec[i], ss);
-      const float inv = 1.0f / sqrtf(block_sum(ss, wsum, ctid, C) / static_cast<float>(H) + p.eps);
-      stage_x<UnitQ4K>(R.xs, US, NormSrc{vec, L.w_pf, inv}, P.K, ctid, C);
-      bar_sync(kConsumerBar, C);
-      ok = consume_phase<UnitQ4K, false>(P, R, pos, XOfPlain{nullptr, 0}, ctid, C, &g_err_chain);
-    } else {
-      if (P.fmt == 14) {
-        stage_x<UnitQ6K>(R.xs, US, XCoherent{p.m}, P.K, ctid, C);
-        bar_sync(kConsumerBar, C);
-        ok = consume_phase<UnitQ6K, false>(P, R, pos, XOfPlain{nullptr, 0}, ctid, C, &g_err_chain);
-      } else {
-        stage_x<UnitQ4K>(R.xs, US, XCoherent{p.m}, P.K, ctid, C);
-        bar_sync(kConsumerBar, C);
-        ok = consume_phase<UnitQ4K, false>(P, R, pos, XOfPlain{nullptr, 0}, ctid, C, &g_err_chain);
-      }
-    }
+    // the phase's input vector, staged in R.xs (transposed per lane unit)
+    const bool q6 = (ph & 3) == PH_DOWN && down_q6k;
+    chain_prologue(p, ph, R, vec, wsum, q6, ctid, C);
+    const bool ok = q6 ? chain_consume_q6k(P, R, pos, ctid, C)
+                       : chain_consume_q4k(P, R, pos, ctid, C);
     if (!ok) *abort_flag = 1;   // the reducer will time out too and abort at the next barrier
   }
   // final residual: h = h1 + rms_norm(f, w_post_ffn) (or h1 + f)
   bar_sync(kChainBar, C + 32);
   if (*abort_flag) return;
   if (blockIdx.x == 0) {
+    const bool post = p.post_norms != 0;
     const ChainLayer& Lp = p.L[p.n_layers - 1];
-    const float inv_f = post ? inv_rms_global(p.f, H, p.eps, wsum, ctid, C) : 1.f;
-    residual_into(vec, p.h1, p.f, Lp.w_pff, inv_f, post, p.h, H, ctid, C);
+    const float inv_f = post ? inv_rms_global(p.f, p.H, p.eps, wsum, ctid, C) : 1.f;
+    residual_into(vec, p.h1, p.f, Lp.w_pff, inv_f, post, p.h, p.H, ctid, C);
   }
+}
+
+// r = base + (post ? add * rms_inv(add) * wa : add)      (or r = base if !add)
+// x = r * rms_inv(r) * wn                                 -> staged for Q4_K units
+// store[i] = r[i] when store != nullptr.  All global loads of a thread are
+// issued at once (one memory latency), provided H <= 8 * C.
+__device__ __forceinline__ void resnorm_stage(const ChainParams& p, const Ring& R, float* wsum,
+                                              const float* base, const float* add,
+                                              const float* wa, const float* wn, float* store,
+                                              int US, int ctid, int C) {
+  constexpr int kJ = 8;
+  const int64_t H = p.H;
+  const bool post = p.post_norms != 0;
+  float bs[kJ], ad[kJ], wwa[kJ], wwn[kJ];
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    const int64_t i = ctid + static_cast<int64_t>(j) * C;
+    const bool in = i < H;
+    bs[j] = in ? ld_cg(base + i) : 0.f;
+    ad[j] = (in && add) ? ld_cg(add + i) : 0.f;
+    wwa[j] = (in && add && post) ? wa[i] : 0.f;
+    wwn[j] = in ? wn[i] : 0.f;
+  }
+  float inv1 = 1.f;
+  if (add && post) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) ss = fmaf(ad[j], ad[j], ss);
+    inv1 = 1.0f / sqrtf(block_sum(ss, wsum, ctid, C) / static_cast<float>(H) + p.eps);
+  }
+  float ss2 = 0.f;
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    // explicit roundings: every CTA and call site computes the same r
+    float r = bs[j];
+    if (add) r = __fadd_rn(bs[j], post ? __fmul_rn(__fmul_rn(ad[j], inv1), wwa[j]) : ad[j]);
+    bs[j] = r;
+    ss2 = fmaf(r, r, ss2);
+  }
+  if (store) {
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int64_t i = ctid + static_cast<int64_t>(j) * C;
+      if (i < H) store[i] = bs[j];
+    }
+    __threadfence();   // published to other CTAs through the phase barrier
+  }
+  const float inv2 = 1.0f / sqrtf(block_sum(ss2, wsum, ctid, C) / static_cast<float>(H) + p.eps);
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    const int64_t i = ctid + static_cast<int64_t>(j) * C;
+    if (i < H) {
+      int u, l;
+      UnitQ4K::unit_of(i, u, l);
+      R.xs[l * US + u] = __fmul_rn(__fmul_rn(bs[j], inv2), wwn[j]);
+    }
+  }
+}
+
+__device__ __noinline__ void chain_prologue(const ChainParams& p, int ph, const Ring& R,
+                                            float* vec, float* wsum, bool q6, int ctid, int C) {
+  const int l = ph >> 2, kind = ph & 3;
+  const ChainLayer& L = p.L[l];
+  const int64_t H = p.H;
+  const bool post = p.post_norms != 0;
+  const KindPlan& kp = p.kp[kind];
+  const int US = red_stride(kp.U);
+  const bool fast = H <= 8 * static_cast<int64_t>(C);
+  if ((kind == PH_QKV || kind == PH_GU) && fast) {
+    if (kind == PH_QKV) {
+      if (l == 0)
+        resnorm_stage(p, R, wsum, p.h, nullptr, nullptr, L.w_in,
+                      blockIdx.x == 0 ? p.hin : nullptr, US, ctid, C);
+      else
+        resnorm_stage(p, R, wsum, p.h1, p.f, p.L[l - 1].w_pff, L.w_in,
+                      blockIdx.x == 0 ? p.hin : nullptr, US, ctid, C);
+    } else {
+      resnorm_stage(p, R, wsum, p.hin, p.o, L.w_pa, L.w_pf, blockIdx.x == 0 ? p.h1 : nullptr, US,
+                    ctid, C);
+    }
+  } else if (kind == PH_QKV || kind == PH_GU) {
+    // general sizes: several passes through shared memory
+    if (kind == PH_QKV) {
+      if (l == 0) {
+        copy_into(vec, p.h, blockIdx.x == 0 ? p.hin : nullptr, H, ctid, C);
+      } else {
+        const ChainLayer& Lp = p.L[l - 1];
+        const float inv_f = post ? inv_rms_global(p.f, H, p.eps, wsum, ctid, C) : 1.f;
+        residual_into(vec, p.h1, p.f, Lp.w_pff, inv_f, post, blockIdx.x == 0 ? p.hin : nullptr,
+                      H, ctid, C);
+      }
+    } else {
+      const float inv_o = post ? inv_rms_global(p.o, H, p.eps, wsum, ctid, C) : 1.f;
+      residual_into(vec, p.hin, p.o, L.w_pa, inv_o, post, blockIdx.x == 0 ? p.h1 : nullptr, H,
+                    ctid, C);
+    }
+    bar_sync(kConsumerBar, C);
+    float ss = 0.f;
+    for (int64_t i = ctid; i < H; i += C) ss = fmaf(vec[i], vec[i], ss);
+    const float inv =
+        1.0f / sqrtf(block_sum(ss, wsum, ctid, C) / static_cast<float>(H) + p.eps);
+    stage_x<UnitQ4K>(R.xs, US, NormSrc{vec, kind == PH_QKV ? L.w_in : L.w_pf, inv}, kp.K, ctid,
+                     C);
+  } else if (kind == PH_O) {
+    stage_x<UnitQ4K>(R.xs, US, GatherSrc{p.v, p.head_dim, p.n_q_heads / p.n_kv_heads}, kp.K, ctid,
+                     C);
+  } else if (q6) {
+    stage_x<UnitQ6K, XCoherent, 32>(R.xs, US, XCoherent{p.m}, kp.K, ctid, C);
+  } else {
+    stage_x<UnitQ4K, XCoherent, 32>(R.xs, US, XCoherent{p.m}, kp.K, ctid, C);
+  }
+  // stores of h / h1 by CTA 0 are published by the reducer's release at the
+  // end of this phase (they precede it in CTA order through the barriers)
+  bar_sync(kConsumerBar, C);
 }
 
 // ------------------------------------------------------------------ host side
@@ -431,7 +566,7 @@ qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
                        row_bytes_of(kinds[i].fmt, kinds[i].K)};
     stage_need = std::max(stage_need, tp.stage_need);
     red = std::max(red, tp.red_floats);
-    xs = std::max<uint32_t>(xs, kUnitWeights * red_stride(tp.U));
+    xs = std::max<uint32_t>(xs, unit_weights(kinds[i].fmt) * red_stride(tp.U));
   }
   p.stage_bytes = round_up(stage_need + 16, 128);
   p.red_floats = red;

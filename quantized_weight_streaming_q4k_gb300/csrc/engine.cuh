@@ -281,14 +281,28 @@ struct XUnit {
 };
 
 // Copies activation vector `src` (K columns) into the transposed staging
-// buffer with coalesced reads.  Called by all C consumer threads.
-template <class Unit, class Src>
+// buffer with coalesced reads.  Called by all C consumer threads.  Loads are
+// issued in chunks of 8 before any is used, so a thread waits for one memory
+// latency per chunk rather than per element.
+template <class Unit, class Src, int kChunk = 8>
 __device__ __forceinline__ void stage_x(float* xs, int US, const Src& src, int64_t K, int ctid,
                                         int C) {
-  for (int64_t col = ctid; col < K; col += C) {
-    int u, l;
-    Unit::unit_of(col, u, l);
-    xs[l * US + u] = src(col);
+  for (int64_t base = ctid; base < K; base += static_cast<int64_t>(kChunk) * C) {
+    float v[kChunk];
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const int64_t col = base + static_cast<int64_t>(j) * C;
+      v[j] = col < K ? src(col) : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kChunk; ++j) {
+      const int64_t col = base + static_cast<int64_t>(j) * C;
+      if (col < K) {
+        int u, l;
+        Unit::unit_of(col, u, l);
+        xs[l * US + u] = v[j];
+      }
+    }
   }
 }
 
@@ -299,9 +313,13 @@ __device__ __forceinline__ void stage_x(float* xs, int US, const Src& src, int64
 // returns a column loader of vector b; vectors are staged one at a time
 // through shared memory.  With STAGED = false the caller has already written
 // the single vector (B = 1) into R.xs.  Returns false on a timeout.
-template <class Unit, bool STAGED = true, class XOf>
-__device__ __forceinline__ bool consume_phase(const Phase& P, const Ring& R, RingPos& pos,
+template <class Unit, bool STAGED = true, bool PIPE = true, class XOf>
+__device__ __forceinline__ bool consume_phase(const Phase& Pref, const Ring& Rref, RingPos& pos,
                                               const XOf& x_of, int ctid, int C, unsigned* err) {
+  // private copies: the loop stores through generic pointers, which could
+  // otherwise alias a referenced Phase and force reloads
+  const Phase P = Pref;
+  const Ring R = Rref;
   const int cta = static_cast<int>(blockIdx.x) - P.cta0;
   if (cta < 0 || cta >= P.ncta) return true;
   const int U = P.U, G = P.G, US = red_stride(P.U);
@@ -333,7 +351,12 @@ __device__ __forceinline__ bool consume_phase(const Phase& P, const Ring& R, Rin
     const uint8_t* st = R.stage(pos.s);
     float* red = red_b + static_cast<size_t>(pos.s) * R.red_floats;
     const int nr = pair ? 2 * tr.nrows : tr.nrows;
-    if (active && gg < nr) {
+    if (!PIPE && active) {
+      for (int r = gg; r < nr; r += G) {
+        const int slot = (pair && r >= tr.nrows) ? P.T + (r - tr.nrows) : r;
+        red[slot * US] = unit.row(st + slot * rb);
+      }
+    } else if (active && gg < nr) {
       // row r of the tile lives at slot(r) rows into the stage; the next
       // row's bytes are loaded while the current one is decoded
       int r = gg;
@@ -359,6 +382,21 @@ __device__ __forceinline__ bool consume_phase(const Phase& P, const Ring& R, Rin
   return true;
 }
 
+// sum of p[c] for c = c0, c0 + step, ... < n, in a fixed order: four
+// interleaved partial sums (independent loads), then ((s0 + s1) + (s2 + s3)).
+__device__ __forceinline__ float strided_sum(const float* p, int c0, int n, int step) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  int c = c0;
+  for (; c + 3 * step < n; c += 4 * step) {
+    s0 += p[c];
+    s1 += p[c + step];
+    s2 += p[c + 2 * step];
+    s3 += p[c + 3 * step];
+  }
+  for (; c < n; c += step) s0 += p[c];
+  return (s0 + s1) + (s2 + s3);
+}
+
 // Reduce all tiles of phase P for this CTA (one warp).  Output i of a tile is
 // (vector b, row o), i = b * nrows + o.  Lanes form groups of gsz lanes per
 // output (gsz = 32 when the tile has one output, 1 when it has >= 32); each
@@ -366,8 +404,10 @@ __device__ __forceinline__ bool consume_phase(const Phase& P, const Ring& R, Rin
 // its lanes with a fixed xor tree: the order never changes between runs.
 // epi(P, tr, b, o, v, v2) stores the result (v2 = the up row for GEGLU).
 template <class Epi>
-__device__ __forceinline__ bool reduce_phase(const Phase& P, const Ring& R, RingPos& pos,
+__device__ __forceinline__ bool reduce_phase(const Phase& Pref, const Ring& Rref, RingPos& pos,
                                              const Epi& epi, unsigned* err) {
+  const Phase P = Pref;
+  const Ring R = Rref;
   const int cta = static_cast<int>(blockIdx.x) - P.cta0;
   if (cta < 0 || cta >= P.ncta) return true;
   const int lane = threadIdx.x & 31;
@@ -395,9 +435,8 @@ __device__ __forceinline__ bool reduce_phase(const Phase& P, const Ring& R, Ring
       const float* rr = red + (ob * slots + o) * US;
       float v = 0.f, v2 = 0.f;
       if (valid) {
-        for (int c = sub; c < U; c += gsz) v += rr[c];
-        if (pair)
-          for (int c = sub; c < U; c += gsz) v2 += rr[P.T * US + c];
+        v = strided_sum(rr, sub, U, gsz);
+        if (pair) v2 = strided_sum(rr + P.T * US, sub, U, gsz);
       }
       for (int w = gsz >> 1; w > 0; w >>= 1) {
         v += __shfl_xor_sync(0xFFFFFFFFu, v, w);

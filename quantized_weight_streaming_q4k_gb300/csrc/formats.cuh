@@ -8,9 +8,9 @@
 //                        w = d*sc[i/16]*(q-32)
 //   Q4_0  18 B /  32 w : f16 d, 16 B nibbles;  w = d*(q-8)
 //
-// Lane unit.  Every lane owns a fixed group of 64 columns of the row ("unit")
-// and keeps the matching 64 activations in registers for the whole phase
-// (x-stationary).  The weight bytes of one row stream through shared memory;
+// Lane unit.  Every lane owns a fixed group of 64 (Q6_K: 32) columns of the
+// row ("unit") and keeps the matching activations in registers for the whole
+// phase (x-stationary).  The weight bytes of one row stream through shared memory;
 // for each row the lane decodes its unit and returns a partial dot product.
 //
 // Decode without int->float conversion.  A 4- or 6-bit field masked in place
@@ -32,7 +32,9 @@
 namespace qws {
 
 constexpr int kE = 89;                 // x' = x * 2^(kE - pos)
-constexpr int kUnitWeights = 64;       // columns per lane unit, all formats
+
+// columns per lane unit of each format
+__host__ __device__ constexpr int unit_weights(int fmt) { return fmt == 14 ? 32 : 64; }
 
 __device__ __forceinline__ float bits(uint32_t v) { return __uint_as_float(v); }
 
@@ -65,6 +67,7 @@ __device__ __forceinline__ void nibble_word(uint32_t w, const float* xl, const f
 // ---------------------------------------------------------------------------
 struct UnitQ4K {
   static constexpr int kFmt = 12;
+  static constexpr int kUnitW = 64;
   static constexpr int kBlockW = 256;
   static constexpr int kBlockBytes = 144;
   float xa[32];   // sub-block 2c,   column 64c + l,      pre-scaled
@@ -153,58 +156,58 @@ struct UnitQ4K {
 };
 
 // ---------------------------------------------------------------------------
-// Q6_K.  Unit u -> super-block kb = u/4, half h = (u/2)%2, column group
-// j = u%2: weights 128h + 32a + 16j + i for a = 0..3, i = 0..15.  Bytes:
-// ql[64h+16j ..+16] (a=0 low nibbles, a=2 high), ql[64h+32+16j ..+16] (a=1,
-// a=3), qh[32h+16j ..+16] (2-bit fields a=0..3 at bits 0,2,4,6), scales
-// sc[8h+2a+j].  Blocks are 210 B, so a block starts on a 2-byte boundary:
-// the lane loads aligned words and funnel-shifts them.
+// Q6_K.  Unit u -> super-block kb = u/8, half h = (u/4)%2, column group
+// jj = u%4: weights 128h + 32a + 8jj + i for a = 0..3, i = 0..7 (32 weights).
+// Bytes: ql[64h+8jj ..+8] (a=0 low nibbles, a=2 high), ql[64h+32+8jj ..+8]
+// (a=1, a=3), qh[32h+8jj ..+8] (2-bit fields a=0..3 at bits 0,2,4,6); scale
+// of column group a is sc[(128h + 32a + 8jj) / 16] = sc[8h + 2a + jj/2].
+// Blocks are 210 B, so a block starts on a 2-byte boundary: the lane loads
+// aligned words and funnel-shifts them.  A 32-column unit keeps the lane's
+// activations at 32 registers.
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void load16_a2(const uint8_t* p, uint32_t (&w)[4]) {
+__device__ __forceinline__ void load8_a2(const uint8_t* p, uint32_t& w0, uint32_t& w1) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p);
   const uint32_t* q = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
   const uint32_t s = static_cast<uint32_t>(a & 3u) * 8u;
-  const uint32_t r0 = q[0], r1 = q[1], r2 = q[2], r3 = q[3], r4 = q[4];
-  w[0] = __funnelshift_r(r0, r1, s);
-  w[1] = __funnelshift_r(r1, r2, s);
-  w[2] = __funnelshift_r(r2, r3, s);
-  w[3] = __funnelshift_r(r3, r4, s);
+  const uint32_t r0 = q[0], r1 = q[1], r2 = q[2];
+  w0 = __funnelshift_r(r0, r1, s);
+  w1 = __funnelshift_r(r1, r2, s);
 }
 
 struct UnitQ6K {
   static constexpr int kFmt = 14;
+  static constexpr int kUnitW = 32;
   static constexpr int kBlockW = 256;
   static constexpr int kBlockBytes = 210;
-  float x[4][16];   // [a][i], pre-scaled by 2^(kE - pos(i%4))
+  float x[4][8];    // [a][i], pre-scaled by 2^(kE - pos(i%4))
   float sx32[4];    // 32 * sum_i x[a][i] * 2^-60 (the -32 offset, in product units)
-  uint32_t off, oA, oB, oQ;
-  uint32_t j;       // column group within the half
-  bool sh8;         // half h = 1: scales 8..15
+  uint32_t off, oA, oB, oQ, oS;
+  uint32_t sshift;  // bit offset of sc[8h + jj/2] inside the 8-byte scale window
 
-  // Column 256kb + 128h + 32a + 16j + i belongs to unit 4kb + 2h + j with
-  // unit-local index l = 16a + i.
+  // Column 256kb + 128h + 32a + 8jj + i belongs to unit 8kb + 4h + jj with
+  // unit-local index l = 8a + i.
   __device__ __forceinline__ static void unit_of(int64_t col, int& u, int& l) {
     const int kb = static_cast<int>(col >> 8), r = static_cast<int>(col & 255);
-    const int h = r >> 7, a = (r >> 5) & 3, j = (r >> 4) & 1, i = r & 15;
-    u = 4 * kb + 2 * h + j;
-    l = 16 * a + i;
+    const int h = r >> 7, a = (r >> 5) & 3, jj = (r >> 3) & 3, i = r & 7;
+    u = 8 * kb + 4 * h + jj;
+    l = 8 * a + i;
   }
 
   template <class XU>
   __device__ __forceinline__ void setup(int u, const XU& xu) {
-    const int kb = u >> 2, h = (u >> 1) & 1, j = u & 1;
+    const int kb = u >> 3, h = (u >> 2) & 1, jj = u & 3;
     off = static_cast<uint32_t>(kb) * kBlockBytes;
-    oA = 64u * h + 16u * j;
-    oB = 64u * h + 32u + 16u * j;
-    oQ = 128u + 32u * h + 16u * j;
-    this->j = static_cast<uint32_t>(j);
-    sh8 = h != 0;
+    oA = 64u * h + 8u * jj;
+    oB = 64u * h + 32u + 8u * jj;
+    oQ = 128u + 32u * h + 8u * jj;
+    oS = 192u + 8u * h;            // the 8 scales of half h
+    sshift = 8u * static_cast<uint32_t>(jj >> 1);
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
       float s = 0.f;
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const float v = xu(16 * a + i);
+      for (int i = 0; i < 8; ++i) {
+        const float v = xu(8 * a + i);
         s += v;
         const int pos = (i & 3) == 0 ? 0 : (i & 3) == 1 ? 8 : 16;
         x[a][i] = v * exp2i(kE - pos);
@@ -214,16 +217,16 @@ struct UnitQ6K {
   }
 
   struct Frag {
-    uint32_t WA[4], WB[4], H[4], SC[4];
+    uint32_t A0, A1, B0, B1, Q0, Q1, S0, S1;
     uint32_t dbits;
   };
 
   __device__ __forceinline__ void load(const uint8_t* rp, Frag& f) const {
     const uint8_t* bp = rp + off;
-    load16_a2(bp + oA, f.WA);
-    load16_a2(bp + oB, f.WB);
-    load16_a2(bp + oQ, f.H);
-    load16_a2(bp + 192, f.SC);  // the 16 int8 scales
+    load8_a2(bp + oA, f.A0, f.A1);
+    load8_a2(bp + oB, f.B0, f.B1);
+    load8_a2(bp + oQ, f.Q0, f.Q1);
+    load8_a2(bp + oS, f.S0, f.S1);
     const uintptr_t da = reinterpret_cast<uintptr_t>(bp + 208);
     const uint32_t dw = *reinterpret_cast<const uint32_t*>(da & ~uintptr_t(3));
     f.dbits = dw >> ((da & 3u) * 8u);
@@ -235,9 +238,10 @@ struct UnitQ6K {
 #pragma unroll
     for (int a = 0; a < 4; ++a) p[a][0] = p[a][1] = 0.f;
     constexpr uint32_t M = 0x0F0F0F0Fu;
+    const uint32_t WA[2] = {f.A0, f.A1}, WB[2] = {f.B0, f.B1}, H[2] = {f.Q0, f.Q1};
 #pragma unroll
-    for (int t = 0; t < 4; ++t) {
-      const uint32_t wa = f.WA[t], wb = f.WB[t], hh = f.H[t];
+    for (int t = 0; t < 2; ++t) {
+      const uint32_t wa = WA[t], wb = WB[t], hh = H[t];
       // 6-bit quants of four consecutive columns, one per byte (bits 6,7 of
       // each byte are don't-care; the extraction masks drop them)
       const uint32_t v0 = (wa & M) | ((hh << 4) & ~M);
@@ -253,15 +257,12 @@ struct UnitQ6K {
              x[a][4 * t + 3]);
       }
     }
-    // scale of weights 128h + 32a + 16j + i is sc[(128h + 32a + 16j) / 16] = sc[8h + 2a + j]:
-    // byte j + 2a of the 8 scale bytes of half h
-    const uint32_t s_lo = sh8 ? f.SC[2] : f.SC[0];
-    const uint32_t s_hi = sh8 ? f.SC[3] : f.SC[1];
+    // scale of group a: byte 2a + jj/2 of the 8 scale bytes of half h
     float acc = 0.f;
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
-      const uint32_t wsc = a < 2 ? s_lo : s_hi;
-      const uint32_t shift = 8u * (j + 2u * (a & 1));
+      const uint32_t wsc = a < 2 ? f.S0 : f.S1;
+      const uint32_t shift = 16u * (a & 1) + sshift;
       const int sc = static_cast<int>(static_cast<int8_t>((wsc >> shift) & 0xFFu));
       acc = fmaf(static_cast<float>(sc), (p[a][0] + p[a][1]) - sx32[a], acc);
     }
@@ -284,6 +285,7 @@ struct UnitQ6K {
 // ---------------------------------------------------------------------------
 struct UnitQ40 {
   static constexpr int kFmt = 2;
+  static constexpr int kUnitW = 64;
   static constexpr int kBlockW = 32;
   static constexpr int kBlockBytes = 18;
   float e0[4];               // qs0[0..1] via w0 >> 12: lo0 hi0 lo1 hi1 (pos 4, 8, 12, 16)

@@ -39,13 +39,14 @@ struct TilePlan {
 inline bool plan_tiles(int fmt, int epi, int64_t K, int B, int64_t rows_hint, int sms,
                        uint32_t tile_target, TilePlan& tp, std::string& why) {
   const int64_t RB = row_bytes_of(fmt, K);
-  if (K % kUnitWeights) {
-    why = "hidden is not a multiple of 64";
+  const int uw = unit_weights(fmt);
+  if (K % uw) {
+    why = "hidden is not a multiple of the lane unit";
     return false;
   }
-  const int64_t U = K / kUnitWeights;
+  const int64_t U = K / uw;
   if (U > kMaxConsumers) {
-    why = "more than 320 lane units per row (hidden > 20480 in one pass)";
+    why = "more than 320 lane units per row (hidden too large for one pass)";
     return false;
   }
   const int64_t gmax = kMaxConsumers / (U * B);

@@ -198,7 +198,7 @@ cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uin
   p.y_slice_off = static_cast<int64_t>(B) * segs[0].rows;
   p.stage_bytes = round_up(tp.stage_need + 16, 128);
   p.red_floats = tp.red_floats;
-  p.xs_floats = static_cast<uint32_t>(kUnitWeights * red_stride(tp.U));
+  p.xs_floats = static_cast<uint32_t>(unit_weights(fmt) * red_stride(tp.U));
   // ring: as deep as the shared-memory budget allows (one CTA per SM), 2..16
   p.S = 16;
   while (p.S > 2 && ring_smem_bytes(p.S, p.stage_bytes, p.red_floats, p.xs_floats) > kSmemBudget)
