@@ -56,13 +56,14 @@ constexpr int64_t kMaxHidden = 20480;  // 320 lane units of 64 columns
 
 size_t round256(size_t v) { return (v + 255) / 256 * 256; }
 
-// Split count the library picks: 1 unless batch * (hidden/S)/64 must shrink
-// to fit the 320 consumer lanes.
-int auto_splits(int64_t hidden, int batch) {
+// Split count the library picks: 1 unless batch * lane units per row
+// (hidden / S / unit width) must shrink to fit the 320 consumer lanes.
+int auto_splits(int fmt, int64_t hidden, int batch) {
   const int64_t nb = hidden / 256;
+  const int64_t uw = qws::unit_weights(fmt);
   for (int64_t s = 1; s <= nb; ++s) {
     if (nb % s) continue;
-    if ((hidden / s / 64) * batch <= 320) return static_cast<int>(s);
+    if ((hidden / s / uw) * batch <= 320) return static_cast<int>(s);
   }
   return -1;
 }
@@ -89,7 +90,7 @@ qws_status run_matvec(const char* fn, int fmt, const void* W, const float* x, fl
   qws_status rc = check_matvec(fn, fmt, W, x, y, rows, hidden, batch);
   if (rc != QWS_OK) return rc;
   if (split_k < 0) return fail(QWS_ERR_SHAPE, "%s: split_k = %d < 0", fn, split_k);
-  int S = split_k == 0 ? auto_splits(hidden, batch) : split_k;
+  int S = split_k == 0 ? auto_splits(fmt, hidden, batch) : split_k;
   if (S < 1)
     return fail(QWS_ERR_SHAPE, "%s: batch %d too large for hidden %lld", fn, batch,
                 (long long)hidden);
@@ -100,9 +101,11 @@ qws_status run_matvec(const char* fn, int fmt, const void* W, const float* x, fl
   if (Ks > kMaxHidden)
     return fail(QWS_ERR_SHAPE, "%s: hidden / split_k = %lld above %lld; use split_k", fn,
                 (long long)Ks, (long long)kMaxHidden);
-  if ((Ks / 64) * batch > 320)
-    return fail(QWS_ERR_SHAPE, "%s: batch * hidden / split_k / 64 = %lld above 320", fn,
-                (long long)((Ks / 64) * batch));
+  const int64_t lanes = (Ks / qws::unit_weights(fmt)) * batch;
+  if (lanes > 320)
+    return fail(QWS_ERR_SHAPE,
+                "%s: batch * lane units per row = %lld above 320 (use split_k, or a smaller batch)",
+                fn, (long long)lanes);
   if (S > 1) {
     if (qws::row_bytes_of(fmt, hidden) % 16 || qws::row_bytes_of(fmt, Ks) % 16)
       return fail(QWS_ERR_SHAPE, "%s: split rows are not 16-byte multiples for this format", fn);
@@ -125,6 +128,8 @@ qws_status run_matvec(const char* fn, int fmt, const void* W, const float* x, fl
 }
 
 }  // namespace
+
+void qws::set_last_error(const char* msg) { tl_error = msg ? msg : ""; }
 
 extern "C" {
 
@@ -284,7 +289,7 @@ size_t qws_workspace_bytes(qws_op op, int64_t rows, int64_t hidden, int64_t inte
   switch (op) {
     case QWS_OP_MATVEC: {
       if (rows <= 0 || hidden <= 0 || batch < 1) return 0;
-      const int S = split_k == 0 ? auto_splits(hidden, batch) : split_k;
+      const int S = split_k == 0 ? auto_splits(QWS_Q4_K, hidden, batch) : split_k;
       if (S <= 1) return 0;
       return round256(sizeof(float) * static_cast<size_t>(S) * batch * rows);
     }

@@ -103,6 +103,9 @@ cudaError_t launch_rms_norm(const float* x, const float* w, float* y, int64_t n,
 cudaError_t launch_residual_add(float* h, const float* y, int64_t n, int batch, cudaStream_t st);
 unsigned read_clear_matvec_errors();
 
+// message returned by qws_last_error() on the calling thread (abi.cu)
+void set_last_error(const char* msg);
+
 // decode chain (chain.cu)
 size_t chain_workspace_bytes(int64_t hidden, int64_t inter);
 unsigned read_clear_chain_errors();

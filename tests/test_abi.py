@@ -69,6 +69,12 @@ def test_matvec_shapes(lib):
     assert "320" in _err(lib)
 
 
+def test_q6k_lane_limit(lib):
+    # Q6_K lanes own 32 columns: batch 8 x 2560 columns needs 640 lanes, and a
+    # column split of a 10-block Q6_K row is not 16-byte aligned
+    assert lib.qws_q6k_matvec(A, A, A, 10, 2560, 8, None) == SHAPE
+
+
 def test_matvec_alignment(lib):
     assert lib.qws_q4k_matvec(A + 8, A, A, 10, 256, 1, None) == ALIGN
     assert lib.qws_q4k_matvec(A, A + 2, A, 10, 256, 1, None) == ALIGN
