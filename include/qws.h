@@ -141,6 +141,31 @@ qws_status qws_q4k_ffn_gate_up_geglu(const void* Wg, const void* Wu, const float
                                      int64_t hidden, int64_t inter, qws_stream stream);
 
 /* ------------------------------------------------------------------------
+ * The gated FFN above for callers that cannot allocate device memory.  The
+ * pages have no counterpart; this is a convenience of this library.  It is for
+ * callers that may not allocate at call time and have no spare device buffer
+ * to lend as workspace (for example a serving runtime whose device memory pool
+ * is fixed at start-up, or a plugin whose host forbids device allocations
+ * outside its own allocator).  The intermediate m lives in a fixed array
+ * inside the library: every device that loads the library holds
+ * QWS_FFN_NOALLOC_MAX_INTER floats (80 KiB) of it until the process exits.
+ *   Arguments, layouts and results as qws_q4k_ffn_gate_up_geglu_down, without
+ *   ws / ws_bytes; inter <= QWS_FFN_NOALLOC_MAX_INTER, else QWS_ERR_SHAPE.
+ *   Allocates nothing: no cudaMalloc / cudaFree and no allocating library call.
+ *   The first call on a device looks up the array's device address (once per
+ *   device, with that device current); make that first call before any stream
+ *   capture.  Every call on a device shares the one array, and m is rewritten
+ *   from scratch by each call; calls that overlap on the GPU (streams with no
+ *   ordering between them) race on it and must be serialised by the caller.
+ * ---------------------------------------------------------------------- */
+#define QWS_FFN_NOALLOC_MAX_INTER 20480
+
+qws_status qws_q4k_ffn_gate_up_geglu_down_noalloc(const void* Wg, const void* Wu, const void* Wd,
+                                                  qws_format wd_fmt, const float* x, float* y,
+                                                  int64_t hidden, int64_t inter,
+                                                  qws_stream stream);
+
+/* ------------------------------------------------------------------------
  * rms_norm (infer-compute README §Shaders "Normalization"):
  *   y[b][i] = x[b][i] / sqrt(mean_j x[b][j]^2 + eps) * w[i]
  * x, y [batch][n], w [n] f32 (device); y may equal x.  n > 0, batch >= 1.
