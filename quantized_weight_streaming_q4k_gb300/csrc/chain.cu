@@ -10,15 +10,25 @@
 //                                       h1 = h + rms_norm(o, w_post_attn)  (or h + o)
 //   DOWN  : f = W_d m
 // and the next layer's input is h = h1 + rms_norm(f, w_post_ffn) (or h1 + f).
-// A phase's input vector depends on every output of the previous phase, so
-// the grid meets at a barrier between phases; the producer warp does not:
-// weights never depend on activations, so it keeps streaming the next phase's
-// tiles into the ring while the grid waits.
 //
-// Per CTA, the consumers rebuild the phase's input vector themselves from the
-// (L2-resident) previous outputs -- each needs only a few KB -- with sums of
-// squares reduced in a fixed order, so every CTA computes bit-identical
-// vectors; CTA 0 also stores h and h1 for the residual adds.
+// Synchronisation without grid barriers.  A phase's input depends on every
+// output of the previous phase.  Every output element is stored as one 64-bit
+// word {value, stamp}, stamp = 1 + the index of the phase that wrote it, and a
+// CTA starting phase p loads the words it needs until their stamps say they
+// come from phase p-1 (bounded polling): the data and the "it is ready" signal
+// arrive in the same round trip.  The producer warp never waits for
+// activations: weights do not depend on them, so it keeps streaming the next
+// phases' tiles into the ring.
+//
+// Write-after-read: before overwriting a buffer, a writer checks (one load,
+// normally already satisfied) that every CTA has finished the phase prologue
+// that last read the old contents; each CTA bumps a counter after each
+// prologue.  The vectors h and h1 that CTA 0 stores alternate between two
+// buffers by layer parity, so that check does not wait in practice.
+//
+// Every CTA rebuilds a phase's input vector itself from the (L2-resident)
+// previous outputs; sums of squares are reduced in a fixed order, so every CTA
+// computes bit-identical vectors.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -34,7 +44,7 @@ __device__ unsigned g_err_chain;
 
 constexpr int kMaxLayers = 64;
 constexpr uint32_t kChainTileTarget = 23 * 1024;  // deeper ring, finer balance across CTAs
-constexpr int kChainBar = 2;  // named barrier: reducer + consumers at phase starts
+constexpr int64_t kMaxChainHidden = 16 * kMaxConsumers;  // residual vectors: 16 per thread
 
 enum : int { PH_QKV = 0, PH_O = 1, PH_GU = 2, PH_DOWN = 3 };
 
@@ -48,6 +58,8 @@ struct KindPlan {
   int64_t K, row_bytes;
 };
 
+using Word = unsigned long long;  // {value bits, stamp << 32}
+
 struct ChainParams {
   ChainLayer L[kMaxLayers];
   int n_layers;
@@ -56,14 +68,43 @@ struct ChainParams {
   float eps;
   int post_norms;
   KindPlan kp[4];
-  // workspace vectors (device)
-  float *q, *k, *v, *o, *m, *f, *hin, *h1;
-  unsigned* counter;          // grid barrier arrivals (zeroed before launch)
-  float* h;                   // user's h (in: layer 0 input, out: chain output)
+  // stamped workspace vectors (device); hin and h1 hold two buffers of H each
+  Word *q, *k, *v, *o, *m, *f, *hin, *h1;
+  unsigned* prologues;        // [4 * n_layers]: CTAs done with each phase's prologue (zeroed per launch)
+  float* h;                   // the caller's h (in: layer 0 input, out: chain output)
   uint32_t S, stage_bytes, red_floats, xs_floats;
 };
 
-// Phase p = 4 * layer + kind.
+__device__ __forceinline__ Word ld_word(const Word* p) {
+  Word w;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(w) : "l"(p) : "memory");
+  return w;
+}
+__device__ __forceinline__ void st_word(Word* p, float v, unsigned stamp) {
+  const Word w = static_cast<Word>(__float_as_uint(v)) | (static_cast<Word>(stamp) << 32);
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+__device__ __forceinline__ unsigned stamp_of(Word w) { return static_cast<unsigned>(w >> 32); }
+__device__ __forceinline__ float value_of(Word w) {
+  return __uint_as_float(static_cast<unsigned>(w & 0xFFFFFFFFu));
+}
+
+// Waits (bounded) until every CTA has finished the prologue of phase ph.
+__device__ __forceinline__ bool wait_prologues(const ChainParams& p, int ph) {
+  if (ph < 0) return true;
+  const unsigned* c = p.prologues + ph;
+  if (ld_acquire_gpu(c) >= gridDim.x) return true;
+  const long long t0 = clock64();
+  while (ld_acquire_gpu(c) < gridDim.x) {
+    if (clock64() - t0 > kWaitCycles) {
+      atomicOr(&g_err_chain, kErrGridBarrier);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Phase p = 4 * layer + kind; its outputs carry stamp p + 1.
 struct ChainPhases {
   const ChainParams* p;
   __device__ __forceinline__ int count() const { return 4 * p->n_layers; }
@@ -85,22 +126,47 @@ struct ChainPhases {
     P.cta0 = 0;
     P.ncta = static_cast<int>(gridDim.x);
     P.nseg = 1;
+    // a segment's y names its stamped destination (Word*), which only the
+    // chain's epilogue uses
+    auto dst = [](Word* w) { return reinterpret_cast<float*>(w); };
     for (int i = 0; i < kMaxSeg; ++i) P.seg[i] = Seg{nullptr, nullptr, 0, 0};
     if (kind == PH_QKV) {
       P.nseg = 3;
-      P.seg[0] = Seg{L.Wq, p->q, p->QD, static_cast<int>((p->QD + kp.T - 1) / kp.T)};
-      P.seg[1] = Seg{L.Wk, p->k, p->KD, static_cast<int>((p->KD + kp.T - 1) / kp.T)};
-      P.seg[2] = Seg{L.Wv, p->v, p->KD, static_cast<int>((p->KD + kp.T - 1) / kp.T)};
+      P.seg[0] = Seg{L.Wq, dst(p->q), p->QD, static_cast<int>((p->QD + kp.T - 1) / kp.T)};
+      P.seg[1] = Seg{L.Wk, dst(p->k), p->KD, static_cast<int>((p->KD + kp.T - 1) / kp.T)};
+      P.seg[2] = Seg{L.Wv, dst(p->v), p->KD, static_cast<int>((p->KD + kp.T - 1) / kp.T)};
     } else if (kind == PH_O) {
-      P.seg[0] = Seg{L.Wo, p->o, p->H, static_cast<int>((p->H + kp.T - 1) / kp.T)};
+      P.seg[0] = Seg{L.Wo, dst(p->o), p->H, static_cast<int>((p->H + kp.T - 1) / kp.T)};
     } else if (kind == PH_GU) {
-      P.seg[0] = Seg{L.Wg, p->m, p->I, static_cast<int>((p->I + kp.T - 1) / kp.T)};
+      P.seg[0] = Seg{L.Wg, dst(p->m), p->I, static_cast<int>((p->I + kp.T - 1) / kp.T)};
       P.W2 = L.Wu;
     } else {
-      P.seg[0] = Seg{L.Wd, p->f, p->H, static_cast<int>((p->H + kp.T - 1) / kp.T)};
+      P.seg[0] = Seg{L.Wd, dst(p->f), p->H, static_cast<int>((p->H + kp.T - 1) / kp.T)};
     }
     P.n_tiles = P.seg[0].tiles + P.seg[1].tiles + P.seg[2].tiles;
     return P;
+  }
+};
+
+// Reducer epilogue: stores each reduced row (GEGLU for the gate/up pair) as a
+// stamped word in the segment's destination (q / k / v, o, m or f).  Before the first store of
+// a phase ph it makes sure that every CTA has finished the prologue that last
+// read the buffer's old contents: phase ph - 3 (v by O, o by GU, m by DOWN, f by
+// the next QKV -- each three phases later than its writer).
+struct EpiStamped {
+  const ChainParams* p;
+  int ph;
+  mutable bool checked;
+  mutable bool ok;
+  __device__ __forceinline__ void operator()(const Phase& P, const TileRef& tr, int, int o, float v,
+                                             float v2) const {
+    if (!checked) {
+      ok = wait_prologues(*p, ph - 3);
+      checked = true;
+    }
+    Word* dst = reinterpret_cast<Word*>(tr.y);
+    const float val = (ph & 3) == PH_GU ? gelu_tanh(v) * v2 : v;
+    st_word(dst + tr.r0 + o, val, static_cast<unsigned>(ph + 1));
   }
 };
 
@@ -117,175 +183,370 @@ __device__ __forceinline__ float block_sum(float v, float* wsum, int ctid, int C
   return t;
 }
 
-// 1 / sqrt(mean(v^2) + eps) over n values read through ld_cg (other CTAs'
-// outputs), identical in every CTA.  Loads go out 8 at a time.
-__device__ __forceinline__ float inv_rms_global(const float* v, int64_t n, float eps,
-                                                float* wsum, int ctid, int C) {
-  constexpr int kChunk = 8;
-  float ss = 0.f;
-  for (int64_t base = ctid; base < n; base += static_cast<int64_t>(kChunk) * C) {
-    float t[kChunk];
+constexpr int kC = kMaxConsumers;   // the chain always runs this many consumer threads
+
+// Polls the words b[j * kC] (j < kJ, b + j * kC < end) until each carries stamp
+// `want` and hands each value to put(j, value) as it arrives.  The first round
+// issues every load at once, so a vector costs one L2 round trip when it is
+// ready.  Bounded: returns false (error bit set) on timeout.
+template <int kJ, class Put>
+__device__ __forceinline__ bool poll_stamped(const Word* b, const Word* end, unsigned want,
+                                             Put&& put) {
+  unsigned pending = 0;
 #pragma unroll
-    for (int j = 0; j < kChunk; ++j) {
-      const int64_t i = base + static_cast<int64_t>(j) * C;
-      t[j] = i < n ? ld_cg(v + i) : 0.f;
+  for (int j = 0; j < kJ; ++j)
+    if (b + j * kC < end) pending |= 1u << j;
+  long long t0 = 0;
+  bool first = true;
+  while (pending) {
+    Word w[kJ];
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) w[j] = (pending >> j & 1u) ? ld_word(b + j * kC) : 0ull;
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      if ((pending >> j & 1u) && stamp_of(w[j]) == want) {
+        put(j, value_of(w[j]));
+        pending &= ~(1u << j);
+      }
     }
-#pragma unroll
-    for (int j = 0; j < kChunk; ++j) ss = fmaf(t[j], t[j], ss);
+    if (!pending) break;
+    if (first) {
+      t0 = clock64();
+      first = false;
+    } else if (clock64() - t0 > kWaitCycles) {
+      atomicOr(&g_err_chain, kErrFullWait);
+      return false;
+    }
   }
-  ss = block_sum(ss, wsum, ctid, C);
-  return 1.0f / sqrtf(ss / static_cast<float>(n) + eps);
+  return true;
 }
 
-struct VecSrc {  // shared-memory vector
-  const float* p;
-  __device__ __forceinline__ float operator()(int64_t i) const { return p[i]; }
-};
-
-struct NormSrc {  // vec[i] * inv * w[i]
-  const float* vec;
-  const float* w;
-  float inv;
-  __device__ __forceinline__ float operator()(int64_t i) const {
-    return __fmul_rn(__fmul_rn(vec[i], inv), w[i]);
-  }
-};
-
-struct GatherSrc {  // attention at seq 1: query head i / hd reads kv head (i / hd) / group
-  const float* v;
-  int hd, group;
-  __device__ __forceinline__ float operator()(int64_t i) const {
-    const int head = static_cast<int>(i / hd);
-    return ld_cg(v + static_cast<int64_t>(head / group) * hd + (i - static_cast<int64_t>(head) * hd));
-  }
-};
-
-// vec[i] = base[i] + (post ? add[i] * inv * w[i] : add[i]); CTA 0 also stores
-// it to global `store` (if non-null).  base and add may be written by other
-// CTAs (read with ld_cg).  Loads go out 8 elements at a time.
-__device__ __forceinline__ void residual_into(float* vec, const float* base, const float* add,
-                                              const float* w, float inv, bool post,
-                                              float* store, int64_t n, int ctid, int C) {
-  constexpr int kChunk = 8;
-  for (int64_t b0 = ctid; b0 < n; b0 += static_cast<int64_t>(kChunk) * C) {
-    float a[kChunk], h[kChunk], ww[kChunk];
+// r = base + (post ? add * rms_inv(add) * wa : add)      (r = base when add == null)
+// x = r * rms_inv(r) * wn  -> staged for Q4_K lane units (transposed)
+// Element ctid + j * kC of each vector lives in thread ctid's registers
+// (H <= kJ * kC).  When store != null (CTA 0) r is also stored as stamped
+// words, after the write-after-read check against phase store_war.  `base` is
+// the caller's plain h when base_plain != null (layer 0), else a stamped
+// vector.  kEarlyW: load the norm weights together with the vectors (one round
+// trip; more registers).
+template <int kJ, bool kEarlyW>
+__device__ __forceinline__ bool resnorm_stage(const ChainParams& p, const Ring& R, float* wsum,
+                                              const Word* base, unsigned base_stamp,
+                                              const float* base_plain, const Word* add,
+                                              unsigned add_stamp, const float* wa,
+                                              const float* wn, Word* store, unsigned store_stamp,
+                                              int store_war, int US, int ctid) {
+  const int64_t H = p.H;
+  const bool post = p.post_norms != 0;
+  float bs[kJ], ad[kJ], wwa[kJ], wwn[kJ];
+  if constexpr (kEarlyW) {
 #pragma unroll
-    for (int j = 0; j < kChunk; ++j) {
-      const int64_t i = b0 + static_cast<int64_t>(j) * C;
-      const bool in = i < n;
-      a[j] = in ? ld_cg(add + i) : 0.f;
-      h[j] = in ? ld_cg(base + i) : 0.f;
-      ww[j] = (in && post) ? w[i] : 0.f;
+    for (int j = 0; j < kJ; ++j) {
+      const int64_t i = ctid + static_cast<int64_t>(j) * kC;
+      wwa[j] = (i < H && add && post) ? wa[i] : 0.f;
+      wwn[j] = i < H ? wn[i] : 0.f;
     }
+  }
 #pragma unroll
-    for (int j = 0; j < kChunk; ++j) {
-      const int64_t i = b0 + static_cast<int64_t>(j) * C;
+  for (int j = 0; j < kJ; ++j) {
+    const int64_t i = ctid + static_cast<int64_t>(j) * kC;
+    bs[j] = (i < H && base_plain) ? base_plain[i] : 0.f;
+    ad[j] = 0.f;
+  }
+  bool ok = true;
+  if (!base_plain)
+    ok = poll_stamped<kJ>(base + ctid, base + H, base_stamp, [&](int j, float v) { bs[j] = v; });
+  if (add)
+    ok = poll_stamped<kJ>(add + ctid, add + H, add_stamp, [&](int j, float v) { ad[j] = v; }) && ok;
+  if constexpr (!kEarlyW) {
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int64_t i = ctid + static_cast<int64_t>(j) * kC;
+      wwa[j] = (i < H && add && post) ? wa[i] : 0.f;
+      wwn[j] = i < H ? wn[i] : 0.f;
+    }
+  }
+  float inv1 = 1.f;
+  if (add && post) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) ss = fmaf(ad[j], ad[j], ss);
+    inv1 = 1.0f / sqrtf(block_sum(ss, wsum, ctid, kC) / static_cast<float>(H) + p.eps);
+  }
+  float ss2 = 0.f;
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    // explicit roundings: every CTA computes the same r
+    float r = bs[j];
+    if (add) r = __fadd_rn(bs[j], post ? __fmul_rn(__fmul_rn(ad[j], inv1), wwa[j]) : ad[j]);
+    bs[j] = r;
+    ss2 = fmaf(r, r, ss2);
+  }
+  if (store) {
+    if (!wait_prologues(p, store_war)) ok = false;
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int64_t i = ctid + static_cast<int64_t>(j) * kC;
+      if (i < H) st_word(store + i, bs[j], store_stamp);
+    }
+  }
+  const float inv2 = 1.0f / sqrtf(block_sum(ss2, wsum, ctid, kC) / static_cast<float>(H) + p.eps);
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    const int64_t i = ctid + static_cast<int64_t>(j) * kC;
+    if (i < H) {
+      int u, l;
+      UnitQ4K::unit_of(i, u, l);
+      R.xs[l * US + u] = __fmul_rn(__fmul_rn(bs[j], inv2), wwn[j]);
+    }
+  }
+  return ok;
+}
+
+// Stages a stamped vector of n values for the lane units of Unit, kJ values per
+// thread per round trip.
+template <class Unit, int kJ>
+__device__ __forceinline__ bool stage_stamped(const Ring& R, int US, const Word* src,
+                                              unsigned want, int64_t n, int ctid) {
+  bool ok = true;
+  for (int64_t b0 = ctid; b0 < n; b0 += static_cast<int64_t>(kJ) * kC) {
+    ok = poll_stamped<kJ>(src + b0, src + n, want,
+                          [&](int j, float v) {
+                            int u, l;
+                            Unit::unit_of(b0 + static_cast<int64_t>(j) * kC, u, l);
+                            R.xs[l * US + u] = v;
+                          }) &&
+         ok;
+  }
+  return ok;
+}
+
+// Stages the seq-1 attention output for the O projection: query head i / hd
+// takes kv head (i / hd) / group, i.e. column i reads v[(head / group) * hd + i % hd].
+template <int kJ>
+__device__ __forceinline__ bool stage_gather(const Ring& R, int US, const Word* v, unsigned want,
+                                             int64_t n, int hd, int group, int ctid) {
+  bool ok = true;
+  for (int64_t b0 = ctid; b0 < n; b0 += static_cast<int64_t>(kJ) * kC) {
+    unsigned pending = 0;
+    const Word* at[kJ];
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int64_t i = b0 + static_cast<int64_t>(j) * kC;
+      at[j] = v;
       if (i < n) {
-        // explicit roundings: the same value must come out of every call site
-        const float r = __fadd_rn(h[j], post ? __fmul_rn(__fmul_rn(a[j], inv), ww[j]) : a[j]);
-        vec[i] = r;
-        if (store) store[i] = r;
+        const int64_t head = i / hd;
+        at[j] = v + (head / group) * hd + (i - head * hd);
+        pending |= 1u << j;
+      }
+    }
+    long long t0 = 0;
+    bool first = true;
+    while (pending) {
+      Word w[kJ];
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) w[j] = (pending >> j & 1u) ? ld_word(at[j]) : 0ull;
+#pragma unroll
+      for (int j = 0; j < kJ; ++j) {
+        if ((pending >> j & 1u) && stamp_of(w[j]) == want) {
+          int u, l;
+          UnitQ4K::unit_of(b0 + static_cast<int64_t>(j) * kC, u, l);
+          R.xs[l * US + u] = value_of(w[j]);
+          pending &= ~(1u << j);
+        }
+      }
+      if (!pending) break;
+      if (first) {
+        t0 = clock64();
+        first = false;
+      } else if (clock64() - t0 > kWaitCycles) {
+        atomicOr(&g_err_chain, kErrFullWait);
+        ok = false;
+        break;
       }
     }
   }
+  return ok;
 }
 
-// vec[i] = src[i] (and store[i] = src[i] if store), loads 8 at a time.
-__device__ __forceinline__ void copy_into(float* vec, const float* src, float* store, int64_t n,
-                                          int ctid, int C) {
-  constexpr int kChunk = 8;
-  for (int64_t b0 = ctid; b0 < n; b0 += static_cast<int64_t>(kChunk) * C) {
-    float t[kChunk];
-#pragma unroll
-    for (int j = 0; j < kChunk; ++j) {
-      const int64_t i = b0 + static_cast<int64_t>(j) * C;
-      t[j] = i < n ? ld_cg(src + i) : 0.f;
+// Builds the input vector of phase ph into R.xs, then counts this CTA's
+// prologue as finished.  Out of line: it runs once per phase and must not take
+// registers from the decode loop.
+__device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const Ring& R,
+                                            float* wsum, bool q6, int ctid, int C) {
+  const int l = ph >> 2, kind = ph & 3;
+  const ChainLayer& L = p.L[l];
+  const KindPlan& kp = p.kp[kind];
+  const int US = red_stride(kp.U);
+  const unsigned prev = static_cast<unsigned>(ph);   // stamp of the previous phase's outputs
+  const bool wide = p.H > 8 * static_cast<int64_t>(C);
+  bool ok = true;
+  // every consumer thread of this CTA is done with R.xs of the previous phase
+  bar_sync(kConsumerBar, C);
+  if (kind == PH_QKV || kind == PH_GU) {
+    const Word* base;
+    const float* base_plain = nullptr;
+    const Word* add = nullptr;
+    const float *wa = nullptr, *wn;
+    unsigned base_stamp = 0, add_stamp = prev;
+    Word* store;
+    int war;
+    if (kind == PH_QKV) {
+      // h = layer input: the caller's h, or h1 + norm(f) of the previous layer;
+      // CTA 0 keeps it in hin[l & 1] for the GU residual
+      base = l ? p.h1 + ((l - 1) & 1) * p.H : nullptr;
+      base_stamp = static_cast<unsigned>(4 * l - 1);
+      base_plain = l ? nullptr : p.h;
+      add = l ? p.f : nullptr;
+      wa = l ? p.L[l - 1].w_pff : nullptr;
+      wn = L.w_in;
+      store = blockIdx.x == 0 ? p.hin + (l & 1) * p.H : nullptr;
+      war = 4 * l - 6;   // GU(l - 2) read hin[l & 1] last
+    } else {
+      // h1 = h + rms_norm(o, w_post_attn) (or h + o); CTA 0 keeps it in h1[l & 1]
+      base = p.hin + (l & 1) * p.H;
+      base_stamp = static_cast<unsigned>(4 * l + 1);
+      add = p.o;
+      wa = L.w_pa;
+      wn = L.w_pf;
+      store = blockIdx.x == 0 ? p.h1 + (l & 1) * p.H : nullptr;
+      war = 4 * l - 4;   // QKV(l - 1) read h1[l & 1] last
     }
-#pragma unroll
-    for (int j = 0; j < kChunk; ++j) {
-      const int64_t i = b0 + static_cast<int64_t>(j) * C;
-      if (i < n) {
-        vec[i] = t[j];
-        if (store) store[i] = t[j];
-      }
-    }
+    ok = wide ? resnorm_stage<16, false>(p, R, wsum, base, base_stamp, base_plain, add, add_stamp,
+                                         wa, wn, store, static_cast<unsigned>(ph + 1), war, US,
+                                         ctid)
+              : resnorm_stage<8, true>(p, R, wsum, base, base_stamp, base_plain, add, add_stamp,
+                                       wa, wn, store, static_cast<unsigned>(ph + 1), war, US,
+                                       ctid);
+  } else if (kind == PH_O) {
+    ok = stage_gather<8>(R, US, p.v, prev, kp.K, p.head_dim, p.n_q_heads / p.n_kv_heads, ctid);
+  } else if (q6) {
+    ok = stage_stamped<UnitQ6K, 32>(R, US, p.m, prev, kp.K, ctid);
+  } else {
+    ok = stage_stamped<UnitQ4K, 32>(R, US, p.m, prev, kp.K, ctid);
   }
+  bar_sync(kConsumerBar, C);
+  // this CTA has read everything its prologue needed
+  if (ctid == 0) red_release_gpu_add(p.prologues + ph, 1u);
+  return ok;
 }
 
-// The per-format decode loops and the two reducer epilogues as separate
-// functions: each gets the whole register budget instead of sharing one
-// allocation with every other role and phase of the kernel.
-__device__ __noinline__ bool chain_consume_q4k(const Phase& P, const Ring& R, RingPos& pos,
-                                               int ctid, int C) {
-  return consume_phase<UnitQ4K, false, false>(P, R, pos, XOfPlain{nullptr, 0}, ctid, C, &g_err_chain);
-}
-__device__ __noinline__ bool chain_consume_q6k(const Phase& P, const Ring& R, RingPos& pos,
-                                               int ctid, int C) {
-  return consume_phase<UnitQ6K, false, false>(P, R, pos, XOfPlain{nullptr, 0}, ctid, C, &g_err_chain);
-}
-__device__ __forceinline__ bool chain_reduce(const Phase& P, const Ring& R, RingPos& pos) {
-  return P.epi == EPI_GEGLU ? reduce_phase(P, R, pos, EpiGeglu{}, &g_err_chain)
-                            : reduce_phase(P, R, pos, EpiStore{}, &g_err_chain);
+// Final residual on CTA 0: h = h1 + rms_norm(f, w_post_ffn) (or h1 + f).
+template <int kJ>
+__device__ __noinline__ bool chain_final(const ChainParams& p, float* wsum, int ctid, int C) {
+  const int Ll = p.n_layers - 1;
+  const bool post = p.post_norms != 0;
+  float hv[kJ], fv[kJ];
+  const Word* h1 = p.h1 + (Ll & 1) * p.H;
+  // every CTA is past its last prologue, so none still reads the caller's h
+  bool ok = wait_prologues(p, 4 * p.n_layers - 1);
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) hv[j] = fv[j] = 0.f;
+  ok = poll_stamped<kJ>(h1 + ctid, h1 + p.H, static_cast<unsigned>(4 * Ll + 3),
+                        [&](int j, float v) { hv[j] = v; }) &&
+       ok;
+  ok = poll_stamped<kJ>(p.f + ctid, p.f + p.H, static_cast<unsigned>(4 * Ll + 4),
+                        [&](int j, float v) { fv[j] = v; }) &&
+       ok;
+  float inv = 1.f;
+  if (post) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) ss = fmaf(fv[j], fv[j], ss);
+    inv = 1.0f / sqrtf(block_sum(ss, wsum, ctid, C) / static_cast<float>(p.H) + p.eps);
+  }
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    const int64_t i = ctid + static_cast<int64_t>(j) * kC;
+    if (i < p.H)
+      p.h[i] = __fadd_rn(hv[j], post ? __fmul_rn(__fmul_rn(fv[j], inv), p.L[Ll].w_pff[i]) : fv[j]);
+  }
+  return ok;
 }
 
-// Builds the input vector of phase ph into the staging buffer R.xs (all
-// consumer threads; ends with a consumer barrier).  Kept out of line: it runs
-// once per phase and must not inflate the decode loop's registers.
-__device__ __noinline__ void chain_prologue(const ChainParams& p, int ph, const Ring& R,
-                                            float* vec, float* wsum, bool q6, int ctid, int C);
+// The decode loop of every phase, out of line and fed with scalars only: it
+// rebuilds the ring from the dynamic shared-memory base, so no structure goes
+// through local memory and the loop gets a register allocation of its own
+// (UnitChain serves both formats).  Returns the new ring position (s, ph, n)
+// packed with an ok bit.
+__device__ __noinline__ unsigned long long chain_consume(
+    int fmt, int epi, int nseg, int rows0, int rows1, int rows2, int tiles0, int tiles1,
+    int tiles2, int T, int U, int G, int row_bytes, int n_tiles, unsigned S, unsigned stage_bytes,
+    unsigned red_floats, unsigned xs_floats, unsigned pos_s, unsigned pos_ph, unsigned pos_n,
+    int ctid, int C) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const Ring R = make_ring(smem, S, stage_bytes, red_floats, xs_floats);
+  Phase P;
+  P.fmt = fmt;
+  P.epi = epi;
+  P.nseg = nseg;
+  P.seg[0] = Seg{nullptr, nullptr, rows0, tiles0};
+  P.seg[1] = Seg{nullptr, nullptr, rows1, tiles1};
+  P.seg[2] = Seg{nullptr, nullptr, rows2, tiles2};
+  P.W2 = nullptr;
+  P.K = 0;
+  P.row_bytes = row_bytes;
+  P.row_stride = row_bytes;
+  P.B = 1;
+  P.U = U;
+  P.G = G;
+  P.T = T;
+  P.n_tiles = n_tiles;
+  P.cta0 = 0;
+  P.ncta = static_cast<int>(gridDim.x);
+  RingPos pos;
+  pos.s = pos_s;
+  pos.ph = pos_ph;
+  pos.n = pos_n;
+  const bool ok = consume_phase<UnitChain, false, false>(P, R, pos, XOfPlain{nullptr, 0}, ctid, C,
+                                                         &g_err_chain);
+  return static_cast<unsigned long long>(pos.s) | (static_cast<unsigned long long>(pos.ph) << 8) |
+         (static_cast<unsigned long long>(pos.n) << 16) | (ok ? (1ull << 63) : 0ull);
+}
+
+// Asks L2 to fetch n bytes at w (skipped unless 16-byte aligned and sized).
+__device__ __forceinline__ void prefetch_l2(const float* w, int64_t n) {
+  if (w && (reinterpret_cast<uintptr_t>(w) & 15) == 0 && n % 16 == 0)
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(w),
+                 "r"(static_cast<unsigned>(n))
+                 : "memory");
+}
 
 // ------------------------------------------------------------------ kernel
 __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
     chain_kernel(const __grid_constant__ ChainParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const Ring R = make_ring(smem, p.S, p.stage_bytes, p.red_floats, p.xs_floats);
-  // after the ring: [vec: H floats][wsum: 32 floats][abort flag]
-  float* vec = reinterpret_cast<float*>(smem + ring_smem_bytes(p.S, p.stage_bytes, p.red_floats,
-                                                                p.xs_floats));
-  float* wsum = vec + p.H;
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(wsum + 32);
+  float* wsum = reinterpret_cast<float*>(smem + ring_smem_bytes(p.S, p.stage_bytes, p.red_floats,
+                                                                 p.xs_floats));
   const int C = static_cast<int>(blockDim.x) - kRoleThreads;
-  if (threadIdx.x == 0) {
-    ring_init(R, C / 32);
-    *abort_flag = 0;
-  }
+  if (threadIdx.x == 0) ring_init(R, C / 32);
   __syncthreads();
   const ChainPhases phases{&p};
   const int nph = phases.count();
 
   if (threadIdx.x < kProducerThreads) {
-    if (threadIdx.x == 0) run_producer(phases, R, &g_err_chain);
+    if (threadIdx.x == 0) {
+      // warm L2 with this CTA's share of the (small, static) norm weights
+      for (int l = blockIdx.x; l < p.n_layers; l += gridDim.x) {
+        prefetch_l2(p.L[l].w_in, p.H * 4);
+        prefetch_l2(p.L[l].w_pa, p.H * 4);
+        prefetch_l2(p.L[l].w_pf, p.H * 4);
+        prefetch_l2(p.L[l].w_pff, p.H * 4);
+      }
+      run_producer(phases, R, &g_err_chain);
+    }
     return;
   }
 
   RingPos pos;
   if (threadIdx.x < kRoleThreads) {
-    // ---------------- reducer: epilogues, then the grid barrier per phase
-    const int lane = threadIdx.x & 31;
+    // ---------------- reducer: sums and stamped stores, phase after phase
     for (int ph = 0; ph < nph; ++ph) {
       const Phase P = phases.get(ph);
-      bool ok = chain_reduce(P, R, pos);
-      __syncwarp();
-      if (lane == 0) {
-        if (ok) {
-          // __syncwarp above orders the warp's epilogue stores before this
-          // lane's release; the release-add publishes them at gpu scope
-          red_release_gpu_add(p.counter, 1u);
-          const unsigned target = static_cast<unsigned>(ph + 1) * gridDim.x;
-          const long long t0 = clock64();
-          while (ld_acquire_gpu(p.counter) < target) {
-            if (clock64() - t0 > kWaitCycles) {
-              atomicOr(&g_err_chain, kErrGridBarrier);
-              ok = false;
-              break;
-            }
-          }
-        }
-        if (!ok) *abort_flag = 1;
-      }
-      __syncwarp();
-      bar_sync(kChainBar, C + 32);   // releases the consumers into the next phase
-      if (*abort_flag) return;
+      const EpiStamped epi{&p, ph, false, true};
+      const bool ok = reduce_phase(P, R, pos, epi, &g_err_chain);
+      if (!ok || !epi.ok) return;
     }
     return;
   }
@@ -294,153 +555,38 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
   const int ctid = static_cast<int>(threadIdx.x) - kRoleThreads;
   const bool down_q6k = p.kp[PH_DOWN].fmt == 14;
   for (int ph = 0; ph < nph; ++ph) {
-    if (ph > 0) {
-      bar_sync(kChainBar, C + 32);   // previous phase complete on every CTA
-      if (*abort_flag) return;
-    }
     const Phase P = phases.get(ph);
-    // the phase's input vector, staged in R.xs (transposed per lane unit)
     const bool q6 = (ph & 3) == PH_DOWN && down_q6k;
-    chain_prologue(p, ph, R, vec, wsum, q6, ctid, C);
-    const bool ok = q6 ? chain_consume_q6k(P, R, pos, ctid, C)
-                       : chain_consume_q4k(P, R, pos, ctid, C);
-    if (!ok) *abort_flag = 1;   // the reducer will time out too and abort at the next barrier
+    if (!chain_prologue(p, ph, R, wsum, q6, ctid, C)) return;
+    const unsigned long long r = chain_consume(
+        P.fmt, P.epi, P.nseg, static_cast<int>(P.seg[0].rows), static_cast<int>(P.seg[1].rows),
+        static_cast<int>(P.seg[2].rows), P.seg[0].tiles, P.seg[1].tiles, P.seg[2].tiles, P.T, P.U,
+        P.G, static_cast<int>(P.row_bytes), P.n_tiles, p.S, p.stage_bytes, p.red_floats,
+        p.xs_floats, pos.s, pos.ph, pos.n, ctid, C);
+    pos.s = static_cast<uint32_t>(r & 0xFFu);
+    pos.ph = static_cast<uint32_t>((r >> 8) & 1u);
+    pos.n = static_cast<uint32_t>((r >> 16) & 0xFFFFFFFFu);
+    if ((r >> 63) == 0) return;
   }
-  // final residual: h = h1 + rms_norm(f, w_post_ffn) (or h1 + f)
-  bar_sync(kChainBar, C + 32);
-  if (*abort_flag) return;
   if (blockIdx.x == 0) {
-    const bool post = p.post_norms != 0;
-    const ChainLayer& Lp = p.L[p.n_layers - 1];
-    const float inv_f = post ? inv_rms_global(p.f, p.H, p.eps, wsum, ctid, C) : 1.f;
-    residual_into(vec, p.h1, p.f, Lp.w_pff, inv_f, post, p.h, p.H, ctid, C);
+    if (p.H > 8 * static_cast<int64_t>(C))
+      chain_final<16>(p, wsum, ctid, C);
+    else
+      chain_final<8>(p, wsum, ctid, C);
   }
-}
-
-// r = base + (post ? add * rms_inv(add) * wa : add)      (or r = base if !add)
-// x = r * rms_inv(r) * wn                                 -> staged for Q4_K units
-// store[i] = r[i] when store != nullptr.  All global loads of a thread are
-// issued at once (one memory latency), provided H <= 8 * C.
-__device__ __forceinline__ void resnorm_stage(const ChainParams& p, const Ring& R, float* wsum,
-                                              const float* base, const float* add,
-                                              const float* wa, const float* wn, float* store,
-                                              int US, int ctid, int C) {
-  constexpr int kJ = 8;
-  const int64_t H = p.H;
-  const bool post = p.post_norms != 0;
-  float bs[kJ], ad[kJ], wwa[kJ], wwn[kJ];
-#pragma unroll
-  for (int j = 0; j < kJ; ++j) {
-    const int64_t i = ctid + static_cast<int64_t>(j) * C;
-    const bool in = i < H;
-    bs[j] = in ? ld_cg(base + i) : 0.f;
-    ad[j] = (in && add) ? ld_cg(add + i) : 0.f;
-    wwa[j] = (in && add && post) ? wa[i] : 0.f;
-    wwn[j] = in ? wn[i] : 0.f;
-  }
-  float inv1 = 1.f;
-  if (add && post) {
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < kJ; ++j) ss = fmaf(ad[j], ad[j], ss);
-    inv1 = 1.0f / sqrtf(block_sum(ss, wsum, ctid, C) / static_cast<float>(H) + p.eps);
-  }
-  float ss2 = 0.f;
-#pragma unroll
-  for (int j = 0; j < kJ; ++j) {
-    // explicit roundings: every CTA and call site computes the same r
-    float r = bs[j];
-    if (add) r = __fadd_rn(bs[j], post ? __fmul_rn(__fmul_rn(ad[j], inv1), wwa[j]) : ad[j]);
-    bs[j] = r;
-    ss2 = fmaf(r, r, ss2);
-  }
-  if (store) {
-#pragma unroll
-    for (int j = 0; j < kJ; ++j) {
-      const int64_t i = ctid + static_cast<int64_t>(j) * C;
-      if (i < H) store[i] = bs[j];
-    }
-    __threadfence();   // published to other CTAs through the phase barrier
-  }
-  const float inv2 = 1.0f / sqrtf(block_sum(ss2, wsum, ctid, C) / static_cast<float>(H) + p.eps);
-#pragma unroll
-  for (int j = 0; j < kJ; ++j) {
-    const int64_t i = ctid + static_cast<int64_t>(j) * C;
-    if (i < H) {
-      int u, l;
-      UnitQ4K::unit_of(i, u, l);
-      R.xs[l * US + u] = __fmul_rn(__fmul_rn(bs[j], inv2), wwn[j]);
-    }
-  }
-}
-
-__device__ __noinline__ void chain_prologue(const ChainParams& p, int ph, const Ring& R,
-                                            float* vec, float* wsum, bool q6, int ctid, int C) {
-  const int l = ph >> 2, kind = ph & 3;
-  const ChainLayer& L = p.L[l];
-  const int64_t H = p.H;
-  const bool post = p.post_norms != 0;
-  const KindPlan& kp = p.kp[kind];
-  const int US = red_stride(kp.U);
-  const bool fast = H <= 8 * static_cast<int64_t>(C);
-  if ((kind == PH_QKV || kind == PH_GU) && fast) {
-    if (kind == PH_QKV) {
-      if (l == 0)
-        resnorm_stage(p, R, wsum, p.h, nullptr, nullptr, L.w_in,
-                      blockIdx.x == 0 ? p.hin : nullptr, US, ctid, C);
-      else
-        resnorm_stage(p, R, wsum, p.h1, p.f, p.L[l - 1].w_pff, L.w_in,
-                      blockIdx.x == 0 ? p.hin : nullptr, US, ctid, C);
-    } else {
-      resnorm_stage(p, R, wsum, p.hin, p.o, L.w_pa, L.w_pf, blockIdx.x == 0 ? p.h1 : nullptr, US,
-                    ctid, C);
-    }
-  } else if (kind == PH_QKV || kind == PH_GU) {
-    // general sizes: several passes through shared memory
-    if (kind == PH_QKV) {
-      if (l == 0) {
-        copy_into(vec, p.h, blockIdx.x == 0 ? p.hin : nullptr, H, ctid, C);
-      } else {
-        const ChainLayer& Lp = p.L[l - 1];
-        const float inv_f = post ? inv_rms_global(p.f, H, p.eps, wsum, ctid, C) : 1.f;
-        residual_into(vec, p.h1, p.f, Lp.w_pff, inv_f, post, blockIdx.x == 0 ? p.hin : nullptr,
-                      H, ctid, C);
-      }
-    } else {
-      const float inv_o = post ? inv_rms_global(p.o, H, p.eps, wsum, ctid, C) : 1.f;
-      residual_into(vec, p.hin, p.o, L.w_pa, inv_o, post, blockIdx.x == 0 ? p.h1 : nullptr, H,
-                    ctid, C);
-    }
-    bar_sync(kConsumerBar, C);
-    float ss = 0.f;
-    for (int64_t i = ctid; i < H; i += C) ss = fmaf(vec[i], vec[i], ss);
-    const float inv =
-        1.0f / sqrtf(block_sum(ss, wsum, ctid, C) / static_cast<float>(H) + p.eps);
-    stage_x<UnitQ4K>(R.xs, US, NormSrc{vec, kind == PH_QKV ? L.w_in : L.w_pf, inv}, kp.K, ctid,
-                     C);
-  } else if (kind == PH_O) {
-    stage_x<UnitQ4K>(R.xs, US, GatherSrc{p.v, p.head_dim, p.n_q_heads / p.n_kv_heads}, kp.K, ctid,
-                     C);
-  } else if (q6) {
-    stage_x<UnitQ6K, XCoherent, 32>(R.xs, US, XCoherent{p.m}, kp.K, ctid, C);
-  } else {
-    stage_x<UnitQ4K, XCoherent, 32>(R.xs, US, XCoherent{p.m}, kp.K, ctid, C);
-  }
-  // stores of h / h1 by CTA 0 are published by the reducer's release at the
-  // end of this phase (they precede it in CTA order through the barriers)
-  bar_sync(kConsumerBar, C);
 }
 
 // ------------------------------------------------------------------ host side
-static int64_t align_floats(int64_t n) { return (n + 63) / 64 * 64; }
+static int64_t align64(int64_t n) { return (n + 63) / 64 * 64; }
 
+// Workspace (8-byte words): q, k, v [4 * hidden each, enough for q_dim and
+// kv_dim <= 4 * hidden], o [hidden], f [hidden], m [inter], hin [2 * hidden],
+// h1 [2 * hidden], then one prologue counter per phase (4 * kMaxLayers).
 size_t chain_workspace_bytes(int64_t hidden, int64_t inter) {
-  // q, k, v sized for the largest heads layout the dims allow are passed at
-  // call time; here: q <= hidden*... keep generous fixed layout:
-  // q [hidden*4], k [hidden*4], v [hidden*4], o, f, hin, h1 [hidden], m [inter]
   if (hidden <= 0 || inter <= 0) return 0;
-  const int64_t fl = 3 * align_floats(4 * hidden) + 4 * align_floats(hidden) + align_floats(inter);
-  return static_cast<size_t>(fl) * sizeof(float) + 256;
+  const int64_t words = 3 * align64(4 * hidden) + 2 * align64(hidden) + align64(inter) +
+                        2 * align64(2 * hidden);
+  return static_cast<size_t>(words) * sizeof(Word) + 4 * kMaxLayers * sizeof(unsigned) + 256;
 }
 
 unsigned read_clear_chain_errors() {
@@ -477,6 +623,7 @@ qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
     return bad(QWS_ERR_SHAPE,
                "qws_decode_chain: hidden, inter, q_dim must be multiples of 256 in (0, 20480], "
                "q_dim and kv_dim <= 4 * hidden");
+  if (H > kMaxChainHidden) return bad(QWS_ERR_SHAPE, "qws_decode_chain: hidden must be <= 5120");
   if (!(d->eps >= 0.f)) return bad(QWS_ERR_SHAPE, "qws_decode_chain: eps must be >= 0");
   if (reinterpret_cast<uintptr_t>(h) % 4 || reinterpret_cast<uintptr_t>(ws) % 16)
     return bad(QWS_ERR_ALIGN, "qws_decode_chain: h must be 4-byte and ws 16-byte aligned");
@@ -522,25 +669,28 @@ qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
   p.post_norms = d->post_norms ? 1 : 0;
   p.h = h;
 
-  // workspace carve-up (floats)
-  float* w = static_cast<float*>(ws);
+  // workspace carve-up (8-byte {value, stamp} words), then the counter
+  Word* w = static_cast<Word*>(ws);
   p.q = w;
-  w += align_floats(4 * H);
+  w += align64(4 * H);
   p.k = w;
-  w += align_floats(4 * H);
+  w += align64(4 * H);
   p.v = w;
-  w += align_floats(4 * H);
+  w += align64(4 * H);
   p.o = w;
-  w += align_floats(H);
+  w += align64(H);
   p.f = w;
-  w += align_floats(H);
-  p.hin = w;
-  w += align_floats(H);
-  p.h1 = w;
-  w += align_floats(H);
+  w += align64(H);
   p.m = w;
-  w += align_floats(I);
-  p.counter = reinterpret_cast<unsigned*>(w);
+  w += align64(I);
+  p.hin = w;
+  w += align64(2 * H);
+  p.h1 = w;
+  w += align64(2 * H);
+  p.prologues = reinterpret_cast<unsigned*>(w);
+  const size_t clear_bytes =
+      static_cast<size_t>(reinterpret_cast<uint8_t*>(w) - static_cast<uint8_t*>(ws)) +
+      4 * kMaxLayers * sizeof(unsigned);
 
   const int sms = device_sms();
   // tile plans per phase kind (same consumer count for all)
@@ -571,7 +721,7 @@ qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
   p.stage_bytes = round_up(stage_need + 16, 128);
   p.red_floats = red;
   p.xs_floats = xs;
-  const size_t tail = (static_cast<size_t>(H) + 32 + 4) * sizeof(float);
+  const size_t tail = 64 * sizeof(float);   // warp sums
   p.S = 16;
   while (p.S > 2 && ring_smem_bytes(p.S, p.stage_bytes, p.red_floats, p.xs_floats) + tail >
                         kSmemBudget)
@@ -599,7 +749,8 @@ qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
     return QWS_ERR_CUDA;
   }
   const int grid = sms;  // one CTA per SM: all co-resident (cooperative launch)
-  cudaError_t e = cudaMemsetAsync(p.counter, 0, sizeof(unsigned), st);
+  // stamps left by an earlier launch must not look current: clear every word
+  cudaError_t e = cudaMemsetAsync(ws, 0, clear_bytes, st);
   if (e != cudaSuccess) {
     err = std::string("qws_decode_chain: ") + cudaGetErrorString(e);
     return QWS_ERR_CUDA;

@@ -331,15 +331,16 @@ __device__ __forceinline__ bool consume_phase(const Phase& Pref, const Ring& Rre
   const int slots = pair ? 2 * P.T : P.T;      // partial rows per vector
   const size_t rb = static_cast<size_t>(P.row_bytes);
   Unit unit;
-  if (STAGED) {
+  if constexpr (Unit::kMixed) unit.q6 = P.fmt == 14;
+  if constexpr (STAGED) {
     for (int bb = 0; bb < P.B; ++bb) {
       if (bb) bar_sync(kConsumerBar, C);       // previous vector fully read
       stage_x<Unit>(R.xs, US, x_of(bb), P.K, ctid, C);
       bar_sync(kConsumerBar, C);
       if (active && b == bb) unit.setup(u, XUnit{R.xs, US, u});
     }
-  } else if (active) {
-    unit.setup(u, XUnit{R.xs, US, u});
+  } else {
+    if (active) unit.setup(u, XUnit{R.xs, US, u});
   }
   float* const red_b = R.red + static_cast<size_t>(b * slots) * US + u;
   for (int t = cta; t < P.n_tiles; t += P.ncta) {
@@ -351,10 +352,12 @@ __device__ __forceinline__ bool consume_phase(const Phase& Pref, const Ring& Rre
     const uint8_t* st = R.stage(pos.s);
     float* red = red_b + static_cast<size_t>(pos.s) * R.red_floats;
     const int nr = pair ? 2 * tr.nrows : tr.nrows;
-    if (!PIPE && active) {
-      for (int r = gg; r < nr; r += G) {
-        const int slot = (pair && r >= tr.nrows) ? P.T + (r - tr.nrows) : r;
-        red[slot * US] = unit.row(st + slot * rb);
+    if constexpr (!PIPE) {
+      if (active) {
+        for (int r = gg; r < nr; r += G) {
+          const int slot = (pair && r >= tr.nrows) ? P.T + (r - tr.nrows) : r;
+          red[slot * US] = unit.row(st + slot * rb);
+        }
       }
     } else if (active && gg < nr) {
       // row r of the tile lives at slot(r) rows into the stage; the next

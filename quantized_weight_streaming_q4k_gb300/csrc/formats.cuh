@@ -65,9 +65,44 @@ __device__ __forceinline__ void nibble_word(uint32_t w, const float* xl, const f
 // qs[32c .. 32c+31] (weights 64c+l of sub-block 2c in the low nibbles and
 // 64c+32+l of sub-block 2c+1 in the high nibbles) plus the block header.
 // ---------------------------------------------------------------------------
+// Dot product of one Q4_K chunk (32 bytes: 32 low nibbles of sub-block 2c,
+// 32 high nibbles of sub-block 2c+1) with the pre-scaled activations xa / xb;
+// hd is the block header, sh/hi select the chunk's scale pair.
+__device__ __forceinline__ float q4k_chunk_dot(const uint4 hd, const uint4 q0, const uint4 q1,
+                                               const float* xa, const float* xb, float sxa,
+                                               float sxb, uint32_t sh, bool hi) {
+  float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
+  nibble_word(q0.x, xa + 0, xb + 0, a0, a1, b0, b1);
+  nibble_word(q0.y, xa + 4, xb + 4, a0, a1, b0, b1);
+  nibble_word(q0.z, xa + 8, xb + 8, a0, a1, b0, b1);
+  nibble_word(q0.w, xa + 12, xb + 12, a0, a1, b0, b1);
+  nibble_word(q1.x, xa + 16, xb + 16, a0, a1, b0, b1);
+  nibble_word(q1.y, xa + 20, xb + 20, a0, a1, b0, b1);
+  nibble_word(q1.z, xa + 24, xb + 24, a0, a1, b0, b1);
+  nibble_word(q1.w, xa + 28, xb + 28, a0, a1, b0, b1);
+  // 6-bit scales / mins of all eight sub-blocks, one per byte:
+  //   s < 4 : sc[s] & 63 and sc[s+4] & 63
+  //   s >= 4: (sc[s+4] & 15) | (sc[s-4] >> 6) << 4  and
+  //           (sc[s+4] >> 4) | (sc[s]   >> 6) << 4
+  const uint32_t S = hi ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u))
+                        : (hd.y & 0x3F3F3F3Fu);
+  const uint32_t M = hi ? (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u))
+                        : (hd.z & 0x3F3F3F3Fu);
+  const float sca = static_cast<float>((S >> sh) & 0xFFu);
+  const float scb = static_cast<float>((S >> (sh + 8)) & 0xFFu);
+  const float mna = static_cast<float>((M >> sh) & 0xFFu);
+  const float mnb = static_cast<float>((M >> (sh + 8)) & 0xFFu);
+  const float d = half_bits_to_float(hd.x) * exp2i(60);
+  const float dmin = half_bits_to_float(hd.x >> 16);
+  const float qx = fmaf(sca, a0 + a1, scb * (b0 + b1));
+  const float mx = fmaf(mna, sxa, mnb * sxb);
+  return fmaf(d, qx, -dmin * mx);
+}
+
 struct UnitQ4K {
   static constexpr int kFmt = 12;
   static constexpr int kUnitW = 64;
+  static constexpr bool kMixed = false;
   static constexpr int kBlockW = 256;
   static constexpr int kBlockBytes = 144;
   float xa[32];   // sub-block 2c,   column 64c + l,      pre-scaled
@@ -119,33 +154,7 @@ struct UnitQ4K {
 
   // Partial dot product of this unit with one row (its bytes in f).
   __device__ __forceinline__ float compute(const Frag& f) const {
-    const uint4 hd = f.hd, q0 = f.q0, q1 = f.q1;
-    float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-    nibble_word(q0.x, xa + 0, xb + 0, a0, a1, b0, b1);
-    nibble_word(q0.y, xa + 4, xb + 4, a0, a1, b0, b1);
-    nibble_word(q0.z, xa + 8, xb + 8, a0, a1, b0, b1);
-    nibble_word(q0.w, xa + 12, xb + 12, a0, a1, b0, b1);
-    nibble_word(q1.x, xa + 16, xb + 16, a0, a1, b0, b1);
-    nibble_word(q1.y, xa + 20, xb + 20, a0, a1, b0, b1);
-    nibble_word(q1.z, xa + 24, xb + 24, a0, a1, b0, b1);
-    nibble_word(q1.w, xa + 28, xb + 28, a0, a1, b0, b1);
-    // 6-bit scales / mins of all eight sub-blocks, one per byte:
-    //   s < 4 : sc[s] & 63 and sc[s+4] & 63
-    //   s >= 4: (sc[s+4] & 15) | (sc[s-4] >> 6) << 4  and
-    //           (sc[s+4] >> 4) | (sc[s]   >> 6) << 4
-    const uint32_t S = hi ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u))
-                          : (hd.y & 0x3F3F3F3Fu);
-    const uint32_t M = hi ? (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u))
-                          : (hd.z & 0x3F3F3F3Fu);
-    const float sca = static_cast<float>((S >> sh) & 0xFFu);
-    const float scb = static_cast<float>((S >> (sh + 8)) & 0xFFu);
-    const float mna = static_cast<float>((M >> sh) & 0xFFu);
-    const float mnb = static_cast<float>((M >> (sh + 8)) & 0xFFu);
-    const float d = half_bits_to_float(hd.x) * exp2i(60);
-    const float dmin = half_bits_to_float(hd.x >> 16);
-    const float qx = fmaf(sca, a0 + a1, scb * (b0 + b1));
-    const float mx = fmaf(mna, sxa, mnb * sxb);
-    return fmaf(d, qx, -dmin * mx);
+    return q4k_chunk_dot(f.hd, f.q0, f.q1, xa, xb, sxa, sxb, sh, hi);
   }
 
   __device__ __forceinline__ float row(const uint8_t* rp) const {
@@ -174,9 +183,53 @@ __device__ __forceinline__ void load8_a2(const uint8_t* p, uint32_t& w0, uint32_
   w1 = __funnelshift_r(r1, r2, s);
 }
 
+// Dot product of one 32-column Q6_K group (8 bytes of each of the two ql
+// runs, 8 bytes of qh, 8 scale bytes of the half) with activations x[8a + i]
+// pre-scaled by 2^(kE - pos); sx32[a] carries the -32 offset.
+__device__ __forceinline__ float q6k_group_dot(uint32_t A0, uint32_t A1, uint32_t B0, uint32_t B1,
+                                               uint32_t Q0, uint32_t Q1, uint32_t S0, uint32_t S1,
+                                               uint32_t dbits, const float* x, const float* sx32,
+                                               uint32_t sshift) {
+  const float d = half_bits_to_float(dbits) * exp2i(60);
+  float p[4][2];
+#pragma unroll
+  for (int a = 0; a < 4; ++a) p[a][0] = p[a][1] = 0.f;
+  constexpr uint32_t M = 0x0F0F0F0Fu;
+  const uint32_t WA[2] = {A0, A1}, WB[2] = {B0, B1}, H[2] = {Q0, Q1};
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const uint32_t wa = WA[t], wb = WB[t], hh = H[t];
+    // 6-bit quants of four consecutive columns, one per byte (bits 6,7 of
+    // each byte are don't-care; the extraction masks drop them)
+    const uint32_t v0 = (wa & M) | ((hh << 4) & ~M);
+    const uint32_t v1 = (wb & M) | ((hh << 2) & ~M);
+    const uint32_t v2 = ((wa >> 4) & M) | (hh & ~M);
+    const uint32_t v3 = ((wb >> 4) & M) | ((hh >> 2) & ~M);
+    const uint32_t vv[4] = {v0, v1, v2, v3};
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      const uint32_t v = vv[a];
+      const float* xr = x + 8 * a + 4 * t;
+      fma2(p[a][0], p[a][1], bits(v & 0x3Fu), bits(v & 0x3F00u), xr[0], xr[1]);
+      fma2(p[a][0], p[a][1], bits(v & 0x3F0000u), bits((v >> 8) & 0x3F0000u), xr[2], xr[3]);
+    }
+  }
+  // scale of group a: byte 2a + jj/2 of the 8 scale bytes of half h
+  float acc = 0.f;
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const uint32_t wsc = a < 2 ? S0 : S1;
+    const uint32_t shift = 16u * (a & 1) + sshift;
+    const int sc = static_cast<int>(static_cast<int8_t>((wsc >> shift) & 0xFFu));
+    acc = fmaf(static_cast<float>(sc), (p[a][0] + p[a][1]) - sx32[a], acc);
+  }
+  return d * acc;
+}
+
 struct UnitQ6K {
   static constexpr int kFmt = 14;
   static constexpr int kUnitW = 32;
+  static constexpr bool kMixed = false;
   static constexpr int kBlockW = 256;
   static constexpr int kBlockBytes = 210;
   float x[4][8];    // [a][i], pre-scaled by 2^(kE - pos(i%4))
@@ -233,40 +286,8 @@ struct UnitQ6K {
   }
 
   __device__ __forceinline__ float compute(const Frag& f) const {
-    const float d = half_bits_to_float(f.dbits) * exp2i(60);
-    float p[4][2];
-#pragma unroll
-    for (int a = 0; a < 4; ++a) p[a][0] = p[a][1] = 0.f;
-    constexpr uint32_t M = 0x0F0F0F0Fu;
-    const uint32_t WA[2] = {f.A0, f.A1}, WB[2] = {f.B0, f.B1}, H[2] = {f.Q0, f.Q1};
-#pragma unroll
-    for (int t = 0; t < 2; ++t) {
-      const uint32_t wa = WA[t], wb = WB[t], hh = H[t];
-      // 6-bit quants of four consecutive columns, one per byte (bits 6,7 of
-      // each byte are don't-care; the extraction masks drop them)
-      const uint32_t v0 = (wa & M) | ((hh << 4) & ~M);
-      const uint32_t v1 = (wb & M) | ((hh << 2) & ~M);
-      const uint32_t v2 = ((wa >> 4) & M) | (hh & ~M);
-      const uint32_t v3 = ((wb >> 4) & M) | ((hh >> 2) & ~M);
-      const uint32_t vv[4] = {v0, v1, v2, v3};
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        const uint32_t v = vv[a];
-        fma2(p[a][0], p[a][1], bits(v & 0x3Fu), bits(v & 0x3F00u), x[a][4 * t], x[a][4 * t + 1]);
-        fma2(p[a][0], p[a][1], bits(v & 0x3F0000u), bits((v >> 8) & 0x3F0000u), x[a][4 * t + 2],
-             x[a][4 * t + 3]);
-      }
-    }
-    // scale of group a: byte 2a + jj/2 of the 8 scale bytes of half h
-    float acc = 0.f;
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      const uint32_t wsc = a < 2 ? f.S0 : f.S1;
-      const uint32_t shift = 16u * (a & 1) + sshift;
-      const int sc = static_cast<int>(static_cast<int8_t>((wsc >> shift) & 0xFFu));
-      acc = fmaf(static_cast<float>(sc), (p[a][0] + p[a][1]) - sx32[a], acc);
-    }
-    return d * acc;
+    return q6k_group_dot(f.A0, f.A1, f.B0, f.B1, f.Q0, f.Q1, f.S0, f.S1, f.dbits, &x[0][0], sx32,
+                         sshift);
   }
 
   __device__ __forceinline__ float row(const uint8_t* rp) const {
@@ -286,6 +307,7 @@ struct UnitQ6K {
 struct UnitQ40 {
   static constexpr int kFmt = 2;
   static constexpr int kUnitW = 64;
+  static constexpr bool kMixed = false;
   static constexpr int kBlockW = 32;
   static constexpr int kBlockBytes = 18;
   float e0[4];               // qs0[0..1] via w0 >> 12: lo0 hi0 lo1 hi1 (pos 4, 8, 12, 16)
@@ -369,6 +391,95 @@ struct UnitQ40 {
     Frag f;
     load(rp, f);
     return compute(f);
+  }
+};
+
+// ---------------------------------------------------------------------------
+// Decoder for a kernel that streams both Q4_K (64-column units) and Q6_K
+// (32-column units) phases: one 64-float activation array serves either
+// format, so both decode loops share one register allocation.
+// ---------------------------------------------------------------------------
+struct UnitChain {
+  static constexpr bool kMixed = true;
+  bool q6;         // set from the phase's format before setup()
+  float x[64];     // Q4_K: xa = x[0..31], xb = x[32..63]; Q6_K: x[8a + i]
+  float s[4];      // Q4_K: sxa, sxb; Q6_K: sx32[0..3]
+  uint32_t off, o1, o2, o3, o4, sh;
+  bool hi;
+
+  template <class XU>
+  __device__ __forceinline__ void setup_q4k(int u, const XU& xu) {
+    const int kb = u >> 2, c = u & 3;
+    off = static_cast<uint32_t>(kb) * 144u;
+    o1 = 16u + 32u * c;
+    sh = 16u * (c & 1);
+    hi = c >= 2;
+    float sa = 0.f, sb = 0.f;
+#pragma unroll
+    for (int l = 0; l < 32; ++l) {
+      const float va = xu(l), vb = xu(32 + l);
+      sa += va;
+      sb += vb;
+      x[l] = va * exp2i(kE - pos_lo(l & 3));
+      x[32 + l] = vb * exp2i(kE - pos_hi(l & 3));
+    }
+    s[0] = sa;
+    s[1] = sb;
+  }
+
+  template <class XU>
+  __device__ __forceinline__ void setup_q6k(int u, const XU& xu) {
+    const int kb = u >> 3, h = (u >> 2) & 1, jj = u & 3;
+    off = static_cast<uint32_t>(kb) * 210u;
+    o1 = 64u * h + 8u * jj;
+    o2 = 64u * h + 32u + 8u * jj;
+    o3 = 128u + 32u * h + 8u * jj;
+    o4 = 192u + 8u * h;
+    sh = 8u * static_cast<uint32_t>(jj >> 1);
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      float t = 0.f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float v = xu(8 * a + i);
+        t += v;
+        const int pos = (i & 3) == 0 ? 0 : (i & 3) == 1 ? 8 : 16;
+        x[8 * a + i] = v * exp2i(kE - pos);
+      }
+      s[a] = t * exp2i(5 - 60);
+    }
+  }
+
+  template <class XU>
+  __device__ __forceinline__ void setup(int u, const XU& xu) {
+    if (q6)
+      setup_q6k(u, xu);
+    else
+      setup_q4k(u, xu);
+  }
+
+  __device__ __forceinline__ float row(const uint8_t* rp) const {
+    return q6 ? row_q6k(rp) : row_q4k(rp);
+  }
+
+  __device__ __forceinline__ float row_q4k(const uint8_t* rp) const {
+    const uint8_t* bp = rp + off;
+    const uint4 hd = *reinterpret_cast<const uint4*>(bp);
+    const uint4 q0 = *reinterpret_cast<const uint4*>(bp + o1);
+    const uint4 q1 = *reinterpret_cast<const uint4*>(bp + o1 + 16);
+    return q4k_chunk_dot(hd, q0, q1, x, x + 32, s[0], s[1], sh, hi);
+  }
+
+  __device__ __forceinline__ float row_q6k(const uint8_t* rp) const {
+    const uint8_t* bp = rp + off;
+    uint32_t A0, A1, B0, B1, Q0, Q1, S0, S1;
+    load8_a2(bp + o1, A0, A1);
+    load8_a2(bp + o2, B0, B1);
+    load8_a2(bp + o3, Q0, Q1);
+    load8_a2(bp + o4, S0, S1);
+    const uintptr_t da = reinterpret_cast<uintptr_t>(bp + 208);
+    const uint32_t dw = *reinterpret_cast<const uint32_t*>(da & ~uintptr_t(3));
+    return q6k_group_dot(A0, A1, B0, B1, Q0, Q1, S0, S1, dw >> ((da & 3u) * 8u), x, s, sh);
   }
 };
 
