@@ -6,6 +6,7 @@ Metric: achieved HBM GB/s of the packed-weight stream (+ vector bytes), with
 microseconds per token of the 34-layer chain reported alongside.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+       [--n-layers L]   (a shorter chain, for small profiler captures only)
 For N > 1 launch with torchrun; every rank runs an independent replica of the
 step on its own GPU (the path has no data exchange; "replicas only").
 """
@@ -52,9 +53,11 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic():
+def profiled_traffic(n_layers=N_LAYERS):
     """dram bytes per chain launch from the committed ncu summary, if it was
-    taken on the current kernel sources (else None)."""
+    taken on the current kernel sources (else None).  The summary holds the
+    bytes per layer of a shorter chain (traffic is per layer plus a small
+    constant), scaled here by the number of layers."""
     p = os.path.join(ROOT, "profiles", "chain_kernel_traffic.json")
     if not os.path.exists(p):
         return None
@@ -62,10 +65,10 @@ def profiled_traffic():
         d = json.load(f)
     if d.get("kernel_hash") != kernel_hash():
         return None
-    return float(d["bytes_per_launch"])
+    return float(d["bytes_per_layer"]) * n_layers
 
 
-def algorithmic_bytes(dims):
+def algorithmic_bytes(dims, n_layers=N_LAYERS):
     from quantized_weight_streaming_q4k_gb300 import synth
     H, I = dims["hidden"], dims["inter"]
     qd = dims["n_q_heads"] * dims["head_dim"]
@@ -74,7 +77,7 @@ def algorithmic_bytes(dims):
     q6k = lambda r, c: synth.n_blocks(synth.Q6_K, r, c) * 210
     layer_w = q4k(qd + 2 * kd, H) + q4k(H, qd) + 2 * q4k(I, H) + q6k(H, I)
     norm_w = 4 * H * 4
-    chain = N_LAYERS * (layer_w + norm_w) + 2 * H * 4          # + h in and out
+    chain = n_layers * (layer_w + norm_w) + 2 * H * 4          # + h in and out
     lm_head = synth.n_blocks(synth.Q4_0, VOCAB, H) * 18 + H * 4 + VOCAB * 4
     final_norm = 3 * H * 4
     return chain, final_norm, lm_head
@@ -225,11 +228,12 @@ def run_gpu(args, world, rank, local):
     torch.cuda.set_device(dev)
     dims = synth.GEMMA3_4B
     H = dims["hidden"]
-    chain_b, fnorm_b, lm_b = algorithmic_bytes(dims)
+    n_layers = args.n_layers
+    chain_b, fnorm_b, lm_b = algorithmic_bytes(dims, n_layers)
 
     # ---- inputs, resident in HBM
     layers = []
-    for l in range(N_LAYERS):
+    for l in range(n_layers):
         L = synth.chain_layer(l, dims)
         layers.append({k: (torch.from_numpy(v).to(dev) if isinstance(v, np.ndarray) else v)
                        for k, v in L.items()})
@@ -317,28 +321,31 @@ def run_gpu(args, world, rank, local):
     achieved = chain_b / (chain_avg * 1e-3) / 1e9
     if rank != 0:
         return
+    workload = WORKLOAD if n_layers == N_LAYERS else WORKLOAD.replace(
+        f"{N_LAYERS}-layer", f"{n_layers}-layer (profiling case)")
     out = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded random Q4_K/Q6_K/Q4_0 blocks, Gemma-3-4B shapes)",
-        "config": {"workload": WORKLOAD, "n_layers": N_LAYERS, "vocab": VOCAB, "batch": 1,
-                   "l2": "inputs larger than L2: 2.41 GB of weights streamed per step",
+        "config": {"workload": workload, "n_layers": n_layers, "vocab": VOCAB, "batch": 1,
+                   "l2": f"inputs larger than L2: {bytes_step / 1e9:.2f} GB of weights "
+                         "streamed per step",
                    "parallelism": f"replicas x{world}"},
         "chain_us_per_token": 1e3 * chain_avg,
         "lm_head_us": 1e3 * statistics.mean(lm_ms),
         "bytes_per_step": bytes_step,
-        "roofline": {"bound": "hbm", "kernel": "chain_kernel (34-layer decode chain)",
+        "roofline": {"bound": "hbm", "kernel": f"chain_kernel ({n_layers}-layer decode chain)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
-                     "traffic": profiled_traffic()},
+                     "traffic": profiled_traffic(n_layers)},
         "e2e": {"value": world * bytes_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": H * 4, "d2h_bytes_per_step": VOCAB * 4,
                 "ms_per_step": e2e_ms},
         "gpu_launches": 3 * args.steps,
         "clocks": clk,
     }
-    if world == 1 and not args.no_cpu_baseline:
+    if world == 1 and not args.no_cpu_baseline and n_layers == N_LAYERS:
         out["cpu_baseline"] = cpu_oracle_sample()
     print(json.dumps(out))
 
@@ -350,6 +357,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--n-layers", type=int, default=N_LAYERS,
+                    help="chain length (default 34; shorter only for profiler captures)")
     args = ap.parse_args()
     world, rank, local = dist_init()
     if args.impl == "reference":
