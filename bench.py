@@ -130,26 +130,36 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
-def dist_init():
+def dist_init(backend: str = "nccl"):
+    """Rank, world and local rank from the torchrun environment; joins the
+    process group when world > 1 (NCCL on GPUs; gloo for the CPU tests)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
         import torch
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl")
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
     return world, rank, local
 
 
-def max_over_ranks(v: float, world: int) -> float:
+def max_over_ranks(v: float, world: int, device: str = "cuda") -> float:
+    """The largest v over all ranks (every rank gets it)."""
     if world == 1:
         return v
     import torch
     import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device="cuda")
+    t = torch.tensor([v], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step: float, ms_per_step_max: float, world: int) -> float:
+    """Whole-job GB/s: every rank streams its own replica of the step, the job
+    takes as long as its slowest rank."""
+    return world * bytes_per_rank_step / (ms_per_step_max * 1e-3) / 1e9
 
 
 def barrier(world: int):
@@ -315,7 +325,7 @@ def run_gpu(args, world, rank, local):
 
     bytes_step = chain_b + fnorm_b + lm_b
     ms_step = total_ms / args.steps
-    value = world * bytes_step / (ms_step * 1e-3) / 1e9
+    value = job_throughput(bytes_step, ms_step, world)
     chain_avg = statistics.mean(chain_ms)
     peak, peak_kind = peaks()
     achieved = chain_b / (chain_avg * 1e-3) / 1e9
@@ -339,7 +349,7 @@ def run_gpu(args, world, rank, local):
                      "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_kind,
                      "traffic": profiled_traffic(n_layers)},
-        "e2e": {"value": world * bytes_step / (e2e_ms * 1e-3) / 1e9, "unit": "GB/s",
+        "e2e": {"value": job_throughput(bytes_step, e2e_ms, world), "unit": "GB/s",
                 "h2d_bytes_per_step": H * 4, "d2h_bytes_per_step": VOCAB * 4,
                 "ms_per_step": e2e_ms},
         "gpu_launches": 3 * args.steps,

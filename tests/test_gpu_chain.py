@@ -80,6 +80,30 @@ def test_chain_small_teacher_forced(post_norms, fmt_down):
     assert np.array_equal(run_chain(ldev, h0, dims), hall)
 
 
+# Fewer 16-byte row groups than CTAs in the down phase (Q6_K rows of 256
+# columns are 210 B: 8-row groups, 32 of them): most CTAs own no rows there and
+# still take part in every phase's synchronisation.
+TINY = dict(hidden=256, inter=256, n_q_heads=2, n_kv_heads=1, head_dim=128, eps=1e-6,
+            post_norms=1)
+
+
+def test_chain_tiny_idle_ctas():
+    dims = TINY
+    n = 5
+    layers = [synth.chain_layer(l, dims, fmt_down=oracle.Q6_K, workload=54) for l in range(n)]
+    ldev = [to_dev(L) for L in layers]
+    h0 = synth.normal_vector(synth.rng(55), dims["hidden"])
+    h = h0
+    outs = []
+    for l in range(n):
+        hg = run_chain([ldev[l]], h, dims)
+        check_layer(h, hg, layers[l], dims)
+        outs.append(hg)
+        h = hg
+    hall = run_chain(ldev, h0, dims)
+    assert np.array_equal(hall, outs[-1])
+
+
 def test_chain_small_end_to_end():
     dims = SMALL
     n = 4
