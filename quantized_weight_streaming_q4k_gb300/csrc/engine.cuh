@@ -335,7 +335,12 @@ __device__ __forceinline__ bool consume_phase(const Phase& Pref, const Ring& Rre
   if constexpr (STAGED) {
     for (int bb = 0; bb < P.B; ++bb) {
       if (bb) bar_sync(kConsumerBar, C);       // previous vector fully read
-      stage_x<Unit>(R.xs, US, x_of(bb), P.K, ctid, C);
+      // one round of loads per thread when K allows (every CTA reads the same
+      // vector at the same moment: each extra round costs a loaded L2 trip)
+      if (P.K > 8 * static_cast<int64_t>(C))
+        stage_x<Unit, decltype(x_of(bb)), 16>(R.xs, US, x_of(bb), P.K, ctid, C);
+      else
+        stage_x<Unit>(R.xs, US, x_of(bb), P.K, ctid, C);
       bar_sync(kConsumerBar, C);
       if (active && b == bb) unit.setup(u, XUnit{R.xs, US, u});
     }
