@@ -365,30 +365,37 @@ __device__ __forceinline__ bool consume_phase(const Phase& Pref, const Ring& Rre
     const uint8_t* st = R.stage(pos.s);
     float* red = red_b + static_cast<size_t>(pos.s) * R.red_floats;
     const int nr = pair ? 2 * tr.nrows : tr.nrows;
+    // row r of the tile lives at slot(r) rows into the stage; rows are taken
+    // two at a time so that the two independent decode chains interleave
+    auto slot_of = [&](int r) { return (pair && r >= tr.nrows) ? P.T + (r - tr.nrows) : r; };
     if constexpr (!PIPE) {
       if (active) {
-        for (int r = gg; r < nr; r += G) {
-          const int slot = (pair && r >= tr.nrows) ? P.T + (r - tr.nrows) : r;
-          red[slot * US] = unit.row(st + slot * rb);
+        int r = gg;
+        for (; r + G < nr; r += 2 * G) {
+          const int s0 = slot_of(r), s1 = slot_of(r + G);
+          float y0, y1;
+          unit.row2(st + s0 * rb, st + s1 * rb, y0, y1);
+          red[s0 * US] = y0;
+          red[s1 * US] = y1;
         }
+        if (r < nr) red[slot_of(r) * US] = unit.row(st + slot_of(r) * rb);
       }
-    } else if (active && gg < nr) {
-      // row r of the tile lives at slot(r) rows into the stage; the next
-      // row's bytes are loaded while the current one is decoded
+    } else if (active) {
       int r = gg;
-      int slot = (pair && r >= tr.nrows) ? P.T + (r - tr.nrows) : r;
-      typename Unit::Frag f;
-      unit.load(st + slot * rb, f);
-      for (;;) {
-        const int rn = r + G;
-        const int slot_n = (pair && rn >= tr.nrows) ? P.T + (rn - tr.nrows) : rn;
-        typename Unit::Frag fn;
-        if (rn < nr) unit.load(st + slot_n * rb, fn);
-        red[slot * US] = unit.compute(f);
-        if (rn >= nr) break;
-        r = rn;
-        slot = slot_n;
-        f = fn;
+      for (; r + G < nr; r += 2 * G) {
+        const int s0 = slot_of(r), s1 = slot_of(r + G);
+        typename Unit::Frag f0, f1;
+        unit.load(st + s0 * rb, f0);
+        unit.load(st + s1 * rb, f1);
+        const float y0 = unit.compute(f0);
+        const float y1 = unit.compute(f1);
+        red[s0 * US] = y0;
+        red[s1 * US] = y1;
+      }
+      if (r < nr) {
+        typename Unit::Frag f;
+        unit.load(st + slot_of(r) * rb, f);
+        red[slot_of(r) * US] = unit.compute(f);
       }
     }
     __syncwarp();

@@ -462,6 +462,18 @@ struct UnitChain {
     return q6 ? row_q6k(rp) : row_q4k(rp);
   }
 
+  // two rows, one format branch: the two decode chains interleave
+  __device__ __forceinline__ void row2(const uint8_t* r0, const uint8_t* r1, float& y0,
+                                       float& y1) const {
+    if (q6) {
+      y0 = row_q6k(r0);
+      y1 = row_q6k(r1);
+    } else {
+      y0 = row_q4k(r0);
+      y1 = row_q4k(r1);
+    }
+  }
+
   __device__ __forceinline__ float row_q4k(const uint8_t* rp) const {
     const uint8_t* bp = rp + off;
     const uint4 hd = *reinterpret_cast<const uint4*>(bp);
