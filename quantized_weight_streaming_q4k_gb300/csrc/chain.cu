@@ -89,17 +89,31 @@ __device__ __forceinline__ float value_of(Word w) {
   return __uint_as_float(static_cast<unsigned>(w & 0xFFFFFFFFu));
 }
 
+__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void red_relaxed_add(unsigned* p, unsigned v) {
+  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 // Waits (bounded) until every CTA has finished the prologue of phase ph.
+// Relaxed: a CTA counts its prologue only after every value that prologue
+// loaded has been used (a barrier orders the count after those loads), so a
+// write issued once the count is full cannot reach them; and a reader that
+// ever met a newer stamp would time out, not read a wrong value.
 __device__ __forceinline__ bool wait_prologues(const ChainParams& p, int ph) {
   if (ph < 0) return true;
   const unsigned* c = p.prologues + ph;
-  if (ld_acquire_gpu(c) >= gridDim.x) return true;
+  if (ld_relaxed_u32(c) >= gridDim.x) return true;
   const long long t0 = clock64();
-  while (ld_acquire_gpu(c) < gridDim.x) {
+  while (ld_relaxed_u32(c) < gridDim.x) {
     if (clock64() - t0 > kWaitCycles) {
       atomicOr(&g_err_chain, kErrGridBarrier);
       return false;
     }
+    __nanosleep(64);
   }
   return true;
 }
@@ -149,21 +163,14 @@ struct ChainPhases {
 };
 
 // Reducer epilogue: stores each reduced row (GEGLU for the gate/up pair) as a
-// stamped word in the segment's destination (q / k / v, o, m or f).  Before the first store of
-// a phase ph it makes sure that every CTA has finished the prologue that last
-// read the buffer's old contents: phase ph - 3 (v by O, o by GU, m by DOWN, f by
-// the next QKV -- each three phases later than its writer).
+// stamped word in the segment's destination (q / k / v, o, m or f).  The
+// reducer checks before the phase that every CTA has finished the prologue
+// that last read the buffer's old contents: phase ph - 3 (v by O, o by GU, m
+// by DOWN, f by the next QKV -- each three phases later than its writer).
 struct EpiStamped {
-  const ChainParams* p;
   int ph;
-  mutable bool checked;
-  mutable bool ok;
   __device__ __forceinline__ void operator()(const Phase& P, const TileRef& tr, int, int o, float v,
                                              float v2) const {
-    if (!checked) {
-      ok = wait_prologues(*p, ph - 3);
-      checked = true;
-    }
     Word* dst = reinterpret_cast<Word*>(tr.y);
     const float val = (ph & 3) == PH_GU ? gelu_tanh(v) * v2 : v;
     st_word(dst + tr.r0 + o, val, static_cast<unsigned>(ph + 1));
@@ -235,7 +242,8 @@ __device__ __forceinline__ bool resnorm_stage(const ChainParams& p, const Ring& 
                                               const float* base_plain, const Word* add,
                                               unsigned add_stamp, const float* wa,
                                               const float* wn, Word* store, unsigned store_stamp,
-                                              int store_war, int US, int ctid) {
+                                              int store_war, unsigned war_seen, int US,
+                                              int ctid) {
   const int64_t H = p.H;
   const bool post = p.post_norms != 0;
   float bs[kJ], ad[kJ], wwa[kJ], wwn[kJ];
@@ -283,7 +291,8 @@ __device__ __forceinline__ bool resnorm_stage(const ChainParams& p, const Ring& 
     ss2 = fmaf(r, r, ss2);
   }
   if (store) {
-    if (!wait_prologues(p, store_war)) ok = false;
+    // war_seen: the count loaded at the prologue's start (usually full already)
+    if (war_seen < gridDim.x && !wait_prologues(p, store_war)) ok = false;
 #pragma unroll
     for (int j = 0; j < kJ; ++j) {
       const int64_t i = ctid + static_cast<int64_t>(j) * kC;
@@ -381,6 +390,14 @@ __device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const 
   const unsigned prev = static_cast<unsigned>(ph);   // stamp of the previous phase's outputs
   const bool wide = p.H > 8 * static_cast<int64_t>(C);
   bool ok = true;
+  // CTA 0 overwrites hin[l & 1] (QKV; last read by GU(l - 2)) or h1[l & 1]
+  // (GU; last read by QKV(l - 1)): load that count now, check it before the
+  // stores, so its latency hides behind the loads of the vectors
+  unsigned war_seen = gridDim.x;
+  if (blockIdx.x == 0 && (kind == PH_QKV || kind == PH_GU)) {
+    const int w = kind == PH_QKV ? 4 * l - 6 : 4 * l - 4;
+    if (w >= 0) war_seen = ld_relaxed_u32(p.prologues + w);
+  }
   // every consumer thread of this CTA is done with R.xs of the previous phase
   bar_sync(kConsumerBar, C);
   if (kind == PH_QKV || kind == PH_GU) {
@@ -413,11 +430,11 @@ __device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const 
       war = 4 * l - 4;   // QKV(l - 1) read h1[l & 1] last
     }
     ok = wide ? resnorm_stage<16, false>(p, R, wsum, base, base_stamp, base_plain, add, add_stamp,
-                                         wa, wn, store, static_cast<unsigned>(ph + 1), war, US,
-                                         ctid)
+                                         wa, wn, store, static_cast<unsigned>(ph + 1), war,
+                                         war_seen, US, ctid)
               : resnorm_stage<8, true>(p, R, wsum, base, base_stamp, base_plain, add, add_stamp,
-                                       wa, wn, store, static_cast<unsigned>(ph + 1), war, US,
-                                       ctid);
+                                       wa, wn, store, static_cast<unsigned>(ph + 1), war,
+                                       war_seen, US, ctid);
   } else if (kind == PH_O) {
     ok = stage_gather<8>(R, US, p.v, prev, kp.K, p.head_dim, p.n_q_heads / p.n_kv_heads, ctid);
   } else if (q6) {
@@ -427,7 +444,7 @@ __device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const 
   }
   bar_sync(kConsumerBar, C);
   // this CTA has read everything its prologue needed
-  if (ctid == 0) red_release_gpu_add(p.prologues + ph, 1u);
+  if (ctid == 0) red_relaxed_add(p.prologues + ph, 1u);
   return ok;
 }
 
@@ -562,9 +579,10 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
     // ---------------- reducer: sums and stamped stores, phase after phase
     for (int ph = 0; ph < nph; ++ph) {
       const Phase P = phases.get(ph);
-      const EpiStamped epi{&p, ph, false, true};
-      const bool ok = reduce_phase(P, R, pos, epi, &g_err_chain);
-      if (!ok || !epi.ok) return;
+      // (one load, normally already satisfied; it overlaps the consumers'
+      // work on the phase's first tile)
+      if (!wait_prologues(p, ph - 3)) return;
+      if (!reduce_phase(P, R, pos, EpiStamped{ph}, &g_err_chain)) return;
     }
     return;
   }
