@@ -43,7 +43,8 @@ namespace qws {
 __device__ unsigned g_err_chain;
 
 constexpr int kMaxLayers = 64;
-constexpr uint32_t kChainTileTarget = 23 * 1024;  // deeper ring, finer balance across CTAs
+constexpr uint32_t kChainTileTarget = 23 * 1024;  // measured optimum (12, 19, 32, 46 KB slower)
+constexpr uint32_t kChainStages = 4;
 constexpr int64_t kMaxChainHidden = 16 * kMaxConsumers;  // residual vectors: 16 per thread
 
 enum : int { PH_QKV = 0, PH_O = 1, PH_GU = 2, PH_DOWN = 3 };
@@ -761,7 +762,11 @@ qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
   p.red_floats = red;
   p.xs_floats = xs;
   const size_t tail = 64 * sizeof(float);   // warp sums
-  p.S = 16;
+  // Ring depth: at most kChainStages.  A deeper ring prefetches more of the
+  // next phase, and that DRAM traffic slows the L2 loads on every CTA's
+  // critical path at each phase boundary (measured on GB300: 7 stages 1416,
+  // 6: 1336, 4: 1291, 3: 1315, 2: 1503 us per 34-layer token).
+  p.S = kChainStages;
   while (p.S > 2 && ring_smem_bytes(p.S, p.stage_bytes, p.red_floats, p.xs_floats) + tail >
                         kSmemBudget)
     --p.S;
