@@ -43,7 +43,7 @@ namespace qws {
 __device__ unsigned g_err_chain;
 
 constexpr int kMaxLayers = 64;
-constexpr uint32_t kChainTileTarget = 23 * 1024;  // measured optimum (12, 19, 32, 46 KB slower)
+constexpr uint32_t kChainTileTarget = 30 * 1024;  // measured optimum at 4 stages
 constexpr uint32_t kChainStages = 4;
 constexpr int64_t kMaxChainHidden = 16 * kMaxConsumers;  // residual vectors: 16 per thread
 
@@ -530,21 +530,6 @@ __device__ __forceinline__ void prefetch_l2(const float* w, int64_t n) {
                  : "memory");
 }
 
-// Holds the producer's next copy back while this CTA's consumers rebuild a
-// phase input.  Those loads sit on the critical path of every CTA and are
-// L2 hits, but a DRAM stream in flight at the same time makes them several
-// times slower; all CTAs reach a phase boundary together, so pausing here
-// quiets the memory system for the prologue.  Tiles already in the ring keep
-// the consumers busy afterwards.  Bounded: after ~20 us it lets the copy go.
-struct QuietGate {
-  volatile int* quiet;
-  __device__ __forceinline__ void operator()() const {
-    if (!*quiet) return;
-    const long long t0 = clock64();
-    while (*quiet && clock64() - t0 < 40000) __nanosleep(64);
-  }
-};
-
 // ------------------------------------------------------------------ kernel
 __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
     chain_kernel(const __grid_constant__ ChainParams p) {
@@ -552,9 +537,6 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
   const Ring R = make_ring(smem, p.S, p.stage_bytes, p.red_floats, p.xs_floats);
   float* wsum = reinterpret_cast<float*>(smem + ring_smem_bytes(p.S, p.stage_bytes, p.red_floats,
                                                                  p.xs_floats));
-  // set by the consumers while they rebuild a phase's input (see QuietGate)
-  volatile int* quiet = reinterpret_cast<volatile int*>(wsum + 48);
-  if (threadIdx.x == 0) *quiet = 0;
   const int C = static_cast<int>(blockDim.x) - kRoleThreads;
   if (threadIdx.x == 0) ring_init(R, C / 32);
   __syncthreads();
@@ -570,7 +552,7 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
         prefetch_l2(p.L[l].w_pf, p.H * 4);
         prefetch_l2(p.L[l].w_pff, p.H * 4);
       }
-      run_producer(phases, R, &g_err_chain, QuietGate{quiet});
+      run_producer(phases, R, &g_err_chain);
     }
     return;
   }
@@ -594,10 +576,7 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
   for (int ph = 0; ph < nph; ++ph) {
     const Phase P = phases.get(ph);
     const bool q6 = (ph & 3) == PH_DOWN && down_q6k;
-    if (ctid == 0) *quiet = 1;
-    const bool pro_ok = chain_prologue(p, ph, R, wsum, q6, ctid, C);
-    if (ctid == 0) *quiet = 0;
-    if (!pro_ok) return;
+    if (!chain_prologue(p, ph, R, wsum, q6, ctid, C)) return;
     const unsigned long long r = chain_consume(
         P.fmt, P.epi, P.nseg, static_cast<int>(P.seg[0].rows), static_cast<int>(P.seg[1].rows),
         static_cast<int>(P.seg[2].rows), P.seg[0].tiles, P.seg[1].tiles, P.seg[2].tiles, P.T, P.U,

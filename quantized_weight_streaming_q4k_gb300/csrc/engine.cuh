@@ -219,17 +219,10 @@ __device__ __forceinline__ void fill_stage(const Phase& P, int t, const Ring& R,
   }
 }
 
-// Producer gate: called before each copy is issued; may hold the producer
-// back (bounded) while it returns.
-struct NoGate {
-  __device__ __forceinline__ void operator()() const {}
-};
-
 // PhaseList: count() and get(i) -> Phase, evaluated identically by producer
 // and consumers.
-template <class PhaseList, class Gate = NoGate>
-__device__ void run_producer(const PhaseList& L, const Ring& R, unsigned* err,
-                             const Gate& gate = Gate{}) {
+template <class PhaseList>
+__device__ void run_producer(const PhaseList& L, const Ring& R, unsigned* err) {
   const uint64_t pol = l2_policy_evict_first();
   RingPos pos;
   bool ok = true;
@@ -244,7 +237,6 @@ __device__ void run_producer(const PhaseList& L, const Ring& R, unsigned* err,
         ok = false;
         break;
       }
-      gate();
       fill_stage(P, t, R, pos.s, pol);
       pos.advance(R.S);
     }
