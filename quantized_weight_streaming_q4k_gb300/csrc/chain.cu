@@ -23,12 +23,15 @@
 // Write-after-read: before overwriting a buffer, a writer checks (one load,
 // normally already satisfied) that every CTA has finished the phase prologue
 // that last read the old contents; each CTA bumps a counter after each
-// prologue.  The vectors h and h1 that CTA 0 stores alternate between two
-// buffers by layer parity, so that check does not wait in practice.
+// prologue.  The vectors h and h1 that the keeper CTA stores alternate
+// between two buffers by layer parity, so that check does not wait in
+// practice.
 //
 // Every CTA rebuilds a phase's input vector itself from the (L2-resident)
 // previous outputs; sums of squares are reduced in a fixed order, so every CTA
-// computes bit-identical vectors.
+// computes bit-identical vectors.  The keeper is the grid's last CTA: tiles
+// are dealt from CTA 0 up, so it never owns more tiles than any other CTA, and
+// its extra work (storing h, h1 and the final h) stays off the critical path.
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -232,7 +235,7 @@ __device__ __forceinline__ bool poll_stamped(const Word* b, const Word* end, uns
 // r = base + (post ? add * rms_inv(add) * wa : add)      (r = base when add == null)
 // x = r * rms_inv(r) * wn  -> staged for Q4_K lane units (transposed)
 // Element ctid + j * kC of each vector lives in thread ctid's registers
-// (H <= kJ * kC).  When store != null (CTA 0) r is also stored as stamped
+// (H <= kJ * kC).  When store != null (keeper CTA) r is also stored as stamped
 // words, after the write-after-read check against phase store_war.  `base` is
 // the caller's plain h when base_plain != null (layer 0), else a stamped
 // vector.  kEarlyW: load the norm weights together with the vectors (one round
@@ -391,11 +394,11 @@ __device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const 
   const unsigned prev = static_cast<unsigned>(ph);   // stamp of the previous phase's outputs
   const bool wide = p.H > 8 * static_cast<int64_t>(C);
   bool ok = true;
-  // CTA 0 overwrites hin[l & 1] (QKV; last read by GU(l - 2)) or h1[l & 1]
+  // the keeper overwrites hin[l & 1] (QKV; last read by GU(l - 2)) or h1[l & 1]
   // (GU; last read by QKV(l - 1)): load that count now, check it before the
   // stores, so its latency hides behind the loads of the vectors
   unsigned war_seen = gridDim.x;
-  if (blockIdx.x == 0 && (kind == PH_QKV || kind == PH_GU)) {
+  if (blockIdx.x == gridDim.x - 1 && (kind == PH_QKV || kind == PH_GU)) {
     const int w = kind == PH_QKV ? 4 * l - 6 : 4 * l - 4;
     if (w >= 0) war_seen = ld_relaxed_u32(p.prologues + w);
   }
@@ -411,23 +414,23 @@ __device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const 
     int war;
     if (kind == PH_QKV) {
       // h = layer input: the caller's h, or h1 + norm(f) of the previous layer;
-      // CTA 0 keeps it in hin[l & 1] for the GU residual
+      // the keeper CTA keeps it in hin[l & 1] for the GU residual
       base = l ? p.h1 + ((l - 1) & 1) * p.H : nullptr;
       base_stamp = static_cast<unsigned>(4 * l - 1);
       base_plain = l ? nullptr : p.h;
       add = l ? p.f : nullptr;
       wa = l ? p.L[l - 1].w_pff : nullptr;
       wn = L.w_in;
-      store = blockIdx.x == 0 ? p.hin + (l & 1) * p.H : nullptr;
+      store = blockIdx.x == gridDim.x - 1 ? p.hin + (l & 1) * p.H : nullptr;
       war = 4 * l - 6;   // GU(l - 2) read hin[l & 1] last
     } else {
-      // h1 = h + rms_norm(o, w_post_attn) (or h + o); CTA 0 keeps it in h1[l & 1]
+      // h1 = h + rms_norm(o, w_post_attn) (or h + o); the keeper keeps it in h1[l & 1]
       base = p.hin + (l & 1) * p.H;
       base_stamp = static_cast<unsigned>(4 * l + 1);
       add = p.o;
       wa = L.w_pa;
       wn = L.w_pf;
-      store = blockIdx.x == 0 ? p.h1 + (l & 1) * p.H : nullptr;
+      store = blockIdx.x == gridDim.x - 1 ? p.h1 + (l & 1) * p.H : nullptr;
       war = 4 * l - 4;   // QKV(l - 1) read h1[l & 1] last
     }
     ok = wide ? resnorm_stage<16, false>(p, R, wsum, base, base_stamp, base_plain, add, add_stamp,
@@ -449,7 +452,7 @@ __device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const 
   return ok;
 }
 
-// Final residual on CTA 0: h = h1 + rms_norm(f, w_post_ffn) (or h1 + f).
+// Final residual on the keeper CTA: h = h1 + rms_norm(f, w_post_ffn) (or h1 + f).
 template <int kJ>
 __device__ __noinline__ bool chain_final(const ChainParams& p, float* wsum, int ctid, int C) {
   const int Ll = p.n_layers - 1;
@@ -587,7 +590,7 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
     pos.n = static_cast<uint32_t>((r >> 16) & 0xFFFFFFFFu);
     if ((r >> 63) == 0) return;
   }
-  if (blockIdx.x == 0) {
+  if (blockIdx.x == gridDim.x - 1) {
     if (p.H > 8 * static_cast<int64_t>(C))
       chain_final<16>(p, wsum, ctid, C);
     else
