@@ -41,9 +41,9 @@
  *    Nothing is enqueued when a call returns an error.  rows == 0 returns
  *    QWS_OK without a launch.  A bounded wait that expires inside a kernel
  *    (a wedged pipeline) records a code that qws_device_error() returns.
- *  - Limits: every consumer thread owns one lane unit of 64 columns (32 for
- *    Q6_K): batch * hidden / unit <= 320 per pass, so hidden <= 20480 (Q6_K:
- *    10240) at batch 1; larger products need split_k (qws_matvec,
+ *  - Limits: every consumer thread owns one lane unit of 64 columns:
+ *    batch * hidden / 64 <= 320 per pass, so hidden <= 20480 at batch 1 and
+ *    hidden <= 2560 at batch 8; larger products need split_k (qws_matvec,
  *    qws_q4_0_matvec), which divides hidden into column slices.
  */
 #ifndef QWS_H

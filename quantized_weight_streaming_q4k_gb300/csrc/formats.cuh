@@ -34,7 +34,7 @@ namespace qws {
 constexpr int kE = 89;                 // x' = x * 2^(kE - pos)
 
 // columns per lane unit of each format
-__host__ __device__ constexpr int unit_weights(int fmt) { return fmt == 14 ? 32 : 64; }
+__host__ __device__ constexpr int unit_weights(int) { return 64; }
 
 __device__ __forceinline__ float bits(uint32_t v) { return __uint_as_float(v); }
 
@@ -165,14 +165,14 @@ struct UnitQ4K {
 };
 
 // ---------------------------------------------------------------------------
-// Q6_K.  Unit u -> super-block kb = u/8, half h = (u/4)%2, column group
-// jj = u%4: weights 128h + 32a + 8jj + i for a = 0..3, i = 0..7 (32 weights).
-// Bytes: ql[64h+8jj ..+8] (a=0 low nibbles, a=2 high), ql[64h+32+8jj ..+8]
-// (a=1, a=3), qh[32h+8jj ..+8] (2-bit fields a=0..3 at bits 0,2,4,6); scale
-// of column group a is sc[(128h + 32a + 8jj) / 16] = sc[8h + 2a + jj/2].
+// Q6_K.  Unit u -> super-block kb = u/4, half h = (u/2)%2, column group
+// m = u%2: weights 128h + 32a + 16m + i for a = 0..3, i = 0..15 (64 weights).
+// Bytes: ql[64h+16m ..+16] (a=0 low nibbles, a=2 high), ql[64h+32+16m ..+16]
+// (a=1, a=3), qh[32h+16m ..+16] (2-bit fields a=0..3 at bits 0,2,4,6); the
+// scale of column group a is sc[(128h + 32a + 16m) / 16] = sc[8h + 2a + m]:
+// the unit's four scales share one 8-byte window, and one d serves all 64.
 // Blocks are 210 B, so a block starts on a 2-byte boundary: the lane loads
-// aligned words and funnel-shifts them.  A 32-column unit keeps the lane's
-// activations at 32 registers.
+// aligned words and funnel-shifts them.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void load8_a2(const uint8_t* p, uint32_t& w0, uint32_t& w1) {
   const uintptr_t a = reinterpret_cast<uintptr_t>(p);
@@ -183,22 +183,32 @@ __device__ __forceinline__ void load8_a2(const uint8_t* p, uint32_t& w0, uint32_
   w1 = __funnelshift_r(r1, r2, s);
 }
 
-// Dot product of one 32-column Q6_K group (8 bytes of each of the two ql
-// runs, 8 bytes of qh, 8 scale bytes of the half) with activations x[8a + i]
+__device__ __forceinline__ void load16_a2(const uint8_t* p, uint32_t (&w)[4]) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  const uint32_t* q = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
+  const uint32_t s = static_cast<uint32_t>(a & 3u) * 8u;
+  uint32_t r[5];
+#pragma unroll
+  for (int k = 0; k < 5; ++k) r[k] = q[k];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) w[k] = __funnelshift_r(r[k], r[k + 1], s);
+}
+
+// Dot product of one 64-column Q6_K unit (16 bytes of each of the two ql runs,
+// 16 bytes of qh, the 8 scale bytes of the half) with activations x[16a + i]
 // pre-scaled by 2^(kE - pos); sx32[a] carries the -32 offset.
-__device__ __forceinline__ float q6k_group_dot(uint32_t A0, uint32_t A1, uint32_t B0, uint32_t B1,
-                                               uint32_t Q0, uint32_t Q1, uint32_t S0, uint32_t S1,
-                                               uint32_t dbits, const float* x, const float* sx32,
-                                               uint32_t sshift) {
+__device__ __forceinline__ float q6k_unit_dot(const uint32_t (&A)[4], const uint32_t (&B)[4],
+                                              const uint32_t (&Q)[4], uint32_t S0, uint32_t S1,
+                                              uint32_t dbits, const float* x, const float* sx32,
+                                              uint32_t sshift) {
   const float d = half_bits_to_float(dbits) * exp2i(60);
   float p[4][2];
 #pragma unroll
   for (int a = 0; a < 4; ++a) p[a][0] = p[a][1] = 0.f;
   constexpr uint32_t M = 0x0F0F0F0Fu;
-  const uint32_t WA[2] = {A0, A1}, WB[2] = {B0, B1}, H[2] = {Q0, Q1};
 #pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    const uint32_t wa = WA[t], wb = WB[t], hh = H[t];
+  for (int t = 0; t < 4; ++t) {
+    const uint32_t wa = A[t], wb = B[t], hh = Q[t];
     // 6-bit quants of four consecutive columns, one per byte (bits 6,7 of
     // each byte are don't-care; the extraction masks drop them)
     const uint32_t v0 = (wa & M) | ((hh << 4) & ~M);
@@ -209,12 +219,12 @@ __device__ __forceinline__ float q6k_group_dot(uint32_t A0, uint32_t A1, uint32_
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
       const uint32_t v = vv[a];
-      const float* xr = x + 8 * a + 4 * t;
+      const float* xr = x + 16 * a + 4 * t;
       fma2(p[a][0], p[a][1], bits(v & 0x3Fu), bits(v & 0x3F00u), xr[0], xr[1]);
       fma2(p[a][0], p[a][1], bits(v & 0x3F0000u), bits((v >> 8) & 0x3F0000u), xr[2], xr[3]);
     }
   }
-  // scale of group a: byte 2a + jj/2 of the 8 scale bytes of half h
+  // scale of group a: byte 2a + m of the 8 scale bytes of half h
   float acc = 0.f;
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
@@ -226,68 +236,84 @@ __device__ __forceinline__ float q6k_group_dot(uint32_t A0, uint32_t A1, uint32_
   return d * acc;
 }
 
+// Column 256kb + 128h + 32a + 16m + i belongs to Q6_K unit 4kb + 2h + m with
+// unit-local index l = 16a + i.
+__device__ __forceinline__ void q6k_unit_of(int64_t col, int& u, int& l) {
+  const int kb = static_cast<int>(col >> 8), r = static_cast<int>(col & 255);
+  const int h = r >> 7, a = (r >> 5) & 3, m = (r >> 4) & 1, i = r & 15;
+  u = 4 * kb + 2 * h + m;
+  l = 16 * a + i;
+}
+
+// Set-up shared by the Q6_K lane units: byte offsets of the unit's runs and
+// the pre-scaled activations.
+struct Q6kUnitGeom {
+  uint32_t off, oA, oB, oQ, oS, sshift;
+  __device__ __forceinline__ void set(int u) {
+    const int kb = u >> 2, h = (u >> 1) & 1, m = u & 1;
+    off = static_cast<uint32_t>(kb) * 210u;
+    oA = 64u * h + 16u * m;
+    oB = 64u * h + 32u + 16u * m;
+    oQ = 128u + 32u * h + 16u * m;
+    oS = 192u + 8u * h;            // the 8 scales of half h
+    sshift = 8u * static_cast<uint32_t>(m);
+  }
+};
+
+template <class XU>
+__device__ __forceinline__ void q6k_setup_x(const XU& xu, float* x, float* sx32) {
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const float v = xu(16 * a + i);
+      s += v;
+      const int pos = (i & 3) == 0 ? 0 : (i & 3) == 1 ? 8 : 16;
+      x[16 * a + i] = v * exp2i(kE - pos);
+    }
+    sx32[a] = s * exp2i(5 - 60);
+  }
+}
+
 struct UnitQ6K {
   static constexpr int kFmt = 14;
-  static constexpr int kUnitW = 32;
+  static constexpr int kUnitW = 64;
   static constexpr bool kMixed = false;
   static constexpr int kBlockW = 256;
   static constexpr int kBlockBytes = 210;
-  float x[4][8];    // [a][i], pre-scaled by 2^(kE - pos(i%4))
+  float x[64];      // [16a + i], pre-scaled by 2^(kE - pos(i%4))
   float sx32[4];    // 32 * sum_i x[a][i] * 2^-60 (the -32 offset, in product units)
-  uint32_t off, oA, oB, oQ, oS;
-  uint32_t sshift;  // bit offset of sc[8h + jj/2] inside the 8-byte scale window
+  Q6kUnitGeom g;
 
-  // Column 256kb + 128h + 32a + 8jj + i belongs to unit 8kb + 4h + jj with
-  // unit-local index l = 8a + i.
   __device__ __forceinline__ static void unit_of(int64_t col, int& u, int& l) {
-    const int kb = static_cast<int>(col >> 8), r = static_cast<int>(col & 255);
-    const int h = r >> 7, a = (r >> 5) & 3, jj = (r >> 3) & 3, i = r & 7;
-    u = 8 * kb + 4 * h + jj;
-    l = 8 * a + i;
+    q6k_unit_of(col, u, l);
   }
 
   template <class XU>
   __device__ __forceinline__ void setup(int u, const XU& xu) {
-    const int kb = u >> 3, h = (u >> 2) & 1, jj = u & 3;
-    off = static_cast<uint32_t>(kb) * kBlockBytes;
-    oA = 64u * h + 8u * jj;
-    oB = 64u * h + 32u + 8u * jj;
-    oQ = 128u + 32u * h + 8u * jj;
-    oS = 192u + 8u * h;            // the 8 scales of half h
-    sshift = 8u * static_cast<uint32_t>(jj >> 1);
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      float s = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float v = xu(8 * a + i);
-        s += v;
-        const int pos = (i & 3) == 0 ? 0 : (i & 3) == 1 ? 8 : 16;
-        x[a][i] = v * exp2i(kE - pos);
-      }
-      sx32[a] = s * exp2i(5 - 60);
-    }
+    g.set(u);
+    q6k_setup_x(xu, x, sx32);
   }
 
   struct Frag {
-    uint32_t A0, A1, B0, B1, Q0, Q1, S0, S1;
+    uint32_t A[4], B[4], Q[4], S0, S1;
     uint32_t dbits;
   };
 
   __device__ __forceinline__ void load(const uint8_t* rp, Frag& f) const {
-    const uint8_t* bp = rp + off;
-    load8_a2(bp + oA, f.A0, f.A1);
-    load8_a2(bp + oB, f.B0, f.B1);
-    load8_a2(bp + oQ, f.Q0, f.Q1);
-    load8_a2(bp + oS, f.S0, f.S1);
+    const uint8_t* bp = rp + g.off;
+    load16_a2(bp + g.oA, f.A);
+    load16_a2(bp + g.oB, f.B);
+    load16_a2(bp + g.oQ, f.Q);
+    load8_a2(bp + g.oS, f.S0, f.S1);
     const uintptr_t da = reinterpret_cast<uintptr_t>(bp + 208);
     const uint32_t dw = *reinterpret_cast<const uint32_t*>(da & ~uintptr_t(3));
     f.dbits = dw >> ((da & 3u) * 8u);
   }
 
   __device__ __forceinline__ float compute(const Frag& f) const {
-    return q6k_group_dot(f.A0, f.A1, f.B0, f.B1, f.Q0, f.Q1, f.S0, f.S1, f.dbits, &x[0][0], sx32,
-                         sshift);
+    return q6k_unit_dot(f.A, f.B, f.Q, f.S0, f.S1, f.dbits, x, sx32, g.sshift);
   }
 
   __device__ __forceinline__ float row(const uint8_t* rp) const {
@@ -402,7 +428,7 @@ struct UnitQ40 {
 struct UnitChain {
   static constexpr bool kMixed = true;
   bool q6;         // set from the phase's format before setup()
-  float x[64];     // Q4_K: xa = x[0..31], xb = x[32..63]; Q6_K: x[8a + i]
+  float x[64];     // Q4_K: xa = x[0..31], xb = x[32..63]; Q6_K: x[16a + i]
   float s[4];      // Q4_K: sxa, sxb; Q6_K: sx32[0..3]
   uint32_t off, o1, o2, o3, o4, sh;
   bool hi;
@@ -429,25 +455,15 @@ struct UnitChain {
 
   template <class XU>
   __device__ __forceinline__ void setup_q6k(int u, const XU& xu) {
-    const int kb = u >> 3, h = (u >> 2) & 1, jj = u & 3;
-    off = static_cast<uint32_t>(kb) * 210u;
-    o1 = 64u * h + 8u * jj;
-    o2 = 64u * h + 32u + 8u * jj;
-    o3 = 128u + 32u * h + 8u * jj;
-    o4 = 192u + 8u * h;
-    sh = 8u * static_cast<uint32_t>(jj >> 1);
-#pragma unroll
-    for (int a = 0; a < 4; ++a) {
-      float t = 0.f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float v = xu(8 * a + i);
-        t += v;
-        const int pos = (i & 3) == 0 ? 0 : (i & 3) == 1 ? 8 : 16;
-        x[8 * a + i] = v * exp2i(kE - pos);
-      }
-      s[a] = t * exp2i(5 - 60);
-    }
+    Q6kUnitGeom g;
+    g.set(u);
+    off = g.off;
+    o1 = g.oA;
+    o2 = g.oB;
+    o3 = g.oQ;
+    o4 = g.oS;
+    sh = g.sshift;
+    q6k_setup_x(xu, x, s);
   }
 
   template <class XU>
@@ -484,14 +500,14 @@ struct UnitChain {
 
   __device__ __forceinline__ float row_q6k(const uint8_t* rp) const {
     const uint8_t* bp = rp + off;
-    uint32_t A0, A1, B0, B1, Q0, Q1, S0, S1;
-    load8_a2(bp + o1, A0, A1);
-    load8_a2(bp + o2, B0, B1);
-    load8_a2(bp + o3, Q0, Q1);
+    uint32_t A[4], B[4], Q[4], S0, S1;
+    load16_a2(bp + o1, A);
+    load16_a2(bp + o2, B);
+    load16_a2(bp + o3, Q);
     load8_a2(bp + o4, S0, S1);
     const uintptr_t da = reinterpret_cast<uintptr_t>(bp + 208);
     const uint32_t dw = *reinterpret_cast<const uint32_t*>(da & ~uintptr_t(3));
-    return q6k_group_dot(A0, A1, B0, B1, Q0, Q1, S0, S1, dw >> ((da & 3u) * 8u), x, s, sh);
+    return q6k_unit_dot(A, B, Q, S0, S1, dw >> ((da & 3u) * 8u), x, s, sh);
   }
 };
 

@@ -70,9 +70,9 @@ def test_matvec_shapes(lib):
 
 
 def test_q6k_lane_limit(lib):
-    # Q6_K lanes own 32 columns: batch 8 x 2560 columns needs 640 lanes, and a
-    # column split of a 10-block Q6_K row is not 16-byte aligned
-    assert lib.qws_q6k_matvec(A, A, A, 10, 2560, 8, None) == SHAPE
+    # lanes own 64 columns: batch 9 x 2560 columns needs 360 lanes, and a
+    # column split of a 10-block Q6_K row (2100 B) is not 16-byte aligned
+    assert lib.qws_q6k_matvec(A, A, A, 10, 2560, 9, None) == SHAPE
 
 
 def test_matvec_alignment(lib):

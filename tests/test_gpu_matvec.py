@@ -148,7 +148,7 @@ def test_zero_activation_gives_zero():
 
 @pytest.mark.parametrize("fmt,batch", [(oracle.Q4_K, 2), (oracle.Q4_K, 3), (oracle.Q4_K, 8),
                                        (oracle.Q4_0, 2), (oracle.Q4_0, 8), (oracle.Q6_K, 2),
-                                       (oracle.Q6_K, 4)])
+                                       (oracle.Q6_K, 4), (oracle.Q6_K, 8)])
 def test_batched_matvec(fmt, batch):
     rows, hidden = 333, 2560
     g = synth.rng(1007, fmt, batch)
