@@ -442,9 +442,9 @@ __device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const 
   } else if (kind == PH_O) {
     ok = stage_gather<8>(R, US, p.v, prev, kp.K, p.head_dim, p.n_q_heads / p.n_kv_heads, ctid);
   } else if (q6) {
-    ok = stage_stamped<UnitQ6K, 32>(R, US, p.m, prev, kp.K, ctid);
+    ok = stage_stamped<UnitQ6K, 16>(R, US, p.m, prev, kp.K, ctid);
   } else {
-    ok = stage_stamped<UnitQ4K, 32>(R, US, p.m, prev, kp.K, ctid);
+    ok = stage_stamped<UnitQ4K, 16>(R, US, p.m, prev, kp.K, ctid);
   }
   bar_sync(kConsumerBar, C);
   // this CTA has read everything its prologue needed
