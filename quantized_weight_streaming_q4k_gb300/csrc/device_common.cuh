@@ -98,6 +98,17 @@ __device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32
       : "memory");
 }
 
+// Programmatic dependent launch.  launch_dependents lets the next kernel of
+// the stream (launched with programmatic serialization) start now: its CTAs
+// take SMs as ours leave, and its weight copies need nothing from us.  wait
+// blocks until the previous kernel of the stream has completed and its memory
+// is visible; every thread that reads or writes global data another kernel
+// touches calls it first.  Both are no-ops without a programmatic dependency.
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // Named barrier over `nthreads` threads that also ORs a predicate across them.
 __device__ __forceinline__ bool bar_sync_or(int id, int nthreads, bool pred) {
   uint32_t r;

@@ -34,6 +34,7 @@ template <class Unit, class Epi>
 __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers)
     matvec_kernel(const __grid_constant__ MatvecParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  pdl_launch_dependents();
   const Ring R = make_ring(smem, p.S, p.stage_bytes, p.red_floats, p.xs_floats);
   const int C = static_cast<int>(blockDim.x) - kRoleThreads;
   // this CTA's column slice
@@ -49,10 +50,13 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers)
   __syncthreads();
   RingPos pos;
   if (threadIdx.x < kProducerThreads) {
+    // weights are never written by another kernel: stream them right away
     if (threadIdx.x == 0) run_producer(OnePhase{P}, R, &g_err_matvec);
   } else if (threadIdx.x < kRoleThreads) {
+    pdl_wait();   // y may still be read by the previous kernel
     reduce_phase(P, R, pos, Epi{}, &g_err_matvec);
   } else {
+    pdl_wait();   // x may come from the previous kernel
     consume_phase<Unit>(P, R, pos, XOfPlain{p.x + slice * p.x_slice_off, p.x_stride},
                         static_cast<int>(threadIdx.x) - kRoleThreads, C, &g_err_matvec);
   }
@@ -60,6 +64,8 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers)
 
 __global__ void splitk_reduce_kernel(const float* __restrict__ part, float* __restrict__ y,
                                      int64_t n, int splits) {
+  pdl_launch_dependents();
+  pdl_wait();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     float acc = part[i];
@@ -76,6 +82,8 @@ __global__ void __launch_bounds__(1024) rms_norm_kernel(const float* __restrict_
                                                         float eps) {
   __shared__ float wsum[32];
   __shared__ float inv_s;
+  pdl_launch_dependents();
+  pdl_wait();
   const float* xb = x + blockIdx.x * n;
   float* yb = y + blockIdx.x * n;
   float ss = 0.f;
@@ -95,12 +103,32 @@ __global__ void __launch_bounds__(1024) rms_norm_kernel(const float* __restrict_
 
 __global__ void residual_add_kernel(float* __restrict__ h, const float* __restrict__ y,
                                     int64_t n) {
+  pdl_launch_dependents();
+  pdl_wait();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < n;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x)
     h[i] += y[i];
 }
 
 // ------------------------------------------------------------------ host side
+// Launch with programmatic stream serialization: the kernel may start while
+// the previous kernel of the stream finishes (see pdl_wait / pdl_launch_dependents).
+template <class... KArgs, class... Args>
+static cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int threads, size_t smem,
+                              cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 int device_sms() {
   static int cache[64] = {0};
   int dev = 0;
@@ -155,8 +183,7 @@ template <class Unit, class Epi>
 static cudaError_t launch_one(const MatvecParams& p, int threads, size_t smem, int grid,
                               cudaStream_t st) {
   blocks_per_sm<Unit, Epi>(threads, smem);  // makes sure the smem opt-in is set
-  matvec_kernel<Unit, Epi><<<grid, threads, smem, st>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(matvec_kernel<Unit, Epi>, grid, threads, smem, st, p);
 }
 
 cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uint8_t* W2,
@@ -237,16 +264,14 @@ cudaError_t launch_splitk_reduce(const float* part, float* y, int64_t n, int spl
                                  cudaStream_t st) {
   const int threads = 256;
   const int64_t blocks = std::min<int64_t>((n + threads - 1) / threads, 4 * device_sms());
-  splitk_reduce_kernel<<<static_cast<int>(std::max<int64_t>(blocks, 1)), threads, 0, st>>>(
-      part, y, n, splits);
-  return cudaGetLastError();
+  return launch_pdl(splitk_reduce_kernel, static_cast<int>(std::max<int64_t>(blocks, 1)), threads,
+                    0, st, part, y, n, splits);
 }
 
 cudaError_t launch_rms_norm(const float* x, const float* w, float* y, int64_t n, float eps,
                             int batch, cudaStream_t st) {
   const int threads = n >= 1024 ? 1024 : static_cast<int>((n + 31) / 32 * 32);
-  rms_norm_kernel<<<batch, threads, 0, st>>>(x, w, y, n, eps);
-  return cudaGetLastError();
+  return launch_pdl(rms_norm_kernel, batch, threads, 0, st, x, w, y, n, eps);
 }
 
 cudaError_t launch_residual_add(float* h, const float* y, int64_t n, int batch,
@@ -254,9 +279,8 @@ cudaError_t launch_residual_add(float* h, const float* y, int64_t n, int batch,
   const int64_t total = n * batch;
   const int threads = 256;
   const int64_t blocks = std::min<int64_t>((total + threads - 1) / threads, 4 * device_sms());
-  residual_add_kernel<<<static_cast<int>(std::max<int64_t>(blocks, 1)), threads, 0, st>>>(h, y,
-                                                                                          total);
-  return cudaGetLastError();
+  return launch_pdl(residual_add_kernel, static_cast<int>(std::max<int64_t>(blocks, 1)), threads,
+                    0, st, h, y, total);
 }
 
 unsigned read_clear_matvec_errors() {
