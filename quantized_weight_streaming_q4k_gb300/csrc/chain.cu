@@ -149,10 +149,13 @@ struct ChainPhases {
     auto dst = [](Word* w) { return reinterpret_cast<float*>(w); };
     for (int i = 0; i < kMaxSeg; ++i) P.seg[i] = Seg{nullptr, nullptr, 0, 0};
     if (kind == PH_QKV) {
+      // v first: at sequence length 1 the O phase needs only v, and v's tiles
+      // are then dealt in the first round, finished before the CTAs' last
+      // tiles (q and k feed nothing downstream)
       P.nseg = 3;
-      P.seg[0] = Seg{L.Wq, dst(p->q), p->QD, static_cast<int>((p->QD + kp.T - 1) / kp.T)};
+      P.seg[0] = Seg{L.Wv, dst(p->v), p->KD, static_cast<int>((p->KD + kp.T - 1) / kp.T)};
       P.seg[1] = Seg{L.Wk, dst(p->k), p->KD, static_cast<int>((p->KD + kp.T - 1) / kp.T)};
-      P.seg[2] = Seg{L.Wv, dst(p->v), p->KD, static_cast<int>((p->KD + kp.T - 1) / kp.T)};
+      P.seg[2] = Seg{L.Wq, dst(p->q), p->QD, static_cast<int>((p->QD + kp.T - 1) / kp.T)};
     } else if (kind == PH_O) {
       P.seg[0] = Seg{L.Wo, dst(p->o), p->H, static_cast<int>((p->H + kp.T - 1) / kp.T)};
     } else if (kind == PH_GU) {
