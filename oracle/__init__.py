@@ -97,6 +97,12 @@ def _load():
         lib.qo_attn_seq1.argtypes = [P, I, I, I, P]
         lib.qo_ffn.restype = I
         lib.qo_ffn.argtypes = [I, P, P, I, P, I64, I64, P, P, P, P, P, P]
+        lib.qo_ffn_act.restype = I
+        lib.qo_ffn_act.argtypes = [I, I, P, P, I, P, I64, I64, P, P, P, P, P, P]
+        lib.qo_silu.restype = C.c_double
+        lib.qo_silu.argtypes = [C.c_double]
+        lib.qo_residual_rms_norm.restype = None
+        lib.qo_residual_rms_norm.argtypes = [P, P, P, I64, C.c_double, P]
         lib.qo_layer_forward.restype = I
         lib.qo_layer_forward.argtypes = [C.POINTER(_Layer), C.POINTER(_Dims), P, P,
                                          C.POINTER(_Trace)]
@@ -223,17 +229,38 @@ def attn_seq1(v, n_q_heads: int, n_kv_heads: int, head_dim: int) -> np.ndarray:
     return out
 
 
-def ffn(fmt_gu: int, Wg, Wu, fmt_d: int, Wd, hidden: int, inter: int, x) -> dict:
-    """Gated FFN; returns dict with g, u, m (= gelu(g) u), y and bound_y."""
+ACT_GELU_TANH, ACT_SILU = 0, 1
+
+
+def silu(t):
+    lib = _load()
+    arr = np.asarray(t, dtype=np.float64)
+    out = np.array([lib.qo_silu(float(v)) for v in arr.reshape(-1)], dtype=np.float64)
+    return out.reshape(arr.shape) if arr.ndim else float(out[0])
+
+
+def residual_rms_norm(h, y, w, eps: float):
+    """h + y and rms_norm(h + y, w): returns (h_new, x)."""
+    hs = _f64(h).reshape(-1).copy()
+    ys, ws = _f64(y).reshape(-1), _f64(w).reshape(-1)
+    assert hs.size == ys.size == ws.size
+    x = np.empty_like(hs)
+    _load().qo_residual_rms_norm(_ptr(hs), _ptr(ys), _ptr(ws), hs.size, float(eps), _ptr(x))
+    return hs, x
+
+
+def ffn(fmt_gu: int, Wg, Wu, fmt_d: int, Wd, hidden: int, inter: int, x,
+        act: int = ACT_GELU_TANH) -> dict:
+    """Gated FFN; returns dict with g, u, m (= act(g) u), y and bound_y."""
     wg, wu, wd = _u8(Wg), _u8(Wu), _u8(Wd)
     xs = _f64(x).reshape(-1)
     assert xs.size == hidden
     out = {k: np.empty(inter) for k in ("g", "u", "m")}
     out["y"] = np.empty(hidden)
     out["bound_y"] = np.empty(hidden)
-    rc = _load().qo_ffn(fmt_gu, _ptr(wg), _ptr(wu), fmt_d, _ptr(wd), hidden, inter, _ptr(xs),
-                        _ptr(out["g"]), _ptr(out["u"]), _ptr(out["m"]), _ptr(out["y"]),
-                        _ptr(out["bound_y"]))
+    rc = _load().qo_ffn_act(act, fmt_gu, _ptr(wg), _ptr(wu), fmt_d, _ptr(wd), hidden, inter,
+                            _ptr(xs), _ptr(out["g"]), _ptr(out["u"]), _ptr(out["m"]),
+                            _ptr(out["y"]), _ptr(out["bound_y"]))
     if rc:
         raise ValueError(f"qo_ffn failed ({rc})")
     return out

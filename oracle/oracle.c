@@ -28,6 +28,8 @@
 
 #define QO_Q4_0 2
 #define QO_Q4_K 12
+#define QO_ACT_GELU_TANH 0
+#define QO_ACT_SILU 1
 #define QO_Q6_K 14
 
 /* ---------------------------------------------------------------------------
@@ -247,6 +249,16 @@ double qo_gelu_tanh(double t)
 }
 
 /* ---------------------------------------------------------------------------
+ * SiLU ([compute] §Shaders: the SiLU-gated down variant for SiLU models;
+ * [perf] §Activation Function Support): silu(t) = t * sigmoid(t)
+ *   = t / (1 + exp(-t)).
+ * ------------------------------------------------------------------------- */
+double qo_silu(double t)
+{
+    return t / (1.0 + exp(-t));
+}
+
+/* ---------------------------------------------------------------------------
  * RMS norm ([compute] §Shaders "rms_norm"; [engine] §Key Components
  * residual.rs): y_i = x_i / sqrt(mean_j x_j^2 + eps) * w_i.
  * The weight multiplies as given (no 1 + w offset).
@@ -263,6 +275,15 @@ void qo_rms_norm(const double *x, const double *w, int64_t n, double eps, double
 void qo_residual_add(double *h, const double *y, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i) h[i] += y[i];
+}
+
+/* residual_norm ([compute] §Shaders "residual_norm"): the residual add
+ * followed by the RMS norm of its result, h <- h + y, x = rms_norm(h, w). */
+void qo_residual_rms_norm(double *h, const double *y, const double *w, int64_t n, double eps,
+                          double *x)
+{
+    qo_residual_add(h, y, n);
+    qo_rms_norm(h, w, n, eps, x);
 }
 
 /* ---------------------------------------------------------------------------
@@ -285,17 +306,20 @@ int qo_attn_seq1(const double *v, int n_q_heads, int n_kv_heads, int head_dim, d
 
 /* ---------------------------------------------------------------------------
  * Gated FFN ([compute] §Shaders "Q4_K fused FFN": q4k_ffn_gate_up then
- * q4k_geglu_gelu_tanh_down; [engine] §WalkFfn steps 1-3: gate and up
- * projections, GEGLU, then the down projection).
+ * q4k_geglu_gelu_tanh_down, or the SiLU-gated variant; [engine] §WalkFfn
+ * steps 1-3: gate and up projections, the gated activation, then the down
+ * projection).
  *   g = Wg x,  u = Wu x            (inter rows, hidden columns)
- *   m_j = gelu_tanh(g_j) * u_j     (the gate takes the activation)
+ *   m_j = act(g_j) * u_j           (the gate takes the activation: gelu_tanh
+ *                                   for act = QO_ACT_GELU_TANH, silu for
+ *                                   QO_ACT_SILU)
  *   y = Wd m                       (hidden rows, inter columns)
  *   bound_y[i] = sum_j |wd[i][j] * m_j|
  * Any of the outputs except y may be NULL.
  * ------------------------------------------------------------------------- */
-int qo_ffn(int fmt_gu, const uint8_t *Wg, const uint8_t *Wu, int fmt_d, const uint8_t *Wd,
-           int64_t hidden, int64_t inter, const double *x,
-           double *g, double *u, double *m, double *y, double *bound_y)
+int qo_ffn_act(int act, int fmt_gu, const uint8_t *Wg, const uint8_t *Wu, int fmt_d,
+               const uint8_t *Wd, int64_t hidden, int64_t inter, const double *x,
+               double *g, double *u, double *m, double *y, double *bound_y)
 {
     double *gg = (double *)malloc(sizeof(double) * (size_t)inter);
     double *uu = (double *)malloc(sizeof(double) * (size_t)inter);
@@ -306,7 +330,8 @@ int qo_ffn(int fmt_gu, const uint8_t *Wg, const uint8_t *Wu, int fmt_d, const ui
     if (rc) goto done;
     rc = qo_matvec(fmt_gu, Wu, inter, hidden, x, 1, 0, inter, uu, NULL);
     if (rc) goto done;
-    for (int64_t j = 0; j < inter; ++j) mm[j] = qo_gelu_tanh(gg[j]) * uu[j];
+    for (int64_t j = 0; j < inter; ++j)
+        mm[j] = (act == QO_ACT_SILU ? qo_silu(gg[j]) : qo_gelu_tanh(gg[j])) * uu[j];
     rc = qo_matvec(fmt_d, Wd, hidden, inter, mm, 1, 0, hidden, y, bound_y);
     if (rc) goto done;
     if (g) memcpy(g, gg, sizeof(double) * (size_t)inter);
@@ -317,6 +342,15 @@ done:
     free(uu);
     free(mm);
     return rc;
+}
+
+/* The GELU-gated FFN of the Gemma chain. */
+int qo_ffn(int fmt_gu, const uint8_t *Wg, const uint8_t *Wu, int fmt_d, const uint8_t *Wd,
+           int64_t hidden, int64_t inter, const double *x,
+           double *g, double *u, double *m, double *y, double *bound_y)
+{
+    return qo_ffn_act(QO_ACT_GELU_TANH, fmt_gu, Wg, Wu, fmt_d, Wd, hidden, inter, x, g, u, m, y,
+                      bound_y);
 }
 
 /* ---------------------------------------------------------------------------

@@ -144,6 +144,47 @@ def test_gelu_tanh_derivative_at_zero_is_half():
     assert abs((oracle.gelu_tanh(h) - oracle.gelu_tanh(-h)) / (2 * h) - 0.5) < 1e-9
 
 
+def test_silu_identities_and_logistic():
+    # silu(t) = t * logistic(t): silu(t) - silu(-t) = t; silu(0) = 0; slope 1/2 at 0
+    from scipy.special import expit
+    assert oracle.silu(0.0) == 0.0
+    for t in (0.1, 0.5, 1.0, 2.5, 7.0, 30.0):
+        assert abs(oracle.silu(t) - oracle.silu(-t) - t) <= 4e-16 * max(1.0, t)
+    ts = np.linspace(-30, 30, 601)
+    assert np.allclose(oracle.silu(ts), ts * expit(ts), rtol=1e-14, atol=1e-300)
+    h = 1e-6
+    assert abs((oracle.silu(h) - oracle.silu(-h)) / (2 * h) - 0.5) < 1e-9
+    assert oracle.silu(-800.0) == 0.0 or abs(oracle.silu(-800.0)) < 1e-300
+
+
+def test_ffn_silu_matches_dense_composition():
+    hidden, inter = 256, 512
+    g = synth.rng(22)
+    Wg = synth.q4_k_matrix(g, inter, hidden)
+    Wu = synth.q4_k_matrix(g, inter, hidden)
+    Wd = synth.q6_k_matrix(g, hidden, inter)
+    x = synth.unit_rms_vector(g, hidden).astype(np.float64)
+    out = oracle.ffn(oracle.Q4_K, Wg, Wu, oracle.Q6_K, Wd, hidden, inter, x, act=oracle.ACT_SILU)
+    gd = oracle.dequant(oracle.Q4_K, Wg, inter, hidden) @ x
+    ud = oracle.dequant(oracle.Q4_K, Wu, inter, hidden) @ x
+    m = gd / (1.0 + np.exp(-gd)) * ud
+    Dd = oracle.dequant(oracle.Q6_K, Wd, hidden, inter)
+    assert np.allclose(out["m"], m, rtol=1e-12, atol=1e-300)
+    assert np.all(np.abs(out["y"] - Dd @ m) <= 1e-11 * (np.abs(Dd) @ np.abs(m)))
+
+
+def test_residual_rms_norm_is_add_then_norm():
+    n, eps = 2560, 1e-6
+    g = synth.rng(23)
+    h = synth.normal_vector(g, n).astype(np.float64)
+    y = synth.normal_vector(g, n).astype(np.float64)
+    w = synth.norm_weights(g, n).astype(np.float64)
+    h2, x = oracle.residual_rms_norm(h, y, w, eps)
+    assert np.array_equal(h2, h + y)
+    r = h + y
+    assert np.allclose(x, r / np.sqrt(np.mean(r * r) + eps) * w, rtol=1e-14)
+
+
 # ---------------------------------------------------------------- rms_norm
 def test_rms_norm_one_hot_and_constant():
     n, eps = 2560, 1e-6
