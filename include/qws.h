@@ -141,6 +141,22 @@ qws_status qws_q4k_ffn_gate_up_geglu(const void* Wg, const void* Wu, const float
                                      int64_t hidden, int64_t inter, qws_stream stream);
 
 /* ------------------------------------------------------------------------
+ * The SiLU-gated FFN for SiLU models (infer-compute README §Shaders, the
+ * SiLU-gated down variant; infer-inference PERFORMANCE.md §Activation
+ * Function Support): as qws_q4k_ffn_gate_up_geglu_down with
+ *   m = silu(g) * u,   silu(t) = t / (1 + exp(-t)).
+ * Arguments, layouts, workspace and errors as the GELU entry points.
+ * ---------------------------------------------------------------------- */
+qws_status qws_q4k_ffn_gate_up_silu_down(const void* Wg, const void* Wu, const void* Wd,
+                                         qws_format wd_fmt, const float* x, float* y,
+                                         int64_t hidden, int64_t inter, void* ws,
+                                         size_t ws_bytes, qws_stream stream);
+
+/* First half of the SiLU FFN alone: m = silu(Wg x) * (Wu x), m [inter]. */
+qws_status qws_q4k_ffn_gate_up_silu(const void* Wg, const void* Wu, const float* x, float* m,
+                                    int64_t hidden, int64_t inter, qws_stream stream);
+
+/* ------------------------------------------------------------------------
  * The gated FFN above for callers that cannot allocate device memory.  The
  * pages have no counterpart; this is a convenience of this library.  It is for
  * callers that may not allocate at call time and have no spare device buffer
@@ -174,6 +190,16 @@ qws_status qws_q4k_ffn_gate_up_geglu_down_noalloc(const void* Wg, const void* Wu
 qws_status qws_rms_norm(const float* x, const float* w, float* y, int64_t n, float eps,
                         int batch, qws_stream stream);
 qws_status qws_residual_add(float* h, const float* y, int64_t n, int batch, qws_stream stream);
+
+/* ------------------------------------------------------------------------
+ * residual_norm (infer-compute README §Shaders "residual_norm"): the residual
+ * add and the RMS norm of its result in one launch:
+ *   h[b][i] += y[b][i];   x[b][i] = h[b][i] / sqrt(mean_j h[b][j]^2 + eps) * w[i]
+ * h (in/out), y, x [batch][n], w [n] f32 (device, 4-byte aligned); x must not
+ * alias h or y.  n > 0, 1 <= batch <= 65535, eps >= 0; errors as rms_norm.
+ * ---------------------------------------------------------------------- */
+qws_status qws_residual_rms_norm(float* h, const float* y, const float* w, float* x, int64_t n,
+                                 float eps, int batch, qws_stream stream);
 
 /* ------------------------------------------------------------------------
  * Decoder chain at sequence length 1 (infer-compute README §Architecture:

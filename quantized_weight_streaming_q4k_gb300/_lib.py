@@ -49,6 +49,9 @@ SIGNATURES = {
     "qws_q4k_ffn_gate_up_geglu_down": (I, [P, P, P, I, F, F, I64, I64, P, SZ, P]),
     "qws_q4k_ffn_gate_up_geglu": (I, [P, P, F, F, I64, I64, P]),
     "qws_q4k_ffn_gate_up_geglu_down_noalloc": (I, [P, P, P, I, F, F, I64, I64, P]),
+    "qws_q4k_ffn_gate_up_silu_down": (I, [P, P, P, I, F, F, I64, I64, P, SZ, P]),
+    "qws_q4k_ffn_gate_up_silu": (I, [P, P, F, F, I64, I64, P]),
+    "qws_residual_rms_norm": (I, [F, F, F, F, I64, C.c_float, I, P]),
     "qws_rms_norm": (I, [F, F, F, I64, C.c_float, I, P]),
     "qws_residual_add": (I, [F, F, I64, I, P]),
     "qws_decode_chain": (I, [C.POINTER(QwsLayer), I, F, C.POINTER(QwsDims), P, SZ, P]),

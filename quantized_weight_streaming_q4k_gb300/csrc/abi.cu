@@ -198,9 +198,11 @@ static qws_status check_ffn_shape(const char* fn, int64_t hidden, int64_t inter)
   return QWS_OK;
 }
 
-qws_status qws_q4k_ffn_gate_up_geglu(const void* Wg, const void* Wu, const float* x, float* m,
-                                     int64_t hidden, int64_t inter, qws_stream stream) {
-  const char* fn = "qws_q4k_ffn_gate_up_geglu";
+namespace {
+
+// The gated FFN's first launch: m = act(Wg x) * (Wu x), act by epilogue.
+qws_status ffn_gate_up(const char* fn, int epi, const void* Wg, const void* Wu, const float* x,
+                       float* m, int64_t hidden, int64_t inter, qws_stream stream) {
   QWS_CHECK_W(Wg);
   QWS_CHECK_W(Wu);
   QWS_CHECK_F(x);
@@ -209,18 +211,17 @@ qws_status qws_q4k_ffn_gate_up_geglu(const void* Wg, const void* Wu, const float
   if (rc != QWS_OK) return rc;
   qws::Seg seg{static_cast<const uint8_t*>(Wg), m, inter, 0};
   std::string why;
-  cudaError_t e = qws::launch_matvec(QWS_Q4_K, qws::EPI_GEGLU, &seg, 1,
-                                     static_cast<const uint8_t*>(Wu), x, hidden, 1, 1,
-                                     reinterpret_cast<cudaStream_t>(stream), &why);
+  cudaError_t e = qws::launch_matvec(QWS_Q4_K, epi, &seg, 1, static_cast<const uint8_t*>(Wu), x,
+                                     hidden, 1, 1, reinterpret_cast<cudaStream_t>(stream), &why);
   if (e != cudaSuccess) return cuda_fail(e, fn, why);
   return ok();
 }
 
-qws_status qws_q4k_ffn_gate_up_geglu_down(const void* Wg, const void* Wu, const void* Wd,
-                                          qws_format wd_fmt, const float* x, float* y,
-                                          int64_t hidden, int64_t inter, void* ws,
-                                          size_t ws_bytes, qws_stream stream) {
-  const char* fn = "qws_q4k_ffn_gate_up_geglu_down";
+// The whole gated FFN: the first launch into the workspace, then the down
+// projection.
+qws_status ffn_full(const char* fn, int epi, const void* Wg, const void* Wu, const void* Wd,
+                    qws_format wd_fmt, const float* x, float* y, int64_t hidden, int64_t inter,
+                    void* ws, size_t ws_bytes, qws_stream stream) {
   QWS_CHECK_W(Wg);
   QWS_CHECK_W(Wu);
   QWS_CHECK_W(Wd);
@@ -238,13 +239,43 @@ qws_status qws_q4k_ffn_gate_up_geglu_down(const void* Wg, const void* Wu, const 
   float* m = static_cast<float*>(ws);
   qws::Seg seg{static_cast<const uint8_t*>(Wg), m, inter, 0};
   std::string why;
-  cudaError_t e = qws::launch_matvec(QWS_Q4_K, qws::EPI_GEGLU, &seg, 1,
-                                     static_cast<const uint8_t*>(Wu), x, hidden, 1, 1, st, &why);
+  cudaError_t e = qws::launch_matvec(QWS_Q4_K, epi, &seg, 1, static_cast<const uint8_t*>(Wu), x,
+                                     hidden, 1, 1, st, &why);
   if (e != cudaSuccess) return cuda_fail(e, fn, why);
   qws::Seg dseg{static_cast<const uint8_t*>(Wd), y, hidden, 0};
   e = qws::launch_matvec(wd_fmt, qws::EPI_STORE, &dseg, 1, nullptr, m, inter, 1, 1, st, &why);
   if (e != cudaSuccess) return cuda_fail(e, fn, why);
   return ok();
+}
+
+}  // namespace
+
+qws_status qws_q4k_ffn_gate_up_geglu(const void* Wg, const void* Wu, const float* x, float* m,
+                                     int64_t hidden, int64_t inter, qws_stream stream) {
+  return ffn_gate_up("qws_q4k_ffn_gate_up_geglu", qws::EPI_GEGLU, Wg, Wu, x, m, hidden, inter,
+                     stream);
+}
+
+qws_status qws_q4k_ffn_gate_up_geglu_down(const void* Wg, const void* Wu, const void* Wd,
+                                          qws_format wd_fmt, const float* x, float* y,
+                                          int64_t hidden, int64_t inter, void* ws,
+                                          size_t ws_bytes, qws_stream stream) {
+  return ffn_full("qws_q4k_ffn_gate_up_geglu_down", qws::EPI_GEGLU, Wg, Wu, Wd, wd_fmt, x, y,
+                  hidden, inter, ws, ws_bytes, stream);
+}
+
+qws_status qws_q4k_ffn_gate_up_silu(const void* Wg, const void* Wu, const float* x, float* m,
+                                    int64_t hidden, int64_t inter, qws_stream stream) {
+  return ffn_gate_up("qws_q4k_ffn_gate_up_silu", qws::EPI_SWIGLU, Wg, Wu, x, m, hidden, inter,
+                     stream);
+}
+
+qws_status qws_q4k_ffn_gate_up_silu_down(const void* Wg, const void* Wu, const void* Wd,
+                                         qws_format wd_fmt, const float* x, float* y,
+                                         int64_t hidden, int64_t inter, void* ws,
+                                         size_t ws_bytes, qws_stream stream) {
+  return ffn_full("qws_q4k_ffn_gate_up_silu_down", qws::EPI_SWIGLU, Wg, Wu, Wd, wd_fmt, x, y,
+                  hidden, inter, ws, ws_bytes, stream);
 }
 
 qws_status qws_rms_norm(const float* x, const float* w, float* y, int64_t n, float eps,
@@ -271,6 +302,22 @@ qws_status qws_residual_add(float* h, const float* y, int64_t n, int batch, qws_
   if (n == 0) return ok();
   cudaError_t e =
       qws::launch_residual_add(h, y, n, batch, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn, "");
+  return ok();
+}
+
+qws_status qws_residual_rms_norm(float* h, const float* y, const float* w, float* x, int64_t n,
+                                 float eps, int batch, qws_stream stream) {
+  const char* fn = "qws_residual_rms_norm";
+  QWS_CHECK_F(h);
+  QWS_CHECK_F(y);
+  QWS_CHECK_F(w);
+  QWS_CHECK_F(x);
+  if (n <= 0) return fail(QWS_ERR_SHAPE, "%s: n = %lld <= 0", fn, (long long)n);
+  if (batch < 1 || batch > 65535) return fail(QWS_ERR_SHAPE, "%s: batch = %d", fn, batch);
+  if (!(eps >= 0.f)) return fail(QWS_ERR_SHAPE, "%s: eps must be >= 0", fn);
+  cudaError_t e = qws::launch_residual_rms_norm(h, y, w, x, n, eps, batch,
+                                                reinterpret_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, fn, "");
   return ok();
 }

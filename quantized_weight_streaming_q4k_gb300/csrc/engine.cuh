@@ -42,7 +42,7 @@ constexpr int kReducerThreads = 32;
 constexpr int kRoleThreads = kProducerThreads + kReducerThreads;  // consumers start here
 constexpr int kConsumerBar = 1;     // named barrier id used by the consumer threads
 
-enum : int { EPI_STORE = 0, EPI_GEGLU = 1 };
+enum : int { EPI_STORE = 0, EPI_GEGLU = 1, EPI_SWIGLU = 2 };   // GLU kinds read row pairs
 
 struct Seg {
   const uint8_t* W;   // packed rows of this segment
@@ -53,10 +53,10 @@ struct Seg {
 
 struct Phase {
   int fmt;            // 2 (Q4_0), 12 (Q4_K), 14 (Q6_K)
-  int epi;            // EPI_STORE or EPI_GEGLU
+  int epi;            // EPI_STORE, or a gated pair: EPI_GEGLU / EPI_SWIGLU
   int nseg;
   Seg seg[kMaxSeg];
-  const uint8_t* W2;  // EPI_GEGLU: up matrix, same shape as seg[0] (the gate)
+  const uint8_t* W2;  // gated pair: up matrix, same shape as seg[0] (the gate)
   int64_t K;          // columns (weights per row)
   int64_t row_bytes;
   int B;              // activation vectors (batch); x is [B][K], y is [B][rows]
@@ -197,7 +197,7 @@ __device__ __forceinline__ void fill_stage(const Phase& P, int t, const Ring& R,
   const uint32_t bytes = static_cast<uint32_t>(tr.nrows * P.row_bytes);
   const uint32_t bulk = bytes & ~15u;
   const uint8_t* g = tr.W + tr.r0 * P.row_bytes;
-  const bool pair = P.epi == EPI_GEGLU;
+  const bool pair = P.epi != EPI_STORE;
   const uint8_t* up = pair ? P.W2 + tr.r0 * P.row_bytes : nullptr;
   uint8_t* dst_up = dst + static_cast<size_t>(P.T) * P.row_bytes;
   if (P.row_stride != P.row_bytes) {
@@ -327,7 +327,7 @@ __device__ __forceinline__ bool consume_phase(const Phase& Pref, const Ring& Rre
   const int b = g / G, gg = g % G;
   const bool active = b < P.B;
   const int lane = ctid & 31;
-  const bool pair = P.epi == EPI_GEGLU;
+  const bool pair = P.epi != EPI_STORE;
   const int slots = pair ? 2 * P.T : P.T;      // partial rows per vector
   const size_t rb = static_cast<size_t>(P.row_bytes);
   Unit unit;
@@ -427,7 +427,7 @@ __device__ __forceinline__ bool reduce_phase(const Phase& Pref, const Ring& Rref
   if (cta < 0 || cta >= P.ncta) return true;
   const int lane = threadIdx.x & 31;
   const int U = P.U, US = red_stride(P.U);
-  const bool pair = P.epi == EPI_GEGLU;
+  const bool pair = P.epi != EPI_STORE;
   const int slots = pair ? 2 * P.T : P.T;
   for (int t = cta; t < P.n_tiles; t += P.ncta) {
     const uint32_t s = pos.s;
@@ -484,6 +484,17 @@ struct EpiGeglu {
   __device__ __forceinline__ void operator()(const Phase& P, const TileRef& tr, int b, int o,
                                              float g, float u) const {
     tr.y[b * tr.seg_rows + tr.r0 + o] = gelu_tanh(g) * u;
+  }
+};
+
+// SiLU, the logistic-gated variant for SiLU models (infer-compute README
+// §Shaders, the SiLU-gated down variant): silu(t) = t / (1 + exp(-t)).
+__device__ __forceinline__ float silu(float t) { return t / (1.0f + expf(-t)); }
+
+struct EpiSwiglu {
+  __device__ __forceinline__ void operator()(const Phase& P, const TileRef& tr, int b, int o,
+                                             float g, float u) const {
+    tr.y[b * tr.seg_rows + tr.r0 + o] = silu(g) * u;
   }
 };
 

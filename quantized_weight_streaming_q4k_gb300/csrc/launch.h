@@ -54,7 +54,7 @@ inline bool plan_tiles(int fmt, int epi, int64_t K, int B, int64_t rows_hint, in
     why = "batch * hidden / 64 exceeds 320 lanes";
     return false;
   }
-  const int pairm = epi == EPI_GEGLU ? 2 : 1;
+  const int pairm = epi != EPI_STORE ? 2 : 1;
   const int64_t align = 16 / gcd64(RB, 16);
   int64_t G = gmax, T0 = 0;
   for (; G >= 1; --G) {
@@ -101,6 +101,8 @@ cudaError_t launch_splitk_reduce(const float* part, float* y, int64_t n, int spl
 cudaError_t launch_rms_norm(const float* x, const float* w, float* y, int64_t n, float eps,
                             int batch, cudaStream_t st);
 cudaError_t launch_residual_add(float* h, const float* y, int64_t n, int batch, cudaStream_t st);
+cudaError_t launch_residual_rms_norm(float* h, const float* y, const float* w, float* x,
+                                    int64_t n, float eps, int batch, cudaStream_t st);
 unsigned read_clear_matvec_errors();
 
 // message returned by qws_last_error() on the calling thread (abi.cu)

@@ -101,6 +101,40 @@ __global__ void __launch_bounds__(1024) rms_norm_kernel(const float* __restrict_
   for (int64_t i = threadIdx.x; i < n; i += blockDim.x) yb[i] = xb[i] * inv * w[i];
 }
 
+// residual_norm: h <- h + y, then x = h / sqrt(mean(h^2) + eps) * w, one CTA
+// per vector, same fixed-order reduction as rms_norm_kernel.
+__global__ void __launch_bounds__(1024) residual_rms_norm_kernel(float* __restrict__ h,
+                                                                 const float* __restrict__ y,
+                                                                 const float* __restrict__ w,
+                                                                 float* __restrict__ x, int64_t n,
+                                                                 float eps) {
+  __shared__ float wsum[32];
+  __shared__ float inv_s;
+  pdl_launch_dependents();
+  pdl_wait();
+  float* hb = h + blockIdx.x * n;
+  const float* yb = y + blockIdx.x * n;
+  float* xb = x + blockIdx.x * n;
+  float ss = 0.f;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    const float r = hb[i] + yb[i];
+    hb[i] = r;
+    ss = fmaf(r, r, ss);
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) t += wsum[i];
+    inv_s = 1.0f / sqrtf(t / static_cast<float>(n) + eps);
+  }
+  __syncthreads();
+  const float inv = inv_s;
+  // each thread reads back the h values it wrote itself
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) xb[i] = hb[i] * inv * w[i];
+}
+
 __global__ void residual_add_kernel(float* __restrict__ h, const float* __restrict__ y,
                                     int64_t n) {
   pdl_launch_dependents();
@@ -234,11 +268,12 @@ cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uin
   const int threads = kRoleThreads + tp.C;
 
   int bps = 1;
-  switch (fmt * 2 + epi) {
-    case 12 * 2 + EPI_STORE: bps = blocks_per_sm<UnitQ4K, EpiStore>(threads, smem); break;
-    case 12 * 2 + EPI_GEGLU: bps = blocks_per_sm<UnitQ4K, EpiGeglu>(threads, smem); break;
-    case 14 * 2 + EPI_STORE: bps = blocks_per_sm<UnitQ6K, EpiStore>(threads, smem); break;
-    case 2 * 2 + EPI_STORE: bps = blocks_per_sm<UnitQ40, EpiStore>(threads, smem); break;
+  switch (fmt * 4 + epi) {
+    case 12 * 4 + EPI_STORE: bps = blocks_per_sm<UnitQ4K, EpiStore>(threads, smem); break;
+    case 12 * 4 + EPI_GEGLU: bps = blocks_per_sm<UnitQ4K, EpiGeglu>(threads, smem); break;
+    case 12 * 4 + EPI_SWIGLU: bps = blocks_per_sm<UnitQ4K, EpiSwiglu>(threads, smem); break;
+    case 14 * 4 + EPI_STORE: bps = blocks_per_sm<UnitQ6K, EpiStore>(threads, smem); break;
+    case 2 * 4 + EPI_STORE: bps = blocks_per_sm<UnitQ40, EpiStore>(threads, smem); break;
     default:
       if (why) *why = "unsupported format / epilogue";
       return cudaErrorInvalidValue;
@@ -252,10 +287,11 @@ cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uin
   P.cta0 = 0;
   P.ncta = p.cps;
   const int grid = static_cast<int>(cps * splits);
-  switch (fmt * 2 + epi) {
-    case 12 * 2 + EPI_STORE: return launch_one<UnitQ4K, EpiStore>(p, threads, smem, grid, st);
-    case 12 * 2 + EPI_GEGLU: return launch_one<UnitQ4K, EpiGeglu>(p, threads, smem, grid, st);
-    case 14 * 2 + EPI_STORE: return launch_one<UnitQ6K, EpiStore>(p, threads, smem, grid, st);
+  switch (fmt * 4 + epi) {
+    case 12 * 4 + EPI_STORE: return launch_one<UnitQ4K, EpiStore>(p, threads, smem, grid, st);
+    case 12 * 4 + EPI_GEGLU: return launch_one<UnitQ4K, EpiGeglu>(p, threads, smem, grid, st);
+    case 12 * 4 + EPI_SWIGLU: return launch_one<UnitQ4K, EpiSwiglu>(p, threads, smem, grid, st);
+    case 14 * 4 + EPI_STORE: return launch_one<UnitQ6K, EpiStore>(p, threads, smem, grid, st);
     default: return launch_one<UnitQ40, EpiStore>(p, threads, smem, grid, st);
   }
 }
@@ -272,6 +308,12 @@ cudaError_t launch_rms_norm(const float* x, const float* w, float* y, int64_t n,
                             int batch, cudaStream_t st) {
   const int threads = n >= 1024 ? 1024 : static_cast<int>((n + 31) / 32 * 32);
   return launch_pdl(rms_norm_kernel, batch, threads, 0, st, x, w, y, n, eps);
+}
+
+cudaError_t launch_residual_rms_norm(float* h, const float* y, const float* w, float* x,
+                                    int64_t n, float eps, int batch, cudaStream_t st) {
+  const int threads = n >= 1024 ? 1024 : static_cast<int>((n + 31) / 32 * 32);
+  return launch_pdl(residual_rms_norm_kernel, batch, threads, 0, st, h, y, w, x, n, eps);
 }
 
 cudaError_t launch_residual_add(float* h, const float* y, int64_t n, int batch,

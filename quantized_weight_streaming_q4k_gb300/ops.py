@@ -124,6 +124,38 @@ def q4k_ffn_gate_up_geglu_down(Wg, Wu, Wd, wd_fmt: int, x, hidden: int, inter: i
     return y
 
 
+def q4k_ffn_gate_up_silu(Wg, Wu, x, hidden: int, inter: int, out=None, stream=None):
+    m = _out(out, (inter,), x)
+    check(lib().qws_q4k_ffn_gate_up_silu(_dev(Wg, "Wg", torch.uint8), _dev(Wu, "Wu", torch.uint8),
+                                         _dev(x, "x", torch.float32), _dev(m, "m", torch.float32),
+                                         hidden, inter, stream_handle(stream)))
+    return m
+
+
+def q4k_ffn_gate_up_silu_down(Wg, Wu, Wd, wd_fmt: int, x, hidden: int, inter: int,
+                              workspace=None, out=None, stream=None):
+    y = _out(out, (hidden,), x)
+    need = workspace_bytes(OP_FFN, 0, hidden, inter, 1, 0)
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=x.device)
+    check(lib().qws_q4k_ffn_gate_up_silu_down(
+        _dev(Wg, "Wg", torch.uint8), _dev(Wu, "Wu", torch.uint8), _dev(Wd, "Wd", torch.uint8),
+        wd_fmt, _dev(x, "x", torch.float32), _dev(y, "y", torch.float32), hidden, inter,
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        stream_handle(stream)))
+    return y
+
+
+def residual_rms_norm(h, y, w, eps: float, batch: int = 1, out=None, stream=None):
+    """h += y (in place), returns x = rms_norm(h, w)."""
+    n = h.numel() // batch
+    x = _out(out, tuple(h.shape), h)
+    check(lib().qws_residual_rms_norm(_dev(h, "h", torch.float32), _dev(y, "y", torch.float32),
+                                      _dev(w, "w", torch.float32), _dev(x, "x", torch.float32), n,
+                                      float(eps), batch, stream_handle(stream)))
+    return x
+
+
 def rms_norm(x, w, eps: float, batch: int = 1, out=None, stream=None):
     y = _out(out, tuple(x.shape), x)
     n = x.numel() // batch

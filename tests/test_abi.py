@@ -114,6 +114,19 @@ def test_qkv_and_ffn_checks(lib):
     assert lib.qws_q4k_ffn_gate_up_geglu(A, A, A, None, 2560, 10240, None) == NULL
 
 
+def test_silu_ffn_and_residual_norm_checks(lib):
+    need = lib.qws_workspace_bytes(_lib.OP_FFN, 0, 2560, 10240, 1, 0)
+    assert lib.qws_q4k_ffn_gate_up_silu_down(A, A, A, 2, A, A, 2560, 10240, A, need, None) == FORMAT
+    assert lib.qws_q4k_ffn_gate_up_silu_down(A, A, A, 14, A, A, 2560, 10240, A, need - 4,
+                                             None) == WORKSPACE
+    assert lib.qws_q4k_ffn_gate_up_silu_down(A, A, A, 14, A, A, 2560, 1000, A, need,
+                                             None) == SHAPE
+    assert lib.qws_q4k_ffn_gate_up_silu(A, A, A, None, 2560, 10240, None) == NULL
+    assert lib.qws_residual_rms_norm(A, A, None, A, 10, C.c_float(1e-6), 1, None) == NULL
+    assert lib.qws_residual_rms_norm(A, A, A, A, 0, C.c_float(1e-6), 1, None) == SHAPE
+    assert lib.qws_residual_rms_norm(A, A, A, A, 10, C.c_float(-1.0), 1, None) == SHAPE
+
+
 def test_vector_op_checks(lib):
     assert lib.qws_rms_norm(A, None, A, 10, C.c_float(1e-6), 1, None) == NULL
     assert lib.qws_rms_norm(A, A, A, 0, C.c_float(1e-6), 1, None) == SHAPE

@@ -263,6 +263,52 @@ def test_ffn_full_size(fmt_d, scale):
     print(f"ffn: {n_second} of {H} elements passed on the cancellation clause")
 
 
+@pytest.mark.parametrize("hidden,inter,scale", [(2560, 10240, 1.0), (2560, 10240, 1e-2)])
+def test_gate_up_silu(hidden, inter, scale):
+    g = synth.rng(1018, hidden, inter, int(scale * 100))
+    Wg = synth.q4_k_matrix(g, inter, hidden)
+    Wu = synth.q4_k_matrix(g, inter, hidden)
+    x = (synth.unit_rms_vector(g, hidden) * np.float32(scale)).astype(np.float32)
+    m = host(ops.q4k_ffn_gate_up_silu(dev(Wg), dev(Wu), dev(x), hidden, inter))
+    gr, bg = oracle.matvec(oracle.Q4_K, Wg, inter, hidden, x, threads=THREADS)
+    ur, bu = oracle.matvec(oracle.Q4_K, Wu, inter, hidden, x, threads=THREADS)
+    act = oracle.silu(gr)
+    # m = silu(g) u;  |silu'| <= 1.1;  first-order propagation of 1e-5 * bound
+    tol = 1e-4 * np.abs(act * ur) + 1e-5 * (1.1 * bg * np.abs(ur) + np.abs(act) * bu)
+    err = np.abs(m - act * ur)
+    assert np.all(err <= tol), f"worst err/tol {np.max(err / tol):.3e}"
+
+
+@pytest.mark.parametrize("scale", [1.0, 1e-2])
+def test_ffn_silu_full_size(scale):
+    H, I = 2560, 10240
+    g = synth.rng(1019, int(scale * 100))
+    Wg = synth.q4_k_matrix(g, I, H)
+    Wu = synth.q4_k_matrix(g, I, H)
+    Wd = synth.q6_k_matrix(g, H, I)
+    x = (synth.unit_rms_vector(g, H) * np.float32(scale)).astype(np.float32)
+    y = host(ops.q4k_ffn_gate_up_silu_down(dev(Wg), dev(Wu), dev(Wd), ops.Q6_K, dev(x), H, I))
+    out = oracle.ffn(oracle.Q4_K, Wg, Wu, oracle.Q6_K, Wd, H, I, x, act=oracle.ACT_SILU)
+    _ffn_check(y, out, f"silu ffn x*{scale}")
+
+
+@pytest.mark.parametrize("n,batch", [(2560, 1), (10240, 1), (2560, 3), (7, 2)])
+def test_residual_rms_norm(n, batch):
+    g = synth.rng(1020, n, batch)
+    h = synth.normal_vector(g, n, batch)
+    y = synth.normal_vector(g, n, batch)
+    w = synth.norm_weights(g, n)
+    hd = dev(h)
+    x = host(ops.residual_rms_norm(hd, dev(y), dev(w), 1e-6, batch=batch))
+    hb = host(hd).reshape(batch, n)
+    for b in range(batch):
+        h_ref, x_ref = oracle.residual_rms_norm(h.reshape(batch, n)[b], y.reshape(batch, n)[b], w,
+                                                1e-6)
+        # the add is exact in f32 rounding; the norm within 1e-5 relative
+        assert np.array_equal(hb[b], h_ref.astype(np.float32).astype(np.float64))
+        assert np.all(np.abs(x.reshape(batch, n)[b] - x_ref) <= 1e-5 * np.abs(x_ref) + 1e-30)
+
+
 @pytest.mark.parametrize("n,batch", [(2560, 1), (10240, 1), (2560, 3), (7, 2)])
 def test_rms_norm(n, batch):
     g = synth.rng(1015, n, batch)
