@@ -19,9 +19,9 @@ from concurrent.futures import ThreadPoolExecutor
 
 import numpy as np
 
-Q4_0, Q4_K, Q6_K = 2, 12, 14
-BLOCK_WEIGHTS = {Q4_0: 32, Q4_K: 256, Q6_K: 256}
-BLOCK_BYTES = {Q4_0: 18, Q4_K: 144, Q6_K: 210}
+Q4_0, Q8_0, Q4_K, Q6_K = 2, 8, 12, 14
+BLOCK_WEIGHTS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q6_K: 256}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q4_K: 144, Q6_K: 210}
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "oracle.c")
@@ -78,7 +78,14 @@ def _load():
         P, I64, I = C.c_void_p, C.c_int64, C.c_int
         lib.qo_half.restype = C.c_double
         lib.qo_half.argtypes = [C.c_uint16]
-        for name in ("qo_dequant_q4_0", "qo_dequant_q4_k", "qo_dequant_q6_k"):
+        lib.qo_half_bits.restype = C.c_uint16
+        lib.qo_half_bits.argtypes = [C.c_float]
+        lib.qo_quantize_q8_0.restype = I
+        lib.qo_quantize_q8_0.argtypes = [P, I64, P]
+        lib.qo_matvec_q8.restype = I
+        lib.qo_matvec_q8.argtypes = [I, P, I64, I64, P, I, I64, I64, P, P]
+        for name in ("qo_dequant_q4_0", "qo_dequant_q8_0", "qo_dequant_q4_k",
+                     "qo_dequant_q6_k"):
             getattr(lib, name).restype = None
             getattr(lib, name).argtypes = [P, P]
         lib.qo_q4_k_scale_min.restype = None
@@ -134,7 +141,8 @@ def dequant_block(fmt: int, blk) -> np.ndarray:
     b = _u8(blk)
     assert b.size == BLOCK_BYTES[fmt]
     out = np.empty(BLOCK_WEIGHTS[fmt], dtype=np.float64)
-    name = {Q4_0: "qo_dequant_q4_0", Q4_K: "qo_dequant_q4_k", Q6_K: "qo_dequant_q6_k"}[fmt]
+    name = {Q4_0: "qo_dequant_q4_0", Q8_0: "qo_dequant_q8_0", Q4_K: "qo_dequant_q4_k",
+            Q6_K: "qo_dequant_q6_k"}[fmt]
     getattr(_load(), name)(_ptr(b), _ptr(out))
     return out
 
@@ -191,6 +199,58 @@ def matvec(fmt: int, W, rows: int, hidden: int, x, threads: int = 1,
             rcs = list(ex.map(lambda t: run(edges[t], edges[t + 1]), range(threads)))
     if any(rcs):
         raise ValueError(f"qo_matvec failed ({rcs})")
+    if squeeze:
+        return y[0], bound[0]
+    return y, bound
+
+
+def half_bits(f) -> int:
+    """f32 value -> binary16 bit pattern (nearest, ties to even)."""
+    return int(_load().qo_half_bits(float(np.float32(f))))
+
+
+def quantize_q8_0(x) -> np.ndarray:
+    """f32 activations [..., n] (n % 32 == 0) -> Q8_0 blocks, uint8
+    [..., n / 32 * 34]; the decisions are taken in f32."""
+    xs = np.ascontiguousarray(np.asarray(x, dtype=np.float32))
+    n = xs.shape[-1]
+    out = np.empty(xs.shape[:-1] + (n // 32 * 34,), dtype=np.uint8)
+    rc = _load().qo_quantize_q8_0(_ptr(xs), xs.size, _ptr(out))
+    if rc or n % 32:
+        raise ValueError(f"qo_quantize_q8_0 failed ({rc})")
+    return out
+
+
+def matvec_q8(wfmt: int, W, rows: int, hidden: int, xq, threads: int = 1,
+              row_begin: int = 0, row_end: int | None = None):
+    """Q4_0 / Q8_0 weights times Q8_0 activations ``xq`` ([hidden / 32 * 34]
+    or [batch, hidden / 32 * 34] bytes): y[b, r] and bound[b, r] in f64.
+    Rows outside [row_begin, row_end) are NaN."""
+    w = _u8(W)
+    assert w.size == rows * (hidden // 32) * BLOCK_BYTES[wfmt]
+    xb = np.ascontiguousarray(np.asarray(xq, dtype=np.uint8))
+    squeeze = xb.ndim == 1
+    xb = xb.reshape(-1, hidden // 32 * 34)
+    batch = xb.shape[0]
+    row_end = rows if row_end is None else row_end
+    y = np.full((batch, rows), np.nan)
+    bound = np.full((batch, rows), np.nan)
+    lib = _load()
+
+    def run(a: int, b: int) -> int:
+        return lib.qo_matvec_q8(wfmt, _ptr(w), rows, hidden, _ptr(xb), batch, a, b,
+                                _ptr(y), _ptr(bound))
+
+    n = row_end - row_begin
+    threads = max(1, min(int(threads), n if n > 0 else 1))
+    if threads == 1:
+        rcs = [run(row_begin, row_end)]
+    else:
+        edges = [row_begin + (n * t) // threads for t in range(threads + 1)]
+        with ThreadPoolExecutor(threads) as ex:
+            rcs = list(ex.map(lambda t: run(edges[t], edges[t + 1]), range(threads)))
+    if any(rcs):
+        raise ValueError(f"qo_matvec_q8 failed ({rcs})")
     if squeeze:
         return y[0], bound[0]
     return y, bound

@@ -9,8 +9,9 @@
  *   [engine]   crates/infer-inference/README.md
  *   [perf]     crates/infer-inference/PERFORMANCE.md
  *
- * The pages name the formats (Q4_0, Q4_K, Q6_K; "GGUF-compatible -- Q4_K/Q6_K
- * formats match Ollama's quantization", [compute] §Design Principles item 8)
+ * The pages name the formats (Q4_0, Q4_K, Q6_K, and Q8_0 for the 8-bit path;
+ * "GGUF-compatible -- Q4_K/Q6_K formats match Ollama's quantization", [compute]
+ * §Design Principles item 8)
  * but print no byte layout.  The layouts below are the plainest reading of
  * "GGUF-compatible": the public GGUF block formats, restated here in prose and
  * written from that understanding.  Every weight is decoded to an f64 value
@@ -31,6 +32,7 @@
 #define QO_ACT_GELU_TANH 0
 #define QO_ACT_SILU 1
 #define QO_Q6_K 14
+#define QO_Q8_0 8
 
 /* ---------------------------------------------------------------------------
  * IEEE-754 binary16 -> double, by bit arithmetic (sign, 5-bit exponent with
@@ -53,6 +55,8 @@ double qo_half(uint16_t h)
 }
 
 static uint16_t rd16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+void qo_dequant_q8_0(const uint8_t *blk, double out[32]);
 
 /* ---------------------------------------------------------------------------
  * Q4_0 ([compute] §Shaders "Q4_0 matvec"): 32 weights in 18 bytes.
@@ -165,6 +169,7 @@ int qo_block_weights(int fmt)
     case QO_Q4_0: return 32;
     case QO_Q4_K: return 256;
     case QO_Q6_K: return 256;
+    case QO_Q8_0: return 32;
     default: return 0;
     }
 }
@@ -175,6 +180,7 @@ int qo_block_bytes(int fmt)
     case QO_Q4_0: return 18;
     case QO_Q4_K: return 144;
     case QO_Q6_K: return 210;
+    case QO_Q8_0: return 34;
     default: return 0;
     }
 }
@@ -182,6 +188,7 @@ int qo_block_bytes(int fmt)
 static void dequant_block(int fmt, const uint8_t *blk, double *out)
 {
     if (fmt == QO_Q4_0) qo_dequant_q4_0(blk, out);
+    else if (fmt == QO_Q8_0) qo_dequant_q8_0(blk, out);
     else if (fmt == QO_Q4_K) qo_dequant_q4_k(blk, out);
     else qo_dequant_q6_k(blk, out);
 }
@@ -233,6 +240,142 @@ int qo_matvec(int fmt, const uint8_t *W, int64_t rows, int64_t hidden,
         }
     }
     free(wrow);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * float -> IEEE-754 binary16 bits, round to nearest, ties to even (the
+ * standard conversion), by arithmetic on the value: the magnitude is split
+ * into an exponent E and a significand counted in units of the binary16
+ * spacing at that exponent (2^(E-10) for normals, 2^-24 below 2^-14); the
+ * count is rounded with rint() in the default ties-to-even mode.  A count
+ * that rounds up to 2048 carries into the next exponent; magnitudes that
+ * round above 65504 become infinity.
+ * ------------------------------------------------------------------------- */
+uint16_t qo_half_bits(float f)
+{
+    double v = (double)f;
+    uint16_t sign = signbit(v) ? 0x8000u : 0u;
+    if (isnan(v)) return (uint16_t)(sign | 0x7E00u);
+    v = fabs(v);
+    if (isinf(v)) return (uint16_t)(sign | 0x7C00u);
+    if (v < ldexp(1.0, -14)) {
+        double m = rint(v / ldexp(1.0, -24));       /* subnormal count, 0..1024 */
+        return (uint16_t)(sign | (uint16_t)m);    /* 1024 is the smallest normal */
+    }
+    int e;
+    frexp(v, &e);                                  /* v = f * 2^e, f in [0.5, 1) */
+    int E = e - 1;                                 /* v in [2^E, 2^(E+1)) */
+    double m = rint(v / ldexp(1.0, E - 10));       /* 1024..2048 */
+    if (m == 2048.0) {
+        m = 1024.0;
+        E += 1;
+    }
+    if (E > 15) return (uint16_t)(sign | 0x7C00u);
+    return (uint16_t)(sign | (uint16_t)((E + 15) << 10) | (uint16_t)(m - 1024.0));
+}
+
+/* ---------------------------------------------------------------------------
+ * Q8_0 ([compute] §Shaders rows "Q8" (q8_matvec) and "Element-wise"
+ * (quantize_q8); the GGUF-compatible 8-bit format of the same README's format
+ * list): 32 values in 34 bytes.
+ *   bytes 0..1   d (binary16)
+ *   bytes 2..33  qs[32], int8 (two's complement)
+ *   w = d * q
+ * ------------------------------------------------------------------------- */
+void qo_dequant_q8_0(const uint8_t *blk, double out[32])
+{
+    double d = qo_half(rd16(blk));
+    for (int j = 0; j < 32; ++j) {
+        int q = blk[2 + j];
+        if (q >= 128) q -= 256;
+        out[j] = d * (double)q;
+    }
+}
+
+/* ---------------------------------------------------------------------------
+ * quantize_q8 ([compute] §Shaders "Element-wise", quantize_q8; the Q4_0 FFN
+ * goes "through legacy Q8 path", §Architecture): activations -> Q8_0 blocks.
+ * The pages give no rounding rule; this is symmetric absmax quantization, the
+ * plainest reading of the 8-bit block format, with every decision in f32:
+ *   amax = max_j |x_j|,  d = amax / 127,  id = d != 0 ? 1 / d : 0,
+ *   q_j  = round(x_j * id)  (nearest, halves away from zero: C roundf)
+ * and the stored scale is d rounded to binary16 (the codes use the f32 d).
+ * n must be a multiple of 32; block k of x goes to out[34k .. 34k + 33].
+ * ------------------------------------------------------------------------- */
+int qo_quantize_q8_0(const float *x, int64_t n, uint8_t *out)
+{
+    if (n < 0 || n % 32 != 0) return -1;
+    for (int64_t k = 0; k < n / 32; ++k) {
+        const float *xb = x + 32 * k;
+        uint8_t *blk = out + 34 * k;
+        float amax = 0.0f;
+        for (int j = 0; j < 32; ++j) {
+            float a = fabsf(xb[j]);
+            if (a > amax) amax = a;
+        }
+        float d = amax / 127.0f;
+        float id = d != 0.0f ? 1.0f / d : 0.0f;
+        uint16_t h = qo_half_bits(d);
+        blk[0] = (uint8_t)(h & 0xFF);
+        blk[1] = (uint8_t)(h >> 8);
+        for (int j = 0; j < 32; ++j) {
+            float t = xb[j] * id;
+            int q = (int)roundf(t);
+            blk[2 + j] = (uint8_t)(q & 0xFF);
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Matvec over Q8_0 activations ([compute] §Architecture "Q4_0 through legacy
+ * Q8 path"; §Shaders "Q8" row, q8_matvec): weights in Q4_0 or Q8_0 times the
+ * quantized activation xq.  Per 32-weight block the integer codes multiply
+ * exactly, then the two scales apply:
+ *   y[b][r]     = sum_k dw[r][k] * dx[b][k] * sum_j qw[r][k][j] * qx[b][k][j]
+ *   bound[b][r] = sum_k |dw * dx| * sum_j |qw * qx|
+ * where qw = q - 8 for Q4_0 and qw = q for Q8_0; the integer sums are exact,
+ * the rest is f64 in block order.  xq is [batch][hidden / 32] blocks of 34 B;
+ * y and bound are [batch][rows], written for rows in [row_begin, row_end).
+ * ------------------------------------------------------------------------- */
+int qo_matvec_q8(int wfmt, const uint8_t *W, int64_t rows, int64_t hidden,
+                 const uint8_t *xq, int batch, int64_t row_begin, int64_t row_end,
+                 double *y, double *bound)
+{
+    if ((wfmt != QO_Q4_0 && wfmt != QO_Q8_0) || hidden % 32 != 0 || batch < 1) return -1;
+    if (row_begin < 0 || row_end > rows || row_begin > row_end) return -1;
+    int64_t nb = hidden / 32;
+    int bb = wfmt == QO_Q4_0 ? 18 : 34;
+    for (int bt = 0; bt < batch; ++bt) {
+        for (int64_t r = row_begin; r < row_end; ++r) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < nb; ++k) {
+                const uint8_t *wb = W + (r * nb + k) * bb;
+                const uint8_t *xb = xq + ((int64_t)bt * nb + k) * 34;
+                int qw[32];
+                if (wfmt == QO_Q4_0) {
+                    for (int j = 0; j < 16; ++j) {
+                        qw[j] = (wb[2 + j] & 15) - 8;
+                        qw[16 + j] = (wb[2 + j] >> 4) - 8;
+                    }
+                } else {
+                    for (int j = 0; j < 32; ++j) qw[j] = wb[2 + j] >= 128 ? wb[2 + j] - 256 : wb[2 + j];
+                }
+                int64_t isum = 0, iabs = 0;
+                for (int j = 0; j < 32; ++j) {
+                    int qx = xb[2 + j] >= 128 ? xb[2 + j] - 256 : xb[2 + j];
+                    isum += (int64_t)qw[j] * qx;
+                    iabs += llabs((int64_t)qw[j] * qx);
+                }
+                double s = qo_half(rd16(wb)) * qo_half(rd16(xb));
+                acc += s * (double)isum;
+                mag += fabs(s) * (double)iabs;
+            }
+            y[(int64_t)bt * rows + r] = acc;
+            if (bound) bound[(int64_t)bt * rows + r] = mag;
+        }
+    }
     return 0;
 }
 

@@ -16,6 +16,8 @@ Path runs the same shapes with random weights):
   ~U{0..63}); the sixteen int8 scales are U{scale_lo..scale_hi} (default
   U{0..63}); d = f16(U(0.001, 0.02)).
 * Q4_0 block (18 B): d = f16(U(0.001, 0.02)); 16 uniform nibble bytes.
+* Q8_0 block (34 B): d = f16(U(0.001, 0.02)); 32 uniform bytes read as int8
+  (every code -128..127, including -128, which a quantizer never writes).
 * Activations: x ~ N(0, 1) f32.  A "unit-RMS" vector is a uniform random point
   on the sphere of radius sqrt(n) (a normal draw divided by its RMS), the
   distribution of an RMS-normalised normal vector with unit weights.
@@ -29,9 +31,9 @@ from __future__ import annotations
 import numpy as np
 
 BASE_SEED = 0x5EED
-Q4_0, Q4_K, Q6_K = 2, 12, 14
-BLOCK_WEIGHTS = {Q4_0: 32, Q4_K: 256, Q6_K: 256}
-BLOCK_BYTES = {Q4_0: 18, Q4_K: 144, Q6_K: 210}
+Q4_0, Q8_0, Q4_K, Q6_K = 2, 8, 12, 14
+BLOCK_WEIGHTS = {Q4_0: 32, Q8_0: 32, Q4_K: 256, Q6_K: 256}
+BLOCK_BYTES = {Q4_0: 18, Q8_0: 34, Q4_K: 144, Q6_K: 210}
 
 
 def rng(*key: int) -> np.random.Generator:
@@ -79,6 +81,14 @@ def q4_0_matrix(g: np.random.Generator, rows: int, hidden: int,
     return b.reshape(-1)
 
 
+def q8_0_matrix(g: np.random.Generator, rows: int, hidden: int,
+                d_range=(0.001, 0.02)) -> np.ndarray:
+    nb = n_blocks(Q8_0, rows, hidden)
+    b = _random_bytes(g, nb * 34).reshape(nb, 34)
+    b[:, 0:2] = _f16_bytes(g, nb, *d_range)
+    return b.reshape(-1)
+
+
 def matrix(fmt: int, g: np.random.Generator, rows: int, hidden: int) -> np.ndarray:
     if fmt == Q4_K:
         return q4_k_matrix(g, rows, hidden)
@@ -86,6 +96,8 @@ def matrix(fmt: int, g: np.random.Generator, rows: int, hidden: int) -> np.ndarr
         return q6_k_matrix(g, rows, hidden)
     if fmt == Q4_0:
         return q4_0_matrix(g, rows, hidden)
+    if fmt == Q8_0:
+        return q8_0_matrix(g, rows, hidden)
     raise ValueError(f"unknown format {fmt}")
 
 
