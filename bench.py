@@ -7,6 +7,10 @@ microseconds per token of the 34-layer chain reported alongside.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
        [--n-layers L]   (a shorter chain, for small profiler captures only)
+       [--op OP --batch B]  time one operation alone, back to back (not the
+                        decode step): lm_head_q4_0 (f32 activations),
+                        lm_head_q8 (quantize_q8 + Q4_0 x Q8_0 matvec),
+                        ffn (fused gate/up GEGLU + Q6_K down, 2560/10240)
 For N > 1 launch with torchrun; every rank runs an independent replica of the
 step on its own GPU (the path has no data exchange; "replicas only").
 """
@@ -360,6 +364,101 @@ def run_gpu(args, world, rank, local):
     print(json.dumps(out))
 
 
+def run_op(args):
+    """One operation timed alone, back to back (weights > L2, so every call
+    streams them from HBM).  Algorithmic bytes: packed weights + activations
+    read + outputs written."""
+    import torch
+
+    from quantized_weight_streaming_q4k_gb300 import build, ops, synth
+    build.build()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    H, I, B = 2560, 10240, args.batch
+    g = synth.rng(synth.W_LM_HEAD, 0)
+    launches = 1
+    if args.op in ("lm_head_q4_0", "lm_head_q8"):
+        W = torch.from_numpy(synth.q4_0_matrix(g, VOCAB, H)).to(dev)
+        x = torch.from_numpy(synth.normal_vector(g, H, B if B > 1 else None)).to(dev)
+        y = torch.empty((B, VOCAB) if B > 1 else (VOCAB,), device=dev)
+        wbytes = synth.n_blocks(synth.Q4_0, VOCAB, H) * 18
+        if args.op == "lm_head_q4_0":
+            split = 0
+            ws = None
+            if B * H // 64 > 320:
+                nbytes = ops.workspace_bytes(ops.OP_MATVEC, VOCAB, H, 0, B, 0)
+                ws = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev)
+
+            def call():
+                ops.q4_0_matvec(W, x, VOCAB, H, B, split, ws, out=y)
+            nbytes = wbytes + B * H * 4 + B * VOCAB * 4
+            kernel = "matvec_kernel<UnitQ40> (f32 activations)"
+        else:
+            xq = torch.empty((B, H // 32 * 34) if B > 1 else (H // 32 * 34,), dtype=torch.uint8,
+                             device=dev)
+
+            def call():
+                ops.quantize_q8_0(x, H, B, out=xq)
+                ops.q8_matvec(ops.Q4_0, W, xq, VOCAB, H, B, out=y)
+            launches = 2
+            # quantize reads x, writes xq; the matvec reads W and xq, writes y
+            nbytes = wbytes + B * H * 4 + 2 * B * (H // 32 * 34) + B * VOCAB * 4
+            kernel = "quantize_q8_0_kernel + matvec_kernel<UnitQ40xQ8>"
+        workload = f"lm_head {VOCAB}x{H} Q4_0, batch {B}"
+    elif args.op == "ffn":
+        gl = synth.rng(synth.W_FFN, 0)
+        Wg = torch.from_numpy(synth.q4_k_matrix(gl, I, H)).to(dev)
+        Wu = torch.from_numpy(synth.q4_k_matrix(gl, I, H)).to(dev)
+        Wd = torch.from_numpy(synth.q6_k_matrix(gl, H, I)).to(dev)
+        x = torch.from_numpy(synth.unit_rms_vector(gl, H)).to(dev)
+        y = torch.empty(H, device=dev)
+        ws = torch.empty(ops.workspace_bytes(ops.OP_FFN, 0, H, I), dtype=torch.uint8, device=dev)
+
+        def call():
+            ops.q4k_ffn_gate_up_geglu_down(Wg, Wu, Wd, ops.Q6_K, x, H, I, workspace=ws, out=y)
+        launches = 2
+        nbytes = (2 * synth.n_blocks(synth.Q4_K, I, H) * 144 + synth.n_blocks(synth.Q6_K, H, I) * 210
+                  + H * 4 + 2 * I * 4 + H * 4)
+        kernel = "gate/up GEGLU + down (two streaming launches)"
+        workload = f"fused FFN hidden {H} inter {I}, Q4_K gate/up, Q6_K down, batch 1"
+        if B != 1:
+            raise SystemExit("--op ffn runs at batch 1")
+    else:
+        raise SystemExit(f"unknown --op {args.op}")
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    clocks = ClockSampler((uuid if uuid.startswith("GPU-") else f"GPU-{uuid}") if uuid else "0")
+    clocks.start()
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(args.steps):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert ops.device_error() == 0
+    us = 1e3 * a.elapsed_time(b) / args.steps
+    gbs = nbytes / (us * 1e-6) / 1e9
+    peak, peak_kind = peaks()
+    print(json.dumps({
+        "metric": f"{args.op} achieved HBM GB/s", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "us_per_call": us,
+        "higher_is_better": True, "dtype": "f32", "data": "synthetic (seeded random blocks)",
+        "config": {"workload": workload, "batch": B,
+                   "l2": "back to back; weights larger than L2"},
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": gbs, "peak": peak,
+                     "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_kind,
+                     "traffic": None},
+        "bytes_per_call": nbytes, "gpu_launches": launches * args.steps, "clocks": clk,
+    }))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -369,7 +468,14 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--n-layers", type=int, default=N_LAYERS,
                     help="chain length (default 34; shorter only for profiler captures)")
+    ap.add_argument("--op", default="step",
+                    choices=["step", "lm_head_q4_0", "lm_head_q8", "ffn"],
+                    help="step (default): the decode step; otherwise one operation alone")
+    ap.add_argument("--batch", type=int, default=1, help="activation vectors (--op only)")
     args = ap.parse_args()
+    if args.op != "step":
+        run_op(args)
+        return
     world, rank, local = dist_init()
     if args.impl == "reference":
         run_reference(args, world, rank)

@@ -70,7 +70,9 @@ typedef enum {
 } qws_status;
 
 /* GGUF type ids. */
-typedef enum { QWS_Q4_0 = 2, QWS_Q4_K = 12, QWS_Q6_K = 14 } qws_format;
+typedef enum { QWS_Q4_0 = 2, QWS_Q8_0 = 8, QWS_Q4_K = 12, QWS_Q6_K = 14 } qws_format;
+/* QWS_Q8_0 is accepted only by the 8-bit path (qws_q8_matvec,
+ * qws_q8_qkv_proj); the f32-activation entry points reject it. */
 
 /* Operations for qws_workspace_bytes(). */
 typedef enum {
@@ -120,6 +122,43 @@ qws_status qws_matvec(qws_format fmt, const void* W, const float* x, float* y, i
 qws_status qws_q4k_qkv_proj(const void* Wq, const void* Wk, const void* Wv, const float* x,
                             float* q, float* k, float* v, int64_t hidden, int64_t q_dim,
                             int64_t kv_dim, qws_stream stream);
+
+/* ------------------------------------------------------------------------
+ * The 8-bit path (infer-compute README §Architecture: the Q4_0 FFN goes
+ * "through legacy Q8 path"; §Shaders rows "Q8" (q8_matvec, q8_qkv_proj) and
+ * "Element-wise" (quantize_q8)).  Activations are first quantized to Q8_0
+ * blocks; the matvecs then multiply integer codes exactly (dp4a) and apply
+ * the two block scales:
+ *   y[b][r] = sum_k dw[r][k] * dx[b][k] * sum_j qw[r][k][j] * qx[b][k][j]
+ * with qw = q - 8 for Q4_0 weights and qw = q for Q8_0 weights.
+ *
+ * Q8_0 block (34 bytes, 32 values): binary16 d, then 32 int8 codes; x ~ d*q.
+ *
+ * qws_quantize_q8_0: x [batch][n] f32 (device, 4-byte aligned, finite) ->
+ *   xq [batch][n / 32 * 34] bytes (device, 2-byte aligned).  Per block of
+ *   32, all in f32:
+ *   amax = max |x|, d = amax / 127, id = (d != 0 ? 1 / d : 0),
+ *   q = round(x * id) (halves away from zero); d is stored rounded to
+ *   binary16 (nearest, ties to even).  The pages give no rounding rule; this
+ *   is the symmetric absmax reading.  n > 0, n % 32 == 0, batch >= 1.
+ *   Output bytes are identical run to run.
+ *
+ * qws_q8_matvec: W rows x hidden in wfmt (QWS_Q4_0 or QWS_Q8_0; device,
+ *   16-byte aligned), xq [batch][hidden / 32 * 34] bytes (device, 4-byte
+ *   aligned), y [batch][rows] f32 (device, 4-byte aligned), overwritten.
+ *   hidden % 64 == 0, 0 < hidden <= 20480, batch * hidden / 64 <= 320.
+ *   Any other format returns QWS_ERR_FORMAT.
+ *
+ * qws_q8_qkv_proj: the fused Q/K/V projection of the 8-bit path (batch 1):
+ *   q = Wq xq (q_dim rows), k = Wk xq, v = Wv xq (kv_dim rows each), all
+ *   three matrices in wfmt, streamed in one launch.
+ * ---------------------------------------------------------------------- */
+qws_status qws_quantize_q8_0(const float* x, void* xq, int64_t n, int batch, qws_stream stream);
+qws_status qws_q8_matvec(qws_format wfmt, const void* W, const void* xq, float* y, int64_t rows,
+                         int64_t hidden, int batch, qws_stream stream);
+qws_status qws_q8_qkv_proj(qws_format wfmt, const void* Wq, const void* Wk, const void* Wv,
+                           const void* xq, float* q, float* k, float* v, int64_t hidden,
+                           int64_t q_dim, int64_t kv_dim, qws_stream stream);
 
 /* ------------------------------------------------------------------------
  * Gated FFN (infer-compute README §Shaders "Q4_K fused FFN": q4k_ffn_gate_up,

@@ -16,7 +16,7 @@ STATUS_NAMES = {
     0: "QWS_OK", 1: "QWS_ERR_NULL", 2: "QWS_ERR_SHAPE", 3: "QWS_ERR_ALIGN",
     4: "QWS_ERR_FORMAT", 5: "QWS_ERR_WORKSPACE", 6: "QWS_ERR_CUDA", 7: "QWS_ERR_TIMEOUT",
 }
-Q4_0, Q4_K, Q6_K = 2, 12, 14
+Q4_0, Q8_0, Q4_K, Q6_K = 2, 8, 12, 14
 OP_MATVEC, OP_FFN, OP_DECODE_CHAIN = 0, 1, 2
 
 
@@ -52,6 +52,9 @@ SIGNATURES = {
     "qws_q4k_ffn_gate_up_silu_down": (I, [P, P, P, I, F, F, I64, I64, P, SZ, P]),
     "qws_q4k_ffn_gate_up_silu": (I, [P, P, F, F, I64, I64, P]),
     "qws_residual_rms_norm": (I, [F, F, F, F, I64, C.c_float, I, P]),
+    "qws_quantize_q8_0": (I, [F, P, I64, I, P]),
+    "qws_q8_matvec": (I, [I, P, P, F, I64, I64, I, P]),
+    "qws_q8_qkv_proj": (I, [I, P, P, P, P, F, F, F, I64, I64, I64, P]),
     "qws_rms_norm": (I, [F, F, F, I64, C.c_float, I, P]),
     "qws_residual_add": (I, [F, F, I64, I, P]),
     "qws_decode_chain": (I, [C.POINTER(QwsLayer), I, F, C.POINTER(QwsDims), P, SZ, P]),

@@ -188,6 +188,83 @@ qws_status qws_q4k_qkv_proj(const void* Wq, const void* Wk, const void* Wv, cons
   return ok();
 }
 
+qws_status qws_quantize_q8_0(const float* x, void* xq, int64_t n, int batch, qws_stream stream) {
+  const char* fn = "qws_quantize_q8_0";
+  QWS_CHECK_F(x);
+  QWS_CHECK_PTR(xq);
+  if (!aligned(xq, 2)) return fail(QWS_ERR_ALIGN, "%s: xq is not 2-byte aligned", fn);
+  if (n <= 0 || n % 32)
+    return fail(QWS_ERR_SHAPE, "%s: n = %lld is not a positive multiple of 32", fn, (long long)n);
+  if (batch < 1) return fail(QWS_ERR_SHAPE, "%s: batch = %d < 1", fn, batch);
+  if (n > (int64_t(1) << 40) / batch) return fail(QWS_ERR_SHAPE, "%s: n * batch too large", fn);
+  cudaError_t e = qws::launch_quantize_q8_0(x, static_cast<uint8_t*>(xq), n / 32 * batch,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn, "");
+  return ok();
+}
+
+static qws_status check_q8_shape(const char* fn, int wfmt, int64_t hidden, int batch) {
+  if (wfmt != QWS_Q4_0 && wfmt != QWS_Q8_0)
+    return fail(QWS_ERR_FORMAT, "%s: weights must be Q4_0 or Q8_0 (got %d)", fn, wfmt);
+  if (hidden <= 0 || hidden % 64 || hidden > kMaxHidden)
+    return fail(QWS_ERR_SHAPE, "%s: hidden = %lld (need a multiple of 64 in (0, 20480])", fn,
+                (long long)hidden);
+  if (batch < 1) return fail(QWS_ERR_SHAPE, "%s: batch = %d < 1", fn, batch);
+  if ((hidden / 64) * batch > 320)
+    return fail(QWS_ERR_SHAPE, "%s: batch * hidden / 64 = %lld above 320", fn,
+                (long long)((hidden / 64) * batch));
+  return QWS_OK;
+}
+
+qws_status qws_q8_matvec(qws_format wfmt, const void* W, const void* xq, float* y, int64_t rows,
+                         int64_t hidden, int batch, qws_stream stream) {
+  const char* fn = "qws_q8_matvec";
+  qws_status rc = check_q8_shape(fn, wfmt, hidden, batch);
+  if (rc != QWS_OK) return rc;
+  QWS_CHECK_W(W);
+  QWS_CHECK_F(xq);
+  QWS_CHECK_F(y);
+  if (rows < 0) return fail(QWS_ERR_SHAPE, "%s: rows = %lld < 0", fn, (long long)rows);
+  if (rows > (int64_t(1) << 31) / batch)
+    return fail(QWS_ERR_SHAPE, "%s: rows * batch above 2^31", fn);
+  if (rows == 0) return ok();
+  std::string why;
+  qws::Seg seg{static_cast<const uint8_t*>(W), y, rows, 0};
+  cudaError_t e = qws::launch_matvec_q8(wfmt, &seg, 1, static_cast<const uint8_t*>(xq), hidden,
+                                        batch, reinterpret_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess) return cuda_fail(e, fn, why);
+  return ok();
+}
+
+qws_status qws_q8_qkv_proj(qws_format wfmt, const void* Wq, const void* Wk, const void* Wv,
+                           const void* xq, float* q, float* k, float* v, int64_t hidden,
+                           int64_t q_dim, int64_t kv_dim, qws_stream stream) {
+  const char* fn = "qws_q8_qkv_proj";
+  qws_status rc = check_q8_shape(fn, wfmt, hidden, 1);
+  if (rc != QWS_OK) return rc;
+  QWS_CHECK_W(Wq);
+  QWS_CHECK_W(Wk);
+  QWS_CHECK_W(Wv);
+  QWS_CHECK_F(xq);
+  QWS_CHECK_F(q);
+  QWS_CHECK_F(k);
+  QWS_CHECK_F(v);
+  if (q_dim < 0 || kv_dim < 0) return fail(QWS_ERR_SHAPE, "%s: negative q_dim / kv_dim", fn);
+  if (q_dim + 2 * kv_dim == 0) return ok();
+  qws::Seg segs[3];
+  int n = 0;
+  if (q_dim) segs[n++] = qws::Seg{static_cast<const uint8_t*>(Wq), q, q_dim, 0};
+  if (kv_dim) {
+    segs[n++] = qws::Seg{static_cast<const uint8_t*>(Wk), k, kv_dim, 0};
+    segs[n++] = qws::Seg{static_cast<const uint8_t*>(Wv), v, kv_dim, 0};
+  }
+  std::string why;
+  cudaError_t e = qws::launch_matvec_q8(wfmt, segs, n, static_cast<const uint8_t*>(xq), hidden, 1,
+                                        reinterpret_cast<cudaStream_t>(stream), &why);
+  if (e != cudaSuccess) return cuda_fail(e, fn, why);
+  return ok();
+}
+
 static qws_status check_ffn_shape(const char* fn, int64_t hidden, int64_t inter) {
   if (hidden <= 0 || hidden % 256 || hidden > kMaxHidden)
     return fail(QWS_ERR_SHAPE, "%s: hidden = %lld (need a multiple of 256 in (0, 20480])", fn,

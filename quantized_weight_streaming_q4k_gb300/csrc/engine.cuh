@@ -312,7 +312,8 @@ __device__ __forceinline__ void stage_x(float* xs, int US, const Src& src, int64
 // b = g / G and rows gg, gg + G, ... of each tile (gg = g % G).  x_of(b)
 // returns a column loader of vector b; vectors are staged one at a time
 // through shared memory.  With STAGED = false the caller has already written
-// the single vector (B = 1) into R.xs.  Returns false on a timeout.
+// the single vector (B = 1) into R.xs.  A unit with kDirect reads its own
+// activations from x_of(b) instead (no staging).  Returns false on a timeout.
 template <class Unit, bool STAGED = true, bool PIPE = true, class XOf>
 __device__ __forceinline__ bool consume_phase(const Phase& Pref, const Ring& Rref, RingPos& pos,
                                               const XOf& x_of, int ctid, int C, unsigned* err) {
@@ -332,7 +333,10 @@ __device__ __forceinline__ bool consume_phase(const Phase& Pref, const Ring& Rre
   const size_t rb = static_cast<size_t>(P.row_bytes);
   Unit unit;
   if constexpr (Unit::kMixed) unit.q6 = P.fmt == 14;
-  if constexpr (STAGED) {
+  if constexpr (Unit::kDirect) {
+    // the unit reads its activation bytes of vector b itself
+    if (active) unit.setup(u, x_of(b));
+  } else if constexpr (STAGED) {
     for (int bb = 0; bb < P.B; ++bb) {
       if (bb) bar_sync(kConsumerBar, C);       // previous vector fully read
       // one round of loads per thread when K allows (every CTA reads the same
@@ -503,6 +507,13 @@ struct XOfPlain {
   const float* x;
   int64_t stride;
   __device__ __forceinline__ XPlain operator()(int b) const { return XPlain{x + b * stride}; }
+};
+
+// Vector b of [B][stride] bytes of Q8_0 blocks (units with kDirect).
+struct XOfQ8 {
+  const uint8_t* xq;
+  int64_t stride;
+  __device__ __forceinline__ const uint8_t* operator()(int b) const { return xq + b * stride; }
 };
 
 }  // namespace qws

@@ -7,6 +7,7 @@
 //   Q6_K 210 B / 256 w : 128 B low nibbles, 64 B 2-bit highs, 16 int8 scales, f16 d
 //                        w = d*sc[i/16]*(q-32)
 //   Q4_0  18 B /  32 w : f16 d, 16 B nibbles;  w = d*(q-8)
+//   Q8_0  34 B /  32 w : f16 d, 32 int8 codes;  w = d*q   (8-bit path)
 //
 // Lane unit.  Every lane owns a fixed group of 64 (Q6_K: 32) columns of the
 // row ("unit") and keeps the matching activations in registers for the whole
@@ -103,6 +104,7 @@ struct UnitQ4K {
   static constexpr int kFmt = 12;
   static constexpr int kUnitW = 64;
   static constexpr bool kMixed = false;
+  static constexpr bool kDirect = false;  // activations staged through shared memory
   static constexpr int kBlockW = 256;
   static constexpr int kBlockBytes = 144;
   float xa[32];   // sub-block 2c,   column 64c + l,      pre-scaled
@@ -280,6 +282,7 @@ struct UnitQ6K {
   static constexpr int kFmt = 14;
   static constexpr int kUnitW = 64;
   static constexpr bool kMixed = false;
+  static constexpr bool kDirect = false;  // activations staged through shared memory
   static constexpr int kBlockW = 256;
   static constexpr int kBlockBytes = 210;
   float x[64];      // [16a + i], pre-scaled by 2^(kE - pos(i%4))
@@ -334,6 +337,7 @@ struct UnitQ40 {
   static constexpr int kFmt = 2;
   static constexpr int kUnitW = 64;
   static constexpr bool kMixed = false;
+  static constexpr bool kDirect = false;  // activations staged through shared memory
   static constexpr int kBlockW = 32;
   static constexpr int kBlockBytes = 18;
   float e0[4];               // qs0[0..1] via w0 >> 12: lo0 hi0 lo1 hi1 (pos 4, 8, 12, 16)
@@ -421,12 +425,195 @@ struct UnitQ40 {
 };
 
 // ---------------------------------------------------------------------------
+// Units over Q8_0 activations (the 8-bit path: infer-compute README §Shaders
+// row "Q8" and §Architecture "Q4_0 through legacy Q8 path").  The activation
+// vector arrives already quantized, as Q8_0 blocks (34 B / 32 values: f16 d,
+// then 32 int8 codes), so a block's product is an exact integer sum of code
+// products times the two scales.  The integer sums run on dp4a (four 8-bit
+// products and their sum per instruction), which needs no decode to float.
+//
+// Unit u covers columns 64u .. 64u + 63: activation blocks 2u and 2u + 1,
+// 68 bytes at offset 68u of the vector (4-byte aligned when hidden % 64 == 0).
+// As 17 words:  x0 = dx0 | a0[0..1] << 16,  x1..x7 = a0[2..29],
+//               x8 = a0[30..31] | dx1 << 16, x9..x16 = a1[0..31].
+// The lanes read these 68 bytes straight from global memory once per phase
+// (kDirect): nothing is staged through shared memory.
+// ---------------------------------------------------------------------------
+
+// sum of the four byte products of a (unsigned) and b (signed), plus c
+__device__ __forceinline__ int dp4a_us(uint32_t a, uint32_t b, int c) {
+  int d;
+  asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+  return d;
+}
+__device__ __forceinline__ int dp4a_ss(uint32_t a, uint32_t b, int c) {
+  return __dp4a(static_cast<int>(a), static_cast<int>(b), c);
+}
+
+__device__ __forceinline__ void load_q8_unit_words(const uint8_t* xq, int u, uint32_t (&x)[17]) {
+  const uint32_t* p = reinterpret_cast<const uint32_t*>(xq + 68 * static_cast<int64_t>(u));
+#pragma unroll
+  for (int i = 0; i < 17; ++i) x[i] = p[i];
+}
+
+// Q4_0 weights x Q8_0 activations.  The Q4_0 unit is 36 bytes at 36u (words
+// w0..w8, as for UnitQ40): w0 = dw0 | qs0[0..1] << 16, w1..w3 = qs0[2..13],
+// w4 = qs0[14..15] | dw1 << 16, w5..w8 = qs1[0..15].  Weight j of a block is
+// the low nibble of qs[j], weight 16 + j the high nibble, value q - 8.
+// The activation words are re-packed once so that byte k of lo0[i] / hi0[i]
+// is the activation of the low / high nibble in byte k of weight word i
+// (zero against the scale bytes of w0 and w4):
+//   lo0 = {x0 & 0xFFFF0000, x1, x2, x3, x4 & 0xFFFF}    a0[0..15]
+//   hi0 = {x4 & 0xFFFF0000, x5, x6, x7, x8 & 0xFFFF}    a0[16..31]
+//   lo1 = x9..x12 (a1[0..15]),  hi1 = x13..x16 (a1[16..31]).
+// Low nibbles are masked in place (0x0F0F0F0F); high nibbles are masked in
+// place too (0xF0F0F0F0: 16 q per byte, unsigned), so that sum is 16x and is
+// shifted down once.  sum_j (q_j - 8) a_j = sum q a - 8 sum a, with 8 sum a
+// precomputed per block.
+struct UnitQ40xQ8 {
+  static constexpr int kFmt = 2;
+  static constexpr int kUnitW = 64;
+  static constexpr bool kMixed = false;
+  static constexpr bool kDirect = true;
+  uint32_t lo0[5], hi0[5], lo1[4], hi1[4];
+  float dx0, dx1;
+  int c0, c1;        // 8 * sum of the block's activation codes
+  uint32_t off;
+
+  __device__ __forceinline__ static void unit_of(int64_t col, int& u, int& l) {
+    u = static_cast<int>(col >> 6);
+    l = static_cast<int>(col & 63);
+  }
+
+  __device__ __forceinline__ void setup(int u, const uint8_t* xq) {
+    uint32_t x[17];
+    load_q8_unit_words(xq, u, x);
+    lo0[0] = x[0] & 0xFFFF0000u;
+    hi0[0] = x[4] & 0xFFFF0000u;
+#pragma unroll
+    for (int i = 1; i < 4; ++i) {
+      lo0[i] = x[i];
+      hi0[i] = x[4 + i];
+    }
+    lo0[4] = x[4] & 0xFFFFu;
+    hi0[4] = x[8] & 0xFFFFu;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      lo1[i] = x[9 + i];
+      hi1[i] = x[13 + i];
+    }
+    dx0 = half_bits_to_float(x[0]);
+    dx1 = half_bits_to_float(x[8] >> 16);
+    int s0 = 0, s1 = 0;
+#pragma unroll
+    for (int i = 0; i < 5; ++i) s0 = dp4a_ss(hi0[i], 0x01010101u, dp4a_ss(lo0[i], 0x01010101u, s0));
+#pragma unroll
+    for (int i = 0; i < 4; ++i) s1 = dp4a_ss(hi1[i], 0x01010101u, dp4a_ss(lo1[i], 0x01010101u, s1));
+    c0 = 8 * s0;
+    c1 = 8 * s1;
+    off = 36u * static_cast<uint32_t>(u);
+  }
+
+  struct Frag {
+    uint32_t w[9];
+  };
+
+  __device__ __forceinline__ void load(const uint8_t* rp, Frag& f) const {
+    const uint32_t* q = reinterpret_cast<const uint32_t*>(rp + off);
+#pragma unroll
+    for (int i = 0; i < 9; ++i) f.w[i] = q[i];
+  }
+
+  __device__ __forceinline__ float compute(const Frag& f) const {
+    int l0 = 0, h0 = 0, l1 = 0, h1 = 0;
+#pragma unroll
+    for (int i = 0; i < 5; ++i) {
+      l0 = dp4a_ss(f.w[i] & 0x0F0F0F0Fu, lo0[i], l0);
+      h0 = dp4a_us(f.w[i] & 0xF0F0F0F0u, hi0[i], h0);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      l1 = dp4a_ss(f.w[5 + i] & 0x0F0F0F0Fu, lo1[i], l1);
+      h1 = dp4a_us(f.w[5 + i] & 0xF0F0F0F0u, hi1[i], h1);
+    }
+    const int i0 = l0 + (h0 >> 4) - c0;
+    const int i1 = l1 + (h1 >> 4) - c1;
+    // f16 x f16 products are exact in f32
+    const float s0 = half_bits_to_float(f.w[0]) * dx0;
+    const float s1 = half_bits_to_float(f.w[4] >> 16) * dx1;
+    return fmaf(s0, static_cast<float>(i0), s1 * static_cast<float>(i1));
+  }
+
+  __device__ __forceinline__ float row(const uint8_t* rp) const {
+    Frag f;
+    load(rp, f);
+    return compute(f);
+  }
+};
+
+// Q8_0 weights x Q8_0 activations: the weight unit (68 bytes at 68u) has the
+// same word layout as the activation unit, so word i of one pairs with word i
+// of the other; the activation's scale bytes are zeroed (x0 low half, x8 high
+// half) so the weight's scale bytes multiply 0.
+struct UnitQ80xQ8 {
+  static constexpr int kFmt = 8;
+  static constexpr int kUnitW = 64;
+  static constexpr bool kMixed = false;
+  static constexpr bool kDirect = true;
+  uint32_t a[17];
+  float dx0, dx1;
+  uint32_t off;
+
+  __device__ __forceinline__ static void unit_of(int64_t col, int& u, int& l) {
+    u = static_cast<int>(col >> 6);
+    l = static_cast<int>(col & 63);
+  }
+
+  __device__ __forceinline__ void setup(int u, const uint8_t* xq) {
+    load_q8_unit_words(xq, u, a);
+    dx0 = half_bits_to_float(a[0]);
+    dx1 = half_bits_to_float(a[8] >> 16);
+    a[0] &= 0xFFFF0000u;
+    a[8] &= 0xFFFFu;
+    off = 68u * static_cast<uint32_t>(u);
+  }
+
+  struct Frag {
+    uint32_t w[17];
+  };
+
+  __device__ __forceinline__ void load(const uint8_t* rp, Frag& f) const {
+    const uint32_t* q = reinterpret_cast<const uint32_t*>(rp + off);
+#pragma unroll
+    for (int i = 0; i < 17; ++i) f.w[i] = q[i];
+  }
+
+  __device__ __forceinline__ float compute(const Frag& f) const {
+    int i0 = 0, i1 = 0;
+#pragma unroll
+    for (int i = 0; i < 9; ++i) i0 = dp4a_ss(f.w[i], a[i], i0);
+#pragma unroll
+    for (int i = 9; i < 17; ++i) i1 = dp4a_ss(f.w[i], a[i], i1);
+    const float s0 = half_bits_to_float(f.w[0]) * dx0;
+    const float s1 = half_bits_to_float(f.w[8] >> 16) * dx1;
+    return fmaf(s0, static_cast<float>(i0), s1 * static_cast<float>(i1));
+  }
+
+  __device__ __forceinline__ float row(const uint8_t* rp) const {
+    Frag f;
+    load(rp, f);
+    return compute(f);
+  }
+};
+
+// ---------------------------------------------------------------------------
 // Decoder for a kernel that streams both Q4_K (64-column units) and Q6_K
 // (32-column units) phases: one 64-float activation array serves either
 // format, so both decode loops share one register allocation.
 // ---------------------------------------------------------------------------
 struct UnitChain {
   static constexpr bool kMixed = true;
+  static constexpr bool kDirect = false;
   bool q6;         // set from the phase's format before setup()
   float x[64];     // Q4_K: xa = x[0..31], xb = x[32..63]; Q6_K: x[16a + i]
   float s[4];      // Q4_K: sxa, sxb; Q6_K: sx32[0..3]

@@ -11,8 +11,10 @@
 
 namespace qws {
 
-inline int64_t block_weights(int fmt) { return fmt == 2 ? 32 : 256; }
-inline int64_t block_bytes(int fmt) { return fmt == 2 ? 18 : fmt == 12 ? 144 : fmt == 14 ? 210 : 0; }
+inline int64_t block_weights(int fmt) { return fmt == 2 || fmt == 8 ? 32 : 256; }
+inline int64_t block_bytes(int fmt) {
+  return fmt == 2 ? 18 : fmt == 8 ? 34 : fmt == 12 ? 144 : fmt == 14 ? 210 : 0;
+}
 inline int64_t row_bytes_of(int fmt, int64_t K) { return K / block_weights(fmt) * block_bytes(fmt); }
 
 inline int64_t gcd64(int64_t a, int64_t b) {
@@ -95,6 +97,12 @@ int device_sms();
 cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uint8_t* W2,
                           const float* x, int64_t K, int B, int splits, cudaStream_t st,
                           std::string* why);
+// Q4_0 (wfmt 2) or Q8_0 (wfmt 8) weights times Q8_0 activations xq
+// ([B][K / 32 * 34] bytes), no column split.
+cudaError_t launch_matvec_q8(int wfmt, const Seg* segs, int nseg, const uint8_t* xq, int64_t K,
+                             int B, cudaStream_t st, std::string* why);
+// x (nblocks * 32 floats) -> nblocks Q8_0 blocks
+cudaError_t launch_quantize_q8_0(const float* x, uint8_t* xq, int64_t nblocks, cudaStream_t st);
 // y[b][r] = sum_s part[s][b][r]
 cudaError_t launch_splitk_reduce(const float* part, float* y, int64_t n, int splits,
                                  cudaStream_t st);

@@ -1,6 +1,7 @@
 // matvec.cu -- standalone streaming kernels: quantized matvec (any format,
 // optional column split), fused QKV (three stacked segments), gate/up with the
 // GEGLU epilogue, the split-K reduction, rms_norm and residual_add.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -17,6 +18,8 @@ struct MatvecParams {
   Phase P;                 // phase of column slice 0
   const float* x;          // [B][x_stride]
   int64_t x_stride;
+  const uint8_t* xq;       // Q8_0 activations [B][xq_stride bytes] (kDirect units)
+  int64_t xq_stride;
   int cps;                 // CTAs per column slice
   int64_t w_slice_off;     // byte offset between column slices within a row
   int64_t x_slice_off;     // column offset between slices
@@ -57,8 +60,41 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers)
     reduce_phase(P, R, pos, Epi{}, &g_err_matvec);
   } else {
     pdl_wait();   // x may come from the previous kernel
-    consume_phase<Unit>(P, R, pos, XOfPlain{p.x + slice * p.x_slice_off, p.x_stride},
-                        static_cast<int>(threadIdx.x) - kRoleThreads, C, &g_err_matvec);
+    const int ctid = static_cast<int>(threadIdx.x) - kRoleThreads;
+    if constexpr (Unit::kDirect)
+      consume_phase<Unit>(P, R, pos, XOfQ8{p.xq, p.xq_stride}, ctid, C, &g_err_matvec);
+    else
+      consume_phase<Unit>(P, R, pos, XOfPlain{p.x + slice * p.x_slice_off, p.x_stride}, ctid, C,
+                          &g_err_matvec);
+  }
+}
+
+// quantize_q8: one warp per 32-value block.  amax by a warp max over the
+// bit patterns of |x| (order-preserving for non-negative floats); every
+// decision in f32 with explicitly rounded operations: d = amax / 127,
+// id = 1 / d (0 when d = 0), q = round-half-away(x * id); d is stored as
+// binary16 (round to nearest even).  x must be finite; xq must be 2-byte
+// aligned (blocks are written as halfwords).
+__global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float* __restrict__ x,
+                                                            uint8_t* __restrict__ xq,
+                                                            int64_t nblocks) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int lane = threadIdx.x & 31;
+  const int64_t wpb = blockDim.x >> 5;
+  const int64_t nw = static_cast<int64_t>(gridDim.x) * wpb;
+  for (int64_t k = blockIdx.x * wpb + (threadIdx.x >> 5); k < nblocks; k += nw) {
+    const float v = x[k * 32 + lane];
+    const float amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(v))));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+    const int q = static_cast<int>(roundf(__fmul_rn(v, id)));
+    // the block is 2-byte aligned: 17 halfwords, d then 16 code pairs
+    const unsigned qb = static_cast<unsigned>(q) & 0xFFu;
+    const unsigned next = __shfl_down_sync(0xFFFFFFFFu, qb, 1);
+    unsigned short* blk = reinterpret_cast<unsigned short*>(xq + k * 34);
+    if ((lane & 1) == 0) blk[1 + (lane >> 1)] = static_cast<unsigned short>(qb | (next << 8));
+    if (lane == 0) blk[0] = __half_as_ushort(__float2half_rn(d));
   }
 }
 
@@ -220,9 +256,11 @@ static cudaError_t launch_one(const MatvecParams& p, int threads, size_t smem, i
   return launch_pdl(matvec_kernel<Unit, Epi>, grid, threads, smem, st, p);
 }
 
-cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uint8_t* W2,
-                          const float* x, int64_t K, int B, int splits, cudaStream_t st,
-                          std::string* why) {
+// Tile plan, ring depth and parameters of one streaming launch (without the
+// activation pointers and the CTA split, which depend on the kernel).
+static bool plan_matvec(int fmt, int epi, const Seg* segs, int nseg, const uint8_t* W2,
+                        int64_t K, int B, int splits, bool staged, MatvecParams& p,
+                        int& threads, size_t& smem, std::string* why) {
   const int sms = device_sms();
   const int64_t Ks = K / splits;
   int64_t rows_total = 0;
@@ -231,9 +269,9 @@ cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uin
   std::string reason;
   if (!plan_tiles(fmt, epi, Ks, B, rows_total * splits, sms, kTileTarget, tp, reason)) {
     if (why) *why = reason;
-    return cudaErrorInvalidValue;
+    return false;
   }
-  MatvecParams p{};
+  p = MatvecParams{};
   Phase& P = p.P;
   P.fmt = fmt;
   P.epi = epi;
@@ -252,21 +290,43 @@ cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uin
   P.U = tp.U;
   P.G = tp.G;
   P.T = tp.T;
-  p.x = x;
-  p.x_stride = K;
   p.w_slice_off = P.row_bytes;
   p.x_slice_off = Ks;
   p.y_slice_off = static_cast<int64_t>(B) * segs[0].rows;
   p.stage_bytes = round_up(tp.stage_need + 16, 128);
   p.red_floats = tp.red_floats;
-  p.xs_floats = static_cast<uint32_t>(unit_weights(fmt) * red_stride(tp.U));
+  p.xs_floats = staged ? static_cast<uint32_t>(unit_weights(fmt) * red_stride(tp.U)) : 0u;
   // ring: as deep as the shared-memory budget allows (one CTA per SM), 2..16
   p.S = 16;
   while (p.S > 2 && ring_smem_bytes(p.S, p.stage_bytes, p.red_floats, p.xs_floats) > kSmemBudget)
     --p.S;
-  const size_t smem = ring_smem_bytes(p.S, p.stage_bytes, p.red_floats, p.xs_floats);
-  const int threads = kRoleThreads + tp.C;
+  smem = ring_smem_bytes(p.S, p.stage_bytes, p.red_floats, p.xs_floats);
+  threads = kRoleThreads + tp.C;
+  return true;
+}
 
+// CTAs per column slice: enough to cover the slice's tiles, and all slices
+// together about fill the device (bps CTAs per SM).
+static int split_grid(MatvecParams& p, int bps, int splits) {
+  const int64_t slots = static_cast<int64_t>(bps) * device_sms();
+  int64_t cps = std::max<int64_t>(1, slots / splits);
+  cps = std::min<int64_t>(cps, p.P.n_tiles);
+  p.cps = static_cast<int>(cps);
+  p.P.cta0 = 0;
+  p.P.ncta = p.cps;
+  return static_cast<int>(cps * splits);
+}
+
+cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uint8_t* W2,
+                          const float* x, int64_t K, int B, int splits, cudaStream_t st,
+                          std::string* why) {
+  MatvecParams p;
+  int threads = 0;
+  size_t smem = 0;
+  if (!plan_matvec(fmt, epi, segs, nseg, W2, K, B, splits, true, p, threads, smem, why))
+    return cudaErrorInvalidValue;
+  p.x = x;
+  p.x_stride = K;
   int bps = 1;
   switch (fmt * 4 + epi) {
     case 12 * 4 + EPI_STORE: bps = blocks_per_sm<UnitQ4K, EpiStore>(threads, smem); break;
@@ -278,15 +338,7 @@ cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uin
       if (why) *why = "unsupported format / epilogue";
       return cudaErrorInvalidValue;
   }
-  // CTAs per column slice: enough to cover the slice's tiles, and all slices
-  // together about fill the device
-  const int64_t slots = static_cast<int64_t>(bps) * sms;
-  int64_t cps = std::max<int64_t>(1, slots / splits);
-  cps = std::min<int64_t>(cps, P.n_tiles);
-  p.cps = static_cast<int>(cps);
-  P.cta0 = 0;
-  P.ncta = p.cps;
-  const int grid = static_cast<int>(cps * splits);
+  const int grid = split_grid(p, bps, splits);
   switch (fmt * 4 + epi) {
     case 12 * 4 + EPI_STORE: return launch_one<UnitQ4K, EpiStore>(p, threads, smem, grid, st);
     case 12 * 4 + EPI_GEGLU: return launch_one<UnitQ4K, EpiGeglu>(p, threads, smem, grid, st);
@@ -294,6 +346,34 @@ cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uin
     case 14 * 4 + EPI_STORE: return launch_one<UnitQ6K, EpiStore>(p, threads, smem, grid, st);
     default: return launch_one<UnitQ40, EpiStore>(p, threads, smem, grid, st);
   }
+}
+
+cudaError_t launch_matvec_q8(int wfmt, const Seg* segs, int nseg, const uint8_t* xq, int64_t K,
+                             int B, cudaStream_t st, std::string* why) {
+  MatvecParams p;
+  int threads = 0;
+  size_t smem = 0;
+  if (!plan_matvec(wfmt, EPI_STORE, segs, nseg, nullptr, K, B, 1, false, p, threads, smem, why))
+    return cudaErrorInvalidValue;
+  p.xq = xq;
+  p.xq_stride = K / 32 * 34;
+  if (wfmt == 2) {
+    const int grid = split_grid(p, blocks_per_sm<UnitQ40xQ8, EpiStore>(threads, smem), 1);
+    return launch_one<UnitQ40xQ8, EpiStore>(p, threads, smem, grid, st);
+  }
+  if (wfmt == 8) {
+    const int grid = split_grid(p, blocks_per_sm<UnitQ80xQ8, EpiStore>(threads, smem), 1);
+    return launch_one<UnitQ80xQ8, EpiStore>(p, threads, smem, grid, st);
+  }
+  if (why) *why = "weights must be Q4_0 or Q8_0";
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_quantize_q8_0(const float* x, uint8_t* xq, int64_t nblocks, cudaStream_t st) {
+  const int threads = 256;
+  const int64_t blocks = std::min<int64_t>((nblocks + 7) / 8, 8 * device_sms());
+  return launch_pdl(quantize_q8_0_kernel, static_cast<int>(std::max<int64_t>(blocks, 1)),
+                    threads, 0, st, x, xq, nblocks);
 }
 
 cudaError_t launch_splitk_reduce(const float* part, float* y, int64_t n, int splits,

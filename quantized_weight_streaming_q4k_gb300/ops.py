@@ -12,10 +12,11 @@ import ctypes as C
 import torch
 
 from . import _lib
-from ._lib import OP_DECODE_CHAIN, OP_FFN, OP_MATVEC, Q4_0, Q4_K, Q6_K, QwsError, check, lib
+from ._lib import OP_DECODE_CHAIN, OP_FFN, OP_MATVEC, Q4_0, Q4_K, Q6_K, Q8_0, QwsError, check, lib
 
 __all__ = [
-    "Q4_0", "Q4_K", "Q6_K", "QwsError", "q4k_matvec", "q6k_matvec", "q4_0_matvec", "matvec",
+    "Q4_0", "Q4_K", "Q6_K", "Q8_0", "QwsError", "q4k_matvec", "q6k_matvec", "q4_0_matvec",
+    "matvec", "quantize_q8_0", "q8_matvec", "q8_qkv_proj",
     "q4k_qkv_proj", "q4k_ffn_gate_up_geglu", "q4k_ffn_gate_up_geglu_down", "rms_norm",
     "residual_add", "decode_chain", "workspace_bytes", "device_error", "Layer", "Dims",
     "stream_handle",
@@ -99,6 +100,42 @@ def q4k_qkv_proj(Wq, Wk, Wv, x, hidden: int, q_dim: int, kv_dim: int, out=None, 
                                  _dev(q, "q", torch.float32), _dev(k, "k", torch.float32),
                                  _dev(v, "v", torch.float32), hidden, q_dim, kv_dim,
                                  stream_handle(stream)))
+    return q, k, v
+
+
+def quantize_q8_0(x, n: int, batch: int = 1, out=None, stream=None):
+    """x [batch, n] (or [n]) f32 -> Q8_0 blocks, uint8 [batch, n / 32 * 34] (or flat)."""
+    nbytes = n // 32 * 34
+    if out is None:
+        out = torch.empty((batch, nbytes) if batch > 1 else (nbytes,), dtype=torch.uint8,
+                          device=x.device)
+    check(lib().qws_quantize_q8_0(_dev(x, "x", torch.float32), _dev(out, "xq", torch.uint8), n,
+                                  batch, stream_handle(stream)))
+    return out
+
+
+def q8_matvec(wfmt: int, W, xq, rows: int, hidden: int, batch: int = 1, out=None, stream=None):
+    """y = W @ xq for Q4_0 / Q8_0 weights and Q8_0 activations xq."""
+    y = _out(out, (batch, rows) if batch > 1 else (rows,), xq)
+    check(lib().qws_q8_matvec(wfmt, _dev(W, "W", torch.uint8), _dev(xq, "xq", torch.uint8),
+                              _dev(y, "y", torch.float32), rows, hidden, batch,
+                              stream_handle(stream)))
+    return y
+
+
+def q8_qkv_proj(wfmt: int, Wq, Wk, Wv, xq, hidden: int, q_dim: int, kv_dim: int, out=None,
+                stream=None):
+    if out is None:
+        q = torch.empty(q_dim, dtype=torch.float32, device=xq.device)
+        k = torch.empty(kv_dim, dtype=torch.float32, device=xq.device)
+        v = torch.empty(kv_dim, dtype=torch.float32, device=xq.device)
+    else:
+        q, k, v = out
+    check(lib().qws_q8_qkv_proj(wfmt, _dev(Wq, "Wq", torch.uint8), _dev(Wk, "Wk", torch.uint8),
+                                _dev(Wv, "Wv", torch.uint8), _dev(xq, "xq", torch.uint8),
+                                _dev(q, "q", torch.float32), _dev(k, "k", torch.float32),
+                                _dev(v, "v", torch.float32), hidden, q_dim, kv_dim,
+                                stream_handle(stream)))
     return q, k, v
 
 

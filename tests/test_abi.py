@@ -32,7 +32,8 @@ def test_header_declares_the_expected_calls():
     names = declared_functions()
     for n in ["qws_q4k_matvec", "qws_q6k_matvec", "qws_q4_0_matvec", "qws_q4k_qkv_proj",
               "qws_q4k_ffn_gate_up_geglu_down", "qws_rms_norm", "qws_residual_add",
-              "qws_decode_chain", "qws_workspace_bytes", "qws_last_error", "qws_device_error"]:
+              "qws_decode_chain", "qws_workspace_bytes", "qws_last_error", "qws_device_error",
+              "qws_quantize_q8_0", "qws_q8_matvec", "qws_q8_qkv_proj"]:
         assert n in names
 
 
@@ -125,6 +126,32 @@ def test_silu_ffn_and_residual_norm_checks(lib):
     assert lib.qws_residual_rms_norm(A, A, None, A, 10, C.c_float(1e-6), 1, None) == NULL
     assert lib.qws_residual_rms_norm(A, A, A, A, 0, C.c_float(1e-6), 1, None) == SHAPE
     assert lib.qws_residual_rms_norm(A, A, A, A, 10, C.c_float(-1.0), 1, None) == SHAPE
+
+
+def test_q8_path_checks(lib):
+    Q40, Q80, Q4K = 2, 8, 12
+    assert lib.qws_quantize_q8_0(None, A, 64, 1, None) == NULL
+    assert lib.qws_quantize_q8_0(A, None, 64, 1, None) == NULL
+    assert lib.qws_quantize_q8_0(A, A, 48, 1, None) == SHAPE
+    assert lib.qws_quantize_q8_0(A, A, 0, 1, None) == SHAPE
+    assert lib.qws_quantize_q8_0(A, A, 64, 0, None) == SHAPE
+    assert lib.qws_quantize_q8_0(A + 2, A, 64, 1, None) == ALIGN
+    assert lib.qws_quantize_q8_0(A, A + 1, 64, 1, None) == ALIGN
+    assert lib.qws_q8_matvec(Q4K, A, A, A, 10, 2560, 1, None) == FORMAT
+    assert "Q4_0 or Q8_0" in _err(lib)
+    assert lib.qws_q8_matvec(Q40, None, A, A, 10, 2560, 1, None) == NULL
+    assert lib.qws_q8_matvec(Q40, A + 4, A, A, 10, 2560, 1, None) == ALIGN
+    assert lib.qws_q8_matvec(Q80, A, A + 2, A, 10, 2560, 1, None) == ALIGN
+    assert lib.qws_q8_matvec(Q40, A, A, A, 10, 2592, 1, None) == SHAPE      # not % 64
+    assert lib.qws_q8_matvec(Q40, A, A, A, 10, 20480 + 64, 1, None) == SHAPE
+    assert lib.qws_q8_matvec(Q40, A, A, A, 10, 2560, 9, None) == SHAPE      # 40 * 9 > 320
+    assert lib.qws_q8_matvec(Q40, A, A, A, -1, 2560, 1, None) == SHAPE
+    assert lib.qws_q8_matvec(Q80, A, A, A, 0, 2560, 8, None) == OK
+    assert lib.qws_q8_qkv_proj(Q40, A, A, None, A, A, A, A, 2560, 2048, 1024, None) == NULL
+    assert lib.qws_q8_qkv_proj(Q4K, A, A, A, A, A, A, A, 2560, 2048, 1024, None) == FORMAT
+    assert lib.qws_q8_qkv_proj(Q80, A, A, A, A, A, A, A, 2560, 0, 0, None) == OK
+    # the f32-activation entry points do not take Q8_0 weights
+    assert lib.qws_matvec(Q80, A, A, A, 10, 2560, 1, 1, None, 0, None) == FORMAT
 
 
 def test_vector_op_checks(lib):
