@@ -10,6 +10,8 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
        [--op OP --batch B]  time one operation alone, back to back (not the
                         decode step): lm_head_q4_0 (f32 activations),
                         lm_head_q8 (quantize_q8 + Q4_0 x Q8_0 matvec),
+                        lm_head_q4_k / lm_head_q6_k (the same 262144 x 2560
+                        shape in Q4_K / Q6_K, f32 activations),
                         ffn (fused gate/up GEGLU + Q6_K down, 2560/10240)
 For N > 1 launch with torchrun; every rank runs an independent replica of the
 step on its own GPU (the path has no data exchange; "replicas only").
@@ -377,7 +379,21 @@ def run_op(args):
     H, I, B = 2560, 10240, args.batch
     g = synth.rng(synth.W_LM_HEAD, 0)
     launches = 1
-    if args.op in ("lm_head_q4_0", "lm_head_q8"):
+    if args.op in ("lm_head_q4_k", "lm_head_q6_k"):
+        fmt = synth.Q4_K if args.op == "lm_head_q4_k" else synth.Q6_K
+        W = torch.from_numpy(synth.matrix(fmt, g, VOCAB, H)).to(dev)
+        x = torch.from_numpy(synth.normal_vector(g, H, B if B > 1 else None)).to(dev)
+        y = torch.empty((B, VOCAB) if B > 1 else (VOCAB,), device=dev)
+        ws = None
+        if B * H // 64 > 320:
+            raise SystemExit("batch too large for one pass at hidden 2560")
+
+        def call():
+            ops.matvec(fmt, W, x, VOCAB, H, B, 1, ws, out=y)
+        nbytes = synth.n_blocks(fmt, VOCAB, H) * synth.BLOCK_BYTES[fmt] + B * H * 4 + B * VOCAB * 4
+        kernel = f"matvec_kernel<{'UnitQ4K' if fmt == synth.Q4_K else 'UnitQ6K'}> (f32 activations)"
+        workload = f"matvec {VOCAB}x{H} {'Q4_K' if fmt == synth.Q4_K else 'Q6_K'}, batch {B}"
+    elif args.op in ("lm_head_q4_0", "lm_head_q8"):
         W = torch.from_numpy(synth.q4_0_matrix(g, VOCAB, H)).to(dev)
         x = torch.from_numpy(synth.normal_vector(g, H, B if B > 1 else None)).to(dev)
         y = torch.empty((B, VOCAB) if B > 1 else (VOCAB,), device=dev)
@@ -469,7 +485,8 @@ def main():
     ap.add_argument("--n-layers", type=int, default=N_LAYERS,
                     help="chain length (default 34; shorter only for profiler captures)")
     ap.add_argument("--op", default="step",
-                    choices=["step", "lm_head_q4_0", "lm_head_q8", "ffn"],
+                    choices=["step", "lm_head_q4_0", "lm_head_q8", "lm_head_q4_k",
+                             "lm_head_q6_k", "ffn"],
                     help="step (default): the decode step; otherwise one operation alone")
     ap.add_argument("--batch", type=int, default=1, help="activation vectors (--op only)")
     args = ap.parse_args()
