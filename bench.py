@@ -12,7 +12,9 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                         lm_head_q8 (quantize_q8 + Q4_0 x Q8_0 matvec),
                         lm_head_q4_k / lm_head_q6_k (the same 262144 x 2560
                         shape in Q4_K / Q6_K, f32 activations),
-                        ffn (fused gate/up GEGLU + Q6_K down, 2560/10240)
+                        ffn (fused gate/up GEGLU + Q6_K down, 2560/10240),
+                        prefill (Q4_K 10240 x 2560 times --batch tokens on the
+                        tensor cores; TFLOP/s)
 For N > 1 launch with torchrun; every rank runs an independent replica of the
 step on its own GPU (the path has no data exchange; "replicas only").
 """
@@ -57,6 +59,18 @@ def peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def tensor_peak():
+    """Dense f16/bf16 tensor peak (same nominal rate for both): the measured
+    cuBLAS bf16 burst figure, else the fallback."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        if "bf16_tflops" in d:
+            return float(d["bf16_tflops"]), "measured (bf16 burst; f16 has the same nominal rate)"
+    return 1900.0, "fallback"
 
 
 def profiled_traffic(n_layers=N_LAYERS):
@@ -421,6 +435,21 @@ def run_op(args):
             nbytes = wbytes + B * H * 4 + 2 * B * (H // 32 * 34) + B * VOCAB * 4
             kernel = "quantize_q8_0_kernel + matvec_kernel<UnitQ40xQ8>"
         workload = f"lm_head {VOCAB}x{H} Q4_0, batch {B}"
+    elif args.op == "prefill":
+        rows, N = I, B
+        W = torch.from_numpy(synth.q4_k_matrix(g, rows, H)).to(dev)
+        x = torch.from_numpy(synth.normal_vector(g, H, N)).to(dev)
+        y = torch.empty((N, rows), device=dev)
+        ws = torch.empty(ops.workspace_bytes(ops.OP_PREFILL, 0, H, 0, N), dtype=torch.uint8,
+                         device=dev)
+
+        def call():
+            ops.q4k_prefill_matmul(W, x, rows, H, N, workspace=ws, out=y)
+        launches = 2
+        nbytes = synth.n_blocks(synth.Q4_K, rows, H) * 144 + N * H * 4 + N * rows * 4
+        flops = 2.0 * rows * H * N
+        kernel = "prefill_q4k_kernel (tcgen05 kind::f16) + prefill_pack_x_kernel"
+        workload = f"prefill Q4_K {rows}x{H}, {N} tokens"
     elif args.op == "ffn":
         gl = synth.rng(synth.W_FFN, 0)
         Wg = torch.from_numpy(synth.q4_k_matrix(gl, I, H)).to(dev)
@@ -462,6 +491,22 @@ def run_op(args):
     us = 1e3 * a.elapsed_time(b) / args.steps
     gbs = nbytes / (us * 1e-6) / 1e9
     peak, peak_kind = peaks()
+    if args.op == "prefill":
+        tfs = flops / (us * 1e-6) / 1e12
+        tpeak, tkind = tensor_peak()
+        print(json.dumps({
+            "metric": "prefill achieved TFLOP/s", "value": tfs, "unit": "TFLOP/s", "n_gpus": 1,
+            "steps": args.steps, "warmup": max(3, args.warmup), "us_per_call": us,
+            "higher_is_better": True, "dtype": "f16 operands, f32 accumulation",
+            "data": "synthetic (seeded random blocks)",
+            "config": {"workload": workload, "batch": B,
+                       "l2": "back to back; weights 14.7 MB (L2-resident across calls)"},
+            "roofline": {"bound": "tensor", "kernel": kernel, "achieved": tfs, "peak": tpeak,
+                         "unit": "TFLOP/s", "frac": tfs / tpeak, "peak_source": tkind,
+                         "traffic": None},
+            "hbm_gbs": gbs, "gpu_launches": launches * args.steps, "clocks": clk,
+        }))
+        return
     print(json.dumps({
         "metric": f"{args.op} achieved HBM GB/s", "value": gbs, "unit": "GB/s", "n_gpus": 1,
         "steps": args.steps, "warmup": max(3, args.warmup), "us_per_call": us,
@@ -486,7 +531,7 @@ def main():
                     help="chain length (default 34; shorter only for profiler captures)")
     ap.add_argument("--op", default="step",
                     choices=["step", "lm_head_q4_0", "lm_head_q8", "lm_head_q4_k",
-                             "lm_head_q6_k", "ffn"],
+                             "lm_head_q6_k", "ffn", "prefill"],
                     help="step (default): the decode step; otherwise one operation alone")
     ap.add_argument("--batch", type=int, default=1, help="activation vectors (--op only)")
     args = ap.parse_args()

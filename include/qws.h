@@ -78,7 +78,8 @@ typedef enum { QWS_Q4_0 = 2, QWS_Q8_0 = 8, QWS_Q4_K = 12, QWS_Q6_K = 14 } qws_fo
 typedef enum {
   QWS_OP_MATVEC = 0,      /* qws_matvec / qws_q4_0_matvec with split_k > 1 */
   QWS_OP_FFN = 1,         /* qws_q4k_ffn_gate_up_geglu_down                */
-  QWS_OP_DECODE_CHAIN = 2 /* qws_decode_chain                              */
+  QWS_OP_DECODE_CHAIN = 2, /* qws_decode_chain                             */
+  QWS_OP_PREFILL = 3       /* qws_q4k_prefill_matmul (batch = n_tokens)     */
 } qws_op;
 
 /* ------------------------------------------------------------------------
@@ -159,6 +160,26 @@ qws_status qws_q8_matvec(qws_format wfmt, const void* W, const void* xq, float* 
 qws_status qws_q8_qkv_proj(qws_format wfmt, const void* Wq, const void* Wk, const void* Wv,
                            const void* xq, float* q, float* k, float* v, int64_t hidden,
                            int64_t q_dim, int64_t kv_dim, qws_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Prefill: the Q4_K product for many tokens at once (infer-compute README
+ * §Quick Start and §Architecture, prefill_q4: the seq > 1 GPU path), on the
+ * tensor cores:   Y[n][r] = sum_k dequant(W)[r][k] * X[n][k].
+ *   W  rows x hidden Q4_K (device, 16-byte aligned)
+ *   X  [n_tokens][hidden] f32 (device, 16-byte aligned)
+ *   Y  [n_tokens][rows] f32 (device, 4-byte aligned), overwritten
+ *   ws >= qws_workspace_bytes(QWS_OP_PREFILL, 0, hidden, 0, n_tokens, 0)
+ *      bytes (device, 16-byte aligned): X rounded to f16, in tiles
+ *   rows >= 0; hidden > 0, hidden % 256 == 0; n_tokens >= 1.
+ * Precision: both operands are rounded to f16 (round to nearest even; the
+ * weight after its f32 dequantization) and multiplied with f32 accumulation,
+ * so |Y - Y_exact| <= ~2^-10 * sum_k |w x| (plus 2^-25 per f16-subnormal
+ * operand).  |x| and |w| must stay below 65504.  Results are identical run
+ * to run.  The pages do not state the precision of their prefill path.
+ * ---------------------------------------------------------------------- */
+qws_status qws_q4k_prefill_matmul(const void* W, const float* X, float* Y, int64_t rows,
+                                  int64_t hidden, int64_t n_tokens, void* ws, size_t ws_bytes,
+                                  qws_stream stream);
 
 /* ------------------------------------------------------------------------
  * Gated FFN (infer-compute README §Shaders "Q4_K fused FFN": q4k_ffn_gate_up,

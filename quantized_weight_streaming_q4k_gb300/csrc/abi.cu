@@ -265,6 +265,37 @@ qws_status qws_q8_qkv_proj(qws_format wfmt, const void* Wq, const void* Wk, cons
   return ok();
 }
 
+qws_status qws_q4k_prefill_matmul(const void* W, const float* X, float* Y, int64_t rows,
+                                  int64_t hidden, int64_t n_tokens, void* ws, size_t ws_bytes,
+                                  qws_stream stream) {
+  const char* fn = "qws_q4k_prefill_matmul";
+  QWS_CHECK_W(W);
+  QWS_CHECK_PTR(X);
+  if (!aligned(X, 16)) return fail(QWS_ERR_ALIGN, "%s: X is not 16-byte aligned", fn);
+  QWS_CHECK_F(Y);
+  if (rows < 0) return fail(QWS_ERR_SHAPE, "%s: rows = %lld < 0", fn, (long long)rows);
+  if (hidden <= 0 || hidden % 256)
+    return fail(QWS_ERR_SHAPE, "%s: hidden = %lld is not a positive multiple of 256", fn,
+                (long long)hidden);
+  if (n_tokens < 1 || n_tokens > (int64_t(1) << 30))
+    return fail(QWS_ERR_SHAPE, "%s: n_tokens = %lld outside [1, 2^30]", fn,
+                (long long)n_tokens);
+  if (rows > (int64_t(1) << 40) / n_tokens)
+    return fail(QWS_ERR_SHAPE, "%s: rows * n_tokens too large", fn);
+  const size_t need = qws::prefill_workspace_bytes(hidden, n_tokens);
+  if (!ws || ws_bytes < need)
+    return fail(QWS_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", fn, ws_bytes, need);
+  if (!aligned(ws, 16)) return fail(QWS_ERR_ALIGN, "%s: ws is not 16-byte aligned", fn);
+  if ((rows + 127) / 128 * ((n_tokens + 255) / 256) > (int64_t(1) << 31) - 1)
+    return fail(QWS_ERR_SHAPE, "%s: too many tiles", fn);
+  if (rows == 0) return ok();
+  cudaError_t e = qws::launch_prefill_q4k(static_cast<const uint8_t*>(W), X, Y, rows, hidden,
+                                          n_tokens, static_cast<uint8_t*>(ws),
+                                          reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn, "");
+  return ok();
+}
+
 static qws_status check_ffn_shape(const char* fn, int64_t hidden, int64_t inter) {
   if (hidden <= 0 || hidden % 256 || hidden > kMaxHidden)
     return fail(QWS_ERR_SHAPE, "%s: hidden = %lld (need a multiple of 256 in (0, 20480])", fn,
@@ -421,6 +452,9 @@ size_t qws_workspace_bytes(qws_op op, int64_t rows, int64_t hidden, int64_t inte
       return inter > 0 ? round256(sizeof(float) * static_cast<size_t>(inter)) : 0;
     case QWS_OP_DECODE_CHAIN:
       return qws::chain_workspace_bytes(hidden, inter);
+    case QWS_OP_PREFILL:
+      if (hidden <= 0 || hidden % 256 || batch < 1) return 0;
+      return round256(qws::prefill_workspace_bytes(hidden, batch));
   }
   return 0;
 }
@@ -431,7 +465,8 @@ qws_status qws_device_error(unsigned* code) {
   if (!code) return fail(QWS_ERR_NULL, "qws_device_error: code is NULL");
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "qws_device_error", "");
-  *code = qws::read_clear_matvec_errors() | qws::read_clear_chain_errors();
+  *code = qws::read_clear_matvec_errors() | qws::read_clear_chain_errors() |
+          qws::read_clear_prefill_errors();
   return *code ? fail(QWS_ERR_TIMEOUT, "device error code 0x%x", *code) : ok();
 }
 

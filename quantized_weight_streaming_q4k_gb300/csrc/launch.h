@@ -103,6 +103,11 @@ cudaError_t launch_matvec_q8(int wfmt, const Seg* segs, int nseg, const uint8_t*
                              int B, cudaStream_t st, std::string* why);
 // x (nblocks * 32 floats) -> nblocks Q8_0 blocks
 cudaError_t launch_quantize_q8_0(const float* x, uint8_t* xq, int64_t nblocks, cudaStream_t st);
+// prefill (prefill.cu): X packed to f16 tiles in ws, then the tcgen05 GEMM
+size_t prefill_workspace_bytes(int64_t hidden, int64_t n_tokens);
+cudaError_t launch_prefill_q4k(const uint8_t* W, const float* X, float* Y, int64_t rows,
+                               int64_t K, int64_t N, uint8_t* ws, cudaStream_t st);
+unsigned read_clear_prefill_errors();
 // y[b][r] = sum_s part[s][b][r]
 cudaError_t launch_splitk_reduce(const float* part, float* y, int64_t n, int splits,
                                  cudaStream_t st);

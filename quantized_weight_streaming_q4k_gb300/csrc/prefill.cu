@@ -1,0 +1,459 @@
+// prefill.cu -- the batch-N (prefill) Q4_K matrix product on the 5th-generation
+// tensor cores: Y[n][r] = sum_k W[r][k] * X[n][k] for N token vectors at once
+// (infer-compute README §Quick Start / §Shaders, prefill_q4: the seq > 1
+// path).  At N >= ~100 the product is compute-bound, so it runs as a GEMM:
+//
+//   * X (f32 [N][K]) is first rounded to f16 and written, by a small packing
+//     kernel, into the workspace already in the shared-memory image the MMA
+//     reads: tiles of 256 tokens x 64 columns (32 KB), each a contiguous run
+//     in the 128-byte-swizzled K-major layout.  A tile then moves into shared
+//     memory as one 1-D bulk copy (TMA).
+//   * The weights stay packed in HBM.  Four decoder warps (one weight row per
+//     thread) read a row's 64-column chunk (its 32 nibble bytes and the
+//     super-block header), dequantize w = d*sc*q - dmin*m in f32, round to f16
+//     and store the 128-byte row into the swizzled A tile.
+//   * One thread issues tcgen05.mma (kind::f16, M = 128 rows, N = 256 tokens,
+//     K = 16 per instruction, f32 accumulation) with both operands in shared
+//     memory and the accumulator in tensor memory (256 TMEM columns); a
+//     tcgen05.commit per stage frees that stage when its MMAs have read it.
+//   * The decoder warps then read the accumulator back with tcgen05.ld (warp
+//     w reads TMEM lanes 32*(w % 4) .. +31 = its 32 weight rows) and store Y
+//     with coalesced 128-byte rows.
+//
+// Shared-memory layout of one operand tile (K-major, 128-byte swizzle): row i
+// (a weight row for A, a token for B) holds 64 f16 = 128 bytes at
+// (i / 8) * 1024 + (i % 8) * 128; inside it, 16-byte chunk c (columns
+// 8c .. 8c+7) sits at chunk position c ^ (i % 8).  Tiles start on 1024-byte
+// boundaries.  Descriptor: start >> 4, leading offset 16 B (unused by this
+// layout), stride offset 1024 B between 8-row groups, version 1, swizzle mode
+// 128 B.  The k-th 16-column slice of a tile starts 32 * k bytes in.
+//
+// Every wait is bounded; on a timeout the thread records kErrPrefill* in the
+// module's error word and the kernel still frees its tensor memory.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+
+#include "launch.h"
+
+namespace qws {
+
+__device__ unsigned g_err_prefill;
+
+constexpr int kPfM = 128;                  // weight rows per tile (MMA M, TMEM lanes)
+constexpr int kPfN = 256;                  // tokens per tile (MMA N, TMEM columns)
+constexpr int kPfK = 64;                   // columns per stage: one 128-byte f16 row
+constexpr int kPfStages = 4;
+constexpr uint32_t kPfATile = kPfM * kPfK * 2;     // 16 KB
+constexpr uint32_t kPfBTile = kPfN * kPfK * 2;     // 32 KB
+constexpr uint32_t kPfStage = kPfATile + kPfBTile;
+constexpr int kPfThreads = 192;            // warp 0 copies, warp 1 MMA, warps 2..5 decode
+constexpr int kPfDecoders = 128;
+constexpr uint32_t kPfTmemCols = 256;
+constexpr size_t kPfSmemBytes = 1024 + kPfStages * kPfStage + 256;
+
+// f32 accumulate, f16 A and B, both K-major, N = 256, M = 128.
+constexpr uint32_t kPfIdesc = (1u << 4) | (0u << 7) | (0u << 10) |
+                              (static_cast<uint32_t>(kPfN >> 3) << 17) |
+                              (static_cast<uint32_t>(kPfM >> 4) << 24);
+
+struct PrefillParams {
+  const uint8_t* W;       // Q4_K, rows x K
+  const uint8_t* X16;     // packed f16 tiles [n_tiles_n][KC][32 KB]
+  float* Y;               // [N][rows]
+  int64_t rows, K, N;
+  int KC;                 // K / 64
+  int n_tiles_n;
+};
+
+// ------------------------------------------------------------ tcgen05 wrappers
+__device__ __forceinline__ void tmem_alloc(uint32_t* dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                   smem_addr(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// arrives on `bar` once every tcgen05.mma this thread issued before has completed
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+          smem_addr(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+        "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+        "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tc_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// two f32 -> packed f16x2 (round to nearest even); lo in bits 0..15
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Shared-memory matrix descriptor of a 128-byte-swizzled K-major tile.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr) {
+  return static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4) | (static_cast<uint64_t>(1) << 16) |
+         (static_cast<uint64_t>(1024 >> 4) << 32) | (static_cast<uint64_t>(1) << 46) |
+         (static_cast<uint64_t>(2) << 61);
+}
+
+// byte offset of 16-byte chunk c of row i inside a swizzled tile
+__host__ __device__ constexpr uint32_t sw128_off(uint32_t i, uint32_t c) {
+  return (i >> 3) * 1024u + (i & 7u) * 128u + ((c ^ (i & 7u)) << 4);
+}
+
+// ------------------------------------------------------------ X packing
+// X [N][K] f32 -> f16 tiles of 256 tokens x 64 columns in the swizzled image;
+// tokens N .. n_tiles_n * 256 - 1 are zero.
+__global__ void __launch_bounds__(256) prefill_pack_x_kernel(const float* __restrict__ X,
+                                                             uint8_t* __restrict__ X16,
+                                                             int64_t N, int64_t K,
+                                                             int n_tiles_n) {
+  pdl_launch_dependents();
+  pdl_wait();
+  const int64_t chunks = K / 8;
+  const int64_t total = static_cast<int64_t>(n_tiles_n) * kPfN * chunks;
+  const int KC = static_cast<int>(K / kPfK);
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t tok = i / chunks;
+    const int64_t qk = i - tok * chunks;
+    float v[8];
+    if (tok < N) {
+      const float4* p = reinterpret_cast<const float4*>(X + tok * K + qk * 8);
+      const float4 a = p[0], b = p[1];
+      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+    } else {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[j] = 0.f;
+    }
+    uint4 o;
+    o.x = pack_f16x2(v[0], v[1]);
+    o.y = pack_f16x2(v[2], v[3]);
+    o.z = pack_f16x2(v[4], v[5]);
+    o.w = pack_f16x2(v[6], v[7]);
+    const int64_t tn = tok / kPfN;
+    const uint32_t t = static_cast<uint32_t>(tok - tn * kPfN);
+    const int64_t kc = qk / 8;
+    const uint32_t c = static_cast<uint32_t>(qk - kc * 8);
+    uint8_t* tile = X16 + (tn * KC + kc) * static_cast<int64_t>(kPfBTile);
+    *reinterpret_cast<uint4*>(tile + sw128_off(t, c)) = o;
+  }
+}
+
+// ------------------------------------------------------------ Q4_K row chunk
+// Dequantizes columns 64c .. 64c + 63 of one super-block (c = chunk 0..3) to
+// f32 and stores them as one swizzled 128-byte f16 row.  hd = the block's
+// first 16 bytes (d, dmin, 12 scale bytes), q0/q1 = its qs bytes 32c .. 32c+31.
+// Column l < 32 is the low nibble of qs byte 32c + l (sub-block 2c), column
+// 32 + l the high nibble (sub-block 2c + 1); w = d*sc*q - dmin*m.
+__device__ __forceinline__ float nib_to_float(uint32_t v) {
+  // v in 0..15: 2^23 + v is exact, minus 2^23 gives v
+  return __uint_as_float(0x4B000000u | v) - 8388608.0f;
+}
+
+__device__ __forceinline__ void q4k_chunk_to_f16_row(const uint4 hd, const uint4 q0,
+                                                     const uint4 q1, int c, uint8_t* tile,
+                                                     uint32_t row) {
+  const bool hi = c >= 2;
+  const uint32_t sh = 16u * static_cast<uint32_t>(c & 1);
+  const uint32_t S = hi ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u))
+                        : (hd.y & 0x3F3F3F3Fu);
+  const uint32_t M = hi ? (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u))
+                        : (hd.z & 0x3F3F3F3Fu);
+  const float d = half_bits_to_float(hd.x);
+  const float dmin = half_bits_to_float(hd.x >> 16);
+  const float a_lo = d * static_cast<float>((S >> sh) & 0xFFu);
+  const float a_hi = d * static_cast<float>((S >> (sh + 8)) & 0xFFu);
+  const float b_lo = -dmin * static_cast<float>((M >> sh) & 0xFFu);
+  const float b_hi = -dmin * static_cast<float>((M >> (sh + 8)) & 0xFFu);
+  const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+  for (int ch = 0; ch < 8; ++ch) {
+    // chunk ch: columns 8ch .. 8ch + 7; ch < 4 low nibbles of qs 8ch .., else
+    // high nibbles of qs 8(ch - 4) ..
+    const bool high = ch >= 4;
+    const uint32_t wa = w[2 * (ch & 3)], wb = w[2 * (ch & 3) + 1];
+    const float a = high ? a_hi : a_lo;
+    const float b = high ? b_hi : b_lo;
+    const uint32_t s0 = high ? 4u : 0u;
+    float f[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      f[j] = fmaf(a, nib_to_float((wa >> (8 * j + s0)) & 0xFu), b);
+      f[4 + j] = fmaf(a, nib_to_float((wb >> (8 * j + s0)) & 0xFu), b);
+    }
+    uint4 o;
+    o.x = pack_f16x2(f[0], f[1]);
+    o.y = pack_f16x2(f[2], f[3]);
+    o.z = pack_f16x2(f[4], f[5]);
+    o.w = pack_f16x2(f[6], f[7]);
+    *reinterpret_cast<uint4*>(tile + sw128_off(row, static_cast<uint32_t>(ch))) = o;
+  }
+}
+
+struct Q4kChunk {
+  uint4 hd, q0, q1;
+};
+
+__device__ __forceinline__ void load_q4k_chunk(const uint8_t* rowp, int kc, Q4kChunk& v) {
+  const uint8_t* bp = rowp + static_cast<int64_t>(kc >> 2) * 144;
+  const int c = kc & 3;
+  v.hd = __ldg(reinterpret_cast<const uint4*>(bp));
+  v.q0 = __ldg(reinterpret_cast<const uint4*>(bp + 16 + 32 * c));
+  v.q1 = __ldg(reinterpret_cast<const uint4*>(bp + 32 + 32 * c));
+}
+
+// ------------------------------------------------------------ the GEMM kernel
+enum : unsigned {
+  kErrPfFull = 16u,      // MMA issuer gave up waiting for a stage
+  kErrPfEmpty = 32u,     // a producer gave up waiting for a free stage
+  kErrPfDone = 64u,      // the epilogue gave up waiting for the accumulator
+};
+
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid_constant__
+                                                                    PrefillParams p) {
+  extern __shared__ __align__(1024) uint8_t pf_smem_raw[];
+  // 1024-byte-aligned stage area, then the barriers and the TMEM address slot
+  const uint32_t raw = smem_addr(pf_smem_raw);
+  uint8_t* stages = pf_smem_raw + ((1024u - (raw & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(stages + kPfStages * kPfStage);
+  uint64_t* empty = full + kPfStages;
+  uint64_t* done = empty + kPfStages;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
+
+  const int warp = static_cast<int>(threadIdx.x >> 5);
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  const int tm = static_cast<int>(blockIdx.x) / p.n_tiles_n;
+  const int tn = static_cast<int>(blockIdx.x) - tm * p.n_tiles_n;
+  const int64_t m0 = static_cast<int64_t>(tm) * kPfM;
+  const int KC = p.KC;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kPfStages; ++s) {
+      mbar_init(&full[s], kPfDecoders + 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kPfTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  pdl_launch_dependents();
+  pdl_wait();   // X16 is written by the packing kernel just before
+
+  bool ok = true;
+  if (warp == 0) {
+    // ---- B producer: one 32 KB bulk copy per stage
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      const uint8_t* xb = p.X16 + static_cast<int64_t>(tn) * KC * kPfBTile;
+      for (int kc = 0; kc < KC; ++kc) {
+        const int s = kc % kPfStages;
+        const uint32_t ph = static_cast<uint32_t>(kc / kPfStages) & 1u;
+        if (!mbar_wait(&empty[s], ph ^ 1u)) {
+          atomicOr(&g_err_prefill, kErrPfEmpty);
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[s], kPfBTile);
+        bulk_copy_g2s(stages + s * kPfStage + kPfATile, xb + static_cast<int64_t>(kc) * kPfBTile,
+                      kPfBTile, &full[s], pol);
+      }
+      (void)ok;
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer
+    if (lane == 0) {
+      for (int kc = 0; kc < KC; ++kc) {
+        const int s = kc % kPfStages;
+        const uint32_t ph = static_cast<uint32_t>(kc / kPfStages) & 1u;
+        if (!mbar_wait(&full[s], ph)) {
+          atomicOr(&g_err_prefill, kErrPfFull);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a = smem_addr(stages + s * kPfStage);
+        const uint32_t b = a + kPfATile;
+#pragma unroll
+        for (int k = 0; k < kPfK / 16; ++k)
+          tc_mma_f16(tmem, sw128_desc(a + 32u * k), sw128_desc(b + 32u * k), kPfIdesc,
+                     (kc | k) != 0 ? 1u : 0u);
+        tc_commit(&empty[s]);
+      }
+      // the accumulator is final once every MMA above has completed
+      tc_commit(done);
+    }
+  } else {
+    // ---- decoders (one weight row each), then the epilogue
+    const int d = static_cast<int>(threadIdx.x) - 64;
+    const uint32_t row = static_cast<uint32_t>(d);
+    const int64_t r = m0 + d;
+    const bool live = r < p.rows;
+    const int64_t row_bytes = p.K / 256 * 144;
+    const uint8_t* rowp = p.W + (live ? r : 0) * row_bytes;
+    Q4kChunk cur, nxt;
+    if (live) load_q4k_chunk(rowp, 0, cur);
+    for (int kc = 0; kc < KC; ++kc) {
+      const int s = kc % kPfStages;
+      const uint32_t ph = static_cast<uint32_t>(kc / kPfStages) & 1u;
+      if (live && kc + 1 < KC) load_q4k_chunk(rowp, kc + 1, nxt);
+      if (!mbar_wait(&empty[s], ph ^ 1u)) {
+        atomicOr(&g_err_prefill, kErrPfEmpty);
+        ok = false;
+        break;
+      }
+      uint8_t* tile = stages + s * kPfStage;
+      if (live) {
+        q4k_chunk_to_f16_row(cur.hd, cur.q0, cur.q1, kc & 3, tile, row);
+      } else {
+        const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int ch = 0; ch < 8; ++ch)
+          *reinterpret_cast<uint4*>(tile + sw128_off(row, static_cast<uint32_t>(ch))) = z;
+      }
+      fence_proxy_async_smem();   // generic-proxy stores -> visible to the MMA
+      mbar_arrive(&full[s]);
+      cur = nxt;
+    }
+    // ---- epilogue: TMEM lanes 32 * (warp % 4) .. + 31 are this warp's rows
+    if (!mbar_wait(done, 0u)) {
+      atomicOr(&g_err_prefill, kErrPfDone);
+      ok = false;
+    }
+    tc_fence_after();
+    if (ok) {
+      const int q = warp & 3;
+      const int64_t rr = m0 + 32 * q + lane;
+      const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16);
+      const int64_t n0 = static_cast<int64_t>(tn) * kPfN;
+      for (int cc = 0; cc < kPfN; cc += 16) {
+        uint32_t v[16];
+        tc_ld16(tbase + static_cast<uint32_t>(cc), v);
+        tc_wait_ld();
+        if (rr < p.rows) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int64_t n = n0 + cc + j;
+            if (n < p.N) p.Y[n * p.rows + rr] = __uint_as_float(v[j]);
+          }
+        }
+      }
+    }
+  }
+  // every MMA has completed before the accumulator is freed: wait (bounded)
+  // for the final commit on all paths, including after a timeout
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    if (lane == 0 && !mbar_wait(done, 0u)) atomicOr(&g_err_prefill, kErrPfDone);
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kPfTmemCols);
+  }
+}
+
+// ------------------------------------------------------------ host side
+size_t prefill_workspace_bytes(int64_t hidden, int64_t n_tokens) {
+  const int64_t tiles = (n_tokens + kPfN - 1) / kPfN;
+  return static_cast<size_t>(tiles) * kPfN * static_cast<size_t>(hidden) * 2;
+}
+
+template <class... KArgs, class... Args>
+static cudaError_t launch_pdl_pf(void (*kernel)(KArgs...), int grid, int threads, size_t smem,
+                                 cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
+cudaError_t launch_prefill_q4k(const uint8_t* W, const float* X, float* Y, int64_t rows,
+                               int64_t K, int64_t N, uint8_t* ws, cudaStream_t st) {
+  const int n_tiles_n = static_cast<int>((N + kPfN - 1) / kPfN);
+  const int n_tiles_m = static_cast<int>((rows + kPfM - 1) / kPfM);
+  const int64_t pack_total = static_cast<int64_t>(n_tiles_n) * kPfN * (K / 8);
+  const int64_t pack_blocks = std::min<int64_t>((pack_total + 255) / 256, 8 * device_sms());
+  cudaError_t e = launch_pdl_pf(prefill_pack_x_kernel, static_cast<int>(pack_blocks), 256, 0, st,
+                                X, ws, N, K, n_tiles_n);
+  if (e != cudaSuccess) return e;
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    e = cudaFuncSetAttribute(prefill_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kPfSmemBytes));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  PrefillParams p;
+  p.W = W;
+  p.X16 = ws;
+  p.Y = Y;
+  p.rows = rows;
+  p.K = K;
+  p.N = N;
+  p.KC = static_cast<int>(K / kPfK);
+  p.n_tiles_n = n_tiles_n;
+  return launch_pdl_pf(prefill_q4k_kernel, n_tiles_m * n_tiles_n, kPfThreads, kPfSmemBytes, st,
+                       p);
+}
+
+unsigned read_clear_prefill_errors() {
+  unsigned v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_prefill, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(g_err_prefill, &z, sizeof(z));
+  return v;
+}
+
+}  // namespace qws

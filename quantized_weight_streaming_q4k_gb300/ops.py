@@ -12,11 +12,12 @@ import ctypes as C
 import torch
 
 from . import _lib
-from ._lib import OP_DECODE_CHAIN, OP_FFN, OP_MATVEC, Q4_0, Q4_K, Q6_K, Q8_0, QwsError, check, lib
+from ._lib import (OP_DECODE_CHAIN, OP_FFN, OP_MATVEC, OP_PREFILL, Q4_0, Q4_K, Q6_K, Q8_0,
+                   QwsError, check, lib)
 
 __all__ = [
     "Q4_0", "Q4_K", "Q6_K", "Q8_0", "QwsError", "q4k_matvec", "q6k_matvec", "q4_0_matvec",
-    "matvec", "quantize_q8_0", "q8_matvec", "q8_qkv_proj",
+    "matvec", "quantize_q8_0", "q8_matvec", "q8_qkv_proj", "q4k_prefill_matmul",
     "q4k_qkv_proj", "q4k_ffn_gate_up_geglu", "q4k_ffn_gate_up_geglu_down", "rms_norm",
     "residual_add", "decode_chain", "workspace_bytes", "device_error", "Layer", "Dims",
     "stream_handle",
@@ -137,6 +138,21 @@ def q8_qkv_proj(wfmt: int, Wq, Wk, Wv, xq, hidden: int, q_dim: int, kv_dim: int,
                                 _dev(v, "v", torch.float32), hidden, q_dim, kv_dim,
                                 stream_handle(stream)))
     return q, k, v
+
+
+def q4k_prefill_matmul(W, X, rows: int, hidden: int, n_tokens: int, workspace=None, out=None,
+                       stream=None):
+    """Y [n_tokens, rows] = X [n_tokens, hidden] @ dequant_Q4_K(W)^T on the tensor cores
+    (f16 operands, f32 accumulation)."""
+    Y = _out(out, (n_tokens, rows), X)
+    need = workspace_bytes(OP_PREFILL, 0, hidden, 0, n_tokens, 0)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=X.device)
+    check(lib().qws_q4k_prefill_matmul(
+        _dev(W, "W", torch.uint8), _dev(X, "X", torch.float32), _dev(Y, "Y", torch.float32),
+        rows, hidden, n_tokens, _dev(workspace, "workspace"),
+        workspace.numel() * workspace.element_size(), stream_handle(stream)))
+    return Y
 
 
 def q4k_ffn_gate_up_geglu(Wg, Wu, x, hidden: int, inter: int, out=None, stream=None):

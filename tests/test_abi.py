@@ -33,7 +33,8 @@ def test_header_declares_the_expected_calls():
     for n in ["qws_q4k_matvec", "qws_q6k_matvec", "qws_q4_0_matvec", "qws_q4k_qkv_proj",
               "qws_q4k_ffn_gate_up_geglu_down", "qws_rms_norm", "qws_residual_add",
               "qws_decode_chain", "qws_workspace_bytes", "qws_last_error", "qws_device_error",
-              "qws_quantize_q8_0", "qws_q8_matvec", "qws_q8_qkv_proj"]:
+              "qws_quantize_q8_0", "qws_q8_matvec", "qws_q8_qkv_proj",
+              "qws_q4k_prefill_matmul"]:
         assert n in names
 
 
@@ -152,6 +153,22 @@ def test_q8_path_checks(lib):
     assert lib.qws_q8_qkv_proj(Q80, A, A, A, A, A, A, A, 2560, 0, 0, None) == OK
     # the f32-activation entry points do not take Q8_0 weights
     assert lib.qws_matvec(Q80, A, A, A, 10, 2560, 1, 1, None, 0, None) == FORMAT
+
+
+def test_prefill_checks(lib):
+    need = lib.qws_workspace_bytes(_lib.OP_PREFILL, 0, 2560, 0, 512, 0)
+    assert need == 512 * 2560 * 2                       # f16 tiles of 256 tokens
+    assert lib.qws_workspace_bytes(_lib.OP_PREFILL, 0, 2560, 0, 1, 0) == 256 * 2560 * 2
+    assert lib.qws_workspace_bytes(_lib.OP_PREFILL, 0, 2500, 0, 8, 0) == 0
+    assert lib.qws_q4k_prefill_matmul(None, A, A, 10, 2560, 8, A, need, None) == NULL
+    assert lib.qws_q4k_prefill_matmul(A, A + 4, A, 10, 2560, 8, A, need, None) == ALIGN
+    assert lib.qws_q4k_prefill_matmul(A, A, A, 10, 2500, 8, A, need, None) == SHAPE
+    assert lib.qws_q4k_prefill_matmul(A, A, A, 10, 2560, 0, A, need, None) == SHAPE
+    assert lib.qws_q4k_prefill_matmul(A, A, A, -1, 2560, 8, A, need, None) == SHAPE
+    small = lib.qws_workspace_bytes(_lib.OP_PREFILL, 0, 2560, 0, 8, 0)
+    assert lib.qws_q4k_prefill_matmul(A, A, A, 10, 2560, 8, A, small - 16, None) == WORKSPACE
+    assert lib.qws_q4k_prefill_matmul(A, A, A, 10, 2560, 8, A + 8, small, None) == ALIGN
+    assert lib.qws_q4k_prefill_matmul(A, A, A, 0, 2560, 8, A, small, None) == OK
 
 
 def test_vector_op_checks(lib):
