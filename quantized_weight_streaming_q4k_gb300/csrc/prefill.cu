@@ -8,17 +8,18 @@
 //     reads: tiles of 256 tokens x 64 columns (32 KB), each a contiguous run
 //     in the 128-byte-swizzled K-major layout.  A tile then moves into shared
 //     memory as one 1-D bulk copy (TMA).
-//   * The weights stay packed in HBM.  Four decoder warps (one weight row per
-//     thread) read a row's 64-column chunk (its 32 nibble bytes and the
-//     super-block header), dequantize w = d*sc*q - dmin*m in f32, round to f16
-//     and store the 128-byte row into the swizzled A tile.
+//   * The weights stay packed in HBM.  One thread copies the tile rows' next
+//     super-block (128 rows x 144 bytes) into shared memory with one 2-D
+//     tensor copy (TMA, two buffers); eight decoder warps (two threads per weight row) dequantize
+//     w = d*sc*q - dmin*m in f32, round to f16 and store the row's 128 bytes
+//     of each 64-column chunk into the swizzled A tile.
 //   * One thread issues tcgen05.mma (kind::f16, M = 128 rows, N = 256 tokens,
 //     K = 16 per instruction, f32 accumulation) with both operands in shared
 //     memory and the accumulator in tensor memory (256 TMEM columns); a
 //     tcgen05.commit per stage frees that stage when its MMAs have read it.
 //   * The decoder warps then read the accumulator back with tcgen05.ld (warp
-//     w reads TMEM lanes 32*(w % 4) .. +31 = its 32 weight rows) and store Y
-//     with coalesced 128-byte rows.
+//     w reads TMEM lanes 32*(w % 4) .. +31 = 32 weight rows, half of the
+//     columns) and store Y with coalesced 128-byte rows.
 //
 // Shared-memory layout of one operand tile (K-major, 128-byte swizzle): row i
 // (a weight row for A, a token for B) holds 64 f16 = 128 bytes at
@@ -30,6 +31,7 @@
 //
 // Every wait is bounded; on a timeout the thread records kErrPrefill* in the
 // module's error word and the kernel still frees its tensor memory.
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
@@ -44,14 +46,20 @@ __device__ unsigned g_err_prefill;
 constexpr int kPfM = 128;                  // weight rows per tile (MMA M, TMEM lanes)
 constexpr int kPfN = 256;                  // tokens per tile (MMA N, TMEM columns)
 constexpr int kPfK = 64;                   // columns per stage: one 128-byte f16 row
-constexpr int kPfStages = 4;
 constexpr uint32_t kPfATile = kPfM * kPfK * 2;     // 16 KB
 constexpr uint32_t kPfBTile = kPfN * kPfK * 2;     // 32 KB
 constexpr uint32_t kPfStage = kPfATile + kPfBTile;
-constexpr int kPfThreads = 192;            // warp 0 copies, warp 1 MMA, warps 2..5 decode
-constexpr int kPfDecoders = 128;
-constexpr uint32_t kPfTmemCols = 256;
-constexpr size_t kPfSmemBytes = 1024 + kPfStages * kPfStage + 256;
+constexpr uint32_t kPfWBuf = kPfM * 144;           // one Q4_K super-block of every row
+constexpr int kPfThreads = 352;            // 3 role warps + 8 decoder warps
+constexpr int kPfDecoders = 256;
+// TMEM columns: a power of two >= 32 that holds the N accumulator columns
+constexpr uint32_t kPfTmemCols = kPfN <= 32 ? 32u : kPfN <= 64 ? 64u : kPfN <= 128 ? 128u : 256u;
+static_assert(kPfN % 16 == 0 && kPfN <= 256, "MMA N must be a multiple of 16 up to 256");
+// as many stages as fit beside the two weight buffers in 227 KB
+constexpr int kPfStages =
+    static_cast<int>((227u * 1024u - 1024u - 2u * kPfWBuf - 256u) / kPfStage);
+constexpr size_t kPfSmemBytes = 1024 + kPfStages * kPfStage + 2 * kPfWBuf + 256;
+static_assert(kPfStages >= 2, "shared memory too small for two stages");
 
 // f32 accumulate, f16 A and B, both K-major, N = 256, M = 128.
 constexpr uint32_t kPfIdesc = (1u << 4) | (0u << 7) | (0u << 10) |
@@ -59,6 +67,7 @@ constexpr uint32_t kPfIdesc = (1u << 4) | (0u << 7) | (0u << 10) |
                               (static_cast<uint32_t>(kPfM >> 4) << 24);
 
 struct PrefillParams {
+  CUtensorMap wmap;       // W as a [rows][row_bytes] byte matrix; box 144 x 128
   const uint8_t* W;       // Q4_K, rows x K
   const uint8_t* X16;     // packed f16 tiles [n_tiles_n][KC][32 KB]
   float* Y;               // [N][rows]
@@ -115,6 +124,17 @@ __device__ __forceinline__ void tc_ld16(uint32_t taddr, uint32_t (&v)[16]) {
 }
 __device__ __forceinline__ void tc_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 2-D tensor copy (TMA) of one box at coordinates (x, y) of `map` into
+// shared memory, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int x, int y,
+                                            uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
 }
 
 // two f32 -> packed f16x2 (round to nearest even); lo in bits 0..15
@@ -177,66 +197,67 @@ __global__ void __launch_bounds__(256) prefill_pack_x_kernel(const float* __rest
 }
 
 // ------------------------------------------------------------ Q4_K row chunk
-// Dequantizes columns 64c .. 64c + 63 of one super-block (c = chunk 0..3) to
-// f32 and stores them as one swizzled 128-byte f16 row.  hd = the block's
-// first 16 bytes (d, dmin, 12 scale bytes), q0/q1 = its qs bytes 32c .. 32c+31.
-// Column l < 32 is the low nibble of qs byte 32c + l (sub-block 2c), column
-// 32 + l the high nibble (sub-block 2c + 1); w = d*sc*q - dmin*m.
-__device__ __forceinline__ float nib_to_float(uint32_t v) {
-  // v in 0..15: 2^23 + v is exact, minus 2^23 gives v
-  return __uint_as_float(0x4B000000u | v) - 8388608.0f;
+// (d0, d1) = (a0, a1) * (b0, b1) + (c0, c1), one rounding each (packed FMA)
+__device__ __forceinline__ void fma2_to(float& d0, float& d1, float a0, float a1, float b0,
+                                        float b1, float c0, float c1) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rc, ra, rb, rc;\n\t"
+      "mov.b64 {%0, %1}, rc;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
-__device__ __forceinline__ void q4k_chunk_to_f16_row(const uint4 hd, const uint4 q0,
-                                                     const uint4 q1, int c, uint8_t* tile,
-                                                     uint32_t row) {
+// Four nibbles (one per byte of n, each 0..15) -> f16(a * q + nb), packed in
+// two words.  Byte k of n is placed under the exponent of 2^23 by one byte
+// permute (0x4B0000qq = 2^23 + q, exact); subtracting 2^23 gives q exactly, and
+// a * q + nb is rounded once to f32 (the same value as fmaf), then to f16.
+__device__ __forceinline__ void nib4_to_f16(uint32_t n, float a, float nb, uint32_t& o0,
+                                            uint32_t& o1) {
+  const float m0 = __uint_as_float(__byte_perm(n, 0x4B000000u, 0x7650));
+  const float m1 = __uint_as_float(__byte_perm(n, 0x4B000000u, 0x7651));
+  const float m2 = __uint_as_float(__byte_perm(n, 0x4B000000u, 0x7652));
+  const float m3 = __uint_as_float(__byte_perm(n, 0x4B000000u, 0x7653));
+  float q0, q1, q2, q3, w0, w1, w2, w3;
+  fma2_to(q0, q1, m0, m1, 1.0f, 1.0f, -8388608.0f, -8388608.0f);
+  fma2_to(q2, q3, m2, m3, 1.0f, 1.0f, -8388608.0f, -8388608.0f);
+  fma2_to(w0, w1, q0, q1, a, a, nb, nb);
+  fma2_to(w2, w3, q2, q3, a, a, nb, nb);
+  o0 = pack_f16x2(w0, w1);
+  o1 = pack_f16x2(w2, w3);
+}
+
+// Dequantizes half of the 64-column chunk c (0..3) of one super-block row to
+// f32 and stores it as four swizzled 16-byte f16 chunks of the A tile row.
+// hd = the block's first 16 bytes (d, dmin, 12 scale bytes), q0/q1 = its qs
+// bytes 32c .. 32c+31.  Column l < 32 is the low nibble of qs byte 32c + l
+// (sub-block 2c, half 0), column 32 + l the high nibble (sub-block 2c + 1,
+// half 1); w = d*sc*q - dmin*m.
+__device__ __forceinline__ void q4k_half_to_f16(const uint4 hd, const uint4 q0, const uint4 q1,
+                                                int c, int half, uint8_t* tile, uint32_t row) {
   const bool hi = c >= 2;
-  const uint32_t sh = 16u * static_cast<uint32_t>(c & 1);
+  const uint32_t sh = 16u * static_cast<uint32_t>(c & 1) + 8u * static_cast<uint32_t>(half);
   const uint32_t S = hi ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u))
                         : (hd.y & 0x3F3F3F3Fu);
   const uint32_t M = hi ? (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u))
                         : (hd.z & 0x3F3F3F3Fu);
-  const float d = half_bits_to_float(hd.x);
-  const float dmin = half_bits_to_float(hd.x >> 16);
-  const float a_lo = d * static_cast<float>((S >> sh) & 0xFFu);
-  const float a_hi = d * static_cast<float>((S >> (sh + 8)) & 0xFFu);
-  const float b_lo = -dmin * static_cast<float>((M >> sh) & 0xFFu);
-  const float b_hi = -dmin * static_cast<float>((M >> (sh + 8)) & 0xFFu);
+  // half 0: sub-block 2c, low nibbles (columns 0..31 of the chunk);
+  // half 1: sub-block 2c + 1, high nibbles (columns 32..63)
+  const float a = half_bits_to_float(hd.x) * static_cast<float>((S >> sh) & 0xFFu);
+  const float nb = -half_bits_to_float(hd.x >> 16) * static_cast<float>((M >> sh) & 0xFFu);
+  const uint32_t s0 = 4u * static_cast<uint32_t>(half);
   const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
-  for (int ch = 0; ch < 8; ++ch) {
-    // chunk ch: columns 8ch .. 8ch + 7; ch < 4 low nibbles of qs 8ch .., else
-    // high nibbles of qs 8(ch - 4) ..
-    const bool high = ch >= 4;
-    const uint32_t wa = w[2 * (ch & 3)], wb = w[2 * (ch & 3) + 1];
-    const float a = high ? a_hi : a_lo;
-    const float b = high ? b_hi : b_lo;
-    const uint32_t s0 = high ? 4u : 0u;
-    float f[8];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      f[j] = fmaf(a, nib_to_float((wa >> (8 * j + s0)) & 0xFu), b);
-      f[4 + j] = fmaf(a, nib_to_float((wb >> (8 * j + s0)) & 0xFu), b);
-    }
+  for (int j = 0; j < 4; ++j) {
+    // 16-byte chunk 4*half + j: columns 8j .. 8j + 7 of this half = nibbles of
+    // qs bytes 8j .. 8j + 7 (words 2j, 2j + 1)
     uint4 o;
-    o.x = pack_f16x2(f[0], f[1]);
-    o.y = pack_f16x2(f[2], f[3]);
-    o.z = pack_f16x2(f[4], f[5]);
-    o.w = pack_f16x2(f[6], f[7]);
-    *reinterpret_cast<uint4*>(tile + sw128_off(row, static_cast<uint32_t>(ch))) = o;
+    nib4_to_f16((w[2 * j] >> s0) & 0x0F0F0F0Fu, a, nb, o.x, o.y);
+    nib4_to_f16((w[2 * j + 1] >> s0) & 0x0F0F0F0Fu, a, nb, o.z, o.w);
+    *reinterpret_cast<uint4*>(tile + sw128_off(row, static_cast<uint32_t>(4 * half + j))) = o;
   }
-}
-
-struct Q4kChunk {
-  uint4 hd, q0, q1;
-};
-
-__device__ __forceinline__ void load_q4k_chunk(const uint8_t* rowp, int kc, Q4kChunk& v) {
-  const uint8_t* bp = rowp + static_cast<int64_t>(kc >> 2) * 144;
-  const int c = kc & 3;
-  v.hd = __ldg(reinterpret_cast<const uint4*>(bp));
-  v.q0 = __ldg(reinterpret_cast<const uint4*>(bp + 16 + 32 * c));
-  v.q1 = __ldg(reinterpret_cast<const uint4*>(bp + 32 + 32 * c));
 }
 
 // ------------------------------------------------------------ the GEMM kernel
@@ -244,17 +265,26 @@ enum : unsigned {
   kErrPfFull = 16u,      // MMA issuer gave up waiting for a stage
   kErrPfEmpty = 32u,     // a producer gave up waiting for a free stage
   kErrPfDone = 64u,      // the epilogue gave up waiting for the accumulator
+  kErrPfW = 128u,        // a wait on the packed-weight buffers gave up
 };
 
+// Roles (11 warps): warp 0 copies X tiles (B), warp 1 issues the MMAs and
+// owns the TMEM allocation, warp 2 copies packed weight rows (one 144-byte
+// super-block per row per copy, two buffers), warps 3..10 decode (two
+// threads per weight row: low-nibble and high-nibble halves) and then run
+// the epilogue (warp w reads TMEM lanes 32 * (w % 4) .. + 31, columns of its
+// half of the tile).
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid_constant__
                                                                     PrefillParams p) {
   extern __shared__ __align__(1024) uint8_t pf_smem_raw[];
-  // 1024-byte-aligned stage area, then the barriers and the TMEM address slot
   const uint32_t raw = smem_addr(pf_smem_raw);
   uint8_t* stages = pf_smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(stages + kPfStages * kPfStage);
+  uint8_t* wbuf = stages + kPfStages * kPfStage;                 // 2 x kPfWBuf
+  uint64_t* full = reinterpret_cast<uint64_t*>(wbuf + 2 * kPfWBuf);
   uint64_t* empty = full + kPfStages;
-  uint64_t* done = empty + kPfStages;
+  uint64_t* wfull = empty + kPfStages;
+  uint64_t* wempty = wfull + 2;
+  uint64_t* done = wempty + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
 
   const int warp = static_cast<int>(threadIdx.x >> 5);
@@ -263,11 +293,18 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
   const int tn = static_cast<int>(blockIdx.x) - tm * p.n_tiles_n;
   const int64_t m0 = static_cast<int64_t>(tm) * kPfM;
   const int KC = p.KC;
+  const int KB = KC / 4;
+  const int64_t rem = p.rows - m0;
+  const int live_rows = static_cast<int>(rem < kPfM ? rem : kPfM);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kPfStages; ++s) {
       mbar_init(&full[s], kPfDecoders + 1);
       mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&wfull[b], 1);
+      mbar_init(&wempty[b], kPfDecoders);
     }
     mbar_init(done, 1);
     fence_barrier_init();
@@ -295,14 +332,28 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
         const uint32_t ph = static_cast<uint32_t>(kc / kPfStages) & 1u;
         if (!mbar_wait(&empty[s], ph ^ 1u)) {
           atomicOr(&g_err_prefill, kErrPfEmpty);
-          ok = false;
           break;
         }
         mbar_arrive_expect_tx(&full[s], kPfBTile);
         bulk_copy_g2s(stages + s * kPfStage + kPfATile, xb + static_cast<int64_t>(kc) * kPfBTile,
                       kPfBTile, &full[s], pol);
       }
-      (void)ok;
+    }
+  } else if (warp == 2) {
+    // ---- W producer: super-block kb of the tile's 128 rows, one 2-D tensor
+    // copy (rows past the matrix end are zero-filled and still counted)
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      for (int kb = 0; kb < KB; ++kb) {
+        const int b = kb & 1;
+        const uint32_t ph = static_cast<uint32_t>(kb >> 1) & 1u;
+        if (!mbar_wait(&wempty[b], ph ^ 1u)) {
+          atomicOr(&g_err_prefill, kErrPfW);
+          break;
+        }
+        mbar_arrive_expect_tx(&wfull[b], kPfWBuf);
+        tma_load_2d(wbuf + b * kPfWBuf, &p.wmap, kb * 144, static_cast<int>(m0), &wfull[b], pol);
+      }
     }
   } else if (warp == 1) {
     // ---- MMA issuer
@@ -312,7 +363,6 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
         const uint32_t ph = static_cast<uint32_t>(kc / kPfStages) & 1u;
         if (!mbar_wait(&full[s], ph)) {
           atomicOr(&g_err_prefill, kErrPfFull);
-          ok = false;
           break;
         }
         tc_fence_after();
@@ -328,19 +378,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
       tc_commit(done);
     }
   } else {
-    // ---- decoders (one weight row each), then the epilogue
-    const int d = static_cast<int>(threadIdx.x) - 64;
-    const uint32_t row = static_cast<uint32_t>(d);
-    const int64_t r = m0 + d;
-    const bool live = r < p.rows;
-    const int64_t row_bytes = p.K / 256 * 144;
-    const uint8_t* rowp = p.W + (live ? r : 0) * row_bytes;
-    Q4kChunk cur, nxt;
-    if (live) load_q4k_chunk(rowp, 0, cur);
+    // ---- decoders: thread d -> weight row d / 2 of the tile, half d % 2
+    const int d = static_cast<int>(threadIdx.x) - 96;
+    const uint32_t row = static_cast<uint32_t>(d >> 1);
+    const int half = d & 1;
+    const bool live = static_cast<int>(row) < live_rows;
     for (int kc = 0; kc < KC; ++kc) {
       const int s = kc % kPfStages;
       const uint32_t ph = static_cast<uint32_t>(kc / kPfStages) & 1u;
-      if (live && kc + 1 < KC) load_q4k_chunk(rowp, kc + 1, nxt);
+      const int kb = kc >> 2, c = kc & 3, b = kb & 1;
+      if (c == 0 && !mbar_wait(&wfull[b], static_cast<uint32_t>(kb >> 1) & 1u)) {
+        atomicOr(&g_err_prefill, kErrPfW);
+        ok = false;
+        break;
+      }
       if (!mbar_wait(&empty[s], ph ^ 1u)) {
         atomicOr(&g_err_prefill, kErrPfEmpty);
         ok = false;
@@ -348,18 +399,23 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
       }
       uint8_t* tile = stages + s * kPfStage;
       if (live) {
-        q4k_chunk_to_f16_row(cur.hd, cur.q0, cur.q1, kc & 3, tile, row);
+        const uint8_t* bp = wbuf + b * kPfWBuf + row * 144u;
+        const uint4 hd = *reinterpret_cast<const uint4*>(bp);
+        const uint4 q0 = *reinterpret_cast<const uint4*>(bp + 16 + 32 * c);
+        const uint4 q1 = *reinterpret_cast<const uint4*>(bp + 32 + 32 * c);
+        q4k_half_to_f16(hd, q0, q1, c, half, tile, row);
       } else {
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch)
-          *reinterpret_cast<uint4*>(tile + sw128_off(row, static_cast<uint32_t>(ch))) = z;
+        for (int j = 0; j < 4; ++j)
+          *reinterpret_cast<uint4*>(tile + sw128_off(row, static_cast<uint32_t>(4 * half + j))) =
+              z;
       }
       fence_proxy_async_smem();   // generic-proxy stores -> visible to the MMA
       mbar_arrive(&full[s]);
-      cur = nxt;
+      if (c == 3) mbar_arrive(&wempty[b]);   // this super-block's bytes are read
     }
-    // ---- epilogue: TMEM lanes 32 * (warp % 4) .. + 31 are this warp's rows
+    // ---- epilogue
     if (!mbar_wait(done, 0u)) {
       atomicOr(&g_err_prefill, kErrPfDone);
       ok = false;
@@ -367,10 +423,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
     tc_fence_after();
     if (ok) {
       const int q = warp & 3;
+      const int colh = (warp - 3) >> 2;     // 0: columns 0..N/2-1, 1: the rest
       const int64_t rr = m0 + 32 * q + lane;
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16);
       const int64_t n0 = static_cast<int64_t>(tn) * kPfN;
-      for (int cc = 0; cc < kPfN; cc += 16) {
+      for (int cc = colh * (kPfN / 2); cc < (colh + 1) * (kPfN / 2); cc += 16) {
         uint32_t v[16];
         tc_ld16(tbase + static_cast<uint32_t>(cc), v);
         tc_wait_ld();
@@ -400,6 +457,43 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
 size_t prefill_workspace_bytes(int64_t hidden, int64_t n_tokens) {
   const int64_t tiles = (n_tokens + kPfN - 1) / kPfN;
   return static_cast<size_t>(tiles) * kPfN * static_cast<size_t>(hidden) * 2;
+}
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no link
+// against the driver library).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_tiled_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  }
+  return fn;
+}
+
+// W viewed as a byte matrix [rows][row_bytes]; boxes of 144 bytes (one
+// super-block) x 128 rows.
+static bool encode_w_map(CUtensorMap* map, const uint8_t* W, int64_t rows, int64_t K) {
+  EncodeTiledFn fn = encode_tiled_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 256 * 144),
+                              static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 256 * 144)};
+  const cuuint32_t box[2] = {144u, static_cast<cuuint32_t>(kPfM)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(W), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <class... KArgs, class... Args>
@@ -437,6 +531,7 @@ cudaError_t launch_prefill_q4k(const uint8_t* W, const float* X, float* Y, int64
     attr_set[dev] = true;
   }
   PrefillParams p;
+  if (!encode_w_map(&p.wmap, W, rows, K)) return cudaErrorInvalidValue;
   p.W = W;
   p.X16 = ws;
   p.Y = Y;
