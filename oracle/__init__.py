@@ -78,6 +78,13 @@ def _load():
         P, I64, I = C.c_void_p, C.c_int64, C.c_int
         lib.qo_half.restype = C.c_double
         lib.qo_half.argtypes = [C.c_uint16]
+        lib.qo_rope.restype = I
+        lib.qo_rope.argtypes = [P, I, I, I, I64, C.c_double]
+        lib.qo_kv_append.restype = I
+        lib.qo_kv_append.argtypes = [P, P, P, P, I, I, I64, I64]
+        lib.qo_kv_attention.restype = I
+        lib.qo_kv_attention.argtypes = [P, P, P, I, I, I, I64, I64, C.c_double, C.c_double,
+                                        P, P, P]
         lib.qo_half_bits.restype = C.c_uint16
         lib.qo_half_bits.argtypes = [C.c_float]
         lib.qo_quantize_q8_0.restype = I
@@ -287,6 +294,46 @@ def attn_seq1(v, n_q_heads: int, n_kv_heads: int, head_dim: int) -> np.ndarray:
     if rc:
         raise ValueError("bad head counts")
     return out
+
+
+def rope(x, n_heads: int, head_dim: int, rot_dim: int, pos: int, base: float) -> np.ndarray:
+    """Rotary embedding of [n_heads, head_dim] at position pos (half-split pairs)."""
+    xs = _f64(x).reshape(-1).copy()
+    assert xs.size == n_heads * head_dim
+    rc = _load().qo_rope(_ptr(xs), n_heads, head_dim, rot_dim, int(pos), float(base))
+    if rc:
+        raise ValueError("bad rope arguments")
+    return xs.reshape(n_heads, head_dim)
+
+
+def kv_append(kc, vc, k, v, n_kv_heads: int, head_dim: int, max_seq: int, pos: int):
+    """Returns copies of the caches with k, v written at position pos."""
+    kc2, vc2 = _f64(kc).reshape(-1).copy(), _f64(vc).reshape(-1).copy()
+    ks, vs = _f64(k).reshape(-1), _f64(v).reshape(-1)
+    rc = _load().qo_kv_append(_ptr(kc2), _ptr(vc2), _ptr(ks), _ptr(vs), n_kv_heads, head_dim,
+                              max_seq, int(pos))
+    if rc:
+        raise ValueError("bad position")
+    shape = (n_kv_heads, max_seq, head_dim)
+    return kc2.reshape(shape), vc2.reshape(shape)
+
+
+def kv_attention(q, kc, vc, n_q_heads: int, n_kv_heads: int, head_dim: int, max_seq: int,
+                 n_ctx: int, scale: float, softcap: float = 0.0):
+    """One query token over the first n_ctx cache positions.  Returns
+    (out, bound, smax): out and bound [n_q, hd], smax [n_q]."""
+    qs = _f64(q).reshape(-1)
+    ks, vs = _f64(kc).reshape(-1), _f64(vc).reshape(-1)
+    assert qs.size == n_q_heads * head_dim and ks.size == n_kv_heads * max_seq * head_dim
+    out = np.empty(n_q_heads * head_dim)
+    bound = np.empty(n_q_heads * head_dim)
+    smax = np.empty(n_q_heads)
+    rc = _load().qo_kv_attention(_ptr(qs), _ptr(ks), _ptr(vs), n_q_heads, n_kv_heads, head_dim,
+                                 max_seq, int(n_ctx), float(scale), float(softcap), _ptr(out),
+                                 _ptr(bound), _ptr(smax))
+    if rc:
+        raise ValueError(f"qo_kv_attention failed ({rc})")
+    return out.reshape(n_q_heads, head_dim), bound.reshape(n_q_heads, head_dim), smax
 
 
 ACT_GELU_TANH, ACT_SILU = 0, 1

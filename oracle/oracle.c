@@ -448,6 +448,114 @@ int qo_attn_seq1(const double *v, int n_q_heads, int n_kv_heads, int head_dim, d
 }
 
 /* ---------------------------------------------------------------------------
+ * RoPE at one position ([compute] §Shaders "RoPE" row: rope_at_pos,
+ * rope_at_pos_batched; the README's test list names partial RoPE; [perf]
+ * §RoPE comparison: full and 25 % rotary dimensions).  The pages give no
+ * formula; this is the standard rotary embedding in its half-split form:
+ * with r = rot_dim (even, <= head_dim), for i < r/2
+ *   theta_i = pos * base^(-2i / r)
+ *   (x_i, x_{i+r/2}) <- (x_i cos theta_i - x_{i+r/2} sin theta_i,
+ *                        x_i sin theta_i + x_{i+r/2} cos theta_i)
+ * and dimensions r .. head_dim-1 are left as they are.  x is [n_heads][head_dim],
+ * every head rotated the same way.
+ * ------------------------------------------------------------------------- */
+int qo_rope(double *x, int n_heads, int head_dim, int rot_dim, int64_t pos, double base)
+{
+    if (rot_dim < 0 || rot_dim % 2 || rot_dim > head_dim || base <= 0.0) return -1;
+    int half = rot_dim / 2;
+    for (int h = 0; h < n_heads; ++h) {
+        double *xh = x + (int64_t)h * head_dim;
+        for (int i = 0; i < half; ++i) {
+            double theta = (double)pos * pow(base, -2.0 * (double)i / (double)rot_dim);
+            double c = cos(theta), s = sin(theta);
+            double a = xh[i], b = xh[i + half];
+            xh[i] = a * c - b * s;
+            xh[i + half] = a * s + b * c;
+        }
+    }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * kv_append ([compute] §Shaders "Attention" row): the new token's k and v
+ * ([n_kv_heads][head_dim] each) are written at position pos of the caches
+ * ([n_kv_heads][max_seq][head_dim] each).
+ * ------------------------------------------------------------------------- */
+int qo_kv_append(double *kc, double *vc, const double *k, const double *v, int n_kv_heads,
+                 int head_dim, int64_t max_seq, int64_t pos)
+{
+    if (pos < 0 || pos >= max_seq) return -1;
+    for (int g = 0; g < n_kv_heads; ++g)
+        for (int i = 0; i < head_dim; ++i) {
+            kc[((int64_t)g * max_seq + pos) * head_dim + i] = k[(int64_t)g * head_dim + i];
+            vc[((int64_t)g * max_seq + pos) * head_dim + i] = v[(int64_t)g * head_dim + i];
+        }
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
+ * Attention of one query token over the KV cache ([compute] §Shaders
+ * "Attention" row: kv_attention, GQA, softcap; [engine] §BLAS-Fused
+ * Attention steps 1-3: scores = K q, scale and optional softcap, softmax,
+ * output = V^T p).  For query head h (kv head g = h / (n_q / n_kv), the
+ * contiguous GQA grouping):
+ *   s_t = scale * (q_h . k_{g,t})                 t = 0 .. n_ctx-1
+ *   s_t <- softcap * tanh(s_t / softcap)          only if softcap > 0
+ *   p_t = exp(s_t - max s) / sum_u exp(s_u - max s)
+ *   out_h = sum_t p_t v_{g,t}
+ * also returns bound_h[i] = sum_t p_t |v_{g,t,i}| and smax_h = max_t
+ * sum_i |scale q_h,i k_{g,t,i}| (the magnitude the score rounding scales with).
+ * q is [n_q][hd]; caches [n_kv][max_seq][hd]; out and bound [n_q][hd].
+ * ------------------------------------------------------------------------- */
+int qo_kv_attention(const double *q, const double *kc, const double *vc, int n_q_heads,
+                    int n_kv_heads, int head_dim, int64_t max_seq, int64_t n_ctx,
+                    double scale, double softcap, double *out, double *bound, double *smax)
+{
+    if (n_kv_heads <= 0 || n_q_heads % n_kv_heads != 0) return -1;
+    if (n_ctx < 1 || n_ctx > max_seq) return -1;
+    int group = n_q_heads / n_kv_heads;
+    double *s = (double *)malloc(sizeof(double) * (size_t)n_ctx);
+    if (!s) return -2;
+    for (int h = 0; h < n_q_heads; ++h) {
+        int g = h / group;
+        const double *qh = q + (int64_t)h * head_dim;
+        const double *kg = kc + (int64_t)g * max_seq * head_dim;
+        const double *vg = vc + (int64_t)g * max_seq * head_dim;
+        double mx = -INFINITY, mag = 0.0;
+        for (int64_t t = 0; t < n_ctx; ++t) {
+            double acc = 0.0, a = 0.0;
+            for (int i = 0; i < head_dim; ++i) {
+                acc += qh[i] * kg[t * head_dim + i];
+                a += fabs(scale * qh[i] * kg[t * head_dim + i]);
+            }
+            acc *= scale;
+            if (softcap > 0.0) acc = softcap * tanh(acc / softcap);
+            s[t] = acc;
+            if (acc > mx) mx = acc;
+            if (a > mag) mag = a;
+        }
+        double den = 0.0;
+        for (int64_t t = 0; t < n_ctx; ++t) {
+            s[t] = exp(s[t] - mx);
+            den += s[t];
+        }
+        for (int i = 0; i < head_dim; ++i) {
+            double acc = 0.0, b = 0.0;
+            for (int64_t t = 0; t < n_ctx; ++t) {
+                double p = s[t] / den;
+                acc += p * vg[t * head_dim + i];
+                b += p * fabs(vg[t * head_dim + i]);
+            }
+            out[(int64_t)h * head_dim + i] = acc;
+            if (bound) bound[(int64_t)h * head_dim + i] = b;
+        }
+        if (smax) smax[h] = mag;
+    }
+    free(s);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
  * Gated FFN ([compute] §Shaders "Q4_K fused FFN": q4k_ffn_gate_up then
  * q4k_geglu_gelu_tanh_down, or the SiLU-gated variant; [engine] §WalkFfn
  * steps 1-3: gate and up projections, the gated activation, then the down
