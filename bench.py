@@ -14,7 +14,9 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                         shape in Q4_K / Q6_K, f32 activations),
                         ffn (fused gate/up GEGLU + Q6_K down, 2560/10240),
                         prefill (Q4_K 10240 x 2560 times --batch tokens on the
-                        tensor cores; TFLOP/s)
+                        tensor cores; TFLOP/s),
+                        kv_attention (one token over 32768 cached positions,
+                        Gemma-3-4B heads: 8 query, 4 kv, head_dim 256)
 For N > 1 launch with torchrun; every rank runs an independent replica of the
 step on its own GPU (the path has no data exchange; "replicas only").
 """
@@ -435,6 +437,24 @@ def run_op(args):
             nbytes = wbytes + B * H * 4 + 2 * B * (H // 32 * 34) + B * VOCAB * 4
             kernel = "quantize_q8_0_kernel + matvec_kernel<UnitQ40xQ8>"
         workload = f"lm_head {VOCAB}x{H} Q4_0, batch {B}"
+    elif args.op == "kv_attention":
+        nq, nkv, hd, L = 8, 4, 256, 32768
+        gk = synth.rng(synth.W_CHAIN, 7)
+        kc = torch.from_numpy(gk.standard_normal((nkv, L, hd)).astype(np.float32)).to(dev)
+        vc = torch.from_numpy(gk.standard_normal((nkv, L, hd)).astype(np.float32)).to(dev)
+        x = torch.from_numpy(gk.standard_normal((nq, hd)).astype(np.float32)).to(dev)
+        y = torch.empty((nq, hd), device=dev)
+        ws = torch.empty(ops.workspace_bytes(ops.OP_KV_ATTENTION, L, hd, nq, nkv),
+                         dtype=torch.uint8, device=dev)
+
+        def call():
+            ops.kv_attention(x, kc, vc, nq, nkv, hd, L, L, 1.0 / 16, workspace=ws, out=y)
+        launches = 2
+        nbytes = 2 * nkv * L * hd * 4 + 2 * nq * hd * 4
+        kernel = "kv_attention_split_kernel<8> + kv_attention_merge_kernel"
+        workload = f"kv_attention, {L} positions, {nq} query / {nkv} kv heads of {hd}"
+        if B != 1:
+            raise SystemExit("--op kv_attention runs one query token")
     elif args.op == "prefill":
         rows, N = I, B
         W = torch.from_numpy(synth.q4_k_matrix(g, rows, H)).to(dev)
@@ -531,7 +551,7 @@ def main():
                     help="chain length (default 34; shorter only for profiler captures)")
     ap.add_argument("--op", default="step",
                     choices=["step", "lm_head_q4_0", "lm_head_q8", "lm_head_q4_k",
-                             "lm_head_q6_k", "ffn", "prefill"],
+                             "lm_head_q6_k", "ffn", "prefill", "kv_attention"],
                     help="step (default): the decode step; otherwise one operation alone")
     ap.add_argument("--batch", type=int, default=1, help="activation vectors (--op only)")
     args = ap.parse_args()

@@ -79,7 +79,9 @@ typedef enum {
   QWS_OP_MATVEC = 0,      /* qws_matvec / qws_q4_0_matvec with split_k > 1 */
   QWS_OP_FFN = 1,         /* qws_q4k_ffn_gate_up_geglu_down                */
   QWS_OP_DECODE_CHAIN = 2, /* qws_decode_chain                             */
-  QWS_OP_PREFILL = 3       /* qws_q4k_prefill_matmul (batch = n_tokens)     */
+  QWS_OP_PREFILL = 3,      /* qws_q4k_prefill_matmul (batch = n_tokens)     */
+  QWS_OP_KV_ATTENTION = 4  /* qws_kv_attention: rows = n_ctx, hidden =
+                              head_dim, inter = n_q_heads, batch = n_kv_heads */
 } qws_op;
 
 /* ------------------------------------------------------------------------
@@ -180,6 +182,42 @@ qws_status qws_q8_qkv_proj(qws_format wfmt, const void* Wq, const void* Wk, cons
 qws_status qws_q4k_prefill_matmul(const void* W, const float* X, float* Y, int64_t rows,
                                   int64_t hidden, int64_t n_tokens, void* ws, size_t ws_bytes,
                                   qws_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Decode attention over a KV cache, sequence length > 1 (infer-compute README
+ * §Shaders rows "RoPE" (rope_at_pos) and "Attention" (kv_append,
+ * kv_attention: GQA, softcap); infer-inference README §BLAS-Fused Attention).
+ * Caches are f32 [n_kv_heads][max_seq][head_dim] (device); vectors f32.
+ *
+ * qws_rope_at_pos: x [n_heads][head_dim] (device) rotated in place at
+ *   position pos: for i < rot_dim / 2, theta_i = pos * base^(-2i / rot_dim),
+ *   (x_i, x_{i+rot/2}) <- (x_i cos - x_{i+rot/2} sin, x_i sin + x_{i+rot/2} cos);
+ *   dimensions rot_dim.. unchanged (partial RoPE).  Angle, sine, cosine and
+ *   the rotation in f64, rounded once to f32.  rot_dim even, 0 < rot_dim <=
+ *   head_dim; pos >= 0; base > 0.  (The pages give no formula: this is the
+ *   standard half-split rotary embedding.)
+ * qws_kv_append: k, v [n_kv_heads][head_dim] written at position pos of the
+ *   caches (0 <= pos < max_seq).
+ * qws_kv_attention: one query token q [n_q_heads][head_dim] over cache
+ *   positions 0 .. n_ctx-1; query head h reads kv head h / (n_q / n_kv):
+ *     s_t = scale * q_h . k_t;  s_t <- softcap * tanh(s_t / softcap) if
+ *     softcap > 0;  out_h = sum_t softmax(s)_t v_t.
+ *   out [n_q_heads][head_dim] (device, overwritten); ws >=
+ *   qws_workspace_bytes(QWS_OP_KV_ATTENTION, n_ctx, head_dim, n_q_heads,
+ *   n_kv_heads, 0) bytes (device, 16-byte aligned).  head_dim in {32, 64,
+ *   128, 256}; n_q_heads / n_kv_heads in 1..4; 1 <= n_ctx <= max_seq; caches
+ *   and q 16-byte aligned.  Split along the positions, merged in a fixed
+ *   order: identical run to run.
+ * ---------------------------------------------------------------------- */
+qws_status qws_rope_at_pos(float* x, int n_heads, int head_dim, int rot_dim, int64_t pos,
+                           double base, qws_stream stream);
+qws_status qws_kv_append(float* k_cache, float* v_cache, const float* k, const float* v,
+                         int n_kv_heads, int head_dim, int64_t max_seq, int64_t pos,
+                         qws_stream stream);
+qws_status qws_kv_attention(const float* q, const float* k_cache, const float* v_cache,
+                            float* out, int n_q_heads, int n_kv_heads, int head_dim,
+                            int64_t max_seq, int64_t n_ctx, float scale, float softcap,
+                            void* ws, size_t ws_bytes, qws_stream stream);
 
 /* ------------------------------------------------------------------------
  * Gated FFN (infer-compute README §Shaders "Q4_K fused FFN": q4k_ffn_gate_up,

@@ -17,7 +17,7 @@ STATUS_NAMES = {
     4: "QWS_ERR_FORMAT", 5: "QWS_ERR_WORKSPACE", 6: "QWS_ERR_CUDA", 7: "QWS_ERR_TIMEOUT",
 }
 Q4_0, Q8_0, Q4_K, Q6_K = 2, 8, 12, 14
-OP_MATVEC, OP_FFN, OP_DECODE_CHAIN, OP_PREFILL = 0, 1, 2, 3
+OP_MATVEC, OP_FFN, OP_DECODE_CHAIN, OP_PREFILL, OP_KV_ATTENTION = 0, 1, 2, 3, 4
 
 
 class QwsLayer(C.Structure):
@@ -54,6 +54,9 @@ SIGNATURES = {
     "qws_residual_rms_norm": (I, [F, F, F, F, I64, C.c_float, I, P]),
     "qws_quantize_q8_0": (I, [F, P, I64, I, P]),
     "qws_q4k_prefill_matmul": (I, [P, F, F, I64, I64, I64, P, SZ, P]),
+    "qws_rope_at_pos": (I, [F, I, I, I, I64, C.c_double, P]),
+    "qws_kv_append": (I, [F, F, F, F, I, I, I64, I64, P]),
+    "qws_kv_attention": (I, [F, F, F, F, I, I, I, I64, I64, C.c_float, C.c_float, P, SZ, P]),
     "qws_q8_matvec": (I, [I, P, P, F, I64, I64, I, P]),
     "qws_q8_qkv_proj": (I, [I, P, P, P, P, F, F, F, I64, I64, I64, P]),
     "qws_rms_norm": (I, [F, F, F, I64, C.c_float, I, P]),

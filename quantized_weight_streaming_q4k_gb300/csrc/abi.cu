@@ -2,6 +2,7 @@
 // before anything is enqueued), workspace sizing and dispatch to launchers.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <string>
@@ -296,6 +297,70 @@ qws_status qws_q4k_prefill_matmul(const void* W, const float* X, float* Y, int64
   return ok();
 }
 
+qws_status qws_rope_at_pos(float* x, int n_heads, int head_dim, int rot_dim, int64_t pos,
+                           double base, qws_stream stream) {
+  const char* fn = "qws_rope_at_pos";
+  QWS_CHECK_F(x);
+  if (n_heads < 1 || head_dim < 2 || rot_dim < 2 || rot_dim % 2 || rot_dim > head_dim)
+    return fail(QWS_ERR_SHAPE, "%s: need n_heads >= 1 and an even 0 < rot_dim <= head_dim", fn);
+  if (pos < 0 || !(base > 0.0)) return fail(QWS_ERR_SHAPE, "%s: need pos >= 0 and base > 0", fn);
+  cudaError_t e = qws::launch_rope(x, n_heads, head_dim, rot_dim, pos, base,
+                                   reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn, "");
+  return ok();
+}
+
+qws_status qws_kv_append(float* k_cache, float* v_cache, const float* k, const float* v,
+                         int n_kv_heads, int head_dim, int64_t max_seq, int64_t pos,
+                         qws_stream stream) {
+  const char* fn = "qws_kv_append";
+  QWS_CHECK_F(k_cache);
+  QWS_CHECK_F(v_cache);
+  QWS_CHECK_F(k);
+  QWS_CHECK_F(v);
+  if (n_kv_heads < 1 || head_dim < 1 || max_seq < 1)
+    return fail(QWS_ERR_SHAPE, "%s: empty cache shape", fn);
+  if (pos < 0 || pos >= max_seq)
+    return fail(QWS_ERR_SHAPE, "%s: pos = %lld outside [0, max_seq = %lld)", fn, (long long)pos,
+                (long long)max_seq);
+  cudaError_t e = qws::launch_kv_append(k_cache, v_cache, k, v, n_kv_heads, head_dim, max_seq,
+                                        pos, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn, "");
+  return ok();
+}
+
+qws_status qws_kv_attention(const float* q, const float* k_cache, const float* v_cache,
+                            float* out, int n_q_heads, int n_kv_heads, int head_dim,
+                            int64_t max_seq, int64_t n_ctx, float scale, float softcap,
+                            void* ws, size_t ws_bytes, qws_stream stream) {
+  const char* fn = "qws_kv_attention";
+  QWS_CHECK_PTR(q);
+  QWS_CHECK_PTR(k_cache);
+  QWS_CHECK_PTR(v_cache);
+  if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+    return fail(QWS_ERR_ALIGN, "%s: q and the caches must be 16-byte aligned", fn);
+  QWS_CHECK_F(out);
+  if (head_dim != 32 && head_dim != 64 && head_dim != 128 && head_dim != 256)
+    return fail(QWS_ERR_SHAPE, "%s: head_dim = %d not in {32, 64, 128, 256}", fn, head_dim);
+  if (n_kv_heads < 1 || n_q_heads < n_kv_heads || n_q_heads % n_kv_heads ||
+      n_q_heads / n_kv_heads > 4)
+    return fail(QWS_ERR_SHAPE, "%s: n_q_heads / n_kv_heads must be an integer in 1..4", fn);
+  if (n_ctx < 1 || n_ctx > max_seq)
+    return fail(QWS_ERR_SHAPE, "%s: need 1 <= n_ctx <= max_seq", fn);
+  if (!std::isfinite(scale) || !(softcap >= 0.f) || !std::isfinite(softcap))
+    return fail(QWS_ERR_SHAPE, "%s: scale must be finite and softcap >= 0", fn);
+  const size_t need = qws::kv_attention_workspace_bytes(n_q_heads, n_kv_heads, head_dim, n_ctx);
+  if (!ws || ws_bytes < need)
+    return fail(QWS_ERR_WORKSPACE, "%s: workspace %zu bytes, need %zu", fn, ws_bytes, need);
+  if (!aligned(ws, 16)) return fail(QWS_ERR_ALIGN, "%s: ws is not 16-byte aligned", fn);
+  cudaError_t e = qws::launch_kv_attention(q, k_cache, v_cache, out, n_q_heads, n_kv_heads,
+                                           head_dim, max_seq, n_ctx, scale, softcap,
+                                           static_cast<float*>(ws),
+                                           reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn, "");
+  return ok();
+}
+
 static qws_status check_ffn_shape(const char* fn, int64_t hidden, int64_t inter) {
   if (hidden <= 0 || hidden % 256 || hidden > kMaxHidden)
     return fail(QWS_ERR_SHAPE, "%s: hidden = %lld (need a multiple of 256 in (0, 20480])", fn,
@@ -455,6 +520,10 @@ size_t qws_workspace_bytes(qws_op op, int64_t rows, int64_t hidden, int64_t inte
     case QWS_OP_PREFILL:
       if (hidden <= 0 || hidden % 256 || batch < 1) return 0;
       return round256(qws::prefill_workspace_bytes(hidden, batch));
+    case QWS_OP_KV_ATTENTION:
+      if (rows < 1 || hidden <= 0 || inter <= 0 || batch <= 0 || inter % batch) return 0;
+      return round256(qws::kv_attention_workspace_bytes(static_cast<int>(inter), batch,
+                                                        static_cast<int>(hidden), rows));
   }
   return 0;
 }

@@ -103,6 +103,15 @@ cudaError_t launch_matvec_q8(int wfmt, const Seg* segs, int nseg, const uint8_t*
                              int B, cudaStream_t st, std::string* why);
 // x (nblocks * 32 floats) -> nblocks Q8_0 blocks
 cudaError_t launch_quantize_q8_0(const float* x, uint8_t* xq, int64_t nblocks, cudaStream_t st);
+// attention over a KV cache (attention.cu)
+size_t kv_attention_workspace_bytes(int n_q, int n_kv, int head_dim, int64_t n_ctx);
+cudaError_t launch_rope(float* x, int n_heads, int head_dim, int rot_dim, int64_t pos,
+                        double base, cudaStream_t st);
+cudaError_t launch_kv_append(float* kc, float* vc, const float* k, const float* v, int n_kv,
+                             int head_dim, int64_t max_seq, int64_t pos, cudaStream_t st);
+cudaError_t launch_kv_attention(const float* q, const float* kc, const float* vc, float* out,
+                                int n_q, int n_kv, int head_dim, int64_t max_seq, int64_t n_ctx,
+                                float scale, float softcap, float* ws, cudaStream_t st);
 // prefill (prefill.cu): X packed to f16 tiles in ws, then the tcgen05 GEMM
 size_t prefill_workspace_bytes(int64_t hidden, int64_t n_tokens);
 cudaError_t launch_prefill_q4k(const uint8_t* W, const float* X, float* Y, int64_t rows,

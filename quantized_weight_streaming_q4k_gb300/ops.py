@@ -12,12 +12,14 @@ import ctypes as C
 import torch
 
 from . import _lib
-from ._lib import (OP_DECODE_CHAIN, OP_FFN, OP_MATVEC, OP_PREFILL, Q4_0, Q4_K, Q6_K, Q8_0,
+from ._lib import (OP_DECODE_CHAIN, OP_FFN, OP_KV_ATTENTION, OP_MATVEC, OP_PREFILL, Q4_0,
+                   Q4_K, Q6_K, Q8_0,
                    QwsError, check, lib)
 
 __all__ = [
     "Q4_0", "Q4_K", "Q6_K", "Q8_0", "QwsError", "q4k_matvec", "q6k_matvec", "q4_0_matvec",
     "matvec", "quantize_q8_0", "q8_matvec", "q8_qkv_proj", "q4k_prefill_matmul",
+    "rope_at_pos", "kv_append", "kv_attention",
     "q4k_qkv_proj", "q4k_ffn_gate_up_geglu", "q4k_ffn_gate_up_geglu_down", "rms_norm",
     "residual_add", "decode_chain", "workspace_bytes", "device_error", "Layer", "Dims",
     "stream_handle",
@@ -153,6 +155,40 @@ def q4k_prefill_matmul(W, X, rows: int, hidden: int, n_tokens: int, workspace=No
         rows, hidden, n_tokens, _dev(workspace, "workspace"),
         workspace.numel() * workspace.element_size(), stream_handle(stream)))
     return Y
+
+
+def rope_at_pos(x, n_heads: int, head_dim: int, rot_dim: int, pos: int, base: float,
+                stream=None):
+    """Rotates x [n_heads, head_dim] in place at position pos; returns x."""
+    check(lib().qws_rope_at_pos(_dev(x, "x", torch.float32), n_heads, head_dim, rot_dim, pos,
+                                float(base), stream_handle(stream)))
+    return x
+
+
+def kv_append(k_cache, v_cache, k, v, n_kv_heads: int, head_dim: int, max_seq: int, pos: int,
+              stream=None):
+    check(lib().qws_kv_append(_dev(k_cache, "k_cache", torch.float32),
+                              _dev(v_cache, "v_cache", torch.float32),
+                              _dev(k, "k", torch.float32), _dev(v, "v", torch.float32),
+                              n_kv_heads, head_dim, max_seq, pos, stream_handle(stream)))
+
+
+def kv_attention(q, k_cache, v_cache, n_q_heads: int, n_kv_heads: int, head_dim: int,
+                 max_seq: int, n_ctx: int, scale: float, softcap: float = 0.0, workspace=None,
+                 out=None, stream=None):
+    """One query token q [n_q_heads, head_dim] over cache positions 0 .. n_ctx-1."""
+    y = out if out is not None else torch.empty((n_q_heads, head_dim), dtype=torch.float32,
+                                                device=q.device)
+    need = workspace_bytes(OP_KV_ATTENTION, n_ctx, head_dim, n_q_heads, n_kv_heads)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=q.device)
+    check(lib().qws_kv_attention(
+        _dev(q, "q", torch.float32), _dev(k_cache, "k_cache", torch.float32),
+        _dev(v_cache, "v_cache", torch.float32), _dev(y, "out", torch.float32), n_q_heads,
+        n_kv_heads, head_dim, max_seq, n_ctx, float(scale), float(softcap),
+        _dev(workspace, "workspace"), workspace.numel() * workspace.element_size(),
+        stream_handle(stream)))
+    return y
 
 
 def q4k_ffn_gate_up_geglu(Wg, Wu, x, hidden: int, inter: int, out=None, stream=None):

@@ -34,7 +34,8 @@ def test_header_declares_the_expected_calls():
               "qws_q4k_ffn_gate_up_geglu_down", "qws_rms_norm", "qws_residual_add",
               "qws_decode_chain", "qws_workspace_bytes", "qws_last_error", "qws_device_error",
               "qws_quantize_q8_0", "qws_q8_matvec", "qws_q8_qkv_proj",
-              "qws_q4k_prefill_matmul"]:
+              "qws_q4k_prefill_matmul", "qws_rope_at_pos", "qws_kv_append",
+              "qws_kv_attention"]:
         assert n in names
 
 
@@ -169,6 +170,32 @@ def test_prefill_checks(lib):
     assert lib.qws_q4k_prefill_matmul(A, A, A, 10, 2560, 8, A, small - 16, None) == WORKSPACE
     assert lib.qws_q4k_prefill_matmul(A, A, A, 10, 2560, 8, A + 8, small, None) == ALIGN
     assert lib.qws_q4k_prefill_matmul(A, A, A, 0, 2560, 8, A, small, None) == OK
+
+
+def test_attention_checks(lib):
+    ws = lib.qws_workspace_bytes(_lib.OP_KV_ATTENTION, 4096, 256, 8, 4, 0)
+    assert ws > 0
+    assert lib.qws_workspace_bytes(_lib.OP_KV_ATTENTION, 4096, 256, 6, 4, 0) == 0
+    f, d = C.c_float, C.c_double
+    assert lib.qws_rope_at_pos(None, 8, 256, 256, 5, d(1e4), None) == NULL
+    assert lib.qws_rope_at_pos(A, 8, 256, 255, 5, d(1e4), None) == SHAPE
+    assert lib.qws_rope_at_pos(A, 8, 256, 258, 5, d(1e4), None) == SHAPE
+    assert lib.qws_rope_at_pos(A, 8, 256, 256, -1, d(1e4), None) == SHAPE
+    assert lib.qws_rope_at_pos(A, 8, 256, 256, 5, d(0.0), None) == SHAPE
+    assert lib.qws_kv_append(A, A, A, None, 4, 256, 100, 5, None) == NULL
+    assert lib.qws_kv_append(A, A, A, A, 4, 256, 100, 100, None) == SHAPE
+    assert lib.qws_kv_attention(A, A, A, A, 8, 4, 200, 4096, 4096, f(0.0625), f(0.0), A, ws,
+                                None) == SHAPE
+    assert lib.qws_kv_attention(A, A, A, A, 10, 2, 256, 4096, 4096, f(0.0625), f(0.0), A, ws,
+                                None) == SHAPE                       # group 5 > 4
+    assert lib.qws_kv_attention(A, A, A, A, 8, 4, 256, 4096, 4097, f(0.0625), f(0.0), A, ws,
+                                None) == SHAPE
+    assert lib.qws_kv_attention(A, A, A, A, 8, 4, 256, 4096, 4096, f(0.0625), f(-1.0), A, ws,
+                                None) == SHAPE
+    assert lib.qws_kv_attention(A, A, A, A, 8, 4, 256, 4096, 4096, f(0.0625), f(0.0), A, ws - 16,
+                                None) == WORKSPACE
+    assert lib.qws_kv_attention(A + 4, A, A, A, 8, 4, 256, 4096, 4096, f(0.0625), f(0.0), A, ws,
+                                None) == ALIGN
 
 
 def test_vector_op_checks(lib):

@@ -18,7 +18,6 @@ What pins each function:
   softcap and softcap bounds every score; GQA grouping; the returned bound
   dominates |out|.
 """
-import math
 
 import numpy as np
 import pytest
