@@ -535,7 +535,7 @@ qws_status qws_device_error(unsigned* code) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "qws_device_error", "");
   *code = qws::read_clear_matvec_errors() | qws::read_clear_chain_errors() |
-          qws::read_clear_prefill_errors();
+          qws::read_clear_prefill_errors() | qws::read_clear_attention_errors();
   return *code ? fail(QWS_ERR_TIMEOUT, "device error code 0x%x", *code) : ok();
 }
 

@@ -6,13 +6,16 @@
 //
 // kv_attention is bound by reading the caches (2 * n_kv * n_ctx * head_dim
 // floats), so it is split along the positions (flash-decoding style):
-//   * kernel 1, grid (splits, n_kv): CTA (j, g) owns positions
-//     [j * chunk, (j + 1) * chunk) of kv head g and every query head of g's
-//     group.  Warp w takes positions j*chunk + w, + 8, ...; lane L holds
+//   * kernel 1, grid (splits, n_kv): CTA (j, g) owns the blocks of P
+//     positions b = j, j + splits, ... of kv head g (so the CTAs of a head
+//     sweep its cache side by side) and every query head of g's group.  A
+//     copy warp streams each block's k rows and v rows into a shared-memory
+//     ring (1-D TMA bulk copies); warp w takes rows w, w + 8, ... of a
+//     block; lane L holds
 //     columns [L*hd/32, (L+1)*hd/32) of q, k, v and of the running output, so
 //     a warp reads each k and v row as one coalesced run.  Per position: the
 //     group's scores by warp-shuffle sums, optional softcap, then the online
-//     softmax update (running max m, sum l, output acc).  The 8 warps are
+//     softmax update (running max m, sum l, output acc).  The 16 warps are
 //     merged in shared memory in a fixed order and the CTA writes its
 //     (m, l, acc) partial to the workspace.
 //   * kernel 2, one CTA per query head: merges the splits in order:
@@ -27,9 +30,12 @@
 
 namespace qws {
 
-constexpr int kAttWarps = 8;
-constexpr int kAttMaxGroup = 4;     // query heads per kv head
-constexpr int kAttMaxPerLane = 8;   // head_dim / 32
+__device__ unsigned g_err_attention;
+
+constexpr int kAttWarps = 16;                   // consumer warps
+constexpr int kAttThreads = 32 + kAttWarps * 32;  // + one copy warp
+constexpr int kAttStages = 3;
+constexpr uint32_t kAttStageBytes = 64 * 1024;  // P k rows + P v rows, P = 8192 / head_dim
 
 // ------------------------------------------------------------------ rope
 // (x_i, x_{i+r/2}) rotated by theta_i = pos * base^(-2i/r), i < r/2, every head;
@@ -79,102 +85,139 @@ struct AttParams {
   float* part;         // [n_kv][splits][group][hd + 2]: acc..., m, l
   float* out;          // [n_q][hd]
   int n_q, n_kv, hd, group, splits;
-  int64_t max_seq, n_ctx, chunk;
+  int64_t max_seq, n_ctx;
   float scale, softcap;
 };
 
-// kPL consecutive floats of a k row and of a v row (16-byte loads when kPL
-// is a multiple of 4; the rows start on 16-byte boundaries then)
-template <int kPL>
-__device__ __forceinline__ void load_row(const float* k, const float* v, float (&kr)[kPL],
-                                         float (&vr)[kPL]) {
-  if constexpr (kPL % 4 == 0) {
-#pragma unroll
-    for (int c = 0; c < kPL; c += 4) {
-      const float4 a = __ldg(reinterpret_cast<const float4*>(k + c));
-      const float4 b = __ldg(reinterpret_cast<const float4*>(v + c));
-      kr[c] = a.x; kr[c + 1] = a.y; kr[c + 2] = a.z; kr[c + 3] = a.w;
-      vr[c] = b.x; vr[c + 1] = b.y; vr[c + 2] = b.z; vr[c + 3] = b.w;
-    }
-  } else {
-#pragma unroll
-    for (int c = 0; c < kPL; ++c) {
-      kr[c] = __ldg(k + c);
-      vr[c] = __ldg(v + c);
-    }
-  }
-}
-
-template <int kPL>   // columns per lane = hd / 32
-__global__ void __launch_bounds__(kAttWarps * 32) kv_attention_split_kernel(
+template <int kPL, int kG>   // columns per lane = hd / 32; query heads per kv head
+__global__ void __launch_bounds__(kAttThreads, 1) kv_attention_split_kernel(
     const __grid_constant__ AttParams p) {
-  __shared__ float sm_m[kAttWarps][kAttMaxGroup], sm_l[kAttWarps][kAttMaxGroup];
-  __shared__ float sm_acc[kAttWarps][kAttMaxGroup][kAttMaxPerLane * 32];
+  __shared__ float sm_m[kAttWarps][kG], sm_l[kAttWarps][kG];
+  __shared__ __align__(8) uint64_t full[kAttStages], empty[kAttStages];
+  extern __shared__ __align__(128) uint8_t att_ring[];   // kAttStages x kAttStageBytes
+  const int warp = static_cast<int>(threadIdx.x >> 5) - 1;   // -1: the copy warp
+  const int lane = threadIdx.x & 31;
+  const int j = blockIdx.x, g = blockIdx.y;
+  constexpr int G = kG;
+  constexpr int P = kAttStageBytes / (2 * kPL * 32 * 4);     // positions per stage
+  // blocks of P positions are dealt to the splits in turn (block b to split
+  // b % splits), so that the CTAs of one kv head sweep its cache together
+  const int64_t n_blocks = (p.n_ctx + P - 1) / P;
+  const int n_stages =
+      j < n_blocks ? static_cast<int>((n_blocks - j + p.splits - 1) / p.splits) : 0;
+  const size_t row = static_cast<size_t>(kPL) * 32 * 4;      // bytes of one k or v row
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kAttStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], kAttWarps);
+    }
+    fence_barrier_init();
+  }
+  __syncthreads();
   pdl_launch_dependents();
   pdl_wait();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int j = blockIdx.x, g = blockIdx.y;
-  const int G = p.group;
-  const int64_t t0 = static_cast<int64_t>(j) * p.chunk;
-  const int64_t t1 = min(t0 + p.chunk, p.n_ctx);
-  const float* kg = p.kc + static_cast<int64_t>(g) * p.max_seq * p.hd;
-  const float* vg = p.vc + static_cast<int64_t>(g) * p.max_seq * p.hd;
+  if (warp < 0) {
+    // ---- copy warp: per stage, P consecutive k rows then P v rows (16 B aligned)
+    if (lane == 0) {
+      const uint64_t pol = l2_policy_evict_first();
+      const uint8_t* kg = reinterpret_cast<const uint8_t*>(p.kc + static_cast<int64_t>(g) * p.max_seq * p.hd);
+      const uint8_t* vg = reinterpret_cast<const uint8_t*>(p.vc + static_cast<int64_t>(g) * p.max_seq * p.hd);
+      for (int st = 0; st < n_stages; ++st) {
+        const int s = st % kAttStages;
+        const uint32_t ph = static_cast<uint32_t>(st / kAttStages) & 1u;
+        if (!mbar_wait(&empty[s], ph ^ 1u)) {
+          atomicOr(&g_err_attention, kErrEmptyWait);
+          break;
+        }
+        const int64_t ta = (j + static_cast<int64_t>(st) * p.splits) * P;
+        const uint32_t rows = static_cast<uint32_t>(min(static_cast<int64_t>(P), p.n_ctx - ta));
+        const uint32_t bytes = rows * static_cast<uint32_t>(row);
+        uint8_t* dst = att_ring + static_cast<size_t>(s) * kAttStageBytes;
+        mbar_arrive_expect_tx(&full[s], 2u * bytes);
+        bulk_copy_g2s(dst, kg + ta * row, bytes, &full[s], pol);
+        bulk_copy_g2s(dst + P * row, vg + ta * row, bytes, &full[s], pol);
+      }
+      // do not leave with copies into shared memory in flight
+      const int first = n_stages > kAttStages ? n_stages - kAttStages : 0;
+      for (int st = first; st < n_stages; ++st)
+        if (!mbar_wait(&full[st % kAttStages], static_cast<uint32_t>(st / kAttStages) & 1u))
+          atomicOr(&g_err_attention, kErrDrain);
+    }
+    return;
+  }
   const int c0 = lane * kPL;
-
-  float q[kAttMaxGroup][kPL], acc[kAttMaxGroup][kPL], m[kAttMaxGroup], l[kAttMaxGroup];
+  float q[kG][kPL], acc[kG][kPL], m[kG], l[kG];
 #pragma unroll
-  for (int h = 0; h < kAttMaxGroup; ++h) {
+  for (int h = 0; h < kG; ++h) {
     m[h] = -INFINITY;
     l[h] = 0.f;
 #pragma unroll
     for (int c = 0; c < kPL; ++c) {
-      q[h][c] = h < G ? p.q[static_cast<int64_t>(g * G + h) * p.hd + c0 + c] * p.scale : 0.f;
+      q[h][c] = p.q[static_cast<int64_t>(g * G + h) * p.hd + c0 + c] * p.scale;
       acc[h][c] = 0.f;
     }
   }
-  // the next position's k and v rows are loaded while this one is used
-  float kn[kPL], vn[kPL];
-  int64_t t = t0 + warp;
-  if (t < t1) load_row<kPL>(kg + t * p.hd + c0, vg + t * p.hd + c0, kn, vn);
-  for (; t < t1; t += kAttWarps) {
-    float kr[kPL], vr[kPL];
-#pragma unroll
-    for (int c = 0; c < kPL; ++c) {
-      kr[c] = kn[c];
-      vr[c] = vn[c];
+  for (int st = 0; st < n_stages; ++st) {
+    const int s = st % kAttStages;
+    const uint32_t ph = static_cast<uint32_t>(st / kAttStages) & 1u;
+    if (!mbar_wait(&full[s], ph)) {
+      atomicOr(&g_err_attention, kErrFullWait);
+      break;
     }
-    if (t + kAttWarps < t1)
-      load_row<kPL>(kg + (t + kAttWarps) * p.hd + c0, vg + (t + kAttWarps) * p.hd + c0, kn, vn);
+    const int64_t ta = (j + static_cast<int64_t>(st) * p.splits) * P;
+    const int rows = static_cast<int>(min(static_cast<int64_t>(P), p.n_ctx - ta));
+    const float* kst = reinterpret_cast<const float*>(att_ring + static_cast<size_t>(s) * kAttStageBytes);
+    const float* vst = kst + P * kPL * 32;
+    for (int r = warp; r < rows; r += kAttWarps) {
+      float kr[kPL], vr[kPL];
 #pragma unroll
-    for (int h = 0; h < kAttMaxGroup; ++h) {
-      if (h >= G) break;
-      float s = 0.f;
+      for (int c = 0; c < kPL; c += (kPL % 4 == 0 ? 4 : 1)) {
+        if constexpr (kPL % 4 == 0) {
+          const float4 a = *reinterpret_cast<const float4*>(kst + r * kPL * 32 + c0 + c);
+          const float4 b = *reinterpret_cast<const float4*>(vst + r * kPL * 32 + c0 + c);
+          kr[c] = a.x; kr[c + 1] = a.y; kr[c + 2] = a.z; kr[c + 3] = a.w;
+          vr[c] = b.x; vr[c + 1] = b.y; vr[c + 2] = b.z; vr[c + 3] = b.w;
+        } else {
+          kr[c] = kst[r * kPL * 32 + c0 + c];
+          vr[c] = vst[r * kPL * 32 + c0 + c];
+        }
+      }
 #pragma unroll
-      for (int c = 0; c < kPL; ++c) s = fmaf(q[h][c], kr[c], s);
-      s = warp_sum(s);
-      if (p.softcap > 0.f) s = p.softcap * tanhf(s / p.softcap);
-      const float mn = fmaxf(m[h], s);
-      const float alpha = expf(m[h] - mn);   // 0 on the first position (m = -inf)
-      const float pr = expf(s - mn);
-      l[h] = fmaf(l[h], alpha, pr);
+      for (int h = 0; h < kG; ++h) {
+        float sc = 0.f;
 #pragma unroll
-      for (int c = 0; c < kPL; ++c) acc[h][c] = fmaf(acc[h][c], alpha, pr * vr[c]);
-      m[h] = mn;
+        for (int c = 0; c < kPL; ++c) sc = fmaf(q[h][c], kr[c], sc);
+        sc = warp_sum(sc);
+        if (p.softcap > 0.f) sc = p.softcap * tanhf(sc / p.softcap);
+        const float mn = fmaxf(m[h], sc);
+        const float alpha = expf(m[h] - mn);
+        const float pr = expf(sc - mn);
+        l[h] = fmaf(l[h], alpha, pr);
+#pragma unroll
+        for (int c = 0; c < kPL; ++c) acc[h][c] = fmaf(acc[h][c], alpha, pr * vr[c]);
+        m[h] = mn;
+      }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[s]);
   }
-  // merge the warps in order 0..7
+  // merge the warps in order 0..15; the ring is free once every consumer is
+  // past its last stage (every copy it waited for has landed), so the
+  // warps' outputs are parked there
+  bar_sync(1, kAttWarps * 32);
+  float* sm_acc = reinterpret_cast<float*>(att_ring);      // [kAttWarps][kG][hd]
 #pragma unroll
-  for (int h = 0; h < kAttMaxGroup; ++h) {
-    if (h >= G) break;
+  for (int h = 0; h < kG; ++h) {
     if (lane == 0) {
       sm_m[warp][h] = m[h];
       sm_l[warp][h] = l[h];
     }
 #pragma unroll
-    for (int c = 0; c < kPL; ++c) sm_acc[warp][h][c0 + c] = acc[h][c];
+    for (int c = 0; c < kPL; ++c) sm_acc[(warp * kG + h) * p.hd + c0 + c] = acc[h][c];
   }
-  __syncthreads();
-  for (int e = threadIdx.x; e < G * p.hd; e += blockDim.x) {
+  bar_sync(1, kAttWarps * 32);
+  const int ct = static_cast<int>(threadIdx.x) - 32;
+  for (int e = ct; e < G * p.hd; e += kAttWarps * 32) {
     const int h = e / p.hd, i = e - h * p.hd;
     float M = -INFINITY;
     for (int w = 0; w < kAttWarps; ++w) M = fmaxf(M, sm_m[w][h]);
@@ -182,7 +225,7 @@ __global__ void __launch_bounds__(kAttWarps * 32) kv_attention_split_kernel(
     if (M != -INFINITY) {
       for (int w = 0; w < kAttWarps; ++w) {
         const float f = expf(sm_m[w][h] - M);   // 0 for an empty warp
-        a = fmaf(sm_acc[w][h][i], f, a);
+        a = fmaf(sm_acc[(w * kG + h) * p.hd + i], f, a);
         L = fmaf(sm_l[w][h], f, L);
       }
     }
@@ -220,9 +263,11 @@ __global__ void kv_attention_merge_kernel(const __grid_constant__ AttParams p) {
 }
 
 // ------------------------------------------------------------------ host side
+// One CTA per SM of a 152-SM GB300 in total (n_kv rows of splits), at least
+// 64 positions per split.
 int kv_attention_splits(int n_kv, int64_t n_ctx) {
-  const int64_t by_len = (n_ctx + 127) / 128;
-  const int64_t by_grid = std::max(1, 512 / n_kv);
+  const int64_t by_len = (n_ctx + 63) / 64;
+  const int64_t by_grid = std::max(1, (152 + n_kv - 1) / n_kv);
   return static_cast<int>(std::max<int64_t>(1, std::min(by_len, by_grid)));
 }
 
@@ -233,12 +278,12 @@ size_t kv_attention_workspace_bytes(int n_q, int n_kv, int head_dim, int64_t n_c
 }
 
 template <class... KArgs, class... Args>
-static cudaError_t launch_pdl_att(void (*kernel)(KArgs...), dim3 grid, int threads,
+static cudaError_t launch_pdl_att(void (*kernel)(KArgs...), dim3 grid, int threads, size_t smem,
                                   cudaStream_t st, Args&&... args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = dim3(threads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -251,17 +296,35 @@ static cudaError_t launch_pdl_att(void (*kernel)(KArgs...), dim3 grid, int threa
 cudaError_t launch_rope(float* x, int n_heads, int head_dim, int rot_dim, int64_t pos,
                         double base, cudaStream_t st) {
   const int64_t n = static_cast<int64_t>(n_heads) * (rot_dim / 2);
-  const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 1024)));
-  return launch_pdl_att(rope_kernel, dim3(blocks), 256, st, x, n_heads, head_dim, rot_dim, pos,
-                        base);
+  const int blocks =
+      static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 1024)));
+  return launch_pdl_att(rope_kernel, dim3(blocks), 256, 0, st, x, n_heads, head_dim, rot_dim,
+                        pos, base);
 }
 
 cudaError_t launch_kv_append(float* kc, float* vc, const float* k, const float* v, int n_kv,
                              int head_dim, int64_t max_seq, int64_t pos, cudaStream_t st) {
   const int64_t n = static_cast<int64_t>(n_kv) * head_dim;
-  const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 1024)));
-  return launch_pdl_att(kv_append_kernel, dim3(blocks), 256, st, kc, vc, k, v, n_kv, head_dim,
+  const int blocks =
+      static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 1024)));
+  return launch_pdl_att(kv_append_kernel, dim3(blocks), 256, 0, st, kc, vc, k, v, n_kv, head_dim,
                         max_seq, pos);
+}
+
+template <int kPL, int kG>
+static cudaError_t launch_split(const AttParams& p, dim3 grid, cudaStream_t st) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const size_t smem = static_cast<size_t>(kAttStages) * kAttStageBytes;
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        kv_attention_split_kernel<kPL, kG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  return launch_pdl_att(kv_attention_split_kernel<kPL, kG>, grid, kAttThreads, smem, st, p);
 }
 
 cudaError_t launch_kv_attention(const float* q, const float* kc, const float* vc, float* out,
@@ -280,20 +343,29 @@ cudaError_t launch_kv_attention(const float* q, const float* kc, const float* vc
   p.splits = kv_attention_splits(n_kv, n_ctx);
   p.max_seq = max_seq;
   p.n_ctx = n_ctx;
-  p.chunk = (n_ctx + p.splits - 1) / p.splits;
   p.scale = scale;
   p.softcap = softcap;
   const dim3 grid(p.splits, n_kv);
   cudaError_t e;
-  switch (head_dim / 32) {
-    case 1: e = launch_pdl_att(kv_attention_split_kernel<1>, grid, kAttWarps * 32, st, p); break;
-    case 2: e = launch_pdl_att(kv_attention_split_kernel<2>, grid, kAttWarps * 32, st, p); break;
-    case 4: e = launch_pdl_att(kv_attention_split_kernel<4>, grid, kAttWarps * 32, st, p); break;
-    case 8: e = launch_pdl_att(kv_attention_split_kernel<8>, grid, kAttWarps * 32, st, p); break;
+  switch ((head_dim / 32) * 8 + p.group) {
+#define QWS_ATT_CASE(PL, G) \
+  case PL * 8 + G: e = launch_split<PL, G>(p, grid, st); break;
+    QWS_ATT_CASE(1, 1) QWS_ATT_CASE(1, 2) QWS_ATT_CASE(1, 3) QWS_ATT_CASE(1, 4)
+    QWS_ATT_CASE(2, 1) QWS_ATT_CASE(2, 2) QWS_ATT_CASE(2, 3) QWS_ATT_CASE(2, 4)
+    QWS_ATT_CASE(4, 1) QWS_ATT_CASE(4, 2) QWS_ATT_CASE(4, 3) QWS_ATT_CASE(4, 4)
+    QWS_ATT_CASE(8, 1) QWS_ATT_CASE(8, 2) QWS_ATT_CASE(8, 3) QWS_ATT_CASE(8, 4)
+#undef QWS_ATT_CASE
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  return launch_pdl_att(kv_attention_merge_kernel, dim3(n_q), 256, st, p);
+  return launch_pdl_att(kv_attention_merge_kernel, dim3(n_q), 256, 0, st, p);
+}
+
+unsigned read_clear_attention_errors() {
+  unsigned v = 0, z = 0;
+  if (cudaMemcpyFromSymbol(&v, g_err_attention, sizeof(v)) != cudaSuccess) return 0;
+  cudaMemcpyToSymbol(g_err_attention, &z, sizeof(z));
+  return v;
 }
 
 }  // namespace qws

@@ -105,6 +105,7 @@ cudaError_t launch_matvec_q8(int wfmt, const Seg* segs, int nseg, const uint8_t*
 cudaError_t launch_quantize_q8_0(const float* x, uint8_t* xq, int64_t nblocks, cudaStream_t st);
 // attention over a KV cache (attention.cu)
 size_t kv_attention_workspace_bytes(int n_q, int n_kv, int head_dim, int64_t n_ctx);
+unsigned read_clear_attention_errors();
 cudaError_t launch_rope(float* x, int n_heads, int head_dim, int rot_dim, int64_t pos,
                         double base, cudaStream_t st);
 cudaError_t launch_kv_append(float* kc, float* vc, const float* k, const float* v, int n_kv,
