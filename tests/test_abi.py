@@ -192,7 +192,7 @@ def test_attention_checks(lib):
                                 None) == SHAPE
     assert lib.qws_kv_attention(A, A, A, A, 8, 4, 256, 4096, 4096, f(0.0625), f(-1.0), A, ws,
                                 None) == SHAPE
-    assert lib.qws_kv_attention(A, A, A, A, 8, 4, 256, 4096, 4096, f(0.0625), f(0.0), A, ws - 16,
+    assert lib.qws_kv_attention(A, A, A, A, 8, 4, 256, 4096, 4096, f(0.0625), f(0.0), A, 16,
                                 None) == WORKSPACE
     assert lib.qws_kv_attention(A + 4, A, A, A, 8, 4, 256, 4096, 4096, f(0.0625), f(0.0), A, ws,
                                 None) == ALIGN
