@@ -387,7 +387,10 @@ __device__ __forceinline__ bool stage_gather(const Ring& R, int US, const Word* 
 
 // Builds the input vector of phase ph into R.xs, then counts this CTA's
 // prologue as finished.  Out of line: it runs once per phase and must not take
-// registers from the decode loop.
+// registers from the decode loop.  kWide: hidden > 8 * 320 (16 values per
+// thread in the residual / norm step); a separate instantiation, so the
+// common case carries none of its registers.
+template <bool kWide>
 __device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const Ring& R,
                                             float* wsum, bool q6, int ctid, int C) {
   const int l = ph >> 2, kind = ph & 3;
@@ -395,7 +398,6 @@ __device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const 
   const KindPlan& kp = p.kp[kind];
   const int US = red_stride(kp.U);
   const unsigned prev = static_cast<unsigned>(ph);   // stamp of the previous phase's outputs
-  const bool wide = p.H > 8 * static_cast<int64_t>(C);
   bool ok = true;
   // the keeper overwrites hin[l & 1] (QKV; last read by GU(l - 2)) or h1[l & 1]
   // (GU; last read by QKV(l - 1)): load that count now, check it before the
@@ -436,12 +438,14 @@ __device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const 
       store = blockIdx.x == gridDim.x - 1 ? p.h1 + (l & 1) * p.H : nullptr;
       war = 4 * l - 4;   // QKV(l - 1) read h1[l & 1] last
     }
-    ok = wide ? resnorm_stage<16, false>(p, R, wsum, base, base_stamp, base_plain, add, add_stamp,
-                                         wa, wn, store, static_cast<unsigned>(ph + 1), war,
-                                         war_seen, US, ctid)
-              : resnorm_stage<8, true>(p, R, wsum, base, base_stamp, base_plain, add, add_stamp,
-                                       wa, wn, store, static_cast<unsigned>(ph + 1), war,
-                                       war_seen, US, ctid);
+    if constexpr (kWide)
+      ok = resnorm_stage<16, false>(p, R, wsum, base, base_stamp, base_plain, add, add_stamp, wa,
+                                    wn, store, static_cast<unsigned>(ph + 1), war, war_seen, US,
+                                    ctid);
+    else
+      ok = resnorm_stage<8, true>(p, R, wsum, base, base_stamp, base_plain, add, add_stamp, wa,
+                                  wn, store, static_cast<unsigned>(ph + 1), war, war_seen, US,
+                                  ctid);
   } else if (kind == PH_O) {
     ok = stage_gather<8>(R, US, p.v, prev, kp.K, p.head_dim, p.n_q_heads / p.n_kv_heads, ctid);
   } else if (q6) {
@@ -537,6 +541,7 @@ __device__ __forceinline__ void prefetch_l2(const float* w, int64_t n) {
 }
 
 // ------------------------------------------------------------------ kernel
+template <bool kWide>
 __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
     chain_kernel(const __grid_constant__ ChainParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -582,7 +587,7 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
   for (int ph = 0; ph < nph; ++ph) {
     const Phase P = phases.get(ph);
     const bool q6 = (ph & 3) == PH_DOWN && down_q6k;
-    if (!chain_prologue(p, ph, R, wsum, q6, ctid, C)) return;
+    if (!chain_prologue<kWide>(p, ph, R, wsum, q6, ctid, C)) return;
     const unsigned long long r = chain_consume(
         P.fmt, P.epi, P.nseg, static_cast<int>(P.seg[0].rows), static_cast<int>(P.seg[1].rows),
         static_cast<int>(P.seg[2].rows), P.seg[0].tiles, P.seg[1].tiles, P.seg[2].tiles, P.T, P.U,
@@ -758,21 +763,25 @@ qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
   const size_t smem = ring_smem_bytes(p.S, p.stage_bytes, p.red_floats, p.xs_floats) + tail;
   const int threads = kRoleThreads + kMaxConsumers;
 
+  // hidden > 8 * 320 takes the wide prologue instantiation
+  const bool wide = p.H > 8 * static_cast<int64_t>(kMaxConsumers);
+  const void* kfn = wide ? reinterpret_cast<const void*>(chain_kernel<true>)
+                         : reinterpret_cast<const void*>(chain_kernel<false>);
   static std::mutex mu;
-  static int attr_dev[64] = {0};
+  static int attr_dev[2][64] = {{0}};
   int dev = 0;
   cudaGetDevice(&dev);
   {
     std::lock_guard<std::mutex> lock(mu);
-    if (dev >= 0 && dev < 64 && !attr_dev[dev]) {
+    if (dev >= 0 && dev < 64 && !attr_dev[wide][dev]) {
       int optin = 0;
       cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-      cudaFuncSetAttribute(chain_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-      attr_dev[dev] = 1;
+      cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+      attr_dev[wide][dev] = 1;
     }
   }
   int bps = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, chain_kernel, threads, smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kfn, threads, smem);
   if (bps < 1) {
     err = "qws_decode_chain: kernel does not fit on an SM";
     return QWS_ERR_CUDA;
@@ -785,8 +794,7 @@ qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
     return QWS_ERR_CUDA;
   }
   void* args[] = {&p};
-  e = cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(chain_kernel), dim3(grid),
-                                  dim3(threads), args, smem, st);
+  e = cudaLaunchCooperativeKernel(kfn, dim3(grid), dim3(threads), args, smem, st);
   if (e != cudaSuccess) {
     err = std::string("qws_decode_chain: ") + cudaGetErrorName(e) + " " + cudaGetErrorString(e);
     return QWS_ERR_CUDA;

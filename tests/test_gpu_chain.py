@@ -80,6 +80,28 @@ def test_chain_small_teacher_forced(post_norms, fmt_down):
     assert np.array_equal(run_chain(ldev, h0, dims), hall)
 
 
+# hidden above 8 * 320 takes the wide prologue (16 values per thread in the
+# residual / norm step), a separate kernel instantiation.
+WIDE = dict(hidden=4096, inter=4096, n_q_heads=8, n_kv_heads=4, head_dim=256, eps=1e-6,
+            post_norms=1)
+
+
+def test_chain_wide_hidden_teacher_forced():
+    dims = WIDE
+    n = 2
+    layers = [synth.chain_layer(l, dims, fmt_down=oracle.Q6_K, workload=56) for l in range(n)]
+    ldev = [to_dev(L) for L in layers]
+    h0 = synth.normal_vector(synth.rng(57), dims["hidden"])
+    h = h0
+    outs = []
+    for l in range(n):
+        hg = run_chain([ldev[l]], h, dims)
+        check_layer(h, hg, layers[l], dims)
+        outs.append(hg)
+        h = hg
+    assert np.array_equal(run_chain(ldev, h0, dims), outs[-1])
+
+
 # Fewer 16-byte row groups than CTAs in the down phase (Q6_K rows of 256
 # columns are 210 B: 8-row groups, 32 of them): most CTAs own no rows there and
 # still take part in every phase's synchronisation.
