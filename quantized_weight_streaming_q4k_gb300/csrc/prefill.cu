@@ -48,18 +48,26 @@ constexpr int kPfN = 256;                  // tokens per tile (MMA N, TMEM colum
 constexpr int kPfK = 64;                   // columns per stage: one 128-byte f16 row
 constexpr uint32_t kPfATile = kPfM * kPfK * 2;     // 16 KB
 constexpr uint32_t kPfBTile = kPfN * kPfK * 2;     // 32 KB
-constexpr uint32_t kPfStage = kPfATile + kPfBTile;
 constexpr uint32_t kPfWBuf = kPfM * 144;           // one Q4_K super-block of every row
 constexpr int kPfThreads = 352;            // 3 role warps + 8 decoder warps
 constexpr int kPfDecoders = 256;
 // TMEM columns: a power of two >= 32 that holds the N accumulator columns
 constexpr uint32_t kPfTmemCols = kPfN <= 32 ? 32u : kPfN <= 64 ? 64u : kPfN <= 128 ? 128u : 256u;
 static_assert(kPfN % 16 == 0 && kPfN <= 256, "MMA N must be a multiple of 16 up to 256");
-// as many stages as fit beside the two weight buffers in 227 KB
-constexpr int kPfStages =
-    static_cast<int>((227u * 1024u - 1024u - 2u * kPfWBuf - 256u) / kPfStage);
-constexpr size_t kPfSmemBytes = 1024 + kPfStages * kPfStage + 2 * kPfWBuf + 256;
-static_assert(kPfStages >= 2, "shared memory too small for two stages");
+// A CTA computes kAcc token tiles of 256 against one decoded weight tile
+// (kAcc accumulators of 256 TMEM columns side by side), so one decode of the
+// weights serves 256 * kAcc tokens.  A stage holds the weight tile and kAcc
+// token tiles; as many stages as fit beside the two weight buffers in 227 KB.
+template <int kAcc>
+struct PfCfg {
+  static constexpr uint32_t kStage = kPfATile + kAcc * kPfBTile;
+  static constexpr int kStages =
+      static_cast<int>((227u * 1024u - 1024u - 2u * kPfWBuf - 256u) / kStage);
+  static constexpr size_t kSmem = 1024 + kStages * kStage + 2 * kPfWBuf + 256;
+  static constexpr uint32_t kTmemCols = kAcc == 1 ? kPfTmemCols : 512u;
+  static_assert(kStages >= 2, "shared memory too small for two stages");
+  static_assert(kAcc == 1 || (kAcc == 2 && kPfN == 256), "two accumulators fill the 512 columns");
+};
 
 // f32 accumulate, f16 A and B, both K-major, N = 256, M = 128.
 constexpr uint32_t kPfIdesc = (1u << 4) | (0u << 7) | (0u << 10) |
@@ -69,7 +77,7 @@ constexpr uint32_t kPfIdesc = (1u << 4) | (0u << 7) | (0u << 10) |
 struct PrefillParams {
   CUtensorMap wmap;       // W as a [rows][row_bytes] byte matrix; box 144 x 128
   const uint8_t* W;       // Q4_K, rows x K
-  const uint8_t* X16;     // packed f16 tiles [n_tiles_n][KC][32 KB]
+  const uint8_t* X16;     // packed f16 tiles [n_tiles_n][KC][32 KB] (n_tiles_n % kAcc == 0)
   float* Y;               // [N][rows]
   int64_t rows, K, N;
   int KC;                 // K / 64
@@ -274,8 +282,11 @@ enum : unsigned {
 // threads per weight row: low-nibble and high-nibble halves) and then run
 // the epilogue (warp w reads TMEM lanes 32 * (w % 4) .. + 31, columns of its
 // half of the tile).
+template <int kAcc>
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid_constant__
                                                                     PrefillParams p) {
+  constexpr int kPfStages = PfCfg<kAcc>::kStages;
+  constexpr uint32_t kPfStage = PfCfg<kAcc>::kStage;
   extern __shared__ __align__(1024) uint8_t pf_smem_raw[];
   const uint32_t raw = smem_addr(pf_smem_raw);
   uint8_t* stages = pf_smem_raw + ((1024u - (raw & 1023u)) & 1023u);
@@ -289,8 +300,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
 
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31);
-  const int tm = static_cast<int>(blockIdx.x) / p.n_tiles_n;
-  const int tn = static_cast<int>(blockIdx.x) - tm * p.n_tiles_n;
+  const int n_groups = p.n_tiles_n / kAcc;
+  const int tm = static_cast<int>(blockIdx.x) / n_groups;
+  const int tg = static_cast<int>(blockIdx.x) - tm * n_groups;   // token tiles kAcc*tg ..
   const int64_t m0 = static_cast<int64_t>(tm) * kPfM;
   const int KC = p.KC;
   const int KB = KC / 4;
@@ -310,7 +322,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kPfTmemCols);
+    tmem_alloc(tmem_slot, PfCfg<kAcc>::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -326,7 +338,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
     // ---- B producer: one 32 KB bulk copy per stage
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      const uint8_t* xb = p.X16 + static_cast<int64_t>(tn) * KC * kPfBTile;
+      const uint8_t* xb = p.X16 + static_cast<int64_t>(tg) * kAcc * KC * kPfBTile;
       for (int kc = 0; kc < KC; ++kc) {
         const int s = kc % kPfStages;
         const uint32_t ph = static_cast<uint32_t>(kc / kPfStages) & 1u;
@@ -334,9 +346,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
           atomicOr(&g_err_prefill, kErrPfEmpty);
           break;
         }
-        mbar_arrive_expect_tx(&full[s], kPfBTile);
-        bulk_copy_g2s(stages + s * kPfStage + kPfATile, xb + static_cast<int64_t>(kc) * kPfBTile,
-                      kPfBTile, &full[s], pol);
+        mbar_arrive_expect_tx(&full[s], kAcc * kPfBTile);
+#pragma unroll
+        for (int a = 0; a < kAcc; ++a)
+          bulk_copy_g2s(stages + s * kPfStage + kPfATile + a * kPfBTile,
+                        xb + (static_cast<int64_t>(a) * KC + kc) * kPfBTile, kPfBTile, &full[s],
+                        pol);
       }
     }
   } else if (warp == 2) {
@@ -367,11 +382,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
         }
         tc_fence_after();
         const uint32_t a = smem_addr(stages + s * kPfStage);
-        const uint32_t b = a + kPfATile;
 #pragma unroll
-        for (int k = 0; k < kPfK / 16; ++k)
-          tc_mma_f16(tmem, sw128_desc(a + 32u * k), sw128_desc(b + 32u * k), kPfIdesc,
-                     (kc | k) != 0 ? 1u : 0u);
+        for (int k = 0; k < kPfK / 16; ++k) {
+#pragma unroll
+          for (int t = 0; t < kAcc; ++t)
+            tc_mma_f16(tmem + static_cast<uint32_t>(t * kPfN), sw128_desc(a + 32u * k),
+                       sw128_desc(a + kPfATile + t * kPfBTile + 32u * k), kPfIdesc,
+                       (kc | k) != 0 ? 1u : 0u);
+        }
         tc_commit(&empty[s]);
       }
       // the accumulator is final once every MMA above has completed
@@ -423,11 +441,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
     tc_fence_after();
     if (ok) {
       const int q = warp & 3;
-      const int colh = (warp - 3) >> 2;     // 0: columns 0..N/2-1, 1: the rest
+      // warps 3..6 take the first half of the kAcc * 256 columns, 7..10 the
+      // rest; column c is token n0 + c (the accumulators are adjacent)
+      constexpr int kCols = kAcc * kPfN / 2;
+      const int colh = (warp - 3) >> 2;
       const int64_t rr = m0 + 32 * q + lane;
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16);
-      const int64_t n0 = static_cast<int64_t>(tn) * kPfN;
-      for (int cc = colh * (kPfN / 2); cc < (colh + 1) * (kPfN / 2); cc += 16) {
+      const int64_t n0 = static_cast<int64_t>(tg) * kAcc * kPfN;
+      for (int cc = colh * kCols; cc < (colh + 1) * kCols; cc += 16) {
         uint32_t v[16];
         tc_ld16(tbase + static_cast<uint32_t>(cc), v);
         tc_wait_ld();
@@ -449,14 +470,31 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
     if (lane == 0 && !mbar_wait(done, 0u)) atomicOr(&g_err_prefill, kErrPfDone);
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, kPfTmemCols);
+    tmem_dealloc(tmem, PfCfg<kAcc>::kTmemCols);
   }
 }
 
 // ------------------------------------------------------------ host side
+// Token tiles of 256; the workspace always has room for an even count (the
+// two-accumulator kernel reads tiles in pairs, the last one zero when odd).
+static int64_t token_tiles(int64_t n_tokens) { return (n_tokens + kPfN - 1) / kPfN; }
+
 size_t prefill_workspace_bytes(int64_t hidden, int64_t n_tokens) {
-  const int64_t tiles = (n_tokens + kPfN - 1) / kPfN;
-  return static_cast<size_t>(tiles) * kPfN * static_cast<size_t>(hidden) * 2;
+  const int64_t t = token_tiles(n_tokens);
+  const int64_t padded = t >= 2 ? (t + 1) / 2 * 2 : t;
+  return static_cast<size_t>(padded) * kPfN * static_cast<size_t>(hidden) * 2;
+}
+
+// One or two accumulators per CTA: two halve the weight decoding per token
+// but give a CTA about 1.72x the work of a one-accumulator CTA (measured on
+// GB300 at 10240 x 2560: two stages instead of three), so they pay when they
+// save a wave: compare waves x relative CTA time.
+static int prefill_acc(int64_t rows, int64_t n_tokens, int sms) {
+  const int64_t mt = (rows + kPfM - 1) / kPfM, t1 = token_tiles(n_tokens);
+  if (t1 < 2) return 1;
+  const int64_t r1 = (mt * t1 + sms - 1) / sms;
+  const int64_t r2 = (mt * ((t1 + 1) / 2) + sms - 1) / sms;
+  return r2 * 172 < r1 * 100 ? 2 : 1;
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
@@ -512,24 +550,32 @@ static cudaError_t launch_pdl_pf(void (*kernel)(KArgs...), int grid, int threads
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+template <int kAcc>
+static cudaError_t launch_prefill_kernel(const PrefillParams& p, int grid, cudaStream_t st) {
+  static bool attr_set[64] = {false};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(prefill_q4k_kernel<kAcc>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(PfCfg<kAcc>::kSmem));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  return launch_pdl_pf(prefill_q4k_kernel<kAcc>, grid, kPfThreads, PfCfg<kAcc>::kSmem, st, p);
+}
+
 cudaError_t launch_prefill_q4k(const uint8_t* W, const float* X, float* Y, int64_t rows,
                                int64_t K, int64_t N, uint8_t* ws, cudaStream_t st) {
-  const int n_tiles_n = static_cast<int>((N + kPfN - 1) / kPfN);
+  const int acc = prefill_acc(rows, N, device_sms());
+  const int64_t t1 = token_tiles(N);
+  const int n_tiles_n = static_cast<int>(acc == 2 ? (t1 + 1) / 2 * 2 : t1);
   const int n_tiles_m = static_cast<int>((rows + kPfM - 1) / kPfM);
   const int64_t pack_total = static_cast<int64_t>(n_tiles_n) * kPfN * (K / 8);
   const int64_t pack_blocks = std::min<int64_t>((pack_total + 255) / 256, 8 * device_sms());
   cudaError_t e = launch_pdl_pf(prefill_pack_x_kernel, static_cast<int>(pack_blocks), 256, 0, st,
                                 X, ws, N, K, n_tiles_n);
   if (e != cudaSuccess) return e;
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    e = cudaFuncSetAttribute(prefill_q4k_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kPfSmemBytes));
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
   PrefillParams p;
   if (!encode_w_map(&p.wmap, W, rows, K)) return cudaErrorInvalidValue;
   p.W = W;
@@ -540,8 +586,8 @@ cudaError_t launch_prefill_q4k(const uint8_t* W, const float* X, float* Y, int64
   p.N = N;
   p.KC = static_cast<int>(K / kPfK);
   p.n_tiles_n = n_tiles_n;
-  return launch_pdl_pf(prefill_q4k_kernel, n_tiles_m * n_tiles_n, kPfThreads, kPfSmemBytes, st,
-                       p);
+  const int grid = n_tiles_m * (n_tiles_n / acc);
+  return acc == 2 ? launch_prefill_kernel<2>(p, grid, st) : launch_prefill_kernel<1>(p, grid, st);
 }
 
 unsigned read_clear_prefill_errors() {

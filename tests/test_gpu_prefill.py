@@ -85,6 +85,18 @@ def test_prefill_gemma_gate_shape_sampled_rows():
     check_prefill(W, X, rows, K, N, rows_sel=sel)
 
 
+def test_prefill_two_accumulators_odd_token_tiles():
+    # 76 row tiles x 3 token tiles: on 152 SMs the two-accumulator kernel
+    # (two token tiles per CTA) saves a wave, and its second pair is half
+    # padding (a zero token tile)
+    rows, K, N = 76 * 128, 1024, 600
+    g = synth.rng(W_PF, 5)
+    W = synth.q4_k_matrix(g, rows, K)
+    X = synth.normal_vector(g, K, N)
+    sel = np.concatenate([np.arange(0, 140), np.arange(4800, 4900), np.arange(rows - 140, rows)])
+    check_prefill(W, X, rows, K, N, rows_sel=sel)
+
+
 def test_prefill_matches_matvec_per_token_within_f16_rounding():
     # every token of the prefill equals the batch-1 matvec of that token up to
     # the f16 operand rounding (a property at any size)
