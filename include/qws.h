@@ -157,6 +157,18 @@ qws_status qws_q4k_qkv_proj(const void* Wq, const void* Wk, const void* Wv, cons
  *   three matrices in wfmt, streamed in one launch.
  * ---------------------------------------------------------------------- */
 qws_status qws_quantize_q8_0(const float* x, void* xq, int64_t n, int batch, qws_stream stream);
+
+/* Fused norm + quantize (infer-compute README §Shaders "Fused ops":
+ * rms_norm_q8, residual_norm_q8): the rms_norm of qws_rms_norm (after h <- h + y
+ * for the residual form, as qws_residual_rms_norm) quantized to Q8_0 blocks
+ * as qws_quantize_q8_0 does, in one launch; the f32 normalized vector is not
+ * stored.  x / h, y [batch][n] f32 (device, 4-byte aligned; h updated in
+ * place), w [n] f32, xq [batch][n / 32 * 34] bytes (device, 2-byte aligned);
+ * n > 0, n % 32 == 0, 1 <= batch <= 65535, eps >= 0. */
+qws_status qws_rms_norm_q8(const float* x, const float* w, void* xq, int64_t n, float eps,
+                           int batch, qws_stream stream);
+qws_status qws_residual_rms_norm_q8(float* h, const float* y, const float* w, void* xq,
+                                    int64_t n, float eps, int batch, qws_stream stream);
 qws_status qws_q8_matvec(qws_format wfmt, const void* W, const void* xq, float* y, int64_t rows,
                          int64_t hidden, int batch, qws_stream stream);
 qws_status qws_q8_qkv_proj(qws_format wfmt, const void* Wq, const void* Wk, const void* Wv,

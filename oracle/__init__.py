@@ -228,6 +228,22 @@ def quantize_q8_0(x) -> np.ndarray:
     return out
 
 
+def rms_norm_q8(x, w, eps: float) -> np.ndarray:
+    """rms_norm_q8 ([compute] §Shaders "Fused ops"): the f64 rms_norm of each
+    row of x, rounded to f32 (the activation type), then quantize_q8_0."""
+    xs = _f64(x)
+    rows = xs.reshape(-1, xs.shape[-1])
+    y = np.stack([rms_norm(r, w, eps) for r in rows]).astype(np.float32)
+    return quantize_q8_0(y.reshape(xs.shape))
+
+
+def residual_rms_norm_q8(h, y, w, eps: float):
+    """residual_norm_q8: h + y (f64), then rms_norm_q8 of the sum.  Returns
+    (h + y, blocks)."""
+    hs = _f64(h) + _f64(y)
+    return hs, rms_norm_q8(hs, w, eps)
+
+
 def matvec_q8(wfmt: int, W, rows: int, hidden: int, xq, threads: int = 1,
               row_begin: int = 0, row_end: int | None = None):
     """Q4_0 / Q8_0 weights times Q8_0 activations ``xq`` ([hidden / 32 * 34]

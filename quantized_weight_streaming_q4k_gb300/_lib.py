@@ -58,6 +58,8 @@ SIGNATURES = {
     "qws_kv_append": (I, [F, F, F, F, I, I, I64, I64, P]),
     "qws_kv_attention": (I, [F, F, F, F, I, I, I, I64, I64, C.c_float, C.c_float, P, SZ, P]),
     "qws_q8_matvec": (I, [I, P, P, F, I64, I64, I, P]),
+    "qws_rms_norm_q8": (I, [F, F, P, I64, C.c_float, I, P]),
+    "qws_residual_rms_norm_q8": (I, [F, F, F, P, I64, C.c_float, I, P]),
     "qws_q8_qkv_proj": (I, [I, P, P, P, P, F, F, F, I64, I64, I64, P]),
     "qws_rms_norm": (I, [F, F, F, I64, C.c_float, I, P]),
     "qws_residual_add": (I, [F, F, I64, I, P]),

@@ -495,6 +495,35 @@ qws_status qws_residual_rms_norm(float* h, const float* y, const float* w, float
   return ok();
 }
 
+static qws_status run_norm_q8(const char* fn, float* h, const float* y, const float* w,
+                              void* xq, int64_t n, float eps, int batch, bool residual,
+                              qws_stream stream) {
+  QWS_CHECK_F(h);
+  if (residual) QWS_CHECK_F(y);
+  QWS_CHECK_F(w);
+  QWS_CHECK_PTR(xq);
+  if (!aligned(xq, 2)) return fail(QWS_ERR_ALIGN, "%s: xq is not 2-byte aligned", fn);
+  if (n <= 0 || n % 32)
+    return fail(QWS_ERR_SHAPE, "%s: n = %lld is not a positive multiple of 32", fn, (long long)n);
+  if (batch < 1 || batch > 65535) return fail(QWS_ERR_SHAPE, "%s: batch = %d", fn, batch);
+  if (!(eps >= 0.f)) return fail(QWS_ERR_SHAPE, "%s: eps must be >= 0", fn);
+  cudaError_t e = qws::launch_norm_q8(h, y, w, static_cast<uint8_t*>(xq), n, eps, batch,
+                                      residual, reinterpret_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, fn, "");
+  return ok();
+}
+
+qws_status qws_rms_norm_q8(const float* x, const float* w, void* xq, int64_t n, float eps,
+                           int batch, qws_stream stream) {
+  return run_norm_q8("qws_rms_norm_q8", const_cast<float*>(x), nullptr, w, xq, n, eps, batch,
+                     false, stream);
+}
+
+qws_status qws_residual_rms_norm_q8(float* h, const float* y, const float* w, void* xq,
+                                    int64_t n, float eps, int batch, qws_stream stream) {
+  return run_norm_q8("qws_residual_rms_norm_q8", h, y, w, xq, n, eps, batch, true, stream);
+}
+
 qws_status qws_decode_chain(const qws_layer* layers, int n_layers, float* h,
                             const qws_dims* dims, void* ws, size_t ws_bytes, qws_stream stream) {
   std::string err;

@@ -599,7 +599,7 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
     if ((r >> 63) == 0) return;
   }
   if (blockIdx.x == gridDim.x - 1) {
-    if (p.H > 8 * static_cast<int64_t>(C))
+    if constexpr (kWide)
       chain_final<16>(p, wsum, ctid, C);
     else
       chain_final<8>(p, wsum, ctid, C);

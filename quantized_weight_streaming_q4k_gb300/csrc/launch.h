@@ -101,6 +101,10 @@ cudaError_t launch_matvec(int fmt, int epi, const Seg* segs, int nseg, const uin
 // ([B][K / 32 * 34] bytes), no column split.
 cudaError_t launch_matvec_q8(int wfmt, const Seg* segs, int nseg, const uint8_t* xq, int64_t K,
                              int B, cudaStream_t st, std::string* why);
+// rms_norm (after h += y when residual) quantized to Q8_0 in one launch;
+// h is read only (const-cast) when !residual
+cudaError_t launch_norm_q8(float* h, const float* y, const float* w, uint8_t* xq, int64_t n,
+                           float eps, int batch, bool residual, cudaStream_t st);
 // x (nblocks * 32 floats) -> nblocks Q8_0 blocks
 cudaError_t launch_quantize_q8_0(const float* x, uint8_t* xq, int64_t nblocks, cudaStream_t st);
 // attention over a KV cache (attention.cu)

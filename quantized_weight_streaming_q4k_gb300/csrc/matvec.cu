@@ -171,6 +171,59 @@ __global__ void __launch_bounds__(1024) residual_rms_norm_kernel(float* __restri
   for (int64_t i = threadIdx.x; i < n; i += blockDim.x) xb[i] = hb[i] * inv * w[i];
 }
 
+// rms_norm_q8 / residual_norm_q8: the norm of rms_norm_kernel (or of
+// residual_rms_norm_kernel, with h <- h + y first) and, in the same launch,
+// its output quantized to Q8_0 blocks exactly as quantize_q8_0_kernel does,
+// one warp per block.  The normalized vector itself is not stored.
+template <bool kResidual>
+__global__ void __launch_bounds__(1024) norm_q8_kernel(float* __restrict__ h,
+                                                       const float* __restrict__ y,
+                                                       const float* __restrict__ w,
+                                                       uint8_t* __restrict__ xq, int64_t n,
+                                                       float eps) {
+  __shared__ float wsum[32];
+  __shared__ float inv_s;
+  pdl_launch_dependents();
+  pdl_wait();
+  float* hb = h + blockIdx.x * n;
+  const float* yb = kResidual ? y + blockIdx.x * n : nullptr;
+  float ss = 0.f;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) {
+    float r = hb[i];
+    if constexpr (kResidual) {
+      r = r + yb[i];
+      hb[i] = r;
+    }
+    ss = fmaf(r, r, ss);
+  }
+  ss = warp_sum(ss);
+  if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = ss;
+  __syncthreads();   // also makes the h written above visible to the block
+  if (threadIdx.x == 0) {
+    float t = 0.f;
+    for (int i = 0; i < static_cast<int>(blockDim.x >> 5); ++i) t += wsum[i];
+    inv_s = 1.0f / sqrtf(t / static_cast<float>(n) + eps);
+  }
+  __syncthreads();
+  const float inv = inv_s;
+  const int lane = threadIdx.x & 31;
+  const int64_t nblk = n / 32;
+  uint8_t* xqb = xq + blockIdx.x * (nblk * 34);
+  for (int64_t k = threadIdx.x >> 5; k < nblk; k += blockDim.x >> 5) {
+    const int64_t i = k * 32 + lane;
+    const float v = hb[i] * inv * w[i];
+    const float amax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(fabsf(v))));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = d != 0.0f ? __fdiv_rn(1.0f, d) : 0.0f;
+    const int q = static_cast<int>(roundf(__fmul_rn(v, id)));
+    const unsigned qb = static_cast<unsigned>(q) & 0xFFu;
+    const unsigned next = __shfl_down_sync(0xFFFFFFFFu, qb, 1);
+    unsigned short* blk = reinterpret_cast<unsigned short*>(xqb + k * 34);
+    if ((lane & 1) == 0) blk[1 + (lane >> 1)] = static_cast<unsigned short>(qb | (next << 8));
+    if (lane == 0) blk[0] = __half_as_ushort(__float2half_rn(d));
+  }
+}
+
 __global__ void residual_add_kernel(float* __restrict__ h, const float* __restrict__ y,
                                     int64_t n) {
   pdl_launch_dependents();
@@ -394,6 +447,13 @@ cudaError_t launch_residual_rms_norm(float* h, const float* y, const float* w, f
                                     int64_t n, float eps, int batch, cudaStream_t st) {
   const int threads = n >= 1024 ? 1024 : static_cast<int>((n + 31) / 32 * 32);
   return launch_pdl(residual_rms_norm_kernel, batch, threads, 0, st, h, y, w, x, n, eps);
+}
+
+cudaError_t launch_norm_q8(float* h, const float* y, const float* w, uint8_t* xq, int64_t n,
+                           float eps, int batch, bool residual, cudaStream_t st) {
+  const int threads = n >= 1024 ? 1024 : static_cast<int>((n + 31) / 32 * 32);
+  return residual ? launch_pdl(norm_q8_kernel<true>, batch, threads, 0, st, h, y, w, xq, n, eps)
+                  : launch_pdl(norm_q8_kernel<false>, batch, threads, 0, st, h, y, w, xq, n, eps);
 }
 
 cudaError_t launch_residual_add(float* h, const float* y, int64_t n, int batch,

@@ -19,7 +19,7 @@ from ._lib import (OP_DECODE_CHAIN, OP_FFN, OP_KV_ATTENTION, OP_MATVEC, OP_PREFI
 __all__ = [
     "Q4_0", "Q4_K", "Q6_K", "Q8_0", "QwsError", "q4k_matvec", "q6k_matvec", "q4_0_matvec",
     "matvec", "quantize_q8_0", "q8_matvec", "q8_qkv_proj", "q4k_prefill_matmul",
-    "rope_at_pos", "kv_append", "kv_attention",
+    "rope_at_pos", "kv_append", "kv_attention", "rms_norm_q8", "residual_rms_norm_q8",
     "q4k_qkv_proj", "q4k_ffn_gate_up_geglu", "q4k_ffn_gate_up_geglu_down", "rms_norm",
     "residual_add", "decode_chain", "workspace_bytes", "device_error", "Layer", "Dims",
     "stream_handle",
@@ -115,6 +115,32 @@ def quantize_q8_0(x, n: int, batch: int = 1, out=None, stream=None):
     check(lib().qws_quantize_q8_0(_dev(x, "x", torch.float32), _dev(out, "xq", torch.uint8), n,
                                   batch, stream_handle(stream)))
     return out
+
+
+def _xq_out(out, n: int, batch: int, like):
+    if out is not None:
+        return out
+    nbytes = n // 32 * 34
+    return torch.empty((batch, nbytes) if batch > 1 else (nbytes,), dtype=torch.uint8,
+                       device=like.device)
+
+
+def rms_norm_q8(x, w, eps: float, n: int, batch: int = 1, out=None, stream=None):
+    """Q8_0 blocks of rms_norm(x, w) ([batch, n] or [n] f32 -> uint8 [.., n / 32 * 34])."""
+    xq = _xq_out(out, n, batch, x)
+    check(lib().qws_rms_norm_q8(_dev(x, "x", torch.float32), _dev(w, "w", torch.float32),
+                                _dev(xq, "xq", torch.uint8), n, eps, batch,
+                                stream_handle(stream)))
+    return xq
+
+
+def residual_rms_norm_q8(h, y, w, eps: float, n: int, batch: int = 1, out=None, stream=None):
+    """h += y (in place), then the Q8_0 blocks of rms_norm(h, w)."""
+    xq = _xq_out(out, n, batch, h)
+    check(lib().qws_residual_rms_norm_q8(_dev(h, "h", torch.float32), _dev(y, "y", torch.float32),
+                                         _dev(w, "w", torch.float32), _dev(xq, "xq", torch.uint8),
+                                         n, eps, batch, stream_handle(stream)))
+    return xq
 
 
 def q8_matvec(wfmt: int, W, xq, rows: int, hidden: int, batch: int = 1, out=None, stream=None):

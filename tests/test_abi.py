@@ -152,6 +152,11 @@ def test_q8_path_checks(lib):
     assert lib.qws_q8_qkv_proj(Q40, A, A, None, A, A, A, A, 2560, 2048, 1024, None) == NULL
     assert lib.qws_q8_qkv_proj(Q4K, A, A, A, A, A, A, A, 2560, 2048, 1024, None) == FORMAT
     assert lib.qws_q8_qkv_proj(Q80, A, A, A, A, A, A, A, 2560, 0, 0, None) == OK
+    assert lib.qws_rms_norm_q8(A, A, None, 64, C.c_float(1e-6), 1, None) == NULL
+    assert lib.qws_rms_norm_q8(A, A, A, 48, C.c_float(1e-6), 1, None) == SHAPE
+    assert lib.qws_rms_norm_q8(A, A, A + 1, 64, C.c_float(1e-6), 1, None) == ALIGN
+    assert lib.qws_residual_rms_norm_q8(A, None, A, A, 64, C.c_float(1e-6), 1, None) == NULL
+    assert lib.qws_residual_rms_norm_q8(A, A, A, A, 64, C.c_float(-1.0), 1, None) == SHAPE
     # the f32-activation entry points do not take Q8_0 weights
     assert lib.qws_matvec(Q80, A, A, A, 10, 2560, 1, 1, None, 0, None) == FORMAT
 

@@ -9,6 +9,12 @@ ABI, against the oracle.
                          sum_k |dw dx| sum_j |qw qx| (the integer sums are
                          exact on both sides; only the f32 scaling and the
                          f32 accumulation over blocks round).
+  rms_norm_q8 /        : the GPU's f32 norm may differ from the oracle's in the
+  residual_norm_q8       last bit, so a binary16 scale may differ by one step
+                         and a code by one near a rounding half; every block
+                         must still quantize the oracle's norm to within
+                         0.57 steps (half a step plus the binary16 rounding of
+                         d times 127) and 99.9 % of the bytes must agree.
 """
 import os
 
@@ -186,3 +192,48 @@ def test_q8_lm_head_full_size(batch):
     assert np.array_equal(host(xq_d).reshape(batch, -1), xq)
     ref, bound = oracle.matvec_q8(oracle.Q4_0, W, V, H, xq, threads=THREADS)
     assert_bound(y, ref.reshape(batch, V), bound.reshape(batch, V), what=f"lm_head q8 b{batch}")
+
+
+# ------------------------------------------------------------------ fused norm + quantize
+def check_norm_q8(got, y_ref, want):
+    """got / want: Q8_0 blocks of the GPU and the oracle; y_ref: the oracle's
+    f64 normalised values.  The GPU's norm differs from the oracle's in the
+    last f32 bit, so a scale may differ by one binary16 step and a code by
+    one where x * id falls within rounding of a half; every block must still
+    be a valid quantization of y_ref and almost all bytes must agree."""
+    g2, w2 = got.reshape(-1, 34), want.reshape(-1, 34)
+    y = y_ref.reshape(-1, 32)
+    for blk_g, blk_w, yb in zip(g2, w2, y):
+        dg, dw = int(blk_g[0]) | int(blk_g[1]) << 8, int(blk_w[0]) | int(blk_w[1]) << 8
+        assert abs(dg - dw) <= 1
+        d = oracle.half(dg)
+        q = blk_g[2:].view(np.int8).astype(np.int64)
+        assert np.all(np.abs(yb - d * q) <= 0.57 * d + 1e-30)
+    assert np.mean(got == want) >= 0.999
+
+
+@pytest.mark.parametrize("n,batch", [(32, 1), (2560, 1), (2560, 3), (10240, 1)])
+def test_rms_norm_q8(n, batch):
+    g = synth.rng(W_Q8, 10, n, batch)
+    x = synth.normal_vector(g, n, batch if batch > 1 else None)
+    w = synth.norm_weights(g, n)
+    got = host(ops.rms_norm_q8(dev(x), dev(w), 1e-6, n, batch))
+    want = oracle.rms_norm_q8(x, w, 1e-6)
+    xs = np.asarray(x, dtype=np.float64).reshape(-1, n)
+    y_ref = np.stack([oracle.rms_norm(r, w, 1e-6) for r in xs])
+    check_norm_q8(got, y_ref, want)
+
+
+@pytest.mark.parametrize("n,batch", [(2560, 1), (512, 4)])
+def test_residual_rms_norm_q8(n, batch):
+    g = synth.rng(W_Q8, 11, n, batch)
+    h = synth.normal_vector(g, n, batch if batch > 1 else None)
+    y = synth.normal_vector(g, n, batch if batch > 1 else None)
+    w = synth.norm_weights(g, n)
+    hd = dev(h)
+    got = host(ops.residual_rms_norm_q8(hd, dev(y), dev(w), 1e-6, n, batch))
+    hs, want = oracle.residual_rms_norm_q8(h, y, w, 1e-6)
+    # the residual sum is one f32 rounding of the exact sum on both sides
+    assert np.array_equal(host(hd), hs.astype(np.float32))
+    y_ref = np.stack([oracle.rms_norm(r, w, 1e-6) for r in hs.astype(np.float32).astype(np.float64).reshape(-1, n)])
+    check_norm_q8(got, y_ref, oracle.rms_norm_q8(hs.astype(np.float32), w, 1e-6))

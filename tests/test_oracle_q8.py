@@ -224,3 +224,42 @@ def test_matvec_f32_path_accepts_q8_0_weights():
     y, _ = oracle.matvec(oracle.Q8_0, W, rows, hidden, x)
     ref = oracle.dequant(oracle.Q8_0, W, rows, hidden) @ x.astype(np.float64)
     assert np.allclose(y, ref, rtol=1e-13, atol=1e-13)
+
+
+# ---------------------------------------------------------------- fused norm + quantize
+def test_rms_norm_q8_constant_and_one_hot():
+    # a constant vector normalises to +-1 (to within eps): every code is +-127
+    x = np.full(64, -3.0, dtype=np.float32)
+    out = oracle.rms_norm_q8(x, np.ones(64), 1e-6).reshape(-1, 34)
+    assert np.all(_s8(out[:, 2:]) == -127)
+    # a one-hot vector: sqrt(n) * w_0 at index 0, zeros elsewhere
+    x = np.zeros(64, dtype=np.float32)
+    x[0] = 5.0
+    out = oracle.rms_norm_q8(x, np.ones(64), 0.0).reshape(-1, 34)
+    q = _s8(out[0, 2:])
+    assert q[0] == 127 and np.all(q[1:] == 0)
+    assert np.all(out[1] == 0)                      # second block all zero: d = 0, codes 0
+    assert oracle.half(_d_bits(out[0])) == pytest.approx(8.0 / 127, rel=2.0 ** -11)
+
+
+def test_rms_norm_q8_reconstructs_the_norm():
+    g = np.random.default_rng(21)
+    x = g.standard_normal((2, 256)).astype(np.float32)
+    w = g.normal(1.0, 0.1, 256)
+    out = oracle.rms_norm_q8(x, w, 1e-6).reshape(2, -1, 34)
+    for b in range(2):
+        y = oracle.rms_norm(x[b], w, 1e-6)
+        for k in range(8):
+            d = oracle.half(_d_bits(out[b, k]))
+            rec = d * _s8(out[b, k, 2:])
+            assert np.all(np.abs(rec - y[32 * k:32 * k + 32]) <= d * 0.57)
+
+
+def test_residual_rms_norm_q8_adds_then_normalises():
+    g = np.random.default_rng(22)
+    h = g.standard_normal(128).astype(np.float32)
+    y = g.standard_normal(128).astype(np.float32)
+    w = g.normal(1.0, 0.1, 128)
+    hs, out = oracle.residual_rms_norm_q8(h, y, w, 1e-6)
+    assert np.array_equal(hs, h.astype(np.float64) + y.astype(np.float64))
+    assert np.array_equal(out, oracle.rms_norm_q8(hs, w, 1e-6))
