@@ -116,6 +116,13 @@ qws_status run_matvec(const char* fn, int fmt, const void* W, const float* x, fl
     if (!aligned(ws, 16)) return fail(QWS_ERR_ALIGN, "%s: ws is not 16-byte aligned", fn);
   }
   if (rows == 0) return ok();
+  if (fmt == QWS_Q4_0 && S == 1 && qws::batch_q40_eligible(hidden, batch)) {
+    // 2..8 vectors: every weight decoded once for all of them
+    const cudaError_t e = qws::launch_batch_q40_matvec(static_cast<const uint8_t*>(W), x, y,
+                                                       rows, hidden, batch, st);
+    if (e != cudaSuccess) return cuda_fail(e, fn, "");
+    return ok();
+  }
   std::string why;
   qws::Seg seg{static_cast<const uint8_t*>(W), S > 1 ? static_cast<float*>(ws) : y, rows, 0};
   cudaError_t e = qws::launch_matvec(fmt, qws::EPI_STORE, &seg, 1, nullptr, x, hidden, batch, S,
@@ -564,7 +571,8 @@ qws_status qws_device_error(unsigned* code) {
   cudaError_t e = cudaDeviceSynchronize();
   if (e != cudaSuccess) return cuda_fail(e, "qws_device_error", "");
   *code = qws::read_clear_matvec_errors() | qws::read_clear_chain_errors() |
-          qws::read_clear_prefill_errors() | qws::read_clear_attention_errors();
+          qws::read_clear_prefill_errors() | qws::read_clear_attention_errors() |
+          qws::read_clear_batchmv_errors();
   return *code ? fail(QWS_ERR_TIMEOUT, "device error code 0x%x", *code) : ok();
 }
 
