@@ -116,10 +116,10 @@ qws_status run_matvec(const char* fn, int fmt, const void* W, const float* x, fl
     if (!aligned(ws, 16)) return fail(QWS_ERR_ALIGN, "%s: ws is not 16-byte aligned", fn);
   }
   if (rows == 0) return ok();
-  if (fmt == QWS_Q4_0 && S == 1 && qws::batch_q40_eligible(hidden, batch)) {
+  if (S == 1 && qws::batch_q4_eligible(fmt, hidden, batch)) {
     // 2..8 vectors: every weight decoded once for all of them
-    const cudaError_t e = qws::launch_batch_q40_matvec(static_cast<const uint8_t*>(W), x, y,
-                                                       rows, hidden, batch, st);
+    const cudaError_t e = qws::launch_batch_q4_matvec(fmt, static_cast<const uint8_t*>(W), x, y,
+                                                      rows, hidden, batch, st);
     if (e != cudaSuccess) return cuda_fail(e, fn, "");
     return ok();
   }

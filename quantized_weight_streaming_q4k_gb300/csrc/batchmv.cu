@@ -1,5 +1,5 @@
-// batchmv.cu -- Q4_0 matvec for 2..8 activation vectors that decodes every
-// weight once for all vectors (the 262144-row lm_head at batch 8).
+// batchmv.cu -- Q4_0 / Q4_K matvec for 2..8 activation vectors that decodes
+// every weight once for all vectors (the 262144-row lm_head at batch 8).
 //
 // The lane-unit engine decodes a weight once per vector (each lane holds one
 // vector's activations), which at batch 8 makes the stream ALU-bound.  Here a
@@ -18,6 +18,9 @@
 //     over 32 columns), is multiplied by the block's scale d per row and
 //     added to an f32 running sum in registers; the sums are scaled back by
 //     2^-s at the end.
+//   * Q4_K: the same per 32-column sub-block with A = the codes q (0..15),
+//     scale a = d * sc and the min term b = dmin * m times the sub-block's
+//     sum of x' (summed once per launch): acc += a C - b S.
 //
 // CTA: one copy warp streams 16-row tiles (1-D TMA bulk copies) into a
 // shared-memory ring; 8 consumer warps each take one eighth of the blocks of
@@ -43,13 +46,13 @@ constexpr int kBmStages = 4;
 constexpr int64_t kBmMaxK = 3072;
 
 struct BmParams {
-  const uint8_t* W;     // Q4_0, rows x K
+  const uint8_t* W;     // Q4_0 or Q4_K, rows x K
   const float* x;       // [B][K]
   float* y;             // [B][rows]
   int64_t rows, K;
   int B;
   int n_tiles;          // ceil(rows / 16)
-  uint32_t row_bytes;   // K / 32 * 18
+  uint32_t row_bytes;   // K / 32 * 18 = K / 256 * 144
   uint32_t xs_stride;   // f16 elements per staged activation row: K + 8
 };
 
@@ -62,7 +65,9 @@ __host__ __device__ constexpr size_t bm_stage_bytes(int64_t K) {
 __host__ __device__ constexpr size_t bm_smem_bytes(int64_t K) {
   return bm_xs_bytes(K) + kBmStages * bm_stage_bytes(K) +
          2 * kBmWarps * kBmRows * kBmMaxB * sizeof(float) +   // slice sums, two buffers
-         kBmMaxB * sizeof(float) + 2 * kBmStages * sizeof(uint64_t) + 64;
+         kBmMaxB * sizeof(float) +                              // 2^-s per vector
+         static_cast<size_t>(kBmMaxB) * (K / 32) * sizeof(float) +   // Q4_K: sub-block sums of x'
+         2 * kBmStages * sizeof(uint64_t) + 64;
 }
 
 __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -88,12 +93,112 @@ __device__ __forceinline__ uint32_t codes_lo(uint32_t u) {
 __device__ __forceinline__ uint32_t codes_hi(uint32_t u) {
   return f16x2_sub(((u >> 4) & 0x000Fu) | ((u & 0xF000u) << 4) | 0x64006400u, 0x64086408u);
 }
+// Q4_K codes q (no offset): the low or the high nibble pair as f16x2 of q
+__device__ __forceinline__ uint32_t kcodes(uint32_t u, bool high) {
+  const uint32_t v = high ? (((u >> 4) & 0x000Fu) | ((u & 0xF000u) << 4))
+                          : ((u & 0x000Fu) | ((u & 0x0F00u) << 8));
+  return f16x2_sub(v | 0x64006400u, 0x64006400u);
+}
 
 __device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) {
   return *reinterpret_cast<const unsigned short*>(p);
 }
 
-__global__ void __launch_bounds__(kBmThreads, 1) batch_q40_matvec_kernel(
+// 6-bit scale and min of sub-block j (0..7) from the 12 packed bytes at sc
+// (the GGUF packing), times d and dmin
+__device__ __forceinline__ void q4k_ab(const uint8_t* h, int j, float& a, float& b) {
+  const uint32_t dd = *reinterpret_cast<const uint32_t*>(h);
+  const uint8_t* sc = h + 4;
+  uint32_t scv, mv;
+  if (j < 4) {
+    scv = sc[j] & 63u;
+    mv = sc[j + 4] & 63u;
+  } else {
+    scv = (sc[j + 4] & 0xFu) | ((sc[j - 4] >> 6) << 4);
+    mv = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
+  }
+  a = half_bits_to_float(dd) * static_cast<float>(scv);
+  b = half_bits_to_float(dd >> 16) * static_cast<float>(mv);
+}
+
+// acc (rows g, g + 8 x vectors 2tq, 2tq + 1) += a C - b S of Q4_K sub-block bi
+__device__ __forceinline__ void q4k_sub(const uint8_t* rg, const uint8_t* rg8, int bi, int tq,
+                                        const uint32_t* xh, const uint32_t* xl,
+                                        const float* ssum, int64_t K, float (&acc)[4]) {
+  const int kb = bi >> 3, j = bi & 7, c = j >> 1;
+  const bool high = (j & 1) != 0;
+  const uint8_t* ha = rg + kb * 144;
+  const uint8_t* hb = rg8 + kb * 144;
+  const uint8_t* qa = ha + 16 + 32 * c + 2 * tq;
+  const uint8_t* qb = hb + 16 + 32 * c + 2 * tq;
+  const uint32_t alo[4] = {kcodes(ld_u16(qa), high), kcodes(ld_u16(qb), high),
+                           kcodes(ld_u16(qa + 8), high), kcodes(ld_u16(qb + 8), high)};
+  const uint32_t ahi[4] = {kcodes(ld_u16(qa + 16), high), kcodes(ld_u16(qb + 16), high),
+                           kcodes(ld_u16(qa + 24), high), kcodes(ld_u16(qb + 24), high)};
+  const int w0 = bi * 16 + tq;
+  float cc[4] = {0.f, 0.f, 0.f, 0.f};
+  mma_16816(cc, alo, xh[w0], xh[w0 + 4]);
+  mma_16816(cc, alo, xl[w0], xl[w0 + 4]);
+  mma_16816(cc, ahi, xh[w0 + 8], xh[w0 + 12]);
+  mma_16816(cc, ahi, xl[w0 + 8], xl[w0 + 12]);
+  float a0, b0, a1, b1;
+  q4k_ab(ha, j, a0, b0);
+  q4k_ab(hb, j, a1, b1);
+  const float s0 = ssum[(2 * tq) * (K / 32) + bi], s1 = ssum[(2 * tq + 1) * (K / 32) + bi];
+  acc[0] = fmaf(a0, cc[0], fmaf(-b0, s0, acc[0]));
+  acc[1] = fmaf(a0, cc[1], fmaf(-b0, s1, acc[1]));
+  acc[2] = fmaf(a1, cc[2], fmaf(-b1, s0, acc[2]));
+  acc[3] = fmaf(a1, cc[3], fmaf(-b1, s1, acc[3]));
+}
+
+// the aligned pair bi (even), bi + 1: one load of the shared code bytes
+__device__ __forceinline__ void q4k_pair(const uint8_t* rg, const uint8_t* rg8, int bi, int tq,
+                                         const uint32_t* xh, const uint32_t* xl,
+                                         const float* ssum, int64_t K, float (&acc)[4]) {
+  const int kb = bi >> 3, j = bi & 7, c = j >> 1;
+  const uint8_t* ha = rg + kb * 144;
+  const uint8_t* hb = rg8 + kb * 144;
+  const uint8_t* qa = ha + 16 + 32 * c + 2 * tq;
+  const uint8_t* qb = hb + 16 + 32 * c + 2 * tq;
+  const uint32_t u0 = ld_u16(qa), u1 = ld_u16(qb), u2 = ld_u16(qa + 8), u3 = ld_u16(qb + 8);
+  const uint32_t u4 = ld_u16(qa + 16), u5 = ld_u16(qb + 16), u6 = ld_u16(qa + 24),
+                 u7 = ld_u16(qb + 24);
+  const uint32_t l0[4] = {kcodes(u0, false), kcodes(u1, false), kcodes(u2, false),
+                          kcodes(u3, false)};
+  const uint32_t l1[4] = {kcodes(u4, false), kcodes(u5, false), kcodes(u6, false),
+                          kcodes(u7, false)};
+  const uint32_t h0[4] = {kcodes(u0, true), kcodes(u1, true), kcodes(u2, true), kcodes(u3, true)};
+  const uint32_t h1[4] = {kcodes(u4, true), kcodes(u5, true), kcodes(u6, true), kcodes(u7, true)};
+  const int w0 = bi * 16 + tq, w1 = w0 + 16;
+  float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+  mma_16816(c0, l0, xh[w0], xh[w0 + 4]);
+  mma_16816(c1, h0, xh[w1], xh[w1 + 4]);
+  mma_16816(c0, l0, xl[w0], xl[w0 + 4]);
+  mma_16816(c1, h0, xl[w1], xl[w1 + 4]);
+  mma_16816(c0, l1, xh[w0 + 8], xh[w0 + 12]);
+  mma_16816(c1, h1, xh[w1 + 8], xh[w1 + 12]);
+  mma_16816(c0, l1, xl[w0 + 8], xl[w0 + 12]);
+  mma_16816(c1, h1, xl[w1 + 8], xl[w1 + 12]);
+  float a0, b0, a1, b1, a2, b2, a3, b3;
+  q4k_ab(ha, j, a0, b0);
+  q4k_ab(hb, j, a1, b1);
+  q4k_ab(ha, j + 1, a2, b2);
+  q4k_ab(hb, j + 1, a3, b3);
+  const int nb = static_cast<int>(K / 32);
+  const float s0 = ssum[(2 * tq) * nb + bi], s1 = ssum[(2 * tq + 1) * nb + bi];
+  const float t0 = ssum[(2 * tq) * nb + bi + 1], t1 = ssum[(2 * tq + 1) * nb + bi + 1];
+  acc[0] = fmaf(a0, c0[0], fmaf(-b0, s0, acc[0]));
+  acc[1] = fmaf(a0, c0[1], fmaf(-b0, s1, acc[1]));
+  acc[2] = fmaf(a1, c0[2], fmaf(-b1, s0, acc[2]));
+  acc[3] = fmaf(a1, c0[3], fmaf(-b1, s1, acc[3]));
+  acc[0] = fmaf(a2, c1[0], fmaf(-b2, t0, acc[0]));
+  acc[1] = fmaf(a2, c1[1], fmaf(-b2, t1, acc[1]));
+  acc[2] = fmaf(a3, c1[2], fmaf(-b3, t0, acc[2]));
+  acc[3] = fmaf(a3, c1[3], fmaf(-b3, t1, acc[3]));
+}
+
+template <int kFmt>   // 2: Q4_0, 12: Q4_K
+__global__ void __launch_bounds__(kBmThreads, 1) batch_q4_matvec_kernel(
     const __grid_constant__ BmParams p) {
   extern __shared__ __align__(128) uint8_t bm_smem[];
   const int64_t K = p.K;
@@ -103,7 +208,8 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q40_matvec_kernel(
   const size_t stage_bytes = bm_stage_bytes(K);
   float* red = reinterpret_cast<float*>(ring + kBmStages * stage_bytes);   // [2][8][128]
   float* unscale = red + 2 * kBmWarps * kBmRows * kBmMaxB;                  // [8]
-  uint64_t* full = reinterpret_cast<uint64_t*>(unscale + kBmMaxB);
+  float* ssum = unscale + kBmMaxB;                                          // [8][K / 32]
+  uint64_t* full = reinterpret_cast<uint64_t*>(ssum + kBmMaxB * (K / 32));
   uint64_t* empty = full + kBmStages;
 
   const int warp = static_cast<int>(threadIdx.x >> 5) - 1;   // -1: the copy warp
@@ -169,6 +275,15 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q40_matvec_kernel(
       xs_hi[n * p.xs_stride + i] = hi;
       xs_lo[n * p.xs_stride + i] = lo;
     }
+    if constexpr (kFmt == 12) {
+      // sum of x' over each 32-column sub-block, in column order
+      for (int64_t bk = lane; bk < K / 32; bk += 32) {
+        float t = 0.f;
+        if (n < p.B)
+          for (int i = 0; i < 32; ++i) t += p.x[n * K + bk * 32 + i] * sc;
+        ssum[n * (K / 32) + bk] = t;
+      }
+    }
   }
   bar_sync(1, kBmWarps * 32);
 
@@ -192,64 +307,77 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q40_matvec_kernel(
     const uint8_t* rg = st + g * p.row_bytes;          // row g of the tile
     const uint8_t* rg8 = st + (g + 8) * p.row_bytes;   // row g + 8
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    // two blocks at a time: two independent MMA chains interleave (an odd
-    // slice ends with one block alone)
-    int bi = b0;
-    for (; landed && bi + 1 < b0 + per; bi += 2) {
-      float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint8_t* pa0 = rg + bi * 18;
-      const uint8_t* pb0 = rg8 + bi * 18;
-      const uint8_t* pa1 = pa0 + 18;
-      const uint8_t* pb1 = pb0 + 18;
-      // bytes 2tq, 2tq+1 and 2tq+8, 2tq+9 of each row's 16 code bytes;
-      // columns 0..15 of a block are the low nibbles, 16..31 the high ones
-      const uint32_t u0 = ld_u16(pa0 + 2 + 2 * tq), u1 = ld_u16(pb0 + 2 + 2 * tq);
-      const uint32_t u2 = ld_u16(pa0 + 10 + 2 * tq), u3 = ld_u16(pb0 + 10 + 2 * tq);
-      const uint32_t v0 = ld_u16(pa1 + 2 + 2 * tq), v1 = ld_u16(pb1 + 2 + 2 * tq);
-      const uint32_t v2 = ld_u16(pa1 + 10 + 2 * tq), v3 = ld_u16(pb1 + 10 + 2 * tq);
-      const uint32_t alo0[4] = {codes_lo(u0), codes_lo(u1), codes_lo(u2), codes_lo(u3)};
-      const uint32_t ahi0[4] = {codes_hi(u0), codes_hi(u1), codes_hi(u2), codes_hi(u3)};
-      const uint32_t alo1[4] = {codes_lo(v0), codes_lo(v1), codes_lo(v2), codes_lo(v3)};
-      const uint32_t ahi1[4] = {codes_hi(v0), codes_hi(v1), codes_hi(v2), codes_hi(v3)};
-      const int w0 = bi * 16 + tq;                      // f16x2 word of column 32 bi + 2 tq
-      const int w1 = w0 + 16;                           // block bi + 1
-      mma_16816(c0, alo0, xh[w0], xh[w0 + 4]);
-      mma_16816(c1, alo1, xh[w1], xh[w1 + 4]);
-      mma_16816(c0, alo0, xl[w0], xl[w0 + 4]);
-      mma_16816(c1, alo1, xl[w1], xl[w1 + 4]);
-      mma_16816(c0, ahi0, xh[w0 + 8], xh[w0 + 12]);
-      mma_16816(c1, ahi1, xh[w1 + 8], xh[w1 + 12]);
-      mma_16816(c0, ahi0, xl[w0 + 8], xl[w0 + 12]);
-      mma_16816(c1, ahi1, xl[w1 + 8], xl[w1 + 12]);
-      const float da0 = half_bits_to_float(ld_u16(pa0)), db0 = half_bits_to_float(ld_u16(pb0));
-      const float da1 = half_bits_to_float(ld_u16(pa1)), db1 = half_bits_to_float(ld_u16(pb1));
-      acc[0] = fmaf(da0, c0[0], acc[0]);
-      acc[1] = fmaf(da0, c0[1], acc[1]);
-      acc[2] = fmaf(db0, c0[2], acc[2]);
-      acc[3] = fmaf(db0, c0[3], acc[3]);
-      acc[0] = fmaf(da1, c1[0], acc[0]);
-      acc[1] = fmaf(da1, c1[1], acc[1]);
-      acc[2] = fmaf(db1, c1[2], acc[2]);
-      acc[3] = fmaf(db1, c1[3], acc[3]);
-    }
-    if (landed && bi < b0 + per) {
-      float c0[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint8_t* pa0 = rg + bi * 18;
-      const uint8_t* pb0 = rg8 + bi * 18;
-      const uint32_t u0 = ld_u16(pa0 + 2 + 2 * tq), u1 = ld_u16(pb0 + 2 + 2 * tq);
-      const uint32_t u2 = ld_u16(pa0 + 10 + 2 * tq), u3 = ld_u16(pb0 + 10 + 2 * tq);
-      const uint32_t alo0[4] = {codes_lo(u0), codes_lo(u1), codes_lo(u2), codes_lo(u3)};
-      const uint32_t ahi0[4] = {codes_hi(u0), codes_hi(u1), codes_hi(u2), codes_hi(u3)};
-      const int w0 = bi * 16 + tq;
-      mma_16816(c0, alo0, xh[w0], xh[w0 + 4]);
-      mma_16816(c0, alo0, xl[w0], xl[w0 + 4]);
-      mma_16816(c0, ahi0, xh[w0 + 8], xh[w0 + 12]);
-      mma_16816(c0, ahi0, xl[w0 + 8], xl[w0 + 12]);
-      const float da0 = half_bits_to_float(ld_u16(pa0)), db0 = half_bits_to_float(ld_u16(pb0));
-      acc[0] = fmaf(da0, c0[0], acc[0]);
-      acc[1] = fmaf(da0, c0[1], acc[1]);
-      acc[2] = fmaf(db0, c0[2], acc[2]);
-      acc[3] = fmaf(db0, c0[3], acc[3]);
+    if constexpr (kFmt == 2) {
+      // two blocks at a time: two independent MMA chains interleave (an odd
+      // slice ends with one block alone)
+      int bi = b0;
+      for (; landed && bi + 1 < b0 + per; bi += 2) {
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint8_t* pa0 = rg + bi * 18;
+        const uint8_t* pb0 = rg8 + bi * 18;
+        const uint8_t* pa1 = pa0 + 18;
+        const uint8_t* pb1 = pb0 + 18;
+        // bytes 2tq, 2tq+1 and 2tq+8, 2tq+9 of each row's 16 code bytes;
+        // columns 0..15 of a block are the low nibbles, 16..31 the high ones
+        const uint32_t u0 = ld_u16(pa0 + 2 + 2 * tq), u1 = ld_u16(pb0 + 2 + 2 * tq);
+        const uint32_t u2 = ld_u16(pa0 + 10 + 2 * tq), u3 = ld_u16(pb0 + 10 + 2 * tq);
+        const uint32_t v0 = ld_u16(pa1 + 2 + 2 * tq), v1 = ld_u16(pb1 + 2 + 2 * tq);
+        const uint32_t v2 = ld_u16(pa1 + 10 + 2 * tq), v3 = ld_u16(pb1 + 10 + 2 * tq);
+        const uint32_t alo0[4] = {codes_lo(u0), codes_lo(u1), codes_lo(u2), codes_lo(u3)};
+        const uint32_t ahi0[4] = {codes_hi(u0), codes_hi(u1), codes_hi(u2), codes_hi(u3)};
+        const uint32_t alo1[4] = {codes_lo(v0), codes_lo(v1), codes_lo(v2), codes_lo(v3)};
+        const uint32_t ahi1[4] = {codes_hi(v0), codes_hi(v1), codes_hi(v2), codes_hi(v3)};
+        const int w0 = bi * 16 + tq;                      // f16x2 word of column 32 bi + 2 tq
+        const int w1 = w0 + 16;                           // block bi + 1
+        mma_16816(c0, alo0, xh[w0], xh[w0 + 4]);
+        mma_16816(c1, alo1, xh[w1], xh[w1 + 4]);
+        mma_16816(c0, alo0, xl[w0], xl[w0 + 4]);
+        mma_16816(c1, alo1, xl[w1], xl[w1 + 4]);
+        mma_16816(c0, ahi0, xh[w0 + 8], xh[w0 + 12]);
+        mma_16816(c1, ahi1, xh[w1 + 8], xh[w1 + 12]);
+        mma_16816(c0, ahi0, xl[w0 + 8], xl[w0 + 12]);
+        mma_16816(c1, ahi1, xl[w1 + 8], xl[w1 + 12]);
+        const float da0 = half_bits_to_float(ld_u16(pa0)), db0 = half_bits_to_float(ld_u16(pb0));
+        const float da1 = half_bits_to_float(ld_u16(pa1)), db1 = half_bits_to_float(ld_u16(pb1));
+        acc[0] = fmaf(da0, c0[0], acc[0]);
+        acc[1] = fmaf(da0, c0[1], acc[1]);
+        acc[2] = fmaf(db0, c0[2], acc[2]);
+        acc[3] = fmaf(db0, c0[3], acc[3]);
+        acc[0] = fmaf(da1, c1[0], acc[0]);
+        acc[1] = fmaf(da1, c1[1], acc[1]);
+        acc[2] = fmaf(db1, c1[2], acc[2]);
+        acc[3] = fmaf(db1, c1[3], acc[3]);
+      }
+      if (landed && bi < b0 + per) {
+        float c0[4] = {0.f, 0.f, 0.f, 0.f};
+        const uint8_t* pa0 = rg + bi * 18;
+        const uint8_t* pb0 = rg8 + bi * 18;
+        const uint32_t u0 = ld_u16(pa0 + 2 + 2 * tq), u1 = ld_u16(pb0 + 2 + 2 * tq);
+        const uint32_t u2 = ld_u16(pa0 + 10 + 2 * tq), u3 = ld_u16(pb0 + 10 + 2 * tq);
+        const uint32_t alo0[4] = {codes_lo(u0), codes_lo(u1), codes_lo(u2), codes_lo(u3)};
+        const uint32_t ahi0[4] = {codes_hi(u0), codes_hi(u1), codes_hi(u2), codes_hi(u3)};
+        const int w0 = bi * 16 + tq;
+        mma_16816(c0, alo0, xh[w0], xh[w0 + 4]);
+        mma_16816(c0, alo0, xl[w0], xl[w0 + 4]);
+        mma_16816(c0, ahi0, xh[w0 + 8], xh[w0 + 12]);
+        mma_16816(c0, ahi0, xl[w0 + 8], xl[w0 + 12]);
+        const float da0 = half_bits_to_float(ld_u16(pa0)), db0 = half_bits_to_float(ld_u16(pb0));
+        acc[0] = fmaf(da0, c0[0], acc[0]);
+        acc[1] = fmaf(da0, c0[1], acc[1]);
+        acc[2] = fmaf(db0, c0[2], acc[2]);
+        acc[3] = fmaf(db0, c0[3], acc[3]);
+      }
+    } else {
+      int bi = b0;
+      // a sub-block on its own when the slice starts on an odd one
+      if (landed && per > 0 && (bi & 1)) {
+        q4k_sub(rg, rg8, bi, tq, xh, xl, ssum, K, acc);
+        ++bi;
+      }
+      // aligned pairs (2c, 2c + 1): the same 32 code bytes, low nibbles for
+      // the first, high for the second; two independent MMA chains
+      for (; landed && bi + 1 < b0 + per; bi += 2) q4k_pair(rg, rg8, bi, tq, xh, xl, ssum, K, acc);
+      if (landed && bi < b0 + per) q4k_sub(rg, rg8, bi, tq, xh, xl, ssum, K, acc);
     }
     // slice sums: [row][vector] of this warp, buffer k & 1
     float* rw = red + (static_cast<size_t>(k & 1) * kBmWarps + warp) * (kBmRows * kBmMaxB);
@@ -274,12 +402,28 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q40_matvec_kernel(
 }
 
 // ------------------------------------------------------------------ host side
-bool batch_q40_eligible(int64_t K, int B) {
-  return B >= 2 && B <= kBmMaxB && K >= 256 && K % 256 == 0 && K <= kBmMaxK;
+bool batch_q4_eligible(int fmt, int64_t K, int B) {
+  return (fmt == 2 || fmt == 12) && B >= 2 && B <= kBmMaxB && K >= 256 && K % 256 == 0 &&
+         K <= kBmMaxK;
 }
 
-cudaError_t launch_batch_q40_matvec(const uint8_t* W, const float* x, float* y, int64_t rows,
-                                    int64_t K, int B, cudaStream_t st) {
+template <int kFmt>
+static cudaError_t set_smem_attr() {
+  static size_t attr_smem[64] = {0};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev >= 0 && dev < 64 && attr_smem[dev] == 0) {
+    const cudaError_t e = cudaFuncSetAttribute(batch_q4_matvec_kernel<kFmt>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               static_cast<int>(bm_smem_bytes(kBmMaxK)));
+    if (e != cudaSuccess) return e;
+    attr_smem[dev] = bm_smem_bytes(kBmMaxK);
+  }
+  return cudaSuccess;
+}
+
+cudaError_t launch_batch_q4_matvec(int fmt, const uint8_t* W, const float* x, float* y,
+                                   int64_t rows, int64_t K, int B, cudaStream_t st) {
   BmParams p;
   p.W = W;
   p.x = x;
@@ -291,16 +435,8 @@ cudaError_t launch_batch_q40_matvec(const uint8_t* W, const float* x, float* y, 
   p.row_bytes = static_cast<uint32_t>(K / 32 * 18);
   p.xs_stride = static_cast<uint32_t>(K + 8);
   const size_t smem = bm_smem_bytes(K);
-  static size_t attr_smem[64] = {0};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && attr_smem[dev] < smem) {
-    const cudaError_t e = cudaFuncSetAttribute(batch_q40_matvec_kernel,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(bm_smem_bytes(kBmMaxK)));
-    if (e != cudaSuccess) return e;
-    attr_smem[dev] = bm_smem_bytes(kBmMaxK);
-  }
+  const cudaError_t ea = fmt == 12 ? set_smem_attr<12>() : set_smem_attr<2>();
+  if (ea != cudaSuccess) return ea;
   const int grid = static_cast<int>(std::min<int64_t>(p.n_tiles, device_sms()));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -312,7 +448,8 @@ cudaError_t launch_batch_q40_matvec(const uint8_t* W, const float* x, float* y, 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, batch_q40_matvec_kernel, p);
+  return fmt == 12 ? cudaLaunchKernelEx(&cfg, batch_q4_matvec_kernel<12>, p)
+                   : cudaLaunchKernelEx(&cfg, batch_q4_matvec_kernel<2>, p);
 }
 
 unsigned read_clear_batchmv_errors() {

@@ -410,34 +410,36 @@ def test_lm_head_split_k_matches_single_pass():
     assert np.all(np.abs(y1 - y5) <= 2e-5 * bound)
 
 
-# Q4_0 at 2..8 vectors takes the decode-once kernel (mma.sync on the codes
-# and an f16 hi + lo split of x scaled by a power of two); the tolerance is
-# the matvec's 1e-5 * sum |w x|.
+# Q4_0 and Q4_K at 2..8 vectors take the decode-once kernel (mma.sync on the
+# codes and an f16 hi + lo split of x scaled by a power of two); the
+# tolerance is the matvec's 1e-5 * sum |w x|.
+@pytest.mark.parametrize("fmt", [oracle.Q4_0, oracle.Q4_K])
 @pytest.mark.parametrize("rows,hidden,batch", [(37, 256, 2), (1000, 2560, 8), (4099, 3072, 5),
                                                (16, 512, 3), (17, 1024, 7), (300, 3328, 4)])
-def test_q4_0_batched_decode_once(rows, hidden, batch):
-    g = synth.rng(1010, rows, hidden, batch)
-    W = synth.q4_0_matrix(g, rows, hidden)
+def test_q4_batched_decode_once(fmt, rows, hidden, batch):
+    g = synth.rng(1010, fmt, rows, hidden, batch)
+    W = synth.matrix(fmt, g, rows, hidden)
     x = synth.normal_vector(g, hidden, batch=batch)
-    y = run_matvec(oracle.Q4_0, W, x, rows, hidden, batch=batch, split_k=0)
-    ref, bound = oracle.matvec(oracle.Q4_0, W, rows, hidden, x, threads=THREADS)
-    assert_bound(y, ref, bound, what=f"q4_0 {rows}x{hidden} batch {batch}")
+    y = run_matvec(fmt, W, x, rows, hidden, batch=batch, split_k=0)
+    ref, bound = oracle.matvec(fmt, W, rows, hidden, x, threads=THREADS)
+    assert_bound(y, ref, bound, what=f"{FMT_NAME[fmt]} {rows}x{hidden} batch {batch}")
 
 
-def test_q4_0_batched_scales_and_dynamic_range():
+@pytest.mark.parametrize("fmt", [oracle.Q4_0, oracle.Q4_K])
+def test_q4_batched_scales_and_dynamic_range(fmt):
     # vectors at very different magnitudes (each gets its own power-of-two
     # scale), one all-zero vector and wide dynamic range inside a vector
     rows, hidden, batch = 500, 2560, 6
-    g = synth.rng(1011)
-    W = synth.q4_0_matrix(g, rows, hidden)
+    g = synth.rng(1011, fmt)
+    W = synth.matrix(fmt, g, rows, hidden)
     x = synth.normal_vector(g, hidden, batch=batch)
     x[0] *= 1e-20
     x[1] *= 3e15
     x[2] = 0.0
     x[3] *= np.exp(g.uniform(-8, 8, hidden)).astype(np.float32)
     x[4, :7] = 65504.0 * 4
-    y = run_matvec(oracle.Q4_0, W, x, rows, hidden, batch=batch, split_k=0)
-    ref, bound = oracle.matvec(oracle.Q4_0, W, rows, hidden, x)
+    y = run_matvec(fmt, W, x, rows, hidden, batch=batch, split_k=0)
+    ref, bound = oracle.matvec(fmt, W, rows, hidden, x)
     assert np.all(y[2] == 0.0)
     assert_bound(y, ref, bound, what="scales")
 
