@@ -108,7 +108,7 @@ qws_status qws_q6k_matvec(const void* W, const float* x, float* y, int64_t rows,
  *   a kernel that decodes each weight once for all vectors (tensor-core
  *   products of the exact codes with x split into two f16 parts after a
  *   per-vector power-of-two scale); the result meets the same tolerance
- *   for any finite x. */
+ *   for any finite x.
  *   ws, ws_bytes  workspace of at least
  *            qws_workspace_bytes(QWS_OP_MATVEC, rows, hidden, 0, batch, S)
  *            bytes (device, 16-byte aligned); may be NULL when split_k == 1. */
