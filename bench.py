@@ -435,7 +435,9 @@ def run_op(args):
             launches = 2
             # quantize reads x, writes xq; the matvec reads W and xq, writes y
             nbytes = wbytes + B * H * 4 + 2 * B * (H // 32 * 34) + B * VOCAB * 4
-            kernel = "quantize_q8_0_kernel + matvec_kernel<UnitQ40xQ8>"
+            kernel = ("quantize_q8_0_kernel + batch_q4_matvec_kernel<102> (decode once for all "
+                      "vectors)" if 2 <= B <= 8 else
+                      "quantize_q8_0_kernel + matvec_kernel<UnitQ40xQ8>")
         workload = f"lm_head {VOCAB}x{H} Q4_0, batch {B}"
     elif args.op == "kv_attention":
         nq, nkv, hd, L = 8, 4, 256, 32768

@@ -155,6 +155,10 @@ qws_status qws_q4k_qkv_proj(const void* Wq, const void* Wk, const void* Wv, cons
  *   16-byte aligned), xq [batch][hidden / 32 * 34] bytes (device, 4-byte
  *   aligned), y [batch][rows] f32 (device, 4-byte aligned), overwritten.
  *   hidden % 64 == 0, 0 < hidden <= 20480, batch * hidden / 64 <= 320.
+ *   With 2..8 vectors, hidden % 256 == 0 and hidden <= 3072 a kernel that
+ *   decodes each weight once for all vectors runs instead (tensor-core
+ *   products of the exact integer codes, each block scaled by dw * dx in
+ *   f32); the tolerance is the same.
  *   Any other format returns QWS_ERR_FORMAT.
  *
  * qws_q8_qkv_proj: the fused Q/K/V projection of the 8-bit path (batch 1):

@@ -236,6 +236,14 @@ qws_status qws_q8_matvec(qws_format wfmt, const void* W, const void* xq, float* 
   if (rows > (int64_t(1) << 31) / batch)
     return fail(QWS_ERR_SHAPE, "%s: rows * batch above 2^31", fn);
   if (rows == 0) return ok();
+  if (qws::batch_q4_eligible(100 + wfmt, hidden, batch)) {
+    // 2..8 vectors: every weight decoded once for all of them
+    const cudaError_t e = qws::launch_batch_q4_matvec(
+        100 + wfmt, static_cast<const uint8_t*>(W), nullptr, y, rows, hidden, batch,
+        reinterpret_cast<cudaStream_t>(stream), static_cast<const uint8_t*>(xq));
+    if (e != cudaSuccess) return cuda_fail(e, fn, "");
+    return ok();
+  }
   std::string why;
   qws::Seg seg{static_cast<const uint8_t*>(W), y, rows, 0};
   cudaError_t e = qws::launch_matvec_q8(wfmt, &seg, 1, static_cast<const uint8_t*>(xq), hidden,

@@ -42,16 +42,20 @@ constexpr int kBmRows = 16;                     // rows per tile (MMA M)
 constexpr int kBmWarps = 8;                     // consumer warps = column slices
 constexpr int kBmThreads = 32 + kBmWarps * 32;
 constexpr int kBmMaxB = 8;                      // MMA N
-constexpr int kBmStages = 4;
+constexpr int kBmStages = 4;                    // at most; fewer when the rows are wide
 constexpr int64_t kBmMaxK = 3072;
 
+// kFmt: 2 Q4_0 / 12 Q4_K weights with f32 activations x; 102 Q4_0 / 108
+// Q8_0 weights with Q8_0 activations xq (integer codes exact in f16, no split)
 struct BmParams {
-  const uint8_t* W;     // Q4_0 or Q4_K, rows x K
-  const float* x;       // [B][K]
+  const uint8_t* W;     // rows x K in the weight format
+  const float* x;       // [B][K] (f32 activations)
+  const uint8_t* xq;    // [B][K / 32 * 34] (Q8_0 activations)
   float* y;             // [B][rows]
   int64_t rows, K;
   int B;
   int n_tiles;          // ceil(rows / 16)
+  int stages;           // ring depth, 2..kBmStages
   uint32_t row_bytes;   // K / 32 * 18 = K / 256 * 144
   uint32_t xs_stride;   // f16 elements per staged activation row: K + 8
 };
@@ -59,15 +63,25 @@ struct BmParams {
 __host__ __device__ constexpr size_t bm_xs_bytes(int64_t K) {
   return static_cast<size_t>(2 * kBmMaxB) * static_cast<size_t>(K + 8) * 2;  // hi and lo
 }
-__host__ __device__ constexpr size_t bm_stage_bytes(int64_t K) {
-  return (static_cast<size_t>(kBmRows) * (K / 32 * 18) + 16 + 127) / 128 * 128;
+// block bytes per 32 weights: Q8_0 34, Q4_0 18, Q4_K 144 / 8 = 18
+__host__ __device__ constexpr int64_t bm_block_bytes(int fmt) { return fmt == 108 ? 34 : 18; }
+__host__ __device__ constexpr size_t bm_stage_bytes(int64_t K, int fmt) {
+  return (static_cast<size_t>(kBmRows) * (K / 32 * bm_block_bytes(fmt)) + 16 + 127) / 128 * 128;
 }
-__host__ __device__ constexpr size_t bm_smem_bytes(int64_t K) {
-  return bm_xs_bytes(K) + kBmStages * bm_stage_bytes(K) +
-         2 * kBmWarps * kBmRows * kBmMaxB * sizeof(float) +   // slice sums, two buffers
-         kBmMaxB * sizeof(float) +                              // 2^-s per vector
-         static_cast<size_t>(kBmMaxB) * (K / 32) * sizeof(float) +   // Q4_K: sub-block sums of x'
+__host__ __device__ constexpr size_t bm_fixed_bytes(int64_t K) {
+  return bm_xs_bytes(K) + 2 * kBmWarps * kBmRows * kBmMaxB * sizeof(float) +
+         kBmMaxB * sizeof(float) + static_cast<size_t>(kBmMaxB) * (K / 32) * sizeof(float) +
          2 * kBmStages * sizeof(uint64_t) + 64;
+}
+constexpr size_t kBmSmemBudget = 227 * 1024;
+// ring depth that fits beside the activations (0 when not even two do)
+__host__ __device__ constexpr int bm_stages(int64_t K, int fmt) {
+  const size_t f = bm_fixed_bytes(K), st = bm_stage_bytes(K, fmt);
+  const size_t n = f >= kBmSmemBudget ? 0 : (kBmSmemBudget - f) / st;
+  return n >= kBmStages ? kBmStages : static_cast<int>(n);
+}
+__host__ __device__ constexpr size_t bm_smem_bytes(int64_t K, int fmt) {
+  return bm_fixed_bytes(K) + bm_stages(K, fmt) * bm_stage_bytes(K, fmt);
 }
 
 __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -92,6 +106,12 @@ __device__ __forceinline__ uint32_t codes_lo(uint32_t u) {
 }
 __device__ __forceinline__ uint32_t codes_hi(uint32_t u) {
   return f16x2_sub(((u >> 4) & 0x000Fu) | ((u & 0xF000u) << 4) | 0x64006400u, 0x64086408u);
+}
+// two int8 codes (byte 0 -> low half) as f16x2: offset to 0..255 under the
+// f16 exponent of 1024, then 1152 subtracted (exact)
+__device__ __forceinline__ uint32_t s8codes(uint32_t u) {
+  const uint32_t v = u ^ 0x8080u;
+  return f16x2_sub((v & 0x00FFu) | ((v & 0xFF00u) << 8) | 0x64006400u, 0x64806480u);
 }
 // Q4_K codes q (no offset): the low or the high nibble pair as f16x2 of q
 __device__ __forceinline__ uint32_t kcodes(uint32_t u, bool high) {
@@ -197,16 +217,17 @@ __device__ __forceinline__ void q4k_pair(const uint8_t* rg, const uint8_t* rg8, 
   acc[3] = fmaf(a3, c1[3], fmaf(-b3, t1, acc[3]));
 }
 
-template <int kFmt>   // 2: Q4_0, 12: Q4_K
+template <int kFmt>   // 2: Q4_0, 12: Q4_K (f32 x); 102: Q4_0, 108: Q8_0 (Q8_0 x)
 __global__ void __launch_bounds__(kBmThreads, 1) batch_q4_matvec_kernel(
     const __grid_constant__ BmParams p) {
   extern __shared__ __align__(128) uint8_t bm_smem[];
   const int64_t K = p.K;
   __half* xs_hi = reinterpret_cast<__half*>(bm_smem);
   __half* xs_lo = xs_hi + kBmMaxB * p.xs_stride;
+  const int S = p.stages;
   uint8_t* ring = bm_smem + bm_xs_bytes(K);
-  const size_t stage_bytes = bm_stage_bytes(K);
-  float* red = reinterpret_cast<float*>(ring + kBmStages * stage_bytes);   // [2][8][128]
+  const size_t stage_bytes = bm_stage_bytes(K, kFmt);
+  float* red = reinterpret_cast<float*>(ring + S * stage_bytes);          // [2][8][128]
   float* unscale = red + 2 * kBmWarps * kBmRows * kBmMaxB;                  // [8]
   float* ssum = unscale + kBmMaxB;                                          // [8][K / 32]
   uint64_t* full = reinterpret_cast<uint64_t*>(ssum + kBmMaxB * (K / 32));
@@ -215,7 +236,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q4_matvec_kernel(
   const int warp = static_cast<int>(threadIdx.x >> 5) - 1;   // -1: the copy warp
   const int lane = threadIdx.x & 31;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kBmStages; ++s) {
+    for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
@@ -231,8 +252,8 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q4_matvec_kernel(
       const uint64_t pol = l2_policy_evict_first();
       int k = 0;
       for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++k) {
-        const int s = k % kBmStages;
-        const uint32_t ph = static_cast<uint32_t>(k / kBmStages) & 1u;
+        const int s = k % S;
+        const uint32_t ph = static_cast<uint32_t>(k / S) & 1u;
         if (!mbar_wait(&empty[s], ph ^ 1u)) {
           atomicOr(&g_err_batchmv, kErrEmptyWait);
           break;
@@ -243,9 +264,9 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q4_matvec_kernel(
         mbar_arrive_expect_tx(&full[s], bytes);
         bulk_copy_g2s(ring + s * stage_bytes, p.W + r0 * p.row_bytes, bytes, &full[s], pol);
       }
-      const int first = k > kBmStages ? k - kBmStages : 0;
+      const int first = k > S ? k - S : 0;
       for (int i = first; i < k; ++i)
-        if (!mbar_wait(&full[i % kBmStages], static_cast<uint32_t>(i / kBmStages) & 1u))
+        if (!mbar_wait(&full[i % S], static_cast<uint32_t>(i / S) & 1u))
           atomicOr(&g_err_batchmv, kErrDrain);
     }
     return;
@@ -254,6 +275,22 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q4_matvec_kernel(
   // ---- consumers: stage the activations (x comes from the previous kernel)
   pdl_wait();
   const int ct = static_cast<int>(threadIdx.x) - 32;
+  if constexpr (kFmt >= 100) {
+    // Q8_0 activations: codes to f16 (exact), block scales to f32
+    const int64_t nb = K / 32;
+    for (int n = warp; n < kBmMaxB; n += kBmWarps) {
+      if (lane == 0) unscale[n] = 1.f;
+      const uint8_t* xb = p.xq + static_cast<int64_t>(n) * nb * 34;
+      for (int64_t i = lane; i < K + 8; i += 32) {
+        float v = 0.f;
+        if (n < p.B && i < K) v = static_cast<float>(static_cast<int8_t>(xb[(i >> 5) * 34 + 2 + (i & 31)]));
+        xs_hi[n * p.xs_stride + i] = __float2half_rn(v);
+        xs_lo[n * p.xs_stride + i] = __float2half_rn(0.f);
+      }
+      for (int64_t bk = lane; bk < nb; bk += 32)
+        ssum[n * nb + bk] = n < p.B ? half_bits_to_float(ld_u16(xb + bk * 34)) : 0.f;
+    }
+  } else
   for (int n = warp; n < kBmMaxB; n += kBmWarps) {
     // vector n: its power-of-two scale 2^s with max |x| 2^s in [2^13, 2^14)
     float m = 0.f;
@@ -299,8 +336,8 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q4_matvec_kernel(
   const uint32_t* xl = reinterpret_cast<const uint32_t*>(xs_lo + g * p.xs_stride);
   int k = 0;
   for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++k) {
-    const int s = k % kBmStages;
-    const uint32_t ph = static_cast<uint32_t>(k / kBmStages) & 1u;
+    const int s = k % S;
+    const uint32_t ph = static_cast<uint32_t>(k / S) & 1u;
     const bool landed = mbar_wait(&full[s], ph);
     if (!landed) atomicOr(&g_err_batchmv, kErrFullWait);
     const uint8_t* st = ring + s * stage_bytes;
@@ -367,6 +404,41 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q4_matvec_kernel(
         acc[2] = fmaf(db0, c0[2], acc[2]);
         acc[3] = fmaf(db0, c0[3], acc[3]);
       }
+    } else if constexpr (kFmt >= 100) {
+      // weights x Q8_0 activations: one MMA per 16 columns (codes exact),
+      // then the two block scales: acc += (dw dx) C, dw dx exact in f32
+      const int nb = static_cast<int>(K / 32);
+      constexpr int kBB = kFmt == 102 ? 18 : 34;   // weight block bytes
+      for (int bi = b0; landed && bi < b0 + per; ++bi) {
+        const uint8_t* pa = rg + bi * kBB;
+        const uint8_t* pb = rg8 + bi * kBB;
+        uint32_t a0[4], a1[4];
+        if constexpr (kFmt == 102) {
+          const uint32_t u0 = ld_u16(pa + 2 + 2 * tq), u1 = ld_u16(pb + 2 + 2 * tq);
+          const uint32_t u2 = ld_u16(pa + 10 + 2 * tq), u3 = ld_u16(pb + 10 + 2 * tq);
+          a0[0] = codes_lo(u0); a0[1] = codes_lo(u1); a0[2] = codes_lo(u2); a0[3] = codes_lo(u3);
+          a1[0] = codes_hi(u0); a1[1] = codes_hi(u1); a1[2] = codes_hi(u2); a1[3] = codes_hi(u3);
+        } else {
+          a0[0] = s8codes(ld_u16(pa + 2 + 2 * tq));
+          a0[1] = s8codes(ld_u16(pb + 2 + 2 * tq));
+          a0[2] = s8codes(ld_u16(pa + 10 + 2 * tq));
+          a0[3] = s8codes(ld_u16(pb + 10 + 2 * tq));
+          a1[0] = s8codes(ld_u16(pa + 18 + 2 * tq));
+          a1[1] = s8codes(ld_u16(pb + 18 + 2 * tq));
+          a1[2] = s8codes(ld_u16(pa + 26 + 2 * tq));
+          a1[3] = s8codes(ld_u16(pb + 26 + 2 * tq));
+        }
+        const int w0 = bi * 16 + tq;
+        float cc[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(cc, a0, xh[w0], xh[w0 + 4]);
+        mma_16816(cc, a1, xh[w0 + 8], xh[w0 + 12]);
+        const float da = half_bits_to_float(ld_u16(pa)), db = half_bits_to_float(ld_u16(pb));
+        const float x0 = ssum[(2 * tq) * nb + bi], x1 = ssum[(2 * tq + 1) * nb + bi];
+        acc[0] = fmaf(da * x0, cc[0], acc[0]);
+        acc[1] = fmaf(da * x1, cc[1], acc[1]);
+        acc[2] = fmaf(db * x0, cc[2], acc[2]);
+        acc[3] = fmaf(db * x1, cc[3], acc[3]);
+      }
     } else {
       int bi = b0;
       // a sub-block on its own when the slice starts on an odd one
@@ -403,39 +475,45 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q4_matvec_kernel(
 
 // ------------------------------------------------------------------ host side
 bool batch_q4_eligible(int fmt, int64_t K, int B) {
-  return (fmt == 2 || fmt == 12) && B >= 2 && B <= kBmMaxB && K >= 256 && K % 256 == 0 &&
-         K <= kBmMaxK;
+  return (fmt == 2 || fmt == 12 || fmt == 102 || fmt == 108) && B >= 2 && B <= kBmMaxB &&
+         K >= 256 && K % 256 == 0 && K <= kBmMaxK && bm_stages(K, fmt) >= 2;
 }
 
 template <int kFmt>
 static cudaError_t set_smem_attr() {
-  static size_t attr_smem[64] = {0};
+  static bool attr_set[64] = {false};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && attr_smem[dev] == 0) {
+  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
     const cudaError_t e = cudaFuncSetAttribute(batch_q4_matvec_kernel<kFmt>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(bm_smem_bytes(kBmMaxK)));
+                                               static_cast<int>(kBmSmemBudget));
     if (e != cudaSuccess) return e;
-    attr_smem[dev] = bm_smem_bytes(kBmMaxK);
+    attr_set[dev] = true;
   }
   return cudaSuccess;
 }
 
 cudaError_t launch_batch_q4_matvec(int fmt, const uint8_t* W, const float* x, float* y,
-                                   int64_t rows, int64_t K, int B, cudaStream_t st) {
+                                   int64_t rows, int64_t K, int B, cudaStream_t st,
+                                   const uint8_t* xq) {
   BmParams p;
   p.W = W;
   p.x = x;
+  p.xq = xq;
   p.y = y;
   p.rows = rows;
   p.K = K;
   p.B = B;
   p.n_tiles = static_cast<int>((rows + kBmRows - 1) / kBmRows);
-  p.row_bytes = static_cast<uint32_t>(K / 32 * 18);
+  p.row_bytes = static_cast<uint32_t>(K / 32 * (fmt == 108 ? 34 : 18));
   p.xs_stride = static_cast<uint32_t>(K + 8);
-  const size_t smem = bm_smem_bytes(K);
-  const cudaError_t ea = fmt == 12 ? set_smem_attr<12>() : set_smem_attr<2>();
+  p.stages = bm_stages(K, fmt);
+  const size_t smem = bm_smem_bytes(K, fmt);
+  const cudaError_t ea = fmt == 12    ? set_smem_attr<12>()
+                         : fmt == 102 ? set_smem_attr<102>()
+                         : fmt == 108 ? set_smem_attr<108>()
+                                      : set_smem_attr<2>();
   if (ea != cudaSuccess) return ea;
   const int grid = static_cast<int>(std::min<int64_t>(p.n_tiles, device_sms()));
   cudaLaunchConfig_t cfg = {};
@@ -448,8 +526,12 @@ cudaError_t launch_batch_q4_matvec(int fmt, const uint8_t* W, const float* x, fl
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return fmt == 12 ? cudaLaunchKernelEx(&cfg, batch_q4_matvec_kernel<12>, p)
-                   : cudaLaunchKernelEx(&cfg, batch_q4_matvec_kernel<2>, p);
+  switch (fmt) {
+    case 12: return cudaLaunchKernelEx(&cfg, batch_q4_matvec_kernel<12>, p);
+    case 102: return cudaLaunchKernelEx(&cfg, batch_q4_matvec_kernel<102>, p);
+    case 108: return cudaLaunchKernelEx(&cfg, batch_q4_matvec_kernel<108>, p);
+    default: return cudaLaunchKernelEx(&cfg, batch_q4_matvec_kernel<2>, p);
+  }
 }
 
 unsigned read_clear_batchmv_errors() {

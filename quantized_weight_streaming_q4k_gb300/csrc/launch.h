@@ -117,11 +117,12 @@ cudaError_t launch_kv_append(float* kc, float* vc, const float* k, const float* 
 cudaError_t launch_kv_attention(const float* q, const float* kc, const float* vc, float* out,
                                 int n_q, int n_kv, int head_dim, int64_t max_seq, int64_t n_ctx,
                                 float scale, float softcap, float* ws, cudaStream_t st);
-// Q4_0 (fmt 2) / Q4_K (fmt 12) for 2..8 vectors, each weight decoded once
-// (batchmv.cu)
+// 2..8 vectors, each weight decoded once (batchmv.cu): fmt 2 Q4_0 / 12 Q4_K
+// with f32 x; 102 Q4_0 / 108 Q8_0 with Q8_0 activations xq (x unused)
 bool batch_q4_eligible(int fmt, int64_t K, int B);
 cudaError_t launch_batch_q4_matvec(int fmt, const uint8_t* W, const float* x, float* y,
-                                   int64_t rows, int64_t K, int B, cudaStream_t st);
+                                   int64_t rows, int64_t K, int B, cudaStream_t st,
+                                   const uint8_t* xq = nullptr);
 unsigned read_clear_batchmv_errors();
 // prefill (prefill.cu): X packed to f16 tiles in ws, then the tcgen05 GEMM
 size_t prefill_workspace_bytes(int64_t hidden, int64_t n_tokens);
