@@ -44,7 +44,9 @@
  *  - Limits: every consumer thread owns one lane unit of 64 columns:
  *    batch * hidden / 64 <= 320 per pass, so hidden <= 20480 at batch 1 and
  *    hidden <= 2560 at batch 8; larger products need split_k (qws_matvec,
- *    qws_q4_0_matvec), which divides hidden into column slices.
+ *    qws_q4_0_matvec), which divides hidden into column slices.  The
+ *    decode-once kernel for 2..8 vectors (Q4_0 and Q4_K weights, or the
+ *    8-bit path) has no lane limit; it takes hidden % 256 == 0, <= 3072.
  */
 #ifndef QWS_H
 #define QWS_H
@@ -104,11 +106,11 @@ qws_status qws_q6k_matvec(const void* W, const float* x, float* y, int64_t rows,
  *            hidden slices of hidden/S columns (S must divide hidden/256),
  *            written to the workspace and then added in a fixed order, so
  *            results are run-to-run identical.
- *   With 2..8 vectors, hidden <= 3072 and a single pass, Q4_0 and Q4_K run
- *   a kernel that decodes each weight once for all vectors (tensor-core
+ *   With 2..8 vectors, hidden <= 3072 and split_k 0 or 1, Q4_0 and Q4_K
+ *   run a kernel that decodes each weight once for all vectors (tensor-core
  *   products of the exact codes with x split into two f16 parts after a
  *   per-vector power-of-two scale); the result meets the same tolerance
- *   for any finite x.
+ *   for any finite x, the 320-lane limit does not apply and ws is unused.
  *   ws, ws_bytes  workspace of at least
  *            qws_workspace_bytes(QWS_OP_MATVEC, rows, hidden, 0, batch, S)
  *            bytes (device, 16-byte aligned); may be NULL when split_k == 1. */
@@ -158,7 +160,7 @@ qws_status qws_q4k_qkv_proj(const void* Wq, const void* Wk, const void* Wv, cons
  *   With 2..8 vectors, hidden % 256 == 0 and hidden <= 3072 a kernel that
  *   decodes each weight once for all vectors runs instead (tensor-core
  *   products of the exact integer codes, each block scaled by dw * dx in
- *   f32); the tolerance is the same.
+ *   f32; no lane limit); the tolerance is the same.
  *   Any other format returns QWS_ERR_FORMAT.
  *
  * qws_q8_qkv_proj: the fused Q/K/V projection of the 8-bit path (batch 1):

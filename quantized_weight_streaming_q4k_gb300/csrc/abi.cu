@@ -91,6 +91,14 @@ qws_status run_matvec(const char* fn, int fmt, const void* W, const float* x, fl
   qws_status rc = check_matvec(fn, fmt, W, x, y, rows, hidden, batch);
   if (rc != QWS_OK) return rc;
   if (split_k < 0) return fail(QWS_ERR_SHAPE, "%s: split_k = %d < 0", fn, split_k);
+  if (split_k <= 1 && qws::batch_q4_eligible(fmt, hidden, batch)) {
+    // 2..8 vectors: every weight decoded once for all of them (no lane limit)
+    if (rows == 0) return ok();
+    const cudaError_t e = qws::launch_batch_q4_matvec(fmt, static_cast<const uint8_t*>(W), x, y,
+                                                      rows, hidden, batch, st);
+    if (e != cudaSuccess) return cuda_fail(e, fn, "");
+    return ok();
+  }
   int S = split_k == 0 ? auto_splits(fmt, hidden, batch) : split_k;
   if (S < 1)
     return fail(QWS_ERR_SHAPE, "%s: batch %d too large for hidden %lld", fn, batch,
@@ -116,13 +124,6 @@ qws_status run_matvec(const char* fn, int fmt, const void* W, const float* x, fl
     if (!aligned(ws, 16)) return fail(QWS_ERR_ALIGN, "%s: ws is not 16-byte aligned", fn);
   }
   if (rows == 0) return ok();
-  if (S == 1 && qws::batch_q4_eligible(fmt, hidden, batch)) {
-    // 2..8 vectors: every weight decoded once for all of them
-    const cudaError_t e = qws::launch_batch_q4_matvec(fmt, static_cast<const uint8_t*>(W), x, y,
-                                                      rows, hidden, batch, st);
-    if (e != cudaSuccess) return cuda_fail(e, fn, "");
-    return ok();
-  }
   std::string why;
   qws::Seg seg{static_cast<const uint8_t*>(W), S > 1 ? static_cast<float*>(ws) : y, rows, 0};
   cudaError_t e = qws::launch_matvec(fmt, qws::EPI_STORE, &seg, 1, nullptr, x, hidden, batch, S,
@@ -218,7 +219,8 @@ static qws_status check_q8_shape(const char* fn, int wfmt, int64_t hidden, int b
     return fail(QWS_ERR_SHAPE, "%s: hidden = %lld (need a multiple of 64 in (0, 20480])", fn,
                 (long long)hidden);
   if (batch < 1) return fail(QWS_ERR_SHAPE, "%s: batch = %d < 1", fn, batch);
-  if ((hidden / 64) * batch > 320)
+  // the decode-once kernel (2..8 vectors) has no lane limit
+  if ((hidden / 64) * batch > 320 && !qws::batch_q4_eligible(100 + wfmt, hidden, batch))
     return fail(QWS_ERR_SHAPE, "%s: batch * hidden / 64 = %lld above 320", fn,
                 (long long)((hidden / 64) * batch));
   return QWS_OK;

@@ -126,6 +126,38 @@ __device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) {
 
 // 6-bit scale and min of sub-block j (0..7) from the 12 packed bytes at sc
 // (the GGUF packing), times d and dmin
+// A fragments of one 32-column block of Q4_0 / Q8_0 weights for rows g
+// (pa) and g + 8 (pb): a0 = columns 0..15, a1 = 16..31, as exact f16 codes
+template <int kFmt>
+__device__ __forceinline__ void q8_block_codes(const uint8_t* pa, const uint8_t* pb, int tq,
+                                               uint32_t (&a0)[4], uint32_t (&a1)[4]) {
+  if constexpr (kFmt == 102) {
+    const uint32_t u0 = ld_u16(pa + 2 + 2 * tq), u1 = ld_u16(pb + 2 + 2 * tq);
+    const uint32_t u2 = ld_u16(pa + 10 + 2 * tq), u3 = ld_u16(pb + 10 + 2 * tq);
+    a0[0] = codes_lo(u0); a0[1] = codes_lo(u1); a0[2] = codes_lo(u2); a0[3] = codes_lo(u3);
+    a1[0] = codes_hi(u0); a1[1] = codes_hi(u1); a1[2] = codes_hi(u2); a1[3] = codes_hi(u3);
+  } else {
+    a0[0] = s8codes(ld_u16(pa + 2 + 2 * tq));
+    a0[1] = s8codes(ld_u16(pb + 2 + 2 * tq));
+    a0[2] = s8codes(ld_u16(pa + 10 + 2 * tq));
+    a0[3] = s8codes(ld_u16(pb + 10 + 2 * tq));
+    a1[0] = s8codes(ld_u16(pa + 18 + 2 * tq));
+    a1[1] = s8codes(ld_u16(pb + 18 + 2 * tq));
+    a1[2] = s8codes(ld_u16(pa + 26 + 2 * tq));
+    a1[3] = s8codes(ld_u16(pb + 26 + 2 * tq));
+  }
+}
+
+// acc += (dw dx) C for one block's integer product C: rows g (da) and g + 8
+// (db), vectors 2 tq and 2 tq + 1 (dx)
+__device__ __forceinline__ void q8_block_scale(float (&acc)[4], const float (&c)[4], float da,
+                                               float db, float2 dx) {
+  acc[0] = fmaf(da * dx.x, c[0], acc[0]);
+  acc[1] = fmaf(da * dx.y, c[1], acc[1]);
+  acc[2] = fmaf(db * dx.x, c[2], acc[2]);
+  acc[3] = fmaf(db * dx.y, c[3], acc[3]);
+}
+
 __device__ __forceinline__ void q4k_ab(const uint8_t* h, int j, float& a, float& b) {
   const uint32_t dd = *reinterpret_cast<const uint32_t*>(h);
   const uint8_t* sc = h + 4;
@@ -144,7 +176,7 @@ __device__ __forceinline__ void q4k_ab(const uint8_t* h, int j, float& a, float&
 // acc (rows g, g + 8 x vectors 2tq, 2tq + 1) += a C - b S of Q4_K sub-block bi
 __device__ __forceinline__ void q4k_sub(const uint8_t* rg, const uint8_t* rg8, int bi, int tq,
                                         const uint32_t* xh, const uint32_t* xl,
-                                        const float* ssum, int64_t K, float (&acc)[4]) {
+                                        const float* ssum, float (&acc)[4]) {
   const int kb = bi >> 3, j = bi & 7, c = j >> 1;
   const bool high = (j & 1) != 0;
   const uint8_t* ha = rg + kb * 144;
@@ -164,17 +196,18 @@ __device__ __forceinline__ void q4k_sub(const uint8_t* rg, const uint8_t* rg8, i
   float a0, b0, a1, b1;
   q4k_ab(ha, j, a0, b0);
   q4k_ab(hb, j, a1, b1);
-  const float s0 = ssum[(2 * tq) * (K / 32) + bi], s1 = ssum[(2 * tq + 1) * (K / 32) + bi];
-  acc[0] = fmaf(a0, cc[0], fmaf(-b0, s0, acc[0]));
-  acc[1] = fmaf(a0, cc[1], fmaf(-b0, s1, acc[1]));
-  acc[2] = fmaf(a1, cc[2], fmaf(-b1, s0, acc[2]));
-  acc[3] = fmaf(a1, cc[3], fmaf(-b1, s1, acc[3]));
+  // ssum [sub-block][vector]: the sums of vectors 2 tq, 2 tq + 1 in one load
+  const float2 sv = reinterpret_cast<const float2*>(ssum)[bi * 4 + tq];
+  acc[0] = fmaf(a0, cc[0], fmaf(-b0, sv.x, acc[0]));
+  acc[1] = fmaf(a0, cc[1], fmaf(-b0, sv.y, acc[1]));
+  acc[2] = fmaf(a1, cc[2], fmaf(-b1, sv.x, acc[2]));
+  acc[3] = fmaf(a1, cc[3], fmaf(-b1, sv.y, acc[3]));
 }
 
 // the aligned pair bi (even), bi + 1: one load of the shared code bytes
 __device__ __forceinline__ void q4k_pair(const uint8_t* rg, const uint8_t* rg8, int bi, int tq,
                                          const uint32_t* xh, const uint32_t* xl,
-                                         const float* ssum, int64_t K, float (&acc)[4]) {
+                                         const float* ssum, float (&acc)[4]) {
   const int kb = bi >> 3, j = bi & 7, c = j >> 1;
   const uint8_t* ha = rg + kb * 144;
   const uint8_t* hb = rg8 + kb * 144;
@@ -204,17 +237,16 @@ __device__ __forceinline__ void q4k_pair(const uint8_t* rg, const uint8_t* rg8, 
   q4k_ab(hb, j, a1, b1);
   q4k_ab(ha, j + 1, a2, b2);
   q4k_ab(hb, j + 1, a3, b3);
-  const int nb = static_cast<int>(K / 32);
-  const float s0 = ssum[(2 * tq) * nb + bi], s1 = ssum[(2 * tq + 1) * nb + bi];
-  const float t0 = ssum[(2 * tq) * nb + bi + 1], t1 = ssum[(2 * tq + 1) * nb + bi + 1];
-  acc[0] = fmaf(a0, c0[0], fmaf(-b0, s0, acc[0]));
-  acc[1] = fmaf(a0, c0[1], fmaf(-b0, s1, acc[1]));
-  acc[2] = fmaf(a1, c0[2], fmaf(-b1, s0, acc[2]));
-  acc[3] = fmaf(a1, c0[3], fmaf(-b1, s1, acc[3]));
-  acc[0] = fmaf(a2, c1[0], fmaf(-b2, t0, acc[0]));
-  acc[1] = fmaf(a2, c1[1], fmaf(-b2, t1, acc[1]));
-  acc[2] = fmaf(a3, c1[2], fmaf(-b3, t0, acc[2]));
-  acc[3] = fmaf(a3, c1[3], fmaf(-b3, t1, acc[3]));
+  const float2 sv = reinterpret_cast<const float2*>(ssum)[bi * 4 + tq];
+  const float2 tv = reinterpret_cast<const float2*>(ssum)[(bi + 1) * 4 + tq];
+  acc[0] = fmaf(a0, c0[0], fmaf(-b0, sv.x, acc[0]));
+  acc[1] = fmaf(a0, c0[1], fmaf(-b0, sv.y, acc[1]));
+  acc[2] = fmaf(a1, c0[2], fmaf(-b1, sv.x, acc[2]));
+  acc[3] = fmaf(a1, c0[3], fmaf(-b1, sv.y, acc[3]));
+  acc[0] = fmaf(a2, c1[0], fmaf(-b2, tv.x, acc[0]));
+  acc[1] = fmaf(a2, c1[1], fmaf(-b2, tv.y, acc[1]));
+  acc[2] = fmaf(a3, c1[2], fmaf(-b3, tv.x, acc[2]));
+  acc[3] = fmaf(a3, c1[3], fmaf(-b3, tv.y, acc[3]));
 }
 
 template <int kFmt>   // 2: Q4_0, 12: Q4_K (f32 x); 102: Q4_0, 108: Q8_0 (Q8_0 x)
@@ -229,7 +261,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q4_matvec_kernel(
   const size_t stage_bytes = bm_stage_bytes(K, kFmt);
   float* red = reinterpret_cast<float*>(ring + S * stage_bytes);          // [2][8][128]
   float* unscale = red + 2 * kBmWarps * kBmRows * kBmMaxB;                  // [8]
-  float* ssum = unscale + kBmMaxB;                                          // [8][K / 32]
+  float* ssum = unscale + kBmMaxB;                                          // [K / 32][8]
   uint64_t* full = reinterpret_cast<uint64_t*>(ssum + kBmMaxB * (K / 32));
   uint64_t* empty = full + kBmStages;
 
@@ -287,8 +319,9 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q4_matvec_kernel(
         xs_hi[n * p.xs_stride + i] = __float2half_rn(v);
         xs_lo[n * p.xs_stride + i] = __float2half_rn(0.f);
       }
+      // block scales [block][vector]: one float2 per thread and block below
       for (int64_t bk = lane; bk < nb; bk += 32)
-        ssum[n * nb + bk] = n < p.B ? half_bits_to_float(ld_u16(xb + bk * 34)) : 0.f;
+        ssum[bk * kBmMaxB + n] = n < p.B ? half_bits_to_float(ld_u16(xb + bk * 34)) : 0.f;
     }
   } else
   for (int n = warp; n < kBmMaxB; n += kBmWarps) {
@@ -318,7 +351,7 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q4_matvec_kernel(
         float t = 0.f;
         if (n < p.B)
           for (int i = 0; i < 32; ++i) t += p.x[n * K + bk * 32 + i] * sc;
-        ssum[n * (K / 32) + bk] = t;
+        ssum[bk * kBmMaxB + n] = t;                // [sub-block][vector]
       }
     }
   }
@@ -406,50 +439,51 @@ __global__ void __launch_bounds__(kBmThreads, 1) batch_q4_matvec_kernel(
       }
     } else if constexpr (kFmt >= 100) {
       // weights x Q8_0 activations: one MMA per 16 columns (codes exact),
-      // then the two block scales: acc += (dw dx) C, dw dx exact in f32
-      const int nb = static_cast<int>(K / 32);
+      // then the two block scales: acc += (dw dx) C, dw dx exact in f32; two
+      // blocks at a time so that two independent MMA chains interleave
       constexpr int kBB = kFmt == 102 ? 18 : 34;   // weight block bytes
-      for (int bi = b0; landed && bi < b0 + per; ++bi) {
+      const float2* dx2 = reinterpret_cast<const float2*>(ssum) + tq;   // [block][4]
+      int bi = b0;
+      for (; landed && bi + 1 < b0 + per; bi += 2) {
+        const uint8_t* pa = rg + bi * kBB;
+        const uint8_t* pb = rg8 + bi * kBB;
+        uint32_t a0[4], a1[4], e0[4], e1[4];
+        q8_block_codes<kFmt>(pa, pb, tq, a0, a1);
+        q8_block_codes<kFmt>(pa + kBB, pb + kBB, tq, e0, e1);
+        const int w0 = bi * 16 + tq, w1 = w0 + 16;
+        float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(c0, a0, xh[w0], xh[w0 + 4]);
+        mma_16816(c1, e0, xh[w1], xh[w1 + 4]);
+        mma_16816(c0, a1, xh[w0 + 8], xh[w0 + 12]);
+        mma_16816(c1, e1, xh[w1 + 8], xh[w1 + 12]);
+        q8_block_scale(acc, c0, half_bits_to_float(ld_u16(pa)), half_bits_to_float(ld_u16(pb)),
+                       dx2[bi * 4]);
+        q8_block_scale(acc, c1, half_bits_to_float(ld_u16(pa + kBB)),
+                       half_bits_to_float(ld_u16(pb + kBB)), dx2[(bi + 1) * 4]);
+      }
+      if (landed && bi < b0 + per) {
         const uint8_t* pa = rg + bi * kBB;
         const uint8_t* pb = rg8 + bi * kBB;
         uint32_t a0[4], a1[4];
-        if constexpr (kFmt == 102) {
-          const uint32_t u0 = ld_u16(pa + 2 + 2 * tq), u1 = ld_u16(pb + 2 + 2 * tq);
-          const uint32_t u2 = ld_u16(pa + 10 + 2 * tq), u3 = ld_u16(pb + 10 + 2 * tq);
-          a0[0] = codes_lo(u0); a0[1] = codes_lo(u1); a0[2] = codes_lo(u2); a0[3] = codes_lo(u3);
-          a1[0] = codes_hi(u0); a1[1] = codes_hi(u1); a1[2] = codes_hi(u2); a1[3] = codes_hi(u3);
-        } else {
-          a0[0] = s8codes(ld_u16(pa + 2 + 2 * tq));
-          a0[1] = s8codes(ld_u16(pb + 2 + 2 * tq));
-          a0[2] = s8codes(ld_u16(pa + 10 + 2 * tq));
-          a0[3] = s8codes(ld_u16(pb + 10 + 2 * tq));
-          a1[0] = s8codes(ld_u16(pa + 18 + 2 * tq));
-          a1[1] = s8codes(ld_u16(pb + 18 + 2 * tq));
-          a1[2] = s8codes(ld_u16(pa + 26 + 2 * tq));
-          a1[3] = s8codes(ld_u16(pb + 26 + 2 * tq));
-        }
+        q8_block_codes<kFmt>(pa, pb, tq, a0, a1);
         const int w0 = bi * 16 + tq;
-        float cc[4] = {0.f, 0.f, 0.f, 0.f};
-        mma_16816(cc, a0, xh[w0], xh[w0 + 4]);
-        mma_16816(cc, a1, xh[w0 + 8], xh[w0 + 12]);
-        const float da = half_bits_to_float(ld_u16(pa)), db = half_bits_to_float(ld_u16(pb));
-        const float x0 = ssum[(2 * tq) * nb + bi], x1 = ssum[(2 * tq + 1) * nb + bi];
-        acc[0] = fmaf(da * x0, cc[0], acc[0]);
-        acc[1] = fmaf(da * x1, cc[1], acc[1]);
-        acc[2] = fmaf(db * x0, cc[2], acc[2]);
-        acc[3] = fmaf(db * x1, cc[3], acc[3]);
+        float c0[4] = {0.f, 0.f, 0.f, 0.f};
+        mma_16816(c0, a0, xh[w0], xh[w0 + 4]);
+        mma_16816(c0, a1, xh[w0 + 8], xh[w0 + 12]);
+        q8_block_scale(acc, c0, half_bits_to_float(ld_u16(pa)), half_bits_to_float(ld_u16(pb)),
+                       dx2[bi * 4]);
       }
     } else {
       int bi = b0;
       // a sub-block on its own when the slice starts on an odd one
       if (landed && per > 0 && (bi & 1)) {
-        q4k_sub(rg, rg8, bi, tq, xh, xl, ssum, K, acc);
+        q4k_sub(rg, rg8, bi, tq, xh, xl, ssum, acc);
         ++bi;
       }
       // aligned pairs (2c, 2c + 1): the same 32 code bytes, low nibbles for
       // the first, high for the second; two independent MMA chains
-      for (; landed && bi + 1 < b0 + per; bi += 2) q4k_pair(rg, rg8, bi, tq, xh, xl, ssum, K, acc);
-      if (landed && bi < b0 + per) q4k_sub(rg, rg8, bi, tq, xh, xl, ssum, K, acc);
+      for (; landed && bi + 1 < b0 + per; bi += 2) q4k_pair(rg, rg8, bi, tq, xh, xl, ssum, acc);
+      if (landed && bi < b0 + per) q4k_sub(rg, rg8, bi, tq, xh, xl, ssum, acc);
     }
     // slice sums: [row][vector] of this warp, buffer k & 1
     float* rw = red + (static_cast<size_t>(k & 1) * kBmWarps + warp) * (kBmRows * kBmMaxB);

@@ -415,7 +415,8 @@ def test_lm_head_split_k_matches_single_pass():
 # tolerance is the matvec's 1e-5 * sum |w x|.
 @pytest.mark.parametrize("fmt", [oracle.Q4_0, oracle.Q4_K])
 @pytest.mark.parametrize("rows,hidden,batch", [(37, 256, 2), (1000, 2560, 8), (4099, 3072, 5),
-                                               (16, 512, 3), (17, 1024, 7), (300, 3328, 4)])
+                                               (16, 512, 3), (17, 1024, 7), (300, 3328, 4),
+                                               (333, 3072, 8)])   # 384 lanes: decode-once only
 def test_q4_batched_decode_once(fmt, rows, hidden, batch):
     g = synth.rng(1010, fmt, rows, hidden, batch)
     W = synth.matrix(fmt, g, rows, hidden)

@@ -115,6 +115,51 @@ def test_q8_matvec_batch(wfmt, batch):
     assert_bound(y, ref, bound, what=f"fmt {wfmt} batch {batch}")
 
 
+@pytest.mark.parametrize("wfmt", [oracle.Q4_0, oracle.Q8_0])
+@pytest.mark.parametrize("rows,hidden,batch", [
+    (17, 256, 8),      # smallest hidden of the decode-once kernel; one full tile + 1 row
+    (333, 3072, 8),    # largest hidden: Q8_0 rows leave room for two ring stages only
+    (16, 512, 5),      # exactly one tile
+    (1, 768, 2),       # one row: the tile is almost all tail
+    (250, 2624, 4),    # hidden % 256 != 0: the lane-unit engine instead
+    (40, 3584, 2),     # hidden > 3072: the lane-unit engine instead
+])
+def test_q8_matvec_batch_kernel_edges(wfmt, rows, hidden, batch):
+    g = synth.rng(W_Q8, 10, wfmt, rows, hidden, batch)
+    W = synth.matrix(wfmt, g, rows, hidden)
+    xq = oracle.quantize_q8_0(synth.normal_vector(g, hidden, batch))
+    y = host(ops.q8_matvec(wfmt, dev(W), dev(xq), rows, hidden, batch)).reshape(batch, rows)
+    ref, bound = oracle.matvec_q8(wfmt, W, rows, hidden, xq)
+    assert_bound(y, ref, bound, what=f"fmt {wfmt} {rows}x{hidden} batch {batch}")
+
+
+def test_q8_matvec_batch_extreme_codes():
+    # every weight code -128 / 127 and every activation code +-127 at batch 8:
+    # the per-block integer products reach 32 * 128 * 127 in the tensor-core sum
+    rows, hidden, batch = 24, 1024, 8
+    g = synth.rng(W_Q8, 11)
+    W = synth.q8_0_matrix(g, rows, hidden).reshape(-1, 34)
+    W[0::2, 2:] = 0x80
+    W[1::2, 2:] = 0x7F
+    sign = np.where(np.arange(hidden) % 2 == 0, 1.0, -1.0)
+    x = np.stack([sign * (n + 1) * (-1.0) ** n for n in range(batch)]).astype(np.float32)
+    xq = oracle.quantize_q8_0(x)
+    assert np.all(np.abs(xq.reshape(-1, 34)[:, 2:].view(np.int8)) == 127)
+    y = host(ops.q8_matvec(oracle.Q8_0, dev(W.reshape(-1)), dev(xq), rows, hidden, batch))
+    ref, bound = oracle.matvec_q8(oracle.Q8_0, W.reshape(-1), rows, hidden, xq)
+    assert_bound(y.reshape(batch, rows), ref, bound, what="batch extreme codes")
+
+
+def test_q8_matvec_batch_is_run_to_run_identical():
+    rows, hidden, batch = 4099, 2560, 8
+    g = synth.rng(W_Q8, 12)
+    W = dev(synth.matrix(oracle.Q4_0, g, rows, hidden))
+    xq = dev(oracle.quantize_q8_0(synth.normal_vector(g, hidden, batch)))
+    a = host(ops.q8_matvec(oracle.Q4_0, W, xq, rows, hidden, batch))
+    b = host(ops.q8_matvec(oracle.Q4_0, W, xq, rows, hidden, batch))
+    assert np.array_equal(a, b)
+
+
 def test_q8_matvec_lane_limit_batch_at_maximum_hidden():
     # batch * hidden / 64 == 320: every consumer lane holds one unit
     rows, hidden, batch = 97, 5120, 4
