@@ -90,6 +90,19 @@ def test_matvec_format_and_zero_rows(lib):
     assert lib.qws_q4k_matvec(A, A, A, 0, 256, 1, None) == OK
 
 
+def test_decode_once_batch_has_no_lane_limit(lib):
+    # Q4_0 / Q4_K with 2..8 vectors, hidden % 256 == 0 and <= 3072, split_k 0
+    # or 1: the decode-once kernel (no 320-lane limit, no workspace); zero
+    # rows keep every call launch-free
+    assert lib.qws_q4_0_matvec(A, A, A, 0, 3072, 8, 1, None, 0, None) == OK
+    assert lib.qws_q4_0_matvec(A, A, A, 0, 3072, 8, 0, None, 0, None) == OK
+    assert lib.qws_matvec(12, A, A, A, 0, 3072, 8, 1, None, 0, None) == OK
+    # Q6_K has no decode-once kernel: 48 * 8 lanes is refused in one pass
+    assert lib.qws_matvec(14, A, A, A, 10, 3072, 8, 1, None, 0, None) == SHAPE
+    # nine vectors: the lane-unit engine, where 48 * 9 = 432 lanes do not fit one pass
+    assert lib.qws_q4_0_matvec(A, A, A, 10, 3072, 9, 1, None, 0, None) == SHAPE
+
+
 def test_splitk_workspace_checks(lib):
     need = lib.qws_workspace_bytes(_lib.OP_MATVEC, 1000, 2560, 0, 1, 5)
     assert need >= 5 * 1000 * 4
@@ -149,6 +162,14 @@ def test_q8_path_checks(lib):
     assert lib.qws_q8_matvec(Q40, A, A, A, 10, 2560, 9, None) == SHAPE      # 40 * 9 > 320
     assert lib.qws_q8_matvec(Q40, A, A, A, -1, 2560, 1, None) == SHAPE
     assert lib.qws_q8_matvec(Q80, A, A, A, 0, 2560, 8, None) == OK
+    # 2..8 vectors at hidden % 256 == 0, <= 3072 take the decode-once kernel,
+    # which has no lane limit: 48 * 8 = 384 lanes is accepted there (zero
+    # rows: no launch), and refused where the lane-unit engine would run
+    assert lib.qws_q8_matvec(Q40, A, A, A, 0, 3072, 8, None) == OK
+    assert lib.qws_q8_matvec(Q80, A, A, A, 0, 3072, 8, None) == OK
+    assert lib.qws_q8_matvec(Q40, A, A, A, 0, 3072 + 64, 8, None) == SHAPE    # not % 256
+    assert lib.qws_q8_matvec(Q40, A, A, A, 0, 3328, 8, None) == SHAPE         # above 3072
+    assert lib.qws_q8_matvec(Q40, A, A, A, 0, 1536, 14, None) == SHAPE        # 9+ vectors: 336
     assert lib.qws_q8_qkv_proj(Q40, A, A, None, A, A, A, A, 2560, 2048, 1024, None) == NULL
     assert lib.qws_q8_qkv_proj(Q4K, A, A, A, A, A, A, A, 2560, 2048, 1024, None) == FORMAT
     assert lib.qws_q8_qkv_proj(Q80, A, A, A, A, A, A, A, 2560, 0, 0, None) == OK
