@@ -289,8 +289,10 @@ qws_status qws_q4k_ffn_gate_up_silu(const void* Wg, const void* Wu, const float*
  *   Arguments, layouts and results as qws_q4k_ffn_gate_up_geglu_down, without
  *   ws / ws_bytes; inter <= QWS_FFN_NOALLOC_MAX_INTER, else QWS_ERR_SHAPE.
  *   Allocates nothing: no cudaMalloc / cudaFree and no allocating library call.
- *   The first call on a device looks up the array's device address (once per
- *   device, with that device current); make that first call before any stream
+ *   Each call looks up the array's device address in the current device's
+ *   context (the lookup allocates nothing, and a context recreated after a
+ *   device reset gets its own address); the first call on a device may load
+ *   the library's module there, so make that first call before any stream
  *   capture.  Every call on a device shares the one array, and m is rewritten
  *   from scratch by each call; calls that overlap on the GPU (streams with no
  *   ordering between them) race on it and must be serialised by the caller.

@@ -313,17 +313,12 @@ cudaError_t launch_kv_append(float* kc, float* vc, const float* k, const float* 
 
 template <int kPL, int kG>
 static cudaError_t launch_split(const AttParams& p, dim3 grid, cudaStream_t st) {
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
+  // set on every launch (cheap): no per-device cache shared between threads
   const size_t smem = static_cast<size_t>(kAttStages) * kAttStageBytes;
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(
-        kv_attention_split_kernel<kPL, kG>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-        static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  const cudaError_t e = cudaFuncSetAttribute(kv_attention_split_kernel<kPL, kG>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+  if (e != cudaSuccess) return e;
   return launch_pdl_att(kv_attention_split_kernel<kPL, kG>, grid, kAttThreads, smem, st, p);
 }
 

@@ -515,17 +515,10 @@ bool batch_q4_eligible(int fmt, int64_t K, int B) {
 
 template <int kFmt>
 static cudaError_t set_smem_attr() {
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(batch_q4_matvec_kernel<kFmt>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(kBmSmemBudget));
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
-  return cudaSuccess;
+  // set on every launch (cheap): no per-device cache shared between threads
+  return cudaFuncSetAttribute(batch_q4_matvec_kernel<kFmt>,
+                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              static_cast<int>(kBmSmemBudget));
 }
 
 cudaError_t launch_batch_q4_matvec(int fmt, const uint8_t* W, const float* x, float* y,

@@ -36,7 +36,6 @@
 
 #include <algorithm>
 #include <cstring>
-#include <mutex>
 
 #include "../../include/qws.h"
 #include "launch.h"
@@ -93,26 +92,27 @@ __device__ __forceinline__ float value_of(Word w) {
   return __uint_as_float(static_cast<unsigned>(w & 0xFFFFFFFFu));
 }
 
-__device__ __forceinline__ unsigned ld_relaxed_u32(const unsigned* p) {
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
   unsigned v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void red_relaxed_add(unsigned* p, unsigned v) {
-  asm volatile("red.relaxed.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
 // Waits (bounded) until every CTA has finished the prologue of phase ph.
-// Relaxed: a CTA counts its prologue only after every value that prologue
-// loaded has been used (a barrier orders the count after those loads), so a
-// write issued once the count is full cannot reach them; and a reader that
-// ever met a newer stamp would time out, not read a wrong value.
+// Release / acquire: a CTA counts its prologue with a release add after a
+// barrier that follows every load of that prologue, and a writer reads the
+// full count with an acquire load before it stores, so by the memory model
+// the prologue's loads cannot observe the later stores (a reader that ever
+// met a newer stamp would time out, not read a wrong value, in any case).
 __device__ __forceinline__ bool wait_prologues(const ChainParams& p, int ph) {
   if (ph < 0) return true;
   const unsigned* c = p.prologues + ph;
-  if (ld_relaxed_u32(c) >= gridDim.x) return true;
+  if (ld_acquire_u32(c) >= gridDim.x) return true;
   const long long t0 = clock64();
-  while (ld_relaxed_u32(c) < gridDim.x) {
+  while (ld_acquire_u32(c) < gridDim.x) {
     if (clock64() - t0 > kWaitCycles) {
       atomicOr(&g_err_chain, kErrGridBarrier);
       return false;
@@ -405,7 +405,7 @@ __device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const 
   unsigned war_seen = gridDim.x;
   if (blockIdx.x == gridDim.x - 1 && (kind == PH_QKV || kind == PH_GU)) {
     const int w = kind == PH_QKV ? 4 * l - 6 : 4 * l - 4;
-    if (w >= 0) war_seen = ld_relaxed_u32(p.prologues + w);
+    if (w >= 0) war_seen = ld_acquire_u32(p.prologues + w);
   }
   // every consumer thread of this CTA is done with R.xs of the previous phase
   bar_sync(kConsumerBar, C);
@@ -455,7 +455,7 @@ __device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const 
   }
   bar_sync(kConsumerBar, C);
   // this CTA has read everything its prologue needed
-  if (ctid == 0) red_relaxed_add(p.prologues + ph, 1u);
+  if (ctid == 0) red_release_add(p.prologues + ph, 1u);
   return ok;
 }
 
@@ -767,19 +767,12 @@ qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
   const bool wide = p.H > 8 * static_cast<int64_t>(kMaxConsumers);
   const void* kfn = wide ? reinterpret_cast<const void*>(chain_kernel<true>)
                          : reinterpret_cast<const void*>(chain_kernel<false>);
-  static std::mutex mu;
-  static int attr_dev[2][64] = {{0}};
+  // set on every launch (cheap next to the chain): nothing cached per device
   int dev = 0;
   cudaGetDevice(&dev);
-  {
-    std::lock_guard<std::mutex> lock(mu);
-    if (dev >= 0 && dev < 64 && !attr_dev[wide][dev]) {
-      int optin = 0;
-      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-      cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-      attr_dev[wide][dev] = 1;
-    }
-  }
+  int optin = 0;
+  cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   int bps = 0;
   cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kfn, threads, smem);
   if (bps < 1) {

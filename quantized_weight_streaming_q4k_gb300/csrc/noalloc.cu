@@ -12,7 +12,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdio>
-#include <mutex>
 #include <string>
 
 #include "../../include/qws.h"
@@ -26,35 +25,19 @@ constexpr int64_t kMaxInter = QWS_FFN_NOALLOC_MAX_INTER;
 // on the GPU (different streams, no ordering between them) race on it.
 static __device__ __align__(256) float g_ffn_scratch[kMaxInter];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-float* g_scratch_addr[kMaxDevices] = {nullptr};
-
-// Device address of g_ffn_scratch on the current device, looked up once per
-// device (with that device current).  In host code the array's name only
-// stands for the symbol; the kernels need the address the runtime reports.
+// Device address of g_ffn_scratch in the current device's context.  In host
+// code the array's name only stands for the symbol; the kernels need the
+// address the runtime reports.  It is looked up on every call (the lookup
+// allocates nothing), so a context that was destroyed and recreated -- after
+// cudaDeviceReset, say -- never leaves a stale address behind.
 qws_status scratch_address(float** out, std::string& err) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    err = std::string("cudaGetDevice: ") + cudaGetErrorString(e);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_ffn_scratch);
+  if (e != cudaSuccess || !p) {
+    err = std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e);
     return QWS_ERR_CUDA;
   }
-  if (dev < 0 || dev >= kMaxDevices) {
-    err = "device index out of range";
-    return QWS_ERR_CUDA;
-  }
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_ffn_scratch);
-    if (e != cudaSuccess || !p) {
-      err = std::string("cudaGetSymbolAddress: ") + cudaGetErrorString(e);
-      return QWS_ERR_CUDA;
-    }
-    g_scratch_addr[dev] = static_cast<float*>(p);
-  }
-  *out = g_scratch_addr[dev];
+  *out = static_cast<float*>(p);
   return QWS_OK;
 }
 

@@ -505,17 +505,16 @@ using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t
                                    CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 static EncodeTiledFn encode_tiled_fn() {
-  static EncodeTiledFn fn = nullptr;
-  static bool tried = false;
-  if (!tried) {
-    tried = true;
+  // a function-local static: initialised once, thread-safe
+  static const EncodeTiledFn fn = []() -> EncodeTiledFn {
     void* ptr = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
                                          &q) == cudaSuccess &&
         q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
+      return reinterpret_cast<EncodeTiledFn>(ptr);
+    return nullptr;
+  }();
   return fn;
 }
 
@@ -552,16 +551,11 @@ static cudaError_t launch_pdl_pf(void (*kernel)(KArgs...), int grid, int threads
 
 template <int kAcc>
 static cudaError_t launch_prefill_kernel(const PrefillParams& p, int grid, cudaStream_t st) {
-  static bool attr_set[64] = {false};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev >= 0 && dev < 64 && !attr_set[dev]) {
-    const cudaError_t e = cudaFuncSetAttribute(prefill_q4k_kernel<kAcc>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(PfCfg<kAcc>::kSmem));
-    if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
-  }
+  // set on every launch (cheap): no per-device cache shared between threads
+  const cudaError_t e = cudaFuncSetAttribute(prefill_q4k_kernel<kAcc>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(PfCfg<kAcc>::kSmem));
+  if (e != cudaSuccess) return e;
   return launch_pdl_pf(prefill_q4k_kernel<kAcc>, grid, kPfThreads, PfCfg<kAcc>::kSmem, st, p);
 }
 

@@ -1,8 +1,14 @@
 """GPU parity of the decode chain (qws_decode_chain) against the oracle.
 
-Layer tolerance (derived in the design doc from the step tolerances): a layer adds
-two branches to h, a = post-attention branch and b = post-FFN branch, each an
-RMS-normalised matvec output.  Per element:
+Layer tolerance, from the step tolerances: a layer adds two branches to h,
+a = post-attention branch and b = post-FFN branch, each an RMS-normalised
+matvec output.  A branch's matvec output carries at most the FFN's 1e-4
+relative error per element (the plain projections' 1e-5 * sum|w x| is
+smaller); the RMS norm divides by rms(.) of the whole vector, so a relative
+error e in every element moves the normalised element by at most e * |a_i|
+plus e * rms(a) through the scale; the input norms feed the next matvec with
+1e-5 relative error, inside the same budget; the two f32 residual adds round
+by 2^-24 (|h| + |a| + |b|) at most.  Per element:
     |h'_gpu - h'_ref| <= 1e-4 * (|h| + |a| + |b|) + 1e-4 * (rms(a) + rms(b))
 checked teacher-forced: the oracle runs each layer on the GPU's input to that
 layer.  One launch over L layers must equal L single-layer launches bit for bit

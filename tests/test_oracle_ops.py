@@ -139,6 +139,27 @@ def test_gelu_tanh_close_to_erf_gelu():
     assert err > 1e-5   # and it is the tanh form, not the erf form itself
 
 
+def test_gelu_tanh_matches_independent_tanh_gelu():
+    # Pins both constants (sqrt(2/pi) and 0.044715) of the tanh form.  The
+    # oracle is compared at 241 points of [-6, 6] (the curved region included)
+    # with two implementations written elsewhere: torch's float64
+    # gelu(approximate="tanh"), and the logistic identity
+    # 0.5 (1 + tanh z) = 1 / (1 + exp(-2 z)) evaluated with Python's math.
+    # The bound is relative to |t| (|gelu(t)| <= |t|): in the negative tail the
+    # output is a difference of nearly equal terms, where libm rounding, not
+    # the constants, sets its relative error.  A change of either constant in
+    # its 4th significant digit moves gelu by > 1e-6 |t| near |t| = 2.
+    torch = pytest.importorskip("torch")
+    ts = np.linspace(-6.0, 6.0, 241)
+    got = oracle.gelu_tanh(ts)
+    ref_torch = torch.nn.functional.gelu(torch.from_numpy(ts), approximate="tanh").numpy()
+    k = math.sqrt(2.0 / math.pi)
+    ref_logistic = np.array([t / (1.0 + math.exp(-2.0 * k * (t + 0.044715 * t ** 3))) for t in ts])
+    scale = np.maximum(np.abs(ts), 1e-300)
+    assert np.max(np.abs(got - ref_torch) / scale) <= 1e-14
+    assert np.max(np.abs(got - ref_logistic) / scale) <= 1e-14
+
+
 def test_gelu_tanh_derivative_at_zero_is_half():
     h = 1e-6
     assert abs((oracle.gelu_tanh(h) - oracle.gelu_tanh(-h)) / (2 * h) - 0.5) < 1e-9

@@ -43,10 +43,15 @@ def test_ffn_noalloc_matches_workspace_entry_point():
         dx = torch.from_numpy(x).cuda()
         y_ws = ops.q4k_ffn_gate_up_geglu_down(dWg, dWu, dWd, ops.Q6_K, dx, H, I)
         y = torch.full((H,), float("nan"), device="cuda")
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
         st = lib.qws_q4k_ffn_gate_up_geglu_down_noalloc(_ptr(dWg), _ptr(dWu), _ptr(dWd),
                                                         ops.Q6_K, _ptr(dx), _ptr(y), H, I, stream)
         assert st == 0, lib.qws_last_error().decode()
         torch.cuda.synchronize()
+        if call > 0:
+            # the module is loaded by now: a call must not take device memory
+            assert torch.cuda.mem_get_info()[0] == free_before, "the no-alloc call allocated"
         a = y.cpu().numpy().astype(np.float64)
         b = y_ws.cpu().numpy().astype(np.float64)
         ref_oracle = oracle.ffn(oracle.Q4_K, Wg, Wu, oracle.Q6_K, Wd, H, I, x)
