@@ -12,11 +12,17 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                         lm_head_q8 (quantize_q8 + Q4_0 x Q8_0 matvec),
                         lm_head_q4_k / lm_head_q6_k (the same 262144 x 2560
                         shape in Q4_K / Q6_K, f32 activations),
-                        ffn (fused gate/up GEGLU + Q6_K down, 2560/10240),
+                        matvec_q4k (Q4_K 2560 x 2560), qkv (fused Q/K/V
+                        4096 x 2560 + O 2560 x 2048), ffn (fused gate/up
+                        GEGLU + Q6_K down, 2560/10240): each back to back
+                        over a ring of weight copies >= 4 x L2 and isolated
+                        after an L2 flush,
                         prefill (Q4_K 10240 x 2560 times --batch tokens on the
                         tensor cores; TFLOP/s),
                         kv_attention (one token over 32768 cached positions,
-                        Gemma-3-4B heads: 8 query, 4 kv, head_dim 256)
+                        Gemma-3-4B heads: 8 query, 4 kv, head_dim 256),
+                        decode_kv (all layers of a decode step over a KV
+                        cache at --pos, default 1024)
 For N > 1 launch with torchrun; every rank runs an independent replica of the
 step on its own GPU (the path has no data exchange; "replicas only").
 """
@@ -434,6 +440,204 @@ def run_gpu(args, world, rank, local):
     print(json.dumps(out))
 
 
+def run_decode_kv(args):
+    """One decode step over a KV cache, all 34 Gemma-3-4B layers at position
+    pos (qws_decode_kv), timed back to back; every step rewrites position pos,
+    so each step does the same work.  Algorithmic bytes: the packed weights
+    of every layer, the norm weights, the K and V rows of positions 0..pos
+    read per layer, plus h in and out."""
+    import torch
+
+    from quantized_weight_streaming_q4k_gb300 import build, ops, synth
+    build.build()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    dims = synth.GEMMA3_4B
+    H, hd, nkv = dims["hidden"], dims["head_dim"], dims["n_kv_heads"]
+    pos, max_seq = args.pos, args.pos + 64
+    n_layers = args.n_layers
+    layers, kcs, vcs = [], [], []
+    for l in range(n_layers):
+        L = synth.chain_layer(l, dims)
+        layers.append({k: (torch.from_numpy(v).to(dev) if isinstance(v, np.ndarray) else v)
+                       for k, v in L.items()})
+        g = synth.rng(synth.W_CHAIN, 500, l)
+        kcs.append(torch.from_numpy((0.5 * g.standard_normal((nkv, max_seq, hd))).astype(
+            np.float32)).to(dev))
+        vcs.append(torch.from_numpy(g.standard_normal((nkv, max_seq, hd)).astype(np.float32)).to(dev))
+    structs = [ops.make_layer(L) for L in layers]
+    h0 = torch.from_numpy(synth.normal_vector(synth.rng(synth.W_CHAIN, 99), H)).to(dev)
+    h = torch.empty_like(h0)
+    ws = torch.empty(ops.decode_kv_workspace_bytes(dims, max_seq), dtype=torch.uint8, device=dev)
+    scale = 1.0 / np.sqrt(hd)
+
+    def call():
+        h.copy_(h0)
+        ops.decode_kv(structs, h, dims, kcs, vcs, max_seq, pos, hd, 10000.0, scale, workspace=ws)
+
+    chain_b, _, _ = algorithmic_bytes(dims, n_layers)
+    kv_b = n_layers * 2 * nkv * (pos + 1) * hd * 4
+    nbytes = chain_b + kv_b
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, args.warmup)):
+        call()
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    props = torch.cuda.get_device_properties(dev)
+    uuid = str(getattr(props, "uuid", "") or "")
+    clocks = ClockSampler((uuid if uuid.startswith("GPU-") else f"GPU-{uuid}") if uuid else "0")
+    clocks.start()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(args.steps):
+        call()
+    b.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert ops.device_error() == 0
+    us = 1e3 * a.elapsed_time(b) / args.steps
+    gbs = nbytes / (us * 1e-6) / 1e9
+    peak, peak_kind = peaks()
+    print(json.dumps({
+        "metric": "decode step with KV cache: us/token and achieved HBM GB/s", "value": gbs,
+        "unit": "GB/s", "n_gpus": 1, "steps": args.steps, "warmup": max(3, args.warmup),
+        "us_per_token": us, "higher_is_better": True, "dtype": "f32",
+        "data": "synthetic (seeded random blocks, random K/V cache contents)",
+        "config": {"workload": f"{n_layers} Gemma-3-4B layers at position {pos} "
+                               f"({pos + 1} cached positions, 4 kv heads of 256), batch 1",
+                   "l2": f"{nbytes / 1e9:.2f} GB streamed per token (> L2)"},
+        "roofline": {"bound": "hbm", "kernel": "decode_kv launch sequence (10 launches/layer)",
+                     "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                     "peak_source": peak_kind, "traffic": None},
+        "bytes_per_token": nbytes, "gpu_launches": (1 + 10 * n_layers) * args.steps,
+        "clocks": clk,
+    }))
+
+
+def run_ring_op(args):
+    """The small per-layer operations (weights smaller than L2), each timed two
+    ways: back to back over a ring of distinct weight copies totalling at least
+    four times the L2 size (so every call streams its weights from HBM), and
+    isolated, one call after an L2 flush (a write of twice the L2 size),
+    median over calls.  Algorithmic bytes: packed weights + activations read
+    + outputs written (+ the FFN's intermediate written and read)."""
+    import torch
+
+    from quantized_weight_streaming_q4k_gb300 import build, ops, synth
+    build.build()
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 126 * 1024 * 1024)
+    H, I = 2560, 10240
+    qd, kd = 8 * 256, 4 * 256
+    if args.batch != 1:
+        raise SystemExit(f"--op {args.op} runs at batch 1")
+    g = synth.rng(synth.W_LM_HEAD, 1)
+    if args.op == "matvec_q4k":
+        mats = [synth.q4_k_matrix(g, H, H)]
+        x = torch.from_numpy(synth.normal_vector(g, H)).to(dev)
+        y = torch.empty(H, device=dev)
+
+        def call(ws):
+            ops.q4k_matvec(ws[0], x, H, H, out=y)
+        launches = 1
+        nbytes = synth.n_blocks(synth.Q4_K, H, H) * 144 + H * 4 + H * 4
+        kernel = "matvec_kernel<UnitQ4K, EpiStore>"
+        workload = f"Q4_K matvec {H}x{H}, batch 1"
+    elif args.op == "qkv":
+        mats = [synth.q4_k_matrix(g, qd, H), synth.q4_k_matrix(g, kd, H),
+                synth.q4_k_matrix(g, kd, H), synth.q4_k_matrix(g, H, qd)]
+        x = torch.from_numpy(synth.normal_vector(g, H)).to(dev)
+        a = torch.from_numpy(synth.normal_vector(g, qd)).to(dev)
+        q = torch.empty(qd, device=dev)
+        k = torch.empty(kd, device=dev)
+        v = torch.empty(kd, device=dev)
+        o = torch.empty(H, device=dev)
+
+        def call(ws):
+            ops.q4k_qkv_proj(ws[0], ws[1], ws[2], x, H, qd, kd, out=(q, k, v))
+            ops.q4k_matvec(ws[3], a, H, qd, out=o)
+        launches = 2
+        nbytes = (synth.n_blocks(synth.Q4_K, qd + 2 * kd, H) * 144 + H * 4 + (qd + 2 * kd) * 4
+                  + synth.n_blocks(synth.Q4_K, H, qd) * 144 + qd * 4 + H * 4)
+        kernel = "matvec_kernel<UnitQ4K, EpiStore> (QKV: three segments in one launch; then O)"
+        workload = (f"fused QKV Q4_K {qd}+{kd}+{kd} x {H} and O projection {H}x{qd}, batch 1")
+    elif args.op == "ffn":
+        gl = synth.rng(synth.W_FFN, 0)
+        mats = [synth.q4_k_matrix(gl, I, H), synth.q4_k_matrix(gl, I, H),
+                synth.q6_k_matrix(gl, H, I)]
+        x = torch.from_numpy(synth.unit_rms_vector(gl, H)).to(dev)
+        y = torch.empty(H, device=dev)
+        wsp = torch.empty(ops.workspace_bytes(ops.OP_FFN, 0, H, I), dtype=torch.uint8, device=dev)
+
+        def call(ws):
+            ops.q4k_ffn_gate_up_geglu_down(ws[0], ws[1], ws[2], ops.Q6_K, x, H, I, workspace=wsp,
+                                           out=y)
+        launches = 2
+        nbytes = (2 * synth.n_blocks(synth.Q4_K, I, H) * 144 + synth.n_blocks(synth.Q6_K, H, I) * 210
+                  + H * 4 + 2 * I * 4 + H * 4)
+        kernel = ("matvec_kernel<UnitQ4K, EpiGeglu> (gate+up) + matvec_kernel<UnitQ6K, EpiStore> "
+                  "(down)")
+        workload = f"fused FFN hidden {H} inter {I}, Q4_K gate/up, GEGLU, Q6_K down, batch 1"
+    else:
+        raise SystemExit(f"unknown --op {args.op}")
+    wbytes = sum(m.nbytes for m in mats)
+    n_copies = max(2, -(-4 * l2 // wbytes))
+    base = [torch.from_numpy(m).to(dev) for m in mats]
+    ring = [base] + [[t.clone() for t in base] for _ in range(n_copies - 1)]
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    for i in range(max(3, args.warmup)):
+        call(ring[i % n_copies])
+    torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    # isolated: one call after an L2 flush, median over calls
+    n_iso = min(200, max(20, args.steps // 10))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(n_iso)]
+    for i, (ea, eb) in enumerate(evs):
+        flush.zero_()
+        ea.record(stream)
+        call(ring[i % n_copies])
+        eb.record(stream)
+    torch.cuda.synchronize()
+    iso_us = statistics.median(1e3 * ea.elapsed_time(eb) for ea, eb in evs)
+    # back to back over the ring
+    uuid = str(getattr(props, "uuid", "") or "")
+    clocks = ClockSampler((uuid if uuid.startswith("GPU-") else f"GPU-{uuid}") if uuid else "0")
+    clocks.start()
+    ta, tb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    ta.record(stream)
+    for i in range(args.steps):
+        call(ring[i % n_copies])
+    tb.record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    assert ops.device_error() == 0
+    us = 1e3 * ta.elapsed_time(tb) / args.steps
+    gbs = nbytes / (us * 1e-6) / 1e9
+    peak, peak_kind = peaks()
+    print(json.dumps({
+        "metric": f"{args.op} achieved HBM GB/s", "value": gbs, "unit": "GB/s", "n_gpus": 1,
+        "steps": args.steps, "warmup": max(3, args.warmup), "us_per_call": us,
+        "higher_is_better": True, "dtype": "f32", "data": "synthetic (seeded random blocks)",
+        "config": {"workload": workload, "batch": 1,
+                   "l2": f"back to back over a ring of {n_copies} distinct weight copies "
+                         f"({n_copies * wbytes / 1e6:.0f} MB >= 4 x L2 of {l2 / 1e6:.0f} MB)"},
+        "roofline": {"bound": "hbm", "kernel": kernel, "achieved": gbs, "peak": peak,
+                     "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_kind,
+                     "traffic": None},
+        "isolated": {"us_per_call": iso_us, "gbs": nbytes / (iso_us * 1e-6) / 1e9,
+                     "frac": nbytes / (iso_us * 1e-6) / 1e9 / peak,
+                     "method": f"one call after a {2 * l2 / 1e6:.0f} MB L2 flush, median of "
+                               f"{n_iso}"},
+        "bytes_per_call": nbytes, "gpu_launches": launches * args.steps, "clocks": clk,
+    }))
+
+
 def run_op(args):
     """One operation timed alone, back to back (weights > L2, so every call
     streams them from HBM).  Algorithmic bytes: packed weights + activations
@@ -524,24 +728,6 @@ def run_op(args):
         flops = 2.0 * rows * H * N
         kernel = "prefill_q4k_kernel (tcgen05 kind::f16) + prefill_pack_x_kernel"
         workload = f"prefill Q4_K {rows}x{H}, {N} tokens"
-    elif args.op == "ffn":
-        gl = synth.rng(synth.W_FFN, 0)
-        Wg = torch.from_numpy(synth.q4_k_matrix(gl, I, H)).to(dev)
-        Wu = torch.from_numpy(synth.q4_k_matrix(gl, I, H)).to(dev)
-        Wd = torch.from_numpy(synth.q6_k_matrix(gl, H, I)).to(dev)
-        x = torch.from_numpy(synth.unit_rms_vector(gl, H)).to(dev)
-        y = torch.empty(H, device=dev)
-        ws = torch.empty(ops.workspace_bytes(ops.OP_FFN, 0, H, I), dtype=torch.uint8, device=dev)
-
-        def call():
-            ops.q4k_ffn_gate_up_geglu_down(Wg, Wu, Wd, ops.Q6_K, x, H, I, workspace=ws, out=y)
-        launches = 2
-        nbytes = (2 * synth.n_blocks(synth.Q4_K, I, H) * 144 + synth.n_blocks(synth.Q6_K, H, I) * 210
-                  + H * 4 + 2 * I * 4 + H * 4)
-        kernel = "gate/up GEGLU + down (two streaming launches)"
-        workload = f"fused FFN hidden {H} inter {I}, Q4_K gate/up, Q6_K down, batch 1"
-        if B != 1:
-            raise SystemExit("--op ffn runs at batch 1")
     else:
         raise SystemExit(f"unknown --op {args.op}")
     stream = torch.cuda.current_stream()
@@ -605,10 +791,19 @@ def main():
                     help="chain length (default 34; shorter only for profiler captures)")
     ap.add_argument("--op", default="step",
                     choices=["step", "lm_head_q4_0", "lm_head_q8", "lm_head_q4_k",
-                             "lm_head_q6_k", "ffn", "prefill", "kv_attention"],
+                             "lm_head_q6_k", "matvec_q4k", "qkv", "ffn", "prefill",
+                             "kv_attention", "decode_kv"],
                     help="step (default): the decode step; otherwise one operation alone")
     ap.add_argument("--batch", type=int, default=1, help="activation vectors (--op only)")
+    ap.add_argument("--pos", type=int, default=1024,
+                    help="--op decode_kv: position of the token (pos cached positions before it)")
     args = ap.parse_args()
+    if args.op in ("matvec_q4k", "qkv", "ffn"):
+        run_ring_op(args)
+        return
+    if args.op == "decode_kv":
+        run_decode_kv(args)
+        return
     if args.op != "step":
         run_op(args)
         return

@@ -360,6 +360,47 @@ qws_status qws_decode_chain(const qws_layer* layers, int n_layers, float* h,
                             const qws_dims* dims, void* ws, size_t ws_bytes, qws_stream stream);
 
 /* ------------------------------------------------------------------------
+ * One decode step at sequence position pos with a KV cache (infer-compute
+ * README §Architecture: decode is norm -> QKV -> attend -> O -> FFN per layer;
+ * §Shaders rows "RoPE" rope_at_pos and "Attention" kv_append, kv_attention;
+ * infer-compute §Quick Start decode_token(..., rope_base)).  Per layer, the
+ * layer of qws_decode_chain with the sequence-1 broadcast replaced by real
+ * attention:
+ *   n = rms_norm(h, w_in); [q|k|v] = W n; q, k <- RoPE at pos (the first
+ *   rot_dim dimensions of every head, half-split pairs, base rope_base);
+ *   caches[l][pos] <- k, v; a = attention of q over positions 0..pos (scale
+ *   attn_scale, optional softcap, query head h reads kv head h / (n_q / n_kv));
+ *   o = Wo a; then the residuals and norms of qws_decode_chain (sandwich norms
+ *   when dims->post_norms) and the GEGLU FFN.
+ *   h [hidden] f32 device, in: the token's input, out: the last layer's output.
+ *   kv->k_caches[l], kv->v_caches[l]: device pointers (an array of n_layers on
+ *   the host) to f32 [n_kv_heads][max_seq][head_dim], 16-byte aligned,
+ *   caller-owned; positions 0..pos-1 are read, position pos is written.
+ *   ws: device, >= qws_decode_kv_workspace_bytes(dims, max_seq) bytes,
+ *   16-byte aligned; on return it holds, for the last layer, q and k (after
+ *   RoPE) then v at float offset 0 (contiguous: n_q_heads*head_dim, then
+ *   n_kv_heads*head_dim twice).
+ *   Shapes: as qws_decode_chain; head_dim in {32, 64, 128, 256};
+ *   n_q_heads / n_kv_heads in 1..4; 0 <= pos < max_seq; rot_dim even in
+ *   (0, head_dim]; rope_base > 0; attn_scale finite; softcap >= 0 (0 = off).
+ *   Asynchronous on stream; errors as above, nothing enqueued on an error.
+ * ---------------------------------------------------------------------- */
+typedef struct {
+  float* const* k_caches;
+  float* const* v_caches;
+  int64_t max_seq;
+  int64_t pos;
+  int rot_dim;
+  double rope_base;
+  float attn_scale;
+  float softcap;
+} qws_kv;
+
+size_t qws_decode_kv_workspace_bytes(const qws_dims* dims, int64_t max_seq);
+qws_status qws_decode_kv(const qws_layer* layers, int n_layers, float* h, const qws_dims* dims,
+                         const qws_kv* kv, void* ws, size_t ws_bytes, qws_stream stream);
+
+/* ------------------------------------------------------------------------
  * Bookkeeping.
  * qws_workspace_bytes: bytes of workspace an op needs (0 if none); for
  *   QWS_OP_MATVEC pass the split count in split_k (0 = the library's choice).
@@ -374,6 +415,24 @@ qws_status qws_decode_chain(const qws_layer* layers, int n_layers, float* h,
  * ---------------------------------------------------------------------- */
 size_t qws_workspace_bytes(qws_op op, int64_t rows, int64_t hidden, int64_t inter, int batch,
                            int split_k);
+
+/* ------------------------------------------------------------------------
+ * Self-test of the failure path (no counterpart on the pages; the pages'
+ * checked buffer access, infer-compute README §Safe Buffer Access, is the
+ * convention this extends to device-side waits).  Runs one of the library's
+ * bounded wait primitives on something that never becomes ready, with a wait
+ * limit of limit_cycles clock cycles instead of the kernels' ~1 s default:
+ *   kind 0: the streaming engine's mbarrier wait, on a barrier that no thread
+ *           and no copy ever completes;
+ *   kind 1: the decode chain's stamped-word poll, on the 8-byte word at word8
+ *           (device memory, 8-byte aligned, caller-owned; the call clears it
+ *           first, so its stamp never matches).
+ * The wait gives up, records code 1 (a consumer gave up waiting for data) for
+ * qws_device_error() and the kernel returns; nothing else is in flight, so
+ * the context stays usable.  limit_cycles in [1, ~2e9]; errors as above.
+ * ---------------------------------------------------------------------- */
+qws_status qws_selftest_wait_timeout(int kind, long long limit_cycles, void* word8,
+                                     qws_stream stream);
 const char* qws_last_error(void);
 qws_status qws_device_error(unsigned* code);
 const char* qws_version(void);

@@ -437,6 +437,67 @@ def layer_forward(layer: dict, dims: dict, h, trace: bool = False):
     return (out, tr) if trace else out
 
 
+class _KV(C.Structure):
+    _fields_ = [("k_cache", C.c_void_p), ("v_cache", C.c_void_p), ("max_seq", C.c_int64),
+                ("pos", C.c_int64), ("rot_dim", C.c_int), ("rope_base", C.c_double),
+                ("scale", C.c_double), ("softcap", C.c_double)]
+
+
+def layer_forward_kv(layer: dict, dims: dict, kv: dict, h, trace: bool = False):
+    """One decoder layer at position kv["pos"] with a KV cache (see
+    qo_layer_forward_kv in oracle.c).  ``kv`` holds k_cache and v_cache (f64
+    arrays [n_kv_heads, max_seq, head_dim], updated in place at pos), max_seq,
+    pos, rot_dim, rope_base, scale and softcap.  Returns h_out, or
+    (h_out, trace_dict) when ``trace`` is true (q and k after the rotation)."""
+    keep = []
+
+    def u8(a):
+        a = _u8(a)
+        keep.append(a)
+        return _ptr(a)
+
+    def f64(a):
+        a = _f64(a).reshape(-1)
+        keep.append(a)
+        return _ptr(a)
+
+    for name in ("k_cache", "v_cache"):
+        arr = kv[name]
+        if not (isinstance(arr, np.ndarray) and arr.dtype == np.float64 and arr.flags.c_contiguous):
+            raise TypeError(f"kv[{name!r}] must be a C-contiguous float64 array (updated in place)")
+    L = _Layer(layer["fmt_qkv"], layer["fmt_o"], layer["fmt_gu"], layer["fmt_down"],
+               u8(layer["Wq"]), u8(layer["Wk"]), u8(layer["Wv"]), u8(layer["Wo"]),
+               u8(layer["Wg"]), u8(layer["Wu"]), u8(layer["Wd"]),
+               f64(layer["w_in"]), f64(layer["w_post_attn"]), f64(layer["w_pre_ffn"]),
+               f64(layer["w_post_ffn"]))
+    D = _Dims(dims["hidden"], dims["inter"], dims["n_q_heads"], dims["n_kv_heads"],
+              dims["head_dim"], float(dims["eps"]), int(dims["post_norms"]))
+    K = _KV(_ptr(kv["k_cache"]), _ptr(kv["v_cache"]), int(kv["max_seq"]), int(kv["pos"]),
+            int(kv["rot_dim"]), float(kv["rope_base"]), float(kv["scale"]),
+            float(kv.get("softcap", 0.0)))
+    H, I = dims["hidden"], dims["inter"]
+    qd = dims["n_q_heads"] * dims["head_dim"]
+    kd = dims["n_kv_heads"] * dims["head_dim"]
+    assert kv["k_cache"].size == dims["n_kv_heads"] * int(kv["max_seq"]) * dims["head_dim"]
+    assert kv["v_cache"].size == kv["k_cache"].size
+    hs = _f64(h).reshape(-1)
+    assert hs.size == H
+    out = np.empty(H)
+    tr = None
+    tptr = None
+    if trace:
+        sizes = dict(n1=H, q=qd, k=kd, v=kd, attn=qd, o=H, h1=H, n2=H, g=I, u=I, m=I, f=H,
+                     bound_f=H)
+        tr = {k: np.empty(sizes[k]) for k in _TRACE_FIELDS}
+        T = _Trace(*[_ptr(tr[k]) for k in _TRACE_FIELDS])
+        tptr = C.pointer(T)
+    rc = _load().qo_layer_forward_kv(C.pointer(L), C.pointer(D), C.pointer(K), _ptr(hs),
+                                     _ptr(out), tptr)
+    if rc:
+        raise ValueError(f"qo_layer_forward_kv failed ({rc})")
+    return (out, tr) if trace else out
+
+
 def topk(v, k: int) -> np.ndarray:
     vs = _f64(v).reshape(-1)
     idx = np.empty(k, dtype=np.int64)

@@ -698,6 +698,96 @@ int qo_layer_forward(const qo_layer *L, const qo_dims *D, const double *h, doubl
 }
 
 /* ---------------------------------------------------------------------------
+ * One decoder layer at sequence position pos with a KV cache ([compute]
+ * §Architecture decode: norm -> QKV -> attend -> O -> FFN, and §Shaders rows
+ * "RoPE" (rope_at_pos) and "Attention" (kv_append, kv_attention); [engine]
+ * §BLAS-Fused Attention).  The same steps as qo_layer_forward with the
+ * attention of a real decode step in place of the sequence-1 broadcast:
+ *   n1 = rms_norm(h, w_in)
+ *   q, k, v = Wq n1, Wk n1, Wv n1
+ *   q <- rope(q, pos), k <- rope(k, pos)        (qo_rope, rot_dim, base)
+ *   caches[pos] <- k, v                          (qo_kv_append)
+ *   a  = attention of q over positions 0..pos    (qo_kv_attention, scale,
+ *                                                 softcap)
+ *   o  = Wo a, then the post-attention part of qo_layer_forward unchanged.
+ * At pos = 0 the rotation angle is 0 (q and k unchanged) and the softmax is
+ * over one key (weight exactly 1), so the result equals qo_layer_forward's.
+ * The caches are [n_kv_heads][max_seq][head_dim] and are updated in place.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+    double *k_cache, *v_cache;
+    int64_t max_seq, pos;
+    int rot_dim;
+    double rope_base, scale, softcap;
+} qo_kv;
+
+int qo_layer_forward_kv(const qo_layer *L, const qo_dims *D, qo_kv *KV, const double *h,
+                        double *h_out, qo_trace *T)
+{
+    int64_t H = D->hidden, I = D->inter;
+    int64_t qd = (int64_t)D->n_q_heads * D->head_dim;
+    int64_t kd = (int64_t)D->n_kv_heads * D->head_dim;
+    if (KV->pos < 0 || KV->pos >= KV->max_seq) return -1;
+    size_t need = (size_t)(H * 6 + qd * 2 + kd * 2 + I * 3);
+    double *buf = (double *)malloc(sizeof(double) * need);
+    if (!buf) return -2;
+    double *n1 = buf, *q = n1 + H, *k = q + qd, *v = k + kd, *a = v + kd, *o = a + qd;
+    double *h1 = o + H, *n2 = h1 + H, *t = n2 + H, *f = t + H;
+    double *g = f + H, *u = g + I, *m = u + I;
+    int rc;
+
+    qo_rms_norm(h, L->w_in, H, D->eps, n1);
+    rc = qo_matvec(L->fmt_qkv, L->Wq, qd, H, n1, 1, 0, qd, q, NULL);
+    if (!rc) rc = qo_matvec(L->fmt_qkv, L->Wk, kd, H, n1, 1, 0, kd, k, NULL);
+    if (!rc) rc = qo_matvec(L->fmt_qkv, L->Wv, kd, H, n1, 1, 0, kd, v, NULL);
+    if (!rc) rc = qo_rope(q, D->n_q_heads, D->head_dim, KV->rot_dim, KV->pos, KV->rope_base);
+    if (!rc) rc = qo_rope(k, D->n_kv_heads, D->head_dim, KV->rot_dim, KV->pos, KV->rope_base);
+    if (!rc) rc = qo_kv_append(KV->k_cache, KV->v_cache, k, v, D->n_kv_heads, D->head_dim,
+                               KV->max_seq, KV->pos);
+    if (!rc) rc = qo_kv_attention(q, KV->k_cache, KV->v_cache, D->n_q_heads, D->n_kv_heads,
+                                  D->head_dim, KV->max_seq, KV->pos + 1, KV->scale, KV->softcap,
+                                  a, NULL, NULL);
+    if (!rc) rc = qo_matvec(L->fmt_o, L->Wo, H, qd, a, 1, 0, H, o, NULL);
+    if (rc) { free(buf); return rc; }
+
+    memcpy(h1, h, sizeof(double) * (size_t)H);
+    if (D->post_norms) {
+        qo_rms_norm(o, L->w_post_attn, H, D->eps, t);
+        qo_residual_add(h1, t, H);
+    } else {
+        qo_residual_add(h1, o, H);
+    }
+    qo_rms_norm(h1, L->w_pre_ffn, H, D->eps, n2);
+    rc = qo_ffn(L->fmt_gu, L->Wg, L->Wu, L->fmt_down, L->Wd, H, I, n2, g, u, m, f,
+                T ? T->bound_f : NULL);
+    if (rc) { free(buf); return rc; }
+    memcpy(h_out, h1, sizeof(double) * (size_t)H);
+    if (D->post_norms) {
+        qo_rms_norm(f, L->w_post_ffn, H, D->eps, t);
+        qo_residual_add(h_out, t, H);
+    } else {
+        qo_residual_add(h_out, f, H);
+    }
+
+    if (T) {
+        if (T->n1) memcpy(T->n1, n1, sizeof(double) * (size_t)H);
+        if (T->q) memcpy(T->q, q, sizeof(double) * (size_t)qd);
+        if (T->k) memcpy(T->k, k, sizeof(double) * (size_t)kd);
+        if (T->v) memcpy(T->v, v, sizeof(double) * (size_t)kd);
+        if (T->attn) memcpy(T->attn, a, sizeof(double) * (size_t)qd);
+        if (T->o) memcpy(T->o, o, sizeof(double) * (size_t)H);
+        if (T->h1) memcpy(T->h1, h1, sizeof(double) * (size_t)H);
+        if (T->n2) memcpy(T->n2, n2, sizeof(double) * (size_t)H);
+        if (T->g) memcpy(T->g, g, sizeof(double) * (size_t)I);
+        if (T->u) memcpy(T->u, u, sizeof(double) * (size_t)I);
+        if (T->m) memcpy(T->m, m, sizeof(double) * (size_t)I);
+        if (T->f) memcpy(T->f, f, sizeof(double) * (size_t)H);
+    }
+    free(buf);
+    return 0;
+}
+
+/* ---------------------------------------------------------------------------
  * Top-k indices of v by value, descending; equal values keep the lower index
  * first ([perf] §Production Benchmark "top 5" predictions).  Plain repeated
  * selection: k passes over v.

@@ -38,6 +38,14 @@ class QwsDims(C.Structure):
     ]
 
 
+class QwsKv(C.Structure):
+    _fields_ = [
+        ("k_caches", C.c_void_p), ("v_caches", C.c_void_p), ("max_seq", C.c_int64),
+        ("pos", C.c_int64), ("rot_dim", C.c_int), ("rope_base", C.c_double),
+        ("attn_scale", C.c_float), ("softcap", C.c_float),
+    ]
+
+
 # name -> (restype, argtypes); mirrors include/qws.h
 P, F, I64, I, SZ, U = C.c_void_p, C.c_void_p, C.c_int64, C.c_int, C.c_size_t, C.c_uint
 SIGNATURES = {
@@ -68,6 +76,10 @@ SIGNATURES = {
     "qws_last_error": (C.c_char_p, []),
     "qws_device_error": (I, [C.POINTER(U)]),
     "qws_version": (C.c_char_p, []),
+    "qws_selftest_wait_timeout": (I, [C.c_int, C.c_longlong, C.c_void_p, C.c_void_p]),
+    "qws_decode_kv_workspace_bytes": (SZ, [C.POINTER(QwsDims), I64]),
+    "qws_decode_kv": (I, [C.POINTER(QwsLayer), I, F, C.POINTER(QwsDims), C.POINTER(QwsKv), P,
+                          SZ, P]),
 }
 
 _lib = None

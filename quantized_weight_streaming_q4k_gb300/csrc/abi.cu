@@ -586,6 +586,35 @@ qws_status qws_device_error(unsigned* code) {
   return *code ? fail(QWS_ERR_TIMEOUT, "device error code 0x%x", *code) : ok();
 }
 
+size_t qws_decode_kv_workspace_bytes(const qws_dims* dims, int64_t max_seq) {
+  return qws::decode_kv_workspace_bytes(dims, max_seq);
+}
+
+qws_status qws_decode_kv(const qws_layer* layers, int n_layers, float* h, const qws_dims* dims,
+                         const qws_kv* kv, void* ws, size_t ws_bytes, qws_stream stream) {
+  std::string err;
+  const qws_status st = qws::decode_kv(layers, n_layers, h, dims, kv, ws, ws_bytes,
+                                       reinterpret_cast<cudaStream_t>(stream), err);
+  if (st != QWS_OK) return fail(st, "%s", err.c_str());
+  return ok();
+}
+
+qws_status qws_selftest_wait_timeout(int kind, long long limit_cycles, void* word8,
+                                     qws_stream stream) {
+  const char* fn = "qws_selftest_wait_timeout";
+  if (kind != 0 && kind != 1) return fail(QWS_ERR_SHAPE, "%s: kind must be 0 or 1", fn);
+  if (limit_cycles < 1 || limit_cycles > qws::kWaitCycles)
+    return fail(QWS_ERR_SHAPE, "%s: limit_cycles must be in [1, %lld]", fn, qws::kWaitCycles);
+  if (kind == 1 && !word8) return fail(QWS_ERR_NULL, "%s: word8 is NULL", fn);
+  if (kind == 1 && reinterpret_cast<uintptr_t>(word8) % 8)
+    return fail(QWS_ERR_ALIGN, "%s: word8 must be 8-byte aligned", fn);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const cudaError_t e = kind == 0 ? qws::launch_selftest_mbar(limit_cycles, s)
+                                  : qws::launch_selftest_poll(word8, limit_cycles, s);
+  if (e != cudaSuccess) return cuda_fail(e, fn, "");
+  return ok();
+}
+
 const char* qws_version(void) { return "qws 0.1.0 (sm_103a)"; }
 
 }  // extern "C"

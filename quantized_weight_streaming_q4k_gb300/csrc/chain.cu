@@ -92,15 +92,6 @@ __device__ __forceinline__ float value_of(Word w) {
   return __uint_as_float(static_cast<unsigned>(w & 0xFFFFFFFFu));
 }
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
-  unsigned v;
-  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
-__device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
-  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 // Waits (bounded) until every CTA has finished the prologue of phase ph.
 // Release / acquire: a CTA counts its prologue with a release add after a
 // barrier that follows every load of that prologue, and a writer reads the
@@ -110,9 +101,9 @@ __device__ __forceinline__ void red_release_add(unsigned* p, unsigned v) {
 __device__ __forceinline__ bool wait_prologues(const ChainParams& p, int ph) {
   if (ph < 0) return true;
   const unsigned* c = p.prologues + ph;
-  if (ld_acquire_u32(c) >= gridDim.x) return true;
+  if (ld_acquire_gpu(c) >= gridDim.x) return true;
   const long long t0 = clock64();
-  while (ld_acquire_u32(c) < gridDim.x) {
+  while (ld_acquire_gpu(c) < gridDim.x) {
     if (clock64() - t0 > kWaitCycles) {
       atomicOr(&g_err_chain, kErrGridBarrier);
       return false;
@@ -205,7 +196,7 @@ constexpr int kC = kMaxConsumers;   // the chain always runs this many consumer 
 // ready.  Bounded: returns false (error bit set) on timeout.
 template <int kJ, class Put>
 __device__ __forceinline__ bool poll_stamped(const Word* b, const Word* end, unsigned want,
-                                             Put&& put) {
+                                             Put&& put, long long limit = kWaitCycles) {
   unsigned pending = 0;
 #pragma unroll
   for (int j = 0; j < kJ; ++j)
@@ -227,7 +218,7 @@ __device__ __forceinline__ bool poll_stamped(const Word* b, const Word* end, uns
     if (first) {
       t0 = clock64();
       first = false;
-    } else if (clock64() - t0 > kWaitCycles) {
+    } else if (clock64() - t0 > limit) {
       atomicOr(&g_err_chain, kErrFullWait);
       return false;
     }
@@ -343,6 +334,9 @@ template <int kJ>
 __device__ __forceinline__ bool stage_gather(const Ring& R, int US, const Word* v, unsigned want,
                                              int64_t n, int hd, int group, int ctid) {
   bool ok = true;
+  // 32-bit index arithmetic (n <= 4 * 20480): the 64-bit division it replaces
+  // is a long software sequence on the boundary's critical path
+  const unsigned uhd = static_cast<unsigned>(hd), ugroup = static_cast<unsigned>(group);
   for (int64_t b0 = ctid; b0 < n; b0 += static_cast<int64_t>(kJ) * kC) {
     unsigned pending = 0;
     const Word* at[kJ];
@@ -351,8 +345,9 @@ __device__ __forceinline__ bool stage_gather(const Ring& R, int US, const Word* 
       const int64_t i = b0 + static_cast<int64_t>(j) * kC;
       at[j] = v;
       if (i < n) {
-        const int64_t head = i / hd;
-        at[j] = v + (head / group) * hd + (i - head * hd);
+        const unsigned ui = static_cast<unsigned>(i);
+        const unsigned head = ui / uhd;
+        at[j] = v + (head / ugroup) * uhd + (ui - head * uhd);
         pending |= 1u << j;
       }
     }
@@ -405,7 +400,7 @@ __device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const 
   unsigned war_seen = gridDim.x;
   if (blockIdx.x == gridDim.x - 1 && (kind == PH_QKV || kind == PH_GU)) {
     const int w = kind == PH_QKV ? 4 * l - 6 : 4 * l - 4;
-    if (w >= 0) war_seen = ld_acquire_u32(p.prologues + w);
+    if (w >= 0) war_seen = ld_acquire_gpu(p.prologues + w);
   }
   // every consumer thread of this CTA is done with R.xs of the previous phase
   bar_sync(kConsumerBar, C);
@@ -455,7 +450,7 @@ __device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const 
   }
   bar_sync(kConsumerBar, C);
   // this CTA has read everything its prologue needed
-  if (ctid == 0) red_release_add(p.prologues + ph, 1u);
+  if (ctid == 0) red_release_gpu_add(p.prologues + ph, 1u);
   return ok;
 }
 
@@ -604,6 +599,24 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
     else
       chain_final<8>(p, wsum, ctid, C);
   }
+}
+
+// Self-test of the failure path: the chain's stamped-word poll on a word
+// whose stamp nothing ever writes (the word is cleared by the host first), with
+// the given wait limit.  The poll gives up, records kErrFullWait and the
+// kernel returns; nothing else is in flight.
+__global__ void selftest_poll_kernel(const Word* word, long long limit) {
+  if (threadIdx.x != 0) return;
+  float sink = 0.f;
+  poll_stamped<1>(word, word + 1, 1u, [&](int, float v) { sink = v; }, limit);
+  if (sink != 0.f) atomicOr(&g_err_chain, 0u);   // keeps the poll's result live
+}
+
+cudaError_t launch_selftest_poll(void* word8, long long limit, cudaStream_t st) {
+  cudaError_t e = cudaMemsetAsync(word8, 0, sizeof(Word), st);
+  if (e != cudaSuccess) return e;
+  selftest_poll_kernel<<<1, 32, 0, st>>>(static_cast<const Word*>(word8), limit);
+  return cudaGetLastError();
 }
 
 // ------------------------------------------------------------------ host side

@@ -62,25 +62,116 @@ __device__ __forceinline__ void nibble_word(uint32_t w, const float* xl, const f
 }
 
 // ---------------------------------------------------------------------------
+// Byte split: both nibbles of a byte from one mask and two FP operations.
+// A byte b = lo + 16 hi masked in place at bit p (p <= 16; the top byte is
+// shifted down to p = 0 first) is the float B = b * 2^(p-149).  Multiplying
+// by 2^(-p-4) with round-toward-zero lands on the subnormal grid 2^-149 and
+// drops the low nibble: H = hi * 2^-149 exactly; then L = B - 16 * 2^p * H =
+// lo * 2^(p-149) exactly (an FMA whose result is representable).  So H takes
+// activations pre-scaled by 2^kE and L by 2^(kE - p), and both products are
+// q * x * 2^-60 as for the in-place masks.  One integer operation per two
+// weights instead of two: the work moves to the FMA pipe, which the in-place
+// decode leaves mostly idle.  (mul.rz / fma on f32 keep subnormals: no .ftz.)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mul2_rz(float& d0, float& d1, float a0, float a1, float b0,
+                                        float b1) {
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%2, %3};\n\t"
+      "mov.b64 rb, {%4, %5};\n\t"
+      "mul.rz.f32x2 rc, ra, rb;\n\t"
+      "mov.b64 {%0, %1}, rc;\n\t}"
+      : "=f"(d0), "=f"(d1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// Bit position of byte b (0..3) of a word in the byte split: bytes 0..2 in
+// place, byte 3 shifted down to 0.
+__host__ __device__ constexpr int split_pos(int b) { return b == 3 ? 0 : 8 * b; }
+
+// lo[0..3] += low nibbles of bytes 0..3 times xl[0..3], hi likewise with xh;
+// xl[b] pre-scaled by 2^(kE - split_pos(b)), xh by 2^kE.
+__device__ __forceinline__ void nibble_word_split(uint32_t w, const float* xl, const float* xh,
+                                                  float& l0, float& l1, float& h0, float& h1) {
+  const float B0 = bits(w & 0xFFu), B3 = bits(w >> 24);          // p = 0, 0
+  const float B1 = bits(w & 0xFF00u), B2 = bits(w & 0xFF0000u);  // p = 8, 16
+  float H0, H3, H1, H2;
+  mul2_rz(H0, H3, B0, B3, exp2i(-4), exp2i(-4));
+  mul2_rz(H1, H2, B1, B2, exp2i(-12), exp2i(-20));
+  float L0 = B0, L3 = B3, L1 = B1, L2 = B2;
+  fma2(L0, L3, H0, H3, -16.f, -16.f);
+  fma2(L1, L2, H1, H2, -4096.f, -1048576.f);
+  fma2(l0, l1, L0, L3, xl[0], xl[3]);
+  fma2(l0, l1, L1, L2, xl[1], xl[2]);
+  fma2(h0, h1, H0, H3, xh[0], xh[3]);
+  fma2(h0, h1, H1, H2, xh[1], xh[2]);
+}
+
+// Which of the eight words of a 32-byte Q4_K chunk take the byte split (bit
+// k set: word k), the rest the in-place masks: a mix keeps both the integer
+// and the FMA pipe busy.
+constexpr unsigned kQ4kSplitWords = 0x55u;
+
+__host__ __device__ constexpr bool q4k_word_split(int k) { return (kQ4kSplitWords >> k) & 1u; }
+
+// Pre-scale exponents of the activations of chunk byte l (0..31): xa for the
+// low nibble (sub-block 2c), xb for the high nibble (sub-block 2c+1).
+__host__ __device__ constexpr int q4k_xa_exp(int l) {
+  return q4k_word_split(l >> 2) ? kE - split_pos(l & 3) : kE - pos_lo(l & 3);
+}
+__host__ __device__ constexpr int q4k_xb_exp(int l) {
+  return q4k_word_split(l >> 2) ? kE : kE - pos_hi(l & 3);
+}
+
+// Exponents of the activation pre-scale for byte b of a full nibble word,
+// decoded in place (kSplit false) or by the byte split.
+template <bool kSplit>
+__host__ __device__ constexpr int lo_exp(int b) {
+  return kSplit ? kE - split_pos(b) : kE - pos_lo(b);
+}
+template <bool kSplit>
+__host__ __device__ constexpr int hi_exp(int b) {
+  return kSplit ? kE : kE - pos_hi(b);
+}
+
+template <bool kSplit>
+__device__ __forceinline__ void nib_word(uint32_t w, const float* xl, const float* xh, float& l0,
+                                         float& l1, float& h0, float& h1) {
+  if constexpr (kSplit)
+    nibble_word_split(w, xl, xh, l0, l1, h0, h1);
+  else
+    nibble_word(w, xl, xh, l0, l1, h0, h1);
+}
+
+template <int k>
+__device__ __forceinline__ void q4k_word(uint32_t w, const float* xa, const float* xb, float& a0,
+                                         float& a1, float& b0, float& b1) {
+  if constexpr (q4k_word_split(k))
+    nibble_word_split(w, xa + 4 * k, xb + 4 * k, a0, a1, b0, b1);
+  else
+    nibble_word(w, xa + 4 * k, xb + 4 * k, a0, a1, b0, b1);
+}
+
+// ---------------------------------------------------------------------------
 // Q4_K.  Unit u -> super-block kb = u/4, chunk c = u%4: the 32 qs bytes
 // qs[32c .. 32c+31] (weights 64c+l of sub-block 2c in the low nibbles and
 // 64c+32+l of sub-block 2c+1 in the high nibbles) plus the block header.
 // ---------------------------------------------------------------------------
 // Dot product of one Q4_K chunk (32 bytes: 32 low nibbles of sub-block 2c,
-// 32 high nibbles of sub-block 2c+1) with the pre-scaled activations xa / xb;
-// hd is the block header, sh/hi select the chunk's scale pair.
+// 32 high nibbles of sub-block 2c+1) with the pre-scaled activations xa / xb
+// (q4k_xa_exp / q4k_xb_exp); hd is the block header, sh/hi select the chunk's
+// scale pair.
 __device__ __forceinline__ float q4k_chunk_dot(const uint4 hd, const uint4 q0, const uint4 q1,
                                                const float* xa, const float* xb, float sxa,
                                                float sxb, uint32_t sh, bool hi) {
   float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
-  nibble_word(q0.x, xa + 0, xb + 0, a0, a1, b0, b1);
-  nibble_word(q0.y, xa + 4, xb + 4, a0, a1, b0, b1);
-  nibble_word(q0.z, xa + 8, xb + 8, a0, a1, b0, b1);
-  nibble_word(q0.w, xa + 12, xb + 12, a0, a1, b0, b1);
-  nibble_word(q1.x, xa + 16, xb + 16, a0, a1, b0, b1);
-  nibble_word(q1.y, xa + 20, xb + 20, a0, a1, b0, b1);
-  nibble_word(q1.z, xa + 24, xb + 24, a0, a1, b0, b1);
-  nibble_word(q1.w, xa + 28, xb + 28, a0, a1, b0, b1);
+  q4k_word<0>(q0.x, xa, xb, a0, a1, b0, b1);
+  q4k_word<1>(q0.y, xa, xb, a0, a1, b0, b1);
+  q4k_word<2>(q0.z, xa, xb, a0, a1, b0, b1);
+  q4k_word<3>(q0.w, xa, xb, a0, a1, b0, b1);
+  q4k_word<4>(q1.x, xa, xb, a0, a1, b0, b1);
+  q4k_word<5>(q1.y, xa, xb, a0, a1, b0, b1);
+  q4k_word<6>(q1.z, xa, xb, a0, a1, b0, b1);
+  q4k_word<7>(q1.w, xa, xb, a0, a1, b0, b1);
   // 6-bit scales / mins of all eight sub-blocks, one per byte:
   //   s < 4 : sc[s] & 63 and sc[s+4] & 63
   //   s >= 4: (sc[s+4] & 15) | (sc[s-4] >> 6) << 4  and
@@ -135,8 +226,8 @@ struct UnitQ4K {
       const float va = xu(l), vb = xu(32 + l);
       sa += va;
       sb += vb;
-      xa[l] = va * exp2i(kE - pos_lo(l & 3));
-      xb[l] = vb * exp2i(kE - pos_hi(l & 3));
+      xa[l] = va * exp2i(q4k_xa_exp(l));
+      xb[l] = vb * exp2i(q4k_xb_exp(l));
     }
     sxa = sa;
     sxb = sb;
@@ -198,7 +289,7 @@ __device__ __forceinline__ void load16_a2(const uint8_t* p, uint32_t (&w)[4]) {
 
 // Dot product of one 64-column Q6_K unit (16 bytes of each of the two ql runs,
 // 16 bytes of qh, the 8 scale bytes of the half) with activations x[16a + i]
-// pre-scaled by 2^(kE - pos); sx32[a] carries the -32 offset.
+// pre-scaled by 2^kE; sx32[a] carries the -32 offset.
 __device__ __forceinline__ float q6k_unit_dot(const uint32_t (&A)[4], const uint32_t (&B)[4],
                                               const uint32_t (&Q)[4], uint32_t S0, uint32_t S1,
                                               uint32_t dbits, const float* x, const float* sx32,
@@ -220,10 +311,18 @@ __device__ __forceinline__ float q6k_unit_dot(const uint32_t (&A)[4], const uint
     const uint32_t vv[4] = {v0, v1, v2, v3};
 #pragma unroll
     for (int a = 0; a < 4; ++a) {
+      // two 6-bit fields per 16-bit half (bits 0-5 and 8-13 after the mask),
+      // split like the nibbles of a byte: H = upper field, L = lower field,
+      // both on the 2^-149 grid (activations pre-scaled by 2^kE)
       const uint32_t v = vv[a];
+      const float P0 = bits(v & 0x3F3Fu), P1 = bits((v >> 16) & 0x3F3Fu);
+      float H0, H1;
+      mul2_rz(H0, H1, P0, P1, exp2i(-8), exp2i(-8));
+      float L0 = P0, L1 = P1;
+      fma2(L0, L1, H0, H1, -256.f, -256.f);
       const float* xr = x + 16 * a + 4 * t;
-      fma2(p[a][0], p[a][1], bits(v & 0x3Fu), bits(v & 0x3F00u), xr[0], xr[1]);
-      fma2(p[a][0], p[a][1], bits(v & 0x3F0000u), bits((v >> 8) & 0x3F0000u), xr[2], xr[3]);
+      fma2(p[a][0], p[a][1], L0, L1, xr[0], xr[2]);
+      fma2(p[a][0], p[a][1], H0, H1, xr[1], xr[3]);
     }
   }
   // scale of group a: byte 2a + m of the 8 scale bytes of half h
@@ -271,8 +370,7 @@ __device__ __forceinline__ void q6k_setup_x(const XU& xu, float* x, float* sx32)
     for (int i = 0; i < 16; ++i) {
       const float v = xu(16 * a + i);
       s += v;
-      const int pos = (i & 3) == 0 ? 0 : (i & 3) == 1 ? 8 : 16;
-      x[16 * a + i] = v * exp2i(kE - pos);
+      x[16 * a + i] = v * exp2i(kE);
     }
     sx32[a] = s * exp2i(5 - 60);
   }
@@ -285,7 +383,7 @@ struct UnitQ6K {
   static constexpr bool kDirect = false;  // activations staged through shared memory
   static constexpr int kBlockW = 256;
   static constexpr int kBlockBytes = 210;
-  float x[64];      // [16a + i], pre-scaled by 2^(kE - pos(i%4))
+  float x[64];      // [16a + i], pre-scaled by 2^kE
   float sx32[4];    // 32 * sum_i x[a][i] * 2^-60 (the -32 offset, in product units)
   Q6kUnitGeom g;
 
@@ -333,6 +431,11 @@ struct UnitQ6K {
 //   w5..w8 = qs1[0..15].
 // Block 0 weight j is the low nibble of qs0[j], weight 16+j the high nibble.
 // ---------------------------------------------------------------------------
+// Full nibble words of a Q4_0 unit that take the byte split (the rest are
+// decoded in place): w1..w3 of block 0 (index 0..2), w5..w8 of block 1 (0..3).
+__host__ __device__ constexpr bool q40_split0(int k) { return k == 0 || k == 2; }
+__host__ __device__ constexpr bool q40_split1(int k) { return k == 0 || k == 2; }
+
 struct UnitQ40 {
   static constexpr int kFmt = 2;
   static constexpr int kUnitW = 64;
@@ -369,8 +472,9 @@ struct UnitQ40 {
     e0[3] = xu(17) * exp2i(kE - 16);
 #pragma unroll
     for (int k = 0; k < 12; ++k) {
-      xl0[k] = xu(2 + k) * exp2i(kE - pos_lo(k & 3));
-      xh0[k] = xu(18 + k) * exp2i(kE - pos_hi(k & 3));
+      const bool sp = q40_split0(k >> 2);
+      xl0[k] = xu(2 + k) * exp2i(sp ? lo_exp<true>(k & 3) : lo_exp<false>(k & 3));
+      xh0[k] = xu(18 + k) * exp2i(sp ? hi_exp<true>(k & 3) : hi_exp<false>(k & 3));
     }
     g0[0] = xu(14) * exp2i(kE - 0);
     g0[1] = xu(30) * exp2i(kE - 4);
@@ -378,8 +482,9 @@ struct UnitQ40 {
     g0[3] = xu(31) * exp2i(kE - 12);
 #pragma unroll
     for (int k = 0; k < 16; ++k) {
-      xl1[k] = xu(32 + k) * exp2i(kE - pos_lo(k & 3));
-      xh1[k] = xu(48 + k) * exp2i(kE - pos_hi(k & 3));
+      const bool sp = q40_split1(k >> 2);
+      xl1[k] = xu(32 + k) * exp2i(sp ? lo_exp<true>(k & 3) : lo_exp<false>(k & 3));
+      xh1[k] = xu(48 + k) * exp2i(sp ? hi_exp<true>(k & 3) : hi_exp<false>(k & 3));
     }
   }
 
@@ -400,16 +505,16 @@ struct UnitQ40 {
     const uint32_t s = w0 >> 12;
     fma2(a0, a1, bits(s & 0xF0u), bits(s & 0xF00u), e0[0], e0[1]);
     fma2(a0, a1, bits(s & 0xF000u), bits(s & 0xF0000u), e0[2], e0[3]);
-    nibble_word(w1, xl0 + 0, xh0 + 0, a0, a1, b0, b1);
-    nibble_word(w2, xl0 + 4, xh0 + 4, a0, a1, b0, b1);
-    nibble_word(w3, xl0 + 8, xh0 + 8, a0, a1, b0, b1);
+    nib_word<q40_split0(0)>(w1, xl0 + 0, xh0 + 0, a0, a1, b0, b1);
+    nib_word<q40_split0(1)>(w2, xl0 + 4, xh0 + 4, a0, a1, b0, b1);
+    nib_word<q40_split0(2)>(w3, xl0 + 8, xh0 + 8, a0, a1, b0, b1);
     fma2(b0, b1, bits(w4 & 0xFu), bits(w4 & 0xF0u), g0[0], g0[1]);
     fma2(b0, b1, bits(w4 & 0xF00u), bits(w4 & 0xF000u), g0[2], g0[3]);
     float c0 = 0.f, c1 = 0.f, e0a = 0.f, e1a = 0.f;
-    nibble_word(w5, xl1 + 0, xh1 + 0, c0, c1, e0a, e1a);
-    nibble_word(w6, xl1 + 4, xh1 + 4, c0, c1, e0a, e1a);
-    nibble_word(w7, xl1 + 8, xh1 + 8, c0, c1, e0a, e1a);
-    nibble_word(w8, xl1 + 12, xh1 + 12, c0, c1, e0a, e1a);
+    nib_word<q40_split1(0)>(w5, xl1 + 0, xh1 + 0, c0, c1, e0a, e1a);
+    nib_word<q40_split1(1)>(w6, xl1 + 4, xh1 + 4, c0, c1, e0a, e1a);
+    nib_word<q40_split1(2)>(w7, xl1 + 8, xh1 + 8, c0, c1, e0a, e1a);
+    nib_word<q40_split1(3)>(w8, xl1 + 12, xh1 + 12, c0, c1, e0a, e1a);
     const float d0 = half_bits_to_float(w0) * exp2i(60);
     const float d1 = half_bits_to_float(w4 >> 16) * exp2i(60);
     const float p0 = ((a0 + a1) + (b0 + b1)) - s8_0;
@@ -633,8 +738,8 @@ struct UnitChain {
       const float va = xu(l), vb = xu(32 + l);
       sa += va;
       sb += vb;
-      x[l] = va * exp2i(kE - pos_lo(l & 3));
-      x[32 + l] = vb * exp2i(kE - pos_hi(l & 3));
+      x[l] = va * exp2i(q4k_xa_exp(l));
+      x[32 + l] = vb * exp2i(q4k_xb_exp(l));
     }
     s[0] = sa;
     s[1] = sb;

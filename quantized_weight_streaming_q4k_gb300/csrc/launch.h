@@ -138,9 +138,17 @@ cudaError_t launch_residual_add(float* h, const float* y, int64_t n, int batch, 
 cudaError_t launch_residual_rms_norm(float* h, const float* y, const float* w, float* x,
                                     int64_t n, float eps, int batch, cudaStream_t st);
 unsigned read_clear_matvec_errors();
+cudaError_t launch_selftest_mbar(long long limit, cudaStream_t st);
+cudaError_t launch_selftest_poll(void* word8, long long limit, cudaStream_t st);
 
 // message returned by qws_last_error() on the calling thread (abi.cu)
 void set_last_error(const char* msg);
+
+// one decode step over a KV cache (decode_kv.cu)
+size_t decode_kv_workspace_bytes(const qws_dims* d, int64_t max_seq);
+qws_status decode_kv(const qws_layer* layers, int n_layers, float* h, const qws_dims* d,
+                     const qws_kv* kv, void* ws, size_t ws_bytes, cudaStream_t st,
+                     std::string& err);
 
 // decode chain (chain.cu)
 size_t chain_workspace_bytes(int64_t hidden, int64_t inter);

@@ -233,6 +233,26 @@ __global__ void residual_add_kernel(float* __restrict__ h, const float* __restri
     h[i] += y[i];
 }
 
+// Self-test of the failure path: the engine's bounded mbarrier wait on a
+// barrier that nothing ever arrives at (no copy is issued), with the given
+// wait limit.  The wait gives up, records kErrFullWait and the kernel
+// returns; nothing is in flight.
+__global__ void selftest_mbar_kernel(long long limit) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0u, limit)) atomicOr(&g_err_matvec, kErrFullWait);
+  __syncthreads();
+}
+
+cudaError_t launch_selftest_mbar(long long limit, cudaStream_t st) {
+  selftest_mbar_kernel<<<1, 32, 0, st>>>(limit);
+  return cudaGetLastError();
+}
+
 // ------------------------------------------------------------------ host side
 // Launch with programmatic stream serialization: the kernel may start while
 // the previous kernel of the stream finishes (see pdl_wait / pdl_launch_dependents).

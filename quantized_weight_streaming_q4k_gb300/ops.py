@@ -21,7 +21,8 @@ __all__ = [
     "matvec", "quantize_q8_0", "q8_matvec", "q8_qkv_proj", "q4k_prefill_matmul",
     "rope_at_pos", "kv_append", "kv_attention", "rms_norm_q8", "residual_rms_norm_q8",
     "q4k_qkv_proj", "q4k_ffn_gate_up_geglu", "q4k_ffn_gate_up_geglu_down", "rms_norm",
-    "residual_add", "decode_chain", "workspace_bytes", "device_error", "Layer", "Dims",
+    "residual_add", "decode_chain", "decode_kv", "decode_kv_workspace_bytes", "workspace_bytes",
+    "device_error", "Layer", "Dims",
     "stream_handle",
 ]
 
@@ -322,6 +323,36 @@ def decode_chain(layers, h, dims: dict, workspace=None, stream=None):
                                  _dev(workspace, "workspace"),
                                  workspace.numel() * workspace.element_size(),
                                  stream_handle(stream)))
+    return h
+
+
+def decode_kv_workspace_bytes(dims: dict, max_seq: int) -> int:
+    D = make_dims(dims)
+    return int(lib().qws_decode_kv_workspace_bytes(C.byref(D), int(max_seq)))
+
+
+def decode_kv(layers, h, dims: dict, k_caches, v_caches, max_seq: int, pos: int, rot_dim: int,
+              rope_base: float, attn_scale: float, softcap: float = 0.0, workspace=None,
+              stream=None):
+    """One decode step at position pos over len(layers) layers with KV caches
+    (qws_decode_kv): h in place; k_caches[l] / v_caches[l] are f32 device
+    tensors [n_kv_heads, max_seq, head_dim], position pos is written."""
+    n = len(layers)
+    if len(k_caches) != n or len(v_caches) != n:
+        raise ValueError("one k and one v cache per layer")
+    arr = (Layer * n)(*[L if isinstance(L, Layer) else make_layer(L) for L in layers])
+    D = make_dims(dims)
+    kp = (C.c_void_p * n)(*[_dev(t, "k_cache", torch.float32) for t in k_caches])
+    vp = (C.c_void_p * n)(*[_dev(t, "v_cache", torch.float32) for t in v_caches])
+    kv = _lib.QwsKv(C.cast(kp, C.c_void_p), C.cast(vp, C.c_void_p), int(max_seq), int(pos),
+                    int(rot_dim), float(rope_base), float(attn_scale), float(softcap))
+    need = decode_kv_workspace_bytes(dims, max_seq)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=h.device)
+    check(lib().qws_decode_kv(arr, n, _dev(h, "h", torch.float32), C.byref(D), C.byref(kv),
+                              _dev(workspace, "workspace"),
+                              workspace.numel() * workspace.element_size(),
+                              stream_handle(stream)))
     return h
 
 

@@ -234,3 +234,12 @@ def test_vector_op_checks(lib):
 
 def test_device_error_null(lib):
     assert lib.qws_device_error(None) == NULL
+
+
+def test_selftest_wait_timeout_checks_arguments(lib):
+    # refused on the host, nothing launched
+    assert lib.qws_selftest_wait_timeout(2, 1000, None, None) == SHAPE
+    assert lib.qws_selftest_wait_timeout(0, 0, None, None) == SHAPE
+    assert lib.qws_selftest_wait_timeout(0, 3_000_000_000, None, None) == SHAPE
+    assert lib.qws_selftest_wait_timeout(1, 1000, None, None) == NULL
+    assert lib.qws_selftest_wait_timeout(1, 1000, C.c_void_p(0x10004), None) == ALIGN

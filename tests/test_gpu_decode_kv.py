@@ -1,0 +1,151 @@
+"""GPU parity of the decode step over a KV cache (qws_decode_kv) against the
+oracle's qo_layer_forward_kv.
+
+Checked teacher-forced, one layer at a time: the oracle runs layer l on the
+GPU's input to layer l and on the same cache contents (positions 0..pos-1
+filled with seeded values, the same numbers in f32 and f64).
+
+Layer tolerance, from the step tolerances: the layer adds two branches to h,
+a = h1 - h (post-attention) and b = h' - h1 (post-FFN), each an RMS-normalised
+matvec output.  The attention output carries the matvec error of q, k, v
+(1e-5 * sum|w x|) plus its own (the score and softmax roundings, a few 2^-24
+times the score magnitude, which is O(1) here: the q and k projections are
+drawn with small block scales so the softmax mixes many positions); the O
+projection adds 1e-5 * sum|w a|.  All of it stays inside the FFN's 1e-4
+relative budget that the chain's tolerance carries through both branches:
+    |h'_gpu - h'_ref| <= 1e-4 * (|h| + |a| + |b|) + 1e-4 * (rms(a) + rms(b)).
+The caches: every position but pos is untouched (bit for bit), and position
+pos holds the step's v (within the matvec tolerance of the oracle's).
+One launch over L layers equals L single-layer launches bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from quantized_weight_streaming_q4k_gb300 import build, ops, synth
+
+pytestmark = pytest.mark.gpu
+
+SMALL = dict(hidden=512, inter=1024, n_q_heads=4, n_kv_heads=2, head_dim=64, eps=1e-6,
+             post_norms=1)
+
+
+def _layer(l, dims, workload):
+    L = synth.chain_layer(l, dims, workload=workload)
+    g = synth.rng(workload, 77, l)
+    small = dict(d_range=(2e-5, 4e-5), dmin_range=(2e-5, 4e-5))
+    L["Wq"] = synth.q4_k_matrix(g, dims["n_q_heads"] * dims["head_dim"], dims["hidden"], **small)
+    L["Wk"] = synth.q4_k_matrix(g, dims["n_kv_heads"] * dims["head_dim"], dims["hidden"], **small)
+    return L
+
+
+def _caches(dims, max_seq, pos, seed):
+    g = synth.rng(950, seed)
+    shape = (dims["n_kv_heads"], max_seq, dims["head_dim"])
+    kc = (0.5 * g.standard_normal(shape)).astype(np.float32)
+    vc = g.standard_normal(shape).astype(np.float32)
+    kc[:, pos:] = 0.0
+    vc[:, pos:] = 0.0
+    return kc, vc
+
+
+def _dev(L):
+    return {k: (torch.from_numpy(np.ascontiguousarray(v)).cuda() if isinstance(v, np.ndarray)
+                else v) for k, v in L.items()}
+
+
+def _tol(h_in, tr, ref):
+    hb = np.asarray(h_in, np.float64)
+    a = tr["h1"] - hb
+    b = ref - tr["h1"]
+    return 1e-4 * (np.abs(hb) + np.abs(a) + np.abs(b)) + 1e-4 * (
+        np.sqrt(np.mean(a * a)) + np.sqrt(np.mean(b * b)))
+
+
+def _run_layers(dims, layers, n_layers, max_seq, pos, h0, workload, rot_dim=None, softcap=0.0):
+    build.build()
+    torch.cuda.set_device(0)
+    hd = dims["head_dim"]
+    rot = hd if rot_dim is None else rot_dim
+    scale = 1.0 / np.sqrt(hd)
+    ldev = [_dev(L) for L in layers]
+    caches = [_caches(dims, max_seq, pos, workload * 10 + l) for l in range(n_layers)]
+    h_in = h0.copy()
+    worst = 0.0
+    for l in range(n_layers):
+        kc, vc = caches[l]
+        kd, vd = torch.from_numpy(kc.copy()).cuda(), torch.from_numpy(vc.copy()).cuda()
+        h = torch.from_numpy(h_in.copy()).cuda()
+        ops.decode_kv([ldev[l]], h, dims, [kd], [vd], max_seq, pos, rot, 10000.0, scale, softcap)
+        torch.cuda.synchronize()
+        hg = h.cpu().numpy()
+        kv = dict(k_cache=kc.astype(np.float64), v_cache=vc.astype(np.float64), max_seq=max_seq,
+                  pos=pos, rot_dim=rot, rope_base=10000.0, scale=scale, softcap=softcap)
+        ref, tr = oracle.layer_forward_kv(layers[l], dims, kv, h_in, trace=True)
+        tol = _tol(h_in, tr, ref)
+        err = np.abs(hg.astype(np.float64) - ref)
+        assert np.all(err <= tol), f"layer {l}: max err/tol {np.max(err / tol):.3g}"
+        worst = max(worst, float(np.max(err / tol)))
+        # caches: only position pos changed; v at pos is the step's v
+        kg, vg = kd.cpu().numpy(), vd.cpu().numpy()
+        keep = np.ones(max_seq, bool)
+        keep[pos] = False
+        assert np.array_equal(kg[:, keep], kc[:, keep]) and np.array_equal(vg[:, keep], vc[:, keep])
+        v_ref = tr["v"].reshape(dims["n_kv_heads"], hd)
+        k_ref = tr["k"].reshape(dims["n_kv_heads"], hd)
+        vmag = np.max(np.abs(v_ref)) + 1e-30
+        kmag = np.max(np.abs(k_ref)) + 1e-30
+        assert np.max(np.abs(vg[:, pos] - v_ref)) <= 1e-4 * vmag
+        assert np.max(np.abs(kg[:, pos] - k_ref)) <= 1e-4 * kmag
+        h_in = hg
+    assert ops.device_error() == 0
+    return h_in, caches, worst
+
+
+@pytest.mark.parametrize("post_norms,pos,rot_dim,softcap",
+                         [(1, 37, None, 0.0), (0, 5, 32, 0.0), (1, 0, None, 0.0),
+                          (1, 63, None, 30.0)])
+def test_decode_kv_small(post_norms, pos, rot_dim, softcap):
+    dims = dict(SMALL, post_norms=post_norms)
+    layers = [_layer(l, dims, 960 + post_norms) for l in range(2)]
+    h0 = synth.normal_vector(synth.rng(961, pos), dims["hidden"])
+    _run_layers(dims, layers, 2, 64, pos, h0, 960, rot_dim, softcap)
+
+
+def test_decode_kv_multi_layer_launch_equals_single_layer_launches():
+    build.build()
+    torch.cuda.set_device(0)
+    dims = SMALL
+    max_seq, pos = 32, 9
+    layers = [_layer(l, dims, 962) for l in range(3)]
+    ldev = [_dev(L) for L in layers]
+    h0 = synth.normal_vector(synth.rng(963), dims["hidden"])
+    base = [_caches(dims, max_seq, pos, 970 + l) for l in range(3)]
+    scale = 1.0 / np.sqrt(dims["head_dim"])
+
+    def fresh():
+        return ([torch.from_numpy(k.copy()).cuda() for k, _ in base],
+                [torch.from_numpy(v.copy()).cuda() for _, v in base])
+
+    ks, vs = fresh()
+    h = torch.from_numpy(h0.copy()).cuda()
+    ops.decode_kv(ldev, h, dims, ks, vs, max_seq, pos, 64, 10000.0, scale)
+    ks1, vs1 = fresh()
+    h1 = torch.from_numpy(h0.copy()).cuda()
+    for l in range(3):
+        ops.decode_kv([ldev[l]], h1, dims, [ks1[l]], [vs1[l]], max_seq, pos, 64, 10000.0, scale)
+    torch.cuda.synchronize()
+    assert torch.equal(h, h1)
+    for l in range(3):
+        assert torch.equal(ks[l], ks1[l]) and torch.equal(vs[l], vs1[l])
+    assert ops.device_error() == 0
+
+
+def test_decode_kv_gemma3_4b_1024_cached_positions():
+    dims = synth.GEMMA3_4B
+    pos, max_seq = 1024, 1088
+    layers = [_layer(0, dims, 964)]
+    h0 = synth.normal_vector(synth.rng(965), dims["hidden"])
+    _, _, worst = _run_layers(dims, layers, 1, max_seq, pos, h0, 964)
+    print(f"decode_kv Gemma-3-4B, 1025 positions: max err/tol {worst:.3g}")
