@@ -45,7 +45,7 @@ namespace qws {
 __device__ unsigned g_err_chain;
 
 constexpr int kMaxLayers = 64;
-constexpr uint32_t kChainTileTarget = 30 * 1024;  // measured optimum at 4 stages
+constexpr uint32_t kChainTileTarget = 46 * 1024;  // measured optimum at 4 stages (inlined prologue / decode)
 constexpr uint32_t kChainStages = 4;
 constexpr int64_t kMaxChainHidden = 16 * kMaxConsumers;  // residual vectors: 16 per thread
 
@@ -58,6 +58,7 @@ struct ChainLayer {
 
 struct KindPlan {
   int fmt, U, G, T;
+  int T2, n1;        // balanced last round: tiles from n1 on hold T2 rows
   int64_t K, row_bytes;
 };
 
@@ -132,6 +133,8 @@ struct ChainPhases {
     P.U = kp.U;
     P.G = kp.G;
     P.T = kp.T;
+    P.T2 = kp.T2;
+    P.n1 = kp.n1;
     P.cta0 = 0;
     P.ncta = static_cast<int>(gridDim.x);
     P.nseg = 1;
@@ -139,6 +142,12 @@ struct ChainPhases {
     // chain's epilogue uses
     auto dst = [](Word* w) { return reinterpret_cast<float*>(w); };
     for (int i = 0; i < kMaxSeg; ++i) P.seg[i] = Seg{nullptr, nullptr, 0, 0};
+    // tiles of a one-segment phase: n1 tiles of T rows, the rest of T2 rows
+    auto tiles = [&](int64_t rows) {
+      const int64_t big = static_cast<int64_t>(kp.n1) * kp.T;
+      if (rows <= big) return static_cast<int>((rows + kp.T - 1) / kp.T);
+      return kp.n1 + static_cast<int>((rows - big + kp.T2 - 1) / kp.T2);
+    };
     if (kind == PH_QKV) {
       // v first: at sequence length 1 the O phase needs only v, and v's tiles
       // are then dealt in the first round, finished before the CTAs' last
@@ -148,12 +157,12 @@ struct ChainPhases {
       P.seg[1] = Seg{L.Wk, dst(p->k), p->KD, static_cast<int>((p->KD + kp.T - 1) / kp.T)};
       P.seg[2] = Seg{L.Wq, dst(p->q), p->QD, static_cast<int>((p->QD + kp.T - 1) / kp.T)};
     } else if (kind == PH_O) {
-      P.seg[0] = Seg{L.Wo, dst(p->o), p->H, static_cast<int>((p->H + kp.T - 1) / kp.T)};
+      P.seg[0] = Seg{L.Wo, dst(p->o), p->H, tiles(p->H)};
     } else if (kind == PH_GU) {
-      P.seg[0] = Seg{L.Wg, dst(p->m), p->I, static_cast<int>((p->I + kp.T - 1) / kp.T)};
+      P.seg[0] = Seg{L.Wg, dst(p->m), p->I, tiles(p->I)};
       P.W2 = L.Wu;
     } else {
-      P.seg[0] = Seg{L.Wd, dst(p->f), p->H, static_cast<int>((p->H + kp.T - 1) / kp.T)};
+      P.seg[0] = Seg{L.Wd, dst(p->f), p->H, tiles(p->H)};
     }
     P.n_tiles = P.seg[0].tiles + P.seg[1].tiles + P.seg[2].tiles;
     return P;
@@ -381,12 +390,14 @@ __device__ __forceinline__ bool stage_gather(const Ring& R, int US, const Word* 
 }
 
 // Builds the input vector of phase ph into R.xs, then counts this CTA's
-// prologue as finished.  Out of line: it runs once per phase and must not take
-// registers from the decode loop.  kWide: hidden > 8 * 320 (16 values per
-// thread in the residual / norm step); a separate instantiation, so the
+// prologue as finished.  Inlined, like the decode loop below: a call would
+// save and restore the caller's live registers through local memory at every
+// phase boundary, on the critical path (measured: 1316 -> 1172 us per
+// 34-layer token once both are inlined).  kWide: hidden > 8 * 320 (16 values
+// per thread in the residual / norm step); a separate instantiation, so the
 // common case carries none of its registers.
 template <bool kWide>
-__device__ __noinline__ bool chain_prologue(const ChainParams& p, int ph, const Ring& R,
+__device__ __forceinline__ bool chain_prologue(const ChainParams& p, int ph, const Ring& R,
                                             float* wsum, bool q6, int ctid, int C) {
   const int l = ph >> 2, kind = ph & 3;
   const ChainLayer& L = p.L[l];
@@ -487,14 +498,14 @@ __device__ __noinline__ bool chain_final(const ChainParams& p, float* wsum, int 
   return ok;
 }
 
-// The decode loop of every phase, out of line and fed with scalars only: it
-// rebuilds the ring from the dynamic shared-memory base, so no structure goes
-// through local memory and the loop gets a register allocation of its own
-// (UnitChain serves both formats).  Returns the new ring position (s, ph, n)
-// packed with an ok bit.
-__device__ __noinline__ unsigned long long chain_consume(
+// The decode loop of every phase, fed with scalars only: it rebuilds the ring
+// from the dynamic shared-memory base, so no structure goes through local
+// memory (UnitChain serves both formats).  Returns the new ring position
+// (s, ph, n) packed with an ok bit.
+__device__ __forceinline__ unsigned long long chain_consume(
     int fmt, int epi, int nseg, int rows0, int rows1, int rows2, int tiles0, int tiles1,
-    int tiles2, int T, int U, int G, int row_bytes, int n_tiles, unsigned S, unsigned stage_bytes,
+    int tiles2, int T, int T2, int n1, int U, int G, int row_bytes, int n_tiles, unsigned S,
+    unsigned stage_bytes,
     unsigned red_floats, unsigned xs_floats, unsigned pos_s, unsigned pos_ph, unsigned pos_n,
     int ctid, int C) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -514,6 +525,8 @@ __device__ __noinline__ unsigned long long chain_consume(
   P.U = U;
   P.G = G;
   P.T = T;
+  P.T2 = T2;
+  P.n1 = n1;
   P.n_tiles = n_tiles;
   P.cta0 = 0;
   P.ncta = static_cast<int>(gridDim.x);
@@ -585,8 +598,9 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
     if (!chain_prologue<kWide>(p, ph, R, wsum, q6, ctid, C)) return;
     const unsigned long long r = chain_consume(
         P.fmt, P.epi, P.nseg, static_cast<int>(P.seg[0].rows), static_cast<int>(P.seg[1].rows),
-        static_cast<int>(P.seg[2].rows), P.seg[0].tiles, P.seg[1].tiles, P.seg[2].tiles, P.T, P.U,
-        P.G, static_cast<int>(P.row_bytes), P.n_tiles, p.S, p.stage_bytes, p.red_floats,
+        static_cast<int>(P.seg[2].rows), P.seg[0].tiles, P.seg[1].tiles, P.seg[2].tiles, P.T,
+        P.T2, P.n1, P.U, P.G, static_cast<int>(P.row_bytes), P.n_tiles, p.S, p.stage_bytes,
+        p.red_floats,
         p.xs_floats, pos.s, pos.ph, pos.n, ctid, C);
     pos.s = static_cast<uint32_t>(r & 0xFFu);
     pos.ph = static_cast<uint32_t>((r >> 8) & 1u);
@@ -755,7 +769,24 @@ qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
       return QWS_ERR_SHAPE;
     }
     // all kinds run with the same thread count: C = kMaxConsumers
-    p.kp[i] = KindPlan{kinds[i].fmt, tp.U, tp.G, tp.T, kinds[i].K,
+    // One-segment phases end in a balanced round: whole rounds of T-row
+    // tiles (one per CTA), then the remaining rows in tiles of T2 <= T rows,
+    // at most one per CTA.  With T-row tiles alone a phase of R rows takes
+    // ceil(R / (T * sms)) tile times on the CTAs that hold an extra tile.
+    // T2 is a multiple of the rows that keep every tile's first byte 16-byte
+    // aligned (the bulk copies need it; T is one already).
+    int T2 = tp.T, n1 = 0x7FFFFFFF;
+    if (i != PH_QKV) {
+      const int64_t R = kinds[i].rows;
+      const int64_t RB = row_bytes_of(kinds[i].fmt, kinds[i].K);
+      const int64_t align = 16 / gcd64(RB, 16);
+      const int64_t full = R / (static_cast<int64_t>(tp.T) * sms);
+      const int64_t rem = R - full * tp.T * sms;
+      n1 = static_cast<int>(full * sms);
+      const int64_t t2 = ((rem + sms - 1) / sms + align - 1) / align * align;
+      T2 = rem > 0 ? static_cast<int>(std::min<int64_t>(tp.T, t2)) : tp.T;
+    }
+    p.kp[i] = KindPlan{kinds[i].fmt, tp.U,  tp.G, tp.T, T2, n1, kinds[i].K,
                        row_bytes_of(kinds[i].fmt, kinds[i].K)};
     stage_need = std::max(stage_need, tp.stage_need);
     red = std::max(red, tp.red_floats);

@@ -63,6 +63,8 @@ struct Phase {
   int U;              // lane units per row = K / 64
   int G;              // row slots per activation vector (B * G * U <= consumers)
   int T;              // rows per tile (per matrix for EPI_GEGLU)
+  int T2;             // rows per tile from tile n1 on (T2 <= T): tiles [0, n1) hold
+  int n1;             // T rows each, later tiles T2 rows from row n1 * T (one segment)
   int n_tiles;
   int64_t row_stride; // bytes between consecutive rows in global memory
                       // (> row_bytes when the phase covers a column slice)
@@ -98,9 +100,16 @@ __device__ __forceinline__ TileRef tile_ref(const Phase& P, int t) {
       more = false;
     }
   }
-  tr.r0 = static_cast<int64_t>(t) * P.T;
+  int lim = P.T;
+  if (t >= P.n1) {
+    // the last round of a balanced phase: smaller tiles
+    tr.r0 = static_cast<int64_t>(P.n1) * P.T + static_cast<int64_t>(t - P.n1) * P.T2;
+    lim = P.T2;
+  } else {
+    tr.r0 = static_cast<int64_t>(t) * P.T;
+  }
   const int64_t rem = tr.seg_rows - tr.r0;
-  tr.nrows = static_cast<int>(rem < P.T ? rem : P.T);
+  tr.nrows = static_cast<int>(rem < lim ? rem : lim);
   return tr;
 }
 

@@ -363,6 +363,8 @@ static bool plan_matvec(int fmt, int epi, const Seg* segs, int nseg, const uint8
   P.U = tp.U;
   P.G = tp.G;
   P.T = tp.T;
+  P.T2 = tp.T;
+  P.n1 = 0x7FFFFFFF;   // one tile size
   p.w_slice_off = P.row_bytes;
   p.x_slice_off = Ks;
   p.y_slice_off = static_cast<int64_t>(B) * segs[0].rows;
