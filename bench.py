@@ -726,7 +726,8 @@ def run_op(args):
         launches = 2
         nbytes = synth.n_blocks(synth.Q4_K, rows, H) * 144 + N * H * 4 + N * rows * 4
         flops = 2.0 * rows * H * N
-        kernel = "prefill_q4k_kernel (tcgen05 kind::f16) + prefill_pack_x_kernel"
+        kernel = ("prefill_q4k_kernel (tcgen05 kind::f16, operands split into f16 hi + lo: "
+                  "3 MMAs per product) + prefill_pack_x_kernel")
         workload = f"prefill Q4_K {rows}x{H}, {N} tokens"
     else:
         raise SystemExit(f"unknown --op {args.op}")
@@ -757,7 +758,9 @@ def run_op(args):
         print(json.dumps({
             "metric": "prefill achieved TFLOP/s", "value": tfs, "unit": "TFLOP/s", "n_gpus": 1,
             "steps": args.steps, "warmup": max(3, args.warmup), "us_per_call": us,
-            "higher_is_better": True, "dtype": "f16 operands, f32 accumulation",
+            "higher_is_better": True,
+            "dtype": "f16 hi + lo operand splits (3 tensor products each), f32 accumulation",
+            "tensor_tflops_executed": 3 * tfs,
             "data": "synthetic (seeded random blocks)",
             "config": {"workload": workload, "batch": B,
                        "l2": "back to back; weights 14.7 MB (L2-resident across calls)"},

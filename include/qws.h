@@ -194,13 +194,18 @@ qws_status qws_q8_qkv_proj(qws_format wfmt, const void* Wq, const void* Wk, cons
  *   X  [n_tokens][hidden] f32 (device, 16-byte aligned)
  *   Y  [n_tokens][rows] f32 (device, 4-byte aligned), overwritten
  *   ws >= qws_workspace_bytes(QWS_OP_PREFILL, 0, hidden, 0, n_tokens, 0)
- *      bytes (device, 16-byte aligned): X rounded to f16, in tiles
+ *      bytes (device, 16-byte aligned): X split into f16 hi and lo parts, in
+ *      tiles, and one scale per token
  *   rows >= 0; hidden > 0, hidden % 256 == 0; n_tokens >= 1.
- * Precision: both operands are rounded to f16 (round to nearest even; the
- * weight after its f32 dequantization) and multiplied with f32 accumulation,
- * so |Y - Y_exact| <= ~2^-10 * sum_k |w x| (plus 2^-25 per f16-subnormal
- * operand).  |x| and |w| must stay below 65504.  Results are identical run
- * to run.  The pages do not state the precision of their prefill path.
+ * Precision: the matvecs' bound, |Y - Y_exact| <= 1e-5 * sum_k |w x| per
+ * output.  Each operand is split into two f16 parts (the weight, dequantized
+ * in f32, scaled by 2^10; each token scaled by a power of two that puts its
+ * largest |x| in [2^14, 2^15)); three f16 products per pair (hi*hi, hi*lo,
+ * lo*hi) accumulate in f32.  The split needs |w| < 64 (every sub-block's
+ * |d*sc|*15 + |dmin*m| < 64); a larger one records device error code 256
+ * (read by qws_device_error).  Results are identical run to run.  The pages
+ * do not state the precision of their prefill path; this keeps the one they
+ * state for the matvecs.
  * ---------------------------------------------------------------------- */
 qws_status qws_q4k_prefill_matmul(const void* W, const float* X, float* Y, int64_t rows,
                                   int64_t hidden, int64_t n_tokens, void* ws, size_t ws_bytes,
@@ -409,8 +414,10 @@ qws_status qws_decode_kv(const qws_layer* layers, int n_layers, float* h, const 
  * qws_device_error: waits for the device, returns the OR of the error codes
  *   recorded by kernels since the last call (1 = a consumer gave up waiting
  *   for data, 2 = a producer gave up waiting for a free stage, 4 = a grid
- *   barrier gave up, 8 = a producer gave up draining its copies) and clears
- *   them.  Returns QWS_ERR_TIMEOUT when the code is non-zero.
+ *   barrier gave up, 8 = a producer gave up draining its copies; 16..128 the
+ *   prefill kernel's waits; 256 = a prefill weight outside the f16 split's
+ *   range) and clears them.  Returns QWS_ERR_TIMEOUT when the code is
+ *   non-zero.
  * qws_version: library version string.
  * ---------------------------------------------------------------------- */
 size_t qws_workspace_bytes(qws_op op, int64_t rows, int64_t hidden, int64_t inter, int batch,

@@ -1,25 +1,42 @@
 // prefill.cu -- the batch-N (prefill) Q4_K matrix product on the 5th-generation
 // tensor cores: Y[n][r] = sum_k W[r][k] * X[n][k] for N token vectors at once
 // (infer-compute README §Quick Start / §Shaders, prefill_q4: the seq > 1
-// path).  At N >= ~100 the product is compute-bound, so it runs as a GEMM:
+// path).  At N >= ~100 the product is compute-bound, so it runs as a GEMM, to
+// the same accuracy as the matvecs (|y - y_exact| <= 1e-5 * sum_k |w x|):
+// each operand is split into two f16 parts, hi + lo, and three f16 products
+// (hi*hi, hi*lo, lo*hi; the lo*lo term is below 2^-22 of the product) are
+// accumulated in f32 in tensor memory.
 //
-//   * X (f32 [N][K]) is first rounded to f16 and written, by a small packing
-//     kernel, into the workspace already in the shared-memory image the MMA
-//     reads: tiles of 256 tokens x 64 columns (32 KB), each a contiguous run
-//     in the 128-byte-swizzled K-major layout.  A tile then moves into shared
-//     memory as one 1-D bulk copy (TMA).
+//   * X (f32 [N][K]) is scaled per token by a power of two 2^e (max |x| of
+//     the token into [2^14, 2^15), exact) and split by a small packing kernel,
+//     one warp per token, into hi = f16(x') and lo = f16(x' - hi), written
+//     into the workspace already in the shared-memory image the MMA reads:
+//     tiles of 256 tokens x 64 columns (32 KB), each a contiguous run in the
+//     128-byte-swizzled K-major layout, hi and lo side by side; 2^-e is kept
+//     per token for the epilogue.
 //   * The weights stay packed in HBM.  One thread copies the tile rows' next
-//     super-block (128 rows x 144 bytes) into shared memory with one 2-D
-//     tensor copy (TMA, two buffers); eight decoder warps (two threads per weight row) dequantize
-//     w = d*sc*q - dmin*m in f32, round to f16 and store the row's 128 bytes
-//     of each 64-column chunk into the swizzled A tile.
+//     super-block (128 rows x 144 bytes) into shared memory with one 2-D tensor
+//     copy (TMA); eight decoder warps (two threads per weight row) take their
+//     row's 144 bytes into registers (which frees the buffer for the next
+//     super-block at once), dequantize w = d*sc*q - dmin*m in f32, scale by
+//     2^10 (exact) and split it into f16 hi + lo, stored into the swizzled A
+//     tiles.
 //   * One thread issues tcgen05.mma (kind::f16, M = 128 rows, N = 256 tokens,
-//     K = 16 per instruction, f32 accumulation) with both operands in shared
-//     memory and the accumulator in tensor memory (256 TMEM columns); a
-//     tcgen05.commit per stage frees that stage when its MMAs have read it.
-//   * The decoder warps then read the accumulator back with tcgen05.ld (warp
+//     K = 16 per instruction, f32 accumulation) with all operands in shared
+//     memory: hi*hi into one accumulator, hi*lo and lo*hi into a second (256
+//     TMEM columns each); a tcgen05.commit per stage frees that stage when its
+//     MMAs have read it.
+//   * The decoder warps then read both accumulators back with tcgen05.ld (warp
 //     w reads TMEM lanes 32*(w % 4) .. +31 = 32 weight rows, half of the
-//     columns) and store Y with coalesced 128-byte rows.
+//     columns), add them, undo the two power-of-two scales and store Y with
+//     coalesced 128-byte rows.
+//
+// Error per output: the splits leave <= 2^-22 of |w| and of |x| each (f16 hi
+// keeps 11 bits, lo the next 11), the dropped lo*lo term <= 2^-22 of |w x|, and
+// the f32 accumulation in tensor memory adds one rounding per 16-column MMA to
+// each accumulator (K / 16 of them): together far inside 1e-5 * sum |w x|.
+// Range: the split needs |w| < 64 (2^10 |w| within f16); a decoder that meets
+// a larger sub-block scale records kErrPfRange.
 //
 // Shared-memory layout of one operand tile (K-major, 128-byte swizzle): row i
 // (a weight row for A, a token for B) holds 64 f16 = 128 bytes at
@@ -51,22 +68,16 @@ constexpr uint32_t kPfBTile = kPfN * kPfK * 2;     // 32 KB
 constexpr uint32_t kPfWBuf = kPfM * 144;           // one Q4_K super-block of every row
 constexpr int kPfThreads = 352;            // 3 role warps + 8 decoder warps
 constexpr int kPfDecoders = 256;
-// TMEM columns: a power of two >= 32 that holds the N accumulator columns
-constexpr uint32_t kPfTmemCols = kPfN <= 32 ? 32u : kPfN <= 64 ? 64u : kPfN <= 128 ? 128u : 256u;
-static_assert(kPfN % 16 == 0 && kPfN <= 256, "MMA N must be a multiple of 16 up to 256");
-// A CTA computes kAcc token tiles of 256 against one decoded weight tile
-// (kAcc accumulators of 256 TMEM columns side by side), so one decode of the
-// weights serves 256 * kAcc tokens.  A stage holds the weight tile and kAcc
-// token tiles; as many stages as fit beside the two weight buffers in 227 KB.
-template <int kAcc>
+constexpr float kPfWScale = 1024.0f;       // 2^10: weights into the f16 split's range
+static_assert(kPfN == 256, "two accumulators of N = 256 fill the 512 TMEM columns");
+// A stage holds A hi, A lo (weight rows) then B hi, B lo (tokens); two stages
+// beside the one weight buffer.
 struct PfCfg {
-  static constexpr uint32_t kStage = kPfATile + kAcc * kPfBTile;
-  static constexpr int kStages =
-      static_cast<int>((227u * 1024u - 1024u - 2u * kPfWBuf - 256u) / kStage);
-  static constexpr size_t kSmem = 1024 + kStages * kStage + 2 * kPfWBuf + 256;
-  static constexpr uint32_t kTmemCols = kAcc == 1 ? kPfTmemCols : 512u;
-  static_assert(kStages >= 2, "shared memory too small for two stages");
-  static_assert(kAcc == 1 || (kAcc == 2 && kPfN == 256), "two accumulators fill the 512 columns");
+  static constexpr uint32_t kStage = 2 * kPfATile + 2 * kPfBTile;   // 96 KB
+  static constexpr int kStages = 2;
+  static constexpr size_t kSmem = 1024 + kStages * kStage + kPfWBuf + 256;
+  static constexpr uint32_t kTmemCols = 512;   // hi*hi accumulator, cross-term accumulator
+  static_assert(kSmem <= 227 * 1024, "shared memory");
 };
 
 // f32 accumulate, f16 A and B, both K-major, N = 256, M = 128.
@@ -77,7 +88,8 @@ constexpr uint32_t kPfIdesc = (1u << 4) | (0u << 7) | (0u << 10) |
 struct PrefillParams {
   CUtensorMap wmap;       // W as a [rows][row_bytes] byte matrix; box 144 x 128
   const uint8_t* W;       // Q4_K, rows x K
-  const uint8_t* X16;     // packed f16 tiles [n_tiles_n][KC][32 KB] (n_tiles_n % kAcc == 0)
+  const uint8_t* X16;     // packed f16 tiles [n_tiles_n][KC][hi, lo][32 KB]
+  const float* xscale;    // [n_tiles_n * 256] 2^-e per token
   float* Y;               // [N][rows]
   int64_t rows, K, N;
   int KC;                 // K / 64
@@ -165,42 +177,73 @@ __host__ __device__ constexpr uint32_t sw128_off(uint32_t i, uint32_t c) {
 }
 
 // ------------------------------------------------------------ X packing
-// X [N][K] f32 -> f16 tiles of 256 tokens x 64 columns in the swizzled image;
+// f32 -> f16 hi, and the f32 remainder x - hi (exact) -> f16 lo
+__device__ __forceinline__ void split_f16x2(float a, float b, uint32_t& hi, uint32_t& lo) {
+  hi = pack_f16x2(a, b);
+  const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&hi));
+  lo = pack_f16x2(a - h.x, b - h.y);
+}
+
+// X [N][K] f32 -> per token: 2^e with max |x| 2^e in [2^14, 2^15) (e = 0 for a
+// zero token, e clamped to [-126, 126]), then hi / lo f16 tiles of 256 tokens x
+// 64 columns in the swizzled image, and xscale = 2^-e.  One warp per token;
 // tokens N .. n_tiles_n * 256 - 1 are zero.
 __global__ void __launch_bounds__(256) prefill_pack_x_kernel(const float* __restrict__ X,
                                                              uint8_t* __restrict__ X16,
+                                                             float* __restrict__ xscale,
                                                              int64_t N, int64_t K,
                                                              int n_tiles_n) {
   pdl_launch_dependents();
   pdl_wait();
-  const int64_t chunks = K / 8;
-  const int64_t total = static_cast<int64_t>(n_tiles_n) * kPfN * chunks;
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  const int64_t tokens = static_cast<int64_t>(n_tiles_n) * kPfN;
+  const int64_t wpb = blockDim.x >> 5;
   const int KC = static_cast<int>(K / kPfK);
-  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t tok = i / chunks;
-    const int64_t qk = i - tok * chunks;
-    float v[8];
-    if (tok < N) {
-      const float4* p = reinterpret_cast<const float4*>(X + tok * K + qk * 8);
-      const float4 a = p[0], b = p[1];
-      v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-      v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-    } else {
+  const int64_t chunks = K / 8;
+  for (int64_t tok = blockIdx.x * wpb + (threadIdx.x >> 5); tok < tokens;
+       tok += static_cast<int64_t>(gridDim.x) * wpb) {
+    const bool live = tok < N;
+    const float* xr = X + tok * K;
+    float m = 0.f;
+    if (live)
+      for (int64_t i = lane * 4; i < K; i += 128) {
+        const float4 v = *reinterpret_cast<const float4*>(xr + i);
+        m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+      }
 #pragma unroll
-      for (int j = 0; j < 8; ++j) v[j] = 0.f;
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    int e = 0;
+    if (m > 0.f) {
+      int E;
+      frexpf(m, &E);                  // m = f * 2^E, f in [0.5, 1)
+      e = min(126, max(-126, 15 - E));
     }
-    uint4 o;
-    o.x = pack_f16x2(v[0], v[1]);
-    o.y = pack_f16x2(v[2], v[3]);
-    o.z = pack_f16x2(v[4], v[5]);
-    o.w = pack_f16x2(v[6], v[7]);
+    const float sc = ldexpf(1.0f, e);
+    if (lane == 0) xscale[tok] = ldexpf(1.0f, -e);
     const int64_t tn = tok / kPfN;
     const uint32_t t = static_cast<uint32_t>(tok - tn * kPfN);
-    const int64_t kc = qk / 8;
-    const uint32_t c = static_cast<uint32_t>(qk - kc * 8);
-    uint8_t* tile = X16 + (tn * KC + kc) * static_cast<int64_t>(kPfBTile);
-    *reinterpret_cast<uint4*>(tile + sw128_off(t, c)) = o;
+    for (int64_t qk = lane; qk < chunks; qk += 32) {
+      float v[8];
+      if (live) {
+        const float4* p = reinterpret_cast<const float4*>(xr + qk * 8);
+        const float4 a = p[0], b = p[1];
+        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = 0.f;
+      }
+      uint4 hi, lo;
+      split_f16x2(v[0] * sc, v[1] * sc, hi.x, lo.x);
+      split_f16x2(v[2] * sc, v[3] * sc, hi.y, lo.y);
+      split_f16x2(v[4] * sc, v[5] * sc, hi.z, lo.z);
+      split_f16x2(v[6] * sc, v[7] * sc, hi.w, lo.w);
+      const int64_t kc = qk / 8;
+      const uint32_t c = static_cast<uint32_t>(qk - kc * 8);
+      uint8_t* tile = X16 + ((tn * KC + kc) * 2) * static_cast<int64_t>(kPfBTile);
+      *reinterpret_cast<uint4*>(tile + sw128_off(t, c)) = hi;
+      *reinterpret_cast<uint4*>(tile + kPfBTile + sw128_off(t, c)) = lo;
+    }
   }
 }
 
@@ -218,12 +261,12 @@ __device__ __forceinline__ void fma2_to(float& d0, float& d1, float a0, float a1
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
 }
 
-// Four nibbles (one per byte of n, each 0..15) -> f16(a * q + nb), packed in
-// two words.  Byte k of n is placed under the exponent of 2^23 by one byte
-// permute (0x4B0000qq = 2^23 + q, exact); subtracting 2^23 gives q exactly, and
-// a * q + nb is rounded once to f32 (the same value as fmaf), then to f16.
-__device__ __forceinline__ void nib4_to_f16(uint32_t n, float a, float nb, uint32_t& o0,
-                                            uint32_t& o1) {
+// Four nibbles (one per byte of n, each 0..15) -> w = a * q + nb (rounded once
+// to f32, as fmaf), split into f16 hi (o_hi) and lo (o_lo), two per word.
+// Byte k of n is placed under the exponent of 2^23 by one byte permute
+// (0x4B0000qq = 2^23 + q, exact); subtracting 2^23 gives q exactly.
+__device__ __forceinline__ void nib4_split(uint32_t n, float a, float nb, uint32_t& h0,
+                                           uint32_t& h1, uint32_t& l0, uint32_t& l1) {
   const float m0 = __uint_as_float(__byte_perm(n, 0x4B000000u, 0x7650));
   const float m1 = __uint_as_float(__byte_perm(n, 0x4B000000u, 0x7651));
   const float m2 = __uint_as_float(__byte_perm(n, 0x4B000000u, 0x7652));
@@ -233,18 +276,20 @@ __device__ __forceinline__ void nib4_to_f16(uint32_t n, float a, float nb, uint3
   fma2_to(q2, q3, m2, m3, 1.0f, 1.0f, -8388608.0f, -8388608.0f);
   fma2_to(w0, w1, q0, q1, a, a, nb, nb);
   fma2_to(w2, w3, q2, q3, a, a, nb, nb);
-  o0 = pack_f16x2(w0, w1);
-  o1 = pack_f16x2(w2, w3);
+  split_f16x2(w0, w1, h0, l0);
+  split_f16x2(w2, w3, h1, l1);
 }
 
-// Dequantizes half of the 64-column chunk c (0..3) of one super-block row to
-// f32 and stores it as four swizzled 16-byte f16 chunks of the A tile row.
-// hd = the block's first 16 bytes (d, dmin, 12 scale bytes), q0/q1 = its qs
-// bytes 32c .. 32c+31.  Column l < 32 is the low nibble of qs byte 32c + l
-// (sub-block 2c, half 0), column 32 + l the high nibble (sub-block 2c + 1,
-// half 1); w = d*sc*q - dmin*m.
-__device__ __forceinline__ void q4k_half_to_f16(const uint4 hd, const uint4 q0, const uint4 q1,
-                                                int c, int half, uint8_t* tile, uint32_t row) {
+// Dequantizes half of the 64-column chunk c (0..3) of one super-block row,
+// scaled by 2^10, and stores it as four swizzled 16-byte chunks of the A hi
+// tile row and four of the A lo tile row.  hd = the block's first 16 bytes (d,
+// dmin, 12 scale bytes), q0/q1 = its qs bytes 32c .. 32c+31.  Column l < 32 is
+// the low nibble of qs byte 32c + l (sub-block 2c, half 0), column 32 + l the
+// high nibble (sub-block 2c + 1, half 1); w = d*sc*q - dmin*m.  Returns false
+// when 2^10 |w| could leave the f16 range (|d sc| * 15 + |dmin m| >= 64).
+__device__ __forceinline__ bool q4k_half_split(const uint4 hd, const uint4 q0, const uint4 q1,
+                                               int c, int half, uint8_t* tile_hi,
+                                               uint8_t* tile_lo, uint32_t row) {
   const bool hi = c >= 2;
   const uint32_t sh = 16u * static_cast<uint32_t>(c & 1) + 8u * static_cast<uint32_t>(half);
   const uint32_t S = hi ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u))
@@ -253,19 +298,24 @@ __device__ __forceinline__ void q4k_half_to_f16(const uint4 hd, const uint4 q0, 
                         : (hd.z & 0x3F3F3F3Fu);
   // half 0: sub-block 2c, low nibbles (columns 0..31 of the chunk);
   // half 1: sub-block 2c + 1, high nibbles (columns 32..63)
-  const float a = half_bits_to_float(hd.x) * static_cast<float>((S >> sh) & 0xFFu);
-  const float nb = -half_bits_to_float(hd.x >> 16) * static_cast<float>((M >> sh) & 0xFFu);
+  const float a = half_bits_to_float(hd.x) * static_cast<float>((S >> sh) & 0xFFu) * kPfWScale;
+  const float nb =
+      -half_bits_to_float(hd.x >> 16) * static_cast<float>((M >> sh) & 0xFFu) * kPfWScale;
+  const bool in_range = fabsf(a) * 15.0f + fabsf(nb) < 65504.0f;
   const uint32_t s0 = 4u * static_cast<uint32_t>(half);
   const uint32_t w[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     // 16-byte chunk 4*half + j: columns 8j .. 8j + 7 of this half = nibbles of
     // qs bytes 8j .. 8j + 7 (words 2j, 2j + 1)
-    uint4 o;
-    nib4_to_f16((w[2 * j] >> s0) & 0x0F0F0F0Fu, a, nb, o.x, o.y);
-    nib4_to_f16((w[2 * j + 1] >> s0) & 0x0F0F0F0Fu, a, nb, o.z, o.w);
-    *reinterpret_cast<uint4*>(tile + sw128_off(row, static_cast<uint32_t>(4 * half + j))) = o;
+    uint4 oh, ol;
+    nib4_split((w[2 * j] >> s0) & 0x0F0F0F0Fu, a, nb, oh.x, oh.y, ol.x, ol.y);
+    nib4_split((w[2 * j + 1] >> s0) & 0x0F0F0F0Fu, a, nb, oh.z, oh.w, ol.z, ol.w);
+    const uint32_t off = sw128_off(row, static_cast<uint32_t>(4 * half + j));
+    *reinterpret_cast<uint4*>(tile_hi + off) = oh;
+    *reinterpret_cast<uint4*>(tile_lo + off) = ol;
   }
+  return in_range;
 }
 
 // ------------------------------------------------------------ the GEMM kernel
@@ -273,36 +323,35 @@ enum : unsigned {
   kErrPfFull = 16u,      // MMA issuer gave up waiting for a stage
   kErrPfEmpty = 32u,     // a producer gave up waiting for a free stage
   kErrPfDone = 64u,      // the epilogue gave up waiting for the accumulator
-  kErrPfW = 128u,        // a wait on the packed-weight buffers gave up
+  kErrPfW = 128u,        // a wait on the packed-weight buffer gave up
+  kErrPfRange = 256u,    // a weight sub-block outside the split's range (|w| >= 64)
 };
 
-// Roles (11 warps): warp 0 copies X tiles (B), warp 1 issues the MMAs and
-// owns the TMEM allocation, warp 2 copies packed weight rows (one 144-byte
-// super-block per row per copy, two buffers), warps 3..10 decode (two
-// threads per weight row: low-nibble and high-nibble halves) and then run
-// the epilogue (warp w reads TMEM lanes 32 * (w % 4) .. + 31, columns of its
-// half of the tile).
-template <int kAcc>
+// Roles (11 warps): warp 0 copies X tiles (B hi and lo), warp 1 issues the
+// MMAs and owns the TMEM allocation, warp 2 copies packed weight rows (one
+// 144-byte super-block per row per copy, one buffer), warps 3..10 decode (two
+// threads per weight row: low-nibble and high-nibble halves) and then run the
+// epilogue (warp w reads TMEM lanes 32 * (w % 4) .. + 31, columns of its half
+// of the tile).
 __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid_constant__
                                                                     PrefillParams p) {
-  constexpr int kPfStages = PfCfg<kAcc>::kStages;
-  constexpr uint32_t kPfStage = PfCfg<kAcc>::kStage;
+  constexpr int kStages = PfCfg::kStages;
+  constexpr uint32_t kStage = PfCfg::kStage;
   extern __shared__ __align__(1024) uint8_t pf_smem_raw[];
   const uint32_t raw = smem_addr(pf_smem_raw);
   uint8_t* stages = pf_smem_raw + ((1024u - (raw & 1023u)) & 1023u);
-  uint8_t* wbuf = stages + kPfStages * kPfStage;                 // 2 x kPfWBuf
-  uint64_t* full = reinterpret_cast<uint64_t*>(wbuf + 2 * kPfWBuf);
-  uint64_t* empty = full + kPfStages;
-  uint64_t* wfull = empty + kPfStages;
-  uint64_t* wempty = wfull + 2;
-  uint64_t* done = wempty + 2;
+  uint8_t* wbuf = stages + kStages * kStage;                      // one super-block buffer
+  uint64_t* full = reinterpret_cast<uint64_t*>(wbuf + kPfWBuf);
+  uint64_t* empty = full + kStages;
+  uint64_t* wfull = empty + kStages;
+  uint64_t* wempty = wfull + 1;
+  uint64_t* done = wempty + 1;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(done + 1);
 
   const int warp = static_cast<int>(threadIdx.x >> 5);
   const int lane = static_cast<int>(threadIdx.x & 31);
-  const int n_groups = p.n_tiles_n / kAcc;
-  const int tm = static_cast<int>(blockIdx.x) / n_groups;
-  const int tg = static_cast<int>(blockIdx.x) - tm * n_groups;   // token tiles kAcc*tg ..
+  const int tm = static_cast<int>(blockIdx.x) / p.n_tiles_n;
+  const int tn = static_cast<int>(blockIdx.x) - tm * p.n_tiles_n;   // token tile
   const int64_t m0 = static_cast<int64_t>(tm) * kPfM;
   const int KC = p.KC;
   const int KB = KC / 4;
@@ -310,19 +359,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
   const int live_rows = static_cast<int>(rem < kPfM ? rem : kPfM);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kPfStages; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], kPfDecoders + 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&wfull[b], 1);
-      mbar_init(&wempty[b], kPfDecoders);
-    }
+    mbar_init(wfull, 1);
+    mbar_init(wempty, kPfDecoders);
     mbar_init(done, 1);
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, PfCfg<kAcc>::kTmemCols);
+    tmem_alloc(tmem_slot, PfCfg::kTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -331,68 +378,71 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
   const uint32_t tmem = *tmem_slot;
 
   pdl_launch_dependents();
-  pdl_wait();   // X16 is written by the packing kernel just before
+  pdl_wait();   // X16 and xscale are written by the packing kernel just before
 
   bool ok = true;
   if (warp == 0) {
-    // ---- B producer: one 32 KB bulk copy per stage
+    // ---- B producer: the hi and lo tiles of one 64-column chunk per stage
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      const uint8_t* xb = p.X16 + static_cast<int64_t>(tg) * kAcc * KC * kPfBTile;
+      const uint8_t* xb = p.X16 + static_cast<int64_t>(tn) * KC * 2 * kPfBTile;
       for (int kc = 0; kc < KC; ++kc) {
-        const int s = kc % kPfStages;
-        const uint32_t ph = static_cast<uint32_t>(kc / kPfStages) & 1u;
+        const int s = kc % kStages;
+        const uint32_t ph = static_cast<uint32_t>(kc / kStages) & 1u;
         if (!mbar_wait(&empty[s], ph ^ 1u)) {
           atomicOr(&g_err_prefill, kErrPfEmpty);
           break;
         }
-        mbar_arrive_expect_tx(&full[s], kAcc * kPfBTile);
-#pragma unroll
-        for (int a = 0; a < kAcc; ++a)
-          bulk_copy_g2s(stages + s * kPfStage + kPfATile + a * kPfBTile,
-                        xb + (static_cast<int64_t>(a) * KC + kc) * kPfBTile, kPfBTile, &full[s],
-                        pol);
+        mbar_arrive_expect_tx(&full[s], 2 * kPfBTile);
+        uint8_t* dst = stages + s * kStage + 2 * kPfATile;
+        const uint8_t* src = xb + static_cast<int64_t>(kc) * 2 * kPfBTile;
+        bulk_copy_g2s(dst, src, kPfBTile, &full[s], pol);
+        bulk_copy_g2s(dst + kPfBTile, src + kPfBTile, kPfBTile, &full[s], pol);
       }
     }
   } else if (warp == 2) {
     // ---- W producer: super-block kb of the tile's 128 rows, one 2-D tensor
-    // copy (rows past the matrix end are zero-filled and still counted)
+    // copy (rows past the matrix end are zero-filled and still counted); the
+    // decoders take the bytes into registers and free the buffer at once
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
       for (int kb = 0; kb < KB; ++kb) {
-        const int b = kb & 1;
-        const uint32_t ph = static_cast<uint32_t>(kb >> 1) & 1u;
-        if (!mbar_wait(&wempty[b], ph ^ 1u)) {
+        if (!mbar_wait(wempty, (static_cast<uint32_t>(kb) & 1u) ^ 1u)) {
           atomicOr(&g_err_prefill, kErrPfW);
           break;
         }
-        mbar_arrive_expect_tx(&wfull[b], kPfWBuf);
-        tma_load_2d(wbuf + b * kPfWBuf, &p.wmap, kb * 144, static_cast<int>(m0), &wfull[b], pol);
+        mbar_arrive_expect_tx(wfull, kPfWBuf);
+        tma_load_2d(wbuf, &p.wmap, kb * 144, static_cast<int>(m0), wfull, pol);
       }
     }
   } else if (warp == 1) {
-    // ---- MMA issuer
+    // ---- MMA issuer: per 16-column slice, hi*hi into accumulator 0, hi*lo
+    // and lo*hi into accumulator 1 (256 columns further)
     if (lane == 0) {
       for (int kc = 0; kc < KC; ++kc) {
-        const int s = kc % kPfStages;
-        const uint32_t ph = static_cast<uint32_t>(kc / kPfStages) & 1u;
+        const int s = kc % kStages;
+        const uint32_t ph = static_cast<uint32_t>(kc / kStages) & 1u;
         if (!mbar_wait(&full[s], ph)) {
           atomicOr(&g_err_prefill, kErrPfFull);
           break;
         }
         tc_fence_after();
-        const uint32_t a = smem_addr(stages + s * kPfStage);
+        const uint32_t ahi = smem_addr(stages + s * kStage);
+        const uint32_t alo = ahi + kPfATile;
+        const uint32_t bhi = ahi + 2 * kPfATile;
+        const uint32_t blo = bhi + kPfBTile;
 #pragma unroll
         for (int k = 0; k < kPfK / 16; ++k) {
-#pragma unroll
-          for (int t = 0; t < kAcc; ++t)
-            tc_mma_f16(tmem + static_cast<uint32_t>(t * kPfN), sw128_desc(a + 32u * k),
-                       sw128_desc(a + kPfATile + t * kPfBTile + 32u * k), kPfIdesc,
-                       (kc | k) != 0 ? 1u : 0u);
+          const uint32_t first = (kc | k) != 0 ? 1u : 0u;
+          tc_mma_f16(tmem, sw128_desc(ahi + 32u * k), sw128_desc(bhi + 32u * k), kPfIdesc, first);
+          tc_mma_f16(tmem + static_cast<uint32_t>(kPfN), sw128_desc(ahi + 32u * k),
+                     sw128_desc(blo + 32u * k), kPfIdesc, first);
+          tc_mma_f16(tmem + static_cast<uint32_t>(kPfN), sw128_desc(alo + 32u * k),
+                     sw128_desc(bhi + 32u * k), kPfIdesc, 1u);
         }
         tc_commit(&empty[s]);
       }
-      // the accumulator is final once every MMA above has completed
+      // the accumulators are final once every MMA above has completed
       tc_commit(done);
     }
   } else {
@@ -401,39 +451,52 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
     const uint32_t row = static_cast<uint32_t>(d >> 1);
     const int half = d & 1;
     const bool live = static_cast<int>(row) < live_rows;
+    bool in_range = true;
+    uint4 hd = make_uint4(0u, 0u, 0u, 0u), qs[8];
     for (int kc = 0; kc < KC; ++kc) {
-      const int s = kc % kPfStages;
-      const uint32_t ph = static_cast<uint32_t>(kc / kPfStages) & 1u;
-      const int kb = kc >> 2, c = kc & 3, b = kb & 1;
-      if (c == 0 && !mbar_wait(&wfull[b], static_cast<uint32_t>(kb >> 1) & 1u)) {
-        atomicOr(&g_err_prefill, kErrPfW);
-        ok = false;
-        break;
+      const int s = kc % kStages;
+      const uint32_t ph = static_cast<uint32_t>(kc / kStages) & 1u;
+      const int kb = kc >> 2, c = kc & 3;
+      if (c == 0) {
+        // the row's super-block: into registers, then the buffer is free
+        if (!mbar_wait(wfull, static_cast<uint32_t>(kb) & 1u)) {
+          atomicOr(&g_err_prefill, kErrPfW);
+          ok = false;
+          break;
+        }
+        const uint8_t* bp = wbuf + row * 144u;
+        hd = *reinterpret_cast<const uint4*>(bp);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) qs[i] = *reinterpret_cast<const uint4*>(bp + 16 + 16 * i);
+        mbar_arrive(wempty);
       }
       if (!mbar_wait(&empty[s], ph ^ 1u)) {
         atomicOr(&g_err_prefill, kErrPfEmpty);
         ok = false;
         break;
       }
-      uint8_t* tile = stages + s * kPfStage;
+      uint8_t* tile = stages + s * kStage;
       if (live) {
-        const uint8_t* bp = wbuf + b * kPfWBuf + row * 144u;
-        const uint4 hd = *reinterpret_cast<const uint4*>(bp);
-        const uint4 q0 = *reinterpret_cast<const uint4*>(bp + 16 + 32 * c);
-        const uint4 q1 = *reinterpret_cast<const uint4*>(bp + 32 + 32 * c);
-        q4k_half_to_f16(hd, q0, q1, c, half, tile, row);
+        // chunk c's 32 qs bytes are registers 2c and 2c + 1
+        uint4 q0 = qs[0], q1 = qs[1];
+        if (c == 1) { q0 = qs[2]; q1 = qs[3]; }
+        if (c == 2) { q0 = qs[4]; q1 = qs[5]; }
+        if (c == 3) { q0 = qs[6]; q1 = qs[7]; }
+        in_range = q4k_half_split(hd, q0, q1, c, half, tile, tile + kPfATile, row) && in_range;
       } else {
         const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-        for (int j = 0; j < 4; ++j)
-          *reinterpret_cast<uint4*>(tile + sw128_off(row, static_cast<uint32_t>(4 * half + j))) =
-              z;
+        for (int j = 0; j < 4; ++j) {
+          const uint32_t off = sw128_off(row, static_cast<uint32_t>(4 * half + j));
+          *reinterpret_cast<uint4*>(tile + off) = z;
+          *reinterpret_cast<uint4*>(tile + kPfATile + off) = z;
+        }
       }
       fence_proxy_async_smem();   // generic-proxy stores -> visible to the MMA
       mbar_arrive(&full[s]);
-      if (c == 3) mbar_arrive(&wempty[b]);   // this super-block's bytes are read
     }
-    // ---- epilogue
+    if (!in_range) atomicOr(&g_err_prefill, kErrPfRange);
+    // ---- epilogue: y = (hi*hi + cross terms) * 2^-10 * 2^-e(token)
     if (!mbar_wait(done, 0u)) {
       atomicOr(&g_err_prefill, kErrPfDone);
       ok = false;
@@ -441,28 +504,31 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
     tc_fence_after();
     if (ok) {
       const int q = warp & 3;
-      // warps 3..6 take the first half of the kAcc * 256 columns, 7..10 the
-      // rest; column c is token n0 + c (the accumulators are adjacent)
-      constexpr int kCols = kAcc * kPfN / 2;
+      // warps 3..6 take the first 128 token columns, 7..10 the rest
+      constexpr int kCols = kPfN / 2;
       const int colh = (warp - 3) >> 2;
       const int64_t rr = m0 + 32 * q + lane;
       const uint32_t tbase = tmem + (static_cast<uint32_t>(32 * q) << 16);
-      const int64_t n0 = static_cast<int64_t>(tg) * kAcc * kPfN;
+      const int64_t n0 = static_cast<int64_t>(tn) * kPfN;
       for (int cc = colh * kCols; cc < (colh + 1) * kCols; cc += 16) {
-        uint32_t v[16];
-        tc_ld16(tbase + static_cast<uint32_t>(cc), v);
+        uint32_t v0[16], v1[16];
+        tc_ld16(tbase + static_cast<uint32_t>(cc), v0);
+        tc_ld16(tbase + static_cast<uint32_t>(kPfN + cc), v1);
         tc_wait_ld();
         if (rr < p.rows) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int64_t n = n0 + cc + j;
-            if (n < p.N) p.Y[n * p.rows + rr] = __uint_as_float(v[j]);
+            if (n < p.N) {
+              const float y = __uint_as_float(v0[j]) + __uint_as_float(v1[j]);
+              p.Y[n * p.rows + rr] = y * (1.0f / kPfWScale) * p.xscale[n];
+            }
           }
         }
       }
     }
   }
-  // every MMA has completed before the accumulator is freed: wait (bounded)
+  // every MMA has completed before the accumulators are freed: wait (bounded)
   // for the final commit on all paths, including after a timeout
   tc_fence_before();
   __syncthreads();
@@ -470,31 +536,22 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_q4k_kernel(const __grid
     if (lane == 0 && !mbar_wait(done, 0u)) atomicOr(&g_err_prefill, kErrPfDone);
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, PfCfg<kAcc>::kTmemCols);
+    tmem_dealloc(tmem, PfCfg::kTmemCols);
   }
 }
 
 // ------------------------------------------------------------ host side
-// Token tiles of 256; the workspace always has room for an even count (the
-// two-accumulator kernel reads tiles in pairs, the last one zero when odd).
+// Token tiles of 256.  Workspace: per token tile and 64-column chunk the hi and
+// lo f16 tiles (2 x 32 KB), then one f32 scale per padded token.
 static int64_t token_tiles(int64_t n_tokens) { return (n_tokens + kPfN - 1) / kPfN; }
 
-size_t prefill_workspace_bytes(int64_t hidden, int64_t n_tokens) {
-  const int64_t t = token_tiles(n_tokens);
-  const int64_t padded = t >= 2 ? (t + 1) / 2 * 2 : t;
-  return static_cast<size_t>(padded) * kPfN * static_cast<size_t>(hidden) * 2;
+static size_t prefill_tiles_bytes(int64_t hidden, int64_t n_tokens) {
+  return static_cast<size_t>(token_tiles(n_tokens)) * kPfN * static_cast<size_t>(hidden) * 2 * 2;
 }
 
-// One or two accumulators per CTA: two halve the weight decoding per token
-// but give a CTA about 1.72x the work of a one-accumulator CTA (measured on
-// GB300 at 10240 x 2560: two stages instead of three), so they pay when they
-// save a wave: compare waves x relative CTA time.
-static int prefill_acc(int64_t rows, int64_t n_tokens, int sms) {
-  const int64_t mt = (rows + kPfM - 1) / kPfM, t1 = token_tiles(n_tokens);
-  if (t1 < 2) return 1;
-  const int64_t r1 = (mt * t1 + sms - 1) / sms;
-  const int64_t r2 = (mt * ((t1 + 1) / 2) + sms - 1) / sms;
-  return r2 * 172 < r1 * 100 ? 2 : 1;
+size_t prefill_workspace_bytes(int64_t hidden, int64_t n_tokens) {
+  return prefill_tiles_bytes(hidden, n_tokens) +
+         static_cast<size_t>(token_tiles(n_tokens)) * kPfN * sizeof(float);
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link
@@ -549,39 +606,37 @@ static cudaError_t launch_pdl_pf(void (*kernel)(KArgs...), int grid, int threads
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-template <int kAcc>
 static cudaError_t launch_prefill_kernel(const PrefillParams& p, int grid, cudaStream_t st) {
   // set on every launch (cheap): no per-device cache shared between threads
-  const cudaError_t e = cudaFuncSetAttribute(prefill_q4k_kernel<kAcc>,
+  const cudaError_t e = cudaFuncSetAttribute(prefill_q4k_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(PfCfg<kAcc>::kSmem));
+                                             static_cast<int>(PfCfg::kSmem));
   if (e != cudaSuccess) return e;
-  return launch_pdl_pf(prefill_q4k_kernel<kAcc>, grid, kPfThreads, PfCfg<kAcc>::kSmem, st, p);
+  return launch_pdl_pf(prefill_q4k_kernel, grid, kPfThreads, PfCfg::kSmem, st, p);
 }
 
 cudaError_t launch_prefill_q4k(const uint8_t* W, const float* X, float* Y, int64_t rows,
                                int64_t K, int64_t N, uint8_t* ws, cudaStream_t st) {
-  const int acc = prefill_acc(rows, N, device_sms());
-  const int64_t t1 = token_tiles(N);
-  const int n_tiles_n = static_cast<int>(acc == 2 ? (t1 + 1) / 2 * 2 : t1);
+  const int n_tiles_n = static_cast<int>(token_tiles(N));
   const int n_tiles_m = static_cast<int>((rows + kPfM - 1) / kPfM);
-  const int64_t pack_total = static_cast<int64_t>(n_tiles_n) * kPfN * (K / 8);
-  const int64_t pack_blocks = std::min<int64_t>((pack_total + 255) / 256, 8 * device_sms());
+  float* xscale = reinterpret_cast<float*>(ws + prefill_tiles_bytes(K, N));
+  const int64_t tokens = static_cast<int64_t>(n_tiles_n) * kPfN;
+  const int64_t pack_blocks = std::min<int64_t>((tokens + 7) / 8, 16 * device_sms());
   cudaError_t e = launch_pdl_pf(prefill_pack_x_kernel, static_cast<int>(pack_blocks), 256, 0, st,
-                                X, ws, N, K, n_tiles_n);
+                                X, ws, xscale, N, K, n_tiles_n);
   if (e != cudaSuccess) return e;
   PrefillParams p;
   if (!encode_w_map(&p.wmap, W, rows, K)) return cudaErrorInvalidValue;
   p.W = W;
   p.X16 = ws;
+  p.xscale = xscale;
   p.Y = Y;
   p.rows = rows;
   p.K = K;
   p.N = N;
   p.KC = static_cast<int>(K / kPfK);
   p.n_tiles_n = n_tiles_n;
-  const int grid = n_tiles_m * (n_tiles_n / acc);
-  return acc == 2 ? launch_prefill_kernel<2>(p, grid, st) : launch_prefill_kernel<1>(p, grid, st);
+  return launch_prefill_kernel(p, n_tiles_m * n_tiles_n, st);
 }
 
 unsigned read_clear_prefill_errors() {

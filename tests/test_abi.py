@@ -184,8 +184,9 @@ def test_q8_path_checks(lib):
 
 def test_prefill_checks(lib):
     need = lib.qws_workspace_bytes(_lib.OP_PREFILL, 0, 2560, 0, 512, 0)
-    assert need == 512 * 2560 * 2                       # f16 tiles of 256 tokens
-    assert lib.qws_workspace_bytes(_lib.OP_PREFILL, 0, 2560, 0, 1, 0) == 256 * 2560 * 2
+    # f16 hi and lo tiles of 256 tokens, then one f32 scale per padded token
+    assert need == 512 * 2560 * 2 * 2 + 512 * 4
+    assert lib.qws_workspace_bytes(_lib.OP_PREFILL, 0, 2560, 0, 1, 0) == 256 * 2560 * 4 + 256 * 4
     assert lib.qws_workspace_bytes(_lib.OP_PREFILL, 0, 2500, 0, 8, 0) == 0
     assert lib.qws_q4k_prefill_matmul(None, A, A, 10, 2560, 8, A, need, None) == NULL
     assert lib.qws_q4k_prefill_matmul(A, A + 4, A, 10, 2560, 8, A, need, None) == ALIGN

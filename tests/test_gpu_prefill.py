@@ -3,15 +3,11 @@ prefill_q4: seq > 1) on the tensor cores, through the C ABI, against the
 oracle's batch matvec (the same definition, y[n][r] = sum_k w[r][k] x[n][k],
 in f64).
 
-Tolerance, derived from the arithmetic: each weight (after its f32
-dequantization) and each activation is rounded once to f16 (relative error
-<= 2^-11 each for normal values, absolute <= 2^-25 in the f16 subnormal
-range); the products are exact in f32 and summed in f32 (<= K * 2^-24
-relative to sum |w x|).  So per output
-  |y - y_ref| <= (2^-10 + 2^-21 + K * 2^-24) * sum_k |w x|
-                 + 2^-25 * (sum_k |w| * max|x|... bounded here by
-                   2^-25 * (sum_k |w| + sum_k |x|) * max(|w|, |x|))
-and the tests use (2^-10 + K * 2^-24 + 2^-20) * bound + 2^-24 * (sum|w| + sum|x|) * 64.
+Tolerance: the matvecs' bound, |y - y_ref| <= 1e-5 * sum_k |w x| per output.
+The kernel splits each operand into two f16 parts (the weight scaled by 2^10,
+each token by its own power of two), so each operand keeps 22 bits and each
+product is within ~3 * 2^-22 of exact, plus one f32 rounding per 16-column MMA
+in the two tensor-memory accumulators: far inside the bound.
 """
 import os
 
@@ -54,10 +50,7 @@ def check_prefill(W, X, rows, K, N, rows_sel=None):
             ref[:, a] = r1.reshape(N, rows)[:, a]
             bound[:, a] = b1.reshape(N, rows)[:, a]
     ref, bound = ref.reshape(N, rows)[:, sel], bound.reshape(N, rows)[:, sel]
-    wabs = np.abs(oracle.dequant(oracle.Q4_K, W, rows, K)[sel]).sum(axis=1)      # [sel]
-    xabs = np.abs(X.astype(np.float64)).reshape(N, K).sum(axis=1)              # [N]
-    tol = (2.0 ** -10 + K * 2.0 ** -24 + 2.0 ** -20) * bound \
-        + 2.0 ** -24 * 64 * (wabs[None, :] + xabs[:, None])
+    tol = 1e-5 * bound
     err = np.abs(Y[:, sel] - ref)
     bad = err > tol
     assert not bad.any(), (f"{np.count_nonzero(bad)} of {bad.size} outside; worst err/bound "
@@ -85,10 +78,8 @@ def test_prefill_gemma_gate_shape_sampled_rows():
     check_prefill(W, X, rows, K, N, rows_sel=sel)
 
 
-def test_prefill_two_accumulators_odd_token_tiles():
-    # 76 row tiles x 3 token tiles: on 152 SMs the two-accumulator kernel
-    # (two token tiles per CTA) saves a wave, and its second pair is half
-    # padding (a zero token tile)
+def test_prefill_odd_token_tiles_sampled_rows():
+    # 76 row tiles x 3 token tiles, the last one mostly padding
     rows, K, N = 76 * 128, 1024, 600
     g = synth.rng(W_PF, 5)
     W = synth.q4_k_matrix(g, rows, K)
@@ -97,9 +88,44 @@ def test_prefill_two_accumulators_odd_token_tiles():
     check_prefill(W, X, rows, K, N, rows_sel=sel)
 
 
-def test_prefill_matches_matvec_per_token_within_f16_rounding():
-    # every token of the prefill equals the batch-1 matvec of that token up to
-    # the f16 operand rounding (a property at any size)
+@pytest.mark.parametrize("scale", [1e-6, 1e-2, 37.0, 1e4])
+def test_prefill_activation_scales(scale):
+    # the per-token power-of-two scaling keeps the split exact at any
+    # activation magnitude
+    rows, K, N = 256, 1024, 20
+    g = synth.rng(W_PF, 6, int(np.log10(scale) + 10))
+    W = synth.q4_k_matrix(g, rows, K)
+    X = (synth.normal_vector(g, K, N) * np.float32(scale)).astype(np.float32)
+    check_prefill(W, X, rows, K, N)
+
+
+def test_prefill_tokens_of_very_different_magnitudes():
+    # one tile of tokens whose magnitudes span 2^-40 .. 2^30: each token keeps
+    # its own scale
+    rows, K, N = 256, 512, 64
+    g = synth.rng(W_PF, 7)
+    W = synth.q4_k_matrix(g, rows, K)
+    X = synth.normal_vector(g, K, N)
+    X *= np.float32(2.0) ** np.linspace(-40, 30, N, dtype=np.float32)[:, None].astype(np.float32)
+    X[5] = 0.0          # an all-zero token
+    check_prefill(W, X.astype(np.float32), rows, K, N)
+
+
+def test_prefill_flags_weights_outside_the_split_range():
+    # |w| >= 64 cannot be split into f16 after the 2^10 pre-scale: the kernel
+    # records the range error (code 256) instead of returning silently
+    rows, K, N = 128, 256, 4
+    g = synth.rng(W_PF, 8)
+    W = synth.q4_k_matrix(g, rows, K, d_range=(8.0, 8.0))   # d * sc * q up to 8 * 63 * 15
+    X = synth.normal_vector(g, K, N)
+    ops.q4k_prefill_matmul(dev(W), dev(X), rows, K, N)
+    torch.cuda.synchronize()
+    assert ops.device_error() & 256
+
+
+def test_prefill_matches_matvec_per_token():
+    # every token of the prefill equals the batch-1 matvec of that token within
+    # the sum of their tolerances (a property at any size)
     rows, K, N = 512, 2560, 40
     g = synth.rng(W_PF, 3)
     W = synth.q4_k_matrix(g, rows, K)
@@ -109,7 +135,7 @@ def test_prefill_matches_matvec_per_token_within_f16_rounding():
     for n in (0, 17, N - 1):
         y1 = ops.q4k_matvec(Wd, Xd[n].contiguous(), rows, K).cpu().numpy()
         _, bound = oracle.matvec(oracle.Q4_K, W, rows, K, X[n])
-        assert np.all(np.abs(Y[n] - y1) <= 2.0 ** -9 * bound + 1e-6)
+        assert np.all(np.abs(Y[n] - y1) <= 2e-5 * bound)
 
 
 def test_prefill_is_run_to_run_identical():
