@@ -118,9 +118,15 @@ __device__ __forceinline__ TileRef tile_ref(const Phase& P, int t) {
 // staging buffer (xs_floats), then S stages of stage_bytes (128-B aligned,
 // each with >= 16 B of slack after the largest tile for the 2-byte-aligned
 // Q6_K word loads).
-// Partial-buffer and staging row stride: U rounded up to an odd number of
-// floats, so lanes walking rows (or units) hit distinct banks.
+// Staging row stride: U rounded up to an odd number of floats, so lanes
+// walking units (or columns) hit distinct banks.
 __host__ __device__ constexpr int red_stride(int U) { return U | 1; }
+// Partial-buffer row pitch: U rounded up to a multiple of 4 floats (rows start
+// on 16-byte boundaries, so the reducer reads them as float4) with an odd
+// number of float4s, so eight lanes reading eight rows cover all 32 banks.
+__host__ __device__ constexpr int red_pitch(int U) {
+  return (((U + 3) & ~3) >> 2) % 2 == 0 ? ((U + 3) & ~3) + 4 : ((U + 3) & ~3);
+}
 
 struct Ring {
   uint64_t* full;
@@ -138,9 +144,13 @@ struct Ring {
   }
 };
 
+// mbarriers first (24 B per stage, rounded up to 16 B so the partial buffers
+// start 16-byte aligned), then the partials, then the staging buffer.
+__host__ __device__ constexpr uint32_t ring_bar_bytes(uint32_t S) { return (24u * S + 15u) & ~15u; }
+
 __host__ __device__ constexpr size_t ring_header_bytes(uint32_t S, uint32_t red_floats,
                                                        uint32_t xs_floats) {
-  return ((24u * S + 4u * S * red_floats + 4u * xs_floats + 127u) / 128u) * 128u;
+  return ((ring_bar_bytes(S) + 4u * S * red_floats + 4u * xs_floats + 127u) / 128u) * 128u;
 }
 
 __host__ __device__ constexpr size_t ring_smem_bytes(uint32_t S, uint32_t stage_bytes,
@@ -154,7 +164,7 @@ __device__ __forceinline__ Ring make_ring(uint8_t* smem, uint32_t S, uint32_t st
   R.full = reinterpret_cast<uint64_t*>(smem);
   R.ready = R.full + S;
   R.empty = R.ready + S;
-  R.red = reinterpret_cast<float*>(R.empty + S);
+  R.red = reinterpret_cast<float*>(smem + ring_bar_bytes(S));
   R.xs = R.red + static_cast<size_t>(S) * red_floats;
   R.stages = smem + ring_header_bytes(S, red_floats, xs_floats);
   R.S = S;
@@ -360,7 +370,8 @@ __device__ __forceinline__ bool consume_phase(const Phase& Pref, const Ring& Rre
   } else {
     if (active) unit.setup(u, XUnit{R.xs, US, u});
   }
-  float* const red_b = R.red + static_cast<size_t>(b * slots) * US + u;
+  const int UP = red_pitch(U);
+  float* const red_b = R.red + static_cast<size_t>(b * slots) * UP + u;
   for (int t = cta; t < P.n_tiles; t += P.ncta) {
     if (!mbar_wait(&R.full[pos.s], pos.ph)) {
       atomicOr(err, kErrFullWait);
@@ -380,10 +391,10 @@ __device__ __forceinline__ bool consume_phase(const Phase& Pref, const Ring& Rre
           const int s0 = slot_of(r), s1 = slot_of(r + G);
           float y0, y1;
           unit.row2(st + s0 * rb, st + s1 * rb, y0, y1);
-          red[s0 * US] = y0;
-          red[s1 * US] = y1;
+          red[s0 * UP] = y0;
+          red[s1 * UP] = y1;
         }
-        if (r < nr) red[slot_of(r) * US] = unit.row(st + slot_of(r) * rb);
+        if (r < nr) red[slot_of(r) * UP] = unit.row(st + slot_of(r) * rb);
       }
     } else if (active) {
       int r = gg;
@@ -394,13 +405,13 @@ __device__ __forceinline__ bool consume_phase(const Phase& Pref, const Ring& Rre
         unit.load(st + s1 * rb, f1);
         const float y0 = unit.compute(f0);
         const float y1 = unit.compute(f1);
-        red[s0 * US] = y0;
-        red[s1 * US] = y1;
+        red[s0 * UP] = y0;
+        red[s1 * UP] = y1;
       }
       if (r < nr) {
         typename Unit::Frag f;
         unit.load(st + slot_of(r) * rb, f);
-        red[slot_of(r) * US] = unit.compute(f);
+        red[slot_of(r) * UP] = unit.compute(f);
       }
     }
     __syncwarp();
@@ -408,6 +419,25 @@ __device__ __forceinline__ bool consume_phase(const Phase& Pref, const Ring& Rre
     pos.advance(R.S);
   }
   return true;
+}
+
+// sum of p[0 .. n) taken by lane group member c0 of step members, in a fixed
+// order: float4 chunks c0, c0 + step, ... of the row (p 16-byte aligned),
+// summed lane-wise, then ((s0 + s1) + (s2 + s3)), then the member's share of
+// the n % 4 tail entries.
+__device__ __forceinline__ float quad_sum(const float* p, int c0, int n, int step) {
+  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+  const int nq = n >> 2;
+  for (int k = c0; k < nq; k += step) {
+    const float4 v = *reinterpret_cast<const float4*>(p + 4 * k);
+    s0 += v.x;
+    s1 += v.y;
+    s2 += v.z;
+    s3 += v.w;
+  }
+  float t = (s0 + s1) + (s2 + s3);
+  for (int c = 4 * nq + c0; c < n; c += step) t += p[c];
+  return t;
 }
 
 // sum of p[c] for c = c0, c0 + step, ... < n, in a fixed order: four
@@ -439,7 +469,7 @@ __device__ __forceinline__ bool reduce_phase(const Phase& Pref, const Ring& Rref
   const int cta = static_cast<int>(blockIdx.x) - P.cta0;
   if (cta < 0 || cta >= P.ncta) return true;
   const int lane = threadIdx.x & 31;
-  const int U = P.U, US = red_stride(P.U);
+  const int U = P.U, UP = red_pitch(P.U);
   const bool pair = P.epi != EPI_STORE;
   const int slots = pair ? 2 * P.T : P.T;
   for (int t = cta; t < P.n_tiles; t += P.ncta) {
@@ -460,11 +490,11 @@ __device__ __forceinline__ bool reduce_phase(const Phase& Pref, const Ring& Rref
       const bool valid = oi < n_out;
       const int ob = valid ? oi / tr.nrows : 0;
       const int o = valid ? oi - ob * tr.nrows : 0;
-      const float* rr = red + (ob * slots + o) * US;
+      const float* rr = red + (ob * slots + o) * UP;
       float v = 0.f, v2 = 0.f;
       if (valid) {
-        v = strided_sum(rr, sub, U, gsz);
-        if (pair) v2 = strided_sum(rr + P.T * US, sub, U, gsz);
+        v = quad_sum(rr, sub, U, gsz);
+        if (pair) v2 = quad_sum(rr + P.T * UP, sub, U, gsz);
       }
       for (int w = gsz >> 1; w > 0; w >>= 1) {
         v += __shfl_xor_sync(0xFFFFFFFFu, v, w);

@@ -78,7 +78,7 @@ inline bool plan_tiles(int fmt, int epi, int64_t K, int B, int64_t rows_hint, in
   tp.T = static_cast<int>(T0 * m);
   tp.C = static_cast<int>((B * G * U + 31) / 32 * 32);
   tp.stage_need = static_cast<uint32_t>(tp.T * RB * pairm);
-  tp.red_floats = static_cast<uint32_t>(B * tp.T * pairm * red_stride(static_cast<int>(U)));
+  tp.red_floats = static_cast<uint32_t>(B * tp.T * pairm * red_pitch(static_cast<int>(U)));
   return true;
 }
 
