@@ -196,7 +196,7 @@ qws_status qws_q8_qkv_proj(qws_format wfmt, const void* Wq, const void* Wk, cons
  *   ws >= qws_workspace_bytes(QWS_OP_PREFILL, 0, hidden, 0, n_tokens, 0)
  *      bytes (device, 16-byte aligned): X split into f16 hi and lo parts, in
  *      tiles, and one scale per token
- *   rows >= 0; hidden > 0, hidden % 256 == 0; n_tokens >= 1.
+ *   rows >= 0; 0 < hidden <= 20480, hidden % 256 == 0; n_tokens >= 1.
  * Precision: the matvecs' bound, |Y - Y_exact| <= 1e-5 * sum_k |w x| per
  * output.  Each operand is split into two f16 parts (the weight, dequantized
  * in f32, scaled by 2^10; each token scaled by a power of two that puts its

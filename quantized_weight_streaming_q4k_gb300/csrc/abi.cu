@@ -292,8 +292,8 @@ qws_status qws_q4k_prefill_matmul(const void* W, const float* X, float* Y, int64
   if (!aligned(X, 16)) return fail(QWS_ERR_ALIGN, "%s: X is not 16-byte aligned", fn);
   QWS_CHECK_F(Y);
   if (rows < 0) return fail(QWS_ERR_SHAPE, "%s: rows = %lld < 0", fn, (long long)rows);
-  if (hidden <= 0 || hidden % 256)
-    return fail(QWS_ERR_SHAPE, "%s: hidden = %lld is not a positive multiple of 256", fn,
+  if (hidden <= 0 || hidden % 256 || hidden > kMaxHidden)
+    return fail(QWS_ERR_SHAPE, "%s: hidden = %lld (need a multiple of 256 in (0, 20480])", fn,
                 (long long)hidden);
   if (n_tokens < 1 || n_tokens > (int64_t(1) << 30))
     return fail(QWS_ERR_SHAPE, "%s: n_tokens = %lld outside [1, 2^30]", fn,

@@ -186,32 +186,51 @@ __device__ __forceinline__ void split_f16x2(float a, float b, uint32_t& hi, uint
 
 // X [N][K] f32 -> per token: 2^e with max |x| 2^e in [2^14, 2^15) (e = 0 for a
 // zero token, e clamped to [-126, 126]), then hi / lo f16 tiles of 256 tokens x
-// 64 columns in the swizzled image, and xscale = 2^-e.  One warp per token;
-// tokens N .. n_tiles_n * 256 - 1 are zero.
+// 64 columns in the swizzled image, and xscale = 2^-e.  One CTA of 256 threads
+// per token (its maximum by a warp max, then over the 8 warps in shared
+// memory); tokens N .. n_tiles_n * 256 - 1 are zero.
 __global__ void __launch_bounds__(256) prefill_pack_x_kernel(const float* __restrict__ X,
                                                              uint8_t* __restrict__ X16,
                                                              float* __restrict__ xscale,
                                                              int64_t N, int64_t K,
                                                              int n_tiles_n) {
+  __shared__ float wmax[8];
   pdl_launch_dependents();
   pdl_wait();
-  const int lane = static_cast<int>(threadIdx.x & 31);
+  const int lane = static_cast<int>(threadIdx.x & 31), warp = static_cast<int>(threadIdx.x >> 5);
   const int64_t tokens = static_cast<int64_t>(n_tiles_n) * kPfN;
-  const int64_t wpb = blockDim.x >> 5;
   const int KC = static_cast<int>(K / kPfK);
   const int64_t chunks = K / 8;
-  for (int64_t tok = blockIdx.x * wpb + (threadIdx.x >> 5); tok < tokens;
-       tok += static_cast<int64_t>(gridDim.x) * wpb) {
+  for (int64_t tok = blockIdx.x; tok < tokens; tok += gridDim.x) {
     const bool live = tok < N;
     const float* xr = X + tok * K;
+    // each thread keeps the 8-column chunks it packs below in registers
+    // (K <= 20480: at most 10 chunks of 8 per thread)
+    float v[10][8];
     float m = 0.f;
-    if (live)
-      for (int64_t i = lane * 4; i < K; i += 128) {
-        const float4 v = *reinterpret_cast<const float4*>(xr + i);
-        m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+#pragma unroll
+    for (int j = 0; j < 10; ++j) {
+      const int64_t qk = threadIdx.x + static_cast<int64_t>(j) * 256;
+      if (live && qk < chunks) {
+        const float4* p = reinterpret_cast<const float4*>(xr + qk * 8);
+        const float4 a = p[0], b = p[1];
+        v[j][0] = a.x; v[j][1] = a.y; v[j][2] = a.z; v[j][3] = a.w;
+        v[j][4] = b.x; v[j][5] = b.y; v[j][6] = b.z; v[j][7] = b.w;
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[j][i] = 0.f;
       }
 #pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(v[j][i]));
+    }
+#pragma unroll
     for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    if (lane == 0) wmax[warp] = m;
+    __syncthreads();
+    m = wmax[0];
+#pragma unroll
+    for (int w = 1; w < 8; ++w) m = fmaxf(m, wmax[w]);
+    __syncthreads();   // wmax is rewritten by the next token
     int e = 0;
     if (m > 0.f) {
       int E;
@@ -219,30 +238,24 @@ __global__ void __launch_bounds__(256) prefill_pack_x_kernel(const float* __rest
       e = min(126, max(-126, 15 - E));
     }
     const float sc = ldexpf(1.0f, e);
-    if (lane == 0) xscale[tok] = ldexpf(1.0f, -e);
+    if (threadIdx.x == 0) xscale[tok] = ldexpf(1.0f, -e);
     const int64_t tn = tok / kPfN;
     const uint32_t t = static_cast<uint32_t>(tok - tn * kPfN);
-    for (int64_t qk = lane; qk < chunks; qk += 32) {
-      float v[8];
-      if (live) {
-        const float4* p = reinterpret_cast<const float4*>(xr + qk * 8);
-        const float4 a = p[0], b = p[1];
-        v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-        v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-      } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) v[j] = 0.f;
+    for (int j = 0; j < 10; ++j) {
+      const int64_t qk = threadIdx.x + static_cast<int64_t>(j) * 256;
+      if (qk < chunks) {
+        uint4 hi, lo;
+        split_f16x2(v[j][0] * sc, v[j][1] * sc, hi.x, lo.x);
+        split_f16x2(v[j][2] * sc, v[j][3] * sc, hi.y, lo.y);
+        split_f16x2(v[j][4] * sc, v[j][5] * sc, hi.z, lo.z);
+        split_f16x2(v[j][6] * sc, v[j][7] * sc, hi.w, lo.w);
+        const int64_t kc = qk / 8;
+        const uint32_t c = static_cast<uint32_t>(qk - kc * 8);
+        uint8_t* tile = X16 + ((tn * KC + kc) * 2) * static_cast<int64_t>(kPfBTile);
+        *reinterpret_cast<uint4*>(tile + sw128_off(t, c)) = hi;
+        *reinterpret_cast<uint4*>(tile + kPfBTile + sw128_off(t, c)) = lo;
       }
-      uint4 hi, lo;
-      split_f16x2(v[0] * sc, v[1] * sc, hi.x, lo.x);
-      split_f16x2(v[2] * sc, v[3] * sc, hi.y, lo.y);
-      split_f16x2(v[4] * sc, v[5] * sc, hi.z, lo.z);
-      split_f16x2(v[6] * sc, v[7] * sc, hi.w, lo.w);
-      const int64_t kc = qk / 8;
-      const uint32_t c = static_cast<uint32_t>(qk - kc * 8);
-      uint8_t* tile = X16 + ((tn * KC + kc) * 2) * static_cast<int64_t>(kPfBTile);
-      *reinterpret_cast<uint4*>(tile + sw128_off(t, c)) = hi;
-      *reinterpret_cast<uint4*>(tile + kPfBTile + sw128_off(t, c)) = lo;
     }
   }
 }
@@ -621,7 +634,7 @@ cudaError_t launch_prefill_q4k(const uint8_t* W, const float* X, float* Y, int64
   const int n_tiles_m = static_cast<int>((rows + kPfM - 1) / kPfM);
   float* xscale = reinterpret_cast<float*>(ws + prefill_tiles_bytes(K, N));
   const int64_t tokens = static_cast<int64_t>(n_tiles_n) * kPfN;
-  const int64_t pack_blocks = std::min<int64_t>((tokens + 7) / 8, 16 * device_sms());
+  const int64_t pack_blocks = std::min<int64_t>(tokens, 8 * device_sms());
   cudaError_t e = launch_pdl_pf(prefill_pack_x_kernel, static_cast<int>(pack_blocks), 256, 0, st,
                                 X, ws, xscale, N, K, n_tiles_n);
   if (e != cudaSuccess) return e;

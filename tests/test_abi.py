@@ -191,6 +191,7 @@ def test_prefill_checks(lib):
     assert lib.qws_q4k_prefill_matmul(None, A, A, 10, 2560, 8, A, need, None) == NULL
     assert lib.qws_q4k_prefill_matmul(A, A + 4, A, 10, 2560, 8, A, need, None) == ALIGN
     assert lib.qws_q4k_prefill_matmul(A, A, A, 10, 2500, 8, A, need, None) == SHAPE
+    assert lib.qws_q4k_prefill_matmul(A, A, A, 10, 20480 + 256, 8, A, need, None) == SHAPE
     assert lib.qws_q4k_prefill_matmul(A, A, A, 10, 2560, 0, A, need, None) == SHAPE
     assert lib.qws_q4k_prefill_matmul(A, A, A, -1, 2560, 8, A, need, None) == SHAPE
     small = lib.qws_workspace_bytes(_lib.OP_PREFILL, 0, 2560, 0, 8, 0)
