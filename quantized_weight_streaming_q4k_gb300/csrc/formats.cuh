@@ -156,13 +156,48 @@ __device__ __forceinline__ void q4k_word(uint32_t w, const float* xa, const floa
 // qs[32c .. 32c+31] (weights 64c+l of sub-block 2c in the low nibbles and
 // 64c+32+l of sub-block 2c+1 in the high nibbles) plus the block header.
 // ---------------------------------------------------------------------------
+// Scale / min selection of one Q4_K chunk, fixed per lane unit (chunk c of
+// the block: sub-blocks 2c and 2c + 1).  With j = 2 (c & 1):
+//   P = bytes [y_j, y_j+1, z_j, z_j+1] of the header words hd.y (scale bytes
+//       0..3) and hd.z (4..7); Q = [w_j, w_j+1, w_j, w_j+1] of hd.w (8..11)
+//       for c >= 2, zero for c < 2;
+//   R = ((P >> sh) & mask) | (Q's low nibbles in bytes 0, 1 and high nibbles
+//       in bytes 2, 3) = [scale_a, scale_b, min_a, min_b]:
+//   c < 2 : sh = 0, mask 0x3F3F3F3F (the 6-bit fields themselves);
+//   c >= 2: sh = 2, mask 0x30303030 (bits 6, 7 of y / z as bits 4, 5 on top
+//           of w's nibble) -- the GGUF packing of sub-blocks 4..7.
+struct Q4kSel {
+  uint32_t selP, selQ, sh, mask;
+  __device__ __forceinline__ void set(int c) {
+    const uint32_t j = 2u * static_cast<uint32_t>(c & 1);
+    selP = j | (j + 1) << 4 | (4 + j) << 8 | (5 + j) << 12;
+    selQ = c >= 2 ? (j | (j + 1) << 4 | j << 8 | (j + 1) << 12) : 0x4444u;
+    sh = c >= 2 ? 2u : 0u;
+    mask = c >= 2 ? 0x30303030u : 0x3F3F3F3Fu;
+  }
+};
+
+__device__ __forceinline__ uint32_t q4k_scale_bytes(const uint4 hd, uint32_t selP, uint32_t selQ,
+                                                    uint32_t sh, uint32_t mask) {
+  const uint32_t P = __byte_perm(hd.y, hd.z, selP);
+  const uint32_t Q = __byte_perm(hd.w, 0u, selQ);
+  const uint32_t N = ((Q & 0x0000FFFFu) | ((Q >> 4) & 0xFFFF0000u)) & 0x0F0F0F0Fu;
+  return ((P >> sh) & mask) | N;
+}
+
+// byte k of r as an exact float: under the exponent of 2^23, minus 2^23
+__device__ __forceinline__ float byte_to_float(uint32_t r, uint32_t k) {
+  return __uint_as_float(__byte_perm(r, 0x4B000000u, 0x7650u | k)) - 8388608.0f;
+}
+
 // Dot product of one Q4_K chunk (32 bytes: 32 low nibbles of sub-block 2c,
 // 32 high nibbles of sub-block 2c+1) with the pre-scaled activations xa / xb
-// (q4k_xa_exp / q4k_xb_exp); hd is the block header, sh/hi select the chunk's
-// scale pair.
+// (q4k_xa_exp / q4k_xb_exp); hd is the block header, the selection constants
+// come from Q4kSel::set(c).
 __device__ __forceinline__ float q4k_chunk_dot(const uint4 hd, const uint4 q0, const uint4 q1,
                                                const float* xa, const float* xb, float sxa,
-                                               float sxb, uint32_t sh, bool hi) {
+                                               float sxb, uint32_t selP, uint32_t selQ,
+                                               uint32_t sh, uint32_t mask) {
   float a0 = 0.f, a1 = 0.f, b0 = 0.f, b1 = 0.f;
   q4k_word<0>(q0.x, xa, xb, a0, a1, b0, b1);
   q4k_word<1>(q0.y, xa, xb, a0, a1, b0, b1);
@@ -172,18 +207,9 @@ __device__ __forceinline__ float q4k_chunk_dot(const uint4 hd, const uint4 q0, c
   q4k_word<5>(q1.y, xa, xb, a0, a1, b0, b1);
   q4k_word<6>(q1.z, xa, xb, a0, a1, b0, b1);
   q4k_word<7>(q1.w, xa, xb, a0, a1, b0, b1);
-  // 6-bit scales / mins of all eight sub-blocks, one per byte:
-  //   s < 4 : sc[s] & 63 and sc[s+4] & 63
-  //   s >= 4: (sc[s+4] & 15) | (sc[s-4] >> 6) << 4  and
-  //           (sc[s+4] >> 4) | (sc[s]   >> 6) << 4
-  const uint32_t S = hi ? ((hd.w & 0x0F0F0F0Fu) | ((hd.y >> 2) & 0x30303030u))
-                        : (hd.y & 0x3F3F3F3Fu);
-  const uint32_t M = hi ? (((hd.w >> 4) & 0x0F0F0F0Fu) | ((hd.z >> 2) & 0x30303030u))
-                        : (hd.z & 0x3F3F3F3Fu);
-  const float sca = static_cast<float>((S >> sh) & 0xFFu);
-  const float scb = static_cast<float>((S >> (sh + 8)) & 0xFFu);
-  const float mna = static_cast<float>((M >> sh) & 0xFFu);
-  const float mnb = static_cast<float>((M >> (sh + 8)) & 0xFFu);
+  const uint32_t R = q4k_scale_bytes(hd, selP, selQ, sh, mask);
+  const float sca = byte_to_float(R, 0), scb = byte_to_float(R, 1);
+  const float mna = byte_to_float(R, 2), mnb = byte_to_float(R, 3);
   const float d = half_bits_to_float(hd.x) * exp2i(60);
   const float dmin = half_bits_to_float(hd.x >> 16);
   const float qx = fmaf(sca, a0 + a1, scb * (b0 + b1));
@@ -203,8 +229,7 @@ struct UnitQ4K {
   float sxa, sxb; // plain sums of x over the two sub-blocks
   uint32_t off;   // byte offset of the block header within the row
   uint32_t qoff;  // byte offset of the chunk within the block
-  uint32_t sh;    // bit offset of the scale pair inside the 4-scale word
-  bool hi;        // sub-blocks 4..7 (scales split across two byte groups)
+  Q4kSel sel;     // scale / min selection of the unit's chunk
 
   // Unit u covers columns 64u .. 64u + 63; unit-local index l = col % 64.
   __device__ __forceinline__ static void unit_of(int64_t col, int& u, int& l) {
@@ -218,8 +243,7 @@ struct UnitQ4K {
     const int kb = u >> 2, c = u & 3;
     off = static_cast<uint32_t>(kb) * kBlockBytes;
     qoff = 16u + 32u * c;
-    sh = 16u * (c & 1);
-    hi = c >= 2;
+    sel.set(c);
     float sa = 0.f, sb = 0.f;
 #pragma unroll
     for (int l = 0; l < 32; ++l) {
@@ -247,7 +271,8 @@ struct UnitQ4K {
 
   // Partial dot product of this unit with one row (its bytes in f).
   __device__ __forceinline__ float compute(const Frag& f) const {
-    return q4k_chunk_dot(f.hd, f.q0, f.q1, xa, xb, sxa, sxb, sh, hi);
+    return q4k_chunk_dot(f.hd, f.q0, f.q1, xa, xb, sxa, sxb, sel.selP, sel.selQ, sel.sh,
+                         sel.mask);
   }
 
   __device__ __forceinline__ float row(const uint8_t* rp) const {
@@ -722,16 +747,21 @@ struct UnitChain {
   bool q6;         // set from the phase's format before setup()
   float x[64];     // Q4_K: xa = x[0..31], xb = x[32..63]; Q6_K: x[16a + i]
   float s[4];      // Q4_K: sxa, sxb; Q6_K: sx32[0..3]
+  // Q6_K: block offset, the four operand offsets and the scale shift;
+  // Q4_K: off, o1 = chunk offset, o2..o4 / sh = the Q4kSel constants
   uint32_t off, o1, o2, o3, o4, sh;
-  bool hi;
 
   template <class XU>
   __device__ __forceinline__ void setup_q4k(int u, const XU& xu) {
     const int kb = u >> 2, c = u & 3;
     off = static_cast<uint32_t>(kb) * 144u;
     o1 = 16u + 32u * c;
-    sh = 16u * (c & 1);
-    hi = c >= 2;
+    Q4kSel sel;
+    sel.set(c);
+    o2 = sel.selP;
+    o3 = sel.selQ;
+    o4 = sel.mask;
+    sh = sel.sh;
     float sa = 0.f, sb = 0.f;
 #pragma unroll
     for (int l = 0; l < 32; ++l) {
@@ -787,7 +817,7 @@ struct UnitChain {
     const uint4 hd = *reinterpret_cast<const uint4*>(bp);
     const uint4 q0 = *reinterpret_cast<const uint4*>(bp + o1);
     const uint4 q1 = *reinterpret_cast<const uint4*>(bp + o1 + 16);
-    return q4k_chunk_dot(hd, q0, q1, x, x + 32, s[0], s[1], sh, hi);
+    return q4k_chunk_dot(hd, q0, q1, x, x + 32, s[0], s[1], o2, o3, sh, o4);
   }
 
   __device__ __forceinline__ float row_q6k(const uint8_t* rp) const {
