@@ -106,6 +106,25 @@ __device__ __forceinline__ void nibble_word_split(uint32_t w, const float* xl, c
   fma2(h0, h1, H1, H2, xh[1], xh[2]);
 }
 
+// The same byte split with scalar operations (immediate operands, no
+// register pairs to build): for the Q4_K chunk, where the measured mix of
+// scalar and packed FP instructions decodes faster than the packed split
+// (the Q4_0 and Q6_K decoders keep the packed form, faster there).
+__device__ __forceinline__ void nibble_word_split_scalar(uint32_t w, const float* xl,
+                                                         const float* xh, float& l0, float& l1,
+                                                         float& h0, float& h1) {
+  const float B0 = bits(w & 0xFFu), B3 = bits(w >> 24);          // p = 0, 0
+  const float B1 = bits(w & 0xFF00u), B2 = bits(w & 0xFF0000u);  // p = 8, 16
+  const float H0 = __fmul_rz(B0, exp2i(-4)), H3 = __fmul_rz(B3, exp2i(-4));
+  const float H1 = __fmul_rz(B1, exp2i(-12)), H2 = __fmul_rz(B2, exp2i(-20));
+  const float L0 = fmaf(H0, -16.f, B0), L3 = fmaf(H3, -16.f, B3);
+  const float L1 = fmaf(H1, -4096.f, B1), L2 = fmaf(H2, -1048576.f, B2);
+  fma2(l0, l1, L0, L3, xl[0], xl[3]);
+  fma2(l0, l1, L1, L2, xl[1], xl[2]);
+  fma2(h0, h1, H0, H3, xh[0], xh[3]);
+  fma2(h0, h1, H1, H2, xh[1], xh[2]);
+}
+
 // Which of the eight words of a 32-byte Q4_K chunk take the byte split (bit
 // k set: word k), the rest the in-place masks: a mix keeps both the integer
 // and the FMA pipe busy.
@@ -146,7 +165,7 @@ template <int k>
 __device__ __forceinline__ void q4k_word(uint32_t w, const float* xa, const float* xb, float& a0,
                                          float& a1, float& b0, float& b1) {
   if constexpr (q4k_word_split(k))
-    nibble_word_split(w, xa + 4 * k, xb + 4 * k, a0, a1, b0, b1);
+    nibble_word_split_scalar(w, xa + 4 * k, xb + 4 * k, a0, a1, b0, b1);
   else
     nibble_word(w, xa + 4 * k, xb + 4 * k, a0, a1, b0, b1);
 }
@@ -290,21 +309,27 @@ struct UnitQ4K {
 // scale of column group a is sc[(128h + 32a + 16m) / 16] = sc[8h + 2a + m]:
 // the unit's four scales share one 8-byte window, and one d serves all 64.
 // Blocks are 210 B, so a block starts on a 2-byte boundary: the lane loads
-// aligned words and funnel-shifts them.
+// aligned words and funnel-shifts them.  The aligned pointer is p minus its
+// misalignment (pointer arithmetic, not an integer round trip), so that a
+// pointer into shared memory stays one the compiler can load with LDS.
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t misalign4(const uint8_t* p) {
+  return static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p)) & 3u;
+}
+
 __device__ __forceinline__ void load8_a2(const uint8_t* p, uint32_t& w0, uint32_t& w1) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  const uint32_t* q = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-  const uint32_t s = static_cast<uint32_t>(a & 3u) * 8u;
+  const uint32_t m = misalign4(p);
+  const uint32_t* q = reinterpret_cast<const uint32_t*>(p - m);
+  const uint32_t s = m * 8u;
   const uint32_t r0 = q[0], r1 = q[1], r2 = q[2];
   w0 = __funnelshift_r(r0, r1, s);
   w1 = __funnelshift_r(r1, r2, s);
 }
 
 __device__ __forceinline__ void load16_a2(const uint8_t* p, uint32_t (&w)[4]) {
-  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-  const uint32_t* q = reinterpret_cast<const uint32_t*>(a & ~uintptr_t(3));
-  const uint32_t s = static_cast<uint32_t>(a & 3u) * 8u;
+  const uint32_t m = misalign4(p);
+  const uint32_t* q = reinterpret_cast<const uint32_t*>(p - m);
+  const uint32_t s = m * 8u;
   uint32_t r[5];
 #pragma unroll
   for (int k = 0; k < 5; ++k) r[k] = q[k];
@@ -312,9 +337,27 @@ __device__ __forceinline__ void load16_a2(const uint8_t* p, uint32_t (&w)[4]) {
   for (int k = 0; k < 4; ++k) w[k] = __funnelshift_r(r[k], r[k + 1], s);
 }
 
+// Register slot of column j (0..3) of the 4-column group gi = 4a + t inside
+// the unit's 64-float activation array (slot 16a + 4t + q6k_slot(gi, j)).
+// The packed FMAs take columns (0, 2) and (1, 3) of a group as register
+// pairs.  In the plain order (kQ4Pairs false) slot = j.  A decoder that also
+// runs Q4_K on the same array (UnitChain) stores the columns so that these
+// pairs fall on the slots the Q4_K decode pairs: slots (0, 3) / (1, 2) for
+// the groups of byte-split words, (0, 1) / (2, 3) for the in-place ones.  One
+// pairing for both formats lets the compiler keep every activation pair in
+// place instead of copying registers into pairs for one of them.
+template <bool kQ4Pairs>
+__host__ __device__ constexpr int q6k_slot(int gi, int j) {
+  return !kQ4Pairs ? j
+         : q4k_word_split(gi & 7) ? (j == 2 ? 3 : j == 3 ? 2 : j)
+                                  : (j == 1 ? 2 : j == 2 ? 1 : j);
+}
+
 // Dot product of one 64-column Q6_K unit (16 bytes of each of the two ql runs,
-// 16 bytes of qh, the 8 scale bytes of the half) with activations x[16a + i]
-// pre-scaled by 2^kE; sx32[a] carries the -32 offset.
+// 16 bytes of qh, the 8 scale bytes of the half) with activations pre-scaled
+// by 2^kE, column 16a + 4t + j in slot 16a + 4t + q6k_slot(4a + t, j);
+// sx32[a] carries the -32 offset.
+template <bool kQ4Pairs = false>
 __device__ __forceinline__ float q6k_unit_dot(const uint32_t (&A)[4], const uint32_t (&B)[4],
                                               const uint32_t (&Q)[4], uint32_t S0, uint32_t S1,
                                               uint32_t dbits, const float* x, const float* sx32,
@@ -346,8 +389,11 @@ __device__ __forceinline__ float q6k_unit_dot(const uint32_t (&A)[4], const uint
       float L0 = P0, L1 = P1;
       fma2(L0, L1, H0, H1, -256.f, -256.f);
       const float* xr = x + 16 * a + 4 * t;
-      fma2(p[a][0], p[a][1], L0, L1, xr[0], xr[2]);
-      fma2(p[a][0], p[a][1], H0, H1, xr[1], xr[3]);
+      const int gi = 4 * a + t;
+      fma2(p[a][0], p[a][1], L0, L1, xr[q6k_slot<kQ4Pairs>(gi, 0)],
+           xr[q6k_slot<kQ4Pairs>(gi, 2)]);
+      fma2(p[a][0], p[a][1], H0, H1, xr[q6k_slot<kQ4Pairs>(gi, 1)],
+           xr[q6k_slot<kQ4Pairs>(gi, 3)]);
     }
   }
   // scale of group a: byte 2a + m of the 8 scale bytes of half h
@@ -386,7 +432,7 @@ struct Q6kUnitGeom {
   }
 };
 
-template <class XU>
+template <bool kQ4Pairs = false, class XU>
 __device__ __forceinline__ void q6k_setup_x(const XU& xu, float* x, float* sx32) {
 #pragma unroll
   for (int a = 0; a < 4; ++a) {
@@ -395,7 +441,7 @@ __device__ __forceinline__ void q6k_setup_x(const XU& xu, float* x, float* sx32)
     for (int i = 0; i < 16; ++i) {
       const float v = xu(16 * a + i);
       s += v;
-      x[16 * a + i] = v * exp2i(kE);
+      x[16 * a + (i & ~3) + q6k_slot<kQ4Pairs>(4 * a + (i >> 2), i & 3)] = v * exp2i(kE);
     }
     sx32[a] = s * exp2i(5 - 60);
   }
@@ -433,9 +479,8 @@ struct UnitQ6K {
     load16_a2(bp + g.oB, f.B);
     load16_a2(bp + g.oQ, f.Q);
     load8_a2(bp + g.oS, f.S0, f.S1);
-    const uintptr_t da = reinterpret_cast<uintptr_t>(bp + 208);
-    const uint32_t dw = *reinterpret_cast<const uint32_t*>(da & ~uintptr_t(3));
-    f.dbits = dw >> ((da & 3u) * 8u);
+    const uint32_t md = misalign4(bp + 208);
+    f.dbits = *reinterpret_cast<const uint32_t*>(bp + 208 - md) >> (md * 8u);
   }
 
   __device__ __forceinline__ float compute(const Frag& f) const {
@@ -785,7 +830,7 @@ struct UnitChain {
     o3 = g.oQ;
     o4 = g.oS;
     sh = g.sshift;
-    q6k_setup_x(xu, x, s);
+    q6k_setup_x<true>(xu, x, s);
   }
 
   template <class XU>
@@ -827,9 +872,9 @@ struct UnitChain {
     load16_a2(bp + o2, B);
     load16_a2(bp + o3, Q);
     load8_a2(bp + o4, S0, S1);
-    const uintptr_t da = reinterpret_cast<uintptr_t>(bp + 208);
-    const uint32_t dw = *reinterpret_cast<const uint32_t*>(da & ~uintptr_t(3));
-    return q6k_unit_dot(A, B, Q, S0, S1, dw >> ((da & 3u) * 8u), x, s, sh);
+    const uint32_t md = misalign4(bp + 208);
+    const uint32_t dw = *reinterpret_cast<const uint32_t*>(bp + 208 - md);
+    return q6k_unit_dot<true>(A, B, Q, S0, S1, dw >> (md * 8u), x, s, sh);
   }
 };
 
