@@ -775,19 +775,6 @@ qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
     // ceil(R / (T * sms)) tile times on the CTAs that hold an extra tile.
     // T2 is a multiple of the rows that keep every tile's first byte 16-byte
     // aligned (the bulk copies need it; T is one already).
-    // At least two rows per row slot in a tile: the decode loop interleaves
-    // two rows' independent chains, and a tile that gives each slot one row
-    // runs that row alone (the O projection at Gemma-3-4B shapes: 10-row
-    // tiles for 10 slots; 20-row tiles measured 1105 -> 1057 us per token).
-    {
-      const int pairm = kinds[i].epi != EPI_STORE ? 2 : 1;
-      const int64_t RB = row_bytes_of(kinds[i].fmt, kinds[i].K);
-      while (pairm * tp.T < 2 * tp.G && 2 * tp.T * RB * pairm <= kChainTileTarget) {
-        tp.red_floats = tp.red_floats / tp.T * (2 * tp.T);
-        tp.T *= 2;
-        tp.stage_need = static_cast<uint32_t>(tp.T * RB * pairm);
-      }
-    }
     int T2 = tp.T, n1 = 0x7FFFFFFF;
     if (i != PH_QKV) {
       const int64_t R = kinds[i].rows;

@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <string>
 
@@ -72,7 +73,12 @@ inline bool plan_tiles(int fmt, int epi, int64_t K, int B, int64_t rows_hint, in
   // small matrices: aim for about one tile per CTA slot of the grid
   const int64_t per = (rows_hint + 2 * sms - 1) / (2 * static_cast<int64_t>(sms));
   const int64_t m_small = (per + T0 - 1) / T0;
+  const int64_t m_max = m;
   if (m_small >= 1 && m_small < m) m = m_small;
+  // but at least two rows per row slot: the decode loop interleaves two rows'
+  // independent chains, and a slot given one row runs it alone
+  const int64_t m_ilp = (2 * G + pairm * T0 - 1) / (pairm * T0);
+  if (m < m_ilp) m = std::min(m_ilp, m_max);
   tp.U = static_cast<int>(U);
   tp.G = static_cast<int>(G);
   tp.T = static_cast<int>(T0 * m);
