@@ -425,16 +425,29 @@ __device__ __forceinline__ bool consume_phase(const Phase& Pref, const Ring& Rre
 // order: float4 chunks c0, c0 + step, ... of the row (p 16-byte aligned),
 // summed lane-wise, then ((s0 + s1) + (s2 + s3)), then the member's share of
 // the n % 4 tail entries.
+// Chunks are loaded four at a time before they are added (the adds keep the
+// chunk order), so one shared-memory latency covers four chunks.
 __device__ __forceinline__ float quad_sum(const float* p, int c0, int n, int step) {
   float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
   const int nq = n >> 2;
-  for (int k = c0; k < nq; k += step) {
-    const float4 v = *reinterpret_cast<const float4*>(p + 4 * k);
+  auto add = [&](const float4 v) {
     s0 += v.x;
     s1 += v.y;
     s2 += v.z;
     s3 += v.w;
+  };
+  int k = c0;
+  for (; k + 3 * step < nq; k += 4 * step) {
+    const float4 a = *reinterpret_cast<const float4*>(p + 4 * k);
+    const float4 b = *reinterpret_cast<const float4*>(p + 4 * (k + step));
+    const float4 c = *reinterpret_cast<const float4*>(p + 4 * (k + 2 * step));
+    const float4 d = *reinterpret_cast<const float4*>(p + 4 * (k + 3 * step));
+    add(a);
+    add(b);
+    add(c);
+    add(d);
   }
+  for (; k < nq; k += step) add(*reinterpret_cast<const float4*>(p + 4 * k));
   float t = (s0 + s1) + (s2 + s3);
   for (int c = 4 * nq + c0; c < n; c += step) t += p[c];
   return t;
@@ -472,6 +485,7 @@ __device__ __forceinline__ bool reduce_phase(const Phase& Pref, const Ring& Rref
   const int U = P.U, UP = red_pitch(P.U);
   const bool pair = P.epi != EPI_STORE;
   const int slots = pair ? 2 * P.T : P.T;
+  int cached_n_out = -1, lg = 5;
   for (int t = cta; t < P.n_tiles; t += P.ncta) {
     const uint32_t s = pos.s;
     if (!mbar_wait(&R.ready[s], pos.ph)) {
@@ -481,17 +495,24 @@ __device__ __forceinline__ bool reduce_phase(const Phase& Pref, const Ring& Rref
     const TileRef tr = tile_ref(P, t);
     const float* red = R.red + static_cast<size_t>(s) * R.red_floats;
     const int n_out = P.B * tr.nrows;
-    int gsz = 32;
-    while (gsz > 1 && gsz * n_out > 32) gsz >>= 1;
-    const int per_pass = 32 / gsz;
-    const int sub = lane % gsz;
+    // lane grouping: recomputed only when the tile's row count changes (the
+    // balanced last round, a segment's end); the reducer's code is a serial
+    // chain of dependent instructions, on the critical path at a phase's end
+    if (n_out != cached_n_out) {
+      cached_n_out = n_out;
+      lg = 5;
+      while (lg > 0 && (n_out << lg) > 32) --lg;
+    }
+    const int per_pass = 32 >> lg;
+    const int sub = lane & ((1 << lg) - 1);
     for (int base = 0; base < n_out; base += per_pass) {
-      const int oi = base + lane / gsz;
+      const int oi = base + (lane >> lg);
       const bool valid = oi < n_out;
-      const int ob = valid ? oi / tr.nrows : 0;
+      const int ob = (valid && P.B > 1) ? oi / tr.nrows : 0;
       const int o = valid ? oi - ob * tr.nrows : 0;
       const float* rr = red + (ob * slots + o) * UP;
       float v = 0.f, v2 = 0.f;
+      const int gsz = 1 << lg;
       if (valid) {
         v = quad_sum(rr, sub, U, gsz);
         if (pair) v2 = quad_sum(rr + P.T * UP, sub, U, gsz);
