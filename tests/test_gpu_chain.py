@@ -7,12 +7,8 @@ relative error per element (the plain projections' 1e-5 * sum|w x| is
 smaller); the RMS norm divides by rms(.) of the whole vector, so a relative
 error e in every element moves the normalised element by at most e * |a_i|
 plus e * rms(a) through the scale; the input norms feed the next matvec with
-1e-5 relative error, inside the same budget.  The kernel applies an input
-norm's scalar inv = 1/rms after the product (inv * (W (r . w)) instead of
-W (inv * r . w)): the product's error bound sum|W_ij r_j w_j| times inv is
-exactly the bound sum|w x| of the normalised input, and the extra rounding
-of inv and of the final multiply adds 2^-23 relative, far inside 1e-5.  The
-two f32 residual adds round by 2^-24 (|h| + |a| + |b|) at most.  Per element:
+1e-5 relative error, inside the same budget; the two f32 residual adds round
+by 2^-24 (|h| + |a| + |b|) at most.  Per element:
     |h'_gpu - h'_ref| <= 1e-4 * (|h| + |a| + |b|) + 1e-4 * (rms(a) + rms(b))
 checked teacher-forced: the oracle runs each layer on the GPU's input to that
 layer.  One launch over L layers must equal L single-layer launches bit for bit
