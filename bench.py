@@ -224,9 +224,9 @@ def cpu_oracle_sample(max_seconds: float = 15.0):
     whole decoder layers of the chain workload.  Two figures: one host thread
     over up to 34 layers (at most ~max_seconds), and every host core at once,
     one process per core (spawned, so no process is forked from this one after
-    its GPU work), each running its own layers; the all-core value is the
-    packed bytes of all layers over the wall time from the common start to the
-    last finish."""
+    its GPU work), each running its own layers (about max_seconds of CPU work
+    in all); the all-core value is the packed bytes of all layers over the
+    wall time from the common start to the last finish."""
     import multiprocessing as mp
 
     import oracle
@@ -249,7 +249,10 @@ def cpu_oracle_sample(max_seconds: float = 15.0):
 
     cores = host_cores()
     n_proc = max(1, min(cores, N_LAYERS))
-    per_proc = max(1, -(-N_LAYERS // n_proc))            # about 34 layers in all
+    # about max_seconds of CPU work over all processes (each layer costs about
+    # what it cost the single thread), at most 34 layers per process
+    t_layer = elapsed / layers_done
+    per_proc = int(max(1, min(N_LAYERS, round(max_seconds / (n_proc * t_layer)))))
     ctx = mp.get_context("spawn")
     barrier = ctx.Barrier(n_proc)
     out_q = ctx.Queue()
