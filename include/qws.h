@@ -221,9 +221,10 @@ qws_status qws_q4k_prefill_matmul(const void* W, const float* X, float* Y, int64
  *   position pos: for i < rot_dim / 2, theta_i = pos * base^(-2i / rot_dim),
  *   (x_i, x_{i+rot/2}) <- (x_i cos - x_{i+rot/2} sin, x_i sin + x_{i+rot/2} cos);
  *   dimensions rot_dim.. unchanged (partial RoPE).  Angle, sine, cosine and
- *   the rotation in f64, rounded once to f32.  rot_dim even, 0 < rot_dim <=
- *   head_dim; pos >= 0; base > 0.  (The pages give no formula: this is the
- *   standard half-split rotary embedding.)
+ *   the rotation in f64, rounded once to f32 (the angles' sines and cosines
+ *   are evaluated on the host, once per call).  rot_dim even, 0 < rot_dim <=
+ *   min(head_dim, 512), else QWS_ERR_SHAPE; pos >= 0; base > 0.  (The pages
+ *   give no formula: this is the standard half-split rotary embedding.)
  * qws_kv_append: k, v [n_kv_heads][head_dim] written at position pos of the
  *   caches (0 <= pos < max_seq).
  * qws_kv_attention: one query token q [n_q_heads][head_dim] over cache
@@ -382,9 +383,11 @@ qws_status qws_decode_chain(const qws_layer* layers, int n_layers, float* h,
  *   the host) to f32 [n_kv_heads][max_seq][head_dim], 16-byte aligned,
  *   caller-owned; positions 0..pos-1 are read, position pos is written.
  *   ws: device, >= qws_decode_kv_workspace_bytes(dims, max_seq) bytes,
- *   16-byte aligned; on return it holds, for the last layer, q and k (after
- *   RoPE) then v at float offset 0 (contiguous: n_q_heads*head_dim, then
- *   n_kv_heads*head_dim twice).
+ *   16-byte aligned, scratch (its contents on return are unspecified).
+ *   Runs on the decode chain's kernel (one launch per layer for the
+ *   projections, norms and residuals, with the RoPE / append and attention
+ *   launches between them); layers whose down projections differ in format
+ *   take a sequence of standalone launches with the same results' bounds.
  *   Shapes: as qws_decode_chain; head_dim in {32, 64, 128, 256};
  *   n_q_heads / n_kv_heads in 1..4; 0 <= pos < max_seq; rot_dim even in
  *   (0, head_dim]; rope_base > 0; attn_scale finite; softcap >= 0 (0 = off).

@@ -318,8 +318,10 @@ qws_status qws_rope_at_pos(float* x, int n_heads, int head_dim, int rot_dim, int
                            double base, qws_stream stream) {
   const char* fn = "qws_rope_at_pos";
   QWS_CHECK_F(x);
-  if (n_heads < 1 || head_dim < 2 || rot_dim < 2 || rot_dim % 2 || rot_dim > head_dim)
-    return fail(QWS_ERR_SHAPE, "%s: need n_heads >= 1 and an even 0 < rot_dim <= head_dim", fn);
+  if (n_heads < 1 || head_dim < 2 || rot_dim < 2 || rot_dim % 2 || rot_dim > head_dim ||
+      rot_dim > 512)
+    return fail(QWS_ERR_SHAPE,
+                "%s: need n_heads >= 1 and an even 0 < rot_dim <= min(head_dim, 512)", fn);
   if (pos < 0 || !(base > 0.0)) return fail(QWS_ERR_SHAPE, "%s: need pos >= 0 and base > 0", fn);
   cudaError_t e = qws::launch_rope(x, n_heads, head_dim, rot_dim, pos, base,
                                    reinterpret_cast<cudaStream_t>(stream));

@@ -18,7 +18,8 @@
 //     softmax update (running max m, sum l, output acc).  The 16 warps are
 //     merged in shared memory in a fixed order and the CTA writes its
 //     (m, l, acc) partial to the workspace.
-//   * kernel 2, one CTA per query head: merges the splits in order:
+//   * kernel 2, one CTA per query head and 32 columns: merges the splits
+//     (eight interleaved partial sums per column, added in a fixed order):
 //     out = sum_j e^(m_j - M) acc_j / sum_j e^(m_j - M) l_j.
 // Everything is in a fixed order, so results are identical run to run.
 #include <cuda_runtime.h>
@@ -39,9 +40,26 @@ constexpr uint32_t kAttStageBytes = 64 * 1024;  // P k rows + P v rows, P = 8192
 
 // ------------------------------------------------------------------ rope
 // (x_i, x_{i+r/2}) rotated by theta_i = pos * base^(-2i/r), i < r/2, every head;
-// the angle and its sine / cosine in f64, the rotation in f64, rounded once.
+// the angle and its sine / cosine in f64 (computed once per launch on the
+// host: FP64 arithmetic on this GPU is slow), the rotation in f64, rounded
+// once.
+constexpr int kMaxRotDim = 512;
+struct RopeTable {
+  double c[kMaxRotDim / 2], s[kMaxRotDim / 2];   // cos / sin of pos * base^(-2i / rot_dim)
+};
+
+static RopeTable rope_table(int rot_dim, int64_t pos, double base) {
+  RopeTable tab;
+  for (int i = 0; i < rot_dim / 2; ++i) {
+    const double theta = static_cast<double>(pos) * std::pow(base, -2.0 * i / rot_dim);
+    tab.c[i] = std::cos(theta);
+    tab.s[i] = std::sin(theta);
+  }
+  return tab;
+}
+
 __global__ void rope_kernel(float* __restrict__ x, int n_heads, int head_dim, int rot_dim,
-                            int64_t pos, double base) {
+                            const __grid_constant__ RopeTable tab) {
   pdl_launch_dependents();
   pdl_wait();
   const int half = rot_dim / 2;
@@ -50,10 +68,7 @@ __global__ void rope_kernel(float* __restrict__ x, int n_heads, int head_dim, in
        t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int h = static_cast<int>(t / half);
     const int i = static_cast<int>(t - static_cast<int64_t>(h) * half);
-    const double theta =
-        static_cast<double>(pos) * pow(base, -2.0 * static_cast<double>(i) / rot_dim);
-    double s, c;
-    sincos(theta, &s, &c);
+    const double s = tab.s[i], c = tab.c[i];
     float* xh = x + static_cast<int64_t>(h) * head_dim;
     const double a = xh[i], b = xh[i + half];
     xh[i] = static_cast<float>(a * c - b * s);
@@ -84,15 +99,44 @@ struct AttParams {
   const float* vc;
   float* part;         // [n_kv][splits][group][hd + 2]: acc..., m, l
   float* out;          // [n_q][hd]
+  unsigned long long* out_words;   // or, when set: {value, stamp} words [n_q][hd]
+  unsigned stamp;
   int n_q, n_kv, hd, group, splits;
   int64_t max_seq, n_ctx;
   float scale, softcap;
+  // RoPE and append fused in (the decode step on the chain kernel), when qw
+  // is set: q comes as {value, stamp} words, rotated at pos here; k and v of
+  // position pos come as words too: the CTA whose split holds pos rotates k,
+  // writes k and v into the caches (kc_w, vc_w) and uses them for that row
+  // in place of the cache row its copy warp loaded.
+  // The rotation here is in f32 (FP64 arithmetic on this GPU is slow
+  // enough that the f64 rotation of rope_kernel tripled the split's time):
+  // cosine and sine of the f64 angle rounded to f32, then a * c - b * s by
+  // one product and one FMA, a few units of 2^-24 relative to |a| + |b|.
+  const unsigned long long *qw, *kw, *vw;
+  float *kc_w, *vc_w;
+  int64_t pos;
+  int rot_dim;
+  float tc[kMaxRotDim / 2], ts[kMaxRotDim / 2];
 };
+
+// Element i of a head of words x rotated at pos (f32; see AttParams).
+__device__ __forceinline__ float rope_word(const unsigned long long* x, int i, int rot_dim,
+                                           const float* tc, const float* ts) {
+  auto val = [](unsigned long long w) { return __uint_as_float(static_cast<unsigned>(w)); };
+  if (i >= rot_dim) return val(x[i]);
+  const int half = rot_dim / 2;
+  const int j = i < half ? i : i - half;
+  const float a = val(x[j]), b = val(x[j + half]);
+  return i < half ? fmaf(a, tc[j], -(b * ts[j])) : fmaf(a, ts[j], b * tc[j]);
+}
 
 template <int kPL, int kG>   // columns per lane = hd / 32; query heads per kv head
 __global__ void __launch_bounds__(kAttThreads, 1) kv_attention_split_kernel(
     const __grid_constant__ AttParams p) {
   __shared__ float sm_m[kAttWarps][kG], sm_l[kAttWarps][kG];
+  // fused mode: the group's rotated q, and k (rotated) and v of position pos
+  __shared__ float sq[kG][kPL * 32], skv[2][kPL * 32];
   __shared__ __align__(8) uint64_t full[kAttStages], empty[kAttStages];
   extern __shared__ __align__(128) uint8_t att_ring[];   // kAttStages x kAttStageBytes
   const int warp = static_cast<int>(threadIdx.x >> 5) - 1;   // -1: the copy warp
@@ -146,14 +190,43 @@ __global__ void __launch_bounds__(kAttThreads, 1) kv_attention_split_kernel(
     return;
   }
   const int c0 = lane * kPL;
+  const bool fused = p.qw != nullptr;
+  // fused mode: does this CTA's share of the blocks hold position pos?
+  const bool has_pos = fused && (p.pos / P) % p.splits == j;
+  if (fused) {
+    // every element by one consumer thread, so the loads of all of them are
+    // in flight together; then the warps read their columns from shared memory
+    const int ct = static_cast<int>(threadIdx.x) - 32;
+    for (int e = ct; e < kG * p.hd; e += kAttWarps * 32) {
+      const int h = e / p.hd, i = e - h * p.hd;
+      sq[h][i] = rope_word(p.qw + static_cast<int64_t>(g * G + h) * p.hd, i, p.rot_dim, p.tc,
+                           p.ts);
+    }
+    if (has_pos) {
+      const int64_t row = (static_cast<int64_t>(g) * p.max_seq + p.pos) * p.hd;
+      for (int i = ct; i < p.hd; i += kAttWarps * 32) {
+        const float kr =
+            rope_word(p.kw + static_cast<int64_t>(g) * p.hd, i, p.rot_dim, p.tc, p.ts);
+        const float vr =
+            __uint_as_float(static_cast<unsigned>(p.vw[static_cast<int64_t>(g) * p.hd + i]));
+        skv[0][i] = kr;
+        skv[1][i] = vr;
+        p.kc_w[row + i] = kr;
+        p.vc_w[row + i] = vr;
+      }
+    }
+    bar_sync(1, kAttWarps * 32);
+  }
   float q[kG][kPL], acc[kG][kPL], m[kG], l[kG];
 #pragma unroll
   for (int h = 0; h < kG; ++h) {
     m[h] = -INFINITY;
     l[h] = 0.f;
+    const int64_t hq = static_cast<int64_t>(g * G + h);
 #pragma unroll
     for (int c = 0; c < kPL; ++c) {
-      q[h][c] = p.q[static_cast<int64_t>(g * G + h) * p.hd + c0 + c] * p.scale;
+      const float qv = fused ? sq[h][c0 + c] : p.q[hq * p.hd + c0 + c];
+      q[h][c] = qv * p.scale;
       acc[h][c] = 0.f;
     }
   }
@@ -170,6 +243,13 @@ __global__ void __launch_bounds__(kAttThreads, 1) kv_attention_split_kernel(
     const float* vst = kst + P * kPL * 32;
     for (int r = warp; r < rows; r += kAttWarps) {
       float kr[kPL], vr[kPL];
+      if (has_pos && ta + r == p.pos) {
+#pragma unroll
+        for (int c = 0; c < kPL; ++c) {
+          kr[c] = skv[0][c0 + c];
+          vr[c] = skv[1][c0 + c];
+        }
+      } else {
 #pragma unroll
       for (int c = 0; c < kPL; c += (kPL % 4 == 0 ? 4 : 1)) {
         if constexpr (kPL % 4 == 0) {
@@ -181,6 +261,7 @@ __global__ void __launch_bounds__(kAttThreads, 1) kv_attention_split_kernel(
           kr[c] = kst[r * kPL * 32 + c0 + c];
           vr[c] = vst[r * kPL * 32 + c0 + c];
         }
+      }
       }
 #pragma unroll
       for (int h = 0; h < kG; ++h) {
@@ -238,27 +319,71 @@ __global__ void __launch_bounds__(kAttThreads, 1) kv_attention_split_kernel(
   }
 }
 
-__global__ void kv_attention_merge_kernel(const __grid_constant__ AttParams p) {
+// Partials of at most kMaxSplits splits (kv_attention_splits never exceeds
+// the grid of 152 CTAs).  Grid (n_q, ceil(hd / 32)), 256 threads: CTA
+// (hq, y) merges columns 32 y .. 32 y + 31 of query head hq; thread (s, c)
+// adds the splits j = s, s + 8, ... of column c (their loads all in flight
+// at once), then the eight sums are added in order s = 0..7.
+//   out = sum_j e^(m_j - M) acc_j / sum_j e^(m_j - M) l_j,  M = max_j m_j.
+constexpr int kMaxSplits = 256;
+constexpr int kMergeLanes = 8;   // split lanes per column
+
+__global__ void __launch_bounds__(256) kv_attention_merge_kernel(const __grid_constant__ AttParams p) {
+  __shared__ float sm[kMaxSplits], sl[kMaxSplits], sf[kMaxSplits];
+  __shared__ float red[kMergeLanes][32];
+  __shared__ float sL;
   pdl_launch_dependents();
   pdl_wait();
   const int hq = blockIdx.x;                 // query head
   const int g = hq / p.group, h = hq - g * p.group;
   const int64_t stride = static_cast<int64_t>(p.group) * (p.hd + 2);
   const float* base = p.part + (static_cast<int64_t>(g) * p.splits * p.group + h) * (p.hd + 2);
-  float M = -INFINITY;
-  for (int j = 0; j < p.splits; ++j) M = fmaxf(M, base[j * stride + p.hd]);
-  float L = 0.f;
-  for (int j = 0; j < p.splits; ++j) {
-    const float mj = base[j * stride + p.hd];
-    if (mj != -INFINITY) L = fmaf(base[j * stride + p.hd + 1], expf(mj - M), L);
+  for (int j = threadIdx.x; j < p.splits; j += blockDim.x) {
+    sm[j] = base[j * stride + p.hd];
+    sl[j] = base[j * stride + p.hd + 1];
   }
-  for (int i = threadIdx.x; i < p.hd; i += blockDim.x) {
-    float a = 0.f;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = -INFINITY;
+    for (int j = 0; j < p.splits; ++j) M = fmaxf(M, sm[j]);
+    float L = 0.f;
     for (int j = 0; j < p.splits; ++j) {
-      const float mj = base[j * stride + p.hd];
-      if (mj != -INFINITY) a = fmaf(base[j * stride + i], expf(mj - M), a);
+      const float f = sm[j] != -INFINITY ? expf(sm[j] - M) : 0.f;   // 0: an empty split
+      sf[j] = f;
+      L = fmaf(sl[j], f, L);
     }
-    p.out[static_cast<int64_t>(hq) * p.hd + i] = a / L;
+    sL = L;
+  }
+  __syncthreads();
+  const int c = threadIdx.x & 31, sidx = threadIdx.x >> 5;
+  const int i = blockIdx.y * 32 + c;
+  float a = 0.f;
+  if (i < p.hd) {
+    int j = sidx;
+    for (; j + 3 * kMergeLanes < p.splits; j += 4 * kMergeLanes) {
+      const float a0 = base[j * stride + i];
+      const float a1 = base[(j + kMergeLanes) * stride + i];
+      const float a2 = base[(j + 2 * kMergeLanes) * stride + i];
+      const float a3 = base[(j + 3 * kMergeLanes) * stride + i];
+      a = fmaf(a0, sf[j], a);
+      a = fmaf(a1, sf[j + kMergeLanes], a);
+      a = fmaf(a2, sf[j + 2 * kMergeLanes], a);
+      a = fmaf(a3, sf[j + 3 * kMergeLanes], a);
+    }
+    for (; j < p.splits; j += kMergeLanes) a = fmaf(base[j * stride + i], sf[j], a);
+  }
+  red[sidx][c] = a;
+  __syncthreads();
+  if (sidx == 0 && i < p.hd) {
+    float t = 0.f;
+    for (int s2 = 0; s2 < kMergeLanes; ++s2) t += red[s2][c];
+    const float r = t / sL;
+    if (p.out_words)
+      p.out_words[static_cast<int64_t>(hq) * p.hd + i] =
+          static_cast<unsigned long long>(__float_as_uint(r)) |
+          (static_cast<unsigned long long>(p.stamp) << 32);
+    else
+      p.out[static_cast<int64_t>(hq) * p.hd + i] = r;
   }
 }
 
@@ -298,8 +423,9 @@ cudaError_t launch_rope(float* x, int n_heads, int head_dim, int rot_dim, int64_
   const int64_t n = static_cast<int64_t>(n_heads) * (rot_dim / 2);
   const int blocks =
       static_cast<int>(std::max<int64_t>(1, std::min<int64_t>((n + 255) / 256, 1024)));
+  if (rot_dim > kMaxRotDim) return cudaErrorInvalidValue;
   return launch_pdl_att(rope_kernel, dim3(blocks), 256, 0, st, x, n_heads, head_dim, rot_dim,
-                        pos, base);
+                        rope_table(rot_dim, pos, base));
 }
 
 cudaError_t launch_kv_append(float* kc, float* vc, const float* k, const float* v, int n_kv,
@@ -324,13 +450,36 @@ static cudaError_t launch_split(const AttParams& p, dim3 grid, cudaStream_t st) 
 
 cudaError_t launch_kv_attention(const float* q, const float* kc, const float* vc, float* out,
                                 int n_q, int n_kv, int head_dim, int64_t max_seq, int64_t n_ctx,
-                                float scale, float softcap, float* ws, cudaStream_t st) {
+                                float scale, float softcap, float* ws, cudaStream_t st,
+                                unsigned long long* out_words, unsigned stamp,
+                                const KvFuse* fuse) {
   AttParams p;
+  p.qw = p.kw = p.vw = nullptr;
+  p.kc_w = p.vc_w = nullptr;
+  p.pos = 0;
+  p.rot_dim = 0;
+  if (fuse) {
+    if (fuse->rot_dim > kMaxRotDim) return cudaErrorInvalidValue;
+    p.qw = fuse->q;
+    p.kw = fuse->k;
+    p.vw = fuse->v;
+    p.kc_w = fuse->kc;
+    p.vc_w = fuse->vc;
+    p.pos = fuse->pos;
+    p.rot_dim = fuse->rot_dim;
+    const RopeTable tab = rope_table(fuse->rot_dim, fuse->pos, fuse->base);
+    for (int i = 0; i < fuse->rot_dim / 2; ++i) {
+      p.tc[i] = static_cast<float>(tab.c[i]);
+      p.ts[i] = static_cast<float>(tab.s[i]);
+    }
+  }
   p.q = q;
   p.kc = kc;
   p.vc = vc;
   p.part = ws;
   p.out = out;
+  p.out_words = out_words;
+  p.stamp = stamp;
   p.n_q = n_q;
   p.n_kv = n_kv;
   p.hd = head_dim;
@@ -353,7 +502,8 @@ cudaError_t launch_kv_attention(const float* q, const float* kc, const float* vc
     default: return cudaErrorInvalidValue;
   }
   if (e != cudaSuccess) return e;
-  return launch_pdl_att(kv_attention_merge_kernel, dim3(n_q), 256, 0, st, p);
+  return launch_pdl_att(kv_attention_merge_kernel, dim3(n_q, (head_dim + 31) / 32), 256, 0, st,
+                        p);
 }
 
 unsigned read_clear_attention_errors() {

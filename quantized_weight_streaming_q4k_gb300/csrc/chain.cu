@@ -74,9 +74,16 @@ struct ChainParams {
   KindPlan kp[4];
   // stamped workspace vectors (device); hin and h1 hold two buffers of H each
   Word *q, *k, *v, *o, *m, *f, *hin, *h1;
-  unsigned* prologues;        // [4 * n_layers]: CTAs done with each phase's prologue (zeroed per launch)
+  unsigned* prologues;        // [4 * n_layers]: CTAs done with each phase's prologue (zeroed per token)
   float* h;                   // the caller's h (in: layer 0 input, out: chain output)
   uint32_t S, stage_bytes, red_floats, xs_floats;
+  // This launch runs phases [ph_begin, ph_end) of the token; several launches
+  // with the same parameters and workspace (cleared once per token) run a
+  // token in pieces.  With att set (decode over a KV cache), the O phase of
+  // layer l reads the attention output there (q_dim stamped words, stamp
+  // 4 l + 1, written between launches) instead of gathering v.
+  int ph_begin, ph_end;
+  Word* att;
 };
 
 __device__ __forceinline__ Word ld_word(const Word* p) {
@@ -114,7 +121,8 @@ __device__ __forceinline__ bool wait_prologues(const ChainParams& p, int ph) {
   return true;
 }
 
-// Phase p = 4 * layer + kind; its outputs carry stamp p + 1.
+// Phase p = 4 * layer + kind; its outputs carry stamp p + 1.  get(p) takes
+// the absolute phase index; Range views this launch's phases from 0.
 struct ChainPhases {
   const ChainParams* p;
   __device__ __forceinline__ int count() const { return 4 * p->n_layers; }
@@ -167,6 +175,12 @@ struct ChainPhases {
     P.n_tiles = P.seg[0].tiles + P.seg[1].tiles + P.seg[2].tiles;
     return P;
   }
+  struct Range {
+    const ChainPhases* all;
+    int begin, end;
+    __device__ __forceinline__ int count() const { return end - begin; }
+    __device__ __forceinline__ Phase get(int i) const { return all->get(begin + i); }
+  };
 };
 
 // Reducer epilogue: stores each reduced row (GEGLU for the gate/up pair) as a
@@ -396,7 +410,7 @@ __device__ __forceinline__ bool stage_gather(const Ring& R, int US, const Word* 
 // 34-layer token once both are inlined).  kWide: hidden > 8 * 320 (16 values
 // per thread in the residual / norm step); a separate instantiation, so the
 // common case carries none of its registers.
-template <bool kWide>
+template <bool kWide, bool kKV>
 __device__ __forceinline__ bool chain_prologue(const ChainParams& p, int ph, const Ring& R,
                                             float* wsum, bool q6, int ctid, int C) {
   const int l = ph >> 2, kind = ph & 3;
@@ -453,7 +467,10 @@ __device__ __forceinline__ bool chain_prologue(const ChainParams& p, int ph, con
                                   wn, store, static_cast<unsigned>(ph + 1), war, war_seen, US,
                                   ctid);
   } else if (kind == PH_O) {
-    ok = stage_gather<8>(R, US, p.v, prev, kp.K, p.head_dim, p.n_q_heads / p.n_kv_heads, ctid);
+    if constexpr (kKV)
+      ok = stage_stamped<UnitQ4K, 16>(R, US, p.att, prev, kp.K, ctid);
+    else
+      ok = stage_gather<8>(R, US, p.v, prev, kp.K, p.head_dim, p.n_q_heads / p.n_kv_heads, ctid);
   } else if (q6) {
     ok = stage_stamped<UnitQ6K, 16>(R, US, p.m, prev, kp.K, ctid);
   } else {
@@ -549,7 +566,7 @@ __device__ __forceinline__ void prefetch_l2(const float* w, int64_t n) {
 }
 
 // ------------------------------------------------------------------ kernel
-template <bool kWide>
+template <bool kWide, bool kKV>
 __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
     chain_kernel(const __grid_constant__ ChainParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -560,7 +577,6 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
   if (threadIdx.x == 0) ring_init(R, C / 32);
   __syncthreads();
   const ChainPhases phases{&p};
-  const int nph = phases.count();
 
   if (threadIdx.x < kProducerThreads) {
     if (threadIdx.x == 0) {
@@ -571,7 +587,7 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
         prefetch_l2(p.L[l].w_pf, p.H * 4);
         prefetch_l2(p.L[l].w_pff, p.H * 4);
       }
-      run_producer(phases, R, &g_err_chain);
+      run_producer(ChainPhases::Range{&phases, p.ph_begin, p.ph_end}, R, &g_err_chain);
     }
     return;
   }
@@ -579,7 +595,7 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
   RingPos pos;
   if (threadIdx.x < kRoleThreads) {
     // ---------------- reducer: sums and stamped stores, phase after phase
-    for (int ph = 0; ph < nph; ++ph) {
+    for (int ph = p.ph_begin; ph < p.ph_end; ++ph) {
       const Phase P = phases.get(ph);
       // (one load, normally already satisfied; it overlaps the consumers'
       // work on the phase's first tile)
@@ -592,10 +608,10 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
   // ---------------- consumers
   const int ctid = static_cast<int>(threadIdx.x) - kRoleThreads;
   const bool down_q6k = p.kp[PH_DOWN].fmt == 14;
-  for (int ph = 0; ph < nph; ++ph) {
+  for (int ph = p.ph_begin; ph < p.ph_end; ++ph) {
     const Phase P = phases.get(ph);
     const bool q6 = (ph & 3) == PH_DOWN && down_q6k;
-    if (!chain_prologue<kWide>(p, ph, R, wsum, q6, ctid, C)) return;
+    if (!chain_prologue<kWide, kKV>(p, ph, R, wsum, q6, ctid, C)) return;
     const unsigned long long r = chain_consume(
         P.fmt, P.epi, P.nseg, static_cast<int>(P.seg[0].rows), static_cast<int>(P.seg[1].rows),
         static_cast<int>(P.seg[2].rows), P.seg[0].tiles, P.seg[1].tiles, P.seg[2].tiles, P.T,
@@ -607,7 +623,7 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
     pos.n = static_cast<uint32_t>((r >> 16) & 0xFFFFFFFFu);
     if ((r >> 63) == 0) return;
   }
-  if (blockIdx.x == gridDim.x - 1) {
+  if (p.ph_end == 4 * p.n_layers && blockIdx.x == gridDim.x - 1) {
     if constexpr (kWide)
       chain_final<16>(p, wsum, ctid, C);
     else
@@ -657,56 +673,67 @@ unsigned read_clear_chain_errors() {
 
 using namespace qws;
 
-// Argument checks and launch (called by qws_decode_chain in abi.cu); kept in
-// this translation unit with the workspace layout it depends on.
-qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
-                                 const qws_dims* d, void* ws, size_t ws_bytes, cudaStream_t st,
-                                 std::string& err) {
+namespace {
+
+// One prepared chain: parameters, kernel and launch shape.  Launches of
+// phase ranges of one token share it (and the workspace, cleared once).
+struct ChainLaunch {
+  ChainParams p;
+  const void* kfn = nullptr;
+  int grid = 0, threads = 0;
+  size_t smem = 0, clear_bytes = 0;
+};
+
+// Argument checks, parameters and launch shape; ws holds the chain's words.
+// kv: the O phase reads an attention output (ChainParams::att) instead of
+// gathering v (the decode step over a KV cache).
+qws_status chain_prepare(const char* fn, const qws_layer* layers, int n_layers, float* h,
+                         const qws_dims* d, void* ws, size_t ws_bytes, bool kv, ChainLaunch& cl,
+                         std::string& err) {
   auto bad = [&](qws_status s, const char* m) {
-    err = m;
+    err = std::string(fn) + ": " + m;
     return s;
   };
-  if (!layers || !h || !d || !ws) return bad(QWS_ERR_NULL, "qws_decode_chain: NULL argument");
+  if (!layers || !h || !d || !ws) return bad(QWS_ERR_NULL, "NULL argument");
   if (n_layers < 1 || n_layers > kMaxLayers)
-    return bad(QWS_ERR_SHAPE, "qws_decode_chain: n_layers must be in [1, 64]");
+    return bad(QWS_ERR_SHAPE, "n_layers must be in [1, 64]");
   const int64_t H = d->hidden, I = d->inter;
   if (d->n_q_heads <= 0 || d->n_kv_heads <= 0 || d->head_dim <= 0 ||
       d->n_q_heads % d->n_kv_heads)
-    return bad(QWS_ERR_SHAPE, "qws_decode_chain: bad head counts");
+    return bad(QWS_ERR_SHAPE, "bad head counts");
   const int64_t QD = static_cast<int64_t>(d->n_q_heads) * d->head_dim;
   const int64_t KD = static_cast<int64_t>(d->n_kv_heads) * d->head_dim;
   auto ok_dim = [](int64_t v) { return v > 0 && v % 256 == 0 && v <= 20480; };
   if (!ok_dim(H) || !ok_dim(I) || !ok_dim(QD) || KD % 64 || KD <= 0 || QD > 4 * H || KD > 4 * H)
     return bad(QWS_ERR_SHAPE,
-               "qws_decode_chain: hidden, inter, q_dim must be multiples of 256 in (0, 20480], "
+               "hidden, inter, q_dim must be multiples of 256 in (0, 20480], "
                "q_dim and kv_dim <= 4 * hidden");
-  if (H > kMaxChainHidden) return bad(QWS_ERR_SHAPE, "qws_decode_chain: hidden must be <= 5120");
-  if (!(d->eps >= 0.f)) return bad(QWS_ERR_SHAPE, "qws_decode_chain: eps must be >= 0");
+  if (H > kMaxChainHidden) return bad(QWS_ERR_SHAPE, "hidden must be <= 5120");
+  if (!(d->eps >= 0.f)) return bad(QWS_ERR_SHAPE, "eps must be >= 0");
   if (reinterpret_cast<uintptr_t>(h) % 4 || reinterpret_cast<uintptr_t>(ws) % 16)
-    return bad(QWS_ERR_ALIGN, "qws_decode_chain: h must be 4-byte and ws 16-byte aligned");
-  if (ws_bytes < chain_workspace_bytes(H, I))
-    return bad(QWS_ERR_WORKSPACE, "qws_decode_chain: workspace too small");
-  ChainParams p;
+    return bad(QWS_ERR_ALIGN, "h must be 4-byte and ws 16-byte aligned");
+  if (ws_bytes < chain_workspace_bytes(H, I)) return bad(QWS_ERR_WORKSPACE, "workspace too small");
+  ChainParams& p = cl.p;
   std::memset(&p, 0, sizeof(p));
   for (int l = 0; l < n_layers; ++l) {
     const qws_layer& L = layers[l];
     const void* ws8[7] = {L.Wq, L.Wk, L.Wv, L.Wo, L.Wg, L.Wu, L.Wd};
     for (const void* w : ws8) {
-      if (!w) return bad(QWS_ERR_NULL, "qws_decode_chain: a weight pointer is NULL");
+      if (!w) return bad(QWS_ERR_NULL, "a weight pointer is NULL");
       if (reinterpret_cast<uintptr_t>(w) % 16)
-        return bad(QWS_ERR_ALIGN, "qws_decode_chain: weights must be 16-byte aligned");
+        return bad(QWS_ERR_ALIGN, "weights must be 16-byte aligned");
     }
     const float* nw[4] = {L.w_in, L.w_post_attn, L.w_pre_ffn, L.w_post_ffn};
     for (int i = 0; i < 4; ++i) {
       if (!nw[i] && (i == 0 || i == 2 || d->post_norms))
-        return bad(QWS_ERR_NULL, "qws_decode_chain: a norm weight pointer is NULL");
+        return bad(QWS_ERR_NULL, "a norm weight pointer is NULL");
       if (reinterpret_cast<uintptr_t>(nw[i]) % 4)
-        return bad(QWS_ERR_ALIGN, "qws_decode_chain: norm weights must be 4-byte aligned");
+        return bad(QWS_ERR_ALIGN, "norm weights must be 4-byte aligned");
     }
     if (L.fmt_qkv != QWS_Q4_K || L.fmt_o != QWS_Q4_K || L.fmt_gu != QWS_Q4_K ||
         (L.fmt_down != QWS_Q4_K && L.fmt_down != QWS_Q6_K) || L.fmt_down != layers[0].fmt_down)
       return bad(QWS_ERR_FORMAT,
-                 "qws_decode_chain: q/k/v/o/gate/up must be Q4_K; down Q4_K or Q6_K (same in "
+                 "q/k/v/o/gate/up must be Q4_K; down Q4_K or Q6_K (same in "
                  "every layer)");
     p.L[l] = ChainLayer{static_cast<const uint8_t*>(L.Wq), static_cast<const uint8_t*>(L.Wk),
                         static_cast<const uint8_t*>(L.Wv), static_cast<const uint8_t*>(L.Wo),
@@ -725,6 +752,8 @@ qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
   p.eps = d->eps;
   p.post_norms = d->post_norms ? 1 : 0;
   p.h = h;
+  p.ph_begin = 0;
+  p.ph_end = 4 * n_layers;
 
   // workspace carve-up (8-byte {value, stamp} words), then the counter
   Word* w = static_cast<Word*>(ws);
@@ -765,7 +794,7 @@ qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
     std::string why;
     if (!plan_tiles(kinds[i].fmt, kinds[i].epi, kinds[i].K, 1, kinds[i].rows, sms,
                     kChainTileTarget, tp, why)) {
-      err = "qws_decode_chain: " + why;
+      err = "" + why;
       return QWS_ERR_SHAPE;
     }
     // all kinds run with the same thread count: C = kMaxConsumers
@@ -804,37 +833,156 @@ qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
   while (p.S > 2 && ring_smem_bytes(p.S, p.stage_bytes, p.red_floats, p.xs_floats) + tail >
                         kSmemBudget)
     --p.S;
-  const size_t smem = ring_smem_bytes(p.S, p.stage_bytes, p.red_floats, p.xs_floats) + tail;
-  const int threads = kRoleThreads + kMaxConsumers;
+  cl.smem = ring_smem_bytes(p.S, p.stage_bytes, p.red_floats, p.xs_floats) + tail;
+  cl.threads = kRoleThreads + kMaxConsumers;
+  cl.clear_bytes = clear_bytes;
 
   // hidden > 8 * 320 takes the wide prologue instantiation
   const bool wide = p.H > 8 * static_cast<int64_t>(kMaxConsumers);
-  const void* kfn = wide ? reinterpret_cast<const void*>(chain_kernel<true>)
-                         : reinterpret_cast<const void*>(chain_kernel<false>);
+  cl.kfn = wide ? (kv ? reinterpret_cast<const void*>(chain_kernel<true, true>)
+                      : reinterpret_cast<const void*>(chain_kernel<true, false>))
+                : (kv ? reinterpret_cast<const void*>(chain_kernel<false, true>)
+                      : reinterpret_cast<const void*>(chain_kernel<false, false>));
   // set on every launch (cheap next to the chain): nothing cached per device
   int dev = 0;
   cudaGetDevice(&dev);
   int optin = 0;
   cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+  cudaFuncSetAttribute(cl.kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   int bps = 0;
-  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kfn, threads, smem);
+  cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, cl.kfn, cl.threads, cl.smem);
   if (bps < 1) {
-    err = "qws_decode_chain: kernel does not fit on an SM";
+    err = std::string(fn) + ": kernel does not fit on an SM";
     return QWS_ERR_CUDA;
   }
-  const int grid = sms;  // one CTA per SM: all co-resident (cooperative launch)
-  // stamps left by an earlier launch must not look current: clear every word
-  cudaError_t e = cudaMemsetAsync(ws, 0, clear_bytes, st);
-  if (e != cudaSuccess) {
-    err = std::string("qws_decode_chain: ") + cudaGetErrorString(e);
-    return QWS_ERR_CUDA;
-  }
-  void* args[] = {&p};
-  e = cudaLaunchCooperativeKernel(kfn, dim3(grid), dim3(threads), args, smem, st);
+  cl.grid = sms;  // one CTA per SM: all co-resident (cooperative launch)
+  return QWS_OK;
+}
+
+// Stamps left by an earlier token must not look current: clear every word
+// (once per token, before its first launch).
+cudaError_t chain_clear(const ChainLaunch& cl, void* ws, cudaStream_t st) {
+  return cudaMemsetAsync(ws, 0, cl.clear_bytes, st);
+}
+
+// Runs phases [ph_begin, ph_end) of the token.
+cudaError_t chain_run(ChainLaunch& cl, int ph_begin, int ph_end, cudaStream_t st) {
+  cl.p.ph_begin = ph_begin;
+  cl.p.ph_end = ph_end;
+  void* args[] = {&cl.p};
+  return cudaLaunchCooperativeKernel(cl.kfn, dim3(cl.grid), dim3(cl.threads), args, cl.smem, st);
+}
+
+}  // namespace
+
+// Argument checks and launch (called by qws_decode_chain in abi.cu); kept in
+// this translation unit with the workspace layout it depends on.
+qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
+                                 const qws_dims* d, void* ws, size_t ws_bytes, cudaStream_t st,
+                                 std::string& err) {
+  ChainLaunch cl;
+  const qws_status rc =
+      chain_prepare("qws_decode_chain", layers, n_layers, h, d, ws, ws_bytes, false, cl, err);
+  if (rc != QWS_OK) return rc;
+  cudaError_t e = chain_clear(cl, ws, st);
+  if (e == cudaSuccess) e = chain_run(cl, 0, 4 * n_layers, st);
   if (e != cudaSuccess) {
     err = std::string("qws_decode_chain: ") + cudaGetErrorName(e) + " " + cudaGetErrorString(e);
     return QWS_ERR_CUDA;
+  }
+  return QWS_OK;
+}
+
+// ------------------------------------------------------------ KV-cache decode
+// One decode step over a KV cache on the chain kernel (infer-compute README
+// §Architecture, the decode path norm -> QKV -> attend -> O -> FFN).  Per
+// token, in groups of at most 64 layers (the chain's parameter block), the
+// chain runs in pieces between the attention steps:
+//   chain   phase QKV of the group's first layer
+//   per layer l of the group:
+//     attention       split + merge over positions 0..pos, from the chain's
+//                     stamped q, k, v words: the split rotates q and k at pos
+//                     and the CTA whose positions hold pos writes k and v
+//                     into the caches; the merge writes the output as
+//                     stamped words (stamp 4 l + 1)
+//     chain           phases O(l), gate/up(l), down(l) and QKV(l + 1) (the
+//                     group's last piece ends with the final residual)
+// The chain's residuals, norms and stamps carry over between its launches
+// (the workspace is cleared once per group); every launch is stream-ordered
+// after the attention output it reads.
+namespace {
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+struct KvChainLayout {
+  size_t chain, att, part, bytes;   // byte offsets, total
+};
+
+KvChainLayout kv_chain_layout(const qws_dims* d, int64_t max_seq) {
+  KvChainLayout L{};
+  const int64_t QD = static_cast<int64_t>(d->n_q_heads) * d->head_dim;
+  L.chain = 0;
+  L.att = align256(chain_workspace_bytes(d->hidden, d->inter));
+  L.part = L.att + align256(static_cast<size_t>(QD) * sizeof(Word));
+  L.bytes = L.part + align256(kv_attention_workspace_bytes(d->n_q_heads, d->n_kv_heads,
+                                                           d->head_dim, max_seq));
+  return L;
+}
+
+}  // namespace
+
+bool qws::decode_kv_chain_fits(const qws_dims* d) {
+  if (!d || d->hidden <= 0 || d->n_q_heads <= 0 || d->n_kv_heads <= 0 || d->head_dim <= 0)
+    return false;
+  const int64_t H = d->hidden;
+  const int64_t QD = static_cast<int64_t>(d->n_q_heads) * d->head_dim;
+  const int64_t KD = static_cast<int64_t>(d->n_kv_heads) * d->head_dim;
+  return H <= kMaxChainHidden && QD <= 4 * H && KD <= 4 * H;
+}
+
+size_t qws::decode_kv_chain_workspace_bytes(const qws_dims* d, int64_t max_seq) {
+  return kv_chain_layout(d, max_seq).bytes;
+}
+
+qws_status qws::decode_kv_chain(const qws_layer* layers, int n_layers, float* h,
+                                const qws_dims* d, const qws_kv* kv, void* ws, size_t ws_bytes,
+                                cudaStream_t st, std::string& err) {
+  const KvChainLayout Lw = kv_chain_layout(d, kv->max_seq);
+  if (ws_bytes < Lw.bytes) {
+    err = "qws_decode_kv: workspace too small";
+    return QWS_ERR_WORKSPACE;
+  }
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  Word* att = reinterpret_cast<Word*>(base + Lw.att);
+  float* part = reinterpret_cast<float*>(base + Lw.part);
+  const int nq = d->n_q_heads, nkv = d->n_kv_heads, hd = d->head_dim;
+  auto cuda = [&](cudaError_t e, const char* what) {
+    err = std::string("qws_decode_kv: ") + what + ": " + cudaGetErrorName(e) + " " +
+          cudaGetErrorString(e);
+    return QWS_ERR_CUDA;
+  };
+  for (int g0 = 0; g0 < n_layers; g0 += kMaxLayers) {
+    const int n = std::min(kMaxLayers, n_layers - g0);
+    ChainLaunch cl;
+    const qws_status rc =
+        chain_prepare("qws_decode_kv", layers + g0, n, h, d, ws, Lw.att, true, cl, err);
+    if (rc != QWS_OK) return rc;
+    cl.p.att = att;
+    cudaError_t e = chain_clear(cl, ws, st);
+    if (e != cudaSuccess) return cuda(e, "clear");
+    e = chain_run(cl, 0, 1, st);   // QKV of the group's first layer
+    if (e != cudaSuccess) return cuda(e, "chain");
+    for (int l = 0; l < n; ++l) {
+      float* kc = kv->k_caches[g0 + l];
+      float* vc = kv->v_caches[g0 + l];
+      const KvFuse fuse{cl.p.q, cl.p.k, cl.p.v, kc, vc, kv->pos, kv->rot_dim, kv->rope_base};
+      e = launch_kv_attention(nullptr, kc, vc, nullptr, nq, nkv, hd, kv->max_seq, kv->pos + 1,
+                              kv->attn_scale, kv->softcap, part, st, att,
+                              static_cast<unsigned>(4 * l + 1), &fuse);
+      if (e != cudaSuccess) return cuda(e, "attention");
+      e = chain_run(cl, 4 * l + 1, std::min(4 * l + 5, 4 * n), st);
+      if (e != cudaSuccess) return cuda(e, "chain");
+    }
   }
   return QWS_OK;
 }

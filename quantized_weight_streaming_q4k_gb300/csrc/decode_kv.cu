@@ -4,6 +4,12 @@
 // "Attention" kv_append / kv_attention; infer-inference PERFORMANCE.md
 // §Post-Norm Architecture for the Gemma-3 sandwich norms).
 //
+// Shapes that fit the decode chain (hidden <= 5120, q_dim and kv_dim <= 4 *
+// hidden) run on the chain kernel: one chain launch per layer for the
+// projections, norms and residuals, with the rope / append and attention
+// launches between them (decode_kv_chain, chain.cu).  Other shapes take the
+// launch sequence below.
+//
 // Per layer, on one stream, each launch with programmatic stream
 // serialisation (the next launch's weight stream starts while the previous
 // one drains):
@@ -113,9 +119,11 @@ size_t decode_kv_workspace_bytes(const qws_dims* d, int64_t max_seq) {
     return 0;
   const int64_t QD = static_cast<int64_t>(d->n_q_heads) * d->head_dim;
   const int64_t KD = static_cast<int64_t>(d->n_kv_heads) * d->head_dim;
-  return kv_layout(d->hidden, d->inter, QD, KD, d->n_q_heads, d->n_kv_heads, d->head_dim,
-                   max_seq)
-      .bytes;
+  const size_t seq = kv_layout(d->hidden, d->inter, QD, KD, d->n_q_heads, d->n_kv_heads,
+                               d->head_dim, max_seq)
+                         .bytes;
+  return decode_kv_chain_fits(d) ? std::max(seq, decode_kv_chain_workspace_bytes(d, max_seq))
+                                 : seq;
 }
 
 static cudaError_t launch_post_norm_residual(float* h, const float* y, const float* wa,
@@ -166,7 +174,8 @@ qws_status decode_kv(const qws_layer* layers, int n_layers, float* h, const qws_
   if (reinterpret_cast<uintptr_t>(h) % 16 || reinterpret_cast<uintptr_t>(ws) % 16)
     return bad(QWS_ERR_ALIGN, "h and ws must be 16-byte aligned");
   const KvLayout Lw = kv_layout(H, I, QD, KD, nq, nkv, hd, kv->max_seq);
-  if (ws_bytes < Lw.bytes) return bad(QWS_ERR_WORKSPACE, "workspace too small");
+  if (ws_bytes < decode_kv_workspace_bytes(d, kv->max_seq))
+    return bad(QWS_ERR_WORKSPACE, "workspace too small");
   for (int l = 0; l < n_layers; ++l) {
     const qws_layer& L = layers[l];
     const void* wts[7] = {L.Wq, L.Wk, L.Wv, L.Wo, L.Wg, L.Wu, L.Wd};
@@ -188,6 +197,11 @@ qws_status decode_kv(const qws_layer* layers, int n_layers, float* h, const qws_
     if (reinterpret_cast<uintptr_t>(kc) % 16 || reinterpret_cast<uintptr_t>(vc) % 16)
       return bad(QWS_ERR_ALIGN, "caches must be 16-byte aligned");
   }
+  bool same_down = true;   // the chain takes one down-projection format
+  for (int l = 1; l < n_layers; ++l)
+    same_down = same_down && layers[l].fmt_down == layers[0].fmt_down;
+  if (same_down && decode_kv_chain_fits(d))
+    return decode_kv_chain(layers, n_layers, h, d, kv, ws, ws_bytes, st, err);
 
   float* w = static_cast<float*>(ws);
   float *q = w + Lw.q, *k = w + Lw.k, *v = w + Lw.v, *a = w + Lw.a, *o = w + Lw.o;

@@ -120,9 +120,22 @@ cudaError_t launch_rope(float* x, int n_heads, int head_dim, int rot_dim, int64_
                         double base, cudaStream_t st);
 cudaError_t launch_kv_append(float* kc, float* vc, const float* k, const float* v, int n_kv,
                              int head_dim, int64_t max_seq, int64_t pos, cudaStream_t st);
+// RoPE and append fused into kv_attention: q, k, v as {value, stamp} words,
+// q and k rotated at pos (rot_dim, base), k and v written at pos of kc / vc
+// (the same caches the attention reads; q is then unused)
+struct KvFuse {
+  const unsigned long long *q, *k, *v;
+  float *kc, *vc;
+  int64_t pos;
+  int rot_dim;
+  double base;
+};
+// out_words set: the result goes there as {value, stamp} words instead of out
 cudaError_t launch_kv_attention(const float* q, const float* kc, const float* vc, float* out,
                                 int n_q, int n_kv, int head_dim, int64_t max_seq, int64_t n_ctx,
-                                float scale, float softcap, float* ws, cudaStream_t st);
+                                float scale, float softcap, float* ws, cudaStream_t st,
+                                unsigned long long* out_words = nullptr, unsigned stamp = 0,
+                                const KvFuse* fuse = nullptr);
 // 2..8 vectors, each weight decoded once (batchmv.cu): fmt 2 Q4_0 / 12 Q4_K
 // with f32 x; 102 Q4_0 / 108 Q8_0 with Q8_0 activations xq (x unused)
 bool batch_q4_eligible(int fmt, int64_t K, int B);
@@ -161,5 +174,15 @@ size_t chain_workspace_bytes(int64_t hidden, int64_t inter);
 unsigned read_clear_chain_errors();
 qws_status decode_chain(const qws_layer* layers, int n_layers, float* h, const qws_dims* d,
                         void* ws, size_t ws_bytes, cudaStream_t st, std::string& err);
+// The decode step over a KV cache on the chain kernel: true when the shapes
+// fit the chain (hidden <= 5120, q_dim and kv_dim <= 4 * hidden); the
+// workspace the step needs then (chain words, attention output words and
+// the attention partials).
+bool decode_kv_chain_fits(const qws_dims* d);
+size_t decode_kv_chain_workspace_bytes(const qws_dims* d, int64_t max_seq);
+// Arguments checked by the caller (decode_kv); layers in groups of <= 64.
+qws_status decode_kv_chain(const qws_layer* layers, int n_layers, float* h, const qws_dims* d,
+                           const qws_kv* kv, void* ws, size_t ws_bytes, cudaStream_t st,
+                           std::string& err);
 
 }  // namespace qws

@@ -16,7 +16,10 @@ relative budget that the chain's tolerance carries through both branches:
     |h'_gpu - h'_ref| <= 1e-4 * (|h| + |a| + |b|) + 1e-4 * (rms(a) + rms(b)).
 The caches: every position but pos is untouched (bit for bit), and position
 pos holds the step's v (within the matvec tolerance of the oracle's).
-One launch over L layers equals L single-layer launches bit for bit.
+One launch over L layers equals L single-layer launches bit for bit.  Shapes
+that fit the decode chain run on it (one chain launch per layer between the
+attention steps); layers with mixed down-projection formats take the
+launch sequence of standalone kernels, tested here as well.
 """
 import numpy as np
 import pytest
@@ -31,8 +34,8 @@ SMALL = dict(hidden=512, inter=1024, n_q_heads=4, n_kv_heads=2, head_dim=64, eps
              post_norms=1)
 
 
-def _layer(l, dims, workload):
-    L = synth.chain_layer(l, dims, workload=workload)
+def _layer(l, dims, workload, fmt_down=synth.Q6_K):
+    L = synth.chain_layer(l, dims, fmt_down=fmt_down, workload=workload)
     g = synth.rng(workload, 77, l)
     small = dict(d_range=(2e-5, 4e-5), dmin_range=(2e-5, 4e-5))
     L["Wq"] = synth.q4_k_matrix(g, dims["n_q_heads"] * dims["head_dim"], dims["hidden"], **small)
@@ -111,6 +114,15 @@ def test_decode_kv_small(post_norms, pos, rot_dim, softcap):
     layers = [_layer(l, dims, 960 + post_norms) for l in range(2)]
     h0 = synth.normal_vector(synth.rng(961, pos), dims["hidden"])
     _run_layers(dims, layers, 2, 64, pos, h0, 960, rot_dim, softcap)
+
+
+def test_decode_kv_launch_sequence_path():
+    """Layers whose down projections differ in format take the launch
+    sequence (the chain kernel takes one down format): same parity bar."""
+    dims = SMALL
+    layers = [_layer(0, dims, 966, synth.Q6_K), _layer(1, dims, 966, synth.Q4_K)]
+    h0 = synth.normal_vector(synth.rng(967), dims["hidden"])
+    _run_layers(dims, layers, 2, 48, 21, h0, 966)
 
 
 def test_decode_kv_multi_layer_launch_equals_single_layer_launches():
