@@ -164,8 +164,9 @@ __global__ void __launch_bounds__(kAttThreads, 1) kv_attention_split_kernel(
     // ---- copy warp: per stage, P consecutive k rows then P v rows (16 B aligned)
     if (lane == 0) {
       const uint64_t pol = l2_policy_evict_first();
-      const uint8_t* kg = reinterpret_cast<const uint8_t*>(p.kc + static_cast<int64_t>(g) * p.max_seq * p.hd);
-      const uint8_t* vg = reinterpret_cast<const uint8_t*>(p.vc + static_cast<int64_t>(g) * p.max_seq * p.hd);
+      const int64_t head0 = static_cast<int64_t>(g) * p.max_seq * p.hd;
+      const uint8_t* kg = reinterpret_cast<const uint8_t*>(p.kc + head0);
+      const uint8_t* vg = reinterpret_cast<const uint8_t*>(p.vc + head0);
       for (int st = 0; st < n_stages; ++st) {
         const int s = st % kAttStages;
         const uint32_t ph = static_cast<uint32_t>(st / kAttStages) & 1u;
@@ -239,7 +240,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) kv_attention_split_kernel(
     }
     const int64_t ta = (j + static_cast<int64_t>(st) * p.splits) * P;
     const int rows = static_cast<int>(min(static_cast<int64_t>(P), p.n_ctx - ta));
-    const float* kst = reinterpret_cast<const float*>(att_ring + static_cast<size_t>(s) * kAttStageBytes);
+    const float* kst =
+        reinterpret_cast<const float*>(att_ring + static_cast<size_t>(s) * kAttStageBytes);
     const float* vst = kst + P * kPL * 32;
     for (int r = warp; r < rows; r += kAttWarps) {
       float kr[kPL], vr[kPL];
@@ -328,7 +330,8 @@ __global__ void __launch_bounds__(kAttThreads, 1) kv_attention_split_kernel(
 constexpr int kMaxSplits = 256;
 constexpr int kMergeLanes = 8;   // split lanes per column
 
-__global__ void __launch_bounds__(256) kv_attention_merge_kernel(const __grid_constant__ AttParams p) {
+__global__ void __launch_bounds__(256)
+    kv_attention_merge_kernel(const __grid_constant__ AttParams p) {
   __shared__ float sm[kMaxSplits], sl[kMaxSplits], sf[kMaxSplits];
   __shared__ float red[kMergeLanes][32];
   __shared__ float sL;

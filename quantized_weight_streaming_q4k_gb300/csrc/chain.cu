@@ -45,7 +45,8 @@ namespace qws {
 __device__ unsigned g_err_chain;
 
 constexpr int kMaxLayers = 64;
-constexpr uint32_t kChainTileTarget = 46 * 1024;  // measured optimum at 4 stages (inlined prologue / decode)
+// measured optimum at 4 stages (inlined prologue / decode)
+constexpr uint32_t kChainTileTarget = 46 * 1024;
 constexpr uint32_t kChainStages = 4;
 constexpr int64_t kMaxChainHidden = 16 * kMaxConsumers;  // residual vectors: 16 per thread
 
@@ -74,7 +75,8 @@ struct ChainParams {
   KindPlan kp[4];
   // stamped workspace vectors (device); hin and h1 hold two buffers of H each
   Word *q, *k, *v, *o, *m, *f, *hin, *h1;
-  unsigned* prologues;        // [4 * n_layers]: CTAs done with each phase's prologue (zeroed per token)
+  // [4 * n_layers]: CTAs done with each phase's prologue (zeroed per token)
+  unsigned* prologues;
   float* h;                   // the caller's h (in: layer 0 input, out: chain output)
   uint32_t S, stage_bytes, red_floats, xs_floats;
   // This launch runs phases [ph_begin, ph_end) of the token; several launches
