@@ -208,6 +208,7 @@ def test_attention_checks(lib):
     assert lib.qws_rope_at_pos(None, 8, 256, 256, 5, d(1e4), None) == NULL
     assert lib.qws_rope_at_pos(A, 8, 256, 255, 5, d(1e4), None) == SHAPE
     assert lib.qws_rope_at_pos(A, 8, 256, 258, 5, d(1e4), None) == SHAPE
+    assert lib.qws_rope_at_pos(A, 2, 1024, 514, 5, d(1e4), None) == SHAPE   # rot_dim > 512
     assert lib.qws_rope_at_pos(A, 8, 256, 256, -1, d(1e4), None) == SHAPE
     assert lib.qws_rope_at_pos(A, 8, 256, 256, 5, d(0.0), None) == SHAPE
     assert lib.qws_kv_append(A, A, A, None, 4, 256, 100, 5, None) == NULL

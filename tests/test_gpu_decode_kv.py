@@ -154,6 +154,38 @@ def test_decode_kv_multi_layer_launch_equals_single_layer_launches():
     assert ops.device_error() == 0
 
 
+def test_decode_kv_more_layers_than_one_chain_launch_holds():
+    """70 layers run as a group of 64 and a group of 6 chain launches; the
+    result equals 70 one-layer calls bit for bit (h and every cache)."""
+    build.build()
+    torch.cuda.set_device(0)
+    dims = dict(SMALL, hidden=256, inter=512)
+    n, max_seq, pos = 70, 16, 3
+    layers = [_dev(_layer(l, dims, 968)) for l in range(n)]
+    h0 = synth.normal_vector(synth.rng(969), dims["hidden"])
+    base = [_caches(dims, max_seq, pos, 980 + l) for l in range(n)]
+    scale = 1.0 / np.sqrt(dims["head_dim"])
+
+    def fresh():
+        return ([torch.from_numpy(k.copy()).cuda() for k, _ in base],
+                [torch.from_numpy(v.copy()).cuda() for _, v in base])
+
+    ks, vs = fresh()
+    h = torch.from_numpy(h0.copy()).cuda()
+    ops.decode_kv(layers, h, dims, ks, vs, max_seq, pos, 64, 10000.0, scale)
+    ks1, vs1 = fresh()
+    h1 = torch.from_numpy(h0.copy()).cuda()
+    for l in range(n):
+        ops.decode_kv([layers[l]], h1, dims, [ks1[l]], [vs1[l]], max_seq, pos, 64, 10000.0,
+                      scale)
+    torch.cuda.synchronize()
+    assert torch.isfinite(h).all()
+    assert torch.equal(h, h1)
+    for l in range(n):
+        assert torch.equal(ks[l], ks1[l]) and torch.equal(vs[l], vs1[l])
+    assert ops.device_error() == 0
+
+
 def test_decode_kv_gemma3_4b_1024_cached_positions():
     dims = synth.GEMMA3_4B
     pos, max_seq = 1024, 1088
