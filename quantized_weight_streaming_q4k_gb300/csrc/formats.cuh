@@ -126,9 +126,13 @@ __device__ __forceinline__ void nibble_word_split_scalar(uint32_t w, const float
 }
 
 // Which of the eight words of a 32-byte Q4_K chunk take the byte split (bit
-// k set: word k), the rest the in-place masks: a mix keeps both the integer
-// and the FMA pipe busy.
-constexpr unsigned kQ4kSplitWords = 0x55u;
+// k set: word k), the rest the in-place masks.  Measured with the scalar
+// split (same box, two passes): none 84.3 us for the 262144 x 2560 matvec
+// and 1032 us for the 34-layer chain, 0x11 84.1 / 1035, 0x33 84.8 / 1042,
+// 0x55 86.0 / 1039, 0x77 85.7 / 1044, all 85.3 / 1043: the in-place masks
+// take the fewest instructions (1.6 per weight against 2.0), and the chain
+// is bound by instruction issue.
+constexpr unsigned kQ4kSplitWords = 0x00u;
 
 __host__ __device__ constexpr bool q4k_word_split(int k) { return (kQ4kSplitWords >> k) & 1u; }
 
