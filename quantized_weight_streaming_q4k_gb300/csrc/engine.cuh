@@ -132,6 +132,7 @@ struct Ring {
   uint64_t* full;
   uint64_t* ready;
   uint64_t* empty;
+  int* rows;          // rows of the tile in each stage (set by the producer)
   float* red;
   float* xs;          // activation staging, transposed [64][U | 1]
   uint8_t* stages;
@@ -144,9 +145,10 @@ struct Ring {
   }
 };
 
-// mbarriers first (24 B per stage, rounded up to 16 B so the partial buffers
-// start 16-byte aligned), then the partials, then the staging buffer.
-__host__ __device__ constexpr uint32_t ring_bar_bytes(uint32_t S) { return (24u * S + 15u) & ~15u; }
+// mbarriers and the stages' row counts first (28 B per stage, rounded up to
+// 16 B so the partial buffers start 16-byte aligned), then the partials, then
+// the staging buffer.
+__host__ __device__ constexpr uint32_t ring_bar_bytes(uint32_t S) { return (28u * S + 15u) & ~15u; }
 
 __host__ __device__ constexpr size_t ring_header_bytes(uint32_t S, uint32_t red_floats,
                                                        uint32_t xs_floats) {
@@ -164,6 +166,7 @@ __device__ __forceinline__ Ring make_ring(uint8_t* smem, uint32_t S, uint32_t st
   R.full = reinterpret_cast<uint64_t*>(smem);
   R.ready = R.full + S;
   R.empty = R.ready + S;
+  R.rows = reinterpret_cast<int*>(R.empty + S);
   R.red = reinterpret_cast<float*>(smem + ring_bar_bytes(S));
   R.xs = R.red + static_cast<size_t>(S) * red_floats;
   R.stages = smem + ring_header_bytes(S, red_floats, xs_floats);
@@ -219,6 +222,8 @@ __device__ __forceinline__ void fill_stage(const Phase& P, int t, const Ring& R,
   const bool pair = P.epi != EPI_STORE;
   const uint8_t* up = pair ? P.W2 + tr.r0 * P.row_bytes : nullptr;
   uint8_t* dst_up = dst + static_cast<size_t>(P.T) * P.row_bytes;
+  // the tile's row count for the consumers, published by the arrive below
+  R.rows[s] = tr.nrows;
   if (P.row_stride != P.row_bytes) {
     // column slice (split-K): one copy per row; row_bytes and row_stride are
     // multiples of 16 here (checked on the host)
@@ -377,13 +382,15 @@ __device__ __forceinline__ bool consume_phase(const Phase& Pref, const Ring& Rre
       atomicOr(err, kErrFullWait);
       return false;
     }
-    const TileRef tr = tile_ref(P, t);
+    // the tile's row count as the producer wrote it (a shared-memory load in
+    // place of the segment / balanced-round arithmetic of tile_ref)
+    const int nrows = R.rows[pos.s];
     const uint8_t* st = R.stage(pos.s);
     float* red = red_b + static_cast<size_t>(pos.s) * R.red_floats;
-    const int nr = pair ? 2 * tr.nrows : tr.nrows;
+    const int nr = pair ? 2 * nrows : nrows;
     // row r of the tile lives at slot(r) rows into the stage; rows are taken
     // two at a time so that the two independent decode chains interleave
-    auto slot_of = [&](int r) { return (pair && r >= tr.nrows) ? P.T + (r - tr.nrows) : r; };
+    auto slot_of = [&](int r) { return (pair && r >= nrows) ? P.T + (r - nrows) : r; };
     if constexpr (!PIPE) {
       if (active) {
         int r = gg;
