@@ -321,25 +321,35 @@ __device__ __forceinline__ uint32_t misalign4(const uint8_t* p) {
   return static_cast<uint32_t>(reinterpret_cast<uintptr_t>(p)) & 3u;
 }
 
-__device__ __forceinline__ void load8_a2(const uint8_t* p, uint32_t& w0, uint32_t& w1) {
-  const uint32_t m = misalign4(p);
-  const uint32_t* q = reinterpret_cast<const uint32_t*>(p - m);
-  const uint32_t s = m * 8u;
-  const uint32_t r0 = q[0], r1 = q[1], r2 = q[2];
-  w0 = __funnelshift_r(r0, r1, s);
-  w1 = __funnelshift_r(r1, r2, s);
-}
-
-__device__ __forceinline__ void load16_a2(const uint8_t* p, uint32_t (&w)[4]) {
-  const uint32_t m = misalign4(p);
-  const uint32_t* q = reinterpret_cast<const uint32_t*>(p - m);
-  const uint32_t s = m * 8u;
-  uint32_t r[5];
+// One Q6_K block's runs share the block's misalignment (every run offset
+// is a multiple of 4 bytes): the row's aligned base and funnel shift are
+// formed once, and each run loads aligned words at a word offset from it.
+struct Q6kRow {
+  const uint32_t* base;   // block start rounded down to 4 bytes
+  uint32_t s;             // 8 * (block start & 3)
+  __device__ __forceinline__ explicit Q6kRow(const uint8_t* bp) {
+    const uint32_t m = misalign4(bp);
+    base = reinterpret_cast<const uint32_t*>(bp - m);
+    s = m * 8u;
+  }
+  // 16 bytes at byte offset o (a multiple of 4) of the block
+  __device__ __forceinline__ void run16(uint32_t o, uint32_t (&w)[4]) const {
+    const uint32_t* q = base + (o >> 2);
+    uint32_t r[5];
 #pragma unroll
-  for (int k = 0; k < 5; ++k) r[k] = q[k];
+    for (int k = 0; k < 5; ++k) r[k] = q[k];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) w[k] = __funnelshift_r(r[k], r[k + 1], s);
-}
+    for (int k = 0; k < 4; ++k) w[k] = __funnelshift_r(r[k], r[k + 1], s);
+  }
+  __device__ __forceinline__ void run8(uint32_t o, uint32_t& w0, uint32_t& w1) const {
+    const uint32_t* q = base + (o >> 2);
+    const uint32_t r0 = q[0], r1 = q[1], r2 = q[2];
+    w0 = __funnelshift_r(r0, r1, s);
+    w1 = __funnelshift_r(r1, r2, s);
+  }
+  // the f16 d at byte 208
+  __device__ __forceinline__ uint32_t dbits() const { return base[52] >> s; }
+};
 
 // Register slot of column j (0..3) of the 4-column group gi = 4a + t inside
 // the unit's 64-float activation array (slot 16a + 4t + q6k_slot(gi, j)).
@@ -478,13 +488,12 @@ struct UnitQ6K {
   };
 
   __device__ __forceinline__ void load(const uint8_t* rp, Frag& f) const {
-    const uint8_t* bp = rp + g.off;
-    load16_a2(bp + g.oA, f.A);
-    load16_a2(bp + g.oB, f.B);
-    load16_a2(bp + g.oQ, f.Q);
-    load8_a2(bp + g.oS, f.S0, f.S1);
-    const uint32_t md = misalign4(bp + 208);
-    f.dbits = *reinterpret_cast<const uint32_t*>(bp + 208 - md) >> (md * 8u);
+    const Q6kRow br(rp + g.off);
+    br.run16(g.oA, f.A);
+    br.run16(g.oB, f.B);
+    br.run16(g.oQ, f.Q);
+    br.run8(g.oS, f.S0, f.S1);
+    f.dbits = br.dbits();
   }
 
   __device__ __forceinline__ float compute(const Frag& f) const {
@@ -873,15 +882,13 @@ struct UnitChain {
   }
 
   __device__ __forceinline__ float row_q6k(const uint8_t* rp) const {
-    const uint8_t* bp = rp + off;
+    const Q6kRow br(rp + off);
     uint32_t A[4], B[4], Q[4], S0, S1;
-    load16_a2(bp + o1, A);
-    load16_a2(bp + o2, B);
-    load16_a2(bp + o3, Q);
-    load8_a2(bp + o4, S0, S1);
-    const uint32_t md = misalign4(bp + 208);
-    const uint32_t dw = *reinterpret_cast<const uint32_t*>(bp + 208 - md);
-    return q6k_unit_dot<true>(A, B, Q, S0, S1, dw >> (md * 8u), x, s, sh);
+    br.run16(o1, A);
+    br.run16(o2, B);
+    br.run16(o3, Q);
+    br.run8(o4, S0, S1);
+    return q6k_unit_dot<true>(A, B, Q, S0, S1, br.dbits(), x, s, sh);
   }
 };
 
