@@ -91,9 +91,13 @@ inline bool plan_tiles(int fmt, int epi, int64_t K, int B, int64_t rows_hint, in
 inline uint32_t round_up(uint32_t v, uint32_t a) { return (v + a - 1) / a * a; }
 
 // dynamic shared memory a streaming CTA uses (one CTA per SM), and the
-// target bytes of one tile (per stage)
+// target bytes of one tile (per stage).  Measured for the 262144 x 2560
+// matvecs (same box, two passes; Q4_K / Q6_K / Q4_0 in us): 46 KB 83.7 /
+// 132.6 / 77.3, 56 KB 83.6 / 120.6 / 77.2, 64 KB 81.1 / 120.6 / 74.3,
+// 72 KB 91.2 / 130.8 / 86.7, 80 KB 87.8 / 130.8 / 82.8, 92 KB 84.7 / 133.8 /
+// 80.5: the rows per lane slot of a tile against the ring's depth.
 constexpr size_t kSmemBudget = 216 * 1024;
-constexpr uint32_t kTileTarget = 46 * 1024;
+constexpr uint32_t kTileTarget = 64 * 1024;
 
 // ---------------------------------------------------------------- launchers
 // All return cudaSuccess or the CUDA error; *why gets a message on failure.
