@@ -97,30 +97,33 @@ __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4],
 }
 
 // (lo, hi) nibble pairs of the two bytes of u (byte 0 -> low half) as f16x2
-// of q - 8: nibbles placed under the f16 exponent of 1024 (0x6400 | q =
-// 1024 + q, exact), then 1032 subtracted (exact).
+// of q - 8.  One byte permute spreads the two bytes to bytes 0 and 2; a low
+// nibble masked in place under the f16 exponent of 1024 gives 1024 + q (one
+// three-input logic op), a high nibble under the exponent of 64 gives
+// 64 + q (its mantissa step is 1/16); subtracting 1032 or 72 gives q - 8
+// exactly.
 __device__ __forceinline__ uint32_t f16x2_sub(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
   return r;
 }
+__device__ __forceinline__ uint32_t spread16(uint32_t u) { return __byte_perm(u, 0u, 0x4140u); }
 __device__ __forceinline__ uint32_t codes_lo(uint32_t u) {
-  return f16x2_sub((u & 0x000Fu) | ((u & 0x0F00u) << 8) | 0x64006400u, 0x64086408u);
+  return f16x2_sub((spread16(u) & 0x000F000Fu) | 0x64006400u, 0x64086408u);
 }
 __device__ __forceinline__ uint32_t codes_hi(uint32_t u) {
-  return f16x2_sub(((u >> 4) & 0x000Fu) | ((u & 0xF000u) << 4) | 0x64006400u, 0x64086408u);
+  return f16x2_sub((spread16(u) & 0x00F000F0u) | 0x54005400u, 0x54805480u);
 }
 // two int8 codes (byte 0 -> low half) as f16x2: offset to 0..255 under the
 // f16 exponent of 1024, then 1152 subtracted (exact)
 __device__ __forceinline__ uint32_t s8codes(uint32_t u) {
-  const uint32_t v = u ^ 0x8080u;
-  return f16x2_sub((v & 0x00FFu) | ((v & 0xFF00u) << 8) | 0x64006400u, 0x64806480u);
+  return f16x2_sub((spread16(u) ^ 0x00800080u) | 0x64006400u, 0x64806480u);
 }
 // Q4_K codes q (no offset): the low or the high nibble pair as f16x2 of q
 __device__ __forceinline__ uint32_t kcodes(uint32_t u, bool high) {
-  const uint32_t v = high ? (((u >> 4) & 0x000Fu) | ((u & 0xF000u) << 4))
-                          : ((u & 0x000Fu) | ((u & 0x0F00u) << 8));
-  return f16x2_sub(v | 0x64006400u, 0x64006400u);
+  const uint32_t t = spread16(u);
+  return high ? f16x2_sub((t & 0x00F000F0u) | 0x54005400u, 0x54005400u)
+              : f16x2_sub((t & 0x000F000Fu) | 0x64006400u, 0x64006400u);
 }
 
 __device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) {
