@@ -48,6 +48,15 @@ constexpr int kMaxLayers = 64;
 // measured optimum at 4 stages (inlined prologue / decode)
 constexpr uint32_t kChainTileTarget = 46 * 1024;
 constexpr uint32_t kChainStages = 4;
+// Tiles of a phase the producer may copy before this CTA has built the
+// phase's input vector; the later ones wait for it, so that their bytes do
+// not share the SM's path from L2 with the prologue's polls.  With a 3-stage
+// ring this holds back the one tile that would otherwise land during the
+// boundary.  Measured on the 34-layer Gemma-3-4B chain (same box, two
+// passes): 1015 -> 983 us per token with 2, 1010 with 1; gating only the
+// gate/up phases 990, only the down phases 1011.  The chain that runs over a
+// KV cache copies ungated (1573 us per token ungated, 1613 gated).
+constexpr int kGateTiles = 2;
 constexpr int64_t kMaxChainHidden = 16 * kMaxConsumers;  // residual vectors: 16 per thread
 
 enum : int { PH_QKV = 0, PH_O = 1, PH_GU = 2, PH_DOWN = 3 };
@@ -414,7 +423,8 @@ __device__ __forceinline__ bool stage_gather(const Ring& R, int US, const Word* 
 // common case carries none of its registers.
 template <bool kWide, bool kKV>
 __device__ __forceinline__ bool chain_prologue(const ChainParams& p, int ph, const Ring& R,
-                                            float* wsum, bool q6, int ctid, int C) {
+                                            float* wsum, volatile int* gate, bool q6, int ctid,
+                                            int C) {
   const int l = ph >> 2, kind = ph & 3;
   const ChainLayer& L = p.L[l];
   const KindPlan& kp = p.kp[kind];
@@ -480,7 +490,10 @@ __device__ __forceinline__ bool chain_prologue(const ChainParams& p, int ph, con
   }
   bar_sync(kConsumerBar, C);
   // this CTA has read everything its prologue needed
-  if (ctid == 0) red_release_gpu_add(p.prologues + ph, 1u);
+  if (ctid == 0) {
+    red_release_gpu_add(p.prologues + ph, 1u);
+    *gate = ph + 1;   // the producer may copy the rest of phase ph's tiles
+  }
   return ok;
 }
 
@@ -567,6 +580,23 @@ __device__ __forceinline__ void prefetch_l2(const float* w, int64_t n) {
                  : "memory");
 }
 
+// Holds the copy of tile j >= kGateTiles of launch phase i (> 0) until this
+// CTA's consumers have finished that phase's prologue.  Bounded.
+struct ChainGate {
+  volatile int* done;   // last finished prologue: absolute phase + 1
+  int begin;            // absolute index of launch phase 0
+  __device__ __forceinline__ bool operator()(int i, int j) const {
+    const int want = begin + i + 1;
+    if (i == 0 || j < kGateTiles || *done >= want) return true;
+    const long long t0 = clock64();
+    while (*done < want) {
+      if (clock64() - t0 > kWaitCycles) return false;
+      __nanosleep(32);
+    }
+    return true;
+  }
+};
+
 // ------------------------------------------------------------------ kernel
 template <bool kWide, bool kKV>
 __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
@@ -575,8 +605,13 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
   const Ring R = make_ring(smem, p.S, p.stage_bytes, p.red_floats, p.xs_floats);
   float* wsum = reinterpret_cast<float*>(smem + ring_smem_bytes(p.S, p.stage_bytes, p.red_floats,
                                                                  p.xs_floats));
+  // the last prologue this CTA finished (phase + 1), read by the producer
+  volatile int* gate = reinterpret_cast<volatile int*>(wsum + 64);
   const int C = static_cast<int>(blockDim.x) - kRoleThreads;
-  if (threadIdx.x == 0) ring_init(R, C / 32);
+  if (threadIdx.x == 0) {
+    ring_init(R, C / 32);
+    *gate = 0;
+  }
   __syncthreads();
   const ChainPhases phases{&p};
 
@@ -589,7 +624,11 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
         prefetch_l2(p.L[l].w_pf, p.H * 4);
         prefetch_l2(p.L[l].w_pff, p.H * 4);
       }
-      run_producer(ChainPhases::Range{&phases, p.ph_begin, p.ph_end}, R, &g_err_chain);
+      if constexpr (kKV)   // ungated: see kGateTiles
+        run_producer(ChainPhases::Range{&phases, p.ph_begin, p.ph_end}, R, &g_err_chain);
+      else
+        run_producer(ChainPhases::Range{&phases, p.ph_begin, p.ph_end}, R, &g_err_chain,
+                     ChainGate{gate, p.ph_begin});
     }
     return;
   }
@@ -613,7 +652,7 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
   for (int ph = p.ph_begin; ph < p.ph_end; ++ph) {
     const Phase P = phases.get(ph);
     const bool q6 = (ph & 3) == PH_DOWN && down_q6k;
-    if (!chain_prologue<kWide, kKV>(p, ph, R, wsum, q6, ctid, C)) return;
+    if (!chain_prologue<kWide, kKV>(p, ph, R, wsum, gate, q6, ctid, C)) return;
     const unsigned long long r = chain_consume(
         P.fmt, P.epi, P.nseg, static_cast<int>(P.seg[0].rows), static_cast<int>(P.seg[1].rows),
         static_cast<int>(P.seg[2].rows), P.seg[0].tiles, P.seg[1].tiles, P.seg[2].tiles, P.T,
@@ -826,7 +865,7 @@ qws_status chain_prepare(const char* fn, const qws_layer* layers, int n_layers, 
   p.stage_bytes = round_up(stage_need + 16, 128);
   p.red_floats = red;
   p.xs_floats = xs;
-  const size_t tail = 64 * sizeof(float);   // warp sums
+  const size_t tail = 64 * sizeof(float) + 16;   // warp sums, producer gate
   // Ring depth: at most kChainStages.  A deeper ring prefetches more of the
   // next phase, and that DRAM traffic slows the L2 loads on every CTA's
   // critical path at each phase boundary (measured on GB300: 7 stages 1416,

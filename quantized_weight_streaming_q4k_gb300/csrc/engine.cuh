@@ -243,10 +243,17 @@ __device__ __forceinline__ void fill_stage(const Phase& P, int t, const Ring& R,
   }
 }
 
+// Producer gate: gate(p, j) is asked before tile j (in this CTA's order) of
+// phase p is copied, and may hold the copy back (bounded; false on timeout).
+struct NoGate {
+  __device__ __forceinline__ bool operator()(int, int) const { return true; }
+};
+
 // PhaseList: count() and get(i) -> Phase, evaluated identically by producer
 // and consumers.
-template <class PhaseList>
-__device__ void run_producer(const PhaseList& L, const Ring& R, unsigned* err) {
+template <class PhaseList, class Gate = NoGate>
+__device__ void run_producer(const PhaseList& L, const Ring& R, unsigned* err,
+                             const Gate& gate = Gate()) {
   const uint64_t pol = l2_policy_evict_first();
   RingPos pos;
   bool ok = true;
@@ -255,8 +262,8 @@ __device__ void run_producer(const PhaseList& L, const Ring& R, unsigned* err) {
     const Phase P = L.get(p);
     const int c = static_cast<int>(blockIdx.x) - P.cta0;
     if (c < 0 || c >= P.ncta) continue;
-    for (int t = c; t < P.n_tiles; t += P.ncta) {
-      if (!mbar_wait(&R.empty[pos.s], pos.ph ^ 1u)) {
+    for (int t = c, j = 0; t < P.n_tiles; t += P.ncta, ++j) {
+      if (!gate(p, j) || !mbar_wait(&R.empty[pos.s], pos.ph ^ 1u)) {
         atomicOr(err, kErrEmptyWait);
         ok = false;
         break;
