@@ -130,8 +130,6 @@ __device__ __forceinline__ uint32_t ld_u16(const uint8_t* p) {
   return *reinterpret_cast<const unsigned short*>(p);
 }
 
-// 6-bit scale and min of sub-block j (0..7) from the 12 packed bytes at sc
-// (the GGUF packing), times d and dmin
 // A fragments of one 32-column block of Q4_0 / Q8_0 weights for rows g
 // (pa) and g + 8 (pb): a0 = columns 0..15, a1 = 16..31, as exact f16 codes
 template <int kFmt>
@@ -164,19 +162,20 @@ __device__ __forceinline__ void q8_block_scale(float (&acc)[4], const float (&c)
   acc[3] = fmaf(db * dx.y, c[3], acc[3]);
 }
 
-__device__ __forceinline__ void q4k_ab(const uint8_t* h, int j, float& a, float& b) {
-  const uint32_t dd = *reinterpret_cast<const uint32_t*>(h);
-  const uint8_t* sc = h + 4;
-  uint32_t scv, mv;
-  if (j < 4) {
-    scv = sc[j] & 63u;
-    mv = sc[j + 4] & 63u;
-  } else {
-    scv = (sc[j + 4] & 0xFu) | ((sc[j - 4] >> 6) << 4);
-    mv = (sc[j + 4] >> 4) | ((sc[j] >> 6) << 4);
-  }
-  a = half_bits_to_float(dd) * static_cast<float>(scv);
-  b = half_bits_to_float(dd >> 16) * static_cast<float>(mv);
+// Scales and mins of the aligned sub-block pair (2c, 2c + 1) of one block,
+// from its 16-byte header (d, dmin, the 12 packed scale bytes) in one load:
+// a[k] = d * sc(2c + k), b[k] = dmin * m(2c + k), products exact in f32.
+__device__ __forceinline__ void q4k_pair_ab(const uint8_t* h, int c, float (&a)[2],
+                                            float (&b)[2]) {
+  const uint4 hd = *reinterpret_cast<const uint4*>(h);   // block headers are 16-byte aligned
+  Q4kSel sel;
+  sel.set(c);
+  const uint32_t R = q4k_scale_bytes(hd, sel.selP, sel.selQ, sel.sh, sel.mask);
+  const float d = half_bits_to_float(hd.x), dmin = half_bits_to_float(hd.x >> 16);
+  a[0] = d * byte_to_float(R, 0);
+  a[1] = d * byte_to_float(R, 1);
+  b[0] = dmin * byte_to_float(R, 2);
+  b[1] = dmin * byte_to_float(R, 3);
 }
 
 // acc (rows g, g + 8 x vectors 2tq, 2tq + 1) += a C - b S of Q4_K sub-block bi
@@ -199,9 +198,12 @@ __device__ __forceinline__ void q4k_sub(const uint8_t* rg, const uint8_t* rg8, i
   mma_16816(cc, alo, xl[w0], xl[w0 + 4]);
   mma_16816(cc, ahi, xh[w0 + 8], xh[w0 + 12]);
   mma_16816(cc, ahi, xl[w0 + 8], xl[w0 + 12]);
-  float a0, b0, a1, b1;
-  q4k_ab(ha, j, a0, b0);
-  q4k_ab(hb, j, a1, b1);
+  float aa[2], ba[2], ab[2], bb[2];
+  q4k_pair_ab(ha, c, aa, ba);
+  q4k_pair_ab(hb, c, ab, bb);
+  const bool odd = (j & 1) != 0;
+  const float a0 = odd ? aa[1] : aa[0], b0 = odd ? ba[1] : ba[0];
+  const float a1 = odd ? ab[1] : ab[0], b1 = odd ? bb[1] : bb[0];
   // ssum [sub-block][vector]: the sums of vectors 2 tq, 2 tq + 1 in one load
   const float2 sv = reinterpret_cast<const float2*>(ssum)[bi * 4 + tq];
   acc[0] = fmaf(a0, cc[0], fmaf(-b0, sv.x, acc[0]));
@@ -238,11 +240,11 @@ __device__ __forceinline__ void q4k_pair(const uint8_t* rg, const uint8_t* rg8, 
   mma_16816(c1, h1, xh[w1 + 8], xh[w1 + 12]);
   mma_16816(c0, l1, xl[w0 + 8], xl[w0 + 12]);
   mma_16816(c1, h1, xl[w1 + 8], xl[w1 + 12]);
-  float a0, b0, a1, b1, a2, b2, a3, b3;
-  q4k_ab(ha, j, a0, b0);
-  q4k_ab(hb, j, a1, b1);
-  q4k_ab(ha, j + 1, a2, b2);
-  q4k_ab(hb, j + 1, a3, b3);
+  float aa[2], ba[2], ab[2], bb[2];
+  q4k_pair_ab(ha, c, aa, ba);
+  q4k_pair_ab(hb, c, ab, bb);
+  const float a0 = aa[0], b0 = ba[0], a1 = ab[0], b1 = bb[0];
+  const float a2 = aa[1], b2 = ba[1], a3 = ab[1], b3 = bb[1];
   const float2 sv = reinterpret_cast<const float2*>(ssum)[bi * 4 + tq];
   const float2 tv = reinterpret_cast<const float2*>(ssum)[(bi + 1) * 4 + tq];
   acc[0] = fmaf(a0, c0[0], fmaf(-b0, sv.x, acc[0]));
