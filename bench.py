@@ -669,6 +669,8 @@ def run_op(args):
             ops.matvec(fmt, W, x, VOCAB, H, B, 1, ws, out=y)
         nbytes = synth.n_blocks(fmt, VOCAB, H) * synth.BLOCK_BYTES[fmt] + B * H * 4 + B * VOCAB * 4
         kernel = f"matvec_kernel<{'UnitQ4K' if fmt == synth.Q4_K else 'UnitQ6K'}> (f32 activations)"
+        if fmt == synth.Q4_K and 2 <= B <= 8:
+            kernel = "batch_q4_matvec_kernel<12> (f32 activations, decode once for all vectors)"
         workload = f"matvec {VOCAB}x{H} {'Q4_K' if fmt == synth.Q4_K else 'Q6_K'}, batch {B}"
     elif args.op in ("lm_head_q4_0", "lm_head_q8"):
         W = torch.from_numpy(synth.q4_0_matrix(g, VOCAB, H)).to(dev)
@@ -685,7 +687,8 @@ def run_op(args):
             def call():
                 ops.q4_0_matvec(W, x, VOCAB, H, B, split, ws, out=y)
             nbytes = wbytes + B * H * 4 + B * VOCAB * 4
-            kernel = "matvec_kernel<UnitQ40> (f32 activations)"
+            kernel = ("batch_q4_matvec_kernel<2> (f32 activations, decode once for all vectors)"
+                      if 2 <= B <= 8 else "matvec_kernel<UnitQ40> (f32 activations)")
         else:
             xq = torch.empty((B, H // 32 * 34) if B > 1 else (H // 32 * 34,), dtype=torch.uint8,
                              device=dev)
