@@ -639,8 +639,9 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
     for (int ph = p.ph_begin; ph < p.ph_end; ++ph) {
       const Phase P = phases.get(ph);
       // (one load, normally already satisfied; it overlaps the consumers'
-      // work on the phase's first tile)
-      if (!wait_prologues(p, ph - 3)) return;
+      // work on the phase's first tile).  A phase before this launch's first
+      // ran in an earlier launch, which has finished.
+      if (ph - 3 >= p.ph_begin && !wait_prologues(p, ph - 3)) return;
       if (!reduce_phase(P, R, pos, EpiStamped{ph}, &g_err_chain)) return;
     }
     return;
