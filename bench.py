@@ -15,8 +15,9 @@ Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
                         matvec_q4k (Q4_K 2560 x 2560), qkv (fused Q/K/V
                         4096 x 2560 + O 2560 x 2048), ffn (fused gate/up
                         GEGLU + Q6_K down, 2560/10240): each back to back
-                        over a ring of weight copies >= 4 x L2 and isolated
-                        after an L2 flush,
+                        over a ring of weight copies >= 4 x L2 (a CUDA graph
+                        of the calls; also launched one at a time) and
+                        isolated after an L2 flush,
                         prefill (Q4_K 10240 x 2560 times --batch tokens on the
                         tensor cores; TFLOP/s),
                         kv_attention (one token over 32768 cached positions,
@@ -521,9 +522,11 @@ def run_decode_kv(args):
 
 
 def run_ring_op(args):
-    """The small per-layer operations (weights smaller than L2), each timed two
-    ways: back to back over a ring of distinct weight copies totalling at least
-    four times the L2 size (so every call streams its weights from HBM), and
+    """The small per-layer operations (weights smaller than L2), each timed
+    back to back over a ring of distinct weight copies totalling at least four
+    times the L2 size (so every call streams its weights from HBM): as a CUDA
+    graph of the calls, replayed (the reported value: no host work between
+    calls), and launched from the host one call at a time ("stream"); and
     isolated, one call after an L2 flush (a write of twice the L2 size),
     median over calls.  Algorithmic bytes: packed weights + activations read
     + outputs written (+ the FFN's intermediate written and read)."""
@@ -609,7 +612,7 @@ def run_ring_op(args):
         eb.record(stream)
     torch.cuda.synchronize()
     iso_us = statistics.median(1e3 * ea.elapsed_time(eb) for ea, eb in evs)
-    # back to back over the ring
+    # back to back over the ring, launched from the host one call at a time
     uuid = str(getattr(props, "uuid", "") or "")
     clocks = ClockSampler((uuid if uuid.startswith("GPU-") else f"GPU-{uuid}") if uuid else "0")
     clocks.start()
@@ -620,9 +623,33 @@ def run_ring_op(args):
         call(ring[i % n_copies])
     tb.record(stream)
     torch.cuda.synchronize()
+    assert ops.device_error() == 0
+    us_stream = 1e3 * ta.elapsed_time(tb) / args.steps
+    # back to back over the ring as a CUDA graph (the same calls captured once,
+    # replayed): no host work between calls
+    per_graph = n_copies * max(1, -(-32 // n_copies))
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for i in range(per_graph):
+            call(ring[i % n_copies])
+    side.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for i in range(per_graph):
+            call(ring[i % n_copies])
+    reps = max(3, -(-args.steps // per_graph))
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    ta.record(stream)
+    for _ in range(reps):
+        graph.replay()
+    tb.record(stream)
+    torch.cuda.synchronize()
     clk = clocks.stop()
     assert ops.device_error() == 0
-    us = 1e3 * ta.elapsed_time(tb) / args.steps
+    us = 1e3 * ta.elapsed_time(tb) / (reps * per_graph)
     gbs = nbytes / (us * 1e-6) / 1e9
     peak, peak_kind = peaks()
     print(json.dumps({
@@ -631,7 +658,9 @@ def run_ring_op(args):
         "higher_is_better": True, "dtype": "f32", "data": "synthetic (seeded random blocks)",
         "config": {"workload": workload, "batch": 1,
                    "l2": f"back to back over a ring of {n_copies} distinct weight copies "
-                         f"({n_copies * wbytes / 1e6:.0f} MB >= 4 x L2 of {l2 / 1e6:.0f} MB)"},
+                         f"({n_copies * wbytes / 1e6:.0f} MB >= 4 x L2 of {l2 / 1e6:.0f} MB)",
+                   "method": f"CUDA graph of {per_graph} calls over the ring, replayed {reps} "
+                             f"times"},
         "roofline": {"bound": "hbm", "kernel": kernel, "achieved": gbs, "peak": peak,
                      "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_kind,
                      "traffic": None},
@@ -639,7 +668,10 @@ def run_ring_op(args):
                      "frac": nbytes / (iso_us * 1e-6) / 1e9 / peak,
                      "method": f"one call after a {2 * l2 / 1e6:.0f} MB L2 flush, median of "
                                f"{n_iso}"},
-        "bytes_per_call": nbytes, "gpu_launches": launches * args.steps, "clocks": clk,
+        "stream": {"us_per_call": us_stream, "gbs": nbytes / (us_stream * 1e-6) / 1e9,
+                   "frac": nbytes / (us_stream * 1e-6) / 1e9 / peak,
+                   "method": "the same calls launched from the host one at a time"},
+        "bytes_per_call": nbytes, "gpu_launches": launches * reps * per_graph, "clocks": clk,
     }))
 
 
