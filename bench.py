@@ -512,11 +512,11 @@ def run_decode_kv(args):
                                f"({pos + 1} cached positions, 4 kv heads of 256), batch 1",
                    "l2": f"{nbytes / 1e9:.2f} GB streamed per token (> L2)"},
         "roofline": {"bound": "hbm",
-                     "kernel": "decode_kv on the chain kernel (per layer: chain launch + RoPE/append "
-                               "+ attention split + merge)",
+                     "kernel": "decode_kv on the chain kernel (per layer: attention split with "
+                               "RoPE and the K/V append fused in + merge + chain launch)",
                      "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "peak_source": peak_kind, "traffic": None},
-        "bytes_per_token": nbytes, "gpu_launches": (1 + 4 * n_layers) * args.steps,
+        "bytes_per_token": nbytes, "gpu_launches": (1 + 3 * n_layers) * args.steps,
         "clocks": clk,
     }))
 

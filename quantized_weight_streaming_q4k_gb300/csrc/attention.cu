@@ -58,6 +58,14 @@ static RopeTable rope_table(int rot_dim, int64_t pos, double base) {
   return tab;
 }
 
+void rope_table_f32(int rot_dim, int64_t pos, double base, float* c, float* s) {
+  const RopeTable tab = rope_table(rot_dim, pos, base);
+  for (int i = 0; i < rot_dim / 2; ++i) {
+    c[i] = static_cast<float>(tab.c[i]);
+    s[i] = static_cast<float>(tab.s[i]);
+  }
+}
+
 __global__ void rope_kernel(float* __restrict__ x, int n_heads, int head_dim, int rot_dim,
                             const __grid_constant__ RopeTable tab) {
   pdl_launch_dependents();

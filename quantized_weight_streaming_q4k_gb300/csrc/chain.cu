@@ -95,6 +95,21 @@ struct ChainParams {
   // 4 l + 1, written between launches) instead of gathering v.
   int ph_begin, ph_end;
   Word* att;
+  // Attention inside the O prologue (fused_att = 1; decode over a KV cache,
+  // every layer in one launch).  Step 1: work item (kv head g, chunk j) --
+  // positions [j * chunk_len, (j + 1) * chunk_len) of n_ctx = pos + 1 -- is
+  // taken by CTA (g * chunks + j) mod grid and leaves its partial (acc[hd],
+  // m, l per query head of the group) as stamped words in part; the item
+  // holding pos rotates k and writes k and v into the caches.  Step 2: CTA
+  // b merges attention outputs [b * per, (b + 1) * per) into att.  Stamps:
+  // 4 l + 1 (part and att of layer l; both buffers are cleared per token).
+  int fused_att;
+  float *kc[kMaxLayers], *vc[kMaxLayers];
+  int64_t max_seq, pos;
+  int chunks, chunk_len, rot_dim;
+  float att_scale, softcap;
+  Word* part;
+  float rtc[256], rts[256];   // cos / sin of pos * base^(-2i / rot_dim), f32
 };
 
 __device__ __forceinline__ Word ld_word(const Word* p) {
@@ -362,6 +377,273 @@ __device__ __forceinline__ bool stage_stamped(const Ring& R, int US, const Word*
   return ok;
 }
 
+// ------------------------------------------------------------ fused attention
+// Polls up to kN stamped words at addresses a[0..n) until each carries stamp
+// `want`; their values go to v[].  All pending loads go out together.
+template <int kN>
+__device__ __forceinline__ bool poll_words(const Word* const (&a)[kN], int n, unsigned want,
+                                           float (&v)[kN]) {
+  unsigned pending = 0;
+#pragma unroll
+  for (int k = 0; k < kN; ++k)
+    if (k < n) pending |= 1u << k;
+  long long t0 = 0;
+  bool first = true;
+  while (pending) {
+    Word w[kN];
+#pragma unroll
+    for (int k = 0; k < kN; ++k) w[k] = (pending >> k & 1u) ? ld_word(a[k]) : 0ull;
+#pragma unroll
+    for (int k = 0; k < kN; ++k)
+      if ((pending >> k & 1u) && stamp_of(w[k]) == want) {
+        v[k] = value_of(w[k]);
+        pending &= ~(1u << k);
+      }
+    if (!pending) break;
+    if (first) {
+      t0 = clock64();
+      first = false;
+    } else if (clock64() - t0 > kWaitCycles) {
+      atomicOr(&g_err_chain, kErrFullWait);
+      return false;
+    }
+  }
+  return true;
+}
+
+// Shared-memory floats the fused attention steps use (inside the staging
+// buffer, before the O projection's vector is staged there).
+constexpr int kAttWarpsC = kMaxConsumers / 32;   // 10 consumer warps
+constexpr int kAttGH = 512;                       // group heads x head_dim staged
+constexpr int kAttMergeBatch = 48;                // outputs merged per round (at most)
+// staging-buffer floats both steps need (they run one after the other)
+__host__ __device__ constexpr int att_smem_floats(int chunks) {
+  return 4 * kAttGH + kAttWarpsC * kAttGH + 2 * kAttWarpsC * 4 > 3 * kAttMergeBatch * chunks
+             ? 4 * kAttGH + kAttWarpsC * kAttGH + 2 * kAttWarpsC * 4
+             : 3 * kAttMergeBatch * chunks;
+}
+
+// Element i of a head (raw values at x) rotated at pos (f32 cos / sin).
+__device__ __forceinline__ float rope_at(const float* x, int i, int rot_dim, const float* tc,
+                                         const float* ts) {
+  if (i >= rot_dim) return x[i];
+  const int half = rot_dim / 2;
+  const int j = i < half ? i : i - half;
+  const float a = x[j], b = x[j + half];
+  return i < half ? fmaf(a, tc[j], -(b * ts[j])) : fmaf(a, ts[j], b * tc[j]);
+}
+
+// Step 1 of the fused attention for layer l: this CTA's work items.
+// Per item the group's q (and, for the item holding pos, k and v) come from
+// the QKV phase's stamped words (stamp 4 l + 1); warp w takes positions
+// p0 + w, p0 + w + 10, ...; lane L holds columns [L kPL, (L + 1) kPL) of q,
+// k, v and the running output; the warps are merged in order 0..9 and the
+// item's partial is stored as stamped words.
+template <int kPL, int kG>
+__device__ __forceinline__ bool att_split(const ChainParams& p, int l, float* sm, int ctid) {
+  constexpr int hd = kPL * 32;
+  const unsigned want = static_cast<unsigned>(4 * l + 1);
+  const int warp = ctid >> 5, lane = ctid & 31, c0 = lane * kPL;
+  const int64_t n_ctx = p.pos + 1;
+  const int items = p.n_kv_heads * p.chunks;
+  float* sq = sm;                          // [kG][hd] rotated q
+  float* skv = sm + kAttGH;                // [2][hd] k (rotated), v of pos
+  float* sraw = sm + 2 * kAttGH;           // [kG][hd] raw q, then [2][hd] raw k, v
+  float* sacc = sm + 4 * kAttGH;           // [10][kG][hd]
+  float* smm = sacc + kAttWarpsC * kAttGH;  // [10][4]
+  float* sml = smm + kAttWarpsC * 4;
+  const float* kcl = p.kc[l];
+  const float* vcl = p.vc[l];
+  bool ok = true;
+  for (int item = blockIdx.x; item < items; item += gridDim.x) {
+    const int g = item / p.chunks, j = item - g * p.chunks;
+    const int64_t p0 = static_cast<int64_t>(j) * p.chunk_len;
+    const int64_t p1 = min(p0 + p.chunk_len, n_ctx);
+    const bool has_pos = p.pos >= p0 && p.pos < p1;
+    // raw q of the group's heads (contiguous), k and v of kv head g
+    ok = poll_stamped<2>(p.q + static_cast<int64_t>(g) * kG * hd + ctid,
+                         p.q + static_cast<int64_t>(g + 1) * kG * hd, want,
+                         [&](int jj, float v) { sraw[ctid + jj * kC] = v; }) &&
+         ok;
+    bar_sync(kConsumerBar, kC);
+    for (int e = ctid; e < kG * hd; e += kC) {
+      const int h = e / hd, i = e - h * hd;
+      sq[e] = rope_at(sraw + h * hd, i, p.rot_dim, p.rtc, p.rts);
+    }
+    bar_sync(kConsumerBar, kC);
+    if (has_pos) {
+      ok = poll_stamped<1>(p.k + static_cast<int64_t>(g) * hd + ctid,
+                           p.k + static_cast<int64_t>(g + 1) * hd, want,
+                           [&](int, float v) { sraw[ctid] = v; }) &&
+           ok;
+      ok = poll_stamped<1>(p.v + static_cast<int64_t>(g) * hd + ctid,
+                           p.v + static_cast<int64_t>(g + 1) * hd, want,
+                           [&](int, float v) { sraw[hd + ctid] = v; }) &&
+           ok;
+      bar_sync(kConsumerBar, kC);
+      const int64_t row = (static_cast<int64_t>(g) * p.max_seq + p.pos) * hd;
+      for (int i = ctid; i < hd; i += kC) {
+        const float kr = rope_at(sraw, i, p.rot_dim, p.rtc, p.rts);
+        const float vr = sraw[hd + i];
+        skv[i] = kr;
+        skv[hd + i] = vr;
+        p.kc[l][row + i] = kr;
+        p.vc[l][row + i] = vr;
+      }
+      bar_sync(kConsumerBar, kC);
+    }
+    float q[kG][kPL], acc[kG][kPL], m[kG], lsum[kG];
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+      m[h] = -INFINITY;
+      lsum[h] = 0.f;
+#pragma unroll
+      for (int c = 0; c < kPL; ++c) {
+        q[h][c] = sq[h * hd + c0 + c] * p.att_scale;
+        acc[h][c] = 0.f;
+      }
+    }
+    const float* kh = kcl + static_cast<int64_t>(g) * p.max_seq * hd + c0;
+    const float* vh = vcl + static_cast<int64_t>(g) * p.max_seq * hd + c0;
+    for (int64_t r0 = p0 + warp; r0 < p1; r0 += 2 * kAttWarpsC) {
+      // two positions per round: both rows' loads in flight together
+      float kr[2][kPL], vr[2][kPL];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int64_t r = r0 + u * kAttWarpsC;
+        if (r < p1 && !(has_pos && r == p.pos)) {
+#pragma unroll
+          for (int c = 0; c < kPL; c += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(kh + r * hd + c);
+            const float4 b = *reinterpret_cast<const float4*>(vh + r * hd + c);
+            kr[u][c] = a.x; kr[u][c + 1] = a.y; kr[u][c + 2] = a.z; kr[u][c + 3] = a.w;
+            vr[u][c] = b.x; vr[u][c + 1] = b.y; vr[u][c + 2] = b.z; vr[u][c + 3] = b.w;
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kPL; ++c) {
+            kr[u][c] = skv[c0 + c];
+            vr[u][c] = skv[hd + c0 + c];
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        if (r0 + u * kAttWarpsC >= p1) break;
+#pragma unroll
+        for (int h = 0; h < kG; ++h) {
+          float sc = 0.f;
+#pragma unroll
+          for (int c = 0; c < kPL; ++c) sc = fmaf(q[h][c], kr[u][c], sc);
+          sc = warp_sum(sc);
+          if (p.softcap > 0.f) sc = p.softcap * tanhf(sc / p.softcap);
+          const float mn = fmaxf(m[h], sc);
+          const float alpha = expf(m[h] - mn);
+          const float pr = expf(sc - mn);
+          lsum[h] = fmaf(lsum[h], alpha, pr);
+#pragma unroll
+          for (int c = 0; c < kPL; ++c) acc[h][c] = fmaf(acc[h][c], alpha, pr * vr[u][c]);
+          m[h] = mn;
+        }
+      }
+    }
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+      if (lane == 0) {
+        smm[warp * 4 + h] = m[h];
+        sml[warp * 4 + h] = lsum[h];
+      }
+#pragma unroll
+      for (int c = 0; c < kPL; ++c) sacc[(warp * kG + h) * hd + c0 + c] = acc[h][c];
+    }
+    bar_sync(kConsumerBar, kC);
+    for (int e = ctid; e < kG * hd; e += kC) {
+      const int h = e / hd, i = e - h * hd;
+      float M = -INFINITY;
+      for (int w = 0; w < kAttWarpsC; ++w) M = fmaxf(M, smm[w * 4 + h]);
+      float a = 0.f, L = 0.f;
+      if (M != -INFINITY) {
+        for (int w = 0; w < kAttWarpsC; ++w) {
+          const float f = expf(smm[w * 4 + h] - M);   // 0 for a warp with no position
+          a = fmaf(sacc[(w * kG + h) * hd + i], f, a);
+          L = fmaf(sml[w * 4 + h], f, L);
+        }
+      }
+      Word* dst = p.part + ((static_cast<int64_t>(g) * p.chunks + j) * kG + h) * (hd + 2);
+      st_word(dst + i, a, want);
+      if (i == 0) {
+        st_word(dst + hd, M, want);
+        st_word(dst + hd + 1, L, want);
+      }
+    }
+    bar_sync(kConsumerBar, kC);   // shared memory is reused by the next item
+  }
+  return ok;
+}
+
+// Step 2: attention outputs [o0, o1) of layer l from the items' partials,
+// kAttMergeBatch outputs per round; out = sum_j e^(m_j - M) acc_j /
+// sum_j e^(m_j - M) l_j (M = max_j m_j; chunks added in order).
+__device__ __forceinline__ bool att_merge(const ChainParams& p, int l, float* sm, int ctid) {
+  const unsigned want = static_cast<unsigned>(4 * l + 1);
+  const int hd = p.head_dim, G = p.n_q_heads / p.n_kv_heads, C = p.chunks;
+  const int64_t n_out = static_cast<int64_t>(p.n_q_heads) * hd;
+  const int64_t per = (n_out + gridDim.x - 1) / gridDim.x;
+  const int64_t o0 = blockIdx.x * per, o1 = min(o0 + per, n_out);
+  float* sa = sm;                                   // [batch][C] acc
+  float* smv = sa + kAttMergeBatch * C;             // [batch][C] m
+  float* slv = smv + kAttMergeBatch * C;            // [batch][C] l
+  bool ok = true;
+  for (int64_t b0 = o0; b0 < o1; b0 += kAttMergeBatch) {
+    const int nb = static_cast<int>(min(static_cast<int64_t>(kAttMergeBatch), o1 - b0));
+    for (int t0 = 0; t0 < nb * C; t0 += kC) {
+      const int t = t0 + ctid;
+      if (t < nb * C) {
+        const int k = t / C, j = t - k * C;
+        const int64_t o = b0 + k;
+        const int hq = static_cast<int>(o / hd), i = static_cast<int>(o - static_cast<int64_t>(hq) * hd);
+        const int g = hq / G, h = hq - g * G;
+        const Word* src = p.part + ((static_cast<int64_t>(g) * C + j) * G + h) * (hd + 2);
+        const Word* a[3] = {src + i, src + hd, src + hd + 1};
+        float v[3];
+        ok = poll_words<3>(a, 3, want, v) && ok;
+        sa[t] = v[0];
+        smv[t] = v[1];
+        slv[t] = v[2];
+      }
+    }
+    bar_sync(kConsumerBar, kC);
+    if (ctid < nb) {
+      const float* ma = smv + ctid * C;
+      float M = -INFINITY;
+      for (int j = 0; j < C; ++j) M = fmaxf(M, ma[j]);
+      float a = 0.f, L = 0.f;
+      for (int j = 0; j < C; ++j) {
+        const float f = ma[j] != -INFINITY ? expf(ma[j] - M) : 0.f;   // 0: an empty chunk
+        a = fmaf(sa[ctid * C + j], f, a);
+        L = fmaf(slv[ctid * C + j], f, L);
+      }
+      st_word(p.att + b0 + ctid, a / L, want);
+    }
+    bar_sync(kConsumerBar, kC);
+  }
+  return ok;
+}
+
+// Both steps with the shapes the fused path takes (head_dim / group).
+__device__ __forceinline__ bool att_fused(const ChainParams& p, int l, float* sm, int ctid) {
+  const int G = p.n_q_heads / p.n_kv_heads;
+  bool ok;
+  switch (p.head_dim * 8 + G) {
+    case 256 * 8 + 1: ok = att_split<8, 1>(p, l, sm, ctid); break;
+    case 256 * 8 + 2: ok = att_split<8, 2>(p, l, sm, ctid); break;
+    case 128 * 8 + 1: ok = att_split<4, 1>(p, l, sm, ctid); break;
+    case 128 * 8 + 2: ok = att_split<4, 2>(p, l, sm, ctid); break;
+    default: ok = att_split<4, 4>(p, l, sm, ctid); break;   // 128 * 8 + 4
+  }
+  return att_merge(p, l, sm, ctid) && ok;
+}
+
 // Stages the seq-1 attention output for the O projection: query head i / hd
 // takes kv head (i / hd) / group, i.e. column i reads v[(head / group) * hd + i % hd].
 template <int kJ>
@@ -479,8 +761,12 @@ __device__ __forceinline__ bool chain_prologue(const ChainParams& p, int ph, con
                                   wn, store, static_cast<unsigned>(ph + 1), war, war_seen, US,
                                   ctid);
   } else if (kind == PH_O) {
-    if constexpr (kKV)
-      ok = stage_stamped<UnitQ4K, 16>(R, US, p.att, prev, kp.K, ctid);
+    if constexpr (kKV) {
+      // attention of layer l inside this launch (the staging buffer is free
+      // until the O vector is staged below)
+      if (p.fused_att) ok = att_fused(p, l, R.xs, ctid);
+      ok = stage_stamped<UnitQ4K, 16>(R, US, p.att, prev, kp.K, ctid) && ok;
+    }
     else
       ok = stage_gather<8>(R, US, p.v, prev, kp.K, p.head_dim, p.n_q_heads / p.n_kv_heads, ctid);
   } else if (q6) {
@@ -731,7 +1017,7 @@ struct ChainLaunch {
 // gathering v (the decode step over a KV cache).
 qws_status chain_prepare(const char* fn, const qws_layer* layers, int n_layers, float* h,
                          const qws_dims* d, void* ws, size_t ws_bytes, bool kv, ChainLaunch& cl,
-                         std::string& err) {
+                         std::string& err, uint32_t min_xs = 0) {
   auto bad = [&](qws_status s, const char* m) {
     err = std::string(fn) + ": " + m;
     return s;
@@ -865,7 +1151,7 @@ qws_status chain_prepare(const char* fn, const qws_layer* layers, int n_layers, 
   }
   p.stage_bytes = round_up(stage_need + 16, 128);
   p.red_floats = red;
-  p.xs_floats = xs;
+  p.xs_floats = std::max(xs, min_xs);   // the fused attention's scratch, when larger
   const size_t tail = 64 * sizeof(float) + 16;   // warp sums, producer gate
   // Ring depth: at most kChainStages.  A deeper ring prefetches more of the
   // next phase, and that DRAM traffic slows the L2 loads on every CTA's
@@ -966,8 +1252,9 @@ KvChainLayout kv_chain_layout(const qws_dims* d, int64_t max_seq) {
   L.chain = 0;
   L.att = align256(chain_workspace_bytes(d->hidden, d->inter));
   L.part = L.att + align256(static_cast<size_t>(QD) * sizeof(Word));
-  L.bytes = L.part + align256(kv_attention_workspace_bytes(d->n_q_heads, d->n_kv_heads,
-                                                           d->head_dim, max_seq));
+  // the standalone kernels' float partials, or the fused steps' stamped ones
+  L.bytes = L.part + align256(2 * kv_attention_workspace_bytes(d->n_q_heads, d->n_kv_heads,
+                                                               d->head_dim, max_seq));
   return L;
 }
 
@@ -1003,13 +1290,46 @@ qws_status qws::decode_kv_chain(const qws_layer* layers, int n_layers, float* h,
           cudaGetErrorString(e);
     return QWS_ERR_CUDA;
   };
+  // attention inside the chain's O prologue: one launch per group of layers
+  const int G = nq / nkv;
+  const bool fused = (hd == 256 && G <= 2) || (hd == 128 && (G == 1 || G == 2 || G == 4));
+  const int64_t n_ctx = kv->pos + 1;
+  const int chunks = kv_attention_splits(nkv, n_ctx);
+  const int64_t n_out = static_cast<int64_t>(nq) * hd;
+  const int per = static_cast<int>((n_out + device_sms() - 1) / device_sms());
+  const uint32_t att_floats = static_cast<uint32_t>(
+      std::max(4 * kAttGH + kAttWarpsC * kAttGH + 2 * kAttWarpsC * 4,
+               3 * std::min(kAttMergeBatch, per) * chunks));
   for (int g0 = 0; g0 < n_layers; g0 += kMaxLayers) {
     const int n = std::min(kMaxLayers, n_layers - g0);
     ChainLaunch cl;
-    const qws_status rc =
-        chain_prepare("qws_decode_kv", layers + g0, n, h, d, ws, Lw.att, true, cl, err);
+    const qws_status rc = chain_prepare("qws_decode_kv", layers + g0, n, h, d, ws, Lw.att, true,
+                                        cl, err, fused ? att_floats : 0u);
     if (rc != QWS_OK) return rc;
     cl.p.att = att;
+    if (fused) {
+      ChainParams& p = cl.p;
+      p.fused_att = 1;
+      for (int l = 0; l < n; ++l) {
+        p.kc[l] = kv->k_caches[g0 + l];
+        p.vc[l] = kv->v_caches[g0 + l];
+      }
+      p.max_seq = kv->max_seq;
+      p.pos = kv->pos;
+      p.chunks = chunks;
+      p.chunk_len = static_cast<int>((n_ctx + chunks - 1) / chunks);
+      p.rot_dim = kv->rot_dim;
+      p.att_scale = kv->attn_scale;
+      p.softcap = kv->softcap;
+      p.part = reinterpret_cast<Word*>(part);
+      rope_table_f32(kv->rot_dim, kv->pos, kv->rope_base, p.rtc, p.rts);
+      // every stamped word of the group, the attention's included
+      cudaError_t e = cudaMemsetAsync(ws, 0, Lw.bytes, st);
+      if (e != cudaSuccess) return cuda(e, "clear");
+      e = chain_run(cl, 0, 4 * n, st);
+      if (e != cudaSuccess) return cuda(e, "chain");
+      continue;
+    }
     cudaError_t e = chain_clear(cl, ws, st);
     if (e != cudaSuccess) return cuda(e, "clear");
     e = chain_run(cl, 0, 1, st);   // QKV of the group's first layer

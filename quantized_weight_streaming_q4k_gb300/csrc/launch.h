@@ -127,6 +127,11 @@ cudaError_t launch_kv_append(float* kc, float* vc, const float* k, const float* 
 // RoPE and append fused into kv_attention: q, k, v as {value, stamp} words,
 // q and k rotated at pos (rot_dim, base), k and v written at pos of kc / vc
 // (the same caches the attention reads; q is then unused)
+// cos / sin of pos * base^(-2i / rot_dim), i < rot_dim / 2 (rot_dim <= 512),
+// from the f64 angle, rounded to f32
+void rope_table_f32(int rot_dim, int64_t pos, double base, float* c, float* s);
+int kv_attention_splits(int n_kv, int64_t n_ctx);
+
 struct KvFuse {
   const unsigned long long *q, *k, *v;
   float *kc, *vc;

@@ -17,9 +17,12 @@ relative budget that the chain's tolerance carries through both branches:
 The caches: every position but pos is untouched (bit for bit), and position
 pos holds the step's v (within the matvec tolerance of the oracle's).
 One launch over L layers equals L single-layer launches bit for bit.  Shapes
-that fit the decode chain run on it (one chain launch per layer between the
-attention steps); layers with mixed down-projection formats take the
-launch sequence of standalone kernels, tested here as well.
+that fit the decode chain run on it: with head_dim 256 and at most 2 query
+heads per kv head, or head_dim 128 and 1, 2 or 4, the attention runs inside
+the chain kernel (every layer in one launch); other head shapes take one
+chain launch per layer between the standalone attention launches.  Layers
+with mixed down-projection formats take the launch sequence of standalone
+kernels.  Each path is tested here.
 """
 import numpy as np
 import pytest
@@ -32,6 +35,9 @@ pytestmark = pytest.mark.gpu
 
 SMALL = dict(hidden=512, inter=1024, n_q_heads=4, n_kv_heads=2, head_dim=64, eps=1e-6,
              post_norms=1)
+# (n_q_heads, n_kv_heads, head_dim): standalone attention launches between
+# chain launches, then the three shapes of the in-kernel attention
+HEADS = [(4, 2, 64), (4, 2, 128), (4, 1, 128), (2, 2, 256)]
 
 
 def _layer(l, dims, workload, fmt_down=synth.Q6_K):
@@ -106,11 +112,13 @@ def _run_layers(dims, layers, n_layers, max_seq, pos, h0, workload, rot_dim=None
     return h_in, caches, worst
 
 
+@pytest.mark.parametrize("heads", HEADS)
 @pytest.mark.parametrize("post_norms,pos,rot_dim,softcap",
                          [(1, 37, None, 0.0), (0, 5, 32, 0.0), (1, 0, None, 0.0),
                           (1, 63, None, 30.0)])
-def test_decode_kv_small(post_norms, pos, rot_dim, softcap):
-    dims = dict(SMALL, post_norms=post_norms)
+def test_decode_kv_small(post_norms, pos, rot_dim, softcap, heads):
+    nq, nkv, hd = heads
+    dims = dict(SMALL, post_norms=post_norms, n_q_heads=nq, n_kv_heads=nkv, head_dim=hd)
     layers = [_layer(l, dims, 960 + post_norms) for l in range(2)]
     h0 = synth.normal_vector(synth.rng(961, pos), dims["hidden"])
     _run_layers(dims, layers, 2, 64, pos, h0, 960, rot_dim, softcap)
@@ -125,10 +133,12 @@ def test_decode_kv_launch_sequence_path():
     _run_layers(dims, layers, 2, 48, 21, h0, 966)
 
 
-def test_decode_kv_multi_layer_launch_equals_single_layer_launches():
+@pytest.mark.parametrize("heads", [HEADS[0], HEADS[1]])
+def test_decode_kv_multi_layer_launch_equals_single_layer_launches(heads):
     build.build()
     torch.cuda.set_device(0)
-    dims = SMALL
+    nq, nkv, hd = heads
+    dims = dict(SMALL, n_q_heads=nq, n_kv_heads=nkv, head_dim=hd)
     max_seq, pos = 32, 9
     layers = [_layer(l, dims, 962) for l in range(3)]
     ldev = [_dev(L) for L in layers]
@@ -154,12 +164,15 @@ def test_decode_kv_multi_layer_launch_equals_single_layer_launches():
     assert ops.device_error() == 0
 
 
-def test_decode_kv_more_layers_than_one_chain_launch_holds():
-    """70 layers run as a group of 64 and a group of 6 chain launches; the
-    result equals 70 one-layer calls bit for bit (h and every cache)."""
+@pytest.mark.parametrize("heads", [HEADS[0], HEADS[1]])
+def test_decode_kv_more_layers_than_one_chain_launch_holds(heads):
+    """70 layers run as a group of 64 and a group of 6 (chain launches per
+    group); the result equals 70 one-layer calls bit for bit (h and every
+    cache)."""
     build.build()
     torch.cuda.set_device(0)
-    dims = dict(SMALL, hidden=256, inter=512)
+    nq, nkv, hd = heads
+    dims = dict(SMALL, hidden=256, inter=512, n_q_heads=nq, n_kv_heads=nkv, head_dim=hd)
     n, max_seq, pos = 70, 16, 3
     layers = [_dev(_layer(l, dims, 968)) for l in range(n)]
     h0 = synth.normal_vector(synth.rng(969), dims["hidden"])
