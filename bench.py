@@ -481,6 +481,17 @@ def run_decode_kv(args):
 
     chain_b, _, _ = algorithmic_bytes(dims, n_layers)
     kv_b = n_layers * 2 * nkv * (pos + 1) * hd * 4
+    # head shapes whose attention runs inside the chain kernel: one launch per
+    # group of up to 64 layers; else per layer split + merge + chain launch
+    group = dims["n_q_heads"] // nkv
+    if (hd == 256 and group <= 2) or (hd == 128 and group in (1, 2, 4)):
+        kv_launches = -(-n_layers // 64)
+        kv_kernel = ("chain_kernel with the attention inside the O phase's prologue "
+                     "(one launch per token)")
+    else:
+        kv_launches = 1 + 3 * n_layers
+        kv_kernel = ("decode_kv on the chain kernel (per layer: attention split with RoPE and "
+                     "the K/V append fused in + merge + chain launch)")
     nbytes = chain_b + kv_b
     stream = torch.cuda.current_stream()
     for _ in range(max(3, args.warmup)):
@@ -512,11 +523,10 @@ def run_decode_kv(args):
                                f"({pos + 1} cached positions, 4 kv heads of 256), batch 1",
                    "l2": f"{nbytes / 1e9:.2f} GB streamed per token (> L2)"},
         "roofline": {"bound": "hbm",
-                     "kernel": "decode_kv on the chain kernel (per layer: attention split with "
-                               "RoPE and the K/V append fused in + merge + chain launch)",
+                     "kernel": kv_kernel,
                      "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
                      "peak_source": peak_kind, "traffic": None},
-        "bytes_per_token": nbytes, "gpu_launches": (1 + 3 * n_layers) * args.steps,
+        "bytes_per_token": nbytes, "gpu_launches": kv_launches * args.steps,
         "clocks": clk,
     }))
 
