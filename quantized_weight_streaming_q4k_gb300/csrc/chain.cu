@@ -149,6 +149,9 @@ __device__ __forceinline__ bool wait_prologues(const ChainParams& p, int ph) {
 
 // Phase p = 4 * layer + kind; its outputs carry stamp p + 1.  get(p) takes
 // the absolute phase index; Range views this launch's phases from 0.
+// kQFirst: the QKV phase's segments in the order q, k, v (the decode over a
+// KV cache) instead of v, k, q (the chain at sequence length 1).
+template <bool kQFirst>
 struct ChainPhases {
   const ChainParams* p;
   __device__ __forceinline__ int count() const { return 4 * p->n_layers; }
@@ -185,11 +188,21 @@ struct ChainPhases {
     if (kind == PH_QKV) {
       // v first: at sequence length 1 the O phase needs only v, and v's tiles
       // are then dealt in the first round, finished before the CTAs' last
-      // tiles (q and k feed nothing downstream)
+      // tiles (q and k feed nothing downstream).  Over a KV cache q goes
+      // first instead: every attention item needs the group's q, only the
+      // items holding pos need k and v, and they take that row last.
       P.nseg = 3;
-      P.seg[0] = Seg{L.Wv, dst(p->v), p->KD, static_cast<int>((p->KD + kp.T - 1) / kp.T)};
-      P.seg[1] = Seg{L.Wk, dst(p->k), p->KD, static_cast<int>((p->KD + kp.T - 1) / kp.T)};
-      P.seg[2] = Seg{L.Wq, dst(p->q), p->QD, static_cast<int>((p->QD + kp.T - 1) / kp.T)};
+      const int tkv = static_cast<int>((p->KD + kp.T - 1) / kp.T);
+      const int tq = static_cast<int>((p->QD + kp.T - 1) / kp.T);
+      if constexpr (kQFirst) {
+        P.seg[0] = Seg{L.Wq, dst(p->q), p->QD, tq};
+        P.seg[1] = Seg{L.Wk, dst(p->k), p->KD, tkv};
+        P.seg[2] = Seg{L.Wv, dst(p->v), p->KD, tkv};
+      } else {
+        P.seg[0] = Seg{L.Wv, dst(p->v), p->KD, tkv};
+        P.seg[1] = Seg{L.Wk, dst(p->k), p->KD, tkv};
+        P.seg[2] = Seg{L.Wq, dst(p->q), p->QD, tq};
+      }
     } else if (kind == PH_O) {
       P.seg[0] = Seg{L.Wo, dst(p->o), p->H, tiles(p->H)};
     } else if (kind == PH_GU) {
@@ -471,7 +484,59 @@ __device__ __forceinline__ bool att_split(const ChainParams& p, int l, float* sm
       sq[e] = rope_at(sraw + h * hd, i, p.rot_dim, p.rtc, p.rts);
     }
     bar_sync(kConsumerBar, kC);
+    float q[kG][kPL], acc[kG][kPL], m[kG], lsum[kG];
+#pragma unroll
+    for (int h = 0; h < kG; ++h) {
+      m[h] = -INFINITY;
+      lsum[h] = 0.f;
+#pragma unroll
+      for (int c = 0; c < kPL; ++c) {
+        q[h][c] = sq[h * hd + c0 + c] * p.att_scale;
+        acc[h][c] = 0.f;
+      }
+    }
+    const float* kh = kcl + static_cast<int64_t>(g) * p.max_seq * hd + c0;
+    const float* vh = vcl + static_cast<int64_t>(g) * p.max_seq * hd + c0;
+    // one position's update of the running (m, l, acc) of every head
+    auto update = [&](const float (&kr)[kPL], const float (&vr)[kPL]) {
+#pragma unroll
+      for (int h = 0; h < kG; ++h) {
+        float sc = 0.f;
+#pragma unroll
+        for (int c = 0; c < kPL; ++c) sc = fmaf(q[h][c], kr[c], sc);
+        sc = warp_sum(sc);
+        if (p.softcap > 0.f) sc = p.softcap * tanhf(sc / p.softcap);
+        const float mn = fmaxf(m[h], sc);
+        const float alpha = expf(m[h] - mn);
+        const float pr = expf(sc - mn);
+        lsum[h] = fmaf(lsum[h], alpha, pr);
+#pragma unroll
+        for (int c = 0; c < kPL; ++c) acc[h][c] = fmaf(acc[h][c], alpha, pr * vr[c]);
+        m[h] = mn;
+      }
+    };
+    // the cached positions (pos, when it is in this item, comes last)
+    const int64_t pe = has_pos ? p.pos : p1;
+    for (int64_t r0 = p0 + warp; r0 < pe; r0 += 2 * kAttWarpsC) {
+      // two positions per round: both rows' loads in flight together
+      float kr[2][kPL], vr[2][kPL];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int64_t r = min(r0 + u * kAttWarpsC, pe - 1);
+#pragma unroll
+        for (int c = 0; c < kPL; c += 4) {
+          const float4 a = *reinterpret_cast<const float4*>(kh + r * hd + c);
+          const float4 b = *reinterpret_cast<const float4*>(vh + r * hd + c);
+          kr[u][c] = a.x; kr[u][c + 1] = a.y; kr[u][c + 2] = a.z; kr[u][c + 3] = a.w;
+          vr[u][c] = b.x; vr[u][c + 1] = b.y; vr[u][c + 2] = b.z; vr[u][c + 3] = b.w;
+        }
+      }
+      update(kr[0], vr[0]);
+      if (r0 + kAttWarpsC < pe) update(kr[1], vr[1]);
+    }
     if (has_pos) {
+      // k (rotated) and v of pos from the QKV phase; into the caches; then
+      // warp 0 takes the row
       ok = poll_stamped<1>(p.k + static_cast<int64_t>(g) * hd + ctid,
                            p.k + static_cast<int64_t>(g + 1) * hd, want,
                            [&](int, float v) { sraw[ctid] = v; }) &&
@@ -491,60 +556,14 @@ __device__ __forceinline__ bool att_split(const ChainParams& p, int l, float* sm
         p.vc[l][row + i] = vr;
       }
       bar_sync(kConsumerBar, kC);
-    }
-    float q[kG][kPL], acc[kG][kPL], m[kG], lsum[kG];
+      if (warp == 0) {
+        float kr[kPL], vr[kPL];
 #pragma unroll
-    for (int h = 0; h < kG; ++h) {
-      m[h] = -INFINITY;
-      lsum[h] = 0.f;
-#pragma unroll
-      for (int c = 0; c < kPL; ++c) {
-        q[h][c] = sq[h * hd + c0 + c] * p.att_scale;
-        acc[h][c] = 0.f;
-      }
-    }
-    const float* kh = kcl + static_cast<int64_t>(g) * p.max_seq * hd + c0;
-    const float* vh = vcl + static_cast<int64_t>(g) * p.max_seq * hd + c0;
-    for (int64_t r0 = p0 + warp; r0 < p1; r0 += 2 * kAttWarpsC) {
-      // two positions per round: both rows' loads in flight together
-      float kr[2][kPL], vr[2][kPL];
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int64_t r = r0 + u * kAttWarpsC;
-        if (r < p1 && !(has_pos && r == p.pos)) {
-#pragma unroll
-          for (int c = 0; c < kPL; c += 4) {
-            const float4 a = *reinterpret_cast<const float4*>(kh + r * hd + c);
-            const float4 b = *reinterpret_cast<const float4*>(vh + r * hd + c);
-            kr[u][c] = a.x; kr[u][c + 1] = a.y; kr[u][c + 2] = a.z; kr[u][c + 3] = a.w;
-            vr[u][c] = b.x; vr[u][c + 1] = b.y; vr[u][c + 2] = b.z; vr[u][c + 3] = b.w;
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kPL; ++c) {
-            kr[u][c] = skv[c0 + c];
-            vr[u][c] = skv[hd + c0 + c];
-          }
+        for (int c = 0; c < kPL; ++c) {
+          kr[c] = skv[c0 + c];
+          vr[c] = skv[hd + c0 + c];
         }
-      }
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        if (r0 + u * kAttWarpsC >= p1) break;
-#pragma unroll
-        for (int h = 0; h < kG; ++h) {
-          float sc = 0.f;
-#pragma unroll
-          for (int c = 0; c < kPL; ++c) sc = fmaf(q[h][c], kr[u][c], sc);
-          sc = warp_sum(sc);
-          if (p.softcap > 0.f) sc = p.softcap * tanhf(sc / p.softcap);
-          const float mn = fmaxf(m[h], sc);
-          const float alpha = expf(m[h] - mn);
-          const float pr = expf(sc - mn);
-          lsum[h] = fmaf(lsum[h], alpha, pr);
-#pragma unroll
-          for (int c = 0; c < kPL; ++c) acc[h][c] = fmaf(acc[h][c], alpha, pr * vr[u][c]);
-          m[h] = mn;
-        }
+        update(kr, vr);
       }
     }
 #pragma unroll
@@ -613,17 +632,24 @@ __device__ __forceinline__ bool att_merge(const ChainParams& p, int l, float* sm
       }
     }
     bar_sync(kConsumerBar, kC);
-    if (ctid < nb) {
-      const float* ma = smv + ctid * C;
+    // warp w combines outputs w, w + 10, ...; lane c takes chunks c, c + 32, ...
+    // (lane sums in order, then the warp's shuffle tree: a fixed order)
+    const int warp = ctid >> 5, lane = ctid & 31;
+    for (int k = warp; k < nb; k += kAttWarpsC) {
+      const float* ma = smv + k * C;
       float M = -INFINITY;
-      for (int j = 0; j < C; ++j) M = fmaxf(M, ma[j]);
+      for (int j = lane; j < C; j += 32) M = fmaxf(M, ma[j]);
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
       float a = 0.f, L = 0.f;
-      for (int j = 0; j < C; ++j) {
+      for (int j = lane; j < C; j += 32) {
         const float f = ma[j] != -INFINITY ? expf(ma[j] - M) : 0.f;   // 0: an empty chunk
-        a = fmaf(sa[ctid * C + j], f, a);
-        L = fmaf(slv[ctid * C + j], f, L);
+        a = fmaf(sa[k * C + j], f, a);
+        L = fmaf(slv[k * C + j], f, L);
       }
-      st_word(p.att + b0 + ctid, a / L, want);
+      a = warp_sum(a);
+      L = warp_sum(L);
+      if (lane == 0) st_word(p.att + b0 + k, a / L, want);
     }
     bar_sync(kConsumerBar, kC);
   }
@@ -899,7 +925,7 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
     *gate = 0;
   }
   __syncthreads();
-  const ChainPhases phases{&p};
+  const ChainPhases<kKV> phases{&p};
 
   if (threadIdx.x < kProducerThreads) {
     if (threadIdx.x == 0) {
@@ -911,9 +937,11 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
         prefetch_l2(p.L[l].w_pff, p.H * 4);
       }
       if constexpr (kKV)   // ungated: see kGateTiles
-        run_producer(ChainPhases::Range{&phases, p.ph_begin, p.ph_end}, R, &g_err_chain);
+        run_producer(typename ChainPhases<kKV>::Range{&phases, p.ph_begin, p.ph_end}, R,
+                     &g_err_chain);
       else
-        run_producer(ChainPhases::Range{&phases, p.ph_begin, p.ph_end}, R, &g_err_chain,
+        run_producer(typename ChainPhases<kKV>::Range{&phases, p.ph_begin, p.ph_end}, R,
+                     &g_err_chain,
                      ChainGate{gate, p.ph_begin});
     }
     return;
