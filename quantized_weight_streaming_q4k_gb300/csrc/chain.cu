@@ -54,8 +54,10 @@ constexpr uint32_t kChainStages = 4;
 // ring this holds back the one tile that would otherwise land during the
 // boundary.  Measured on the 34-layer Gemma-3-4B chain (same box, two
 // passes): 1015 -> 983 us per token with 2, 1010 with 1; gating only the
-// gate/up phases 990, only the down phases 1011.  The chain that runs over a
-// KV cache copies ungated (1573 us per token ungated, 1613 gated).
+// gate/up phases 990, only the down phases 1011.  Over a KV cache: gated when
+// the attention runs inside (one launch per token: 1404.9 -> 1394.2 us), but
+// not when the chain runs as one launch per layer between the attention
+// launches (each launch starts with an empty ring: 1573 ungated, 1613 gated).
 constexpr int kGateTiles = 2;
 constexpr int64_t kMaxChainHidden = 16 * kMaxConsumers;  // residual vectors: 16 per thread
 
@@ -936,7 +938,7 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
         prefetch_l2(p.L[l].w_pf, p.H * 4);
         prefetch_l2(p.L[l].w_pff, p.H * 4);
       }
-      if constexpr (kKV)   // ungated: see kGateTiles
+      if (kKV && !p.fused_att)   // launches per layer: ungated (see kGateTiles)
         run_producer(typename ChainPhases<kKV>::Range{&phases, p.ph_begin, p.ph_end}, R,
                      &g_err_chain);
       else
