@@ -384,10 +384,13 @@ qws_status qws_decode_chain(const qws_layer* layers, int n_layers, float* h,
  *   caller-owned; positions 0..pos-1 are read, position pos is written.
  *   ws: device, >= qws_decode_kv_workspace_bytes(dims, max_seq) bytes,
  *   16-byte aligned, scratch (its contents on return are unspecified).
- *   Runs on the decode chain's kernel (one launch per layer for the
- *   projections, norms and residuals, with the RoPE / append and attention
- *   launches between them); layers whose down projections differ in format
- *   take a sequence of standalone launches with the same results' bounds.
+ *   Runs on the decode chain's kernel: with head_dim 256 and at most 2
+ *   query heads per kv head, or head_dim 128 and 1, 2 or 4, the attention
+ *   (RoPE at pos, the K/V append, the softmax over positions 0..pos) runs
+ *   inside it and a token is one launch (per 64 layers); other head shapes
+ *   take one chain launch per layer with the attention launches between
+ *   them; layers whose down projections differ in format take a sequence of
+ *   standalone launches with the same results' bounds.
  *   Shapes: as qws_decode_chain; head_dim in {32, 64, 128, 256};
  *   n_q_heads / n_kv_heads in 1..4; 0 <= pos < max_seq; rot_dim even in
  *   (0, head_dim]; rope_base > 0; attn_scale finite; softcap >= 0 (0 = off).
