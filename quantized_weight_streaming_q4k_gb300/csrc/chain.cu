@@ -251,6 +251,17 @@ __device__ __forceinline__ float block_sum(float v, float* wsum, int ctid, int C
   bar_sync(kConsumerBar, C);   // wsum may be reused right after
   return t;
 }
+// The same sum without the closing barrier: the caller does not write `buf`
+// again before a later barrier of all C threads (the prologue's two norms
+// take the two halves of the warp-sum area).
+__device__ __forceinline__ float block_sum_once(float v, float* buf, int ctid, int C) {
+  v = warp_sum(v);
+  if ((ctid & 31) == 0) buf[ctid >> 5] = v;
+  bar_sync(kConsumerBar, C);
+  float t = 0.f;
+  for (int i = 0; i < (C >> 5); ++i) t += buf[i];
+  return t;
+}
 
 constexpr int kC = kMaxConsumers;   // the chain always runs this many consumer threads
 
@@ -341,7 +352,7 @@ __device__ __forceinline__ bool resnorm_stage(const ChainParams& p, const Ring& 
     float ss = 0.f;
 #pragma unroll
     for (int j = 0; j < kJ; ++j) ss = fmaf(ad[j], ad[j], ss);
-    inv1 = 1.0f / sqrtf(block_sum(ss, wsum, ctid, kC) / static_cast<float>(H) + p.eps);
+    inv1 = 1.0f / sqrtf(block_sum_once(ss, wsum, ctid, kC) / static_cast<float>(H) + p.eps);
   }
   float ss2 = 0.f;
 #pragma unroll
@@ -361,7 +372,8 @@ __device__ __forceinline__ bool resnorm_stage(const ChainParams& p, const Ring& 
       if (i < H) st_word(store + i, bs[j], store_stamp);
     }
   }
-  const float inv2 = 1.0f / sqrtf(block_sum(ss2, wsum, ctid, kC) / static_cast<float>(H) + p.eps);
+  const float inv2 =
+      1.0f / sqrtf(block_sum_once(ss2, wsum + 32, ctid, kC) / static_cast<float>(H) + p.eps);
 #pragma unroll
   for (int j = 0; j < kJ; ++j) {
     const int64_t i = ctid + static_cast<int64_t>(j) * kC;
