@@ -443,11 +443,11 @@ __device__ __forceinline__ bool poll_words(const Word* const (&a)[kN], int n, un
 constexpr int kAttWarpsC = kMaxConsumers / 32;   // 10 consumer warps
 constexpr int kAttGH = 512;                       // group heads x head_dim staged
 constexpr int kAttMergeBatch = 48;                // outputs merged per round (at most)
-// staging-buffer floats both steps need (they run one after the other)
-__host__ __device__ constexpr int att_smem_floats(int chunks) {
-  return 4 * kAttGH + kAttWarpsC * kAttGH + 2 * kAttWarpsC * 4 > 3 * kAttMergeBatch * chunks
-             ? 4 * kAttGH + kAttWarpsC * kAttGH + 2 * kAttWarpsC * 4
-             : 3 * kAttMergeBatch * chunks;
+// staging-buffer floats of the split step: rotated q, k / v of pos, raw q,
+// the warps' partial outputs, m and l (the merge step's need, three floats
+// per merged output and chunk, is added by the host)
+__host__ __device__ constexpr int att_split_floats() {
+  return 4 * kAttGH + kAttWarpsC * kAttGH + 2 * kAttWarpsC * 4;
 }
 
 // Element i of a head (raw values at x) rotated at pos (f32 cos / sin).
@@ -487,7 +487,7 @@ __device__ __forceinline__ bool att_split(const ChainParams& p, int l, float* sm
     const int64_t p0 = static_cast<int64_t>(j) * p.chunk_len;
     const int64_t p1 = min(p0 + p.chunk_len, n_ctx);
     const bool has_pos = p.pos >= p0 && p.pos < p1;
-    // raw q of the group's heads (contiguous), k and v of kv head g
+    // raw q of the group's heads (contiguous)
     ok = poll_stamped<2>(p.q + static_cast<int64_t>(g) * kG * hd + ctid,
                          p.q + static_cast<int64_t>(g + 1) * kG * hd, want,
                          [&](int jj, float v) { sraw[ctid + jj * kC] = v; }) &&
@@ -1340,8 +1340,7 @@ qws_status qws::decode_kv_chain(const qws_layer* layers, int n_layers, float* h,
   const int64_t n_out = static_cast<int64_t>(nq) * hd;
   const int per = static_cast<int>((n_out + device_sms() - 1) / device_sms());
   const uint32_t att_floats = static_cast<uint32_t>(
-      std::max(4 * kAttGH + kAttWarpsC * kAttGH + 2 * kAttWarpsC * 4,
-               3 * std::min(kAttMergeBatch, per) * chunks));
+      std::max(att_split_floats(), 3 * std::min(kAttMergeBatch, per) * chunks));
   for (int g0 = 0; g0 < n_layers; g0 += kMaxLayers) {
     const int n = std::min(kMaxLayers, n_layers - g0);
     ChainLaunch cl;
