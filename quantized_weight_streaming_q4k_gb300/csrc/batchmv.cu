@@ -178,6 +178,16 @@ __device__ __forceinline__ void q4k_pair_ab(const uint8_t* h, int c, float (&a)[
   b[1] = dmin * byte_to_float(R, 3);
 }
 
+// a = d * sc(2c + k), b = dmin * m(2c + k) of one sub-block (k = 0, 1)
+__device__ __forceinline__ void q4k_sub_ab(const uint8_t* h, int c, int k, float& a, float& b) {
+  const uint4 hd = *reinterpret_cast<const uint4*>(h);   // block headers are 16-byte aligned
+  Q4kSel sel;
+  sel.set(c);
+  const uint32_t R = q4k_scale_bytes(hd, sel.selP, sel.selQ, sel.sh, sel.mask);
+  a = half_bits_to_float(hd.x) * byte_to_float(R, static_cast<uint32_t>(k));
+  b = half_bits_to_float(hd.x >> 16) * byte_to_float(R, static_cast<uint32_t>(2 + k));
+}
+
 // acc (rows g, g + 8 x vectors 2tq, 2tq + 1) += a C - b S of Q4_K sub-block bi
 __device__ __forceinline__ void q4k_sub(const uint8_t* rg, const uint8_t* rg8, int bi, int tq,
                                         const uint32_t* xh, const uint32_t* xl,
@@ -240,11 +250,16 @@ __device__ __forceinline__ void q4k_pair(const uint8_t* rg, const uint8_t* rg8, 
   mma_16816(c1, h1, xh[w1 + 8], xh[w1 + 12]);
   mma_16816(c0, l1, xl[w0 + 8], xl[w0 + 12]);
   mma_16816(c1, h1, xl[w1 + 8], xl[w1 + 12]);
-  float aa[2], ba[2], ab[2], bb[2];
-  q4k_pair_ab(ha, c, aa, ba);
-  q4k_pair_ab(hb, c, ab, bb);
-  const float a0 = aa[0], b0 = ba[0], a1 = ab[0], b1 = bb[0];
-  const float a2 = aa[1], b2 = ba[1], a3 = ab[1], b3 = bb[1];
+  // the four threads of an MMA group need the same eight values: thread tq
+  // decodes (row g or g + 8 by tq & 1, sub-block 2c + (tq >> 1)) and the
+  // group exchanges them by shuffles
+  float am, bm;
+  q4k_sub_ab((tq & 1) ? hb : ha, c, tq >> 1, am, bm);
+  const int q0 = (threadIdx.x & 31) & ~3;   // lane of tq = 0
+  const float a0 = __shfl_sync(0xFFFFFFFFu, am, q0), b0 = __shfl_sync(0xFFFFFFFFu, bm, q0);
+  const float a1 = __shfl_sync(0xFFFFFFFFu, am, q0 + 1), b1 = __shfl_sync(0xFFFFFFFFu, bm, q0 + 1);
+  const float a2 = __shfl_sync(0xFFFFFFFFu, am, q0 + 2), b2 = __shfl_sync(0xFFFFFFFFu, bm, q0 + 2);
+  const float a3 = __shfl_sync(0xFFFFFFFFu, am, q0 + 3), b3 = __shfl_sync(0xFFFFFFFFu, bm, q0 + 3);
   const float2 sv = reinterpret_cast<const float2*>(ssum)[bi * 4 + tq];
   const float2 tv = reinterpret_cast<const float2*>(ssum)[(bi + 1) * 4 + tq];
   acc[0] = fmaf(a0, c0[0], fmaf(-b0, sv.x, acc[0]));
