@@ -39,11 +39,12 @@ namespace qws {
 __device__ unsigned g_err_batchmv;
 
 constexpr int kBmRows = 16;                     // rows per tile (MMA M)
-// consumer warps = column slices; 16 (four per scheduler) measured 235.8 us
-// for the Q4_K 262144 x 2560 lm_head at batch 8 against 263.8 with 8; the
-// Q4_0 and Q8_0 forms are unchanged (159.7 / 156.4 against 159.3 / 155.4)
-constexpr int kBmWarps = 16;
-constexpr int kBmThreads = 32 + kBmWarps * 32;
+// consumer warps = column slices, per format.  Measured for the 262144 x
+// 2560 lm_head at batch 8 (same box, us for 16 / 20 warps): Q4_K 206.1 /
+// 199.5 (20: two sub-block pairs per slice, none alone), Q4_0 150.0 / 156.9,
+// Q8_0 activations 145.0 / 152.8; 8 warps: Q4_K 263.8.
+__host__ __device__ constexpr int bm_warps(int fmt) { return fmt == 12 ? 20 : 16; }
+__host__ __device__ constexpr int bm_threads(int fmt) { return 32 + bm_warps(fmt) * 32; }
 constexpr int kBmMaxB = 8;                      // MMA N
 constexpr int kBmStages = 4;                    // at most; fewer when the rows are wide
 constexpr int64_t kBmMaxK = 3072;
@@ -71,20 +72,20 @@ __host__ __device__ constexpr int64_t bm_block_bytes(int fmt) { return fmt == 10
 __host__ __device__ constexpr size_t bm_stage_bytes(int64_t K, int fmt) {
   return (static_cast<size_t>(kBmRows) * (K / 32 * bm_block_bytes(fmt)) + 16 + 127) / 128 * 128;
 }
-__host__ __device__ constexpr size_t bm_fixed_bytes(int64_t K) {
-  return bm_xs_bytes(K) + 2 * kBmWarps * kBmRows * kBmMaxB * sizeof(float) +
+__host__ __device__ constexpr size_t bm_fixed_bytes(int64_t K, int fmt) {
+  return bm_xs_bytes(K) + 2 * bm_warps(fmt) * kBmRows * kBmMaxB * sizeof(float) +
          kBmMaxB * sizeof(float) + static_cast<size_t>(kBmMaxB) * (K / 32) * sizeof(float) +
          2 * kBmStages * sizeof(uint64_t) + 64;
 }
 constexpr size_t kBmSmemBudget = 227 * 1024;
 // ring depth that fits beside the activations (0 when not even two do)
 __host__ __device__ constexpr int bm_stages(int64_t K, int fmt) {
-  const size_t f = bm_fixed_bytes(K), st = bm_stage_bytes(K, fmt);
+  const size_t f = bm_fixed_bytes(K, fmt), st = bm_stage_bytes(K, fmt);
   const size_t n = f >= kBmSmemBudget ? 0 : (kBmSmemBudget - f) / st;
   return n >= kBmStages ? kBmStages : static_cast<int>(n);
 }
 __host__ __device__ constexpr size_t bm_smem_bytes(int64_t K, int fmt) {
-  return bm_fixed_bytes(K) + bm_stages(K, fmt) * bm_stage_bytes(K, fmt);
+  return bm_fixed_bytes(K, fmt) + bm_stages(K, fmt) * bm_stage_bytes(K, fmt);
 }
 
 __device__ __forceinline__ void mma_16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0,
@@ -273,8 +274,9 @@ __device__ __forceinline__ void q4k_pair(const uint8_t* rg, const uint8_t* rg8, 
 }
 
 template <int kFmt>   // 2: Q4_0, 12: Q4_K (f32 x); 102: Q4_0, 108: Q8_0 (Q8_0 x)
-__global__ void __launch_bounds__(kBmThreads, 1) batch_q4_matvec_kernel(
+__global__ void __launch_bounds__(bm_threads(kFmt), 1) batch_q4_matvec_kernel(
     const __grid_constant__ BmParams p) {
+  constexpr int kBmWarps = bm_warps(kFmt);
   extern __shared__ __align__(128) uint8_t bm_smem[];
   const int64_t K = p.K;
   __half* xs_hi = reinterpret_cast<__half*>(bm_smem);
@@ -568,7 +570,7 @@ cudaError_t launch_batch_q4_matvec(int fmt, const uint8_t* W, const float* x, fl
   const int grid = static_cast<int>(std::min<int64_t>(p.n_tiles, device_sms()));
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kBmThreads);
+  cfg.blockDim = dim3(bm_threads(fmt));
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
