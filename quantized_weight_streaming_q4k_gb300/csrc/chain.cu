@@ -615,20 +615,22 @@ __device__ __forceinline__ bool att_split(const ChainParams& p, int l, float* sm
 }
 
 // Step 2: attention outputs [o0, o1) of layer l from the items' partials,
-// kAttMergeBatch outputs per round; out = sum_j e^(m_j - M) acc_j /
-// sum_j e^(m_j - M) l_j (M = max_j m_j; chunks added in order).
+// min(kAttMergeBatch, per) outputs per round (the staging-buffer floats the
+// host reserves: three per output of a round and chunk); out = sum_j
+// e^(m_j - M) acc_j / sum_j e^(m_j - M) l_j (M = max_j m_j).
 __device__ __forceinline__ bool att_merge(const ChainParams& p, int l, float* sm, int ctid) {
   const unsigned want = static_cast<unsigned>(4 * l + 1);
   const int hd = p.head_dim, G = p.n_q_heads / p.n_kv_heads, C = p.chunks;
   const int64_t n_out = static_cast<int64_t>(p.n_q_heads) * hd;
   const int64_t per = (n_out + gridDim.x - 1) / gridDim.x;
   const int64_t o0 = blockIdx.x * per, o1 = min(o0 + per, n_out);
-  float* sa = sm;                                   // [batch][C] acc
-  float* smv = sa + kAttMergeBatch * C;             // [batch][C] m
-  float* slv = smv + kAttMergeBatch * C;            // [batch][C] l
+  const int bmax = static_cast<int>(min(static_cast<int64_t>(kAttMergeBatch), per));
+  float* sa = sm;                                   // [bmax][C] acc
+  float* smv = sa + bmax * C;                       // [bmax][C] m
+  float* slv = smv + bmax * C;                      // [bmax][C] l
   bool ok = true;
-  for (int64_t b0 = o0; b0 < o1; b0 += kAttMergeBatch) {
-    const int nb = static_cast<int>(min(static_cast<int64_t>(kAttMergeBatch), o1 - b0));
+  for (int64_t b0 = o0; b0 < o1; b0 += bmax) {
+    const int nb = static_cast<int>(min(static_cast<int64_t>(bmax), o1 - b0));
     for (int t0 = 0; t0 < nb * C; t0 += kC) {
       const int t = t0 + ctid;
       if (t < nb * C) {

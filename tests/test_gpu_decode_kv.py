@@ -124,6 +124,17 @@ def test_decode_kv_small(post_norms, pos, rot_dim, softcap, heads):
     _run_layers(dims, layers, 2, 64, pos, h0, 960, rot_dim, softcap)
 
 
+@pytest.mark.parametrize("heads", [HEADS[1], HEADS[3]])
+def test_decode_kv_long_cache(heads):
+    """4001 cached positions over 2 kv heads: 76 chunks of 53 positions, so
+    every warp of the in-kernel attention takes three rounds of rows."""
+    nq, nkv, hd = heads
+    dims = dict(SMALL, n_q_heads=nq, n_kv_heads=nkv, head_dim=hd)
+    layers = [_layer(l, dims, 972) for l in range(2)]
+    h0 = synth.normal_vector(synth.rng(973), dims["hidden"])
+    _run_layers(dims, layers, 2, 4096, 4000, h0, 972)
+
+
 def test_decode_kv_launch_sequence_path():
     """Layers whose down projections differ in format take the launch
     sequence (the chain kernel takes one down format): same parity bar."""
