@@ -124,15 +124,22 @@ def test_decode_kv_small(post_norms, pos, rot_dim, softcap, heads):
     _run_layers(dims, layers, 2, 64, pos, h0, 960, rot_dim, softcap)
 
 
-@pytest.mark.parametrize("heads", [HEADS[1], HEADS[3]])
-def test_decode_kv_long_cache(heads):
-    """4001 cached positions over 2 kv heads: 76 chunks of 53 positions, so
-    every warp of the in-kernel attention takes three rounds of rows."""
-    nq, nkv, hd = heads
-    dims = dict(SMALL, n_q_heads=nq, n_kv_heads=nkv, head_dim=hd)
+@pytest.mark.parametrize("shape,pos,max_seq", [
+    # 4001 cached positions over 2 kv heads: 76 chunks of 53 positions, so
+    # every warp of the in-kernel attention takes three rounds of rows
+    (dict(n_q_heads=4, n_kv_heads=2, head_dim=128), 4000, 4096),
+    (dict(n_q_heads=2, n_kv_heads=2, head_dim=256), 4000, 4096),
+    # 3 kv heads: 51 chunks each, 153 items on 152 CTAs (one CTA takes two)
+    (dict(n_q_heads=6, n_kv_heads=3, head_dim=128), 2000, 2048),
+    # 64 query heads of 128: 8192 outputs, 54 per CTA, merged in two rounds;
+    # 32 kv heads x 5 chunks = 160 items
+    (dict(hidden=2048, inter=2048, n_q_heads=64, n_kv_heads=32, head_dim=128), 200, 256),
+])
+def test_decode_kv_long_cache(shape, pos, max_seq):
+    dims = dict(SMALL, **shape)
     layers = [_layer(l, dims, 972) for l in range(2)]
     h0 = synth.normal_vector(synth.rng(973), dims["hidden"])
-    _run_layers(dims, layers, 2, 4096, 4000, h0, 972)
+    _run_layers(dims, layers, 2, max_seq, pos, h0, 972)
 
 
 def test_decode_kv_launch_sequence_path():
