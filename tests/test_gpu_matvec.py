@@ -160,6 +160,22 @@ def test_batched_matvec(fmt, batch):
     assert_bound(y, ref, bound, what=f"{FMT_NAME[fmt]} batch {batch}")
 
 
+@pytest.mark.parametrize("fmt", [oracle.Q4_K, oracle.Q4_0])
+@pytest.mark.parametrize("hidden", [256, 768, 3072])
+def test_batched_matvec_hidden_sizes(fmt, hidden):
+    """Batch 8 on the decode-once kernel at hidden sizes whose column slices
+    do not split evenly: at 256 most warps take no block, at 768 and 3072
+    slices are odd and some start on an odd sub-block."""
+    rows = 100
+    g = synth.rng(1009, fmt, hidden)
+    W = synth.matrix(fmt, g, rows, hidden)
+    x = synth.normal_vector(g, hidden, batch=8)
+    y = run_matvec(fmt, W, x, rows, hidden, batch=8)
+    ref, bound = oracle.matvec(fmt, W, rows, hidden, x, threads=THREADS)
+    assert y.shape == (8, rows)
+    assert_bound(y, ref, bound, what=f"{FMT_NAME[fmt]} batch 8 hidden {hidden}")
+
+
 @pytest.mark.parametrize("split_k", [2, 5, 10])
 @pytest.mark.parametrize("batch", [1, 8])
 def test_q4_0_split_k(split_k, batch):
