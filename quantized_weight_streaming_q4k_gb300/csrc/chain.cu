@@ -930,6 +930,12 @@ template <bool kWide, bool kKV>
 __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
     chain_kernel(const __grid_constant__ ChainParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
+  // A kernel launched after this one with a programmatic dependency may be
+  // scheduled from now on: it waits for this grid's completion before it
+  // touches data of this launch, and its blocks only find room on SMs whose
+  // chain CTA has exited, so e.g. the next matvec's weight copies overlap
+  // the final residual of the keeper CTA instead of following it.
+  pdl_launch_dependents();
   const Ring R = make_ring(smem, p.S, p.stage_bytes, p.red_floats, p.xs_floats);
   float* wsum = reinterpret_cast<float*>(smem + ring_smem_bytes(p.S, p.stage_bytes, p.red_floats,
                                                                  p.xs_floats));
