@@ -246,3 +246,118 @@ def test_selftest_wait_timeout_checks_arguments(lib):
     assert lib.qws_selftest_wait_timeout(0, 3_000_000_000, None, None) == SHAPE
     assert lib.qws_selftest_wait_timeout(1, 1000, None, None) == NULL
     assert lib.qws_selftest_wait_timeout(1, 1000, C.c_void_p(0x10004), None) == ALIGN
+
+
+def _layers(n, **over):
+    """n qws_layer structs of fake aligned addresses, Gemma-3 formats (Q4_K,
+    Q6_K down); keyword arguments override fields of layer 0."""
+    arr = (_lib.QwsLayer * n)()
+    for i in range(n):
+        L = arr[i]
+        for f in ("Wq", "Wk", "Wv", "Wo", "Wg", "Wu", "Wd"):
+            setattr(L, f, A)
+        L.fmt_qkv = L.fmt_o = L.fmt_gu = 12
+        L.fmt_down = 14
+        for f in ("w_in", "w_post_attn", "w_pre_ffn", "w_post_ffn"):
+            setattr(L, f, A)
+    for k, v in over.items():
+        setattr(arr[0], k, v)
+    return arr
+
+
+def _dims(**over):
+    d = dict(hidden=2560, inter=10240, n_q_heads=8, n_kv_heads=4, head_dim=256, eps=1e-6,
+             post_norms=1)
+    d.update(over)
+    return _lib.QwsDims(d["hidden"], d["inter"], d["n_q_heads"], d["n_kv_heads"],
+                        d["head_dim"], d["eps"], d["post_norms"])
+
+
+def test_decode_chain_checks(lib):
+    need = lib.qws_workspace_bytes(_lib.OP_DECODE_CHAIN, 0, 2560, 10240, 1, 0)
+    assert need > 0
+
+    def call(layers=None, n=2, h=A, dims=None, ws=A, ws_bytes=need):
+        layers = _layers(n) if layers is None else layers
+        D = _dims() if dims is None else dims
+        return lib.qws_decode_chain(layers, n, h, C.byref(D), ws, ws_bytes, None)
+
+    assert lib.qws_decode_chain(None, 2, A, C.byref(_dims()), A, need, None) == NULL
+    assert call(h=None) == NULL
+    assert call(ws=None) == NULL
+    assert call(n=0) == SHAPE
+    assert call(layers=_layers(65), n=65) == SHAPE          # one parameter block: <= 64
+    assert call(dims=_dims(n_q_heads=6)) == SHAPE          # 6 % 4 != 0
+    assert call(dims=_dims(hidden=2500)) == SHAPE
+    assert call(dims=_dims(inter=10000)) == SHAPE
+    assert call(dims=_dims(hidden=6144, inter=12288)) == SHAPE   # > 5120
+    assert call(dims=_dims(eps=-1.0)) == SHAPE
+    assert call(h=A + 2) == ALIGN
+    assert call(ws=A + 8) == ALIGN
+    assert call(ws_bytes=need - 8) == WORKSPACE
+    assert call(layers=_layers(2, Wd=None)) == NULL
+    assert call(layers=_layers(2, Wo=A + 8)) == ALIGN
+    assert call(layers=_layers(2, w_pre_ffn=None)) == NULL
+    assert call(layers=_layers(2, w_post_attn=None)) == NULL     # sandwich norms need it
+    assert call(layers=_layers(2, w_in=A + 2)) == ALIGN
+    assert call(layers=_layers(2, fmt_qkv=14)) == FORMAT
+    assert call(layers=_layers(2, fmt_down=2)) == FORMAT
+    assert call(layers=_layers(2, fmt_down=12)) == FORMAT        # differs from layer 1
+    # without the post norms their weights may be NULL: the call gets as far
+    # as the format check
+    assert call(layers=_layers(2, w_post_attn=None, fmt_down=2),
+                dims=_dims(post_norms=0)) == FORMAT
+    assert b"qws_decode_chain" in lib.qws_last_error()
+
+
+def test_decode_kv_checks(lib):
+    D0 = _dims()
+    need = lib.qws_decode_kv_workspace_bytes(C.byref(D0), 2048)
+    assert need > 0
+    caches = (C.c_void_p * 2)(A, A)
+
+    def kv(**over):
+        k = dict(k_caches=C.cast(caches, C.c_void_p), v_caches=C.cast(caches, C.c_void_p),
+                 max_seq=2048, pos=1024, rot_dim=256, rope_base=1e6, attn_scale=0.0625,
+                 softcap=0.0)
+        k.update(over)
+        return _lib.QwsKv(k["k_caches"], k["v_caches"], k["max_seq"], k["pos"], k["rot_dim"],
+                          k["rope_base"], k["attn_scale"], k["softcap"])
+
+    def call(layers=None, n=2, h=A, dims=None, K=None, ws=A, ws_bytes=need):
+        layers = _layers(n) if layers is None else layers
+        D = _dims() if dims is None else dims
+        K = kv() if K is None else K
+        return lib.qws_decode_kv(layers, n, h, C.byref(D), C.byref(K), ws, ws_bytes, None)
+
+    assert lib.qws_decode_kv(_layers(2), 2, A, C.byref(D0), None, A, need, None) == NULL
+    assert call(h=None) == NULL
+    assert call(n=0) == SHAPE
+    assert call(dims=_dims(n_q_heads=8, n_kv_heads=1)) == SHAPE    # group of 8 > 4
+    assert call(dims=_dims(n_q_heads=6)) == SHAPE
+    assert call(dims=_dims(head_dim=96, n_q_heads=8, n_kv_heads=8, hidden=768,
+                           inter=2048)) == SHAPE
+    assert call(dims=_dims(inter=1000)) == SHAPE
+    assert call(dims=_dims(eps=-1.0)) == SHAPE
+    assert call(K=kv(k_caches=None)) == NULL
+    assert call(K=kv(pos=2048)) == SHAPE
+    assert call(K=kv(pos=-1)) == SHAPE
+    assert call(K=kv(max_seq=0, pos=0)) == SHAPE
+    assert call(K=kv(rot_dim=255)) == SHAPE
+    assert call(K=kv(rot_dim=512)) == SHAPE
+    assert call(K=kv(rot_dim=0)) == SHAPE
+    assert call(K=kv(rope_base=0.0)) == SHAPE
+    assert call(K=kv(attn_scale=float("inf"))) == SHAPE
+    assert call(K=kv(softcap=-1.0)) == SHAPE
+    assert call(h=A + 4) == ALIGN
+    assert call(ws=A + 8) == ALIGN
+    assert call(ws_bytes=need - 8) == WORKSPACE
+    assert call(layers=_layers(2, Wk=None)) == NULL
+    assert call(layers=_layers(2, Wg=A + 4)) == ALIGN
+    assert call(layers=_layers(2, w_in=None)) == NULL
+    assert call(layers=_layers(2, fmt_o=2)) == FORMAT
+    bad = (C.c_void_p * 2)(None, A)
+    assert call(K=kv(v_caches=C.cast(bad, C.c_void_p))) == NULL
+    mis = (C.c_void_p * 2)(A + 4, A)
+    assert call(K=kv(k_caches=C.cast(mis, C.c_void_p))) == ALIGN
+    assert b"qws_decode_kv" in lib.qws_last_error()
