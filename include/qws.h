@@ -365,6 +365,22 @@ typedef struct {
 qws_status qws_decode_chain(const qws_layer* layers, int n_layers, float* h,
                             const qws_dims* dims, void* ws, size_t ws_bytes, qws_stream stream);
 
+/* qws_decode_chain followed by the model's final norm in the same launch
+ * (infer-compute README §Architecture: the decode path ends with the final
+ * norm before the lm_head): after the last layer,
+ *   hn = rms_norm(h, w_final) = h * (mean(h^2) + eps)^-1/2 * w_final,
+ * computed by the CTA that writes h, so a following lm_head reads hn with no
+ * norm launch in between.  h, layers, dims, ws: as for qws_decode_chain (h
+ * holds the last layer's output on return, bit-identical to that call's).
+ *   w_final  [hidden] f32 device, 4-byte aligned
+ *   hn       [hidden] f32 device, 4-byte aligned, out; must not overlap h
+ * Errors: those of qws_decode_chain; QWS_ERR_NULL if w_final or hn is NULL,
+ * QWS_ERR_ALIGN if either is misaligned, QWS_ERR_SHAPE if hn overlaps h (all
+ * checked before any launch). */
+qws_status qws_decode_chain_final_norm(const qws_layer* layers, int n_layers, float* h,
+                                      const float* w_final, float* hn, const qws_dims* dims,
+                                      void* ws, size_t ws_bytes, qws_stream stream);
+
 /* ------------------------------------------------------------------------
  * One decode step at sequence position pos with a KV cache (infer-compute
  * README §Architecture: decode is norm -> QKV -> attend -> O -> FFN per layer;

@@ -72,6 +72,8 @@ SIGNATURES = {
     "qws_rms_norm": (I, [F, F, F, I64, C.c_float, I, P]),
     "qws_residual_add": (I, [F, F, I64, I, P]),
     "qws_decode_chain": (I, [C.POINTER(QwsLayer), I, F, C.POINTER(QwsDims), P, SZ, P]),
+    "qws_decode_chain_final_norm": (I, [C.POINTER(QwsLayer), I, F, F, F, C.POINTER(QwsDims), P,
+                                        SZ, P]),
     "qws_workspace_bytes": (SZ, [I, I64, I64, I64, I, I]),
     "qws_last_error": (C.c_char_p, []),
     "qws_device_error": (I, [C.POINTER(U)]),

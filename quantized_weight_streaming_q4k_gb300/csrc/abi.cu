@@ -552,6 +552,18 @@ qws_status qws_decode_chain(const qws_layer* layers, int n_layers, float* h,
   return ok();
 }
 
+qws_status qws_decode_chain_final_norm(const qws_layer* layers, int n_layers, float* h,
+                                      const float* w_final, float* hn, const qws_dims* dims,
+                                      void* ws, size_t ws_bytes, qws_stream stream) {
+  if (!w_final || !hn) return fail(QWS_ERR_NULL, "qws_decode_chain_final_norm: NULL argument");
+  std::string err;
+  const qws_status st = qws::decode_chain(layers, n_layers, h, dims, ws, ws_bytes,
+                                          reinterpret_cast<cudaStream_t>(stream), err, w_final,
+                                          hn, "qws_decode_chain_final_norm");
+  if (st != QWS_OK) return fail(st, "%s", err.c_str());
+  return ok();
+}
+
 size_t qws_workspace_bytes(qws_op op, int64_t rows, int64_t hidden, int64_t inter, int batch,
                            int split_k) {
   switch (op) {

@@ -89,6 +89,9 @@ struct ChainParams {
   // [4 * n_layers]: CTAs done with each phase's prologue (zeroed per token)
   unsigned* prologues;
   float* h;                   // the caller's h (in: layer 0 input, out: chain output)
+  // optional final norm of the last layer's output (keeper CTA): hn = rms_norm(h, w_final)
+  const float* w_final;
+  float* hn;
   uint32_t S, stage_bytes, red_floats, xs_floats;
   // This launch runs phases [ph_begin, ph_end) of the token; several launches
   // with the same parameters and workspace (cleared once per token) run a
@@ -825,13 +828,22 @@ __device__ __forceinline__ bool chain_prologue(const ChainParams& p, int ph, con
   return ok;
 }
 
-// Final residual on the keeper CTA: h = h1 + rms_norm(f, w_post_ffn) (or h1 + f).
+// Final residual on the keeper CTA: h = h1 + rms_norm(f, w_post_ffn) (or h1 + f),
+// then, when hn is set, hn = rms_norm(h, w_final) (the model's final norm, so
+// that the next kernel reads its input straight from this launch).
 template <int kJ>
 __device__ __noinline__ bool chain_final(const ChainParams& p, float* wsum, int ctid, int C) {
   const int Ll = p.n_layers - 1;
   const bool post = p.post_norms != 0;
-  float hv[kJ], fv[kJ];
+  float hv[kJ], fv[kJ], wp[kJ], wf[kJ];
   const Word* h1 = p.h1 + (Ll & 1) * p.H;
+  // the norm weights first: their loads overlap the polls below
+#pragma unroll
+  for (int j = 0; j < kJ; ++j) {
+    const int64_t i = ctid + static_cast<int64_t>(j) * kC;
+    wp[j] = (i < p.H && post) ? p.L[Ll].w_pff[i] : 0.f;
+    wf[j] = (i < p.H && p.hn) ? p.w_final[i] : 0.f;
+  }
   // every CTA is past its last prologue, so none still reads the caller's h
   bool ok = wait_prologues(p, 4 * p.n_layers - 1);
 #pragma unroll
@@ -849,11 +861,24 @@ __device__ __noinline__ bool chain_final(const ChainParams& p, float* wsum, int 
     for (int j = 0; j < kJ; ++j) ss = fmaf(fv[j], fv[j], ss);
     inv = 1.0f / sqrtf(block_sum(ss, wsum, ctid, C) / static_cast<float>(p.H) + p.eps);
   }
+  float ss = 0.f;
 #pragma unroll
   for (int j = 0; j < kJ; ++j) {
     const int64_t i = ctid + static_cast<int64_t>(j) * kC;
-    if (i < p.H)
-      p.h[i] = __fadd_rn(hv[j], post ? __fmul_rn(__fmul_rn(fv[j], inv), p.L[Ll].w_pff[i]) : fv[j]);
+    if (i < p.H) {
+      hv[j] = __fadd_rn(hv[j], post ? __fmul_rn(__fmul_rn(fv[j], inv), wp[j]) : fv[j]);
+      p.h[i] = hv[j];
+      ss = fmaf(hv[j], hv[j], ss);
+    }
+  }
+  if (p.hn) {
+    const float inv_f =
+        1.0f / sqrtf(block_sum(ss, wsum, ctid, C) / static_cast<float>(p.H) + p.eps);
+#pragma unroll
+    for (int j = 0; j < kJ; ++j) {
+      const int64_t i = ctid + static_cast<int64_t>(j) * kC;
+      if (i < p.H) p.hn[i] = __fmul_rn(__fmul_rn(hv[j], inv_f), wf[j]);
+    }
   }
   return ok;
 }
@@ -958,6 +983,7 @@ __global__ void __launch_bounds__(kRoleThreads + kMaxConsumers, 1)
         prefetch_l2(p.L[l].w_pf, p.H * 4);
         prefetch_l2(p.L[l].w_pff, p.H * 4);
       }
+      if (blockIdx.x == gridDim.x - 1) prefetch_l2(p.w_final, p.H * 4);
       if (kKV && !p.fused_att)   // launches per layer: ungated (see kGateTiles)
         run_producer(typename ChainPhases<kKV>::Range{&phases, p.ph_begin, p.ph_end}, R,
                      &g_err_chain);
@@ -1257,15 +1283,34 @@ cudaError_t chain_run(ChainLaunch& cl, int ph_begin, int ph_end, cudaStream_t st
 // this translation unit with the workspace layout it depends on.
 qws_status qws::decode_chain(const qws_layer* layers, int n_layers, float* h,
                                  const qws_dims* d, void* ws, size_t ws_bytes, cudaStream_t st,
-                                 std::string& err) {
+                                 std::string& err, const float* w_final, float* hn,
+                                 const char* fn) {
+  if (hn || w_final) {
+    if (!hn || !w_final) {
+      err = std::string(fn) + ": w_final and hn must both be given";
+      return QWS_ERR_NULL;
+    }
+    if (reinterpret_cast<uintptr_t>(hn) % 4 || reinterpret_cast<uintptr_t>(w_final) % 4) {
+      err = std::string(fn) + ": w_final and hn must be 4-byte aligned";
+      return QWS_ERR_ALIGN;
+    }
+    // the keeper writes h[i] and hn[i] from the same thread, h first
+    const uintptr_t a = reinterpret_cast<uintptr_t>(h), b = reinterpret_cast<uintptr_t>(hn);
+    const uintptr_t n = d ? static_cast<uintptr_t>(std::max<int64_t>(d->hidden, 0)) * 4 : 0;
+    if (h && a < b + n && b < a + n) {
+      err = std::string(fn) + ": hn must not overlap h";
+      return QWS_ERR_SHAPE;
+    }
+  }
   ChainLaunch cl;
-  const qws_status rc =
-      chain_prepare("qws_decode_chain", layers, n_layers, h, d, ws, ws_bytes, false, cl, err);
+  const qws_status rc = chain_prepare(fn, layers, n_layers, h, d, ws, ws_bytes, false, cl, err);
   if (rc != QWS_OK) return rc;
+  cl.p.w_final = w_final;
+  cl.p.hn = hn;
   cudaError_t e = chain_clear(cl, ws, st);
   if (e == cudaSuccess) e = chain_run(cl, 0, 4 * n_layers, st);
   if (e != cudaSuccess) {
-    err = std::string("qws_decode_chain: ") + cudaGetErrorName(e) + " " + cudaGetErrorString(e);
+    err = std::string(fn) + ": " + cudaGetErrorName(e) + " " + cudaGetErrorString(e);
     return QWS_ERR_CUDA;
   }
   return QWS_OK;

@@ -181,8 +181,12 @@ qws_status decode_kv(const qws_layer* layers, int n_layers, float* h, const qws_
 // decode chain (chain.cu)
 size_t chain_workspace_bytes(int64_t hidden, int64_t inter);
 unsigned read_clear_chain_errors();
+// w_final / hn (both or neither): also hn = rms_norm(h_out, w_final) in the
+// same launch (qws_decode_chain_final_norm).
 qws_status decode_chain(const qws_layer* layers, int n_layers, float* h, const qws_dims* d,
-                        void* ws, size_t ws_bytes, cudaStream_t st, std::string& err);
+                        void* ws, size_t ws_bytes, cudaStream_t st, std::string& err,
+                        const float* w_final = nullptr, float* hn = nullptr,
+                        const char* fn = "qws_decode_chain");
 // The decode step over a KV cache on the chain kernel: true when the shapes
 // fit the chain (hidden <= 5120, q_dim and kv_dim <= 4 * hidden); the
 // workspace the step needs then (chain words, attention output words and

@@ -310,19 +310,27 @@ def make_dims(d: dict) -> Dims:
                 int(d["head_dim"]), float(d["eps"]), int(d["post_norms"]))
 
 
-def decode_chain(layers, h, dims: dict, workspace=None, stream=None):
+def decode_chain(layers, h, dims: dict, workspace=None, stream=None, w_final=None, hn=None):
     """Runs len(layers) decoder layers on h (in place).  layers: list of dicts
-    of device tensors (see make_layer) or prepared Layer structs."""
+    of device tensors (see make_layer) or prepared Layer structs.  With
+    w_final and hn (qws_decode_chain_final_norm) the same launch also writes
+    hn = rms_norm(h, w_final) after the last layer."""
     n = len(layers)
     arr = (Layer * n)(*[L if isinstance(L, Layer) else make_layer(L) for L in layers])
     D = make_dims(dims)
     need = workspace_bytes(OP_DECODE_CHAIN, 0, dims["hidden"], dims["inter"], 1, 0)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=h.device)
-    check(lib().qws_decode_chain(arr, n, _dev(h, "h", torch.float32), C.byref(D),
-                                 _dev(workspace, "workspace"),
-                                 workspace.numel() * workspace.element_size(),
-                                 stream_handle(stream)))
+    nbytes = workspace.numel() * workspace.element_size()
+    if w_final is None and hn is None:
+        check(lib().qws_decode_chain(arr, n, _dev(h, "h", torch.float32), C.byref(D),
+                                     _dev(workspace, "workspace"), nbytes,
+                                     stream_handle(stream)))
+        return h
+    check(lib().qws_decode_chain_final_norm(
+        arr, n, _dev(h, "h", torch.float32), _dev(w_final, "w_final", torch.float32),
+        _dev(hn, "hn", torch.float32), C.byref(D), _dev(workspace, "workspace"), nbytes,
+        stream_handle(stream)))
     return h
 
 

@@ -32,7 +32,7 @@ def test_header_declares_the_expected_calls():
     names = declared_functions()
     for n in ["qws_q4k_matvec", "qws_q6k_matvec", "qws_q4_0_matvec", "qws_q4k_qkv_proj",
               "qws_q4k_ffn_gate_up_geglu_down", "qws_rms_norm", "qws_residual_add",
-              "qws_decode_chain", "qws_workspace_bytes", "qws_last_error", "qws_device_error",
+              "qws_decode_chain", "qws_decode_chain_final_norm", "qws_workspace_bytes", "qws_last_error", "qws_device_error",
               "qws_quantize_q8_0", "qws_q8_matvec", "qws_q8_qkv_proj",
               "qws_q4k_prefill_matmul", "qws_rope_at_pos", "qws_kv_append",
               "qws_kv_attention"]:
@@ -308,6 +308,23 @@ def test_decode_chain_checks(lib):
     assert call(layers=_layers(2, w_post_attn=None, fmt_down=2),
                 dims=_dims(post_norms=0)) == FORMAT
     assert b"qws_decode_chain" in lib.qws_last_error()
+
+    def fcall(w_final=A + 0x40000, hn=A + 0x80000, h=A, dims=None, ws_bytes=need):
+        D = _dims() if dims is None else dims
+        return lib.qws_decode_chain_final_norm(_layers(2), 2, h, w_final, hn, C.byref(D), A,
+                                               ws_bytes, None)
+
+    assert fcall(w_final=None) == NULL
+    assert fcall(hn=None) == NULL
+    assert fcall(hn=A + 0x80002) == ALIGN
+    assert fcall(w_final=A + 0x40001) == ALIGN
+    assert fcall(hn=A) == SHAPE                       # hn = h
+    assert fcall(hn=A + 4 * 2559) == SHAPE            # last element of h
+    # adjacent but not overlapping: passes, and the workspace check comes next
+    assert fcall(h=A + 4 * 2560, hn=A, ws_bytes=need - 8) == WORKSPACE
+    assert fcall(dims=_dims(hidden=2500)) == SHAPE    # the chain's own checks follow
+    assert fcall(ws_bytes=need - 8) == WORKSPACE
+    assert b"qws_decode_chain_final_norm" in lib.qws_last_error()
 
 
 def test_decode_kv_checks(lib):

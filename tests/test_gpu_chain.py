@@ -174,6 +174,29 @@ def test_chain_full_size_gemma3_4b():
     assert rel < 1e-3
 
 
+@pytest.mark.parametrize("shape", ["small", "wide", "gemma3_4b"])
+def test_chain_final_norm(shape):
+    """qws_decode_chain_final_norm: h bit-identical to qws_decode_chain's, and
+    hn = rms_norm(h, w_final) within the norm's 1e-5 relative bound against the
+    oracle's norm of the GPU's h (the narrow and the wide keeper step, and the
+    Gemma-3-4B hidden size)."""
+    dims, n = {"small": (SMALL, 3), "wide": (WIDE, 2), "gemma3_4b": (synth.GEMMA3_4B, 2)}[shape]
+    layers = [synth.chain_layer(l, dims, fmt_down=oracle.Q6_K, workload=58) for l in range(n)]
+    ldev = [to_dev(L) for L in layers]
+    H = dims["hidden"]
+    h0 = synth.normal_vector(synth.rng(59, H), H)
+    w = synth.norm_weights(synth.rng(60, H), H)
+    plain = run_chain(ldev, h0, dims)
+    h = torch.from_numpy(h0.copy()).cuda()
+    hn = torch.full((H,), float("nan"), device="cuda")
+    ops.decode_chain(ldev, h, dims, w_final=torch.from_numpy(w).cuda(), hn=hn)
+    torch.cuda.synchronize()
+    hg, hng = h.cpu().numpy(), hn.cpu().numpy()
+    assert np.array_equal(hg, plain)
+    ref = oracle.rms_norm(hg, w, dims["eps"])
+    assert np.all(np.abs(hng - ref) <= 1e-5 * np.abs(ref) + 1e-30)
+
+
 def test_chain_rejects_bad_arguments():
     dims = dict(SMALL)
     L = to_dev(synth.chain_layer(0, dims))
