@@ -174,14 +174,16 @@ def test_chain_full_size_gemma3_4b():
     assert rel < 1e-3
 
 
-@pytest.mark.parametrize("shape", ["small", "wide", "gemma3_4b"])
+@pytest.mark.parametrize("shape", ["small", "small_pre_norms", "wide", "gemma3_4b"])
 def test_chain_final_norm(shape):
     """qws_decode_chain_final_norm: h bit-identical to qws_decode_chain's, and
     hn = rms_norm(h, w_final) within the norm's 1e-5 relative bound against the
-    oracle's norm of the GPU's h (the narrow and the wide keeper step, and the
-    Gemma-3-4B hidden size)."""
-    dims, n = {"small": (SMALL, 3), "wide": (WIDE, 2), "gemma3_4b": (synth.GEMMA3_4B, 2)}[shape]
-    layers = [synth.chain_layer(l, dims, fmt_down=oracle.Q6_K, workload=58) for l in range(n)]
+    oracle's norm of the GPU's h (the narrow and the wide keeper step, without
+    the post norms, and the Gemma-3-4B hidden size)."""
+    dims, n = {"small": (SMALL, 3), "small_pre_norms": (dict(SMALL, post_norms=0), 2),
+               "wide": (WIDE, 2), "gemma3_4b": (synth.GEMMA3_4B, 2)}[shape]
+    fmt = oracle.Q4_K if shape == "small_pre_norms" else oracle.Q6_K
+    layers = [synth.chain_layer(l, dims, fmt_down=fmt, workload=58) for l in range(n)]
     ldev = [to_dev(L) for L in layers]
     H = dims["hidden"]
     h0 = synth.normal_vector(synth.rng(59, H), H)
