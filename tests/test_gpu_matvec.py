@@ -61,7 +61,9 @@ def run_matvec(fmt, W, x, rows, hidden, batch=1, split_k=1):
     return host(ops.matvec(fmt, Wd, xd, rows, hidden, batch, split_k, ws))
 
 
-SHAPES = [(1, 256), (3, 256), (33, 512), (300, 2560), (129, 10240), (77, 2048)]
+# (65, 20480): the widest single pass (320 lane units of 64 columns, one row
+# slot per tile round)
+SHAPES = [(1, 256), (3, 256), (33, 512), (300, 2560), (129, 10240), (77, 2048), (65, 20480)]
 
 
 @pytest.mark.parametrize("fmt", [oracle.Q4_K, oracle.Q6_K, oracle.Q4_0])
