@@ -132,6 +132,28 @@ def test_chain_tiny_idle_ctas():
     assert np.array_equal(hall, outs[-1])
 
 
+def test_chain_64_layers_one_launch():
+    """The most layers one launch takes (64: stamps up to 4 * 64, one
+    prologue counter per phase): equal bit for bit to 64 single-layer
+    launches, and close to the oracle end to end."""
+    dims = TINY
+    n = 64
+    layers = [synth.chain_layer(l, dims, fmt_down=oracle.Q6_K, workload=61) for l in range(n)]
+    ldev = [to_dev(L) for L in layers]
+    h0 = synth.normal_vector(synth.rng(62), dims["hidden"])
+    h = h0
+    for l in range(n):
+        h = run_chain([ldev[l]], h, dims)
+    hall = run_chain(ldev, h0, dims)
+    assert np.array_equal(hall, h)
+    ref = h0.astype(np.float64)
+    for L in layers:
+        ref = oracle.layer_forward(L, dims, ref)
+    rel = np.linalg.norm(hall - ref) / np.linalg.norm(ref)
+    print(f"chain tiny 64 layers: relative L2 error {rel:.2e}")
+    assert rel < 1e-3
+
+
 def test_chain_small_end_to_end():
     dims = SMALL
     n = 4
