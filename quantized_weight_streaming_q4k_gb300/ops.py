@@ -318,6 +318,11 @@ def decode_chain(layers, h, dims: dict, workspace=None, stream=None, w_final=Non
     n = len(layers)
     arr = (Layer * n)(*[L if isinstance(L, Layer) else make_layer(L) for L in layers])
     D = make_dims(dims)
+    # the kernel reads / writes `hidden` values of each: a shorter tensor
+    # would be overrun on the device, so refuse it here
+    for name, t in (("h", h), ("w_final", w_final), ("hn", hn)):
+        if isinstance(t, torch.Tensor) and t.numel() < int(dims["hidden"]):
+            raise ValueError(f"{name} has {t.numel()} elements, hidden is {dims['hidden']}")
     need = workspace_bytes(OP_DECODE_CHAIN, 0, dims["hidden"], dims["inter"], 1, 0)
     if workspace is None:
         workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=h.device)
