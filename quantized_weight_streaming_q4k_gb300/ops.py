@@ -353,6 +353,13 @@ def decode_kv(layers, h, dims: dict, k_caches, v_caches, max_seq: int, pos: int,
     n = len(layers)
     if len(k_caches) != n or len(v_caches) != n:
         raise ValueError("one k and one v cache per layer")
+    # the kernels read / write these extents: refuse shorter tensors here
+    if h.numel() < int(dims["hidden"]):
+        raise ValueError(f"h has {h.numel()} elements, hidden is {dims['hidden']}")
+    cache = int(dims["n_kv_heads"]) * int(max_seq) * int(dims["head_dim"])
+    for t in list(k_caches) + list(v_caches):
+        if isinstance(t, torch.Tensor) and t.numel() < cache:
+            raise ValueError(f"a cache has {t.numel()} elements, needs {cache}")
     arr = (Layer * n)(*[L if isinstance(L, Layer) else make_layer(L) for L in layers])
     D = make_dims(dims)
     kp = (C.c_void_p * n)(*[_dev(t, "k_cache", torch.float32) for t in k_caches])
