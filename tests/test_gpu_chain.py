@@ -221,6 +221,37 @@ def test_chain_final_norm(shape):
     assert np.all(np.abs(hng - ref) <= 1e-5 * np.abs(ref) + 1e-30)
 
 
+def test_chain_then_dependent_matvec_without_sync():
+    """The chain lets the next kernel start as its CTAs exit; a Q4_0 matvec
+    launched right after it (no host synchronisation) must read the final
+    norm the chain wrote: its logits equal, bit for bit, those of the same
+    matvec run after a device synchronise, over several back-to-back steps
+    with different inputs."""
+    dims = SMALL
+    n = 2
+    H = dims["hidden"]
+    layers = [to_dev(synth.chain_layer(l, dims, workload=63)) for l in range(n)]
+    w = torch.from_numpy(synth.norm_weights(synth.rng(64), H)).cuda()
+    V = 4096
+    W = torch.from_numpy(synth.q4_0_matrix(synth.rng(65), V, H)).cuda()
+    hs = [torch.from_numpy(synth.normal_vector(synth.rng(66, i), H)).cuda() for i in range(3)]
+    hn = torch.empty(H, device="cuda")
+    outs = []
+    for h0 in hs:
+        h = h0.clone()
+        ops.decode_chain(layers, h, dims, w_final=w, hn=hn)
+        outs.append(ops.q4_0_matvec(W, hn, V, H))
+    torch.cuda.synchronize()
+    for h0, y in zip(hs, outs):
+        h = h0.clone()
+        hn2 = torch.empty(H, device="cuda")
+        ops.decode_chain(layers, h, dims, w_final=w, hn=hn2)
+        torch.cuda.synchronize()
+        y2 = ops.q4_0_matvec(W, hn2, V, H)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y2)
+
+
 def test_chain_rejects_bad_arguments():
     dims = dict(SMALL)
     L = to_dev(synth.chain_layer(0, dims))
